@@ -1,0 +1,522 @@
+"""CPU reference oracle for the DSpark per-step token path (fp64, numpy).
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and bench.py's
+cpu_baseline / reference leg may import this module.  It shares no code with the
+CUDA library: the only common module is the seeded input generator, which holds
+none of the method's arithmetic.
+
+It computes, plainly and slowly, in IEEE double:
+  S1 draft_block   -- Markov sequential head, left-to-right sampling
+  S2 confidence    -- confidence head + sequential temperature scaling + prefix survival
+  S3 schedule      -- hardware-aware global top-B prefix scheduler
+  S4 pack          -- ragged cu_seqlens packing rounded up to a captured graph tier
+  S5 verify        -- rejection-sampling verification (static / compact / cap-accept, greedy)
+plus the host cost-table preparation (build_sps) and the shared random-number
+contract (Philox4x32-10 uniforms, Gumbel keys, two-level Gumbel-max sampler).
+
+Sources, cited by page and section:
+  [SUMMARY]  "DSpark: Confidence-Scheduled Speculative Decoding with Semi-Autoregressive
+             Generation" -- technical summary page (AI Research survey), sections
+             "Architecture (drafter)", "Verification scheduling (system side)", "Infra".
+  [SGLANG]   "DSpark in SGLang" blog post (Vietnamese and Chinese translations), sections
+             "Verify modes", "Ragged verify under full CUDA graphs" (Fig. 2),
+             "Cost-table profiling" (Fig. 6).
+  [VLLM]     "vLLM adaptive verification with DSpark", sections "DSpark confidence
+             scheduling mechanism", "Technical implementation and CUDA Graphs".
+  [PHILOX]   Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+             SC'11 -- the Philox4x32 round function, multipliers and Weyl key schedule.
+
+Where the pages are silent the reading taken is stated at the function; the design doc
+lists every reading.  Every function here is pinned by tests under tests/
+(test_oracle_*.py) against closed forms, brute force, distributional tests and an
+independent library Philox.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import numpy as np
+
+CHUNK = 128
+
+# Philox purposes (counter word 3, bits 24..31)
+P_DRAFT_CHUNK = 1
+P_DRAFT_ELEM = 2
+P_ACCEPT = 3
+P_DECIDE_CHUNK = 4
+P_DECIDE_ELEM = 5
+
+STATIC, COMPACT, CAP_ACCEPT = 0, 1, 2
+EARLY_STOP, GLOBAL_ARGMAX = 0, 1
+
+_MASK32 = np.uint64(0xFFFFFFFF)
+
+
+# ---------------------------------------------------------------------------
+# Input conversion
+# ---------------------------------------------------------------------------
+
+def to_f64(x, dtype: str) -> np.ndarray:
+    """bf16 bit patterns (uint16) or float32 -> float64 (exact)."""
+    x = np.asarray(x)
+    if dtype == "bf16":
+        return (x.astype(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Random numbers [PHILOX]
+# ---------------------------------------------------------------------------
+
+PHILOX_M0 = 0xD2511F53
+PHILOX_M1 = 0xCD9E8D57
+PHILOX_W0 = 0x9E3779B9
+PHILOX_W1 = 0xBB67AE85
+
+
+def philox4x32_10(c0, c1, c2, c3, k0: int, k1: int):
+    """Philox4x32 with 10 rounds [PHILOX, Sec. 3: the Philox S-box and key schedule].
+
+    One round maps (c0, c1, c2, c3) with key (k0, k1) to
+        (hi(M1*c2) ^ c1 ^ k0,  lo(M1*c2),  hi(M0*c0) ^ c3 ^ k1,  lo(M0*c0))
+    and the key is bumped by the Weyl constants (W0, W1) between rounds."""
+    c = [np.asarray(x).astype(np.uint64) & _MASK32 for x in (c0, c1, c2, c3)]
+    shape = np.broadcast(*c).shape
+    c = [np.broadcast_to(x, shape).copy() for x in c]
+    ka, kb = int(k0) & 0xFFFFFFFF, int(k1) & 0xFFFFFFFF
+    for _ in range(10):
+        p0 = c[0] * np.uint64(PHILOX_M0)
+        p1 = c[2] * np.uint64(PHILOX_M1)
+        hi0, lo0 = p0 >> np.uint64(32), p0 & _MASK32
+        hi1, lo1 = p1 >> np.uint64(32), p1 & _MASK32
+        c = [hi1 ^ c[1] ^ np.uint64(ka), lo1, hi0 ^ c[3] ^ np.uint64(kb), lo0]
+        ka = (ka + PHILOX_W0) & 0xFFFFFFFF
+        kb = (kb + PHILOX_W1) & 0xFFFFFFFF
+    return [x.astype(np.uint32) for x in c]
+
+
+def random_bits(seed: int, step: int, purpose: int, req: int, pos: int, idx) -> np.ndarray:
+    """The 32-bit word drawn for (purpose, request, position, index) at (seed, step).
+
+    Counter = (idx >> 2, req, step_lo32, purpose << 24 | pos << 16 | step_hi16), key = seed
+    (lo, hi); the word is lane idx & 3 of the Philox output.  (The pages name no generator;
+    the counter layout is this library's contract.)"""
+    idx = np.asarray(idx, dtype=np.uint64)
+    step = int(step)
+    seed = int(seed)
+    c3 = ((purpose & 0xFF) << 24) | ((pos & 0xFF) << 16) | ((step >> 32) & 0xFFFF)
+    out = philox4x32_10(idx >> np.uint64(2), np.uint64(req & 0xFFFFFFFF),
+                        np.uint64(step & 0xFFFFFFFF), np.uint64(c3),
+                        seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
+    lane = (idx & np.uint64(3)).astype(np.int64)
+    stacked = np.stack(out, axis=-1)
+    return np.take_along_axis(stacked, lane[..., None], axis=-1)[..., 0]
+
+
+def bits_to_uniform(bits) -> np.ndarray:
+    """u = ((bits >> 9) + 1/2) * 2^-23, strictly inside (0, 1) and exact in fp32 and fp64."""
+    b = np.asarray(bits, dtype=np.uint32)
+    return ((b >> np.uint32(9)).astype(np.float64) + 0.5) * 2.0 ** -23
+
+
+def uniform(seed, step, purpose, req, pos, idx) -> np.ndarray:
+    return bits_to_uniform(random_bits(seed, step, purpose, req, pos, idx))
+
+
+def gumbel(u) -> np.ndarray:
+    """Standard Gumbel variate from a uniform: -ln(-ln u)."""
+    return -np.log(-np.log(np.asarray(u, dtype=np.float64)))
+
+
+# ---------------------------------------------------------------------------
+# Samplers
+# ---------------------------------------------------------------------------
+
+def _top2_gap(keys: np.ndarray) -> float:
+    k = keys[np.isfinite(keys)]
+    if k.size < 2:
+        return math.inf
+    part = np.partition(k, -2)[-2:]
+    return float(part[1] - part[0])
+
+
+def _first_argmax(keys: np.ndarray) -> int:
+    """Index of the largest key, the lowest index among equal maxima."""
+    return int(np.argmax(keys))  # numpy returns the first occurrence
+
+
+def logsumexp(x: np.ndarray) -> float:
+    x = np.asarray(x, dtype=np.float64)
+    m = np.max(x)
+    if not np.isfinite(m):
+        return float(m)
+    return float(m + np.log(np.sum(np.exp(x - m))))
+
+
+def chunk_log_mass(logw: np.ndarray, chunk: int = CHUNK) -> np.ndarray:
+    """L_c = log sum_{v in chunk c} exp(logw[v]) over consecutive chunks (-inf if empty)."""
+    logw = np.asarray(logw, dtype=np.float64)
+    n = logw.size
+    nc = (n + chunk - 1) // chunk
+    padded = np.full(nc * chunk, -np.inf)
+    padded[:n] = logw
+    blocks = padded.reshape(nc, chunk)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        m = blocks.max(axis=1)
+        safe_m = np.where(np.isfinite(m), m, 0.0)
+        return np.where(np.isfinite(m), safe_m + np.log(np.exp(blocks - safe_m[:, None]).sum(axis=1)), -np.inf)
+
+
+def two_level_gumbel(logw: np.ndarray, seed: int, step: int, req: int, pos: int,
+                     purpose_chunk: int, purpose_elem: int, chunk: int = CHUNK):
+    """Exact draw of v with probability proportional to exp(logw[v]).
+
+    Level 1: the vocabulary is cut into consecutive chunks of `chunk` entries; chunk c gets
+    the key L_c + G_c with L_c = log sum_{v in c} exp(logw[v]) and G_c a Gumbel variate
+    (purpose_chunk, index c).  The largest key picks the chunk -- by the Gumbel-max property
+    this chooses c with probability equal to its share of the total mass.
+    Level 2: inside the chosen chunk, entry v gets logw[v] + G'_v (purpose_elem, index =
+    offset of v in the chunk); the largest key is the draw.  Given the chunk, the entry is
+    then drawn in proportion to exp(logw[v]), so the product is exact.
+
+    Entries with logw = -inf never win.  Ties go to the lowest index at both levels.
+    Returns (v, margin) where margin is the smaller of the two levels' top-two key gaps."""
+    logw = np.asarray(logw, dtype=np.float64)
+    n = logw.size
+    L = chunk_log_mass(logw, chunk)
+    nc = L.size
+    Kc = L + gumbel(uniform(seed, step, purpose_chunk, req, pos, np.arange(nc)))
+    if not np.any(np.isfinite(Kc)):
+        raise ValueError("two_level_gumbel: no entry with positive weight")
+    c = _first_argmax(Kc)
+    lo, hi = c * chunk, min(n, (c + 1) * chunk)
+    ke = logw[lo:hi] + gumbel(uniform(seed, step, purpose_elem, req, pos, np.arange(hi - lo)))
+    j = _first_argmax(ke)
+    return lo + j, min(_top2_gap(Kc), _top2_gap(ke))
+
+
+# ---------------------------------------------------------------------------
+# S1 -- Markov-head block draft
+# ---------------------------------------------------------------------------
+
+def markov_logits(U_k: np.ndarray, W1: np.ndarray, W2t: np.ndarray, x_prev: np.ndarray) -> np.ndarray:
+    """l_k = U_k + W1[x_{k-1}] . W2 for every request, [bs, V] in fp64.
+
+    [SUMMARY, "Architecture (drafter)", Markov head]: the transition bias depends only on the
+    previous token and factors through rank r as W1 (V x r, a lookup table) times W2 (r x V).
+    W2 is stored transposed (W2t = W2^T, V x r)."""
+    return U_k + W1[x_prev] @ W2t.T
+
+
+def draft_block(U, W1, W2t, anchor, temperature: float, seed: int, step: int,
+                dtype: str = "bf16", chunk: int = CHUNK):
+    """S1: draw x_1..x_gamma left to right from p_k(v) = softmax(U_k(v) + B_k(v)).
+
+    [SUMMARY, "Architecture (drafter)"]: the parallel backbone yields U_1..U_gamma in one pass
+    with the anchor as the first predicted position, and the sequential head samples from
+    the causal per-position distributions left to right; per-token probabilities stay exact
+    softmax values, which rejection sampling needs.
+    Readings: x_0 = anchor feeds B_1; the sampling temperature divides the logits; at
+    temperature 0 the draw is the argmax (lowest index on ties).
+
+    Returns tokens [bs, gamma] int32, logit_x [bs, gamma] (tempered logit of the drawn
+    token; raw logit at temperature 0), lse [bs, gamma] (log-sum-exp of the tempered
+    logits; 0 at temperature 0) and margin [bs, gamma] (decision margin)."""
+    U = to_f64(U, dtype)
+    W1 = to_f64(W1, dtype)
+    W2t = to_f64(W2t, dtype)
+    bs, gamma, V = U.shape
+    tokens = np.zeros((bs, gamma), dtype=np.int32)
+    logit_x = np.zeros((bs, gamma))
+    lse = np.zeros((bs, gamma))
+    margin = np.zeros((bs, gamma))
+    x_prev = np.asarray(anchor, dtype=np.int64).copy()
+    for k in range(1, gamma + 1):
+        ell = markov_logits(U[:, k - 1], W1, W2t, x_prev)
+        for r in range(bs):
+            if temperature == 0.0:
+                v = _first_argmax(ell[r])
+                tokens[r, k - 1] = v
+                logit_x[r, k - 1] = ell[r, v]
+                margin[r, k - 1] = _top2_gap(ell[r])
+            else:
+                t = ell[r] / temperature
+                v, mg = two_level_gumbel(t, seed, step, r, k, P_DRAFT_CHUNK, P_DRAFT_ELEM, chunk)
+                tokens[r, k - 1] = v
+                logit_x[r, k - 1] = t[v]
+                lse[r, k - 1] = logsumexp(t)
+                margin[r, k - 1] = mg
+        x_prev = tokens[:, k - 1].astype(np.int64)
+    return tokens, logit_x, lse, margin
+
+
+# ---------------------------------------------------------------------------
+# S2 -- confidence head, STS, prefix survival
+# ---------------------------------------------------------------------------
+
+def confidence(h, W1, anchor, tokens, w, b: float, sts_T, dtype: str = "bf16"):
+    """S2: c_{r,k} = sigmoid(z_{r,k} / T_k), a_{r,j} = prod_{i<=j} c_{r,i}.
+
+    [SUMMARY, "Verification scheduling", confidence head]: a linear projection of the
+    concatenation [h_k ; W1[x_{k-1}]] followed by a sigmoid gives c_k, the probability that
+    draft token k passes given that its prefix passed.
+    [SUMMARY, same section, STS]: a per-position temperature calibrates the score; read as
+    dividing the confidence logit by T_k (order preserving at each position).
+    [SUMMARY, same section, scheduler]: prefix survival a_{r,j} is the running product of c.
+    Readings: bias b = 0 unless given; x_0 = anchor; T_k indexed from k = 1.
+    Returns conf [bs, gamma], surv [bs, gamma], z [bs, gamma] (all fp64)."""
+    h = to_f64(h, dtype)
+    W1 = to_f64(W1, dtype)
+    w = np.asarray(w, dtype=np.float64)
+    T = np.asarray(sts_T, dtype=np.float64)
+    bs, gamma, d = h.shape
+    x_prev = np.concatenate([np.asarray(anchor, dtype=np.int64)[:, None],
+                             np.asarray(tokens, dtype=np.int64)[:, :gamma - 1]], axis=1)
+    feats = np.concatenate([h, W1[x_prev]], axis=2)          # [bs, gamma, d + r]
+    z = feats @ w + float(b)
+    conf = 1.0 / (1.0 + np.exp(-z / T[None, :]))
+    surv = np.cumprod(conf, axis=1)
+    return conf, surv, z
+
+
+# ---------------------------------------------------------------------------
+# Cost table (host preparation)
+# ---------------------------------------------------------------------------
+
+def tier_of(M: int, tiers) -> Optional[int]:
+    """Smallest captured total >= M ([VLLM, "CUDA Graph Padding"]: a 121-token batch runs
+    the 128-token graph).  With no tiers every total is its own graph.  None if M exceeds
+    the largest tier."""
+    tiers = list(tiers)
+    if not tiers:
+        return M
+    for t in tiers:
+        if t >= M:
+            return int(t)
+    return None
+
+
+def build_sps(T_raw, tiers) -> np.ndarray:
+    """SPS table from a profiled step-time curve: sps[M] = 1 / T_mono(tier(M)).
+
+    [VLLM, "Cost Modeling"]: the profiled curve is forced monotone increasing (running
+    maximum here).  [VLLM, "CUDA Graph Padding"] and [SGLANG, "Ragged verify"]: the step
+    runs the graph of the next captured tier, so the cost of M tokens is the cost of tier(M).
+    Totals beyond the largest tier or the profiled range get sps = 0 (never admitted)."""
+    T_raw = np.asarray(T_raw, dtype=np.float64)
+    m_max = T_raw.size - 1
+    T_mono = np.maximum.accumulate(T_raw)
+    sps = np.zeros(m_max + 1)
+    for M in range(m_max + 1):
+        t = tier_of(M, tiers)
+        if t is None or t > m_max:
+            sps[M] = 0.0
+        else:
+            sps[M] = 1.0 / T_mono[t]
+    return sps
+
+
+# ---------------------------------------------------------------------------
+# S3 -- hardware-aware global top-B prefix scheduler
+# ---------------------------------------------------------------------------
+
+FIX_SHIFT = 40
+
+
+def schedule(surv_f32, sps, mode: int = EARLY_STOP):
+    """S3: admit draft slots in descending survival, maximising Theta = tau * SPS(bs + K).
+
+    [SUMMARY, "Verification scheduling", Hardware-Aware Prefix Scheduler (Algorithm 1)]:
+    verify-length choice is a global throughput maximisation; because a_{r,j} does not grow
+    with j the greedy admits slots globally in descending a_{r,j}, updates Theta in O(1) per
+    admit from the table, and stops as soon as Theta drops.
+    [VLLM, "DSpark confidence scheduling mechanism"]: expected tokens = one extra token per
+    request plus the survival of the admitted slots; the admitted slots of a request form a
+    contiguous prefix.
+    [SUMMARY, "Infra"]: without the early stop, a global search over the table (GLOBAL_ARGMAX).
+
+    Readings: keys are the fp32 survival values; ties go to the lower request, then the lower
+    position.  Survival sums are exact fixed point, S_K = sum floor(a * 2^40), and
+    tau(K) = bs + S_K * 2^-40 (exact in fp64); Theta(K) = tau(K) * sps[bs + K] with one
+    rounding.  A slot is admitted only if Theta strictly increases (positive expected gain).
+    K ranges over 0..min(bs*gamma, m_max - bs).
+
+    Returns (window [bs] int32, K, Theta(K), Theta array over K)."""
+    a = np.asarray(surv_f32, dtype=np.float32)
+    bs, gamma = a.shape
+    sps = np.asarray(sps, dtype=np.float64)
+    m_max = sps.size - 1
+    if m_max < bs:
+        raise ValueError("sps table shorter than the batch")
+    slots = [(float(a[r, j]), r, j) for r in range(bs) for j in range(gamma)]
+    slots.sort(key=lambda s: (-s[0], s[1], s[2]))
+    n = bs * gamma
+    kmax = min(n, m_max - bs)
+    theta = np.zeros(kmax + 1)
+    S = 0
+    for K in range(kmax + 1):
+        if K > 0:
+            S += int(math.floor(max(slots[K - 1][0], 0.0) * 2.0 ** FIX_SHIFT))
+        tau = bs + math.ldexp(float(S), -FIX_SHIFT)
+        theta[K] = tau * float(sps[bs + K])
+    if mode == EARLY_STOP:
+        K_star = kmax
+        for K in range(kmax):
+            if not theta[K + 1] > theta[K]:
+                K_star = K
+                break
+    else:
+        K_star = int(np.argmax(theta))  # first maximum
+    window = np.zeros(bs, dtype=np.int32)
+    for i in range(K_star):
+        window[slots[i][1]] += 1
+    return window, K_star, float(theta[K_star]), theta
+
+
+# ---------------------------------------------------------------------------
+# S4 -- ragged packing
+# ---------------------------------------------------------------------------
+
+def pack(window, anchor, tokens, tiers, cap: int, gamma: Optional[int] = None):
+    """S4: pack the verify windows front to back into a cu_seqlens batch.
+
+    [SGLANG, "Ragged verify under full CUDA graphs", Fig. 2]: the variable-length requests
+    are packed into one compact buffer keyed by the total token count, rounded up to the
+    nearest captured tier.  [VLLM, "Graph Capture"]: a request verifies 1..gamma+1 tokens.
+    Request r contributes n_r = l_r + 1 query tokens [x_0, x_1..x_{l_r}].  window=None is the
+    static layout (l_r = gamma).  Pad rows carry -1 in ids, req and pos.
+
+    Returns (cu_seqlens [bs+1], ids, req, pos [cap] int32, padded_total)."""
+    tokens = np.asarray(tokens, dtype=np.int32)
+    bs = tokens.shape[0]
+    g = tokens.shape[1] if gamma is None else gamma
+    l = np.full(bs, g, dtype=np.int64) if window is None else np.asarray(window, dtype=np.int64)
+    cu = np.zeros(bs + 1, dtype=np.int64)
+    for r in range(bs):
+        cu[r + 1] = cu[r] + l[r] + 1
+    M = int(cu[bs])
+    padded = tier_of(M, tiers)
+    if padded is None:
+        raise ValueError("packed total exceeds the largest tier")
+    if padded > cap:
+        raise ValueError("packed total exceeds the buffer capacity")
+    ids = np.full(cap, -1, dtype=np.int32)
+    req = np.full(cap, -1, dtype=np.int32)
+    pos = np.full(cap, -1, dtype=np.int32)
+    for r in range(bs):
+        for j in range(int(l[r]) + 1):
+            p = int(cu[r]) + j
+            ids[p] = anchor[r] if j == 0 else tokens[r, j - 1]
+            req[p] = r
+            pos[p] = j
+    return cu.astype(np.int32), ids, req, pos, padded
+
+
+# ---------------------------------------------------------------------------
+# S5 -- rejection-sampling verification
+# ---------------------------------------------------------------------------
+
+def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x, lse,
+           U, W1, W2t, temperature: float, seed: int, step: int, dtype: str = "bf16",
+           chunk: int = CHUNK):
+    """S5: accept the longest valid prefix of each request's window, then one more token.
+
+    [SUMMARY, "Abstract" and "Architecture (drafter)"]: lossless speculative decoding accepts
+    the longest prefix under rejection sampling with exact per-token probabilities: draft
+    token x_k is accepted with probability min(1, p_t(x_k) / p_d(x_k)); on the first rejection
+    a replacement is drawn from normalise(max(0, p_t - p_d)); if every tested token passes, a
+    bonus token is drawn from the target distribution of the next position.
+    [SGLANG, "Verify modes"]: static verifies the whole block; compact verifies only the
+    scheduler's window; cap-accept verifies the whole block but commits only up to the
+    window, committing exactly what compact commits while exposing the full-block ceiling.
+
+    Readings: accept iff u < p_t/p_d (strict); the residual and bonus draws use the
+    two-level Gumbel sampler (P_DECIDE_* streams at the position being drawn); if the
+    residual has no mass the draw falls back to p_t; greedy (temperature 0) accepts iff
+    x_k is the target argmax (lowest index) and the extra token is the target argmax.
+    Draft probabilities come from logit_x - lse (the draft's outputs); the residual's draft
+    distribution p_d is recomputed from U, W1, W2 at the rejected position.
+
+    target_packed row cu[r] + k - 1 holds the target logits that score position k
+    (k = 1..n_r).  Returns out_tokens [bs, gamma+1] (-1 padded), acc_len [bs],
+    ceiling [bs] (tested-window accepted count; the full-block ceiling in cap-accept) and
+    margin [bs] (smallest decision margin among the decisions that shaped the output)."""
+    tgt = to_f64(target_packed, dtype)
+    Uf = to_f64(U, dtype)
+    W1f = to_f64(W1, dtype)
+    W2f = to_f64(W2t, dtype)
+    tokens = np.asarray(tokens, dtype=np.int64)
+    bs, gamma = tokens.shape
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    out = np.full((bs, gamma + 1), -1, dtype=np.int32)
+    acc_len = np.zeros(bs, dtype=np.int32)
+    ceiling = np.zeros(bs, dtype=np.int32)
+    margin = np.full(bs, math.inf)
+    for r in range(bs):
+        lr = int(window[r]) if window is not None else gamma
+        L_test = lr if mode == COMPACT else gamma
+        L_commit = gamma if mode == STATIC else lr
+        n_r = int(cu[r + 1] - cu[r])
+        if n_r != L_test + 1:
+            raise ValueError(f"request {r}: packed rows {n_r} != tested window + 1 = {L_test + 1}")
+
+        def trow(k):  # target logits scoring position k
+            return tgt[cu[r] + k - 1]
+
+        x = [int(anchor[r])] + [int(v) for v in tokens[r]]
+        first_reject = None
+        mg = math.inf
+        for k in range(1, L_test + 1):
+            if temperature == 0.0:
+                row = trow(k)
+                ok = (_first_argmax(row) == x[k])
+                mg = min(mg, _top2_gap(row))
+            else:
+                t = trow(k) / temperature
+                lp_t = t[x[k]] - logsumexp(t)
+                lp_d = float(logit_x[r, k - 1]) - float(lse[r, k - 1])
+                ratio = math.exp(lp_t - lp_d)
+                u = float(uniform(seed, step, P_ACCEPT, r, k, 0))
+                ok = u < ratio
+                mg = min(mg, abs(u - ratio))
+            if not ok:
+                first_reject = k
+                break
+        ceiling[r] = (first_reject - 1) if first_reject is not None else L_test
+        if first_reject is not None and first_reject <= L_commit:
+            k = first_reject
+            acc = k - 1
+            if temperature == 0.0:
+                x_new = _first_argmax(trow(k))
+            else:
+                t = trow(k) / temperature
+                p_t = np.exp(t - logsumexp(t))
+                d = (Uf[r, k - 1] + W1f[x[k - 1]] @ W2f.T) / temperature
+                p_d = np.exp(d - logsumexp(d))
+                res = np.maximum(0.0, p_t - p_d)
+                with np.errstate(divide="ignore"):
+                    logw = np.log(res) if res.sum() > 0.0 else t
+                x_new, m2 = two_level_gumbel(logw, seed, step, r, k, P_DECIDE_CHUNK, P_DECIDE_ELEM, chunk)
+                mg = min(mg, m2)
+        else:
+            acc = L_commit
+            k = L_commit + 1
+            if temperature == 0.0:
+                row = trow(k)
+                x_new = _first_argmax(row)
+                mg = min(mg, _top2_gap(row))
+            else:
+                t = trow(k) / temperature
+                x_new, m2 = two_level_gumbel(t, seed, step, r, k, P_DECIDE_CHUNK, P_DECIDE_ELEM, chunk)
+                mg = min(mg, m2)
+        out[r, :acc] = x[1:acc + 1]
+        out[r, acc] = x_new
+        acc_len[r] = acc
+        margin[r] = mg
+    return out, acc_len, ceiling, margin
+
+
+def step_tokens(acc_len) -> int:
+    """Tokens committed by one step: accepted drafts plus the one extra token per request."""
+    return int(np.sum(np.asarray(acc_len, dtype=np.int64) + 1))

@@ -1,0 +1,134 @@
+"""Pins of the oracle's samplers and of S1 (Markov block draft).
+
+- the two-level Gumbel sampler draws exactly from softmax (chi-square, ragged chunks);
+- Markov logits equal a brute-force triple loop;
+- the drafted joint distribution of (x_1, x_2) is p_1(x_1) p_2(x_2 | x_1) with the bias of
+  position 2 taken from x_1 (catches an off-by-one in the conditioning token);
+- temperature divides the logits; temperature 0 is the argmax."""
+import numpy as np
+from scipy import stats
+from scipy.special import logsumexp as sp_lse, softmax
+
+from oracle import dspark_oracle as O
+
+
+def _chi2_ok(counts, probs, pmin=1e-4):
+    counts = np.asarray(counts, dtype=np.float64)
+    exp = probs * counts.sum()
+    keep = exp > 0
+    return stats.chisquare(counts[keep], exp[keep] * counts[keep].sum() / exp[keep].sum()).pvalue > pmin
+
+
+def test_two_level_sampler_matches_softmax_with_ragged_chunks():
+    rng = np.random.default_rng(3)
+    logw = rng.normal(0, 1.5, size=13)
+    logw[5] = -np.inf  # never drawn
+    p = softmax(np.where(np.isfinite(logw), logw, -1e300))
+    counts = np.zeros(13)
+    for s in range(30000):
+        v, _ = O.two_level_gumbel(logw, 9, s, 0, 1, O.P_DRAFT_CHUNK, O.P_DRAFT_ELEM, chunk=4)
+        counts[v] += 1
+    assert counts[5] == 0
+    assert _chi2_ok(counts, p)
+
+
+def test_two_level_sampler_chunk_marginal_is_chunk_mass():
+    rng = np.random.default_rng(4)
+    logw = rng.normal(0, 2.0, size=40)
+    chunk = 8
+    p = softmax(logw)
+    mass = p.reshape(5, 8).sum(axis=1)
+    counts = np.zeros(5)
+    for s in range(20000):
+        v, _ = O.two_level_gumbel(logw, 1, s, 3, 2, O.P_DECIDE_CHUNK, O.P_DECIDE_ELEM, chunk=chunk)
+        counts[v // chunk] += 1
+    assert _chi2_ok(counts, mass)
+    np.testing.assert_allclose(np.exp(O.chunk_log_mass(logw, chunk)), np.exp(logw).reshape(5, 8).sum(1), rtol=1e-12)
+
+
+def test_markov_logits_brute_force():
+    rng = np.random.default_rng(5)
+    bs, V, r = 3, 11, 4
+    U = rng.normal(size=(bs, V))
+    W1 = rng.normal(size=(V, r))
+    W2t = rng.normal(size=(V, r))
+    x = np.array([2, 10, 0])
+    got = O.markov_logits(U, W1, W2t, x)
+    for b in range(bs):
+        for v in range(V):
+            acc = U[b, v]
+            for i in range(r):
+                acc += W1[x[b], i] * W2t[v, i]
+            assert abs(got[b, v] - acc) < 1e-12
+
+
+def _tiny_draft_inputs(V=6, r=3, gamma=2, seed=0):
+    rng = np.random.default_rng(seed)
+    U = rng.normal(0, 1.0, size=(1, gamma, V)).astype(np.float32)
+    W1 = rng.normal(0, 0.8, size=(V, r)).astype(np.float32)
+    W2t = rng.normal(0, 0.8, size=(V, r)).astype(np.float32)
+    return U, W1, W2t
+
+
+def test_draft_joint_distribution_of_first_two_tokens():
+    V = 6
+    U, W1, W2t = _tiny_draft_inputs(V=V)
+    anchor = np.array([4], dtype=np.int32)
+    U64, W164, W2t64 = (a.astype(np.float64) for a in (U, W1, W2t))
+    p1 = softmax(U64[0, 0] + W164[4] @ W2t64.T)
+    joint = np.zeros((V, V))
+    for a in range(V):
+        joint[a] = p1[a] * softmax(U64[0, 1] + W164[a] @ W2t64.T)
+    counts = np.zeros((V, V))
+    for s in range(12000):
+        tok, lx, lse, _ = O.draft_block(U, W1, W2t, anchor, 1.0, 21, s, dtype="f32", chunk=4)
+        counts[tok[0, 0], tok[0, 1]] += 1
+    assert _chi2_ok(counts.ravel(), joint.ravel())
+
+
+def test_draft_outputs_logit_and_lse():
+    U, W1, W2t = _tiny_draft_inputs(V=300, r=5, gamma=3, seed=2)
+    anchor = np.array([17], dtype=np.int32)
+    tau = 0.7
+    tok, lx, lse, _ = O.draft_block(U, W1, W2t, anchor, tau, 5, 0, dtype="f32")
+    prev = 17
+    for k in range(3):
+        ell = U[0, k].astype(np.float64) + W1[prev].astype(np.float64) @ W2t.astype(np.float64).T
+        assert abs(lx[0, k] - ell[tok[0, k]] / tau) < 1e-12
+        assert abs(lse[0, k] - sp_lse(ell / tau)) < 1e-12
+        prev = tok[0, k]
+
+
+def test_draft_temperature_scales_logits():
+    V = 5
+    U, W1, W2t = _tiny_draft_inputs(V=V, gamma=1, seed=3)
+    anchor = np.array([1], dtype=np.int32)
+    ell = U[0, 0].astype(np.float64) + W1[1].astype(np.float64) @ W2t.astype(np.float64).T
+    counts = np.zeros(V)
+    for s in range(15000):
+        tok, *_ = O.draft_block(U, W1, W2t, anchor, 0.5, 2, s, dtype="f32")
+        counts[tok[0, 0]] += 1
+    assert _chi2_ok(counts, softmax(ell / 0.5))
+
+
+def test_draft_greedy_is_argmax():
+    U, W1, W2t = _tiny_draft_inputs(V=50, r=4, gamma=4, seed=6)
+    U = np.repeat(U, 3, axis=0)
+    anchor = np.array([0, 7, 49], dtype=np.int32)
+    tok, lx, lse, _ = O.draft_block(U, W1, W2t, anchor, 0.0, 1, 0, dtype="f32")
+    for b in range(3):
+        prev = anchor[b]
+        for k in range(4):
+            ell = U[b, k].astype(np.float64) + W1[prev].astype(np.float64) @ W2t.astype(np.float64).T
+            assert tok[b, k] == int(np.argmax(ell))
+            assert lx[b, k] == ell.max() and lse[b, k] == 0.0
+            prev = tok[b, k]
+
+
+def test_greedy_ties_go_to_lowest_index():
+    U = np.zeros((1, 1, 8), dtype=np.float32)
+    U[0, 0, [2, 5, 7]] = 3.0
+    W1 = np.zeros((8, 2), dtype=np.float32)
+    W2t = np.zeros((8, 2), dtype=np.float32)
+    tok, *_ = O.draft_block(U, W1, W2t, np.array([0], dtype=np.int32), 0.0, 0, 0, dtype="f32")
+    assert tok[0, 0] == 2

@@ -1,0 +1,143 @@
+"""Pins of the oracle's S5 (rejection-sampling verification).
+
+- Monte-Carlo acceptance of position 1 equals 1 - 1/2 ||p_d - p_t||_1 (the analytic
+  per-position acceptance of the technical summary's confidence-head section), and the
+  acceptance of position 2 given position 1 equals its exact conditional value;
+- the first committed token is distributed as p_t (lossless), also under random windows
+  and in cap-accept mode (non-anticipating truncation);
+- cap-accept commits bit-identically to compact and its ceiling equals static's count;
+- greedy verification accepts exactly the argmax-matching prefix."""
+import numpy as np
+import pytest
+from scipy import stats
+from scipy.special import softmax
+
+from oracle import dspark_oracle as O
+from speculative_decoding_draft_markov_gb300 import inputs as I
+
+
+def _setup(V=16, r=3, gamma=2, reps=200, seed=0, noise=1.0):
+    rng = np.random.default_rng(seed)
+    U1 = rng.normal(0, 1.2, size=(1, gamma, V)).astype(np.float32)
+    W1 = rng.normal(0, 0.7, size=(V, r)).astype(np.float32)
+    W2t = rng.normal(0, 0.7, size=(V, r)).astype(np.float32)
+    base = np.concatenate([U1, rng.normal(0, 1.2, size=(1, 1, V)).astype(np.float32)], axis=1)
+    target1 = (base + rng.normal(0, noise, size=base.shape)).astype(np.float32)
+    anchor1 = np.array([int(rng.integers(0, V))], dtype=np.int32)
+    U = np.repeat(U1, reps, 0)
+    target = np.repeat(target1, reps, 0)
+    anchor = np.repeat(anchor1, reps)
+    return U, W1, W2t, target, anchor
+
+
+def _run_step(U, W1, W2t, target, anchor, window, mode, step, tau=1.0, seed=5):
+    bs, gamma, V = U.shape
+    tok, lx, lse, _ = O.draft_block(U, W1, W2t, anchor, tau, seed, step, dtype="f32")
+    pack_win = window if mode == O.COMPACT else None
+    cu, ids, req, pos, padded = O.pack(pack_win, anchor, tok, [], cap=bs * (gamma + 1))
+    packed = I.gather_packed_target(target, req, pos, padded)
+    out, acc, ceil, _ = O.verify(packed, cu, window, mode, anchor, tok, lx, lse, U, W1, W2t,
+                                 tau, seed, step, dtype="f32")
+    return tok, out, acc, ceil
+
+
+def test_monte_carlo_acceptance_equals_one_minus_tv():
+    U, W1, W2t, target, anchor = _setup()
+    bs, gamma, V = U.shape
+    f = lambda a: a.astype(np.float64)
+    pd1 = softmax(f(U[0, 0]) + f(W1[anchor[0]]) @ f(W2t).T)
+    pt1 = softmax(f(target[0, 0]))
+    pt2 = softmax(f(target[0, 1]))
+    acc1 = 1.0 - 0.5 * np.abs(pd1 - pt1).sum()
+    # P(accept 2 | accept 1) = sum_x1 min(pd1, pt1)(x1) / acc1 * (1 - TV(pd2(.|x1), pt2))
+    cond = 0.0
+    for x1 in range(V):
+        pd2 = softmax(f(U[0, 1]) + f(W1[x1]) @ f(W2t).T)
+        cond += min(pd1[x1], pt1[x1]) / acc1 * (1.0 - 0.5 * np.abs(pd2 - pt2).sum())
+    window = np.full(bs, gamma, dtype=np.int32)
+    n1 = n2 = n = 0
+    for step in range(60):
+        _, _, acc, _ = _run_step(U, W1, W2t, target, anchor, window, O.COMPACT, step)
+        n += bs
+        n1 += int(np.sum(acc >= 1))
+        n2 += int(np.sum(acc >= 2))
+    p1 = n1 / n
+    assert abs(p1 - acc1) < 4 * np.sqrt(acc1 * (1 - acc1) / n)
+    p21 = n2 / n1
+    assert abs(p21 - cond) < 4 * np.sqrt(cond * (1 - cond) / n1)
+
+
+@pytest.mark.parametrize("mode", ["compact_random", "static", "cap_accept"])
+def test_first_committed_token_is_target_distributed(mode):
+    U, W1, W2t, target, anchor = _setup(seed=1, noise=1.5)
+    bs, gamma, V = U.shape
+    pt1 = softmax(target[0, 0].astype(np.float64))
+    counts = np.zeros(V)
+    for step in range(60):
+        window = I.random_windows(bs, gamma, 1000 + step)
+        m = {"compact_random": O.COMPACT, "static": O.STATIC, "cap_accept": O.CAP_ACCEPT}[mode]
+        _, out, _, _ = _run_step(U, W1, W2t, target, anchor, window, m, step)
+        np.add.at(counts, out[:, 0], 1)
+    assert stats.chisquare(counts, pt1 * counts.sum()).pvalue > 1e-4
+
+
+def test_cap_accept_commits_like_compact_and_exposes_static_ceiling():
+    U, W1, W2t, target, anchor = _setup(V=40, gamma=5, reps=30, seed=3, noise=0.6)
+    bs, gamma, V = U.shape
+    for step in range(10):
+        window = I.random_windows(bs, gamma, 77 + step)
+        _, out_c, acc_c, _ = _run_step(U, W1, W2t, target, anchor, window, O.COMPACT, step)
+        _, out_a, acc_a, ceil_a = _run_step(U, W1, W2t, target, anchor, window, O.CAP_ACCEPT, step)
+        _, out_s, acc_s, _ = _run_step(U, W1, W2t, target, anchor, window, O.STATIC, step)
+        np.testing.assert_array_equal(out_a, out_c)
+        np.testing.assert_array_equal(acc_a, acc_c)
+        np.testing.assert_array_equal(ceil_a, acc_s)
+        assert np.all(ceil_a >= acc_a) and np.all(acc_a <= window)
+
+
+def test_static_equals_compact_with_full_windows():
+    U, W1, W2t, target, anchor = _setup(V=40, gamma=4, reps=20, seed=4)
+    bs, gamma, V = U.shape
+    full = np.full(bs, gamma, dtype=np.int32)
+    _, out_c, acc_c, _ = _run_step(U, W1, W2t, target, anchor, full, O.COMPACT, 3)
+    _, out_s, acc_s, _ = _run_step(U, W1, W2t, target, anchor, full, O.STATIC, 3)
+    np.testing.assert_array_equal(out_c, out_s)
+    np.testing.assert_array_equal(acc_c, acc_s)
+
+
+def test_greedy_accepts_argmax_prefix():
+    V, gamma, r = 30, 4, 2
+    rng = np.random.default_rng(9)
+    U = rng.normal(size=(1, gamma, V)).astype(np.float32)
+    W1 = rng.normal(0, 0.3, size=(V, r)).astype(np.float32)
+    W2t = rng.normal(0, 0.3, size=(V, r)).astype(np.float32)
+    anchor = np.array([3], dtype=np.int32)
+    tok, lx, lse, _ = O.draft_block(U, W1, W2t, anchor, 0.0, 0, 0, dtype="f32")
+    target = rng.normal(size=(1, gamma + 1, V)).astype(np.float32)
+    for k in range(2):                      # positions 1 and 2 agree with the draft
+        target[0, k, tok[0, k]] = 10.0
+    wrong = (tok[0, 2] + 1) % V             # position 3 disagrees
+    target[0, 2, wrong] = 10.0
+    target[0, 2, tok[0, 2]] = 9.0
+    cu, ids, req, pos, padded = O.pack(None, anchor, tok, [], cap=gamma + 1)
+    packed = I.gather_packed_target(target, req, pos, padded)
+    out, acc, ceil, _ = O.verify(packed, cu, None, O.STATIC, anchor, tok, lx, lse, U, W1, W2t,
+                                 0.0, 0, 0, dtype="f32")
+    assert acc[0] == 2 and list(out[0, :3]) == [tok[0, 0], tok[0, 1], wrong] and out[0, 3] == -1
+    # everything agrees -> bonus = argmax of the row after the block
+    for k in range(gamma):
+        target[0, k, tok[0, k]] = 20.0
+    packed = I.gather_packed_target(target, req, pos, padded)
+    out, acc, _, _ = O.verify(packed, cu, None, O.STATIC, anchor, tok, lx, lse, U, W1, W2t,
+                              0.0, 0, 0, dtype="f32")
+    assert acc[0] == gamma and out[0, gamma] == int(np.argmax(target[0, gamma]))
+
+
+def test_verify_rejects_mismatched_packing():
+    U, W1, W2t, target, anchor = _setup(V=16, gamma=3, reps=2)
+    tok, lx, lse, _ = O.draft_block(U, W1, W2t, anchor, 1.0, 0, 0, dtype="f32")
+    cu, ids, req, pos, padded = O.pack(np.array([1, 2]), anchor, tok, [], cap=8)
+    packed = I.gather_packed_target(target, req, pos, padded)
+    with pytest.raises(ValueError):
+        O.verify(packed, cu, np.array([2, 2]), O.COMPACT, anchor, tok, lx, lse, U, W1, W2t,
+                 1.0, 0, 0, dtype="f32")
