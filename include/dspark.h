@@ -1,0 +1,206 @@
+/*
+ * dspark.h -- C ABI of the DSpark per-step speculative-decoding token path on GB300 (sm_103a).
+ *
+ * One decoding step of confidence-scheduled speculative decoding runs as five calls on one
+ * CUDA stream, all asynchronous, none reading anything back to the host:
+ *
+ *   dspark_draft_block -> dspark_confidence -> dspark_schedule -> dspark_pack
+ *       -> [the caller's target forward over the packed batch] -> dspark_verify
+ *
+ * Sources, cited by page and section:
+ *   [SUMMARY] "DSpark: Confidence-Scheduled Speculative Decoding with Semi-Autoregressive
+ *             Generation" (technical summary page): "Architecture (drafter)",
+ *             "Verification scheduling (system side)", "Infra".
+ *   [SGLANG]  "DSpark in SGLang" blog: "Verify modes", "Ragged verify under full CUDA graphs".
+ *   [VLLM]    "vLLM adaptive verification with DSpark": "DSpark confidence scheduling
+ *             mechanism", "Technical implementation and CUDA Graphs".
+ *
+ * Conventions for every entry point
+ *   - Pointers named as device pointers must point to device memory (or managed memory) of the
+ *     current device; host pointers are plain host memory.  All tensors are dense, row-major,
+ *     and every tensor pointer must be 16-byte aligned.
+ *   - The caller owns every buffer.  The library allocates nothing and keeps no per-call
+ *     state; scratch lives in the caller's workspace `ws` (size: dspark_workspace_bytes,
+ *     zeroed once with dspark_workspace_init before first use).
+ *   - Calls are enqueued on `stream` and return immediately.  The return value reports host-
+ *     side argument checks (DSPARK_EINVAL / DSPARK_EUNSUPPORTED, nothing is launched) and
+ *     launch failures (DSPARK_ECUDA).  Conditions only the device can see (a window larger
+ *     than gamma, a packed total beyond the largest tier, a wait that timed out) are recorded
+ *     in the workspace status word; dspark_read_device_status returns and clears it.
+ *   - No exception or abort crosses the ABI.
+ *   - Random numbers: Philox4x32-10 keyed by `seed`, counter (index >> 2, request, step low
+ *     32 bits, purpose << 24 | position << 16 | step bits 32..47).  Purposes: 1 draft chunk
+ *     key, 2 draft entry key, 3 accept uniform, 4 decision chunk key, 5 decision entry key.
+ *     A uniform is ((word >> 9) + 0.5) * 2^-23.  A step is reproducible from (seed, step).
+ *   - Sampling: a categorical draw over the vocabulary uses the two-level Gumbel-max rule:
+ *     chunks of DSPARK_CHUNK consecutive ids get key log(mass) + Gumbel; the best chunk is
+ *     drawn, then an id inside it by Gumbel-max over its log-weights.  Ties: lowest index.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DSPARK_API __attribute__((visibility("default")))
+#else
+#define DSPARK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* dspark_stream_t; /* identical to cudaStream_t; NULL = default stream */
+
+typedef enum {
+    DSPARK_OK = 0,
+    DSPARK_EINVAL = 1,       /* bad argument (host check) or bad data (device check)        */
+    DSPARK_EUNSUPPORTED = 2, /* valid but outside what this build supports (sizes, dtypes)   */
+    DSPARK_ECUDA = 3,        /* a CUDA runtime call or kernel launch failed                  */
+    DSPARK_ETIMEOUT = 4,     /* a device-side wait gave up (status word only)                */
+    DSPARK_EWORKSPACE = 5    /* workspace missing or smaller than dspark_workspace_bytes     */
+} dspark_status;
+
+typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
+
+typedef enum { DSPARK_STATIC = 0, DSPARK_COMPACT = 1, DSPARK_CAP_ACCEPT = 2 } dspark_verify_mode;
+
+typedef enum { DSPARK_SCHED_EARLY_STOP = 0, DSPARK_SCHED_GLOBAL_ARGMAX = 1 } dspark_sched_mode;
+
+#define DSPARK_MAX_BS 256     /* requests per step                                   */
+#define DSPARK_MAX_GAMMA 16   /* draft block length                                  */
+#define DSPARK_CHUNK 128      /* vocabulary chunk width of the two-level sampler     */
+
+/* Human-readable name of a status code (static string, never NULL). */
+DSPARK_API const char* dspark_status_string(int status);
+
+/* Bytes of workspace the calls of one step need for (bs, gamma, V); 0 on invalid sizes.
+ * One workspace serves every call of a step; calls on the same stream may share it, calls
+ * that can overlap on the device (different streams) must not. */
+DSPARK_API size_t dspark_workspace_bytes(int bs, int gamma, int V);
+
+/* Zero the workspace's status word (asynchronous memset on `stream`). */
+DSPARK_API int dspark_workspace_init(void* ws, size_t ws_bytes, dspark_stream_t stream);
+
+/* Synchronise `stream`, return the status recorded by device-side checks since the last
+ * read (DSPARK_OK if none) and clear it.  The only call that waits for the device. */
+DSPARK_API int dspark_read_device_status(void* ws, dspark_stream_t stream);
+
+/* Host: steps-per-second table from a profiled step-time curve ([VLLM] "Cost Modeling",
+ * "CUDA Graph Padding"; [SGLANG] "Ragged verify"; [SUMMARY] "Verification scheduling").
+ *   T_raw[M]   host, m_max+1 doubles: profiled step time (any unit) for M verify tokens.
+ *   tiers      host, n_tiers strictly increasing totals of the captured graphs; n_tiers = 0
+ *              means every total has its own graph.
+ *   sps_out[M] host, m_max+1 doubles: 1 / max_{M' <= tier(M)} T_raw[M'], where tier(M) is the
+ *              smallest tier >= M; 0 when tier(M) does not exist or exceeds m_max.
+ * Returns DSPARK_EINVAL on null pointers, m_max < 0, non-positive or non-finite times, or
+ * tiers that are not strictly increasing and positive. */
+DSPARK_API int dspark_build_sps(const double* T_raw, int m_max, const int32_t* tiers, int n_tiers,
+                     double* sps_out);
+
+/* S1. Markov-head block draft ([SUMMARY] "Architecture (drafter)", Markov head and
+ * left-to-right sampling).  For k = 1..gamma, per request:
+ *     l_k = U[:, k-1] + W1[x_{k-1}] . W2,   W2 = W2t^T,  x_0 = anchor
+ *     temperature > 0:  x_k ~ softmax(l_k / temperature)  (two-level Gumbel-max, purposes 1, 2)
+ *                       logit_x = l_k[x_k] / temperature,  lse = logsumexp(l_k / temperature)
+ *     temperature = 0:  x_k = argmax l_k (lowest index),  logit_x = l_k[x_k],  lse = 0
+ *   U        device [bs, gamma, V]  base logits U_1..U_gamma of the parallel backbone
+ *   W1       device [V, r]          Markov factor (row lookup by previous token)
+ *   W2t      device [V, r]          Markov projection, stored transposed (a Linear(r, V) weight)
+ *   dtype    element type of U, W1, W2t (fp32 or bf16); accumulation is fp32
+ *   anchor   device [bs] int32      x_0, in [0, V)
+ *   tokens   device [bs, gamma] int32 out;  logit_x, lse: device [bs, gamma] fp32 out
+ * Limits: 1 <= bs <= 256, 1 <= gamma <= 16, V % 8 == 0, 8 <= V < 2^24, r in {32, 64, 128, 256}.
+ * Errors: EINVAL (null, sizes, temperature < 0 or not finite, misaligned), EWORKSPACE. */
+DSPARK_API int dspark_draft_block(const void* U, const void* W1, const void* W2t, int dtype,
+                       const int32_t* anchor, int bs, int gamma, int V, int r,
+                       float temperature, uint64_t seed, uint64_t step,
+                       int32_t* tokens, float* logit_x, float* lse,
+                       void* ws, size_t ws_bytes, dspark_stream_t stream);
+
+/* S2. Confidence head, sequential temperature scaling and prefix survival ([SUMMARY]
+ * "Verification scheduling": confidence head, STS, prefix survival):
+ *     z_{r,k} = w[0:d] . h[r, k-1] + w[d:d+r] . W1[x_{r,k-1}] + b      (x_0 = anchor)
+ *     conf_{r,k} = 1 / (1 + exp(-z_{r,k} / sts_T[k-1]))
+ *     surv_{r,k} = conf_{r,1} * ... * conf_{r,k}        (fp32, left to right)
+ *   h        device [bs, gamma, d] (dtype);  W1 device [V, r] (dtype)
+ *   tokens   device [bs, gamma] int32 (x_1..x_gamma);  anchor device [bs] int32
+ *   w        device [d + r] fp32;  sts_T device [gamma] fp32, each > 0
+ *   conf, surv  device [bs, gamma] fp32 out
+ * Limits: as dspark_draft_block, and d % 8 == 0, 8 <= d <= 65536. */
+DSPARK_API int dspark_confidence(const void* h, const void* W1, int dtype, const int32_t* anchor,
+                      const int32_t* tokens, const float* w, float b, const float* sts_T,
+                      int bs, int gamma, int d, int r, int V,
+                      float* conf, float* surv, dspark_stream_t stream);
+
+/* S3. Hardware-aware global top-B prefix scheduler ([SUMMARY] "Verification scheduling",
+ * Algorithm 1; [VLLM] "DSpark confidence scheduling mechanism"; [SUMMARY] "Infra").
+ * Slots (r, j) are ranked by descending fp32 surv[r, j] (ties: lower r, then lower j).
+ * With S_K = sum over the first K slots of floor(surv * 2^40) (exact int64),
+ *     Theta(K) = (bs + S_K * 2^-40) * sps[bs + K],   K = 0 .. min(bs*gamma, m_max - bs)
+ * EARLY_STOP: K* = first K with Theta(K+1) <= Theta(K) (else the last K);
+ * GLOBAL_ARGMAX: K* = smallest K maximising Theta.  window[r] = admitted slots of r.
+ *   surv     device [bs, gamma] fp32, non-increasing along each row, in [0, 1]
+ *   sps      device [m_max + 1] fp64 (dspark_build_sps), m_max >= bs
+ *   window   device [bs] int32 out;  K_out device int32 out;  theta_out device fp64 out
+ * Limits: bs * gamma <= 4096.  One thread block; no host readback. */
+DSPARK_API int dspark_schedule(const float* surv, int bs, int gamma, const double* sps, int m_max,
+                    int mode, int32_t* window, int32_t* K_out, double* theta_out,
+                    dspark_stream_t stream);
+
+/* S4. Ragged cu_seqlens packing rounded up to a captured graph tier ([SGLANG] "Ragged verify
+ * under full CUDA graphs", Fig. 2; [VLLM] "Graph Capture", "CUDA Graph Padding").
+ * Request r contributes n_r = l_r + 1 rows [x_0, x_1 .. x_{l_r}] where l_r = window[r]
+ * (window == NULL: l_r = gamma, the static layout).  cu[0] = 0, cu[r+1] = cu[r] + n_r,
+ * M = cu[bs]; padded = smallest tier >= M (n_tiers = 0: padded = M).  Row p < M holds
+ * ids = token, req = request, pos = j; rows M .. padded-1 hold -1 in all three.
+ *   window   device [bs] int32 or NULL;  anchor device [bs];  tokens device [bs, gamma]
+ *   tiers    device [n_tiers] int32 strictly increasing;  cap = rows of ids/req/pos
+ *   cu_seqlens device [bs+1] int32 out;  ids, req, pos device [cap] int32 out
+ *   padded_total device [1] int32 out (-1 on a device-side error)
+ * Device errors (status word, EINVAL): l_r outside [0, gamma], M beyond the largest tier,
+ * padded > cap. */
+DSPARK_API int dspark_pack(const int32_t* window, const int32_t* anchor, const int32_t* tokens,
+                int bs, int gamma, const int32_t* tiers, int n_tiers, int cap,
+                int32_t* cu_seqlens, int32_t* ids, int32_t* req, int32_t* pos,
+                int32_t* padded_total, void* ws, size_t ws_bytes, dspark_stream_t stream);
+
+/* S5. Rejection-sampling verification ([SUMMARY] "Abstract", "Architecture (drafter)";
+ * [SGLANG] "Verify modes").  Per request r, with l_r = window[r]:
+ *   tested positions  L_test   = l_r (COMPACT) or gamma (STATIC, CAP_ACCEPT)
+ *   committed window  L_commit = l_r (COMPACT, CAP_ACCEPT) or gamma (STATIC)
+ *   target row scoring position k: cu_seqlens[r] + k - 1 (k = 1 .. L_test + 1); the packed
+ *   layout must give n_r = L_test + 1 (device check, EINVAL).
+ *   temperature > 0: x_k is accepted iff u_k < p_t(x_k) / p_d(x_k) with
+ *     log p_t = target_row/temperature at x_k minus its log-sum-exp, log p_d = logit_x - lse,
+ *     u_k the accept uniform (purpose 3, position k, index 0).  At the first rejection
+ *     k* <= L_commit the token is redrawn from normalise(max(0, p_t - p_d)) (p_t if that is
+ *     empty), p_d recomputed from U, W1, W2t at position k*; if no tested position up to
+ *     L_commit is rejected, a bonus token is drawn from p_t of row L_commit + 1
+ *     (decision draws: purposes 4, 5 at the drawn position).
+ *   temperature = 0: x_k is accepted iff it is the target argmax; the extra token is the
+ *     argmax of the deciding row.
+ *   out_tokens  device [bs, gamma+1] int32 out: x_1..x_acc, the extra token, then -1
+ *   acc_len     device [bs] int32 out: accepted draft tokens
+ *   ceiling     device [bs] int32 out or NULL: accepted count over the tested positions
+ *               (the full-block ceiling in CAP_ACCEPT mode)
+ *   target      device [rows, V] (dtype), rows >= cu_seqlens[bs]
+ *   window      device [bs] int32 (ignored in STATIC mode, may be NULL there)
+ *   tokens, logit_x, lse, anchor: the draft's outputs / inputs;  U, W1, W2t, r as in S1.
+ * Limits: as dspark_draft_block. */
+DSPARK_API int dspark_verify(const void* target, int dtype, const int32_t* cu_seqlens,
+                  const int32_t* window, int mode, int bs, int gamma, int V,
+                  const int32_t* anchor, const int32_t* tokens, const float* logit_x,
+                  const float* lse, const void* U, const void* W1, const void* W2t, int r,
+                  float temperature, uint64_t seed, uint64_t step,
+                  int32_t* out_tokens, int32_t* acc_len, int32_t* ceiling,
+                  void* ws, size_t ws_bytes, dspark_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

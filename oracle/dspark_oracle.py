@@ -210,7 +210,7 @@ def markov_logits(U_k: np.ndarray, W1: np.ndarray, W2t: np.ndarray, x_prev: np.n
 
 
 def draft_block(U, W1, W2t, anchor, temperature: float, seed: int, step: int,
-                dtype: str = "bf16", chunk: int = CHUNK):
+                dtype: str = "bf16", chunk: int = CHUNK, req_ids=None):
     """S1: draw x_1..x_gamma left to right from p_k(v) = softmax(U_k(v) + B_k(v)).
 
     [SUMMARY, "Architecture (drafter)"]: the parallel backbone yields U_1..U_gamma in one pass
@@ -222,7 +222,8 @@ def draft_block(U, W1, W2t, anchor, temperature: float, seed: int, step: int,
 
     Returns tokens [bs, gamma] int32, logit_x [bs, gamma] (tempered logit of the drawn
     token; raw logit at temperature 0), lse [bs, gamma] (log-sum-exp of the tempered
-    logits; 0 at temperature 0) and margin [bs, gamma] (decision margin)."""
+    logits; 0 at temperature 0) and margin [bs, gamma] (decision margin).
+    req_ids (optional) gives each row's request index in the random streams (default: row)."""
     U = to_f64(U, dtype)
     W1 = to_f64(W1, dtype)
     W2t = to_f64(W2t, dtype)
@@ -242,7 +243,8 @@ def draft_block(U, W1, W2t, anchor, temperature: float, seed: int, step: int,
                 margin[r, k - 1] = _top2_gap(ell[r])
             else:
                 t = ell[r] / temperature
-                v, mg = two_level_gumbel(t, seed, step, r, k, P_DRAFT_CHUNK, P_DRAFT_ELEM, chunk)
+                rid = r if req_ids is None else int(req_ids[r])
+                v, mg = two_level_gumbel(t, seed, step, rid, k, P_DRAFT_CHUNK, P_DRAFT_ELEM, chunk)
                 tokens[r, k - 1] = v
                 logit_x[r, k - 1] = t[v]
                 lse[r, k - 1] = logsumexp(t)
@@ -419,7 +421,7 @@ def pack(window, anchor, tokens, tiers, cap: int, gamma: Optional[int] = None):
 
 def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x, lse,
            U, W1, W2t, temperature: float, seed: int, step: int, dtype: str = "bf16",
-           chunk: int = CHUNK):
+           chunk: int = CHUNK, req_ids=None):
     """S5: accept the longest valid prefix of each request's window, then one more token.
 
     [SUMMARY, "Abstract" and "Architecture (drafter)"]: lossless speculative decoding accepts
@@ -441,7 +443,8 @@ def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x
     target_packed row cu[r] + k - 1 holds the target logits that score position k
     (k = 1..n_r).  Returns out_tokens [bs, gamma+1] (-1 padded), acc_len [bs],
     ceiling [bs] (tested-window accepted count; the full-block ceiling in cap-accept) and
-    margin [bs] (smallest decision margin among the decisions that shaped the output)."""
+    margin [bs] (smallest decision margin among the decisions that shaped the output).
+    req_ids (optional) gives each row's request index in the random streams (default: row)."""
     tgt = to_f64(target_packed, dtype)
     Uf = to_f64(U, dtype)
     W1f = to_f64(W1, dtype)
@@ -454,6 +457,7 @@ def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x
     ceiling = np.zeros(bs, dtype=np.int32)
     margin = np.full(bs, math.inf)
     for r in range(bs):
+        rid = r if req_ids is None else int(req_ids[r])
         lr = int(window[r]) if window is not None else gamma
         L_test = lr if mode == COMPACT else gamma
         L_commit = gamma if mode == STATIC else lr
@@ -477,7 +481,7 @@ def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x
                 lp_t = t[x[k]] - logsumexp(t)
                 lp_d = float(logit_x[r, k - 1]) - float(lse[r, k - 1])
                 ratio = math.exp(lp_t - lp_d)
-                u = float(uniform(seed, step, P_ACCEPT, r, k, 0))
+                u = float(uniform(seed, step, P_ACCEPT, rid, k, 0))
                 ok = u < ratio
                 mg = min(mg, abs(u - ratio))
             if not ok:
@@ -497,7 +501,7 @@ def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x
                 res = np.maximum(0.0, p_t - p_d)
                 with np.errstate(divide="ignore"):
                     logw = np.log(res) if res.sum() > 0.0 else t
-                x_new, m2 = two_level_gumbel(logw, seed, step, r, k, P_DECIDE_CHUNK, P_DECIDE_ELEM, chunk)
+                x_new, m2 = two_level_gumbel(logw, seed, step, rid, k, P_DECIDE_CHUNK, P_DECIDE_ELEM, chunk)
                 mg = min(mg, m2)
         else:
             acc = L_commit
@@ -508,7 +512,7 @@ def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x
                 mg = min(mg, _top2_gap(row))
             else:
                 t = trow(k) / temperature
-                x_new, m2 = two_level_gumbel(t, seed, step, r, k, P_DECIDE_CHUNK, P_DECIDE_ELEM, chunk)
+                x_new, m2 = two_level_gumbel(t, seed, step, rid, k, P_DECIDE_CHUNK, P_DECIDE_ELEM, chunk)
                 mg = min(mg, m2)
         out[r, :acc] = x[1:acc + 1]
         out[r, acc] = x_new

@@ -1,0 +1,178 @@
+"""Thin ctypes binding over libdspark.so (include/dspark.h).
+
+Same names as the C ABI; the only work here is argument marshalling: sizes are read from
+tensor shapes, pointers from data_ptr(), the stream from torch's current stream.  Every
+step of the path runs in the library's CUDA kernels.  If the library is missing the
+calls raise -- there is no fallback."""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+from . import build as _build
+
+DSPARK_OK, DSPARK_EINVAL, DSPARK_EUNSUPPORTED, DSPARK_ECUDA, DSPARK_ETIMEOUT, DSPARK_EWORKSPACE = range(6)
+DSPARK_F32, DSPARK_BF16 = 0, 1
+DSPARK_STATIC, DSPARK_COMPACT, DSPARK_CAP_ACCEPT = 0, 1, 2
+DSPARK_SCHED_EARLY_STOP, DSPARK_SCHED_GLOBAL_ARGMAX = 0, 1
+DSPARK_MAX_BS, DSPARK_MAX_GAMMA, DSPARK_CHUNK = 256, 16, 128
+
+_vp, _i, _f, _u64, _sz, _d = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t, ctypes.c_double
+
+_SIGS = {
+    "dspark_status_string": (ctypes.c_char_p, [_i]),
+    "dspark_workspace_bytes": (_sz, [_i, _i, _i]),
+    "dspark_workspace_init": (_i, [_vp, _sz, _vp]),
+    "dspark_read_device_status": (_i, [_vp, _vp]),
+    "dspark_build_sps": (_i, [_vp, _i, _vp, _i, _vp]),
+    "dspark_draft_block": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _u64, _u64,
+                                _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dspark_confidence": (_i, [_vp, _vp, _i, _vp, _vp, _vp, _f, _vp, _i, _i, _i, _i, _i,
+                               _vp, _vp, _vp]),
+    "dspark_schedule": (_i, [_vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp]),
+    "dspark_pack": (_i, [_vp, _vp, _vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dspark_verify": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                           _i, _f, _u64, _u64, _vp, _vp, _vp, _vp, _sz, _vp]),
+}
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+class DSparkError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {dspark_status_string(status) if _LIB else status}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load libdspark.so (built by __graft_entry__.build()); raise if it is not there."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libdspark.so is not built ({path}); run __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype, fn.argtypes = res, args
+        _LIB = L
+    return _LIB
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != DSPARK_OK:
+        raise DSparkError(rc, where)
+
+
+def _p(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libdspark must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is not None:
+        return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _dtype(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return DSPARK_F32
+    if t.dtype == torch.bfloat16:
+        return DSPARK_BF16
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+# ----------------------------------------------------------------------------- utilities
+
+def dspark_status_string(status: int) -> str:
+    return lib().dspark_status_string(int(status)).decode()
+
+
+def dspark_workspace_bytes(bs: int, gamma: int, V: int) -> int:
+    return int(lib().dspark_workspace_bytes(bs, gamma, V))
+
+
+def dspark_workspace_init(ws, stream=None) -> None:
+    _check(lib().dspark_workspace_init(_p(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "dspark_workspace_init")
+
+
+def dspark_read_device_status(ws, stream=None) -> int:
+    return int(lib().dspark_read_device_status(_p(ws), _stream(stream)))
+
+
+def alloc_workspace(bs: int, gamma: int, V: int, device="cuda"):
+    """A zero-initialised workspace tensor (allocated by PyTorch) for one step."""
+    import torch
+    n = dspark_workspace_bytes(bs, gamma, V)
+    if n == 0:
+        raise ValueError("invalid sizes for a workspace")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    dspark_workspace_init(ws)
+    return ws
+
+
+def dspark_build_sps(T_raw, tiers) -> np.ndarray:
+    """Host cost-table builder: sps[M] = 1 / T_mono(tier(M))."""
+    T = np.ascontiguousarray(T_raw, dtype=np.float64)
+    t = np.ascontiguousarray(tiers, dtype=np.int32)
+    out = np.empty_like(T)
+    _check(lib().dspark_build_sps(T.ctypes.data, T.size - 1, t.ctypes.data if t.size else None,
+                                  t.size, out.ctypes.data), "dspark_build_sps")
+    return out
+
+
+# ----------------------------------------------------------------------------- the path
+
+def dspark_draft_block(U, W1, W2t, anchor, temperature, seed, step, tokens, logit_x, lse, ws, stream=None):
+    bs, gamma, V = U.shape
+    r = W1.shape[1]
+    _check(lib().dspark_draft_block(_p(U), _p(W1), _p(W2t), _dtype(U), _p(anchor), bs, gamma, V, r,
+                                    float(temperature), int(seed), int(step), _p(tokens), _p(logit_x),
+                                    _p(lse), _p(ws), ws.numel(), _stream(stream)), "dspark_draft_block")
+
+
+def dspark_confidence(h, W1, anchor, tokens, w, b, sts_T, conf, surv, stream=None):
+    bs, gamma, d = h.shape
+    V, r = W1.shape
+    _check(lib().dspark_confidence(_p(h), _p(W1), _dtype(h), _p(anchor), _p(tokens), _p(w), float(b),
+                                   _p(sts_T), bs, gamma, d, r, V, _p(conf), _p(surv), _stream(stream)),
+           "dspark_confidence")
+
+
+def dspark_schedule(surv, sps, mode, window, K_out, theta_out, stream=None):
+    bs, gamma = surv.shape
+    _check(lib().dspark_schedule(_p(surv), bs, gamma, _p(sps), sps.numel() - 1, int(mode), _p(window),
+                                 _p(K_out), _p(theta_out), _stream(stream)), "dspark_schedule")
+
+
+def dspark_pack(window, anchor, tokens, tiers, cu_seqlens, ids, req, pos, padded_total, ws, stream=None):
+    bs, gamma = tokens.shape
+    n_t = 0 if tiers is None else tiers.numel()
+    _check(lib().dspark_pack(_p(window), _p(anchor), _p(tokens), bs, gamma, _p(tiers) if n_t else None, n_t,
+                             ids.numel(), _p(cu_seqlens), _p(ids), _p(req), _p(pos), _p(padded_total),
+                             _p(ws), ws.numel(), _stream(stream)), "dspark_pack")
+
+
+def dspark_verify(target, cu_seqlens, window, mode, anchor, tokens, logit_x, lse, U, W1, W2t,
+                  temperature, seed, step, out_tokens, acc_len, ceiling, ws, stream=None):
+    bs, gamma = tokens.shape
+    V = target.shape[1]
+    r = W1.shape[1]
+    _check(lib().dspark_verify(_p(target), _dtype(target), _p(cu_seqlens), _p(window), int(mode), bs, gamma,
+                               V, _p(anchor), _p(tokens), _p(logit_x), _p(lse), _p(U), _p(W1), _p(W2t), r,
+                               float(temperature), int(seed), int(step), _p(out_tokens), _p(acc_len),
+                               _p(ceiling), _p(ws), ws.numel(), _stream(stream)), "dspark_verify")

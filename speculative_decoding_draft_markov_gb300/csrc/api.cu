@@ -1,0 +1,196 @@
+// C ABI of libdspark: host-side argument checks, workspace handling and kernel launches.
+// Every entry point validates before launching anything; nothing here allocates memory.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace dspark;
+
+namespace {
+
+inline bool al(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA; }
+
+inline bool valid_dtype(int dt) { return dt == DSPARK_F32 || dt == DSPARK_BF16; }
+
+// Sizes shared by the draft, confidence and verify calls.
+int check_core(int bs, int gamma, int V, int r) {
+  if (bs < 1 || gamma < 1 || V < 8 || r < 1) return DSPARK_EINVAL;
+  if (V % 8 != 0) return DSPARK_EINVAL;
+  if (bs > DSPARK_MAX_BS || gamma > DSPARK_MAX_GAMMA || V >= (1 << 24)) return DSPARK_EUNSUPPORTED;
+  if (!(r == 32 || r == 64 || r == 128 || r == 256)) return DSPARK_EUNSUPPORTED;
+  return DSPARK_OK;
+}
+
+int check_ws(const void* ws, size_t ws_bytes, int bs, int gamma, int V) {
+  if (!ws || !al(ws, 256)) return DSPARK_EWORKSPACE;
+  if (ws_bytes < ws_layout(bs, gamma, V).total) return DSPARK_EWORKSPACE;
+  return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dspark_status_string(int status) {
+  switch (status) {
+    case DSPARK_OK: return "DSPARK_OK";
+    case DSPARK_EINVAL: return "DSPARK_EINVAL: invalid argument or data";
+    case DSPARK_EUNSUPPORTED: return "DSPARK_EUNSUPPORTED: outside the supported sizes or types";
+    case DSPARK_ECUDA: return "DSPARK_ECUDA: CUDA runtime or launch failure";
+    case DSPARK_ETIMEOUT: return "DSPARK_ETIMEOUT: a device-side wait timed out";
+    case DSPARK_EWORKSPACE: return "DSPARK_EWORKSPACE: workspace missing, misaligned or too small";
+    default: return "DSPARK_UNKNOWN";
+  }
+}
+
+size_t dspark_workspace_bytes(int bs, int gamma, int V) {
+  if (bs < 1 || gamma < 1 || V < 8 || bs > DSPARK_MAX_BS || gamma > DSPARK_MAX_GAMMA || V >= (1 << 24))
+    return 0;
+  return ws_layout(bs, gamma, V).total;
+}
+
+int dspark_workspace_init(void* ws, size_t ws_bytes, dspark_stream_t stream) {
+  if (!ws || ws_bytes < 256 || !al(ws, 256)) return DSPARK_EWORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, 256, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dspark_read_device_status(void* ws, dspark_stream_t stream) {
+  if (!ws || !al(ws, 256)) return DSPARK_EWORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DSPARK_ECUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return DSPARK_ECUDA;
+  if (word != 0 && cudaMemset(ws, 0, sizeof(word)) != cudaSuccess) return DSPARK_ECUDA;
+  return static_cast<int>(word);
+}
+
+int dspark_build_sps(const double* T_raw, int m_max, const int32_t* tiers, int n_tiers,
+                     double* sps_out) {
+  if (!T_raw || !sps_out || m_max < 0 || n_tiers < 0 || (n_tiers > 0 && !tiers)) return DSPARK_EINVAL;
+  for (int i = 0; i < n_tiers; ++i)
+    if (tiers[i] <= 0 || (i > 0 && tiers[i] <= tiers[i - 1])) return DSPARK_EINVAL;
+  for (int M = 0; M <= m_max; ++M)
+    if (!(T_raw[M] > 0.0) || !std::isfinite(T_raw[M])) return DSPARK_EINVAL;
+  // running maximum of the profiled curve, then the tier staircase
+  double run = 0.0;
+  int ti = 0;
+  for (int M = 0; M <= m_max; ++M) {
+    run = (M == 0 || T_raw[M] > run) ? T_raw[M] : run;
+    sps_out[M] = run;  // T_mono[M] (replaced below)
+  }
+  for (int M = 0; M <= m_max; ++M) {
+    int tier = M;
+    if (n_tiers > 0) {
+      while (ti < n_tiers && tiers[ti] < M) ++ti;
+      tier = (ti < n_tiers) ? tiers[ti] : -1;
+    }
+    // sps_out[t] still holds T_mono for t >= M: tier >= M
+    sps_out[M] = (tier < 0 || tier > m_max) ? 0.0 : 1.0 / sps_out[tier];
+  }
+  return DSPARK_OK;
+}
+
+int dspark_draft_block(const void* U, const void* W1, const void* W2t, int dtype,
+                       const int32_t* anchor, int bs, int gamma, int V, int r, float temperature,
+                       uint64_t seed, uint64_t step, int32_t* tokens, float* logit_x, float* lse,
+                       void* ws, size_t ws_bytes, dspark_stream_t stream) {
+  if (!U || !W1 || !W2t || !anchor || !tokens || !logit_x || !lse) return DSPARK_EINVAL;
+  if (!valid_dtype(dtype) || !std::isfinite(temperature) || temperature < 0.f) return DSPARK_EINVAL;
+  if (int e = check_core(bs, gamma, V, r)) return e;
+  if (!al(U, 16) || !al(W1, 16) || !al(W2t, 16) || !al(anchor, 4) || !al(tokens, 4) ||
+      !al(logit_x, 4) || !al(lse, 4))
+    return DSPARK_EINVAL;
+  if (int e = check_ws(ws, ws_bytes, bs, gamma, V)) return e;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(bs, gamma, V);
+  char* w = static_cast<char*>(ws);
+  void* stats = w + L.stats;
+  uint32_t* status = reinterpret_cast<uint32_t*>(w + L.status);
+  const int greedy = temperature == 0.f;
+  const float inv_tau = greedy ? 1.f : static_cast<float>(1.0 / static_cast<double>(temperature));
+  const bool tc = draft_tc_supported(dtype, bs, V, r);
+  for (int k = 1; k <= gamma; ++k) {
+    cudaError_t e = tc ? launch_draft_stats_tc(U, W1, W2t, anchor, tokens, bs, gamma, V, r, k, inv_tau,
+                                               greedy, stats, L.n_chunks, status, s)
+                       : launch_draft_stats_simt(dtype, U, W1, W2t, anchor, tokens, bs, gamma, V, r, k,
+                                                 inv_tau, greedy, stats, L.n_chunks, s);
+    if (e != cudaSuccess) return DSPARK_ECUDA;
+    e = launch_draft_select(dtype, stats, L.n_chunks, U, W1, W2t, anchor, tokens, logit_x, lse, bs,
+                            gamma, V, r, k, inv_tau, greedy, seed, step, s);
+    if (e != cudaSuccess) return DSPARK_ECUDA;
+  }
+  return DSPARK_OK;
+}
+
+int dspark_confidence(const void* h, const void* W1, int dtype, const int32_t* anchor,
+                      const int32_t* tokens, const float* w, float b, const float* sts_T, int bs,
+                      int gamma, int d, int r, int V, float* conf, float* surv,
+                      dspark_stream_t stream) {
+  if (!h || !W1 || !anchor || !tokens || !w || !sts_T || !conf || !surv) return DSPARK_EINVAL;
+  if (!valid_dtype(dtype) || !std::isfinite(b)) return DSPARK_EINVAL;
+  if (int e = check_core(bs, gamma, V, r)) return e;
+  if (d < 8 || d % 8 != 0) return DSPARK_EINVAL;
+  if (d > 65536) return DSPARK_EUNSUPPORTED;
+  if (!al(h, 16) || !al(W1, 16) || !al(w, 16) || !al(anchor, 4) || !al(tokens, 4) ||
+      !al(sts_T, 4) || !al(conf, 4) || !al(surv, 4))
+    return DSPARK_EINVAL;
+  return cuda_status(launch_confidence(dtype, h, W1, anchor, tokens, w, b, sts_T, bs, gamma, d, r, V,
+                                       conf, surv, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dspark_schedule(const float* surv, int bs, int gamma, const double* sps, int m_max, int mode,
+                    int32_t* window, int32_t* K_out, double* theta_out, dspark_stream_t stream) {
+  if (!surv || !sps || !window || !K_out || !theta_out) return DSPARK_EINVAL;
+  if (bs < 1 || gamma < 1 || m_max < bs) return DSPARK_EINVAL;
+  if (mode != DSPARK_SCHED_EARLY_STOP && mode != DSPARK_SCHED_GLOBAL_ARGMAX) return DSPARK_EINVAL;
+  if (bs > DSPARK_MAX_BS || gamma > DSPARK_MAX_GAMMA || bs * gamma > 4096) return DSPARK_EUNSUPPORTED;
+  if (!al(surv, 4) || !al(sps, 8) || !al(window, 4) || !al(K_out, 4) || !al(theta_out, 8))
+    return DSPARK_EINVAL;
+  return cuda_status(launch_schedule(surv, bs, gamma, sps, m_max, mode, window, K_out, theta_out,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dspark_pack(const int32_t* window, const int32_t* anchor, const int32_t* tokens, int bs,
+                int gamma, const int32_t* tiers, int n_tiers, int cap, int32_t* cu_seqlens,
+                int32_t* ids, int32_t* req, int32_t* pos, int32_t* padded_total, void* ws,
+                size_t ws_bytes, dspark_stream_t stream) {
+  if (!anchor || !tokens || !cu_seqlens || !ids || !req || !pos || !padded_total) return DSPARK_EINVAL;
+  if (n_tiers < 0 || (n_tiers > 0 && !tiers) || cap < 1) return DSPARK_EINVAL;
+  if (bs < 1 || gamma < 1) return DSPARK_EINVAL;
+  if (bs > DSPARK_MAX_BS || gamma > DSPARK_MAX_GAMMA) return DSPARK_EUNSUPPORTED;
+  if (!ws || !al(ws, 256) || ws_bytes < 256) return DSPARK_EWORKSPACE;
+  return cuda_status(launch_pack(window, anchor, tokens, bs, gamma, tiers, n_tiers, cap, cu_seqlens,
+                                 ids, req, pos, padded_total, static_cast<uint32_t*>(ws),
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dspark_verify(const void* target, int dtype, const int32_t* cu_seqlens, const int32_t* window,
+                  int mode, int bs, int gamma, int V, const int32_t* anchor, const int32_t* tokens,
+                  const float* logit_x, const float* lse, const void* U, const void* W1,
+                  const void* W2t, int r, float temperature, uint64_t seed, uint64_t step,
+                  int32_t* out_tokens, int32_t* acc_len, int32_t* ceiling, void* ws,
+                  size_t ws_bytes, dspark_stream_t stream) {
+  if (!target || !cu_seqlens || !anchor || !tokens || !logit_x || !lse || !U || !W1 || !W2t ||
+      !out_tokens || !acc_len)
+    return DSPARK_EINVAL;
+  if (mode != DSPARK_STATIC && mode != DSPARK_COMPACT && mode != DSPARK_CAP_ACCEPT) return DSPARK_EINVAL;
+  if (mode != DSPARK_STATIC && !window) return DSPARK_EINVAL;
+  if (mode == DSPARK_CAP_ACCEPT && !ceiling) return DSPARK_EINVAL;
+  if (!valid_dtype(dtype) || !std::isfinite(temperature) || temperature < 0.f) return DSPARK_EINVAL;
+  if (int e = check_core(bs, gamma, V, r)) return e;
+  if (!al(target, 16) || !al(U, 16) || !al(W1, 16) || !al(W2t, 16)) return DSPARK_EINVAL;
+  if (int e = check_ws(ws, ws_bytes, bs, gamma, V)) return e;
+  const int greedy = temperature == 0.f;
+  const float inv_tau = greedy ? 1.f : static_cast<float>(1.0 / static_cast<double>(temperature));
+  return cuda_status(launch_verify(dtype, target, cu_seqlens, window, mode, bs, gamma, V, anchor,
+                                   tokens, logit_x, lse, U, W1, W2t, r, inv_tau, greedy, seed, step,
+                                   out_tokens, acc_len, ceiling, ws,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

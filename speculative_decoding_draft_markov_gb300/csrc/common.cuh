@@ -1,0 +1,232 @@
+// Shared device helpers of libdspark: status word, workspace layout, Philox4x32-10 uniforms,
+// Gumbel keys, element loads and deterministic block reductions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+constexpr int kChunk = DSPARK_CHUNK;
+
+// Philox purposes (counter word 3, bits 24..31).
+enum Purpose : uint32_t {
+  kDraftChunk = 1,
+  kDraftElem = 2,
+  kAccept = 3,
+  kDecideChunk = 4,
+  kDecideElem = 5,
+};
+
+// Decision kinds written by the verify decide pass.
+enum DecisionKind : int { kDecNone = 0, kDecResidual = 1, kDecBonus = 2 };
+
+// ----------------------------------------------------------------------------------------
+// Workspace layout (all offsets 256-byte aligned)
+//   status   : uint32 status word (first device-detected error wins)
+//   stats    : float2 [bs][n_chunks]       per-(row, chunk) partial statistics
+//   rowstats : RowStat [bs * (gamma + 1)]  per packed target row
+//   dec      : Decision [bs]               per-request verify decision
+// ----------------------------------------------------------------------------------------
+struct RowStat {
+  float lse;     // log-sum-exp of the tempered target row (temperature > 0)
+  float tx;      // tempered target logit of the tested draft token (or raw at T = 0)
+  int argmax;    // lowest-index argmax of the row (temperature 0)
+  int pad;
+};
+
+struct Decision {
+  int kdec;      // position drawn by the decision (1 .. gamma + 1)
+  int pdec;      // packed target row of that position
+  int kind;      // DecisionKind
+  int acc;       // accepted draft tokens
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t status = 0, stats = 0, rowstats = 0, dec = 0, total = 0;
+  int n_chunks = 0;
+};
+
+__host__ __device__ inline WsLayout ws_layout(int bs, int gamma, int V) {
+  WsLayout L;
+  L.n_chunks = (V + kChunk - 1) / kChunk;
+  size_t off = 0;
+  L.status = off;
+  off += 256;
+  L.stats = off;
+  off += align256(size_t(bs) * L.n_chunks * sizeof(float2));
+  L.rowstats = off;
+  off += align256(size_t(bs) * (gamma + 1) * sizeof(RowStat));
+  L.dec = off;
+  off += align256(size_t(bs) * sizeof(Decision));
+  L.total = off;
+  return L;
+}
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t code) {
+  if (status) atomicCAS(status, 0u, code);
+}
+
+// Token ids read from device memory index weight rows: clamp into [0, V) so that bad data
+// can never address outside W1 (the kernels that own a status word also report it).
+__device__ __forceinline__ int clamp_token(int x, int V) { return x < 0 ? 0 : (x >= V ? V - 1 : x); }
+
+// ----------------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): per round
+//   (c0, c1, c2, c3) <- (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0))
+// with the key advanced by the Weyl constants between rounds.
+// ----------------------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// The four words of counter group `grp` (indices 4*grp .. 4*grp+3) of one stream.
+__device__ __forceinline__ uint4 philox_group(uint64_t seed, uint64_t step, uint32_t purpose,
+                                              uint32_t req, uint32_t pos, uint32_t grp) {
+  const uint4 c = make_uint4(grp, req, uint32_t(step),
+                             (purpose << 24) | ((pos & 0xFFu) << 16) | uint32_t((step >> 32) & 0xFFFFu));
+  return philox10(c, uint32_t(seed), uint32_t(seed >> 32));
+}
+
+__device__ __forceinline__ uint32_t pick_word(uint4 w, int lane) {
+  return lane == 0 ? w.x : lane == 1 ? w.y : lane == 2 ? w.z : w.w;
+}
+
+// u = ((bits >> 9) + 1/2) 2^-23, exactly: [1, 2) from the mantissa, minus (1 - 2^-24).
+__device__ __forceinline__ float bits_to_uniform(uint32_t b) {
+  return __uint_as_float(0x3F800000u | (b >> 9)) - __uint_as_float(0x3F7FFFFFu);
+}
+
+__device__ __forceinline__ float gumbel_from_bits(uint32_t b) {
+  return -logf(-logf(bits_to_uniform(b)));
+}
+
+// ----------------------------------------------------------------------------------------
+// Element loads
+// ----------------------------------------------------------------------------------------
+template <typename T> __device__ __forceinline__ float ld_f32(const T* p, size_t i);
+template <> __device__ __forceinline__ float ld_f32<float>(const float* p, size_t i) { return p[i]; }
+template <> __device__ __forceinline__ float ld_f32<__nv_bfloat16>(const __nv_bfloat16* p, size_t i) {
+  return __bfloat162float(p[i]);
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ----------------------------------------------------------------------------------------
+// Deterministic reductions (fixed shuffle tree, fixed warp order)
+// ----------------------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// (value, index) argmax; ties -> lower index.  Index INT_MAX marks "none".
+struct ArgMax {
+  float v;
+  int i;
+};
+__device__ __forceinline__ ArgMax better(ArgMax a, ArgMax b) {
+  if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+  return a;
+}
+__device__ __forceinline__ ArgMax warp_argmax(ArgMax a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ArgMax b{__shfl_xor_sync(0xFFFFFFFFu, a.v, o), __shfl_xor_sync(0xFFFFFFFFu, a.i, o)};
+    a = better(a, b);
+  }
+  return a;
+}
+
+// Online log-sum-exp pair: value = m + log(s).
+struct LsePair {
+  float m;
+  float s;
+};
+__device__ __forceinline__ LsePair lse_merge(LsePair a, LsePair b) {
+  if (b.s == 0.f) return a;
+  if (a.s == 0.f) return b;
+  const float m = fmaxf(a.m, b.m);
+  return LsePair{m, a.s * expf(a.m - m) + b.s * expf(b.m - m)};
+}
+__device__ __forceinline__ LsePair warp_lse(LsePair a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    LsePair b{__shfl_xor_sync(0xFFFFFFFFu, a.m, o), __shfl_xor_sync(0xFFFFFFFFu, a.s, o)};
+    a = lse_merge(a, b);
+  }
+  return a;
+}
+
+// Block-wide reductions for blockDim.x = NT (multiple of 32).  `scratch` needs NT/32 slots.
+// Every thread returns the result.  Order: warp tree, then warps 0..NT/32-1 in order.
+template <int NT>
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) scratch[w] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < NT / 32; ++i) t += scratch[i];
+  return t;
+}
+template <int NT>
+__device__ __forceinline__ float block_max(float v, float* scratch) {
+  v = warp_max(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) scratch[w] = v;
+  __syncthreads();
+  float t = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < NT / 32; ++i) t = fmaxf(t, scratch[i]);
+  return t;
+}
+template <int NT>
+__device__ __forceinline__ ArgMax block_argmax(ArgMax a, float* sv, int* si) {
+  a = warp_argmax(a);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) { sv[w] = a.v; si[w] = a.i; }
+  __syncthreads();
+  ArgMax t{sv[0], si[0]};
+#pragma unroll
+  for (int i = 1; i < NT / 32; ++i) t = better(t, ArgMax{sv[i], si[i]});
+  return t;
+}
+template <int NT>
+__device__ __forceinline__ LsePair block_lse(LsePair a, float* sm, float* ss) {
+  a = warp_lse(a);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) { sm[w] = a.m; ss[w] = a.s; }
+  __syncthreads();
+  LsePair t{sm[0], ss[0]};
+#pragma unroll
+  for (int i = 1; i < NT / 32; ++i) t = lse_merge(t, LsePair{sm[i], ss[i]});
+  return t;
+}
+
+}  // namespace dspark

@@ -1,0 +1,194 @@
+// S1 -- Markov-head block draft: per-position chunk statistics (CUDA-core path) and the
+// per-row merge + two-level Gumbel-max draw.
+//
+// DSpark technical summary, "Architecture (drafter)": the sequential Markov head adds the
+// rank-r bias W1[x_{k-1}] W2 to the backbone's base logits U_k and samples left to right.
+// One position k is two launches: draft_stats (every (row, 128-id chunk) -> partial
+// statistics in the workspace) and draft_select (one block per row: merge, draw x_k).
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dspark {
+
+// ---------------------------------------------------------------------------------------
+// CUDA-core statistics pass.  Block = 128 threads = one 128-id chunk; RB rows per block.
+// Serves fp32 inputs (exact fp32 FMA) and small problems; bf16 at scale uses the
+// tensor-core pass in draft_tc.cu.
+// ---------------------------------------------------------------------------------------
+template <typename T, int RB>
+__global__ void __launch_bounds__(128) draft_stats_simt_kernel(
+    const T* __restrict__ U, const T* __restrict__ W1, const T* __restrict__ W2t,
+    const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens, int bs, int gamma,
+    int V, int r, int k, float inv_tau, int greedy, float2* __restrict__ stats, int n_chunks) {
+  __shared__ float sA[RB][64];
+  __shared__ float sW[kChunk][65];
+  __shared__ float red[4];
+  __shared__ int redi[4];
+  const int c = blockIdx.x, rb = blockIdx.y * RB, tid = threadIdx.x;
+  const int v = c * kChunk + tid;
+  float acc[RB];
+#pragma unroll
+  for (int rr = 0; rr < RB; ++rr) acc[rr] = 0.f;
+
+  for (int i0 = 0; i0 < r; i0 += 64) {
+    const int sl = min(64, r - i0);
+    for (int e = tid; e < RB * sl; e += kChunk) {
+      const int rr = e / sl, ii = e % sl, row = rb + rr;
+      float val = 0.f;
+      if (row < bs) {
+        const int xp = clamp_token((k == 1) ? anchor[row] : tokens[row * gamma + k - 2], V);
+        val = ld_f32(W1, size_t(xp) * r + i0 + ii);
+      }
+      sA[rr][ii] = val;
+    }
+    for (int e = tid; e < kChunk * sl; e += kChunk) {
+      const int vv = e / sl, ii = e % sl, vg = c * kChunk + vv;
+      sW[vv][ii] = (vg < V) ? ld_f32(W2t, size_t(vg) * r + i0 + ii) : 0.f;
+    }
+    __syncthreads();
+    for (int ii = 0; ii < sl; ++ii) {
+      const float w = sW[tid][ii];
+#pragma unroll
+      for (int rr = 0; rr < RB; ++rr) acc[rr] = fmaf(sA[rr][ii], w, acc[rr]);
+    }
+    __syncthreads();
+  }
+
+  const bool valid = v < V;
+#pragma unroll
+  for (int rr = 0; rr < RB; ++rr) {
+    const int row = rb + rr;
+    if (row >= bs) break;  // uniform over the block
+    const float l = valid ? acc[rr] + ld_f32(U, (size_t(row) * gamma + (k - 1)) * V + v) : 0.f;
+    if (greedy) {
+      const ArgMax am = block_argmax<kChunk>(ArgMax{valid ? l : -INFINITY, valid ? v : INT_MAX}, red, redi);
+      if (tid == 0) stats[size_t(row) * n_chunks + c] = make_float2(am.v, __int_as_float(am.i));
+    } else {
+      const float t = valid ? l * inv_tau : -INFINITY;
+      const float m = block_max<kChunk>(t, red);
+      const float s = block_sum<kChunk>(valid ? expf(t - m) : 0.f, red);
+      if (tid == 0) stats[size_t(row) * n_chunks + c] = make_float2(m, s);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Select pass: one 256-thread block per row.
+//   temperature > 0: row LSE = merge of the chunk pairs; chunk key = m_c + log s_c + G_c
+//   (purpose 1, index c); best chunk c*; the 128 logits of c* are recomputed (fixed-order
+//   fp32 dot products) and the entry key t_v + G'_v (purpose 2, index v - 128 c*) picks x_k.
+//   temperature = 0: lowest-index argmax over the chunk maxima.
+// ---------------------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) draft_select_kernel(
+    const float2* __restrict__ stats, int n_chunks, const T* __restrict__ U,
+    const T* __restrict__ W1, const T* __restrict__ W2t, const int32_t* __restrict__ anchor,
+    int32_t* __restrict__ tokens, float* __restrict__ logit_x, float* __restrict__ lse, int bs,
+    int gamma, int V, int r, int k, float inv_tau, int greedy, uint64_t seed, uint64_t step) {
+  __shared__ float sA[256];
+  __shared__ float tv[kChunk];
+  __shared__ float rv[8], rs[8];
+  __shared__ int ri[8];
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const float2* st = stats + size_t(b) * n_chunks;
+  const size_t out = size_t(b) * gamma + (k - 1);
+
+  if (greedy) {
+    ArgMax best{-INFINITY, INT_MAX};
+    for (int c = tid; c < n_chunks; c += 256) {
+      const float2 s2 = st[c];
+      best = better(best, ArgMax{s2.x, __float_as_int(s2.y)});
+    }
+    best = block_argmax<256>(best, rv, ri);
+    if (tid == 0) {
+      tokens[out] = best.i;
+      logit_x[out] = best.v;
+      lse[out] = 0.f;
+    }
+    return;
+  }
+
+  LsePair lp{-INFINITY, 0.f};
+  ArgMax best{-INFINITY, INT_MAX};
+  const int n_grp = (n_chunks + 3) / 4;
+  for (int g = tid; g < n_grp; g += 256) {
+    const uint4 w = philox_group(seed, step, kDraftChunk, b, k, g);
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      const int c = 4 * g + l;
+      if (c >= n_chunks) break;
+      const float2 s2 = st[c];
+      lp = lse_merge(lp, LsePair{s2.x, s2.y});
+      if (s2.y > 0.f) best = better(best, ArgMax{s2.x + logf(s2.y) + gumbel_from_bits(pick_word(w, l)), c});
+    }
+  }
+  lp = block_lse<256>(lp, rv, rs);
+  best = block_argmax<256>(best, rv, ri);
+  const int cstar = (best.i == INT_MAX) ? 0 : best.i;  // only non-finite statistics leave it unset
+
+  const int xp = clamp_token((k == 1) ? anchor[b] : tokens[size_t(b) * gamma + k - 2], V);
+  for (int i = tid; i < r; i += 256) sA[i] = ld_f32(W1, size_t(xp) * r + i);
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int vv = warp; vv < kChunk; vv += 8) {
+    const int v = cstar * kChunk + vv;
+    float dot = 0.f;
+    if (v < V)
+      for (int i = lane; i < r; i += 32) dot = fmaf(sA[i], ld_f32(W2t, size_t(v) * r + i), dot);
+    dot = warp_sum(dot);
+    if (lane == 0)
+      tv[vv] = (v < V) ? (dot + ld_f32(U, (size_t(b) * gamma + (k - 1)) * V + v)) * inv_tau : -INFINITY;
+  }
+  __syncthreads();
+  ArgMax e{-INFINITY, INT_MAX};
+  if (tid < kChunk) {
+    const uint4 w = philox_group(seed, step, kDraftElem, b, k, tid >> 2);
+    const float t = tv[tid];
+    if (t > -INFINITY) e = ArgMax{t + gumbel_from_bits(pick_word(w, tid & 3)), tid};
+  }
+  e = block_argmax<256>(e, rv, ri);
+  if (tid == 0) {
+    const int ei = (e.i == INT_MAX) ? 0 : e.i;
+    tokens[out] = min(cstar * kChunk + ei, V - 1);
+    logit_x[out] = tv[ei];
+    lse[out] = lp.m + logf(lp.s);
+  }
+}
+
+cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, const void* W2t,
+                                    const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
+                                    int V, int r, int k, float inv_tau, int greedy, void* stats,
+                                    int n_chunks, cudaStream_t s) {
+  constexpr int RB = 32;
+  dim3 grid(n_chunks, (bs + RB - 1) / RB);
+  if (dtype == DSPARK_F32)
+    draft_stats_simt_kernel<float, RB><<<grid, kChunk, 0, s>>>(
+        (const float*)U, (const float*)W1, (const float*)W2t, anchor, tokens, bs, gamma, V, r, k,
+        inv_tau, greedy, (float2*)stats, n_chunks);
+  else
+    draft_stats_simt_kernel<__nv_bfloat16, RB><<<grid, kChunk, 0, s>>>(
+        (const __nv_bfloat16*)U, (const __nv_bfloat16*)W1, (const __nv_bfloat16*)W2t, anchor,
+        tokens, bs, gamma, V, r, k, inv_tau, greedy, (float2*)stats, n_chunks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_draft_select(int dtype, const void* stats, int n_chunks, const void* U,
+                                const void* W1, const void* W2t, const int32_t* anchor,
+                                int32_t* tokens, float* logit_x, float* lse, int bs, int gamma,
+                                int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
+                                uint64_t step, cudaStream_t s) {
+  if (dtype == DSPARK_F32)
+    draft_select_kernel<float><<<bs, 256, 0, s>>>(
+        (const float2*)stats, n_chunks, (const float*)U, (const float*)W1, (const float*)W2t,
+        anchor, tokens, logit_x, lse, bs, gamma, V, r, k, inv_tau, greedy, seed, step);
+  else
+    draft_select_kernel<__nv_bfloat16><<<bs, 256, 0, s>>>(
+        (const float2*)stats, n_chunks, (const __nv_bfloat16*)U, (const __nv_bfloat16*)W1,
+        (const __nv_bfloat16*)W2t, anchor, tokens, logit_x, lse, bs, gamma, V, r, k, inv_tau,
+        greedy, seed, step);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

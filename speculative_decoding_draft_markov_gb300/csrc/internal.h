@@ -1,0 +1,51 @@
+// Internal launchers of libdspark (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dspark {
+
+// ---- S1 draft ---------------------------------------------------------------------------
+// Per-(row, chunk) statistics of l_k = U_k + W1[x_{k-1}] W2 for one position k:
+//   temperature > 0: (max t, sum exp(t - max)) with t = l * inv_tau
+//   temperature = 0: (max l, lowest argmax as int bits)
+cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, const void* W2t,
+                                    const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
+                                    int V, int r, int k, float inv_tau, int greedy, void* stats,
+                                    int n_chunks, cudaStream_t s);
+// Same statistics on the tensor cores (tcgen05 + TMEM + TMA), bf16 only.
+cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t,
+                                  const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
+                                  int V, int r, int k, float inv_tau, int greedy, void* stats,
+                                  int n_chunks, uint32_t* status, cudaStream_t s);
+bool draft_tc_supported(int dtype, int bs, int V, int r);
+// Merge the chunk statistics of one position and draw x_k.
+cudaError_t launch_draft_select(int dtype, const void* stats, int n_chunks, const void* U,
+                                const void* W1, const void* W2t, const int32_t* anchor,
+                                int32_t* tokens, float* logit_x, float* lse, int bs, int gamma,
+                                int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
+                                uint64_t step, cudaStream_t s);
+
+// ---- S2 / S3 / S4 -----------------------------------------------------------------------
+cudaError_t launch_confidence(int dtype, const void* h, const void* W1, const int32_t* anchor,
+                              const int32_t* tokens, const float* w, float b, const float* sts_T,
+                              int bs, int gamma, int d, int r, int V, float* conf, float* surv,
+                              cudaStream_t s);
+cudaError_t launch_schedule(const float* surv, int bs, int gamma, const double* sps, int m_max,
+                            int mode, int32_t* window, int32_t* K_out, double* theta_out,
+                            cudaStream_t s);
+cudaError_t launch_pack(const int32_t* window, const int32_t* anchor, const int32_t* tokens,
+                        int bs, int gamma, const int32_t* tiers, int n_tiers, int cap,
+                        int32_t* cu, int32_t* ids, int32_t* req, int32_t* pos, int32_t* padded,
+                        uint32_t* status, cudaStream_t s);
+
+// ---- S5 verify --------------------------------------------------------------------------
+cudaError_t launch_verify(int dtype, const void* target, const int32_t* cu, const int32_t* window,
+                          int mode, int bs, int gamma, int V, const int32_t* anchor,
+                          const int32_t* tokens, const float* logit_x, const float* lse,
+                          const void* U, const void* W1, const void* W2t, int r, float inv_tau,
+                          int greedy, uint64_t seed, uint64_t step, int32_t* out_tokens,
+                          int32_t* acc_len, int32_t* ceiling, void* ws, cudaStream_t s);
+
+}  // namespace dspark

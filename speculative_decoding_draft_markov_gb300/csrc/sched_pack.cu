@@ -1,0 +1,345 @@
+// S2 confidence head + STS + prefix survival, S3 global top-B prefix scheduler, S4 ragged
+// packing.  All three are small, latency-bound kernels that keep the step on the device.
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dspark {
+
+// ---------------------------------------------------------------------------------------
+// S2.  DSpark technical summary, "Verification scheduling (system side)": the confidence
+// head is a linear projection of [h_k ; W1[x_{k-1}]] followed by a sigmoid; sequential
+// temperature scaling divides the logit by T_k; prefix survival is the running product.
+// One block per request, one warp per position; fp32 dot products in a fixed order.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float dot_chunk8(const __nv_bfloat16* x, const float* w) {
+  const uint4 q = *reinterpret_cast<const uint4*>(x);
+  const float4 w0 = *reinterpret_cast<const float4*>(w);
+  const float4 w1 = *reinterpret_cast<const float4*>(w + 4);
+  float a = bf16lo(q.x) * w0.x;
+  a = fmaf(bf16hi(q.x), w0.y, a);
+  a = fmaf(bf16lo(q.y), w0.z, a);
+  a = fmaf(bf16hi(q.y), w0.w, a);
+  a = fmaf(bf16lo(q.z), w1.x, a);
+  a = fmaf(bf16hi(q.z), w1.y, a);
+  a = fmaf(bf16lo(q.w), w1.z, a);
+  a = fmaf(bf16hi(q.w), w1.w, a);
+  return a;
+}
+__device__ __forceinline__ float dot_chunk8(const float* x, const float* w) {
+  const float4 x0 = *reinterpret_cast<const float4*>(x), x1 = *reinterpret_cast<const float4*>(x + 4);
+  const float4 w0 = *reinterpret_cast<const float4*>(w), w1 = *reinterpret_cast<const float4*>(w + 4);
+  float a = x0.x * w0.x;
+  a = fmaf(x0.y, w0.y, a);
+  a = fmaf(x0.z, w0.z, a);
+  a = fmaf(x0.w, w0.w, a);
+  a = fmaf(x1.x, w1.x, a);
+  a = fmaf(x1.y, w1.y, a);
+  a = fmaf(x1.z, w1.z, a);
+  a = fmaf(x1.w, w1.w, a);
+  return a;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(512) confidence_kernel(
+    const T* __restrict__ h, const T* __restrict__ W1, const int32_t* __restrict__ anchor,
+    const int32_t* __restrict__ tokens, const float* __restrict__ w, float b,
+    const float* __restrict__ sts_T, int gamma, int d, int r, int V, float* __restrict__ conf,
+    float* __restrict__ surv) {
+  __shared__ float z[DSPARK_MAX_GAMMA];
+  const int req = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < gamma) {
+    const int k = warp + 1;
+    const int xp = clamp_token((k == 1) ? anchor[req] : tokens[size_t(req) * gamma + k - 2], V);
+    const T* hr = h + (size_t(req) * gamma + warp) * d;
+    const T* wr = W1 + size_t(xp) * r;
+    float acc = 0.f;
+    for (int e = lane * 8; e < d; e += 256) acc += dot_chunk8(hr + e, w + e);
+    for (int i = lane; i < r; i += 32) acc = fmaf(w[d + i], ld_f32(wr, i), acc);
+    acc = warp_sum(acc);
+    if (lane == 0) z[warp] = acc + b;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = 1.f;
+    for (int k = 0; k < gamma; ++k) {
+      const float c = 1.f / (1.f + expf(-z[k] / sts_T[k]));
+      a *= c;
+      conf[size_t(req) * gamma + k] = c;
+      surv[size_t(req) * gamma + k] = a;
+    }
+  }
+}
+
+cudaError_t launch_confidence(int dtype, const void* h, const void* W1, const int32_t* anchor,
+                              const int32_t* tokens, const float* w, float b, const float* sts_T,
+                              int bs, int gamma, int d, int r, int V, float* conf, float* surv,
+                              cudaStream_t s) {
+  const int threads = 32 * gamma;
+  if (dtype == DSPARK_F32)
+    confidence_kernel<float><<<bs, threads, 0, s>>>((const float*)h, (const float*)W1, anchor,
+                                                    tokens, w, b, sts_T, gamma, d, r, V, conf, surv);
+  else
+    confidence_kernel<__nv_bfloat16><<<bs, threads, 0, s>>>(
+        (const __nv_bfloat16*)h, (const __nv_bfloat16*)W1, anchor, tokens, w, b, sts_T, gamma, d,
+        r, V, conf, surv);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------
+// S3.  DSpark technical summary, "Verification scheduling", Hardware-Aware Prefix Scheduler
+// (Algorithm 1): admit slots globally by descending survival, Theta = tau * SPS(bs + K),
+// stop when Theta stops growing ("Infra": or take the global maximum).  vLLM adaptive
+// verification, "DSpark confidence scheduling mechanism": tau counts one extra token per
+// request plus the survival of the admitted slots.
+// One block of 1024 threads: bitonic sort of 64-bit keys (descending fp32 survival bits,
+// then slot index r * gamma + j), exact int64 fixed-point prefix sums of floor(a * 2^40),
+// Theta in fp64 with one rounding per product, block reductions for the stop / argmax.
+// ---------------------------------------------------------------------------------------
+constexpr int kSchedThreads = 1024;
+constexpr int kSchedMaxSlots = 4096;
+
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
+    const float* __restrict__ surv, int bs, int gamma, const double* __restrict__ sps, int m_max,
+    int mode, int32_t* __restrict__ window, int32_t* __restrict__ K_out,
+    double* __restrict__ theta_out) {
+  __shared__ unsigned long long key[kSchedMaxSlots];  // sort keys, then inclusive prefix sums
+  __shared__ unsigned short slot[kSchedMaxSlots];
+  __shared__ long long wsum[32];
+  __shared__ int red_k[32];
+  __shared__ double red_t[32];
+  __shared__ int win[DSPARK_MAX_BS];
+  __shared__ int s_kstar;
+  const int tid = threadIdx.x;
+  const int n = bs * gamma;
+  int N = 1;
+  while (N < n) N <<= 1;
+
+  for (int e = tid; e < N; e += kSchedThreads) {
+    unsigned long long kv = ~0ull;
+    if (e < n) {
+      uint32_t bits = __float_as_uint(surv[e]);
+      if (bits & 0x80000000u) bits = 0u;  // -0 and negatives rank as 0
+      kv = (static_cast<unsigned long long>(0xFFFFFFFFu - bits) << 32) | static_cast<unsigned>(e);
+    }
+    key[e] = kv;
+  }
+  for (int e = tid; e < DSPARK_MAX_BS; e += kSchedThreads) win[e] = 0;
+  __syncthreads();
+  for (int kk = 2; kk <= N; kk <<= 1) {
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      for (int e = tid; e < N; e += kSchedThreads) {
+        const int p = e ^ j;
+        if (p > e) {
+          const unsigned long long a = key[e], c = key[p];
+          const bool up = (e & kk) == 0;
+          if ((a > c) == up) {
+            key[e] = c;
+            key[p] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // fixed-point values in sorted order, 4 consecutive per thread, then an exclusive block scan
+  long long v[4];
+  long long run = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int i = tid * 4 + q;
+    long long x = 0;
+    if (i < n) {
+      const unsigned long long kv = key[i];
+      slot[i] = static_cast<unsigned short>(kv & 0xFFFFFFFFu);
+      const float a = __uint_as_float(0xFFFFFFFFu - static_cast<uint32_t>(kv >> 32));
+      x = static_cast<long long>(static_cast<double>(a) * 1099511627776.0);  // floor(a * 2^40), a >= 0
+    }
+    run += x;
+    v[q] = run;  // inclusive within the thread
+  }
+  const int lane = tid & 31, warp = tid >> 5;
+  long long incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    long long t = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xFFFFFFFFu, t, o);
+      if (lane >= o) t += y;
+    }
+    wsum[lane] = t;  // inclusive over warps
+  }
+  __syncthreads();
+  const long long base = (incl - run) + (warp > 0 ? wsum[warp - 1] : 0ll);
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int i = tid * 4 + q;
+    if (i < N) key[i] = static_cast<unsigned long long>(base + v[q]);  // S_{i+1}
+  }
+  __syncthreads();
+
+  const int kmax = min(n, m_max - bs);
+  auto theta = [&](int K) -> double {
+    const long long S = (K == 0) ? 0ll : static_cast<long long>(key[K - 1]);
+    const double tau = __dadd_rn(static_cast<double>(bs), __dmul_rn(static_cast<double>(S), 0x1p-40));
+    return __dmul_rn(tau, sps[bs + K]);
+  };
+  int cand = INT_MAX;
+  double best_t = -1.0;
+  int best_k = INT_MAX;
+  for (int K = tid; K <= kmax; K += kSchedThreads) {
+    const double t0 = theta(K);
+    if (mode == DSPARK_SCHED_EARLY_STOP) {
+      if (K < kmax && !(theta(K + 1) > t0)) cand = min(cand, K);
+    } else if (t0 > best_t || (t0 == best_t && K < best_k)) {
+      best_t = t0;
+      best_k = K;
+    }
+  }
+  // block reductions (min for early stop; argmax with lowest K for the global search)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    cand = min(cand, __shfl_xor_sync(0xFFFFFFFFu, cand, o));
+    const double ot = __shfl_xor_sync(0xFFFFFFFFu, best_t, o);
+    const int ok = __shfl_xor_sync(0xFFFFFFFFu, best_k, o);
+    if (ot > best_t || (ot == best_t && ok < best_k)) {
+      best_t = ot;
+      best_k = ok;
+    }
+  }
+  if (lane == 0) {
+    red_k[warp] = (mode == DSPARK_SCHED_EARLY_STOP) ? cand : best_k;
+    red_t[warp] = best_t;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int ks;
+    if (mode == DSPARK_SCHED_EARLY_STOP) {
+      ks = INT_MAX;
+      for (int i = 0; i < 32; ++i) ks = min(ks, red_k[i]);
+      if (ks == INT_MAX) ks = kmax;
+    } else {
+      double bt = red_t[0];
+      ks = red_k[0];
+      for (int i = 1; i < 32; ++i)
+        if (red_t[i] > bt || (red_t[i] == bt && red_k[i] < ks)) {
+          bt = red_t[i];
+          ks = red_k[i];
+        }
+    }
+    s_kstar = ks;
+    *K_out = ks;
+    *theta_out = theta(ks);
+  }
+  __syncthreads();
+  const int ks = s_kstar;
+  for (int i = tid; i < ks; i += kSchedThreads) atomicAdd(&win[slot[i] / gamma], 1);
+  __syncthreads();
+  for (int r = tid; r < bs; r += kSchedThreads) window[r] = win[r];
+}
+
+cudaError_t launch_schedule(const float* surv, int bs, int gamma, const double* sps, int m_max,
+                            int mode, int32_t* window, int32_t* K_out, double* theta_out,
+                            cudaStream_t s) {
+  schedule_kernel<<<1, kSchedThreads, 0, s>>>(surv, bs, gamma, sps, m_max, mode, window, K_out,
+                                               theta_out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------
+// S4.  DSpark in SGLang, "Ragged verify under full CUDA graphs" (Fig. 2): requests are
+// packed front to back into a cu_seqlens buffer and the total is rounded up to the nearest
+// captured tier.  One block; thread r owns request r.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(DSPARK_MAX_BS) pack_kernel(
+    const int32_t* __restrict__ window, const int32_t* __restrict__ anchor,
+    const int32_t* __restrict__ tokens, int bs, int gamma, const int32_t* __restrict__ tiers,
+    int n_tiers, int cap, int32_t* __restrict__ cu, int32_t* __restrict__ ids,
+    int32_t* __restrict__ req, int32_t* __restrict__ pos, int32_t* __restrict__ padded_out,
+    uint32_t* status) {
+  __shared__ int wsum[DSPARK_MAX_BS / 32];
+  __shared__ int s_padded, s_M, s_bad;
+  const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
+  if (r == 0) s_bad = 0;
+  __syncthreads();
+  int l = 0;
+  if (r < bs) {
+    l = window ? window[r] : gamma;
+    if (l < 0 || l > gamma) {
+      atomicExch(&s_bad, 1);
+      l = 0;
+    }
+  }
+  const int n = (r < bs) ? l + 1 : 0;
+  int incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int i = 0; i < warp; ++i) base += wsum[i];
+  const int start = base + incl - n;
+  if (r < bs) cu[r] = start;
+  if (r == bs - 1) {
+    cu[bs] = start + n;
+    s_M = start + n;
+  }
+  __syncthreads();
+  if (r == 0) {
+    const int M = s_M;
+    int padded = M;
+    if (n_tiers > 0) {
+      padded = -1;
+      for (int i = 0; i < n_tiers; ++i)
+        if (tiers[i] >= M) {
+          padded = tiers[i];
+          break;
+        }
+    }
+    if (s_bad || padded < 0 || padded > cap) {
+      set_status(status, DSPARK_EINVAL);
+      padded = -1;
+    }
+    s_padded = padded;
+    *padded_out = padded;
+  }
+  __syncthreads();
+  const int padded = s_padded;
+  if (padded < 0) return;
+  if (r < bs) {
+    for (int j = 0; j <= l; ++j) {
+      const int p = start + j;
+      ids[p] = (j == 0) ? anchor[r] : tokens[size_t(r) * gamma + j - 1];
+      req[p] = r;
+      pos[p] = j;
+    }
+  }
+  for (int p = s_M + r; p < padded; p += blockDim.x) {
+    ids[p] = -1;
+    req[p] = -1;
+    pos[p] = -1;
+  }
+}
+
+cudaError_t launch_pack(const int32_t* window, const int32_t* anchor, const int32_t* tokens,
+                        int bs, int gamma, const int32_t* tiers, int n_tiers, int cap,
+                        int32_t* cu, int32_t* ids, int32_t* req, int32_t* pos, int32_t* padded,
+                        uint32_t* status, cudaStream_t s) {
+  pack_kernel<<<1, DSPARK_MAX_BS, 0, s>>>(window, anchor, tokens, bs, gamma, tiers, n_tiers, cap,
+                                          cu, ids, req, pos, padded, status);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

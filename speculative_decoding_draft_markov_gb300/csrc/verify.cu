@@ -1,0 +1,365 @@
+// S5 -- rejection-sampling verification of the packed windows.
+//
+// DSpark technical summary, "Abstract" and "Architecture (drafter)": a draft token is
+// accepted with probability min(1, p_t / p_d) using exact per-token probabilities; the
+// first rejected position is redrawn from normalise(max(0, p_t - p_d)); if every tested
+// token passes, one bonus token comes from the target distribution of the next position.
+// DSpark in SGLang, "Verify modes": static / compact / cap-accept.
+//
+// Launch sequence (one stream):
+//   verify_rows     one block per packed row: row log-sum-exp (or argmax) and the tempered
+//                   target logit of the draft token it tests -- the HBM stream over target
+//   verify_decide   one thread per request: accept tests, first rejection, commit, ceiling
+//   decision_stats  (temperature > 0) per (request, 128-id chunk): residual mass and target
+//                   mass of the deciding row, p_d recomputed from U, W1, W2
+//   decision_select (temperature > 0) one block per request: two-level Gumbel-max draw
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dspark {
+
+// ---------------------------------------------------------------------------------------
+// Row statistics.  16-byte vector loads, per-thread online (max, sum-exp), fixed-order
+// block merge.
+// ---------------------------------------------------------------------------------------
+constexpr int kRowThreads = 512;
+
+template <typename T>
+__device__ __forceinline__ int load_group(const T* row, int e, float* x);
+template <>
+__device__ __forceinline__ int load_group<__nv_bfloat16>(const __nv_bfloat16* row, int e, float* x) {
+  const uint4 q = reinterpret_cast<const uint4*>(row)[e];
+  x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
+  x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
+  return 8;
+}
+template <>
+__device__ __forceinline__ int load_group<float>(const float* row, int e, float* x) {
+  const float4 q = reinterpret_cast<const float4*>(row)[e];
+  x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
+  return 4;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
+    const T* __restrict__ target, const int32_t* __restrict__ cu, const int32_t* __restrict__ tokens,
+    int bs, int gamma, int V, float inv_tau, int greedy, RowStat* __restrict__ rs, uint32_t* status) {
+  __shared__ float sv[kRowThreads / 32], ss[kRowThreads / 32];
+  __shared__ int si[kRowThreads / 32];
+  const int p = blockIdx.x, tid = threadIdx.x;
+  const int M = cu[bs];
+  if (p >= M) return;
+  int lo = 0, hi = bs;  // cu[lo] <= p < cu[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cu[mid] <= p) lo = mid; else hi = mid;
+  }
+  const int r = lo, j = p - cu[r], n_r = cu[r + 1] - cu[r];
+  const T* row = target + size_t(p) * V;
+  constexpr int G = sizeof(T) == 2 ? 8 : 4;
+  const int ng = V / G;
+  float x[8];
+  if (greedy) {
+    ArgMax best{-INFINITY, INT_MAX};
+    for (int e = tid; e < ng; e += kRowThreads) {
+      load_group<T>(row, e, x);
+#pragma unroll
+      for (int q = 0; q < G; ++q)
+        if (x[q] > best.v) best = ArgMax{x[q], e * G + q};
+    }
+    best = block_argmax<kRowThreads>(best, sv, si);
+    if (tid == 0) {
+      RowStat o{0.f, 0.f, best.i, 0};
+      if (j < n_r - 1 && j < gamma) {
+        const int xt = tokens[size_t(r) * gamma + j];
+        if (xt < 0 || xt >= V) set_status(status, DSPARK_EINVAL);
+        else o.tx = ld_f32(row, xt);
+      }
+      rs[p] = o;
+    }
+    return;
+  }
+  LsePair acc{-INFINITY, 0.f};
+  for (int e = tid; e < ng; e += kRowThreads) {
+    load_group<T>(row, e, x);
+    float gm = x[0] * inv_tau;
+#pragma unroll
+    for (int q = 1; q < G; ++q) gm = fmaxf(gm, x[q] * inv_tau);
+    if (gm > acc.m) {
+      acc.s = (acc.s == 0.f) ? 0.f : acc.s * expf(acc.m - gm);
+      acc.m = gm;
+    }
+#pragma unroll
+    for (int q = 0; q < G; ++q) acc.s += expf(x[q] * inv_tau - acc.m);
+  }
+  acc = block_lse<kRowThreads>(acc, sv, ss);
+  if (tid == 0) {
+    RowStat o{acc.m + logf(acc.s), -INFINITY, -1, 0};
+    if (j < n_r - 1 && j < gamma) {
+      const int xt = tokens[size_t(r) * gamma + j];
+      if (xt < 0 || xt >= V) set_status(status, DSPARK_EINVAL);
+      else o.tx = ld_f32(row, xt) * inv_tau;
+    }
+    rs[p] = o;
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Decide: accept tests in order, first rejection, committed prefix, ceiling.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) verify_decide_kernel(
+    const int32_t* __restrict__ cu, const int32_t* __restrict__ window, int mode, int bs, int gamma,
+    const int32_t* __restrict__ tokens, const float* __restrict__ logit_x,
+    const float* __restrict__ lse, const RowStat* __restrict__ rs, int greedy, uint64_t seed,
+    uint64_t step, int32_t* __restrict__ out_tokens, int32_t* __restrict__ acc_len,
+    int32_t* __restrict__ ceiling, Decision* __restrict__ dec, uint32_t* status) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= bs) return;
+  int32_t* out = out_tokens + size_t(r) * (gamma + 1);
+  const int l = (mode == DSPARK_STATIC) ? gamma : window[r];
+  const int n_r = cu[r + 1] - cu[r];
+  const int L_test = (mode == DSPARK_COMPACT) ? l : gamma;
+  const int L_commit = (mode == DSPARK_STATIC) ? gamma : l;
+  if (l < 0 || l > gamma || n_r != L_test + 1) {
+    set_status(status, DSPARK_EINVAL);
+    for (int i = 0; i <= gamma; ++i) out[i] = -1;
+    acc_len[r] = 0;
+    if (ceiling) ceiling[r] = 0;
+    dec[r] = Decision{0, 0, kDecNone, 0};
+    return;
+  }
+  int first = 0;
+  for (int k = 1; k <= L_test; ++k) {
+    const RowStat s = rs[cu[r] + k - 1];
+    const int x = tokens[size_t(r) * gamma + k - 1];
+    bool ok;
+    if (greedy) {
+      ok = (s.argmax == x);
+    } else {
+      const float lp_t = s.tx - s.lse;
+      const float lp_d = logit_x[size_t(r) * gamma + k - 1] - lse[size_t(r) * gamma + k - 1];
+      const float ratio = expf(lp_t - lp_d);
+      const float u = bits_to_uniform(philox_group(seed, step, kAccept, r, k, 0).x);
+      ok = u < ratio;
+    }
+    if (!ok) {
+      first = k;
+      break;
+    }
+  }
+  const int ceil_r = first ? first - 1 : L_test;
+  int acc, kdec, kind;
+  if (first && first <= L_commit) {
+    acc = first - 1;
+    kdec = first;
+    kind = kDecResidual;
+  } else {
+    acc = L_commit;
+    kdec = L_commit + 1;
+    kind = kDecBonus;
+  }
+  const int pdec = cu[r] + kdec - 1;
+  for (int i = 0; i <= gamma; ++i) out[i] = (i < acc) ? tokens[size_t(r) * gamma + i] : -1;
+  if (greedy) out[acc] = rs[pdec].argmax;
+  acc_len[r] = acc;
+  if (ceiling) ceiling[r] = ceil_r;
+  dec[r] = Decision{kdec, pdec, greedy ? kDecNone : kind, acc};
+}
+
+// ---------------------------------------------------------------------------------------
+// Decision chunk masses (temperature > 0).  Block = 128 ids of one chunk, RB requests.
+// Residual rows: w = max(0, p_t - p_d) with p_d recomputed (fp32 FMA, fixed order);
+// bonus rows: w = p_t.  Stores (sum w, sum p_t) per (request, chunk).
+// ---------------------------------------------------------------------------------------
+template <typename T, int RB>
+__global__ void __launch_bounds__(128) decision_stats_simt_kernel(
+    const T* __restrict__ target, const T* __restrict__ U, const T* __restrict__ W1,
+    const T* __restrict__ W2t, const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens,
+    const float* __restrict__ lse_d, const RowStat* __restrict__ rs, const Decision* __restrict__ dec,
+    int bs, int gamma, int V, int r, float inv_tau, float2* __restrict__ stats, int n_chunks) {
+  __shared__ float sA[RB][64];
+  __shared__ float sW[kChunk][65];
+  __shared__ float red[4];
+  const int c = blockIdx.x, rb = blockIdx.y * RB, tid = threadIdx.x;
+  const int v = c * kChunk + tid;
+  float acc[RB];
+#pragma unroll
+  for (int rr = 0; rr < RB; ++rr) acc[rr] = 0.f;
+  for (int i0 = 0; i0 < r; i0 += 64) {
+    const int sl = min(64, r - i0);
+    for (int e = tid; e < RB * sl; e += kChunk) {
+      const int rr = e / sl, ii = e % sl, row = rb + rr;
+      float val = 0.f;
+      if (row < bs) {
+        const Decision d = dec[row];
+        if (d.kind == kDecResidual) {
+          const int xp = clamp_token((d.kdec == 1) ? anchor[row] : tokens[size_t(row) * gamma + d.kdec - 2], V);
+          val = ld_f32(W1, size_t(xp) * r + i0 + ii);
+        }
+      }
+      sA[rr][ii] = val;
+    }
+    for (int e = tid; e < kChunk * sl; e += kChunk) {
+      const int vv = e / sl, ii = e % sl, vg = c * kChunk + vv;
+      sW[vv][ii] = (vg < V) ? ld_f32(W2t, size_t(vg) * r + i0 + ii) : 0.f;
+    }
+    __syncthreads();
+    for (int ii = 0; ii < sl; ++ii) {
+      const float w = sW[tid][ii];
+#pragma unroll
+      for (int rr = 0; rr < RB; ++rr) acc[rr] = fmaf(sA[rr][ii], w, acc[rr]);
+    }
+    __syncthreads();
+  }
+  const bool valid = v < V;
+#pragma unroll
+  for (int rr = 0; rr < RB; ++rr) {
+    const int row = rb + rr;
+    if (row >= bs) break;
+    const Decision d = dec[row];
+    if (d.kind == kDecNone) continue;  // uniform over the block
+    float pt = 0.f, w = 0.f;
+    if (valid) {
+      const float t = ld_f32(target, size_t(d.pdec) * V + v) * inv_tau;
+      pt = expf(t - rs[d.pdec].lse);
+      w = pt;
+      if (d.kind == kDecResidual) {
+        const float dl = (acc[rr] + ld_f32(U, (size_t(row) * gamma + d.kdec - 1) * V + v)) * inv_tau;
+        const float pd = expf(dl - lse_d[size_t(row) * gamma + d.kdec - 1]);
+        w = fmaxf(0.f, pt - pd);
+      }
+    }
+    const float R = block_sum<kChunk>(w, red);
+    const float P = block_sum<kChunk>(pt, red);
+    if (tid == 0) stats[size_t(row) * n_chunks + c] = make_float2(R, P);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Decision draw: one 256-thread block per request (temperature > 0).
+// ---------------------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) decision_select_kernel(
+    const T* __restrict__ target, const T* __restrict__ U, const T* __restrict__ W1,
+    const T* __restrict__ W2t, const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens,
+    const float* __restrict__ lse_d, const RowStat* __restrict__ rs, const Decision* __restrict__ dec,
+    const float2* __restrict__ stats, int n_chunks, int bs, int gamma, int V, int r, float inv_tau,
+    uint64_t seed, uint64_t step, int32_t* __restrict__ out_tokens) {
+  __shared__ float sA[256];
+  __shared__ float tw[kChunk], tp[kChunk];
+  __shared__ float rv[8];
+  __shared__ int ri[8];
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const Decision d = dec[b];
+  if (d.kind == kDecNone) return;
+  const float2* st = stats + size_t(b) * n_chunks;
+  float Rl = 0.f;
+  for (int c = tid; c < n_chunks; c += 256) Rl += st[c].x;
+  const bool use_res = block_sum<256>(Rl, rv) > 0.f;
+  ArgMax best{-INFINITY, INT_MAX};
+  const int n_grp = (n_chunks + 3) / 4;
+  for (int g = tid; g < n_grp; g += 256) {
+    const uint4 w = philox_group(seed, step, kDecideChunk, b, d.kdec, g);
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      const int c = 4 * g + l;
+      if (c >= n_chunks) break;
+      const float mass = use_res ? st[c].x : st[c].y;
+      if (mass > 0.f) best = better(best, ArgMax{logf(mass) + gumbel_from_bits(pick_word(w, l)), c});
+    }
+  }
+  best = block_argmax<256>(best, rv, ri);
+  const int cstar = (best.i == INT_MAX) ? 0 : best.i;  // only non-finite statistics leave it unset
+  const bool resid = (d.kind == kDecResidual) && use_res;
+  if (resid) {
+    const int xp = clamp_token((d.kdec == 1) ? anchor[b] : tokens[size_t(b) * gamma + d.kdec - 2], V);
+    for (int i = tid; i < r; i += 256) sA[i] = ld_f32(W1, size_t(xp) * r + i);
+  }
+  __syncthreads();
+  const float lse_t = rs[d.pdec].lse;
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int vv = warp; vv < kChunk; vv += 8) {
+    const int v = cstar * kChunk + vv;
+    float dot = 0.f;
+    if (resid && v < V)
+      for (int i = lane; i < r; i += 32) dot = fmaf(sA[i], ld_f32(W2t, size_t(v) * r + i), dot);
+    dot = warp_sum(dot);
+    if (lane == 0) {
+      float pt = 0.f, w = 0.f;
+      if (v < V) {
+        pt = expf(ld_f32(target, size_t(d.pdec) * V + v) * inv_tau - lse_t);
+        w = pt;
+        if (resid) {
+          const float dl = (dot + ld_f32(U, (size_t(b) * gamma + d.kdec - 1) * V + v)) * inv_tau;
+          w = fmaxf(0.f, pt - expf(dl - lse_d[size_t(b) * gamma + d.kdec - 1]));
+        }
+      }
+      tw[vv] = w;
+      tp[vv] = pt;
+    }
+  }
+  __syncthreads();
+  ArgMax ew{-INFINITY, INT_MAX}, ep{-INFINITY, INT_MAX};
+  if (tid < kChunk) {
+    const uint4 w = philox_group(seed, step, kDecideElem, b, d.kdec, tid >> 2);
+    const float g = gumbel_from_bits(pick_word(w, tid & 3));
+    if (tw[tid] > 0.f) ew = ArgMax{logf(tw[tid]) + g, tid};
+    if (tp[tid] > 0.f) ep = ArgMax{logf(tp[tid]) + g, tid};
+  }
+  ew = block_argmax<256>(ew, rv, ri);
+  ep = block_argmax<256>(ep, rv, ri);
+  if (tid == 0) {
+    // the recomputed chunk agrees with its mass except in degenerate rounding; fall back to p_t
+    const int e = (ew.i != INT_MAX) ? ew.i : ep.i;
+    out_tokens[size_t(b) * (gamma + 1) + d.acc] = (e != INT_MAX) ? cstar * kChunk + e : -1;
+  }
+}
+
+template <typename T>
+static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_t* window, int mode,
+                               int bs, int gamma, int V, const int32_t* anchor,
+                               const int32_t* tokens, const float* logit_x, const float* lse,
+                               const T* U, const T* W1, const T* W2t, int r, float inv_tau,
+                               int greedy, uint64_t seed, uint64_t step, int32_t* out_tokens,
+                               int32_t* acc_len, int32_t* ceiling, void* ws, cudaStream_t s) {
+  const WsLayout L = ws_layout(bs, gamma, V);
+  char* w = static_cast<char*>(ws);
+  uint32_t* status = reinterpret_cast<uint32_t*>(w + L.status);
+  float2* stats = reinterpret_cast<float2*>(w + L.stats);
+  RowStat* rs = reinterpret_cast<RowStat*>(w + L.rowstats);
+  Decision* dec = reinterpret_cast<Decision*>(w + L.dec);
+  verify_rows_kernel<T><<<bs * (gamma + 1), kRowThreads, 0, s>>>(target, cu, tokens, bs, gamma, V,
+                                                                  inv_tau, greedy, rs, status);
+  verify_decide_kernel<<<(bs + 127) / 128, 128, 0, s>>>(cu, window, mode, bs, gamma, tokens,
+                                                         logit_x, lse, rs, greedy, seed, step,
+                                                         out_tokens, acc_len, ceiling, dec, status);
+  if (!greedy) {
+    constexpr int RB = 32;
+    decision_stats_simt_kernel<T, RB><<<dim3(L.n_chunks, (bs + RB - 1) / RB), kChunk, 0, s>>>(
+        target, U, W1, W2t, anchor, tokens, lse, rs, dec, bs, gamma, V, r, inv_tau, stats, L.n_chunks);
+    decision_select_kernel<T><<<bs, 256, 0, s>>>(target, U, W1, W2t, anchor, tokens, lse, rs, dec,
+                                                 stats, L.n_chunks, bs, gamma, V, r, inv_tau, seed,
+                                                 step, out_tokens);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify(int dtype, const void* target, const int32_t* cu, const int32_t* window,
+                          int mode, int bs, int gamma, int V, const int32_t* anchor,
+                          const int32_t* tokens, const float* logit_x, const float* lse,
+                          const void* U, const void* W1, const void* W2t, int r, float inv_tau,
+                          int greedy, uint64_t seed, uint64_t step, int32_t* out_tokens,
+                          int32_t* acc_len, int32_t* ceiling, void* ws, cudaStream_t s) {
+  if (dtype == DSPARK_F32)
+    return verify_typed<float>((const float*)target, cu, window, mode, bs, gamma, V, anchor, tokens,
+                               logit_x, lse, (const float*)U, (const float*)W1, (const float*)W2t,
+                               r, inv_tau, greedy, seed, step, out_tokens, acc_len, ceiling, ws, s);
+  return verify_typed<__nv_bfloat16>((const __nv_bfloat16*)target, cu, window, mode, bs, gamma, V,
+                                     anchor, tokens, logit_x, lse, (const __nv_bfloat16*)U,
+                                     (const __nv_bfloat16*)W1, (const __nv_bfloat16*)W2t, r, inv_tau,
+                                     greedy, seed, step, out_tokens, acc_len, ceiling, ws, s);
+}
+
+}  // namespace dspark

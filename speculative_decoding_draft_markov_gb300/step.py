@@ -1,0 +1,130 @@
+"""One DSpark decoding step through the C ABI, on one CUDA stream, with no host readback.
+
+    draft_block -> confidence -> schedule -> pack -> target_forward(packed ids) -> verify
+
+`target_forward` is the caller's model: it receives the packed batch (ids / req / pos /
+cu_seqlens / padded total, all on the device) and fills the packed target-logit rows.
+Buffers are allocated once by PyTorch; the library itself allocates nothing."""
+from __future__ import annotations
+
+import dataclasses
+from typing import Callable, Optional
+
+import numpy as np
+
+from . import binding as B
+
+
+@dataclasses.dataclass
+class StepBuffers:
+    bs: int
+    gamma: int
+    V: int
+    cap: int
+    tokens: "object" = None
+    logit_x: "object" = None
+    lse: "object" = None
+    conf: "object" = None
+    surv: "object" = None
+    window: "object" = None
+    K: "object" = None
+    theta: "object" = None
+    cu: "object" = None
+    ids: "object" = None
+    req: "object" = None
+    pos: "object" = None
+    padded: "object" = None
+    packed: "object" = None
+    out_tokens: "object" = None
+    acc_len: "object" = None
+    ceiling: "object" = None
+    ws: "object" = None
+
+    @staticmethod
+    def allocate(bs: int, gamma: int, V: int, cap: int, dtype, device="cuda") -> "StepBuffers":
+        import torch
+        i32 = dict(dtype=torch.int32, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        b = StepBuffers(bs, gamma, V, cap)
+        b.tokens = torch.zeros((bs, gamma), **i32)
+        b.logit_x = torch.zeros((bs, gamma), **f32)
+        b.lse = torch.zeros((bs, gamma), **f32)
+        b.conf = torch.zeros((bs, gamma), **f32)
+        b.surv = torch.zeros((bs, gamma), **f32)
+        b.window = torch.zeros(bs, **i32)
+        b.K = torch.zeros(1, **i32)
+        b.theta = torch.zeros(1, dtype=torch.float64, device=device)
+        b.cu = torch.zeros(bs + 1, **i32)
+        b.ids = torch.full((cap,), -1, **i32)
+        b.req = torch.full((cap,), -1, **i32)
+        b.pos = torch.full((cap,), -1, **i32)
+        b.padded = torch.zeros(1, **i32)
+        b.packed = torch.zeros((cap, V), dtype=dtype, device=device)
+        b.out_tokens = torch.full((bs, gamma + 1), -1, **i32)
+        b.acc_len = torch.zeros(bs, **i32)
+        b.ceiling = torch.zeros(bs, **i32)
+        b.ws = B.alloc_workspace(bs, gamma, V, device)
+        return b
+
+
+def sps_table(T_raw, tiers, device="cuda"):
+    import torch
+    return torch.tensor(B.dspark_build_sps(T_raw, tiers), dtype=torch.float64, device=device)
+
+
+def gather_target_forward(target_full):
+    """A stand-in target model for tests and benchmarks: the packed row p gets the precomputed
+    row target_full[req[p], pos[p]] (pad rows get row 0 of request 0; verify never reads them)."""
+    import torch
+    bs, g1, V = target_full.shape
+    flat = target_full.view(bs * g1, V)
+
+    def fwd(buf: StepBuffers) -> None:
+        idx = torch.where(buf.req >= 0, buf.req * g1 + buf.pos, torch.zeros_like(buf.req)).long()
+        torch.index_select(flat, 0, idx, out=buf.packed)
+
+    return fwd
+
+
+def draft_and_schedule(inp: dict, buf: StepBuffers, sps, temperature: float, seed: int, step: int,
+                       sched_mode: int = B.DSPARK_SCHED_EARLY_STOP, mode: int = B.DSPARK_COMPACT,
+                       tiers=None, stream=None) -> None:
+    """Stages S1-S4 (everything before the target forward)."""
+    B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], temperature, seed, step,
+                         buf.tokens, buf.logit_x, buf.lse, buf.ws, stream)
+    B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], buf.tokens, inp["w"], inp["b"], inp["sts_T"],
+                        buf.conf, buf.surv, stream)
+    B.dspark_schedule(buf.surv, sps, sched_mode, buf.window, buf.K, buf.theta, stream)
+    B.dspark_pack(buf.window if mode == B.DSPARK_COMPACT else None, inp["anchor"], buf.tokens, tiers,
+                  buf.cu, buf.ids, buf.req, buf.pos, buf.padded, buf.ws, stream)
+
+
+def verify(inp: dict, buf: StepBuffers, temperature: float, seed: int, step: int,
+           mode: int = B.DSPARK_COMPACT, stream=None) -> None:
+    """Stage S5 on the packed target rows in buf.packed."""
+    B.dspark_verify(buf.packed, buf.cu, buf.window, mode, inp["anchor"], buf.tokens, buf.logit_x, buf.lse,
+                    inp["U"], inp["W1"], inp["W2t"], temperature, seed, step, buf.out_tokens, buf.acc_len,
+                    buf.ceiling, buf.ws, stream)
+
+
+def run_step(inp: dict, buf: StepBuffers, sps, target_forward: Callable[[StepBuffers], None],
+             temperature: float, seed: int, step: int, mode: int = B.DSPARK_COMPACT,
+             sched_mode: int = B.DSPARK_SCHED_EARLY_STOP, tiers=None, stream=None) -> None:
+    draft_and_schedule(inp, buf, sps, temperature, seed, step, sched_mode, mode, tiers, stream)
+    target_forward(buf)
+    verify(inp, buf, temperature, seed, step, mode, stream)
+
+
+def device_inputs_from_host(host: dict, device="cuda") -> dict:
+    """Copy numpy inputs (bf16 as uint16 bit patterns) to device tensors of the right dtype."""
+    import torch
+    out = {}
+    for k, v in host.items():
+        if isinstance(v, np.ndarray) and k not in ("T_raw",):
+            t = torch.from_numpy(np.ascontiguousarray(v))
+            if v.dtype == np.uint16:
+                t = t.view(torch.int16).view(torch.bfloat16)
+            out[k] = t.to(device)
+        else:
+            out[k] = v
+    return out

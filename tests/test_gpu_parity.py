@@ -1,0 +1,213 @@
+"""GPU parity: every stage through the C ABI against the oracle on the same seeded inputs.
+
+Small cases span several 128-id chunks with a ragged tail; the full-size case uses the
+bs=256, gamma=7, V=151936 workload and checks sampled requests one by one."""
+import numpy as np
+import pytest
+
+from oracle import dspark_oracle as O
+from speculative_decoding_draft_markov_gb300 import inputs as I
+from tests.parity import NEAR, TOL, compare_draft, compare_verify, to_np
+
+from speculative_decoding_draft_markov_gb300 import binding as B
+from speculative_decoding_draft_markov_gb300 import step as S
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _dev(host):
+    return S.device_inputs_from_host(host)
+
+
+def _draft_gpu(inp, temperature, seed, step):
+    U = inp["U"]
+    bs, gamma, V = U.shape
+    tok = torch.zeros((bs, gamma), dtype=torch.int32, device="cuda")
+    lx = torch.zeros((bs, gamma), dtype=torch.float32, device="cuda")
+    lse = torch.zeros_like(lx)
+    ws = B.alloc_workspace(bs, gamma, V)
+    B.dspark_draft_block(U, inp["W1"], inp["W2t"], inp["anchor"], temperature, seed, step, tok, lx, lse, ws)
+    assert B.dspark_read_device_status(ws) == B.DSPARK_OK
+    return tok.cpu().numpy(), lx.cpu().numpy(), lse.cpu().numpy()
+
+
+SMALL = {
+    "tiny_fp32": I.WORKLOADS["tiny_fp32"],
+    "bf16_ragged": I.WORKLOADS["qwen3_4b"].with_(name="bf16_ragged", bs=5, gamma=3, V=2000, d=64, seed=11),
+    "bf16_r64": I.WORKLOADS["qwen3_4b"].with_(name="bf16_r64", bs=9, gamma=4, V=1032, r=64, d=64, seed=12),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("temperature", [1.0, 0.7, 0.0])
+def test_draft_parity_small(name, temperature):
+    wl = SMALL[name]
+    host = I.make_host_inputs(wl, with_target=False, with_hidden=False)
+    inp = _dev(host)
+    for step in (0, 5):
+        tg, lg, sg = _draft_gpu(inp, temperature, wl.seed, step)
+        to, lo, so, mo = O.draft_block(host["U"], host["W1"], host["W2t"], host["anchor"], temperature,
+                                       wl.seed, step, dtype=wl.dtype)
+        checked, near = compare_draft(tg, lg, sg, to, lo, so, mo, wl.dtype, greedy=temperature == 0.0)
+        assert checked >= wl.bs * wl.gamma - near * wl.gamma and near <= 1
+
+
+def test_draft_parity_full_size_sampled_rows():
+    wl = I.WORKLOADS["mixed_bs256"]
+    inp = I.make_device_inputs(wl, "cuda", with_target=False, with_hidden=False)
+    rows = np.array([0, 84, 85, 200, 255])
+    for temperature in (1.0, 0.0):
+        tg, lg, sg = _draft_gpu(inp, temperature, wl.seed, 3)
+        U = to_np(inp["U"][torch.as_tensor(rows, device="cuda")])
+        to, lo, so, mo = O.draft_block(U, to_np(inp["W1"]), to_np(inp["W2t"]), to_np(inp["anchor"])[rows],
+                                       temperature, wl.seed, 3, dtype="bf16", req_ids=rows)
+        compare_draft(tg[rows], lg[rows], sg[rows], to, lo, so, mo, "bf16", greedy=temperature == 0.0)
+
+
+@pytest.mark.parametrize("name,d", [("tiny_fp32", 64), ("bf16_ragged", 4096)])
+def test_confidence_parity(name, d):
+    wl = SMALL[name].with_(d=d, bs=24)
+    host = I.make_host_inputs(wl, with_target=False)
+    tokens = I.random_tokens(wl.bs, wl.gamma, wl.V, 5)
+    inp = _dev(host)
+    conf = torch.zeros((wl.bs, wl.gamma), dtype=torch.float32, device="cuda")
+    surv = torch.zeros_like(conf)
+    B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], torch.as_tensor(tokens, device="cuda"),
+                        inp["w"], 0.25, inp["sts_T"], conf, surv)
+    c_o, a_o, _ = O.confidence(host["h"], host["W1"], host["anchor"], tokens, host["w"], 0.25,
+                               host["sts_T"], dtype=wl.dtype)
+    tol = TOL[wl.dtype]
+    np.testing.assert_allclose(conf.cpu().numpy(), c_o, rtol=tol, atol=0)
+    np.testing.assert_allclose(surv.cpu().numpy(), a_o, rtol=tol * wl.gamma, atol=0)
+
+
+def _sched_cases():
+    cases = []
+    for (bs, gamma, seed, ties, kind) in [(4, 7, 0, False, "tiny"), (256, 7, 1, False, "mixed"),
+                                          (256, 7, 2, True, "mixed"), (256, 16, 3, False, "wide"),
+                                          (1, 1, 4, False, "one"), (33, 5, 5, True, "steep"),
+                                          (128, 15, 6, False, "long"), (64, 7, 7, False, "short")]:
+        a = I.random_survival(bs, gamma, seed, ties=ties)
+        if kind == "tiny":
+            sps = O.build_sps(1.0 + 0.002 * np.arange(65), [])
+        elif kind == "steep":
+            sps = O.build_sps(1.0 + 0.5 * np.arange(bs * (gamma + 1) + 1), [])
+        elif kind == "short":   # table shorter than bs + bs*gamma: K is capped by m_max
+            sps = O.build_sps(5.0 + 0.01 * np.arange(200), list(range(16, 200, 16)) + [199])
+        else:
+            m = bs * (gamma + 1)
+            step = 64 if kind == "mixed" else 16
+            sps = O.build_sps(5.0 + 0.01 * np.arange(m + 1), list(range(step, m, step)) + [m])
+        cases.append((a, sps))
+    return cases
+
+
+@pytest.mark.parametrize("mode", [O.EARLY_STOP, O.GLOBAL_ARGMAX])
+def test_schedule_bit_exact(mode):
+    for a, sps in _sched_cases():
+        bs, gamma = a.shape
+        win = torch.zeros(bs, dtype=torch.int32, device="cuda")
+        K = torch.zeros(1, dtype=torch.int32, device="cuda")
+        th = torch.zeros(1, dtype=torch.float64, device="cuda")
+        B.dspark_schedule(torch.as_tensor(a, device="cuda"), torch.as_tensor(sps, device="cuda"), mode, win, K, th)
+        w_o, K_o, th_o, _ = O.schedule(a, sps, mode)
+        np.testing.assert_array_equal(win.cpu().numpy(), w_o)
+        assert int(K.item()) == K_o
+        assert th.item() == th_o  # bit-exact fp64
+
+
+@pytest.mark.parametrize("static", [False, True])
+def test_pack_bit_exact(static):
+    for bs, gamma, tier_step, seed in [(4, 7, 0, 0), (256, 7, 64, 1), (20, 7, 16, 2), (128, 15, 128, 3), (1, 5, 16, 4)]:
+        win = None if static else I.random_windows(bs, gamma, seed)
+        tokens = I.random_tokens(bs, gamma, 1000, seed)
+        anchor = I.random_tokens(bs, 1, 1000, seed + 50)[:, 0].copy()
+        cap = bs * (gamma + 1) + 64
+        tiers = (list(range(tier_step, bs * (gamma + 1), tier_step)) + [bs * (gamma + 1)]) if tier_step else []
+        cu_o, ids_o, req_o, pos_o, pad_o = O.pack(win, anchor, tokens, tiers, cap, gamma=gamma)
+        t = lambda x: torch.as_tensor(np.asarray(x, dtype=np.int32), device="cuda")
+        cu, ids, req, pos = (torch.full((n,), -7, dtype=torch.int32, device="cuda") for n in (bs + 1, cap, cap, cap))
+        padded = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ws = B.alloc_workspace(bs, gamma, 1000)
+        B.dspark_pack(None if static else t(win), t(anchor), t(tokens), t(tiers) if tiers else None,
+                      cu, ids, req, pos, padded, ws)
+        assert B.dspark_read_device_status(ws) == B.DSPARK_OK
+        assert int(padded.item()) == pad_o
+        np.testing.assert_array_equal(cu.cpu().numpy(), cu_o)
+        for g, o in ((ids, ids_o), (req, req_o), (pos, pos_o)):
+            np.testing.assert_array_equal(g.cpu().numpy()[:pad_o], o[:pad_o])
+
+
+def test_pack_device_errors_and_recovery():
+    bs, gamma = 6, 4
+    t = lambda x: torch.as_tensor(np.asarray(x, dtype=np.int32), device="cuda")
+    anchor, tokens = t(np.arange(bs)), t(np.zeros((bs, gamma)))
+    cu, ids, req, pos = (torch.zeros(n, dtype=torch.int32, device="cuda") for n in (bs + 1, 64, 64, 64))
+    padded = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = B.alloc_workspace(bs, gamma, 64)
+    B.dspark_pack(t([1, 2, 9, 0, 0, 0]), anchor, tokens, None, cu, ids, req, pos, padded, ws)   # window > gamma
+    assert B.dspark_read_device_status(ws) == B.DSPARK_EINVAL and padded.item() == -1
+    B.dspark_pack(t([4] * bs), anchor, tokens, t([8, 16]), cu, ids, req, pos, padded, ws)      # M = 30 > 16
+    assert B.dspark_read_device_status(ws) == B.DSPARK_EINVAL
+    B.dspark_pack(t([1] * bs), anchor, tokens, t([8, 16]), cu, ids, req, pos, padded, ws)      # fine again
+    assert B.dspark_read_device_status(ws) == B.DSPARK_OK and padded.item() == 16
+
+
+def _verify_chain(wl, temperature, mode, windows_seed, step=0):
+    """GPU: draft -> pack(generator windows) -> gather target -> verify; oracle: the same chain."""
+    host = I.make_host_inputs(wl, with_hidden=False)
+    inp = _dev(host)
+    bs, gamma, V = wl.bs, wl.gamma, wl.V
+    tg, lg, sg = _draft_gpu(inp, temperature, wl.seed, step)
+    to, lo, so, mo = O.draft_block(host["U"], host["W1"], host["W2t"], host["anchor"], temperature, wl.seed,
+                                   step, dtype=wl.dtype)
+    win = I.random_windows(bs, gamma, windows_seed)
+    pack_win = win if mode == O.COMPACT else None
+    cap = bs * (gamma + 1)
+    # oracle chain
+    cu_o, ids_o, req_o, pos_o, pad_o = O.pack(pack_win, host["anchor"], to, [], cap)
+    packed_o = I.gather_packed_target(host["target"], req_o, pos_o, cap)
+    out_o, acc_o, ceil_o, mv_o = O.verify(packed_o, cu_o, win, mode, host["anchor"], to, lo, so, host["U"],
+                                          host["W1"], host["W2t"], temperature, wl.seed, step, dtype=wl.dtype)
+    # GPU chain
+    buf = S.StepBuffers.allocate(bs, gamma, V, cap, inp["U"].dtype)
+    buf.tokens.copy_(torch.as_tensor(tg, device="cuda"))
+    buf.logit_x.copy_(torch.as_tensor(lg, device="cuda"))
+    buf.lse.copy_(torch.as_tensor(sg, device="cuda"))
+    buf.window.copy_(torch.as_tensor(win, device="cuda"))
+    B.dspark_pack(buf.window if mode == O.COMPACT else None, inp["anchor"], buf.tokens, None, buf.cu, buf.ids,
+                  buf.req, buf.pos, buf.padded, buf.ws)
+    S.gather_target_forward(inp["target"])(buf)
+    S.verify(inp, buf, temperature, wl.seed, step, mode)
+    assert B.dspark_read_device_status(buf.ws) == B.DSPARK_OK
+    # requests whose draft diverged at a near-margin decision are excluded from the verify check
+    div = np.array([not np.array_equal(tg[r], to[r]) for r in range(bs)])
+    for r in np.nonzero(div)[0]:
+        assert mo[r].min() < NEAR
+    keep = ~div
+    ceil_g = buf.ceiling.cpu().numpy() if mode == O.CAP_ACCEPT else None
+    checked, near = compare_verify(buf.out_tokens.cpu().numpy()[keep], buf.acc_len.cpu().numpy()[keep],
+                                   out_o[keep], acc_o[keep], mv_o[keep],
+                                   ceil_g[keep] if ceil_g is not None else None,
+                                   ceil_o[keep] if ceil_g is not None else None)
+    return checked, near, acc_o
+
+
+VERIFY_WL = {
+    "tiny_fp32": I.WORKLOADS["tiny_fp32"].with_(bs=12),
+    "bf16_ragged": SMALL["bf16_ragged"].with_(bs=16, gamma=5, sigmas=(0.3, 1.0, 3.0)),
+}
+
+
+@pytest.mark.parametrize("name", list(VERIFY_WL))
+@pytest.mark.parametrize("mode", [O.STATIC, O.COMPACT, O.CAP_ACCEPT])
+@pytest.mark.parametrize("temperature", [1.0, 0.0])
+def test_verify_chain_parity(name, mode, temperature):
+    wl = VERIFY_WL[name]
+    total_checked = 0
+    for step, ws in ((0, 1), (1, 2), (2, 3)):
+        checked, near, acc_o = _verify_chain(wl, temperature, mode, ws, step)
+        assert near <= 1
+        total_checked += checked
+    assert total_checked >= 3 * wl.bs - 3
