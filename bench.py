@@ -1,0 +1,343 @@
+"""Benchmark: DSpark step tokens/s at bs=256, V=151936, gamma=7 (the mixed-difficulty batch).
+
+One step = draft_block -> confidence -> schedule -> pack -> [target forward] -> verify, all
+through the C ABI on one stream.  The target forward is the caller's model and is not part
+of this path: it is a row gather here and it sits outside the timed segments; everything
+else is timed with CUDA events on the launching stream.  The L2 is flushed (256 MB write)
+between timed steps.  tokens/step = sum over requests of (accepted + 1).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--gpus N > 1 runs under torchrun: one independent replica per GPU (the path has no
+cross-request exchange that needs a collective), barrier + max-over-ranks timing; value is
+the tokens of all ranks / that time ("scaling": "weak").
+--impl reference times the CPU oracle (plain numpy, fp64) on bounded samples of the same
+workload."""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "mixed_bs256"
+METRIC = "DSpark step tokens/s at bs=256,V=151936,γ=7; % of HBM/tensor roofline"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------- CPU oracle
+_SAMPLE_CACHE = {}
+
+
+def _oracle_sample(n_req: int, step: int, wl_name: str = WORKLOAD):
+    """Run the oracle's full step on the first n_req requests of the workload (host inputs).
+    Returns (tokens, seconds).  Inputs are generated (once per sample size) before the clock starts."""
+    from oracle import dspark_oracle as O
+    from speculative_decoding_draft_markov_gb300 import inputs as I
+    wl = I.WORKLOADS[wl_name].with_(bs=n_req)
+    if n_req not in _SAMPLE_CACHE:
+        h = I.make_host_inputs(wl)
+        _SAMPLE_CACHE[n_req] = (h, O.build_sps(h["T_raw"], h["tiers"]))
+    host, sps = _SAMPLE_CACHE[n_req]
+    t0 = time.perf_counter()
+    tok, lx, lse, _ = O.draft_block(host["U"], host["W1"], host["W2t"], host["anchor"], wl.temperature, wl.seed, step)
+    _, surv, _ = O.confidence(host["h"], host["W1"], host["anchor"], tok, host["w"], host["b"], host["sts_T"])
+    win, K, _, _ = O.schedule(surv.astype(np.float32), sps, O.EARLY_STOP)
+    cap = wl.bs * (wl.gamma + 1)
+    cu, ids, req, pos, padded = O.pack(win, host["anchor"], tok, host["tiers"], max(cap, int(host["tiers"][-1])))
+    packed = I.gather_packed_target(host["target"], req, pos, int(cu[-1]))
+    _, acc, _, _ = O.verify(packed, cu, win, O.COMPACT, host["anchor"], tok, lx, lse, host["U"], host["W1"],
+                            host["W2t"], wl.temperature, wl.seed, step)
+    dt = time.perf_counter() - t0
+    return O.step_tokens(acc), dt
+
+
+def cpu_baseline(n_req: int = 32, reps: int = 3):
+    """Time the oracle in a child process limited to one BLAS/OpenMP thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import sys, json; sys.path.insert(0, %r); import bench; "
+            "r = [bench._oracle_sample(%d, s) for s in range(%d)]; print(json.dumps(r))" % (ROOT, n_req, reps))
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
+    if out.returncode != 0:
+        return {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle", "error": out.stderr[-300:]}
+    res = json.loads(out.stdout.strip().splitlines()[-1])
+    tok = sum(r[0] for r in res)
+    sec = sum(r[1] for r in res)
+    return {"value": tok / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_req} of the 256 requests, full V=151936, gamma=7, all five stages, {reps} step(s); "
+                      f"{tok} tokens in {sec:.1f} s"}
+
+
+# ------------------------------------------------------------------------------- GPU arm
+def run_ours(args, rank: int, world: int):
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_draft_markov_gb300 import binding as B
+    from speculative_decoding_draft_markov_gb300 import inputs as I
+    from speculative_decoding_draft_markov_gb300 import step as S
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl = I.WORKLOADS[WORKLOAD].with_(seed=I.WORKLOADS[WORKLOAD].seed + 1000 * rank)
+    bs, gamma, V, r = wl.bs, wl.gamma, wl.V, wl.r
+    inp = I.make_device_inputs(wl, dev)
+    cap = int(I.tiers_for(wl)[-1])
+    buf = S.StepBuffers.allocate(bs, gamma, V, cap, inp["U"].dtype, dev)
+    sps = S.sps_table(inp["T_raw"], inp["tiers"], dev)
+    tiers_dev = torch.as_tensor(inp["tiers"], device=dev)
+    fwd = S.gather_target_forward(inp["target"])
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    tokens_acc = torch.zeros(1, dtype=torch.int64, device=dev)
+    tau = wl.temperature
+
+    def step(it, timed, evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], tau, wl.seed, it, buf.tokens,
+                             buf.logit_x, buf.lse, buf.ws)
+        if evs is not None:
+            evs[1].record(stream)
+        B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], buf.tokens, inp["w"], inp["b"], inp["sts_T"],
+                            buf.conf, buf.surv)
+        B.dspark_schedule(buf.surv, sps, B.DSPARK_SCHED_EARLY_STOP, buf.window, buf.K, buf.theta)
+        B.dspark_pack(buf.window, inp["anchor"], buf.tokens, tiers_dev, buf.cu, buf.ids, buf.req, buf.pos,
+                      buf.padded, buf.ws)
+        if evs is not None:
+            evs[2].record(stream)
+        fwd(buf)  # the caller's target forward: outside the timed segments
+        if evs is not None:
+            evs[3].record(stream)
+        S.verify(inp, buf, tau, wl.seed, it, B.DSPARK_COMPACT)
+        if evs is not None:
+            evs[4].record(stream)
+        if timed:
+            tokens_acc.add_((buf.acc_len.to(torch.int64) + 1).sum())
+
+    for w in range(args.warmup):
+        step(10_000 + w, False)
+    st = B.dspark_read_device_status(buf.ws)
+    if st != 0:
+        raise RuntimeError("device status after warm-up: " + B.dspark_status_string(st))
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        for it in range(args.steps):
+            flush.fill_(it & 0xFF)  # L2 flush, outside the timed segments
+            step(it, True, evs[it])
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    seg = np.array([[e[0].elapsed_time(e[2]), e[3].elapsed_time(e[4]), e[0].elapsed_time(e[1])] for e in evs])
+    step_ms = seg[:, 0] + seg[:, 1]
+    total_ms = float(step_ms.sum())
+    tokens = int(tokens_acc.item())
+    st = B.dspark_read_device_status(buf.ws)
+    if st != 0:
+        raise RuntimeError("device status after the timed steps: " + B.dspark_status_string(st))
+
+    # ---- end to end through the public API with host buffers (pinned), copies inside the timing
+    host_U = inp["U"].cpu().pin_memory()
+    host_h = inp["h"].cpu().pin_memory()
+    host_a = inp["anchor"].cpu().pin_memory()
+    host_t = inp["target"].cpu().pin_memory()
+    out_host = torch.empty((bs, gamma + 1), dtype=torch.int32).pin_memory()
+    acc_host = torch.empty(bs, dtype=torch.int32).pin_memory()
+    e2e_steps = max(2, min(args.steps, 5))
+    bi = sum(t.numel() * t.element_size() for t in (host_U, host_h, host_a, host_t))
+    bo = out_host.numel() * 4 + acc_host.numel() * 4
+    e2e_tokens = 0
+    torch.cuda.synchronize(dev)
+    t_e2e = []
+    for it in range(e2e_steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        inp["U"].copy_(host_U, non_blocking=True)
+        inp["h"].copy_(host_h, non_blocking=True)
+        inp["anchor"].copy_(host_a, non_blocking=True)
+        inp["target"].copy_(host_t, non_blocking=True)
+        S.run_step(inp, buf, sps, fwd, tau, wl.seed, 20_000 + it, B.DSPARK_COMPACT, tiers=tiers_dev)
+        out_host.copy_(buf.out_tokens, non_blocking=True)
+        acc_host.copy_(buf.acc_len, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        t_e2e.append(e0.elapsed_time(e1))
+        e2e_tokens += int((acc_host.to(torch.int64) + 1).sum())
+    e2e_ms = float(np.sum(t_e2e))
+
+    # aggregate over ranks: max time, summed tokens
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+        n = torch.tensor([tokens, e2e_tokens], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(n, op=dist.ReduceOp.SUM)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+        tokens, e2e_tokens = int(n[0]), int(n[1])
+
+    hbm, bf16, peak_kind = _peaks()
+    n_chunks = (V + 127) // 128
+    draft_bytes = bs * gamma * V * 2 + V * r * 2 + bs * gamma * r * 2 + 2 * gamma * bs * n_chunks * 8
+    draft_ms = float(seg[:, 2].mean())
+    achieved = draft_bytes / (draft_ms * 1e-3) / 1e9
+    launches_per_step = 2 * gamma + 3 + (4 if tau > 0 else 2)
+    return {
+        "metric": METRIC,
+        "value": tokens / (total_ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; U~N(0,3^2), W~N(0,0.05^2), target = base logits + N(0,sigma^2), "
+                "sigma 0.5/1/2 by thirds)",
+        "config": {"workload": "mixed_bs256: bs=256, gamma=7, V=151936, r=256, d=4096, compact verify, "
+                               "temperature 1, sawtooth cost table with tiers every 64 to 2048",
+                   "global_batch": bs * world, "l2": "flushed between steps (256 MB write)",
+                   "timed": "draft+confidence+schedule+pack and verify segments; target forward excluded",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_step": tokens / args.steps / world,
+        "stage_ms": {"draft": draft_ms, "conf_sched_pack": float((seg[:, 0] - seg[:, 2]).mean()),
+                     "verify": float(seg[:, 1].mean())},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None,
+                     "kernel": "dspark_draft_block (all gamma positions: chunk-statistics + select launches)",
+                     "algorithmic_bytes": draft_bytes, "peak_kind": peak_kind},
+        "e2e": {"value": e2e_tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is a bounded sample of the workload."""
+    n_req = 4
+    toks, secs = 0, 0.0
+    for s in range(args.warmup + args.steps):
+        t, dt = _oracle_sample(n_req, s)
+        if s >= args.warmup:
+            toks += t
+            secs += dt
+    v = toks / secs
+    return {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "mixed_bs256 sample: first 4 of the 256 requests, full V=151936, gamma=7"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{n_req} requests per step, {args.steps} timed steps"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    from speculative_decoding_draft_markov_gb300 import build
+    build.build()
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
