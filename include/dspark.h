@@ -89,6 +89,13 @@ DSPARK_API int dspark_workspace_init(void* ws, size_t ws_bytes, dspark_stream_t 
  * read (DSPARK_OK if none) and clear it.  The only call that waits for the device. */
 DSPARK_API int dspark_read_device_status(void* ws, dspark_stream_t stream);
 
+/* Diagnostics: deadline, in nanoseconds from a kernel's start, of every device-side wait in
+ * the tensor-core kernels (default 1 s).  A wait that runs out records DSPARK_ETIMEOUT in the
+ * workspace status word; the kernel then waits (bounded) for its own copies in flight, frees
+ * its tensor memory and returns, leaving the context usable.  Process-wide; returns the
+ * previous value.  Tests use a tiny value to exercise that path. */
+DSPARK_API uint64_t dspark_set_wait_timeout_ns(uint64_t ns);
+
 /* Host: steps-per-second table from a profiled step-time curve ([VLLM] "Cost Modeling",
  * "CUDA Graph Padding"; [SGLANG] "Ragged verify"; [SUMMARY] "Verification scheduling").
  *   T_raw[M]   host, m_max+1 doubles: profiled step time (any unit) for M verify tokens.

@@ -28,6 +28,7 @@ _SIGS = {
     "dspark_workspace_init": (_i, [_vp, _sz, _vp]),
     "dspark_read_device_status": (_i, [_vp, _vp]),
     "dspark_build_sps": (_i, [_vp, _i, _vp, _i, _vp]),
+    "dspark_set_wait_timeout_ns": (_u64, [_u64]),
     "dspark_draft_block": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _u64, _u64,
                                 _vp, _vp, _vp, _vp, _sz, _vp]),
     "dspark_confidence": (_i, [_vp, _vp, _i, _vp, _vp, _vp, _f, _vp, _i, _i, _i, _i, _i,
@@ -112,6 +113,11 @@ def dspark_workspace_init(ws, stream=None) -> None:
 
 def dspark_read_device_status(ws, stream=None) -> int:
     return int(lib().dspark_read_device_status(_p(ws), _stream(stream)))
+
+
+def dspark_set_wait_timeout_ns(ns: int) -> int:
+    """Deadline of device-side waits in the tensor-core kernels; returns the previous value."""
+    return int(lib().dspark_set_wait_timeout_ns(int(ns)))
 
 
 def alloc_workspace(bs: int, gamma: int, V: int, device="cuda"):

@@ -69,6 +69,12 @@ int dspark_read_device_status(void* ws, dspark_stream_t stream) {
   return static_cast<int>(word);
 }
 
+uint64_t dspark_set_wait_timeout_ns(uint64_t ns) {
+  const uint64_t old = g_wait_timeout_ns;
+  g_wait_timeout_ns = ns;
+  return old;
+}
+
 int dspark_build_sps(const double* T_raw, int m_max, const int32_t* tiers, int n_tiers,
                      double* sps_out) {
   if (!T_raw || !sps_out || m_max < 0 || n_tiers < 0 || (n_tiers > 0 && !tiers)) return DSPARK_EINVAL;

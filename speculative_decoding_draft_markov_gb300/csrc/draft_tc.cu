@@ -5,6 +5,8 @@
 
 namespace dspark {
 
+uint64_t g_wait_timeout_ns = 1000000000ull;  // 1 s; changed only through dspark_set_wait_timeout_ns
+
 bool draft_tc_supported(int, int, int, int) { return false; }
 
 cudaError_t launch_draft_stats_tc(const void*, const void*, const void*, const int32_t*,
