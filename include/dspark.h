@@ -206,6 +206,28 @@ DSPARK_API int dspark_verify(const void* target, int dtype, const int32_t* cu_se
                   int32_t* out_tokens, int32_t* acc_len, int32_t* ceiling,
                   void* ws, size_t ws_bytes, dspark_stream_t stream);
 
+/* Allocation-free variant of dspark_draft_block.  The pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory and so have no workspace to
+ * pass -- for example a plugin running inside another framework's device-memory pool (a
+ * cudaMalloc would bypass that framework's allocator and its accounting), or a service that
+ * fixes its device footprint at start-up and forbids later allocation.  Same computation,
+ * arguments and limits as dspark_draft_block, without ws / ws_bytes; it allocates nothing.
+ *   Scratch: a fixed 4 MiB array inside the library (every GPU that loads the library holds it
+ *   until exit).  Sizes whose scratch (256 B + bs * ceil(V / 128) * 8 B) exceeds it are rejected
+ *   with DSPARK_EUNSUPPORTED -- e.g. bs = 256 allows V up to about 262,000.
+ *   The first call on a device looks up the array's device address (once per device, with that
+ *   device current); make that first call before any stream capture.
+ *   All calls share the array and it keeps the last call's contents: calls whose work can
+ *   overlap on the GPU (other streams, other host threads) race and must be serialised.
+ *   device_status: device uint32 or NULL.  If given, device-side errors (a wait timeout) are
+ *   recorded there (first error wins; the caller zeroes it); if NULL, they go to a status word
+ *   in the array that each call clears and that the caller cannot read. */
+DSPARK_API int dspark_draft_block_noalloc(const void* U, const void* W1, const void* W2t, int dtype,
+                                          const int32_t* anchor, int bs, int gamma, int V, int r,
+                                          float temperature, uint64_t seed, uint64_t step,
+                                          int32_t* tokens, float* logit_x, float* lse,
+                                          uint32_t* device_status, dspark_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

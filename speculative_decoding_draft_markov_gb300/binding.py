@@ -31,6 +31,8 @@ _SIGS = {
     "dspark_set_wait_timeout_ns": (_u64, [_u64]),
     "dspark_draft_block": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _u64, _u64,
                                 _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dspark_draft_block_noalloc": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _u64, _u64,
+                                        _vp, _vp, _vp, _vp, _vp]),
     "dspark_confidence": (_i, [_vp, _vp, _i, _vp, _vp, _vp, _f, _vp, _i, _i, _i, _i, _i,
                                _vp, _vp, _vp]),
     "dspark_schedule": (_i, [_vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp]),
@@ -149,6 +151,18 @@ def dspark_draft_block(U, W1, W2t, anchor, temperature, seed, step, tokens, logi
     _check(lib().dspark_draft_block(_p(U), _p(W1), _p(W2t), _dtype(U), _p(anchor), bs, gamma, V, r,
                                     float(temperature), int(seed), int(step), _p(tokens), _p(logit_x),
                                     _p(lse), _p(ws), ws.numel(), _stream(stream)), "dspark_draft_block")
+
+
+def dspark_draft_block_noalloc(U, W1, W2t, anchor, temperature, seed, step, tokens, logit_x, lse,
+                               device_status=None, stream=None):
+    """The draft without a workspace, for callers that cannot allocate device memory: the
+    library's own fixed scratch array is used (see include/dspark.h for its limit and rules)."""
+    bs, gamma, V = U.shape
+    r = W1.shape[1]
+    _check(lib().dspark_draft_block_noalloc(_p(U), _p(W1), _p(W2t), _dtype(U), _p(anchor), bs, gamma, V, r,
+                                            float(temperature), int(seed), int(step), _p(tokens), _p(logit_x),
+                                            _p(lse), _p(device_status), _stream(stream)),
+           "dspark_draft_block_noalloc")
 
 
 def dspark_confidence(h, W1, anchor, tokens, w, b, sts_T, conf, surv, stream=None):
