@@ -36,6 +36,8 @@ SMALL = {
     "tiny_fp32": I.WORKLOADS["tiny_fp32"],
     "bf16_ragged": I.WORKLOADS["qwen3_4b"].with_(name="bf16_ragged", bs=5, gamma=3, V=2000, d=64, seed=11),
     "bf16_r64": I.WORKLOADS["qwen3_4b"].with_(name="bf16_r64", bs=9, gamma=4, V=1032, r=64, d=64, seed=12),
+    "bf16_two_mtiles": I.WORKLOADS["qwen3_4b"].with_(name="bf16_two_mtiles", bs=200, gamma=2, V=3000, r=128,
+                                                     d=64, seed=13),
 }
 
 
