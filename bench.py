@@ -314,6 +314,50 @@ def run_reference(args):
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_profile_case(args):
+    """A small, self-contained case for ncu captures: one stage of the mixed_bs256 workload
+    (bs 256, V 151936) with gamma = args.gamma, repeated args.steps times.  Prints the mean time."""
+    import torch
+
+    from speculative_decoding_draft_markov_gb300 import binding as B
+    from speculative_decoding_draft_markov_gb300 import build
+    from speculative_decoding_draft_markov_gb300 import inputs as I
+    from speculative_decoding_draft_markov_gb300 import step as S
+    build.build()
+    dev = torch.device("cuda", 0)
+    wl = I.WORKLOADS[WORKLOAD].with_(gamma=args.gamma)
+    inp = I.make_device_inputs(wl, dev, with_hidden=args.profile_case != "draft",
+                               with_target=args.profile_case != "draft")
+    bs, gamma, V = wl.bs, wl.gamma, wl.V
+    cap = bs * (gamma + 1)
+    buf = S.StepBuffers.allocate(bs, gamma, V, cap, inp["U"].dtype, dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    if args.profile_case == "draft":
+        def run(it):
+            B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], wl.temperature, wl.seed, it,
+                                 buf.tokens, buf.logit_x, buf.lse, buf.ws)
+    else:
+        sps = S.sps_table(I.cost_curve_ms(wl.with_(tier_max=cap)), np.zeros(0, np.int32), dev)
+        S.draft_and_schedule(inp, buf, sps, wl.temperature, wl.seed, 0, SCHED)
+        S.gather_target_forward(inp["target"])(buf)
+
+        def run(it):
+            S.verify(inp, buf, wl.temperature, wl.seed, it)
+    for it in range(2):
+        run(it)
+    torch.cuda.synchronize()
+    ev[0].record()
+    for it in range(args.steps):
+        run(it)
+    ev[1].record()
+    torch.cuda.synchronize()
+    st = B.dspark_read_device_status(buf.ws)
+    print(json.dumps({"case": args.profile_case, "gamma": gamma, "ms_per_call": ev[0].elapsed_time(ev[1]) / args.steps,
+                      "status": B.dspark_status_string(st)}))
+    if st != 0:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -321,7 +365,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=["draft", "verify"], default=None,
+                    help="run one stage of the workload (small gamma) for an ncu capture; no JSON contract")
+    ap.add_argument("--gamma", type=int, default=2, help="block length of --profile-case")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args)
+        return
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -1,22 +1,26 @@
-// S1 draft statistics on the tensor cores: tcgen05.mma (bf16 in, fp32 accumulate in TMEM),
-// operands staged by TMA, fused epilogue (+ U, temperature, per-chunk max / sum-exp or
-// argmax).  No [bs, V] logit tensor ever reaches HBM.
+// Tensor-core vocabulary passes: tcgen05.mma (bf16 in, fp32 accumulate in TMEM), operands
+// staged by TMA, fused epilogues.  No [bs, V] logit tensor ever reaches HBM.
 //
 // DSpark technical summary, "Architecture (drafter)": the Markov head's bias for position k
 // is W1[x_{k-1}] W2 (rank r = 256), added to the backbone's base logits U_k over the full
-// vocabulary.  Per position this is a GEMM [bs, r] x [r, V] whose output is consumed
-// immediately by the sampler's chunk statistics.
+// vocabulary.  Per position this is a GEMM [bs, r] x [r, V] consumed at once by a sampler.
+// Two passes share the kernel:
+//   DRAFT  (S1, one launch per position k): l = U_k + W1[x_{k-1}] W2; per (request, 128-id
+//          chunk): (max l/tau, sum exp(l/tau - max)), or (max l, argmax) at temperature 0.
+//   DECIDE (S5, after the accept scan): for each request's deciding row, p_t = softmax of the
+//          target row, p_d = softmax of the draft logits recomputed at the rejected position;
+//          per chunk: (sum max(0, p_t - p_d), sum p_t) -- the residual / bonus masses.
 //
-// Work decomposition (one launch = one position k):
+// Work decomposition:
 //   tile      = 128 requests (TMEM lanes) x 128 vocabulary ids (= one sampler chunk), K = r
-//   CTA       = persistent; fixed 128-request M-tile, strided over vocabulary chunks;
-//               the gathered A operand W1[x_{k-1}] (128 x r) stays resident in shared memory
-//   warp 0    = TMA producer: U tile (3-D map over [bs, gamma, V], evict-first) and the W2t
-//               tile in K-stages of 64 (evict-last: W2 is re-read by every position)
+//   CTA       = persistent; fixed 128-request M-tile, strided over vocabulary chunks; the
+//               gathered A operand W1[x] (128 x r) stays resident in shared memory
+//   warp 0    = TMA producer: W2t tiles in K-stages of 64 (evict-last: W2 is re-read by every
+//               position) and, in DRAFT, the U tile (3-D map over [bs, gamma, V], evict-first)
 //   warp 1    = TMEM owner + single-thread tcgen05.mma issuer, commits to mbarriers
-//   warps 2-5 = epilogue: tcgen05.ld of the 128 x 128 fp32 accumulator (one row per thread),
-//               + U from the swizzled tile, chunk statistics to the workspace
-//   2 TMEM accumulators (256 columns) and 2 U stages let MMA, loads and epilogue overlap.
+//   warps 2-5 = epilogue: tcgen05.ld of the 128 x 128 fp32 accumulator (one row per thread)
+//   warp 6    = (DECIDE) cp.async gather of each request's U row and target row
+//   2 TMEM accumulators (256 columns) let MMA, loads and epilogue overlap.
 // Every mbarrier wait is bounded (globaltimer deadline + shared abort flag); on give-up the
 // kernel records DSPARK_ETIMEOUT, waits (bounded) for its own copies / MMAs in flight,
 // frees TMEM and returns.
@@ -38,12 +42,15 @@ constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kBK = 64;
 constexpr int kBStages = 4;
-constexpr int kUStages = 2;
+constexpr int kUStages = 2;                      // DRAFT: U ring; DECIDE: one U + one target stage
 constexpr int kAccBufs = 2;
-constexpr int kThreads = 192;
 constexpr uint32_t kAtomBytes = kBM * kBK * 2;   // 16 KB: 128 rows x 128 bytes
-constexpr uint32_t kUHalf = kBM * 64 * 2;        // 16 KB: one 64-column box of U
+constexpr uint32_t kUHalf = kBM * 64 * 2;        // 16 KB: one 64-column half of a 128 x 128 bf16 tile
 constexpr uint32_t kTmemCols = kAccBufs * kBN;   // 256
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <bool kDecide>
+__host__ __device__ constexpr int threads() { return kDecide ? 224 : 192; }
 
 struct Barriers {
   uint64_t b_full[kBStages], b_empty[kBStages];
@@ -54,32 +61,73 @@ struct Barriers {
   int abort;
 };
 
+// Per-row facts of the DECIDE pass (one request per tile row).
+struct RowMeta {
+  long long u_off;  // element offset of U[b, kdec-1, 0] (residual rows)
+  long long t_off;  // element offset of target[pdec, 0] (live rows)
+  float a_t;        // lse_t * log2(e)
+  float a_d;        // lse_d * log2(e)
+  int resid;        // residual row (else bonus, or dead)
+  int live;         // the request has a decision
+};
+
+struct Params {
+  const __nv_bfloat16* W1;
+  const int32_t* anchor;
+  const int32_t* tokens;
+  int bs, gamma, V, r, k;
+  float inv_tau;
+  int greedy;
+  float2* stats;
+  int n_chunks;
+  uint32_t* status;
+  uint64_t timeout_ns;
+  // DECIDE only
+  const __nv_bfloat16* U;
+  const __nv_bfloat16* target;
+  const float* lse_d;
+  const RowStat* rs;
+  const Decision* dec;
+};
+
 __host__ __device__ constexpr size_t smem_bytes(int r) {
   return 1024 /* alignment slack */ + size_t(r / kBK) * kAtomBytes + kBStages * kAtomBytes +
-         kUStages * 2 * kUHalf + sizeof(Barriers);
+         kUStages * 2 * kUHalf + kBM * sizeof(RowMeta) + sizeof(Barriers);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) draft_stats_tc_kernel(
-    const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_u,
-    const __nv_bfloat16* __restrict__ W1, const int32_t* __restrict__ anchor,
-    const int32_t* __restrict__ tokens, int bs, int gamma, int V, int r, int k, float inv_tau,
-    int greedy, float2* __restrict__ stats, int n_chunks, uint32_t* status, uint64_t timeout_ns) {
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ void unpack8(const uint4 q, float* x) {
+  x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
+  x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
+}
+
+template <bool kDecide>
+__global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
+    const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_u, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int nk = r / kBK;
+  const int nk = p.r / kBK;
   uint8_t* sA = smem;                                   // nk atoms
   uint8_t* sB = sA + nk * kAtomBytes;                   // kBStages atoms
   uint8_t* sU = sB + kBStages * kAtomBytes;             // kUStages x 32 KB
-  Barriers* bar = reinterpret_cast<Barriers*>(sU + kUStages * 2 * kUHalf);
+  RowMeta* meta = reinterpret_cast<RowMeta*>(sU + kUStages * 2 * kUHalf);
+  Barriers* bar = reinterpret_cast<Barriers*>(meta + kBM);
   volatile int* abort_flag = &bar->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bs = p.bs, V = p.V, r = p.r;
   const int n_mt = (bs + kBM - 1) / kBM;
-  const int mt = blockIdx.x % n_mt;
-  const int m0 = mt * kBM;
+  const int m0 = (blockIdx.x % n_mt) * kBM;
   const int cstride = gridDim.x / n_mt;
   const int c0 = blockIdx.x / n_mt;
-  const int n_tiles = (c0 < n_chunks) ? (n_chunks - c0 + cstride - 1) / cstride : 0;
+  const int n_tiles = (c0 < p.n_chunks) ? (p.n_chunks - c0 + cstride - 1) / cstride : 0;
 
   if (tid == 0) {
     for (int s = 0; s < kBStages; ++s) {
@@ -87,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_stats_tc_kernel(
       tc::mbar_init(tc::smem_u32(&bar->b_empty[s]), 1);
     }
     for (int s = 0; s < kUStages; ++s) {
-      tc::mbar_init(tc::smem_u32(&bar->u_full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&bar->u_full[s]), kDecide ? 32 : 1);  // DECIDE: one arrive per loader lane
       tc::mbar_init(tc::smem_u32(&bar->u_empty[s]), kBM);
     }
     for (int s = 0; s < kAccBufs; ++s) {
@@ -98,22 +146,52 @@ __global__ void __launch_bounds__(kThreads, 1) draft_stats_tc_kernel(
     bar->abort = 0;
     tc::fence_mbar_init();
     tc::prefetch_tensormap(&tmap_w2);
-    tc::prefetch_tensormap(&tmap_u);
+    if (!kDecide) tc::prefetch_tensormap(&tmap_u);
   }
   if (warp == 1) {
     tc::tmem_alloc(tc::smem_u32(&bar->tmem_base), kTmemCols);
     tc::tmem_relinquish();
   }
-  // A operand: rows m0..m0+127 of W1[x_{k-1}] in the 128-byte-swizzled K-major layout
+  if (kDecide) {
+    for (int m = tid; m < kBM; m += threads<kDecide>()) {
+      RowMeta rm{0, 0, 0.f, 0.f, 0, 0};
+      const int grow = m0 + m;
+      if (grow < bs) {
+        const Decision d = p.dec[grow];
+        if (d.kind != kDecNone) {
+          rm.live = 1;
+          rm.t_off = (long long)d.pdec * V;
+          rm.a_t = p.rs[d.pdec].lse * kLog2e;
+          if (d.kind == kDecResidual) {
+            rm.resid = 1;
+            rm.u_off = ((long long)grow * p.gamma + d.kdec - 1) * V;
+            rm.a_d = p.lse_d[(size_t)grow * p.gamma + d.kdec - 1] * kLog2e;
+          }
+        }
+      }
+      meta[m] = rm;
+    }
+  }
+  // A operand: rows m0..m0+127 of W1[x] in the 128-byte-swizzled K-major layout, where x is
+  // x_{k-1} (DRAFT) or the token before each residual row's rejected position (DECIDE).
   {
     const int cpr = r / 8;  // 16-byte chunks per row
-    for (int idx = tid; idx < kBM * cpr; idx += kThreads) {
+    for (int idx = tid; idx < kBM * cpr; idx += threads<kDecide>()) {
       const int row = idx / cpr, ch = idx % cpr;
       const int grow = m0 + row;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (grow < bs) {
-        const int xp = clamp_token((k == 1) ? anchor[grow] : tokens[size_t(grow) * gamma + k - 2], V);
-        v = *reinterpret_cast<const uint4*>(W1 + size_t(xp) * r + ch * 8);
+        int kx = p.k;  // position whose previous token selects the W1 row
+        bool use = true;
+        if (kDecide) {
+          const Decision d = p.dec[grow];
+          use = d.kind == kDecResidual;
+          kx = d.kdec;
+        }
+        if (use) {
+          const int xp = clamp_token((kx == 1) ? p.anchor[grow] : p.tokens[size_t(grow) * p.gamma + kx - 2], V);
+          v = *reinterpret_cast<const uint4*>(p.W1 + size_t(xp) * r + ch * 8);
+        }
       }
       const int kb = ch >> 3, j = ch & 7;
       *reinterpret_cast<uint4*>(sA + kb * kAtomBytes + row * 128 + ((j ^ (row & 7)) << 4)) = v;
@@ -124,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_stats_tc_kernel(
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem_base = bar->tmem_base;
-  const uint64_t deadline = tc::globaltimer_ns() + timeout_ns;
+  const uint64_t deadline = tc::globaltimer_ns() + p.timeout_ns;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -137,17 +215,19 @@ __global__ void __launch_bounds__(kThreads, 1) draft_stats_tc_kernel(
       bool ok = true;
       for (int t = 0; t < n_tiles && ok; ++t) {
         const int n0 = (c0 + t * cstride) * kBN;
-        if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->u_empty[us]), uph ^ 1, deadline, abort_flag)) {
-          ok = false;
-          break;
+        if (!kDecide) {
+          if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->u_empty[us]), uph ^ 1, deadline, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t ufull = tc::smem_u32(&bar->u_full[us]);
+          tc::mbar_arrive_expect_tx(ufull, 2 * kUHalf);
+          const uint32_t ud = tc::smem_u32(sU + us * 2 * kUHalf);
+          tc::tma_load_3d(ud, &tmap_u, ufull, n0, p.k - 1, m0, stream);
+          tc::tma_load_3d(ud + kUHalf, &tmap_u, ufull, n0 + 64, p.k - 1, m0, stream);
+          u_issued[us] = uph;
+          if (++us == kUStages) { us = 0; uph ^= 1; }
         }
-        const uint32_t ufull = tc::smem_u32(&bar->u_full[us]);
-        tc::mbar_arrive_expect_tx(ufull, 2 * kUHalf);
-        const uint32_t ud = tc::smem_u32(sU + us * 2 * kUHalf);
-        tc::tma_load_3d(ud, &tmap_u, ufull, n0, k - 1, m0, stream);
-        tc::tma_load_3d(ud + kUHalf, &tmap_u, ufull, n0 + 64, k - 1, m0, stream);
-        u_issued[us] = uph;
-        if (++us == kUStages) { us = 0; uph ^= 1; }
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->b_empty[bstage]), bph ^ 1, deadline, abort_flag)) {
             ok = false;
@@ -162,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_stats_tc_kernel(
       }
       if (!ok) {
         *abort_flag = 1;
-        set_status(status, DSPARK_ETIMEOUT);
+        set_status(p.status, DSPARK_ETIMEOUT);
         // wait (bounded) for every copy this thread put in flight before the CTA exits
         const uint64_t dl = tc::globaltimer_ns() + 200000000ull;
         const volatile int never = 0;
@@ -207,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_stats_tc_kernel(
       }
       if (!ok) {
         *abort_flag = 1;
-        set_status(status, DSPARK_ETIMEOUT);
+        set_status(p.status, DSPARK_ETIMEOUT);
         if (issued) {  // wait (bounded) for the MMAs already issued before TMEM is freed
           tc::mma_commit(tc::smem_u32(&bar->drain));
           const volatile int never = 0;
@@ -215,12 +295,45 @@ __global__ void __launch_bounds__(kThreads, 1) draft_stats_tc_kernel(
         }
       }
     }
-  } else {
+  } else if (kDecide && warp == 6) {
+    // ------------------------------------------------------------------ row gather (DECIDE)
+    // U stage 0 holds the U rows, U stage 1 the target rows of the current tile.
+    int ph = 0;
+    bool ok = true;
+    const int sub = lane >> 4, c16 = lane & 15, h = c16 >> 3, j = c16 & 7;
+    const uint32_t su = tc::smem_u32(sU), st = tc::smem_u32(sU + 2 * kUHalf);
+    for (int t = 0; t < n_tiles; ++t) {
+      const int n0 = (c0 + t * cstride) * kBN;
+      if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->u_empty[0]), ph ^ 1, deadline, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const int col = n0 + c16 * 8;
+      const bool in_v = col < V;
+#pragma unroll 4
+      for (int it = 0; it < kBM / 2; ++it) {
+        const int row = it * 2 + sub;
+        const RowMeta rm = meta[row];
+        const uint32_t off = h * kUHalf + row * 128 + ((j ^ (row & 7)) << 4);
+        const bool gu = rm.resid && in_v, gt = rm.live && in_v;
+        cp_async16(su + off, gu ? p.U + rm.u_off + col : p.U, gu ? 16u : 0u);
+        cp_async16(st + off, gt ? p.target + rm.t_off + col : p.target, gt ? 16u : 0u);
+      }
+      cp_async_arrive_noinc(tc::smem_u32(&bar->u_full[0]));
+      ph ^= 1;
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      set_status(p.status, DSPARK_ETIMEOUT);
+    }
+    cp_async_wait_all();  // no copy of this warp outlives the CTA
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------------ epilogue (128 threads)
     const int wq = warp & 3;          // TMEM lane quarter this warp may access
     const int m = wq * 32 + lane;     // tile row = TMEM lane
     const int grow = m0 + m;
-    const float c2 = inv_tau * 1.4426950408889634f;
+    const float inv_tau = p.inv_tau;
+    const float c2 = inv_tau * kLog2e;
     int us = 0, uph = 0, ab = 0, aph = 0;
     for (int t = 0; t < n_tiles; ++t) {
       const int c = c0 + t * cstride;
@@ -229,56 +342,91 @@ __global__ void __launch_bounds__(kThreads, 1) draft_stats_tc_kernel(
       if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[ab]), aph, deadline, abort_flag) ||
           !tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[us]), uph, deadline, abort_flag)) {
         *abort_flag = 1;
-        set_status(status, DSPARK_ETIMEOUT);
+        set_status(p.status, DSPARK_ETIMEOUT);
         break;
       }
       tc::tc_fence_after();
-      float v[kBN];
       const uint32_t taddr = tmem_base + (uint32_t(wq * 32) << 16) + ab * kBN;
-#pragma unroll
-      for (int q = 0; q < kBN / 32; ++q) tc::tmem_ld32(taddr + q * 32, reinterpret_cast<uint32_t*>(v + q * 32));
-      tc::tmem_ld_wait();
-      tc::tc_fence_before();
-      tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[ab]));
-      if (++ab == kAccBufs) { ab = 0; aph ^= 1; }
-
-      const uint8_t* ub = sU + us * 2 * kUHalf + m * 128;
-#pragma unroll
-      for (int j16 = 0; j16 < kBN / 8; ++j16) {
-        const int h = j16 >> 3, j = j16 & 7;
-        const uint4 q = *reinterpret_cast<const uint4*>(ub + h * kUHalf + ((j ^ (m & 7)) << 4));
-        v[8 * j16 + 0] += bf16lo(q.x);
-        v[8 * j16 + 1] += bf16hi(q.x);
-        v[8 * j16 + 2] += bf16lo(q.y);
-        v[8 * j16 + 3] += bf16hi(q.y);
-        v[8 * j16 + 4] += bf16lo(q.z);
-        v[8 * j16 + 5] += bf16hi(q.z);
-        v[8 * j16 + 6] += bf16lo(q.w);
-        v[8 * j16 + 7] += bf16hi(q.w);
-      }
-      tc::mbar_arrive(tc::smem_u32(&bar->u_empty[us]));
-      if (++us == kUStages) { us = 0; uph ^= 1; }
-
       float2 out;
-      if (greedy) {
-        float best = -INFINITY;
-        int bi = INT_MAX;
+      if (!kDecide) {
+        float v[kBN];
 #pragma unroll
-        for (int i = 0; i < kBN; ++i)
-          if (i < valid && v[i] > best) { best = v[i]; bi = i; }
-        out = make_float2(best, __int_as_float(bi == INT_MAX ? INT_MAX : n0 + bi));
+        for (int q = 0; q < kBN / 32; ++q) tc::tmem_ld32(taddr + q * 32, reinterpret_cast<uint32_t*>(v + q * 32));
+        tc::tmem_ld_wait();
+        tc::tc_fence_before();
+        tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[ab]));
+
+        const uint8_t* ub = sU + us * 2 * kUHalf + m * 128;
+#pragma unroll
+        for (int j16 = 0; j16 < kBN / 8; ++j16) {
+          float x[8];
+          unpack8(*reinterpret_cast<const uint4*>(ub + (j16 >> 3) * kUHalf + (((j16 & 7) ^ (m & 7)) << 4)), x);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[8 * j16 + e] += x[e];
+        }
+        tc::mbar_arrive(tc::smem_u32(&bar->u_empty[us]));
+
+        if (p.greedy) {
+          float best = -INFINITY;
+          int bi = INT_MAX;
+#pragma unroll
+          for (int i = 0; i < kBN; ++i)
+            if (i < valid && v[i] > best) { best = v[i]; bi = i; }
+          out = make_float2(best, __int_as_float(bi == INT_MAX ? INT_MAX : n0 + bi));
+        } else {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < kBN; ++i)
+            if (i < valid) mx = fmaxf(mx, v[i]);
+          float s = 0.f;
+#pragma unroll
+          for (int i = 0; i < kBN; ++i)
+            if (i < valid) s += exp2f((v[i] - mx) * c2);
+          out = make_float2(mx * inv_tau, s);
+        }
       } else {
-        float mx = -INFINITY;
+        // residual / bonus masses, 32 columns at a time
+        const RowMeta rm = meta[m];
+        const uint8_t* ub = sU + m * 128;
+        const uint8_t* tb = sU + 2 * kUHalf + m * 128;
+        float R = 0.f, P = 0.f;
 #pragma unroll
-        for (int i = 0; i < kBN; ++i)
-          if (i < valid) mx = fmaxf(mx, v[i]);
-        float s = 0.f;
+        for (int q = 0; q < kBN / 32; ++q) {
+          float v[32];
+          tc::tmem_ld32(taddr + q * 32, reinterpret_cast<uint32_t*>(v));
+          tc::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < kBN; ++i)
-          if (i < valid) s += exp2f((v[i] - mx) * c2);
-        out = make_float2(mx * inv_tau, s);
+          for (int j4 = 0; j4 < 4; ++j4) {
+            const int j16 = q * 4 + j4;
+            const uint32_t off = (j16 >> 3) * kUHalf + (((j16 & 7) ^ (m & 7)) << 4);
+            float xu[8], xt[8];
+            unpack8(*reinterpret_cast<const uint4*>(ub + off), xu);
+            unpack8(*reinterpret_cast<const uint4*>(tb + off), xt);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int i = 8 * j16 + e;
+              const float pt = exp2f(fmaf(xt[e], c2, -rm.a_t));
+              const float pd = exp2f(fmaf(v[8 * j4 + e] + xu[e], c2, -rm.a_d));
+              const float w = rm.resid ? fmaxf(0.f, pt - pd) : pt;
+              if (i < valid && rm.live) {
+                R += w;
+                P += pt;
+              }
+            }
+          }
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[ab]));
+        tc::mbar_arrive(tc::smem_u32(&bar->u_empty[0]));
+        out = make_float2(R, P);
       }
-      if (grow < bs) stats[size_t(grow) * n_chunks + c] = out;
+      if (++ab == kAccBufs) { ab = 0; aph ^= 1; }
+      if (!kDecide) {
+        if (++us == kUStages) { us = 0; uph ^= 1; }
+      } else {
+        uph ^= 1;  // one stage (index 0) in DECIDE
+      }
+      if (grow < bs) p.stats[size_t(grow) * p.n_chunks + c] = out;
     }
   }
 
@@ -295,12 +443,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
-    void* p = nullptr;
+    void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
   });
   return fn;
 }
@@ -310,6 +458,29 @@ int sm_count() {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   return n > 0 ? n : 1;
+}
+
+bool encode_w2(CUtensorMap* map, const void* W2t, int V, int r) {
+  const cuuint64_t dims[2] = {cuuint64_t(r), cuuint64_t(V)};
+  const cuuint64_t strides[1] = {cuuint64_t(r) * 2};
+  const cuuint32_t box[2] = {kBK, kBN};
+  const cuuint32_t es[2] = {1, 1};
+  return encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2t), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kDecide>
+cudaError_t launch(const CUtensorMap& w2, const CUtensorMap& u, const Params& prm, cudaStream_t s) {
+  const size_t smem = smem_bytes(prm.r);
+  const cudaError_t attr = cudaFuncSetAttribute(stats_tc_kernel<kDecide>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes(256)));
+  if (attr != cudaSuccess) return attr;
+  const int n_mt = (prm.bs + kBM - 1) / kBM;
+  int grid = (sm_count() / n_mt) * n_mt;
+  grid = min(grid, n_mt * prm.n_chunks);
+  stats_tc_kernel<kDecide><<<grid, threads<kDecide>(), smem, s>>>(w2, u, prm);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -325,41 +496,58 @@ cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t
                                   const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
                                   int V, int r, int k, float inv_tau, int greedy, void* stats,
                                   int n_chunks, uint32_t* status, cudaStream_t s) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
+  if (!encode_fn()) return cudaErrorNotSupported;
   CUtensorMap map_w2, map_u;
-  {
-    const cuuint64_t dims[2] = {cuuint64_t(r), cuuint64_t(V)};
-    const cuuint64_t strides[1] = {cuuint64_t(r) * 2};
-    const cuuint32_t box[2] = {kBK, kBN};
-    const cuuint32_t es[2] = {1, 1};
-    if (enc(&map_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2t), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  if (!encode_w2(&map_w2, W2t, V, r)) return cudaErrorInvalidValue;
   {
     const cuuint64_t dims[3] = {cuuint64_t(V), cuuint64_t(gamma), cuuint64_t(bs)};
     const cuuint64_t strides[2] = {cuuint64_t(V) * 2, cuuint64_t(gamma) * V * 2};
     const cuuint32_t box[3] = {64, 1, kBM};
     const cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&map_u, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(U), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (encode_fn()(&map_u, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(U), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const size_t smem = smem_bytes(r);
-  const cudaError_t attr_err = cudaFuncSetAttribute(
-      draft_stats_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes(256)));
-  if (attr_err != cudaSuccess) return attr_err;
-  const int n_mt = (bs + kBM - 1) / kBM;
-  int grid = (sm_count() / n_mt) * n_mt;
-  grid = min(grid, n_mt * n_chunks);
-  draft_stats_tc_kernel<<<grid, kThreads, smem, s>>>(map_w2, map_u, static_cast<const __nv_bfloat16*>(W1), anchor,
-                                                     tokens, bs, gamma, V, r, k, inv_tau, greedy,
-                                                     static_cast<float2*>(stats), n_chunks, status,
-                                                     g_wait_timeout_ns);
-  return cudaGetLastError();
+  Params prm{};
+  prm.W1 = static_cast<const __nv_bfloat16*>(W1);
+  prm.anchor = anchor;
+  prm.tokens = tokens;
+  prm.bs = bs; prm.gamma = gamma; prm.V = V; prm.r = r; prm.k = k;
+  prm.inv_tau = inv_tau;
+  prm.greedy = greedy;
+  prm.stats = static_cast<float2*>(stats);
+  prm.n_chunks = n_chunks;
+  prm.status = status;
+  prm.timeout_ns = g_wait_timeout_ns;
+  return launch<false>(map_w2, map_u, prm, s);
+}
+
+cudaError_t launch_decision_stats_tc(const void* target, const void* U, const void* W1, const void* W2t,
+                                     const int32_t* anchor, const int32_t* tokens, const float* lse_d,
+                                     const void* rs, const void* dec, int bs, int gamma, int V, int r,
+                                     float inv_tau, void* stats, int n_chunks, uint32_t* status,
+                                     cudaStream_t s) {
+  if (!encode_fn()) return cudaErrorNotSupported;
+  CUtensorMap map_w2;
+  if (!encode_w2(&map_w2, W2t, V, r)) return cudaErrorInvalidValue;
+  Params prm{};
+  prm.W1 = static_cast<const __nv_bfloat16*>(W1);
+  prm.anchor = anchor;
+  prm.tokens = tokens;
+  prm.bs = bs; prm.gamma = gamma; prm.V = V; prm.r = r; prm.k = 0;
+  prm.inv_tau = inv_tau;
+  prm.greedy = 0;
+  prm.stats = static_cast<float2*>(stats);
+  prm.n_chunks = n_chunks;
+  prm.status = status;
+  prm.timeout_ns = g_wait_timeout_ns;
+  prm.U = static_cast<const __nv_bfloat16*>(U);
+  prm.target = static_cast<const __nv_bfloat16*>(target);
+  prm.lse_d = lse_d;
+  prm.rs = static_cast<const RowStat*>(rs);
+  prm.dec = static_cast<const Decision*>(dec);
+  return launch<true>(map_w2, map_w2, prm, s);
 }
 
 }  // namespace dspark

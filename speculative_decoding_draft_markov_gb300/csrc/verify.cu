@@ -337,8 +337,15 @@ static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_
                                                          out_tokens, acc_len, ceiling, dec, status);
   if (!greedy) {
     constexpr int RB = 32;
-    decision_stats_simt_kernel<T, RB><<<dim3(L.n_chunks, (bs + RB - 1) / RB), kChunk, 0, s>>>(
-        target, U, W1, W2t, anchor, tokens, lse, rs, dec, bs, gamma, V, r, inv_tau, stats, L.n_chunks);
+    constexpr bool kBf16 = sizeof(T) == 2;
+    if (kBf16 && draft_tc_supported(DSPARK_BF16, bs, V, r)) {
+      const cudaError_t e = launch_decision_stats_tc(target, U, W1, W2t, anchor, tokens, lse, rs, dec, bs, gamma, V,
+                                                     r, inv_tau, stats, L.n_chunks, status, s);
+      if (e != cudaSuccess) return e;
+    } else {
+      decision_stats_simt_kernel<T, RB><<<dim3(L.n_chunks, (bs + RB - 1) / RB), kChunk, 0, s>>>(
+          target, U, W1, W2t, anchor, tokens, lse, rs, dec, bs, gamma, V, r, inv_tau, stats, L.n_chunks);
+    }
     decision_select_kernel<T><<<bs, 256, 0, s>>>(target, U, W1, W2t, anchor, tokens, lse, rs, dec,
                                                  stats, L.n_chunks, bs, gamma, V, r, inv_tau, seed,
                                                  step, out_tokens);
