@@ -127,6 +127,70 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ----------------------------------------------------------------------------------------
+// Dot products W2t[v] . a for the 128 ids v0 .. v0+127 of one sampler chunk, by a 256-thread
+// block: warp w takes ids v0 + 16w .. v0 + 16w + 15, lane l the K slice [8l, 8l + 8).  All 16
+// rows' loads are issued before any arithmetic; fixed summation order.  out[i] (shared memory)
+// receives the dot of id v0 + i, 0 for ids >= V.  Requires r % 8 == 0 and r <= 256.
+// ----------------------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ void chunk_dots(const T* __restrict__ W2t, int r, int V, int v0,
+                                           const float* __restrict__ a, float* out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool on = lane * 8 < r;
+  float av[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) av[e] = on ? a[lane * 8 + e] : 0.f;
+  float part[16];
+  if constexpr (sizeof(T) == 2) {
+    uint4 q[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int v = v0 + warp * 16 + j;
+      q[j] = (on && v < V) ? *reinterpret_cast<const uint4*>(W2t + size_t(v) * r + lane * 8)
+                           : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float acc = bf16lo(q[j].x) * av[0];
+      acc = fmaf(bf16hi(q[j].x), av[1], acc);
+      acc = fmaf(bf16lo(q[j].y), av[2], acc);
+      acc = fmaf(bf16hi(q[j].y), av[3], acc);
+      acc = fmaf(bf16lo(q[j].z), av[4], acc);
+      acc = fmaf(bf16hi(q[j].z), av[5], acc);
+      acc = fmaf(bf16lo(q[j].w), av[6], acc);
+      acc = fmaf(bf16hi(q[j].w), av[7], acc);
+      part[j] = acc;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int v = v0 + warp * 16 + j;
+      float acc = 0.f;
+      if (on && v < V) {
+        const float4 x0 = *reinterpret_cast<const float4*>(W2t + size_t(v) * r + lane * 8);
+        const float4 x1 = *reinterpret_cast<const float4*>(W2t + size_t(v) * r + lane * 8 + 4);
+        acc = x0.x * av[0];
+        acc = fmaf(x0.y, av[1], acc);
+        acc = fmaf(x0.z, av[2], acc);
+        acc = fmaf(x0.w, av[3], acc);
+        acc = fmaf(x1.x, av[4], acc);
+        acc = fmaf(x1.y, av[5], acc);
+        acc = fmaf(x1.z, av[6], acc);
+        acc = fmaf(x1.w, av[7], acc);
+      }
+      part[j] = acc;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float t = part[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+    if (lane == j) out[warp * 16 + j] = t;
+  }
+}
+
+// ----------------------------------------------------------------------------------------
 // Deterministic reductions (fixed shuffle tree, fixed warp order)
 // ----------------------------------------------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v) {

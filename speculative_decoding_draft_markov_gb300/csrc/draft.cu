@@ -131,15 +131,11 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
   const int xp = clamp_token((k == 1) ? anchor[b] : tokens[size_t(b) * gamma + k - 2], V);
   for (int i = tid; i < r; i += 256) sA[i] = ld_f32(W1, size_t(xp) * r + i);
   __syncthreads();
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int vv = warp; vv < kChunk; vv += 8) {
-    const int v = cstar * kChunk + vv;
-    float dot = 0.f;
-    if (v < V)
-      for (int i = lane; i < r; i += 32) dot = fmaf(sA[i], ld_f32(W2t, size_t(v) * r + i), dot);
-    dot = warp_sum(dot);
-    if (lane == 0)
-      tv[vv] = (v < V) ? (dot + ld_f32(U, (size_t(b) * gamma + (k - 1)) * V + v)) * inv_tau : -INFINITY;
+  chunk_dots<T>(W2t, r, V, cstar * kChunk, sA, tv);
+  __syncthreads();
+  if (tid < kChunk) {
+    const int v = cstar * kChunk + tid;
+    tv[tid] = (v < V) ? (tv[tid] + ld_f32(U, (size_t(b) * gamma + (k - 1)) * V + v)) * inv_tau : -INFINITY;
   }
   __syncthreads();
   ArgMax e{-INFINITY, INT_MAX};

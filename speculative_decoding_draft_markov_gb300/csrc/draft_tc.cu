@@ -41,7 +41,7 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kBK = 64;
-constexpr int kBStages = 4;
+constexpr int kBStagesMax = 6;
 constexpr int kUStages = 2;                      // DRAFT: U ring; DECIDE: one U + one target stage
 constexpr int kAccBufs = 2;
 constexpr uint32_t kAtomBytes = kBM * kBK * 2;   // 16 KB: 128 rows x 128 bytes
@@ -49,11 +49,17 @@ constexpr uint32_t kUHalf = kBM * 64 * 2;        // 16 KB: one 64-column half of
 constexpr uint32_t kTmemCols = kAccBufs * kBN;   // 256
 constexpr float kLog2e = 1.4426950408889634f;
 
+// DRAFT: W2t ring of 6 K-stages, 8 epilogue warps (two per TMEM lane quarter, 64 columns
+// each).  DECIDE: 4 K-stages, 4 epilogue warps and one gather warp.
 template <bool kDecide>
-__host__ __device__ constexpr int threads() { return kDecide ? 224 : 192; }
+__host__ __device__ constexpr int b_stages() { return kDecide ? 4 : 6; }
+template <bool kDecide>
+__host__ __device__ constexpr int epi_warps() { return kDecide ? 4 : 8; }
+template <bool kDecide>
+__host__ __device__ constexpr int threads() { return 32 * (2 + epi_warps<kDecide>() + (kDecide ? 1 : 0)); }
 
 struct Barriers {
-  uint64_t b_full[kBStages], b_empty[kBStages];
+  uint64_t b_full[kBStagesMax], b_empty[kBStagesMax];
   uint64_t u_full[kUStages], u_empty[kUStages];
   uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
   uint64_t drain;
@@ -90,9 +96,16 @@ struct Params {
   const Decision* dec;
 };
 
+// Dynamic shared memory: A atoms | W2t ring | U stages | DECIDE row facts or DRAFT half-row
+// exchange | barriers.  The buffer is declared 1024-byte aligned (128-byte swizzle atoms).
+template <bool kDecide>
+__host__ __device__ constexpr size_t extra_bytes() {
+  return kDecide ? kBM * sizeof(RowMeta) : 2 * kBM * sizeof(float2);
+}
+template <bool kDecide>
 __host__ __device__ constexpr size_t smem_bytes(int r) {
-  return 1024 /* alignment slack */ + size_t(r / kBK) * kAtomBytes + kBStages * kAtomBytes +
-         kUStages * 2 * kUHalf + kBM * sizeof(RowMeta) + sizeof(Barriers);
+  return size_t(r / kBK) * kAtomBytes + b_stages<kDecide>() * kAtomBytes + kUStages * 2 * kUHalf +
+         extra_bytes<kDecide>() + sizeof(Barriers);
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
@@ -111,14 +124,22 @@ __device__ __forceinline__ void unpack8(const uint4 q, float* x) {
 template <bool kDecide>
 __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_u, const Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  constexpr int kBStages = b_stages<kDecide>();
+  constexpr int kEpiThreads = 32 * epi_warps<kDecide>();
+  if (tc::smem_u32(smem_raw) & 1023u) {  // the swizzled layouts need 1024-byte alignment
+    if (threadIdx.x == 0) set_status(p.status, DSPARK_EUNSUPPORTED);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   const int nk = p.r / kBK;
   uint8_t* sA = smem;                                   // nk atoms
   uint8_t* sB = sA + nk * kAtomBytes;                   // kBStages atoms
   uint8_t* sU = sB + kBStages * kAtomBytes;             // kUStages x 32 KB
-  RowMeta* meta = reinterpret_cast<RowMeta*>(sU + kUStages * 2 * kUHalf);
-  Barriers* bar = reinterpret_cast<Barriers*>(meta + kBM);
+  uint8_t* sX = sU + kUStages * 2 * kUHalf;             // row facts (DECIDE) / half-row exchange (DRAFT)
+  RowMeta* meta = reinterpret_cast<RowMeta*>(sX);
+  float2* xchg = reinterpret_cast<float2*>(sX);         // [2 tile parities][128 rows]
+  Barriers* bar = reinterpret_cast<Barriers*>(sX + extra_bytes<kDecide>());
   volatile int* abort_flag = &bar->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -136,11 +157,11 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
     }
     for (int s = 0; s < kUStages; ++s) {
       tc::mbar_init(tc::smem_u32(&bar->u_full[s]), kDecide ? 32 : 1);  // DECIDE: one arrive per loader lane
-      tc::mbar_init(tc::smem_u32(&bar->u_empty[s]), kBM);
+      tc::mbar_init(tc::smem_u32(&bar->u_empty[s]), kEpiThreads);
     }
     for (int s = 0; s < kAccBufs; ++s) {
       tc::mbar_init(tc::smem_u32(&bar->acc_full[s]), 1);
-      tc::mbar_init(tc::smem_u32(&bar->acc_empty[s]), kBM);
+      tc::mbar_init(tc::smem_u32(&bar->acc_empty[s]), kEpiThreads);
     }
     tc::mbar_init(tc::smem_u32(&bar->drain), 1);
     bar->abort = 0;
@@ -295,7 +316,7 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
         }
       }
     }
-  } else if (kDecide && warp == 6) {
+  } else if (kDecide && warp == 2 + epi_warps<kDecide>()) {
     // ------------------------------------------------------------------ row gather (DECIDE)
     // U stage 0 holds the U rows, U stage 1 the target rows of the current tile.
     int ph = 0;
@@ -327,10 +348,11 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
       set_status(p.status, DSPARK_ETIMEOUT);
     }
     cp_async_wait_all();  // no copy of this warp outlives the CTA
-  } else if (warp >= 2 && warp <= 5) {
-    // ------------------------------------------------------------------ epilogue (128 threads)
+  } else if (warp >= 2 && warp < 2 + epi_warps<kDecide>()) {
+    // ------------------------------------------------------------------ epilogue
     const int wq = warp & 3;          // TMEM lane quarter this warp may access
     const int m = wq * 32 + lane;     // tile row = TMEM lane
+    const int half = (warp - 2) >> 2; // DRAFT: which 64 of the 128 columns this warp takes
     const int grow = m0 + m;
     const float inv_tau = p.inv_tau;
     const float c2 = inv_tau * kLog2e;
@@ -339,8 +361,13 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
       const int c = c0 + t * cstride;
       const int n0 = c * kBN;
       const int valid = min(kBN, V - n0);
-      if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[ab]), aph, deadline, abort_flag) ||
-          !tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[us]), uph, deadline, abort_flag)) {
+      bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[ab]), aph, deadline, abort_flag) &&
+                tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[us]), uph, deadline, abort_flag);
+      // one decision for every epilogue thread before any .sync.aligned TMEM load or named
+      // barrier, so that no thread can be left waiting on one that gave up
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      ok = tc::named_barrier_and(2, kEpiThreads, ok);
+      if (!ok) {
         *abort_flag = 1;
         set_status(p.status, DSPARK_ETIMEOUT);
         break;
@@ -349,40 +376,62 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
       const uint32_t taddr = tmem_base + (uint32_t(wq * 32) << 16) + ab * kBN;
       float2 out;
       if (!kDecide) {
-        float v[kBN];
+        constexpr int kH = kBN / 2;  // columns per thread
+        float v[kH];
 #pragma unroll
-        for (int q = 0; q < kBN / 32; ++q) tc::tmem_ld32(taddr + q * 32, reinterpret_cast<uint32_t*>(v + q * 32));
+        for (int q = 0; q < kH / 32; ++q)
+          tc::tmem_ld32(taddr + half * kH + q * 32, reinterpret_cast<uint32_t*>(v + q * 32));
         tc::tmem_ld_wait();
         tc::tc_fence_before();
         tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[ab]));
 
-        const uint8_t* ub = sU + us * 2 * kUHalf + m * 128;
+        const uint8_t* ub = sU + us * 2 * kUHalf + half * kUHalf + m * 128;
 #pragma unroll
-        for (int j16 = 0; j16 < kBN / 8; ++j16) {
+        for (int j = 0; j < kH / 8; ++j) {
           float x[8];
-          unpack8(*reinterpret_cast<const uint4*>(ub + (j16 >> 3) * kUHalf + (((j16 & 7) ^ (m & 7)) << 4)), x);
+          unpack8(*reinterpret_cast<const uint4*>(ub + ((j ^ (m & 7)) << 4)), x);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) v[8 * j16 + e] += x[e];
+          for (int e = 0; e < 8; ++e) v[8 * j + e] += x[e];
         }
         tc::mbar_arrive(tc::smem_u32(&bar->u_empty[us]));
 
+        const int vh = valid - half * kH;  // valid columns of this half (may be <= 0)
+        float2 part;
         if (p.greedy) {
           float best = -INFINITY;
           int bi = INT_MAX;
 #pragma unroll
-          for (int i = 0; i < kBN; ++i)
-            if (i < valid && v[i] > best) { best = v[i]; bi = i; }
-          out = make_float2(best, __int_as_float(bi == INT_MAX ? INT_MAX : n0 + bi));
+          for (int i = 0; i < kH; ++i)
+            if (i < vh && v[i] > best) { best = v[i]; bi = i; }
+          part = make_float2(best, __int_as_float(bi == INT_MAX ? INT_MAX : n0 + half * kH + bi));
         } else {
-          float mx = -INFINITY;
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int i = 0; i < kBN; ++i)
-            if (i < valid) mx = fmaxf(mx, v[i]);
-          float s = 0.f;
+          for (int i = 0; i < kH; ++i)
+            if (i < vh) m4[i & 3] = fmaxf(m4[i & 3], v[i]);
+          const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i < kBN; ++i)
-            if (i < valid) s += exp2f((v[i] - mx) * c2);
-          out = make_float2(mx * inv_tau, s);
+          for (int i = 0; i < kH; ++i)
+            if (i < vh) s4[i & 3] += exp2f((v[i] - mx) * c2);
+          part = make_float2(mx * inv_tau, (s4[0] + s4[1]) + (s4[2] + s4[3]));
+        }
+        // combine the two halves of the row: half 1 hands its partial to half 0
+        float2* slot = xchg + (t & 1) * kBM + m;
+        if (half == 1) *slot = part;
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+        if (half == 0) {
+          const float2 o = *slot;
+          if (p.greedy) {
+            out = (o.x > part.x) ? o : part;  // ties keep the lower ids (half 0)
+          } else if (o.y == 0.f) {
+            out = part;
+          } else if (part.y == 0.f) {
+            out = o;
+          } else {
+            const float mm = fmaxf(part.x, o.x);
+            out = make_float2(mm, part.y * __expf(part.x - mm) + o.y * __expf(o.x - mm));
+          }
         }
       } else {
         // residual / bonus masses, 32 columns at a time
@@ -426,7 +475,7 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
       } else {
         uph ^= 1;  // one stage (index 0) in DECIDE
       }
-      if (grow < bs) p.stats[size_t(grow) * p.n_chunks + c] = out;
+      if (grow < bs && (kDecide || half == 0)) p.stats[size_t(grow) * p.n_chunks + c] = out;
     }
   }
 
@@ -472,9 +521,10 @@ bool encode_w2(CUtensorMap* map, const void* W2t, int V, int r) {
 
 template <bool kDecide>
 cudaError_t launch(const CUtensorMap& w2, const CUtensorMap& u, const Params& prm, cudaStream_t s) {
-  const size_t smem = smem_bytes(prm.r);
+  const size_t smem = smem_bytes<kDecide>(prm.r);
   const cudaError_t attr = cudaFuncSetAttribute(stats_tc_kernel<kDecide>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes(256)));
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                int(smem_bytes<kDecide>(256)));
   if (attr != cudaSuccess) return attr;
   const int n_mt = (prm.bs + kBM - 1) / kBM;
   int grid = (sm_count() / n_mt) * n_mt;

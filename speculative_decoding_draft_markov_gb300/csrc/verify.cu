@@ -60,14 +60,23 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
   const T* row = target + size_t(p) * V;
   constexpr int G = sizeof(T) == 2 ? 8 : 4;
   const int ng = V / G;
-  float x[8];
   if (greedy) {
     ArgMax best{-INFINITY, INT_MAX};
-    for (int e = tid; e < ng; e += kRowThreads) {
-      load_group<T>(row, e, x);
+    for (int e0 = tid; e0 < ng; e0 += 4 * kRowThreads) {
+      float xb[4][8];
 #pragma unroll
-      for (int q = 0; q < G; ++q)
-        if (x[q] > best.v) best = ArgMax{x[q], e * G + q};
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kRowThreads;
+        if (e < ng) load_group<T>(row, e, xb[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kRowThreads;
+        if (e >= ng) break;
+#pragma unroll
+        for (int q = 0; q < G; ++q)
+          if (xb[u][q] > best.v) best = ArgMax{xb[u][q], e * G + q};
+      }
     }
     best = block_argmax<kRowThreads>(best, sv, si);
     if (tid == 0) {
@@ -82,17 +91,27 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
     return;
   }
   LsePair acc{-INFINITY, 0.f};
-  for (int e = tid; e < ng; e += kRowThreads) {
-    load_group<T>(row, e, x);
-    float gm = x[0] * inv_tau;
+  constexpr int kBatch = 4;  // independent 16-byte loads in flight per thread
+  for (int e0 = tid; e0 < ng; e0 += kBatch * kRowThreads) {
+    float xb[kBatch][8];
 #pragma unroll
-    for (int q = 1; q < G; ++q) gm = fmaxf(gm, x[q] * inv_tau);
-    if (gm > acc.m) {
-      acc.s = (acc.s == 0.f) ? 0.f : acc.s * expf(acc.m - gm);
-      acc.m = gm;
+    for (int u = 0; u < kBatch; ++u) {
+      const int e = e0 + u * kRowThreads;
+      if (e < ng) load_group<T>(row, e, xb[u]);
     }
 #pragma unroll
-    for (int q = 0; q < G; ++q) acc.s += expf(x[q] * inv_tau - acc.m);
+    for (int u = 0; u < kBatch; ++u) {
+      if (e0 + u * kRowThreads >= ng) break;
+      float gm = xb[u][0] * inv_tau;
+#pragma unroll
+      for (int q = 1; q < G; ++q) gm = fmaxf(gm, xb[u][q] * inv_tau);
+      if (gm > acc.m) {
+        acc.s = (acc.s == 0.f) ? 0.f : acc.s * expf(acc.m - gm);
+        acc.m = gm;
+      }
+#pragma unroll
+      for (int q = 0; q < G; ++q) acc.s += expf(xb[u][q] * inv_tau - acc.m);
+    }
   }
   acc = block_lse<kRowThreads>(acc, sv, ss);
   if (tid == 0) {
@@ -279,26 +298,21 @@ __global__ void __launch_bounds__(256) decision_select_kernel(
   }
   __syncthreads();
   const float lse_t = rs[d.pdec].lse;
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int vv = warp; vv < kChunk; vv += 8) {
-    const int v = cstar * kChunk + vv;
-    float dot = 0.f;
-    if (resid && v < V)
-      for (int i = lane; i < r; i += 32) dot = fmaf(sA[i], ld_f32(W2t, size_t(v) * r + i), dot);
-    dot = warp_sum(dot);
-    if (lane == 0) {
-      float pt = 0.f, w = 0.f;
-      if (v < V) {
-        pt = expf(ld_f32(target, size_t(d.pdec) * V + v) * inv_tau - lse_t);
-        w = pt;
-        if (resid) {
-          const float dl = (dot + ld_f32(U, (size_t(b) * gamma + d.kdec - 1) * V + v)) * inv_tau;
-          w = fmaxf(0.f, pt - expf(dl - lse_d[size_t(b) * gamma + d.kdec - 1]));
-        }
+  if (resid) chunk_dots<T>(W2t, r, V, cstar * kChunk, sA, tw);
+  __syncthreads();
+  if (tid < kChunk) {
+    const int v = cstar * kChunk + tid;
+    float pt = 0.f, w = 0.f;
+    if (v < V) {
+      pt = expf(ld_f32(target, size_t(d.pdec) * V + v) * inv_tau - lse_t);
+      w = pt;
+      if (resid) {
+        const float dl = (tw[tid] + ld_f32(U, (size_t(b) * gamma + d.kdec - 1) * V + v)) * inv_tau;
+        w = fmaxf(0.f, pt - expf(dl - lse_d[size_t(b) * gamma + d.kdec - 1]));
       }
-      tw[vv] = w;
-      tp[vv] = pt;
     }
+    tw[tid] = w;
+    tp[tid] = pt;
   }
   __syncthreads();
   ArgMax ew{-INFINITY, INT_MAX}, ep{-INFINITY, INT_MAX};
