@@ -203,9 +203,11 @@ def run_ours(args, rank: int, world: int):
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index) as clk:
+        t_host = time.perf_counter()
         for it in range(args.steps):
             flush.fill_(it & 0xFF)  # L2 flush, outside the timed segments
             step(it, True, evs[it])
+        t_host = time.perf_counter() - t_host  # host time to enqueue (the device may still run)
         torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
@@ -282,6 +284,7 @@ def run_ours(args, rank: int, world: int):
                    "timed": "draft+confidence+schedule+pack and verify segments; target forward excluded",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_step": tokens / args.steps / world,
+        "host_enqueue_ms_per_step": t_host * 1e3 / args.steps,
         "stage_ms": {"draft": draft_ms, "conf_sched_pack": float((seg[:, 0] - seg[:, 2]).mean()),
                      "verify": float(seg[:, 1].mean())},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",

@@ -212,8 +212,8 @@ DSPARK_API int dspark_verify(const void* target, int dtype, const int32_t* cu_se
  * cudaMalloc would bypass that framework's allocator and its accounting), or a service that
  * fixes its device footprint at start-up and forbids later allocation.  Same computation,
  * arguments and limits as dspark_draft_block, without ws / ws_bytes; it allocates nothing.
- *   Scratch: a fixed 4 MiB array inside the library (every GPU that loads the library holds it
- *   until exit).  Sizes whose scratch (256 B + bs * ceil(V / 128) * 8 B) exceeds it are rejected
+ *   Scratch: a fixed 8 MiB array inside the library (every GPU that loads the library holds it
+ *   until exit).  Sizes whose scratch (256 B + bs * ceil(V / 128) * 16 B) exceeds it are rejected
  *   with DSPARK_EUNSUPPORTED -- e.g. bs = 256 allows V up to about 262,000.
  *   The first call on a device looks up the array's device address (once per device, with that
  *   device current); make that first call before any stream capture.

@@ -11,6 +11,9 @@
 namespace dspark {
 
 constexpr int kChunk = DSPARK_CHUNK;
+// Statistics are kept per half chunk (64 ids): entry 2c + h covers ids [128c + 64h, 128c + 64h + 64).
+// Passes that reduce a whole chunk at once write entry 2c and a neutral entry 2c + 1.
+constexpr int kStatsPerChunk = 2;
 
 // Philox purposes (counter word 3, bits 24..31).
 enum Purpose : uint32_t {
@@ -27,7 +30,7 @@ enum DecisionKind : int { kDecNone = 0, kDecResidual = 1, kDecBonus = 2 };
 // ----------------------------------------------------------------------------------------
 // Workspace layout (all offsets 256-byte aligned)
 //   status   : uint32 status word (first device-detected error wins)
-//   stats    : float2 [bs][n_chunks]       per-(row, chunk) partial statistics
+//   stats    : float2 [bs][2 * n_chunks]   per-(row, half chunk) partial statistics
 //   rowstats : RowStat [bs * (gamma + 1)]  per packed target row
 //   dec      : Decision [bs]               per-request verify decision
 // ----------------------------------------------------------------------------------------
@@ -47,6 +50,10 @@ struct Decision {
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+__host__ __device__ inline size_t stats_bytes(int bs, int n_chunks) {
+  return size_t(bs) * n_chunks * kStatsPerChunk * sizeof(float2);
+}
+
 struct WsLayout {
   size_t status = 0, stats = 0, rowstats = 0, dec = 0, total = 0;
   int n_chunks = 0;
@@ -59,7 +66,7 @@ __host__ __device__ inline WsLayout ws_layout(int bs, int gamma, int V) {
   L.status = off;
   off += 256;
   L.stats = off;
-  off += align256(size_t(bs) * L.n_chunks * sizeof(float2));
+  off += align256(stats_bytes(bs, L.n_chunks));
   L.rowstats = off;
   off += align256(size_t(bs) * (gamma + 1) * sizeof(RowStat));
   L.dec = off;

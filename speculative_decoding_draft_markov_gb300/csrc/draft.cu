@@ -64,12 +64,18 @@ __global__ void __launch_bounds__(128) draft_stats_simt_kernel(
     const float l = valid ? acc[rr] + ld_f32(U, (size_t(row) * gamma + (k - 1)) * V + v) : 0.f;
     if (greedy) {
       const ArgMax am = block_argmax<kChunk>(ArgMax{valid ? l : -INFINITY, valid ? v : INT_MAX}, red, redi);
-      if (tid == 0) stats[size_t(row) * n_chunks + c] = make_float2(am.v, __int_as_float(am.i));
+      if (tid == 0) {
+        stats[(size_t(row) * n_chunks + c) * kStatsPerChunk] = make_float2(am.v, __int_as_float(am.i));
+        stats[(size_t(row) * n_chunks + c) * kStatsPerChunk + 1] = make_float2(-INFINITY, __int_as_float(INT_MAX));
+      }
     } else {
       const float t = valid ? l * inv_tau : -INFINITY;
       const float m = block_max<kChunk>(t, red);
       const float s = block_sum<kChunk>(valid ? expf(t - m) : 0.f, red);
-      if (tid == 0) stats[size_t(row) * n_chunks + c] = make_float2(m, s);
+      if (tid == 0) {
+        stats[(size_t(row) * n_chunks + c) * kStatsPerChunk] = make_float2(m, s);
+        stats[(size_t(row) * n_chunks + c) * kStatsPerChunk + 1] = make_float2(-INFINITY, 0.f);
+      }
     }
   }
 }
@@ -92,12 +98,12 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
   __shared__ float rv[8], rs[8];
   __shared__ int ri[8];
   const int b = blockIdx.x, tid = threadIdx.x;
-  const float2* st = stats + size_t(b) * n_chunks;
+  const float2* st = stats + size_t(b) * n_chunks * kStatsPerChunk;
   const size_t out = size_t(b) * gamma + (k - 1);
 
   if (greedy) {
     ArgMax best{-INFINITY, INT_MAX};
-    for (int c = tid; c < n_chunks; c += 256) {
+    for (int c = tid; c < n_chunks * kStatsPerChunk; c += 256) {
       const float2 s2 = st[c];
       best = better(best, ArgMax{s2.x, __float_as_int(s2.y)});
     }
@@ -119,9 +125,10 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
     for (int l = 0; l < 4; ++l) {
       const int c = 4 * g + l;
       if (c >= n_chunks) break;
-      const float2 s2 = st[c];
-      lp = lse_merge(lp, LsePair{s2.x, s2.y});
-      if (s2.y > 0.f) best = better(best, ArgMax{s2.x + logf(s2.y) + gumbel_from_bits(pick_word(w, l)), c});
+      const float2 h0 = st[2 * c], h1 = st[2 * c + 1];
+      const LsePair cl = lse_merge(LsePair{h0.x, h0.y}, LsePair{h1.x, h1.y});  // the chunk's (max, sum-exp)
+      lp = lse_merge(lp, cl);
+      if (cl.s > 0.f) best = better(best, ArgMax{cl.m + logf(cl.s) + gumbel_from_bits(pick_word(w, l)), c});
     }
   }
   lp = block_lse<256>(lp, rv, rs);

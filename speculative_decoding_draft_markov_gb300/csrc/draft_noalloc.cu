@@ -30,7 +30,7 @@ using namespace dspark;
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -72,9 +72,9 @@ extern "C" DSPARK_API int dspark_draft_block_noalloc(
       !aligned(tokens, 4) || !aligned(logit_x, 4) || !aligned(lse, 4) || !aligned(device_status, 4))
     return DSPARK_EINVAL;
 
-  // the scratch this call needs: status word + bs x ceil(V / 128) chunk statistics
+  // the scratch this call needs: status word + bs x ceil(V / 128) x 2 half-chunk statistics
   const WsLayout L = ws_layout(bs, gamma, V);
-  const size_t need = L.stats + size_t(bs) * L.n_chunks * sizeof(float2);
+  const size_t need = L.stats + stats_bytes(bs, L.n_chunks);
   if (need > kNoAllocScratchBytes) return DSPARK_EUNSUPPORTED;
 
   void* scratch = nullptr;

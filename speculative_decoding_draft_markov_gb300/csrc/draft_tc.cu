@@ -21,7 +21,7 @@
 //   warps 2-5 = epilogue: tcgen05.ld of the 128 x 128 fp32 accumulator (one row per thread)
 //   warp 6    = (DECIDE) cp.async gather of each request's U row and target row
 //   2 TMEM accumulators (256 columns) let MMA, loads and epilogue overlap.
-// Every mbarrier wait is bounded (globaltimer deadline + shared abort flag); on give-up the
+// Every mbarrier wait is bounded (SM cycle-counter deadline + shared abort flag); on give-up the
 // kernel records DSPARK_ETIMEOUT, waits (bounded) for its own copies / MMAs in flight,
 // frees TMEM and returns.
 #include <cuda.h>
@@ -49,12 +49,13 @@ constexpr uint32_t kUHalf = kBM * 64 * 2;        // 16 KB: one 64-column half of
 constexpr uint32_t kTmemCols = kAccBufs * kBN;   // 256
 constexpr float kLog2e = 1.4426950408889634f;
 
-// DRAFT: W2t ring of 6 K-stages, 8 epilogue warps (two per TMEM lane quarter, 64 columns
-// each).  DECIDE: 4 K-stages, 4 epilogue warps and one gather warp.
+// 8 epilogue warps: two per TMEM lane quarter, each reducing 64 of a row's 128 columns into
+// its own half-chunk statistics entry (no cross-warp exchange).  DRAFT: W2t ring of 6
+// K-stages.  DECIDE: 4 K-stages and one extra warp gathering the U and target rows.
 template <bool kDecide>
 __host__ __device__ constexpr int b_stages() { return kDecide ? 4 : 6; }
 template <bool kDecide>
-__host__ __device__ constexpr int epi_warps() { return kDecide ? 4 : 8; }
+__host__ __device__ constexpr int epi_warps() { return 8; }
 template <bool kDecide>
 __host__ __device__ constexpr int threads() { return 32 * (2 + epi_warps<kDecide>() + (kDecide ? 1 : 0)); }
 
@@ -65,6 +66,7 @@ struct Barriers {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int xrow[kBM];  // W1 row of each A row (-1: zero row)
 };
 
 // Per-row facts of the DECIDE pass (one request per tile row).
@@ -96,17 +98,20 @@ struct Params {
   const Decision* dec;
 };
 
-// Dynamic shared memory: A atoms | W2t ring | U stages | DECIDE row facts or DRAFT half-row
-// exchange | barriers.  The buffer is declared 1024-byte aligned (128-byte swizzle atoms).
+// Dynamic shared memory: A atoms | W2t ring | U stages | DECIDE row facts | barriers.  The
+// buffer is declared 1024-byte aligned (128-byte swizzle atoms).
 template <bool kDecide>
 __host__ __device__ constexpr size_t extra_bytes() {
-  return kDecide ? kBM * sizeof(RowMeta) : 2 * kBM * sizeof(float2);
+  return kDecide ? kBM * sizeof(RowMeta) : 0;
 }
 template <bool kDecide>
 __host__ __device__ constexpr size_t smem_bytes(int r) {
   return size_t(r / kBK) * kAtomBytes + b_stages<kDecide>() * kAtomBytes + kUStages * 2 * kUHalf +
          extra_bytes<kDecide>() + sizeof(Barriers);
 }
+
+static_assert(smem_bytes<false>(256) <= 232448 && smem_bytes<true>(256) <= 232448,
+              "dynamic shared memory beyond the 227 KB per-block limit");
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
@@ -136,9 +141,8 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
   uint8_t* sA = smem;                                   // nk atoms
   uint8_t* sB = sA + nk * kAtomBytes;                   // kBStages atoms
   uint8_t* sU = sB + kBStages * kAtomBytes;             // kUStages x 32 KB
-  uint8_t* sX = sU + kUStages * 2 * kUHalf;             // row facts (DECIDE) / half-row exchange (DRAFT)
+  uint8_t* sX = sU + kUStages * 2 * kUHalf;             // row facts (DECIDE)
   RowMeta* meta = reinterpret_cast<RowMeta*>(sX);
-  float2* xchg = reinterpret_cast<float2*>(sX);         // [2 tile parities][128 rows]
   Barriers* bar = reinterpret_cast<Barriers*>(sX + extra_bytes<kDecide>());
   volatile int* abort_flag = &bar->abort;
 
@@ -195,35 +199,40 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
   }
   // A operand: rows m0..m0+127 of W1[x] in the 128-byte-swizzled K-major layout, where x is
   // x_{k-1} (DRAFT) or the token before each residual row's rejected position (DECIDE).
+  // Token ids first, then every 16-byte row chunk as an independent cp.async.
+  for (int m = tid; m < kBM; m += threads<kDecide>()) {
+    const int grow = m0 + m;
+    int xp = -1;
+    if (grow < bs) {
+      int kx = p.k;  // position whose previous token selects the W1 row
+      bool use = true;
+      if (kDecide) {
+        const Decision d = p.dec[grow];
+        use = d.kind == kDecResidual;
+        kx = d.kdec;
+      }
+      if (use) xp = clamp_token((kx == 1) ? p.anchor[grow] : p.tokens[size_t(grow) * p.gamma + kx - 2], V);
+    }
+    bar->xrow[m] = xp;
+  }
+  __syncthreads();
   {
     const int cpr = r / 8;  // 16-byte chunks per row
     for (int idx = tid; idx < kBM * cpr; idx += threads<kDecide>()) {
       const int row = idx / cpr, ch = idx % cpr;
-      const int grow = m0 + row;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (grow < bs) {
-        int kx = p.k;  // position whose previous token selects the W1 row
-        bool use = true;
-        if (kDecide) {
-          const Decision d = p.dec[grow];
-          use = d.kind == kDecResidual;
-          kx = d.kdec;
-        }
-        if (use) {
-          const int xp = clamp_token((kx == 1) ? p.anchor[grow] : p.tokens[size_t(grow) * p.gamma + kx - 2], V);
-          v = *reinterpret_cast<const uint4*>(p.W1 + size_t(xp) * r + ch * 8);
-        }
-      }
+      const int xp = bar->xrow[row];
       const int kb = ch >> 3, j = ch & 7;
-      *reinterpret_cast<uint4*>(sA + kb * kAtomBytes + row * 128 + ((j ^ (row & 7)) << 4)) = v;
+      const uint32_t dst = tc::smem_u32(sA + kb * kAtomBytes + row * 128 + ((j ^ (row & 7)) << 4));
+      cp_async16(dst, xp >= 0 ? p.W1 + size_t(xp) * r + ch * 8 : p.W1, xp >= 0 ? 16u : 0u);
     }
+    cp_async_wait_all();
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem_base = bar->tmem_base;
-  const uint64_t deadline = tc::globaltimer_ns() + p.timeout_ns;
+  const long long deadline = tc::deadline_after_ns(p.timeout_ns);
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -265,7 +274,7 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
         *abort_flag = 1;
         set_status(p.status, DSPARK_ETIMEOUT);
         // wait (bounded) for every copy this thread put in flight before the CTA exits
-        const uint64_t dl = tc::globaltimer_ns() + 200000000ull;
+        const long long dl = tc::deadline_after_ns(200000000ull);
         const volatile int never = 0;
         for (int s = 0; s < kBStages; ++s)
           if (b_issued[s] >= 0) tc::mbar_wait_bounded(tc::smem_u32(&bar->b_full[s]), b_issued[s], dl, &never);
@@ -312,7 +321,7 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
         if (issued) {  // wait (bounded) for the MMAs already issued before TMEM is freed
           tc::mma_commit(tc::smem_u32(&bar->drain));
           const volatile int never = 0;
-          tc::mbar_wait_bounded(tc::smem_u32(&bar->drain), 0, tc::globaltimer_ns() + 200000000ull, &never);
+          tc::mbar_wait_bounded(tc::smem_u32(&bar->drain), 0, tc::deadline_after_ns(200000000ull), &never);
         }
       }
     }
@@ -363,10 +372,9 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
       const int valid = min(kBN, V - n0);
       bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[ab]), aph, deadline, abort_flag) &&
                 tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[us]), uph, deadline, abort_flag);
-      // one decision for every epilogue thread before any .sync.aligned TMEM load or named
-      // barrier, so that no thread can be left waiting on one that gave up
+      // one decision per warp before the .sync.aligned TMEM loads; warps run independently
+      // (no named barrier in this loop), so a warp that gives up can hold up no other
       ok = __all_sync(0xFFFFFFFFu, ok);
-      ok = tc::named_barrier_and(2, kEpiThreads, ok);
       if (!ok) {
         *abort_flag = 1;
         set_status(p.status, DSPARK_ETIMEOUT);
@@ -374,7 +382,7 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
       }
       tc::tc_fence_after();
       const uint32_t taddr = tmem_base + (uint32_t(wq * 32) << 16) + ab * kBN;
-      float2 out;
+      float2 part;
       if (!kDecide) {
         constexpr int kH = kBN / 2;  // columns per thread
         float v[kH];
@@ -396,7 +404,6 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
         tc::mbar_arrive(tc::smem_u32(&bar->u_empty[us]));
 
         const int vh = valid - half * kH;  // valid columns of this half (may be <= 0)
-        float2 part;
         if (p.greedy) {
           float best = -INFINITY;
           int bi = INT_MAX;
@@ -416,48 +423,33 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
             if (i < vh) s4[i & 3] += exp2f((v[i] - mx) * c2);
           part = make_float2(mx * inv_tau, (s4[0] + s4[1]) + (s4[2] + s4[3]));
         }
-        // combine the two halves of the row: half 1 hands its partial to half 0
-        float2* slot = xchg + (t & 1) * kBM + m;
-        if (half == 1) *slot = part;
-        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-        if (half == 0) {
-          const float2 o = *slot;
-          if (p.greedy) {
-            out = (o.x > part.x) ? o : part;  // ties keep the lower ids (half 0)
-          } else if (o.y == 0.f) {
-            out = part;
-          } else if (part.y == 0.f) {
-            out = o;
-          } else {
-            const float mm = fmaxf(part.x, o.x);
-            out = make_float2(mm, part.y * __expf(part.x - mm) + o.y * __expf(o.x - mm));
-          }
-        }
       } else {
-        // residual / bonus masses, 32 columns at a time
+        // residual / bonus masses of this half row, 32 columns at a time
+        constexpr int kH = kBN / 2;
         const RowMeta rm = meta[m];
-        const uint8_t* ub = sU + m * 128;
-        const uint8_t* tb = sU + 2 * kUHalf + m * 128;
+        const uint8_t* ub = sU + half * kUHalf + m * 128;
+        const uint8_t* tb = sU + 2 * kUHalf + half * kUHalf + m * 128;
+        const int vh = valid - half * kH;
         float R = 0.f, P = 0.f;
 #pragma unroll
-        for (int q = 0; q < kBN / 32; ++q) {
+        for (int q = 0; q < kH / 32; ++q) {
           float v[32];
-          tc::tmem_ld32(taddr + q * 32, reinterpret_cast<uint32_t*>(v));
+          tc::tmem_ld32(taddr + half * kH + q * 32, reinterpret_cast<uint32_t*>(v));
           tc::tmem_ld_wait();
 #pragma unroll
           for (int j4 = 0; j4 < 4; ++j4) {
-            const int j16 = q * 4 + j4;
-            const uint32_t off = (j16 >> 3) * kUHalf + (((j16 & 7) ^ (m & 7)) << 4);
+            const int j = q * 4 + j4;  // 16-byte chunk within the half row
+            const uint32_t off = ((j ^ (m & 7)) << 4);
             float xu[8], xt[8];
             unpack8(*reinterpret_cast<const uint4*>(ub + off), xu);
             unpack8(*reinterpret_cast<const uint4*>(tb + off), xt);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              const int i = 8 * j16 + e;
+              const int i = 8 * j + e;
               const float pt = exp2f(fmaf(xt[e], c2, -rm.a_t));
               const float pd = exp2f(fmaf(v[8 * j4 + e] + xu[e], c2, -rm.a_d));
               const float w = rm.resid ? fmaxf(0.f, pt - pd) : pt;
-              if (i < valid && rm.live) {
+              if (i < vh && rm.live) {
                 R += w;
                 P += pt;
               }
@@ -467,7 +459,7 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
         tc::tc_fence_before();
         tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[ab]));
         tc::mbar_arrive(tc::smem_u32(&bar->u_empty[0]));
-        out = make_float2(R, P);
+        part = make_float2(R, P);
       }
       if (++ab == kAccBufs) { ab = 0; aph ^= 1; }
       if (!kDecide) {
@@ -475,7 +467,7 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
       } else {
         uph ^= 1;  // one stage (index 0) in DECIDE
       }
-      if (grow < bs && (kDecide || half == 0)) p.stats[size_t(grow) * p.n_chunks + c] = out;
+      if (grow < bs) p.stats[(size_t(grow) * p.n_chunks + c) * kStatsPerChunk + half] = part;
     }
   }
 
@@ -502,11 +494,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-int sm_count() {
-  int dev = 0, n = 0;
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int dev = 0;
   cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
+  return dev;
+}
+
+// Multiprocessor count of the current device (queried once per device).
+int sm_count() {
+  static int cache[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
 }
 
 bool encode_w2(CUtensorMap* map, const void* W2t, int V, int r) {
@@ -522,10 +528,20 @@ bool encode_w2(CUtensorMap* map, const void* W2t, int V, int r) {
 template <bool kDecide>
 cudaError_t launch(const CUtensorMap& w2, const CUtensorMap& u, const Params& prm, cudaStream_t s) {
   const size_t smem = smem_bytes<kDecide>(prm.r);
-  const cudaError_t attr = cudaFuncSetAttribute(stats_tc_kernel<kDecide>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                int(smem_bytes<kDecide>(256)));
-  if (attr != cudaSuccess) return attr;
+  static bool attr_set[kMaxDevices] = {};  // the shared-memory opt-in, once per device
+  static std::mutex attr_mutex;
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(attr_mutex);
+    if (!attr_set[dev]) {
+      const cudaError_t attr = cudaFuncSetAttribute(stats_tc_kernel<kDecide>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    int(smem_bytes<kDecide>(256)));
+      if (attr != cudaSuccess) return attr;
+      attr_set[dev] = true;
+    }
+  }
   const int n_mt = (prm.bs + kBM - 1) / kBM;
   int grid = (sm_count() / n_mt) * n_mt;
   grid = min(grid, n_mt * prm.n_chunks);

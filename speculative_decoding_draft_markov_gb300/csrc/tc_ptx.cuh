@@ -14,12 +14,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 // ---------------------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -43,29 +37,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar`, giving up when *abort becomes non-zero or when the
-// deadline (globaltimer, ns) passes.  Returns false on give-up; the caller records it.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t deadline,
+// Wait for phase `parity` of `bar`, giving up when *abort becomes non-zero or when the SM
+// cycle counter passes `deadline` (clock64 cycles; read locally, unlike %globaltimer).
+// Returns false on give-up; the caller records it.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long deadline,
                                                   const volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() > deadline) return false;
+    if (clock64() > deadline) return false;
   }
 }
 
-// AND of `v` over the `count` threads (a multiple of 32) that use named barrier `id`; every
-// participating thread gets the same result.
-__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
-      " selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"(uint32_t(v)), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
+// Cycle budget for a wall-clock timeout: 2 cycles per ns (the SM clock is at most ~2.1 GHz, so
+// the wait gives up after at least the requested time).
+__device__ __forceinline__ long long deadline_after_ns(uint64_t ns) {
+  const uint64_t cyc = ns > (uint64_t(1) << 61) ? (uint64_t(1) << 62) : 2 * ns;
+  return clock64() + static_cast<long long>(cyc);
 }
 
 // ---------------------------------------------------------------------------------- TMA

@@ -252,7 +252,10 @@ __global__ void __launch_bounds__(128) decision_stats_simt_kernel(
     }
     const float R = block_sum<kChunk>(w, red);
     const float P = block_sum<kChunk>(pt, red);
-    if (tid == 0) stats[size_t(row) * n_chunks + c] = make_float2(R, P);
+    if (tid == 0) {
+      stats[(size_t(row) * n_chunks + c) * kStatsPerChunk] = make_float2(R, P);
+      stats[(size_t(row) * n_chunks + c) * kStatsPerChunk + 1] = make_float2(0.f, 0.f);
+    }
   }
 }
 
@@ -273,9 +276,9 @@ __global__ void __launch_bounds__(256) decision_select_kernel(
   const int b = blockIdx.x, tid = threadIdx.x;
   const Decision d = dec[b];
   if (d.kind == kDecNone) return;
-  const float2* st = stats + size_t(b) * n_chunks;
+  const float2* st = stats + size_t(b) * n_chunks * kStatsPerChunk;
   float Rl = 0.f;
-  for (int c = tid; c < n_chunks; c += 256) Rl += st[c].x;
+  for (int c = tid; c < n_chunks; c += 256) Rl += st[2 * c].x + st[2 * c + 1].x;
   const bool use_res = block_sum<256>(Rl, rv) > 0.f;
   ArgMax best{-INFINITY, INT_MAX};
   const int n_grp = (n_chunks + 3) / 4;
@@ -285,7 +288,7 @@ __global__ void __launch_bounds__(256) decision_select_kernel(
     for (int l = 0; l < 4; ++l) {
       const int c = 4 * g + l;
       if (c >= n_chunks) break;
-      const float mass = use_res ? st[c].x : st[c].y;
+      const float mass = use_res ? st[2 * c].x + st[2 * c + 1].x : st[2 * c].y + st[2 * c + 1].y;
       if (mass > 0.f) best = better(best, ArgMax{logf(mass) + gumbel_from_bits(pick_word(w, l)), c});
     }
   }
