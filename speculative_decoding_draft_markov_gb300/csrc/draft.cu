@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
     int gamma, int V, int r, int k, float inv_tau, int greedy, uint64_t seed, uint64_t step) {
   __shared__ float sA[256];
   __shared__ float tv[kChunk];
-  __shared__ float rv[8], rs[8];
+  __shared__ float rv[8], rs[8], ru[8];
   __shared__ int ri[8];
   const int b = blockIdx.x, tid = threadIdx.x;
   const float2* st = stats + size_t(b) * n_chunks * kStatsPerChunk;
@@ -116,6 +116,10 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
     return;
   }
 
+  // the W1 row of x_{k-1} does not depend on the chunk choice: fetch it first
+  const int xp = clamp_token((k == 1) ? anchor[b] : tokens[size_t(b) * gamma + k - 2], V);
+  for (int i = tid; i < r; i += 256) sA[i] = ld_f32(W1, size_t(xp) * r + i);
+
   LsePair lp{-INFINITY, 0.f};
   ArgMax best{-INFINITY, INT_MAX};
   const int n_grp = (n_chunks + 3) / 4;
@@ -131,19 +135,29 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
       if (cl.s > 0.f) best = better(best, ArgMax{cl.m + logf(cl.s) + gumbel_from_bits(pick_word(w, l)), c});
     }
   }
-  lp = block_lse<256>(lp, rv, rs);
-  best = block_argmax<256>(best, rv, ri);
+  // one combined block reduction of (row LSE, best chunk)
+  lp = warp_lse(lp);
+  best = warp_argmax(best);
+  {
+    const int w = tid >> 5, l = tid & 31;
+    if (l == 0) { rv[w] = lp.m; rs[w] = lp.s; ru[w] = best.v; ri[w] = best.i; }
+    __syncthreads();
+    lp = LsePair{rv[0], rs[0]};
+    best = ArgMax{ru[0], ri[0]};
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+      lp = lse_merge(lp, LsePair{rv[i], rs[i]});
+      best = better(best, ArgMax{ru[i], ri[i]});
+    }
+  }
   const int cstar = (best.i == INT_MAX) ? 0 : best.i;  // only non-finite statistics leave it unset
-
-  const int xp = clamp_token((k == 1) ? anchor[b] : tokens[size_t(b) * gamma + k - 2], V);
-  for (int i = tid; i < r; i += 256) sA[i] = ld_f32(W1, size_t(xp) * r + i);
-  __syncthreads();
+  // the U values of the chosen chunk load together with its W2t rows
+  float u_v = 0.f;
+  const int v_own = cstar * kChunk + tid;
+  if (tid < kChunk && v_own < V) u_v = ld_f32(U, (size_t(b) * gamma + (k - 1)) * V + v_own);
   chunk_dots<T>(W2t, r, V, cstar * kChunk, sA, tv);
   __syncthreads();
-  if (tid < kChunk) {
-    const int v = cstar * kChunk + tid;
-    tv[tid] = (v < V) ? (tv[tid] + ld_f32(U, (size_t(b) * gamma + (k - 1)) * V + v)) * inv_tau : -INFINITY;
-  }
+  if (tid < kChunk) tv[tid] = (v_own < V) ? (tv[tid] + u_v) * inv_tau : -INFINITY;
   __syncthreads();
   ArgMax e{-INFINITY, INT_MAX};
   if (tid < kChunk) {

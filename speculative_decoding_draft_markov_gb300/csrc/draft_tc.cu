@@ -161,11 +161,11 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
     }
     for (int s = 0; s < kUStages; ++s) {
       tc::mbar_init(tc::smem_u32(&bar->u_full[s]), kDecide ? 32 : 1);  // DECIDE: one arrive per loader lane
-      tc::mbar_init(tc::smem_u32(&bar->u_empty[s]), kEpiThreads);
+      tc::mbar_init(tc::smem_u32(&bar->u_empty[s]), kEpiThreads / 32);  // one arrival per epilogue warp
     }
     for (int s = 0; s < kAccBufs; ++s) {
       tc::mbar_init(tc::smem_u32(&bar->acc_full[s]), 1);
-      tc::mbar_init(tc::smem_u32(&bar->acc_empty[s]), kEpiThreads);
+      tc::mbar_init(tc::smem_u32(&bar->acc_empty[s]), kEpiThreads / 32);
     }
     tc::mbar_init(tc::smem_u32(&bar->drain), 1);
     bar->abort = 0;
@@ -391,7 +391,8 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
           tc::tmem_ld32(taddr + half * kH + q * 32, reinterpret_cast<uint32_t*>(v + q * 32));
         tc::tmem_ld_wait();
         tc::tc_fence_before();
-        tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[ab]));
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[ab]));
 
         const uint8_t* ub = sU + us * 2 * kUHalf + half * kUHalf + m * 128;
 #pragma unroll
@@ -401,7 +402,8 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
 #pragma unroll
           for (int e = 0; e < 8; ++e) v[8 * j + e] += x[e];
         }
-        tc::mbar_arrive(tc::smem_u32(&bar->u_empty[us]));
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->u_empty[us]));
 
         const int vh = valid - half * kH;  // valid columns of this half (may be <= 0)
         if (p.greedy) {
@@ -457,8 +459,11 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
           }
         }
         tc::tc_fence_before();
-        tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[ab]));
-        tc::mbar_arrive(tc::smem_u32(&bar->u_empty[0]));
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[ab]));
+          tc::mbar_arrive(tc::smem_u32(&bar->u_empty[0]));
+        }
         part = make_float2(R, P);
       }
       if (++ab == kAccBufs) { ab = 0; aph ^= 1; }
