@@ -19,7 +19,8 @@
 //               position) and, in DRAFT, the U tile (3-D map over [bs, gamma, V], evict-first)
 //   warp 1    = TMEM owner + single-thread tcgen05.mma issuer, commits to mbarriers
 //   warps 2-5 = epilogue: tcgen05.ld of the 128 x 128 fp32 accumulator (one row per thread)
-//   warp 6    = (DECIDE) cp.async gather of each request's U row and target row
+//   warps 10-11 = (DECIDE) cp.async gather of each request's U row and target row, one warp
+//               per 64-column half, so one half refills while the other is being reduced
 //   2 TMEM accumulators (256 columns) let MMA, loads and epilogue overlap.
 // Every mbarrier wait is bounded (SM cycle-counter deadline + shared abort flag); on give-up the
 // kernel records DSPARK_ETIMEOUT, waits (bounded) for its own copies / MMAs in flight,
@@ -51,13 +52,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // 8 epilogue warps: two per TMEM lane quarter, each reducing 64 of a row's 128 columns into
 // its own half-chunk statistics entry (no cross-warp exchange).  DRAFT: W2t ring of 6
-// K-stages.  DECIDE: 4 K-stages and one extra warp gathering the U and target rows.
+// K-stages.  DECIDE: 4 K-stages and two gather warps, one per 64-column half of the U and
+// target rows, each half with its own full / empty barrier pair.
 template <bool kDecide>
 __host__ __device__ constexpr int b_stages() { return kDecide ? 4 : 6; }
 template <bool kDecide>
 __host__ __device__ constexpr int epi_warps() { return 8; }
 template <bool kDecide>
-__host__ __device__ constexpr int threads() { return 32 * (2 + epi_warps<kDecide>() + (kDecide ? 1 : 0)); }
+__host__ __device__ constexpr int threads() { return 32 * (2 + epi_warps<kDecide>() + (kDecide ? 2 : 0)); }
 
 struct Barriers {
   uint64_t b_full[kBStagesMax], b_empty[kBStagesMax];
@@ -161,7 +163,8 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
     }
     for (int s = 0; s < kUStages; ++s) {
       tc::mbar_init(tc::smem_u32(&bar->u_full[s]), kDecide ? 32 : 1);  // DECIDE: one arrive per loader lane
-      tc::mbar_init(tc::smem_u32(&bar->u_empty[s]), kEpiThreads / 32);  // one arrival per epilogue warp
+      // one arrival per epilogue warp (DECIDE: per warp of the half the stage holds)
+      tc::mbar_init(tc::smem_u32(&bar->u_empty[s]), kDecide ? kEpiThreads / 64 : kEpiThreads / 32);
     }
     for (int s = 0; s < kAccBufs; ++s) {
       tc::mbar_init(tc::smem_u32(&bar->acc_full[s]), 1);
@@ -325,31 +328,33 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
         }
       }
     }
-  } else if (kDecide && warp == 2 + epi_warps<kDecide>()) {
+  } else if (kDecide && warp >= 2 + epi_warps<kDecide>()) {
     // ------------------------------------------------------------------ row gather (DECIDE)
-    // U stage 0 holds the U rows, U stage 1 the target rows of the current tile.
+    // Gather warp h fills column half h of the U rows (first 32 KB) and target rows (second
+    // 32 KB); barrier pair h (u_full / u_empty) guards that half.
+    const int h = warp - (2 + epi_warps<kDecide>());
     int ph = 0;
     bool ok = true;
-    const int sub = lane >> 4, c16 = lane & 15, h = c16 >> 3, j = c16 & 7;
-    const uint32_t su = tc::smem_u32(sU), st = tc::smem_u32(sU + 2 * kUHalf);
+    const int j = lane & 7, rsub = lane >> 3;  // 16-byte chunk in the half row, row within a group of 4
+    const uint32_t su = tc::smem_u32(sU + h * kUHalf), st = tc::smem_u32(sU + 2 * kUHalf + h * kUHalf);
     for (int t = 0; t < n_tiles; ++t) {
       const int n0 = (c0 + t * cstride) * kBN;
-      if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->u_empty[0]), ph ^ 1, deadline, abort_flag)) {
+      if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->u_empty[h]), ph ^ 1, deadline, abort_flag)) {
         ok = false;
         break;
       }
-      const int col = n0 + c16 * 8;
+      const int col = n0 + h * 64 + j * 8;
       const bool in_v = col < V;
 #pragma unroll 4
-      for (int it = 0; it < kBM / 2; ++it) {
-        const int row = it * 2 + sub;
+      for (int it = 0; it < kBM / 4; ++it) {
+        const int row = it * 4 + rsub;
         const RowMeta rm = meta[row];
-        const uint32_t off = h * kUHalf + row * 128 + ((j ^ (row & 7)) << 4);
+        const uint32_t off = row * 128 + ((j ^ (row & 7)) << 4);
         const bool gu = rm.resid && in_v, gt = rm.live && in_v;
         cp_async16(su + off, gu ? p.U + rm.u_off + col : p.U, gu ? 16u : 0u);
         cp_async16(st + off, gt ? p.target + rm.t_off + col : p.target, gt ? 16u : 0u);
       }
-      cp_async_arrive_noinc(tc::smem_u32(&bar->u_full[0]));
+      cp_async_arrive_noinc(tc::smem_u32(&bar->u_full[h]));
       ph ^= 1;
     }
     if (!ok) {
@@ -370,8 +375,9 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
       const int c = c0 + t * cstride;
       const int n0 = c * kBN;
       const int valid = min(kBN, V - n0);
+      const int ustage = kDecide ? half : us;  // DECIDE: the stage of this warp's column half
       bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[ab]), aph, deadline, abort_flag) &&
-                tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[us]), uph, deadline, abort_flag);
+                tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[ustage]), uph, deadline, abort_flag);
       // one decision per warp before the .sync.aligned TMEM loads; warps run independently
       // (no named barrier in this loop), so a warp that gives up can hold up no other
       ok = __all_sync(0xFFFFFFFFu, ok);
@@ -429,8 +435,8 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
         // residual / bonus masses of this half row, 32 columns at a time
         constexpr int kH = kBN / 2;
         const RowMeta rm = meta[m];
-        const uint8_t* ub = sU + half * kUHalf + m * 128;
-        const uint8_t* tb = sU + 2 * kUHalf + half * kUHalf + m * 128;
+        const uint8_t* ub = sU + half * kUHalf + m * 128;              // U rows, this half
+        const uint8_t* tb = sU + 2 * kUHalf + half * kUHalf + m * 128; // target rows, this half
         const int vh = valid - half * kH;
         float R = 0.f, P = 0.f;
 #pragma unroll
@@ -462,7 +468,7 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
         __syncwarp();
         if (lane == 0) {
           tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[ab]));
-          tc::mbar_arrive(tc::smem_u32(&bar->u_empty[0]));
+          tc::mbar_arrive(tc::smem_u32(&bar->u_empty[half]));
         }
         part = make_float2(R, P);
       }
@@ -470,7 +476,7 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
       if (!kDecide) {
         if (++us == kUStages) { us = 0; uph ^= 1; }
       } else {
-        uph ^= 1;  // one stage (index 0) in DECIDE
+        uph ^= 1;  // DECIDE: each half's stage is refilled every tile
       }
       if (grow < bs) p.stats[(size_t(grow) * p.n_chunks + c) * kStatsPerChunk + half] = part;
     }
