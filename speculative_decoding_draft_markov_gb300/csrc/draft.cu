@@ -99,6 +99,10 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
   __shared__ int ri[8];
   const int b = blockIdx.x, tid = threadIdx.x;
   const float2* st = stats + size_t(b) * n_chunks * kStatsPerChunk;
+  // launched as a programmatic dependent of the statistics pass: wait for it to complete, then
+  // let the next position's statistics kernel start its set-up
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const size_t out = size_t(b) * gamma + (k - 1);
 
   if (greedy) {
@@ -200,11 +204,20 @@ cudaError_t launch_draft_select(int dtype, const void* stats, int n_chunks, cons
     draft_select_kernel<float><<<bs, 256, 0, s>>>(
         (const float2*)stats, n_chunks, (const float*)U, (const float*)W1, (const float*)W2t,
         anchor, tokens, logit_x, lse, bs, gamma, V, r, k, inv_tau, greedy, seed, step);
-  else
-    draft_select_kernel<__nv_bfloat16><<<bs, 256, 0, s>>>(
-        (const float2*)stats, n_chunks, (const __nv_bfloat16*)U, (const __nv_bfloat16*)W1,
-        (const __nv_bfloat16*)W2t, anchor, tokens, logit_x, lse, bs, gamma, V, r, k, inv_tau,
-        greedy, seed, step);
+  else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(bs);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, draft_select_kernel<__nv_bfloat16>, (const float2*)stats, n_chunks,
+                              (const __nv_bfloat16*)U, (const __nv_bfloat16*)W1, (const __nv_bfloat16*)W2t,
+                              anchor, tokens, logit_x, lse, bs, gamma, V, r, k, inv_tau, greedy, seed, step);
+  }
   return cudaGetLastError();
 }
 

@@ -51,11 +51,11 @@ constexpr uint32_t kTmemCols = kAccBufs * kBN;   // 256
 constexpr float kLog2e = 1.4426950408889634f;
 
 // 8 epilogue warps: two per TMEM lane quarter, each reducing 64 of a row's 128 columns into
-// its own half-chunk statistics entry (no cross-warp exchange).  DRAFT: W2t ring of 6
-// K-stages.  DECIDE: 4 K-stages and two gather warps, one per 64-column half of the U and
+// its own half-chunk statistics entry (no cross-warp exchange).  DRAFT: W2t ring of 5
+// K-stages (leaving room for a select block to sit beside this one on an SM).  DECIDE: 4 K-stages and two gather warps, one per 64-column half of the U and
 // target rows, each half with its own full / empty barrier pair.
 template <bool kDecide>
-__host__ __device__ constexpr int b_stages() { return kDecide ? 4 : 6; }
+__host__ __device__ constexpr int b_stages() { return kDecide ? 4 : 5; }
 template <bool kDecide>
 __host__ __device__ constexpr int epi_warps() { return 8; }
 template <bool kDecide>
@@ -66,6 +66,7 @@ struct Barriers {
   uint64_t u_full[kUStages], u_empty[kUStages];
   uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
   uint64_t drain;
+  uint64_t a_ready;  // DRAFT: the A operand is in shared memory (one arrival per epilogue warp)
   uint32_t tmem_base;
   int abort;
   int xrow[kBM];  // W1 row of each A row (-1: zero row)
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
       tc::mbar_init(tc::smem_u32(&bar->acc_empty[s]), kEpiThreads / 32);
     }
     tc::mbar_init(tc::smem_u32(&bar->drain), 1);
+    tc::mbar_init(tc::smem_u32(&bar->a_ready), kEpiThreads / 32);
     bar->abort = 0;
     tc::fence_mbar_init();
     tc::prefetch_tensormap(&tmap_w2);
@@ -181,6 +183,7 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
     tc::tmem_relinquish();
   }
   if (kDecide) {
+    tc::grid_dependency_wait();  // the decisions come from the previous kernel
     for (int m = tid; m < kBM; m += threads<kDecide>()) {
       RowMeta rm{0, 0, 0.f, 0.f, 0, 0};
       const int grow = m0 + m;
@@ -202,26 +205,27 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
   }
   // A operand: rows m0..m0+127 of W1[x] in the 128-byte-swizzled K-major layout, where x is
   // x_{k-1} (DRAFT) or the token before each residual row's rejected position (DECIDE).
-  // Token ids first, then every 16-byte row chunk as an independent cp.async.
-  for (int m = tid; m < kBM; m += threads<kDecide>()) {
-    const int grow = m0 + m;
-    int xp = -1;
-    if (grow < bs) {
-      int kx = p.k;  // position whose previous token selects the W1 row
-      bool use = true;
-      if (kDecide) {
-        const Decision d = p.dec[grow];
-        use = d.kind == kDecResidual;
-        kx = d.kdec;
+  // Token ids first, then every 16-byte row chunk as an independent cp.async.  `first` and
+  // `count` select the threads that take part, `sync` makes the token ids visible to them.
+  auto gather_a = [&](int first, int count, auto sync) {
+    for (int m = tid - first; m < kBM; m += count) {
+      const int grow = m0 + m;
+      int xp = -1;
+      if (grow < bs) {
+        int kx = p.k;  // position whose previous token selects the W1 row
+        bool use = true;
+        if (kDecide) {
+          const Decision d = p.dec[grow];
+          use = d.kind == kDecResidual;
+          kx = d.kdec;
+        }
+        if (use) xp = clamp_token((kx == 1) ? p.anchor[grow] : p.tokens[size_t(grow) * p.gamma + kx - 2], V);
       }
-      if (use) xp = clamp_token((kx == 1) ? p.anchor[grow] : p.tokens[size_t(grow) * p.gamma + kx - 2], V);
+      bar->xrow[m] = xp;
     }
-    bar->xrow[m] = xp;
-  }
-  __syncthreads();
-  {
+    sync();
     const int cpr = r / 8;  // 16-byte chunks per row
-    for (int idx = tid; idx < kBM * cpr; idx += threads<kDecide>()) {
+    for (int idx = tid - first; idx < kBM * cpr; idx += count) {
       const int row = idx / cpr, ch = idx % cpr;
       const int xp = bar->xrow[row];
       const int kb = ch >> 3, j = ch & 7;
@@ -229,13 +233,15 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
       cp_async16(dst, xp >= 0 ? p.W1 + size_t(xp) * r + ch * 8 : p.W1, xp >= 0 ? 16u : 0u);
     }
     cp_async_wait_all();
-  }
-  tc::fence_proxy_async_smem();
+    tc::fence_proxy_async_smem();
+  };
+  if (kDecide) gather_a(0, threads<kDecide>(), [] { __syncthreads(); });
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem_base = bar->tmem_base;
   const long long deadline = tc::deadline_after_ns(p.timeout_ns);
+  tc::grid_launch_dependents();  // the next kernel may start its own set-up now
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -290,7 +296,8 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
       int bstage = 0, bph = 0, ab = 0, aph = 0;
-      bool ok = true, issued = false;
+      bool ok = kDecide || tc::mbar_wait_bounded(tc::smem_u32(&bar->a_ready), 0, deadline, abort_flag);
+      bool issued = false;
       for (int t = 0; t < n_tiles && ok; ++t) {
         if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_empty[ab]), aph ^ 1, deadline, abort_flag)) {
           ok = false;
@@ -370,6 +377,14 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
     const int grow = m0 + m;
     const float inv_tau = p.inv_tau;
     const float c2 = inv_tau * kLog2e;
+    if (!kDecide) {
+      // x_{k-1} comes from the previous kernel (the select of position k-1): everything above
+      // -- barrier set-up, TMEM, and the producer's U / W2 prefetch -- overlapped with it
+      tc::grid_dependency_wait();
+      gather_a(64, kEpiThreads, [] { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); });
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->a_ready));
+    }
     int us = 0, uph = 0, ab = 0, aph = 0;
     for (int t = 0; t < n_tiles; ++t) {
       const int c = c0 + t * cstride;
@@ -556,8 +571,18 @@ cudaError_t launch(const CUtensorMap& w2, const CUtensorMap& u, const Params& pr
   const int n_mt = (prm.bs + kBM - 1) / kBM;
   int grid = (sm_count() / n_mt) * n_mt;
   grid = min(grid, n_mt * prm.n_chunks);
-  stats_tc_kernel<kDecide><<<grid, threads<kDecide>(), smem, s>>>(w2, u, prm);
-  return cudaGetLastError();
+  // programmatic dependent launch: set-up and prefetch overlap the previous kernel's tail
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads<kDecide>());
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, stats_tc_kernel<kDecide>, w2, u, prm);
 }
 
 }  // namespace

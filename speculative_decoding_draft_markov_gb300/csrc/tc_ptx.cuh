@@ -57,6 +57,14 @@ __device__ __forceinline__ long long deadline_after_ns(uint64_t ns) {
   return clock64() + static_cast<long long>(cyc);
 }
 
+// Programmatic dependent launch: wait until the previous kernel in the stream has completed and
+// its writes are visible (returns at once when the launch had no such dependency); allow the
+// next kernel to be scheduled early.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
                                             uint64_t policy) {
