@@ -82,7 +82,8 @@ DSPARK_API const char* dspark_status_string(int status);
  * that can overlap on the device (different streams) must not. */
 DSPARK_API size_t dspark_workspace_bytes(int bs, int gamma, int V);
 
-/* Zero the workspace's status word (asynchronous memset on `stream`). */
+/* Zero the whole workspace (asynchronous memset on `stream`); required once before first use:
+ * besides the status word it holds counters that the kernels keep at zero between calls. */
 DSPARK_API int dspark_workspace_init(void* ws, size_t ws_bytes, dspark_stream_t stream);
 
 /* Synchronise `stream`, return the status recorded by device-side checks since the last

@@ -56,7 +56,7 @@ size_t dspark_workspace_bytes(int bs, int gamma, int V) {
 
 int dspark_workspace_init(void* ws, size_t ws_bytes, dspark_stream_t stream) {
   if (!ws || ws_bytes < 256 || !al(ws, 256)) return DSPARK_EWORKSPACE;
-  return cuda_status(cudaMemsetAsync(ws, 0, 256, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int dspark_read_device_status(void* ws, dspark_stream_t stream) {

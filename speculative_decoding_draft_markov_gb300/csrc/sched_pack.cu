@@ -93,8 +93,11 @@ cudaError_t launch_confidence(int dtype, const void* h, const void* W1, const in
 // stop when Theta stops growing ("Infra": or take the global maximum).  vLLM adaptive
 // verification, "DSpark confidence scheduling mechanism": tau counts one extra token per
 // request plus the survival of the admitted slots.
-// One block of 1024 threads: bitonic sort of 64-bit keys (descending fp32 survival bits,
-// then slot index r * gamma + j), exact int64 fixed-point prefix sums of floor(a * 2^40),
+// One block of 1024 threads.  64-bit keys (descending fp32 survival bits, then slot index
+// r * gamma + j) are sorted by a merge tree: each request's gamma keys are sorted by one
+// thread (they normally arrive sorted already, survival being non-increasing), then
+// ceil(log2 bs) levels merge pairs of runs, every key finding its output position by a binary
+// search in the partner run.  Then exact int64 fixed-point prefix sums of floor(a * 2^40),
 // Theta in fp64 with one rounding per product, block reductions for the stop / argmax.
 // ---------------------------------------------------------------------------------------
 constexpr int kSchedThreads = 1024;
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
     const float* __restrict__ surv, int bs, int gamma, const double* __restrict__ sps, int m_max,
     int mode, int32_t* __restrict__ window, int32_t* __restrict__ K_out,
     double* __restrict__ theta_out) {
-  __shared__ unsigned long long key[kSchedMaxSlots];  // sort keys, then inclusive prefix sums
+  extern __shared__ unsigned long long sched_buf[];  // two runs buffers of kSchedMaxSlots keys
   __shared__ unsigned short slot[kSchedMaxSlots];
   __shared__ long long wsum[32];
   __shared__ int red_k[32];
@@ -113,36 +116,52 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   __shared__ int s_kstar;
   const int tid = threadIdx.x;
   const int n = bs * gamma;
-  int N = 1;
-  while (N < n) N <<= 1;
+  unsigned long long* src = sched_buf;
+  unsigned long long* dst = sched_buf + kSchedMaxSlots;
 
-  for (int e = tid; e < N; e += kSchedThreads) {
-    unsigned long long kv = ~0ull;
-    if (e < n) {
-      uint32_t bits = __float_as_uint(surv[e]);
-      if (bits & 0x80000000u) bits = 0u;  // -0 and negatives rank as 0
-      kv = (static_cast<unsigned long long>(0xFFFFFFFFu - bits) << 32) | static_cast<unsigned>(e);
+  // runs of length gamma: one request per thread, insertion sort in registers
+  for (int r = tid; r < bs; r += kSchedThreads) {
+    unsigned long long kv[DSPARK_MAX_GAMMA];
+#pragma unroll
+    for (int j = 0; j < DSPARK_MAX_GAMMA; ++j) {
+      if (j < gamma) {
+        const int e = r * gamma + j;
+        uint32_t bits = __float_as_uint(surv[e]);
+        if (bits & 0x80000000u) bits = 0u;  // -0 and negatives rank as 0
+        const unsigned long long x = (static_cast<unsigned long long>(0xFFFFFFFFu - bits) << 32) | static_cast<unsigned>(e);
+        int i = j;
+        while (i > 0 && kv[i - 1] > x) {
+          kv[i] = kv[i - 1];
+          --i;
+        }
+        kv[i] = x;
+      }
     }
-    key[e] = kv;
+#pragma unroll
+    for (int j = 0; j < DSPARK_MAX_GAMMA; ++j)
+      if (j < gamma) src[r * gamma + j] = kv[j];
   }
   for (int e = tid; e < DSPARK_MAX_BS; e += kSchedThreads) win[e] = 0;
   __syncthreads();
-  for (int kk = 2; kk <= N; kk <<= 1) {
-    for (int j = kk >> 1; j > 0; j >>= 1) {
-      for (int e = tid; e < N; e += kSchedThreads) {
-        const int p = e ^ j;
-        if (p > e) {
-          const unsigned long long a = key[e], c = key[p];
-          const bool up = (e & kk) == 0;
-          if ((a > c) == up) {
-            key[e] = c;
-            key[p] = a;
-          }
-        }
+  // merge levels: runs [i*len, min((i+1)*len, n)) pairwise into runs of 2*len
+  for (int len = gamma; len < n; len <<= 1) {
+    for (int p = tid; p < n; p += kSchedThreads) {
+      const int run = p / len, idx = p - run * len;
+      const unsigned long long x = src[p];
+      const int pbeg = (run ^ 1) * len, pend = min(pbeg + len, n);
+      int lo = pbeg, hi = max(pbeg, pend);
+      while (lo < hi) {  // keys are unique: count of partner keys below x
+        const int mid = (lo + hi) >> 1;
+        if (src[mid] < x) lo = mid + 1; else hi = mid;
       }
-      __syncthreads();
+      dst[min(run, run ^ 1) * len + idx + (lo - pbeg)] = x;
     }
+    __syncthreads();
+    unsigned long long* t = src;
+    src = dst;
+    dst = t;
   }
+  unsigned long long* key = src;  // sorted keys, then inclusive prefix sums
   // fixed-point values in sorted order, 4 consecutive per thread, then an exclusive block scan
   long long v[4];
   long long run = 0;
@@ -183,7 +202,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int i = tid * 4 + q;
-    if (i < N) key[i] = static_cast<unsigned long long>(base + v[q]);  // S_{i+1}
+    if (i < n) key[i] = static_cast<unsigned long long>(base + v[q]);  // S_{i+1}
   }
   __syncthreads();
 
@@ -250,8 +269,17 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
 cudaError_t launch_schedule(const float* surv, int bs, int gamma, const double* sps, int m_max,
                             int mode, int32_t* window, int32_t* K_out, double* theta_out,
                             cudaStream_t s) {
-  schedule_kernel<<<1, kSchedThreads, 0, s>>>(surv, bs, gamma, sps, m_max, mode, window, K_out,
-                                               theta_out);
+  constexpr int kDyn = 2 * kSchedMaxSlots * sizeof(unsigned long long);  // 64 KB: opt in, once per device
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  schedule_kernel<<<1, kSchedThreads, kDyn, s>>>(surv, bs, gamma, sps, m_max, mode, window, K_out, theta_out);
   return cudaGetLastError();
 }
 
