@@ -119,27 +119,32 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   unsigned long long* src = sched_buf;
   unsigned long long* dst = sched_buf + kSchedMaxSlots;
 
-  // runs of length gamma: one request per thread, insertion sort in registers
+  // runs of length gamma, one request per thread: written as they come, then put in order in
+  // place (insertion sort in shared memory) in the rare case a row is not already sorted
   for (int r = tid; r < bs; r += kSchedThreads) {
-    unsigned long long kv[DSPARK_MAX_GAMMA];
-#pragma unroll
-    for (int j = 0; j < DSPARK_MAX_GAMMA; ++j) {
-      if (j < gamma) {
-        const int e = r * gamma + j;
-        uint32_t bits = __float_as_uint(surv[e]);
-        if (bits & 0x80000000u) bits = 0u;  // -0 and negatives rank as 0
-        const unsigned long long x = (static_cast<unsigned long long>(0xFFFFFFFFu - bits) << 32) | static_cast<unsigned>(e);
+    bool sorted = true;
+    unsigned long long prev = 0;
+    for (int j = 0; j < gamma; ++j) {
+      const int e = r * gamma + j;
+      uint32_t bits = __float_as_uint(surv[e]);
+      if (bits & 0x80000000u) bits = 0u;  // -0 and negatives rank as 0
+      const unsigned long long x = (static_cast<unsigned long long>(0xFFFFFFFFu - bits) << 32) | static_cast<unsigned>(e);
+      sorted = sorted && (j == 0 || x > prev);
+      prev = x;
+      src[e] = x;
+    }
+    if (!sorted) {
+      unsigned long long* run = src + r * gamma;
+      for (int j = 1; j < gamma; ++j) {
+        const unsigned long long x = run[j];
         int i = j;
-        while (i > 0 && kv[i - 1] > x) {
-          kv[i] = kv[i - 1];
+        while (i > 0 && run[i - 1] > x) {
+          run[i] = run[i - 1];
           --i;
         }
-        kv[i] = x;
+        run[i] = x;
       }
     }
-#pragma unroll
-    for (int j = 0; j < DSPARK_MAX_GAMMA; ++j)
-      if (j < gamma) src[r * gamma + j] = kv[j];
   }
   for (int e = tid; e < DSPARK_MAX_BS; e += kSchedThreads) win[e] = 0;
   __syncthreads();

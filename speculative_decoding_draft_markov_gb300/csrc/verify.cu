@@ -42,9 +42,10 @@ __device__ __forceinline__ int load_group<float>(const float* row, int e, float*
   return 4;
 }
 
-// Block (p, s) reduces column slice s of packed row p to a partial (max, sum-exp) -- or
-// (max, argmax) at temperature 0 -- and the last slice block of the row to finish merges the
+// Work item (p, s) reduces column slice s of packed row p to a partial (max, sum-exp) -- or
+// (max, argmax) at temperature 0 -- and the last slice of the row to finish merges the
 // kRowSplit partials in slice order (deterministic) into RowStat[p] and resets the counter.
+// A fixed grid strides over the M * kRowSplit work items (M read on the device).
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
     const T* __restrict__ target, const int32_t* __restrict__ cu, const int32_t* __restrict__ tokens,
@@ -53,9 +54,10 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
   __shared__ float sv[kRowThreads / 32], ss[kRowThreads / 32];
   __shared__ int si[kRowThreads / 32];
   __shared__ int s_last;
-  const int p = blockIdx.x, slice = blockIdx.y, tid = threadIdx.x;
+  const int tid = threadIdx.x;
   const int M = cu[bs];
-  if (p >= M) return;
+  for (int item = blockIdx.x; item < M * kRowSplit; item += gridDim.x) {
+  const int p = item / kRowSplit, slice = item % kRowSplit;
   const T* row = target + size_t(p) * V;
   constexpr int G = sizeof(T) == 2 ? 8 : 4;
   const int ng = V / G;
@@ -115,7 +117,9 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
     s_last = (atomicAdd(&rowcnt[p], 1u) == kRowSplit - 1);
   }
   __syncthreads();
-  if (!s_last || tid != 0) return;
+  const bool last = s_last;
+  __syncthreads();  // s_last is rewritten by the next item
+  if (!last || tid != 0) continue;
   __threadfence();
   // merge in slice order
   ArgMax best{-INFINITY, INT_MAX};
@@ -141,6 +145,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
     else o.tx = greedy ? ld_f32(row, xt) : ld_f32(row, xt) * inv_tau;
   }
   rs[p] = o;
+  }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -365,7 +370,11 @@ static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_
   float2* stats = reinterpret_cast<float2*>(w + L.stats);
   RowStat* rs = reinterpret_cast<RowStat*>(w + L.rowstats);
   Decision* dec = reinterpret_cast<Decision*>(w + L.dec);
-  verify_rows_kernel<T><<<dim3(bs * (gamma + 1), kRowSplit), kRowThreads, 0, s>>>(
+  int dev = 0, n_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = max(1, min(4 * n_sm, bs * (gamma + 1) * kRowSplit));
+  verify_rows_kernel<T><<<grid, kRowThreads, 0, s>>>(
       target, cu, tokens, bs, gamma, V, inv_tau, greedy, rs, reinterpret_cast<float2*>(w + L.rowpart),
       reinterpret_cast<uint32_t*>(w + L.rowcnt), status);
   verify_decide_kernel<<<(bs + 127) / 128, 128, 0, s>>>(cu, window, mode, bs, gamma, tokens,
