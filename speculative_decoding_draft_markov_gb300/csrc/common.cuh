@@ -32,8 +32,6 @@ enum DecisionKind : int { kDecNone = 0, kDecResidual = 1, kDecBonus = 2 };
 //   status   : uint32 status word (first device-detected error wins)
 //   stats    : float2 [bs][2 * n_chunks]   per-(row, half chunk) partial statistics
 //   rowstats : RowStat [bs * (gamma + 1)]  per packed target row
-//   rowpart  : float2 [bs * (gamma + 1)][kRowSplit]  partial row statistics (one per column slice)
-//   rowcnt   : uint32 [bs * (gamma + 1)]   slices finished per row (reset by the last one)
 //   dec      : Decision [bs]               per-request verify decision
 // ----------------------------------------------------------------------------------------
 struct RowStat {
@@ -56,10 +54,8 @@ __host__ __device__ inline size_t stats_bytes(int bs, int n_chunks) {
   return size_t(bs) * n_chunks * kStatsPerChunk * sizeof(float2);
 }
 
-constexpr int kRowSplit = 8;  // column slices (thread blocks) per packed target row
-
 struct WsLayout {
-  size_t status = 0, stats = 0, rowstats = 0, rowpart = 0, rowcnt = 0, dec = 0, total = 0;
+  size_t status = 0, stats = 0, rowstats = 0, dec = 0, total = 0;
   int n_chunks = 0;
 };
 
@@ -73,10 +69,6 @@ __host__ __device__ inline WsLayout ws_layout(int bs, int gamma, int V) {
   off += align256(stats_bytes(bs, L.n_chunks));
   L.rowstats = off;
   off += align256(size_t(bs) * (gamma + 1) * sizeof(RowStat));
-  L.rowpart = off;
-  off += align256(size_t(bs) * (gamma + 1) * kRowSplit * sizeof(float2));
-  L.rowcnt = off;
-  off += align256(size_t(bs) * (gamma + 1) * sizeof(uint32_t));
   L.dec = off;
   off += align256(size_t(bs) * sizeof(Decision));
   L.total = off;

@@ -24,7 +24,7 @@ namespace dspark {
 // Row statistics.  16-byte vector loads, per-thread online (max, sum-exp), fixed-order
 // block merge.
 // ---------------------------------------------------------------------------------------
-constexpr int kRowThreads = 256;
+constexpr int kRowThreads = 512;
 
 template <typename T>
 __device__ __forceinline__ int load_group(const T* row, int e, float* x);
@@ -42,109 +42,86 @@ __device__ __forceinline__ int load_group<float>(const float* row, int e, float*
   return 4;
 }
 
-// Work item (p, s) reduces column slice s of packed row p to a partial (max, sum-exp) -- or
-// (max, argmax) at temperature 0 -- and the last slice of the row to finish merges the
-// kRowSplit partials in slice order (deterministic) into RowStat[p] and resets the counter.
-// A fixed grid strides over the M * kRowSplit work items (M read on the device).
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
     const T* __restrict__ target, const int32_t* __restrict__ cu, const int32_t* __restrict__ tokens,
-    int bs, int gamma, int V, float inv_tau, int greedy, RowStat* __restrict__ rs,
-    float2* __restrict__ rowpart, uint32_t* __restrict__ rowcnt, uint32_t* status) {
+    int bs, int gamma, int V, float inv_tau, int greedy, RowStat* __restrict__ rs, uint32_t* status) {
   __shared__ float sv[kRowThreads / 32], ss[kRowThreads / 32];
   __shared__ int si[kRowThreads / 32];
-  __shared__ int s_last;
-  const int tid = threadIdx.x;
+  const int p = blockIdx.x, tid = threadIdx.x;
   const int M = cu[bs];
-  for (int item = blockIdx.x; item < M * kRowSplit; item += gridDim.x) {
-  const int p = item / kRowSplit, slice = item % kRowSplit;
-  const T* row = target + size_t(p) * V;
-  constexpr int G = sizeof(T) == 2 ? 8 : 4;
-  const int ng = V / G;
-  const int per = (ng + kRowSplit - 1) / kRowSplit;
-  const int g0 = slice * per, g1 = min(ng, g0 + per);
-  constexpr int kBatch = 4;  // independent 16-byte loads in flight per thread
-  float2 part;
-  if (greedy) {
-    ArgMax best{-INFINITY, INT_MAX};
-    for (int e0 = g0 + tid; e0 < g1; e0 += kBatch * kRowThreads) {
-      float xb[kBatch][8];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int e = e0 + u * kRowThreads;
-        if (e < g1) load_group<T>(row, e, xb[u]);
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int e = e0 + u * kRowThreads;
-        if (e >= g1) break;
-#pragma unroll
-        for (int q = 0; q < G; ++q)
-          if (xb[u][q] > best.v) best = ArgMax{xb[u][q], e * G + q};
-      }
-    }
-    best = block_argmax<kRowThreads>(best, sv, si);
-    part = make_float2(best.v, __int_as_float(best.i));
-  } else {
-    LsePair acc{-INFINITY, 0.f};
-    for (int e0 = g0 + tid; e0 < g1; e0 += kBatch * kRowThreads) {
-      float xb[kBatch][8];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int e = e0 + u * kRowThreads;
-        if (e < g1) load_group<T>(row, e, xb[u]);
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        if (e0 + u * kRowThreads >= g1) break;
-        float gm = xb[u][0] * inv_tau;
-#pragma unroll
-        for (int q = 1; q < G; ++q) gm = fmaxf(gm, xb[u][q] * inv_tau);
-        if (gm > acc.m) {
-          acc.s = (acc.s == 0.f) ? 0.f : acc.s * expf(acc.m - gm);
-          acc.m = gm;
-        }
-#pragma unroll
-        for (int q = 0; q < G; ++q) acc.s += expf(xb[u][q] * inv_tau - acc.m);
-      }
-    }
-    acc = block_lse<kRowThreads>(acc, sv, ss);
-    part = make_float2(acc.m, acc.s);
-  }
-  if (tid == 0) {
-    rowpart[size_t(p) * kRowSplit + slice] = part;
-    __threadfence();
-    s_last = (atomicAdd(&rowcnt[p], 1u) == kRowSplit - 1);
-  }
-  __syncthreads();
-  const bool last = s_last;
-  __syncthreads();  // s_last is rewritten by the next item
-  if (!last || tid != 0) continue;
-  __threadfence();
-  // merge in slice order
-  ArgMax best{-INFINITY, INT_MAX};
-  LsePair acc{-INFINITY, 0.f};
-  const volatile float2* vp = rowpart + size_t(p) * kRowSplit;
-  for (int k = 0; k < kRowSplit; ++k) {
-    const float2 q = make_float2(vp[k].x, vp[k].y);
-    if (greedy) best = better(best, ArgMax{q.x, __float_as_int(q.y)});
-    else acc = lse_merge(acc, LsePair{q.x, q.y});
-  }
-  rowcnt[p] = 0u;
-  // the request owning row p and the draft token this row tests
+  if (p >= M) return;
   int lo = 0, hi = bs;  // cu[lo] <= p < cu[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (cu[mid] <= p) lo = mid; else hi = mid;
   }
   const int r = lo, j = p - cu[r], n_r = cu[r + 1] - cu[r];
-  RowStat o = greedy ? RowStat{0.f, 0.f, best.i, 0} : RowStat{acc.m + logf(acc.s), -INFINITY, -1, 0};
-  if (j < n_r - 1 && j < gamma) {
-    const int xt = tokens[size_t(r) * gamma + j];
-    if (xt < 0 || xt >= V) set_status(status, DSPARK_EINVAL);
-    else o.tx = greedy ? ld_f32(row, xt) : ld_f32(row, xt) * inv_tau;
+  const T* row = target + size_t(p) * V;
+  constexpr int G = sizeof(T) == 2 ? 8 : 4;
+  const int ng = V / G;
+  if (greedy) {
+    ArgMax best{-INFINITY, INT_MAX};
+    for (int e0 = tid; e0 < ng; e0 += 4 * kRowThreads) {
+      float xb[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kRowThreads;
+        if (e < ng) load_group<T>(row, e, xb[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kRowThreads;
+        if (e >= ng) break;
+#pragma unroll
+        for (int q = 0; q < G; ++q)
+          if (xb[u][q] > best.v) best = ArgMax{xb[u][q], e * G + q};
+      }
+    }
+    best = block_argmax<kRowThreads>(best, sv, si);
+    if (tid == 0) {
+      RowStat o{0.f, 0.f, best.i, 0};
+      if (j < n_r - 1 && j < gamma) {
+        const int xt = tokens[size_t(r) * gamma + j];
+        if (xt < 0 || xt >= V) set_status(status, DSPARK_EINVAL);
+        else o.tx = ld_f32(row, xt);
+      }
+      rs[p] = o;
+    }
+    return;
   }
-  rs[p] = o;
+  LsePair acc{-INFINITY, 0.f};
+  constexpr int kBatch = 4;  // independent 16-byte loads in flight per thread
+  for (int e0 = tid; e0 < ng; e0 += kBatch * kRowThreads) {
+    float xb[kBatch][8];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int e = e0 + u * kRowThreads;
+      if (e < ng) load_group<T>(row, e, xb[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (e0 + u * kRowThreads >= ng) break;
+      float gm = xb[u][0] * inv_tau;
+#pragma unroll
+      for (int q = 1; q < G; ++q) gm = fmaxf(gm, xb[u][q] * inv_tau);
+      if (gm > acc.m) {
+        acc.s = (acc.s == 0.f) ? 0.f : acc.s * expf(acc.m - gm);
+        acc.m = gm;
+      }
+#pragma unroll
+      for (int q = 0; q < G; ++q) acc.s += expf(xb[u][q] * inv_tau - acc.m);
+    }
+  }
+  acc = block_lse<kRowThreads>(acc, sv, ss);
+  if (tid == 0) {
+    RowStat o{acc.m + logf(acc.s), -INFINITY, -1, 0};
+    if (j < n_r - 1 && j < gamma) {
+      const int xt = tokens[size_t(r) * gamma + j];
+      if (xt < 0 || xt >= V) set_status(status, DSPARK_EINVAL);
+      else o.tx = ld_f32(row, xt) * inv_tau;
+    }
+    rs[p] = o;
   }
 }
 
@@ -370,13 +347,8 @@ static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_
   float2* stats = reinterpret_cast<float2*>(w + L.stats);
   RowStat* rs = reinterpret_cast<RowStat*>(w + L.rowstats);
   Decision* dec = reinterpret_cast<Decision*>(w + L.dec);
-  int dev = 0, n_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = max(1, min(4 * n_sm, bs * (gamma + 1) * kRowSplit));
-  verify_rows_kernel<T><<<grid, kRowThreads, 0, s>>>(
-      target, cu, tokens, bs, gamma, V, inv_tau, greedy, rs, reinterpret_cast<float2*>(w + L.rowpart),
-      reinterpret_cast<uint32_t*>(w + L.rowcnt), status);
+  verify_rows_kernel<T><<<bs * (gamma + 1), kRowThreads, 0, s>>>(target, cu, tokens, bs, gamma, V,
+                                                                  inv_tau, greedy, rs, status);
   verify_decide_kernel<<<(bs + 127) / 128, 128, 0, s>>>(cu, window, mode, bs, gamma, tokens,
                                                          logit_x, lse, rs, greedy, seed, step,
                                                          out_tokens, acc_len, ceiling, dec, status);
