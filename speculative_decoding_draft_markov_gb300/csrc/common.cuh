@@ -11,9 +11,20 @@
 namespace dspark {
 
 constexpr int kChunk = DSPARK_CHUNK;
-// Statistics are kept per half chunk (64 ids): entry 2c + h covers ids [128c + 64h, 128c + 64h + 64).
-// Passes that reduce a whole chunk at once write entry 2c and a neutral entry 2c + 1.
+// Verify's decision statistics are kept per half chunk (64 ids): entry 2c + h covers ids
+// [128c + 64h, 128c + 64h + 64).  Passes that reduce a whole chunk at once write entry 2c and
+// a neutral entry 2c + 1.
 constexpr int kStatsPerChunk = 2;
+
+// The draft's partial draw over a set of chunks ("slot") of one request, as a float4:
+//   x, y : running (max t, sum exp(t - max)) of the tempered logits t = l / T over the slot's
+//          chunks (-inf, 0 when empty; unused at temperature 0)
+//   z    : best key -- temperature > 0: max over the slot's chunks of the chunk's log-mass
+//          plus its Gumbel (Philox purpose 1, index c); temperature 0: the max logit
+//   w    : int bits of the argmax of z -- the chunk index (T > 0) or the token id (T = 0);
+//          INT_MAX when empty.  Ties go to the lowest index.
+// The select merges a request's entries: LSE from (x, y), winner = argmax (z, lowest w).
+// Slots never share a chunk, so the merged winner is the two-level draw's chunk.
 
 // Philox purposes (counter word 3, bits 24..31).
 enum Purpose : uint32_t {
@@ -30,7 +41,8 @@ enum DecisionKind : int { kDecNone = 0, kDecResidual = 1, kDecBonus = 2 };
 // ----------------------------------------------------------------------------------------
 // Workspace layout (all offsets 256-byte aligned)
 //   status   : uint32 status word (first device-detected error wins)
-//   stats    : float2 [bs][2 * n_chunks]   per-(row, half chunk) partial statistics
+//   stats    : 16 bytes per (row, chunk): the draft's entries (float4 [bs][n_slots],
+//              n_slots <= n_chunks) or verify's float2 [bs][2 * n_chunks] half-chunk masses
 //   rowstats : RowStat [bs * (gamma + 1)]  per packed target row
 //   dec      : Decision [bs]               per-request verify decision
 // ----------------------------------------------------------------------------------------

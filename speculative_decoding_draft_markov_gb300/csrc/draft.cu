@@ -3,8 +3,8 @@
 //
 // DSpark technical summary, "Architecture (drafter)": the sequential Markov head adds the
 // rank-r bias W1[x_{k-1}] W2 to the backbone's base logits U_k and samples left to right.
-// One position k is two launches: draft_stats (every (row, 128-id chunk) -> partial
-// statistics in the workspace) and draft_select (one block per row: merge, draw x_k).
+// One position k is two launches: draft_stats (partial draws: per row, one DraftEntry per
+// slot of chunks) and draft_select (one block per row: merge the entries, draw x_k).
 #include <climits>
 
 #include "common.cuh"
@@ -13,15 +13,16 @@
 namespace dspark {
 
 // ---------------------------------------------------------------------------------------
-// CUDA-core statistics pass.  Block = 128 threads = one 128-id chunk; RB rows per block.
-// Serves fp32 inputs (exact fp32 FMA) and small problems; bf16 at scale uses the
+// CUDA-core statistics pass.  Block = 128 threads = one 128-id chunk = one slot; RB rows per
+// block.  Serves fp32 inputs (exact fp32 FMA) and small problems; bf16 at scale uses the
 // tensor-core pass in draft_tc.cu.
 // ---------------------------------------------------------------------------------------
 template <typename T, int RB>
 __global__ void __launch_bounds__(128) draft_stats_simt_kernel(
     const T* __restrict__ U, const T* __restrict__ W1, const T* __restrict__ W2t,
     const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens, int bs, int gamma,
-    int V, int r, int k, float inv_tau, int greedy, float2* __restrict__ stats, int n_chunks) {
+    int V, int r, int k, float inv_tau, int greedy, uint64_t seed, uint64_t step,
+    float4* __restrict__ entries, int n_chunks) {
   __shared__ float sA[RB][64];
   __shared__ float sW[kChunk][65];
   __shared__ float red[4];
@@ -62,99 +63,85 @@ __global__ void __launch_bounds__(128) draft_stats_simt_kernel(
     const int row = rb + rr;
     if (row >= bs) break;  // uniform over the block
     const float l = valid ? acc[rr] + ld_f32(U, (size_t(row) * gamma + (k - 1)) * V + v) : 0.f;
+    float4* out = entries + size_t(row) * n_chunks + c;
     if (greedy) {
       const ArgMax am = block_argmax<kChunk>(ArgMax{valid ? l : -INFINITY, valid ? v : INT_MAX}, red, redi);
-      if (tid == 0) {
-        stats[(size_t(row) * n_chunks + c) * kStatsPerChunk] = make_float2(am.v, __int_as_float(am.i));
-        stats[(size_t(row) * n_chunks + c) * kStatsPerChunk + 1] = make_float2(-INFINITY, __int_as_float(INT_MAX));
-      }
+      if (tid == 0) *out = make_float4(-INFINITY, 0.f, am.v, __int_as_float(am.i));
     } else {
       const float t = valid ? l * inv_tau : -INFINITY;
       const float m = block_max<kChunk>(t, red);
       const float s = block_sum<kChunk>(valid ? expf(t - m) : 0.f, red);
       if (tid == 0) {
-        stats[(size_t(row) * n_chunks + c) * kStatsPerChunk] = make_float2(m, s);
-        stats[(size_t(row) * n_chunks + c) * kStatsPerChunk + 1] = make_float2(-INFINITY, 0.f);
+        float4 e = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(INT_MAX));
+        if (m > -INFINITY) {  // chunk key: log-mass + Gumbel (purpose 1, index c)
+          const uint4 w = philox_group(seed, step, kDraftChunk, uint32_t(row), k, uint32_t(c) >> 2);
+          e = make_float4(m, s, m + logf(s) + gumbel_from_bits(pick_word(w, c & 3)), __int_as_float(c));
+        }
+        *out = e;
       }
     }
   }
 }
 
 // ---------------------------------------------------------------------------------------
-// Select pass: one 256-thread block per row.
-//   temperature > 0: row LSE = merge of the chunk pairs; chunk key = m_c + log s_c + G_c
-//   (purpose 1, index c); best chunk c*; the 128 logits of c* are recomputed (fixed-order
-//   fp32 dot products) and the entry key t_v + G'_v (purpose 2, index v - 128 c*) picks x_k.
-//   temperature = 0: lowest-index argmax over the chunk maxima.
+// Select pass: one 256-thread block per row.  Warp 0 merges the row's entries: the row LSE
+// from the (max, sum-exp) pairs, and the winner = argmax of the keys (lowest index on ties).
+//   temperature > 0: the winner is the chunk c* of the first Gumbel level; its 128 logits are
+//   recomputed (fixed-order fp32 dot products) and the entry key t_v + G'_v (purpose 2,
+//   index v - 128 c*) picks x_k.
+//   temperature = 0: the winner is x_k itself (lowest-index argmax).
 // ---------------------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(256) draft_select_kernel(
-    const float2* __restrict__ stats, int n_chunks, const T* __restrict__ U,
+    const float4* __restrict__ entries, int n_slots, const T* __restrict__ U,
     const T* __restrict__ W1, const T* __restrict__ W2t, const int32_t* __restrict__ anchor,
     int32_t* __restrict__ tokens, float* __restrict__ logit_x, float* __restrict__ lse, int bs,
     int gamma, int V, int r, int k, float inv_tau, int greedy, uint64_t seed, uint64_t step) {
   __shared__ float sA[256];
   __shared__ float tv[kChunk];
-  __shared__ float rv[8], rs[8], ru[8];
+  __shared__ float rv[8];
   __shared__ int ri[8];
+  __shared__ float s_lse, s_best;
+  __shared__ int s_win;
   const int b = blockIdx.x, tid = threadIdx.x;
-  const float2* st = stats + size_t(b) * n_chunks * kStatsPerChunk;
+  const float4* en = entries + size_t(b) * n_slots;
   // launched as a programmatic dependent of the statistics pass: wait for it to complete, then
   // let the next position's statistics kernel start its set-up
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const size_t out = size_t(b) * gamma + (k - 1);
 
-  if (greedy) {
+  // the W1 row of x_{k-1} does not depend on the draw: fetch it first
+  if (!greedy) {
+    const int xp = clamp_token((k == 1) ? anchor[b] : tokens[size_t(b) * gamma + k - 2], V);
+    for (int i = tid; i < r; i += 256) sA[i] = ld_f32(W1, size_t(xp) * r + i);
+  }
+  if (tid < 32) {
+    LsePair lp{-INFINITY, 0.f};
     ArgMax best{-INFINITY, INT_MAX};
-    for (int c = tid; c < n_chunks * kStatsPerChunk; c += 256) {
-      const float2 s2 = st[c];
-      best = better(best, ArgMax{s2.x, __float_as_int(s2.y)});
+    for (int i = tid; i < n_slots; i += 32) {
+      const float4 e = en[i];
+      lp = lse_merge(lp, LsePair{e.x, e.y});
+      best = better(best, ArgMax{e.z, __float_as_int(e.w)});
     }
-    best = block_argmax<256>(best, rv, ri);
+    lp = warp_lse(lp);
+    best = warp_argmax(best);
     if (tid == 0) {
-      tokens[out] = best.i;
-      logit_x[out] = best.v;
+      s_lse = lp.m + logf(lp.s);
+      s_best = best.v;
+      s_win = best.i;
+    }
+  }
+  __syncthreads();
+  if (greedy) {
+    if (tid == 0) {
+      tokens[out] = (s_win == INT_MAX) ? 0 : s_win;
+      logit_x[out] = s_best;
       lse[out] = 0.f;
     }
     return;
   }
-
-  // the W1 row of x_{k-1} does not depend on the chunk choice: fetch it first
-  const int xp = clamp_token((k == 1) ? anchor[b] : tokens[size_t(b) * gamma + k - 2], V);
-  for (int i = tid; i < r; i += 256) sA[i] = ld_f32(W1, size_t(xp) * r + i);
-
-  LsePair lp{-INFINITY, 0.f};
-  ArgMax best{-INFINITY, INT_MAX};
-  const int n_grp = (n_chunks + 3) / 4;
-  for (int g = tid; g < n_grp; g += 256) {
-    const uint4 w = philox_group(seed, step, kDraftChunk, b, k, g);
-#pragma unroll
-    for (int l = 0; l < 4; ++l) {
-      const int c = 4 * g + l;
-      if (c >= n_chunks) break;
-      const float2 h0 = st[2 * c], h1 = st[2 * c + 1];
-      const LsePair cl = lse_merge(LsePair{h0.x, h0.y}, LsePair{h1.x, h1.y});  // the chunk's (max, sum-exp)
-      lp = lse_merge(lp, cl);
-      if (cl.s > 0.f) best = better(best, ArgMax{cl.m + logf(cl.s) + gumbel_from_bits(pick_word(w, l)), c});
-    }
-  }
-  // one combined block reduction of (row LSE, best chunk)
-  lp = warp_lse(lp);
-  best = warp_argmax(best);
-  {
-    const int w = tid >> 5, l = tid & 31;
-    if (l == 0) { rv[w] = lp.m; rs[w] = lp.s; ru[w] = best.v; ri[w] = best.i; }
-    __syncthreads();
-    lp = LsePair{rv[0], rs[0]};
-    best = ArgMax{ru[0], ri[0]};
-#pragma unroll
-    for (int i = 1; i < 8; ++i) {
-      lp = lse_merge(lp, LsePair{rv[i], rs[i]});
-      best = better(best, ArgMax{ru[i], ri[i]});
-    }
-  }
-  const int cstar = (best.i == INT_MAX) ? 0 : best.i;  // only non-finite statistics leave it unset
+  const int cstar = (s_win == INT_MAX) ? 0 : s_win;  // only non-finite statistics leave it unset
   // the U values of the chosen chunk load together with its W2t rows
   float u_v = 0.f;
   const int v_own = cstar * kChunk + tid;
@@ -174,35 +161,35 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
     const int ei = (e.i == INT_MAX) ? 0 : e.i;
     tokens[out] = min(cstar * kChunk + ei, V - 1);
     logit_x[out] = tv[ei];
-    lse[out] = lp.m + logf(lp.s);
+    lse[out] = s_lse;
   }
 }
 
 cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, const void* W2t,
                                     const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
-                                    int V, int r, int k, float inv_tau, int greedy, void* stats,
-                                    int n_chunks, cudaStream_t s) {
+                                    int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
+                                    uint64_t step, void* entries, int n_chunks, cudaStream_t s) {
   constexpr int RB = 32;
   dim3 grid(n_chunks, (bs + RB - 1) / RB);
   if (dtype == DSPARK_F32)
     draft_stats_simt_kernel<float, RB><<<grid, kChunk, 0, s>>>(
         (const float*)U, (const float*)W1, (const float*)W2t, anchor, tokens, bs, gamma, V, r, k,
-        inv_tau, greedy, (float2*)stats, n_chunks);
+        inv_tau, greedy, seed, step, (float4*)entries, n_chunks);
   else
     draft_stats_simt_kernel<__nv_bfloat16, RB><<<grid, kChunk, 0, s>>>(
         (const __nv_bfloat16*)U, (const __nv_bfloat16*)W1, (const __nv_bfloat16*)W2t, anchor,
-        tokens, bs, gamma, V, r, k, inv_tau, greedy, (float2*)stats, n_chunks);
+        tokens, bs, gamma, V, r, k, inv_tau, greedy, seed, step, (float4*)entries, n_chunks);
   return cudaGetLastError();
 }
 
-cudaError_t launch_draft_select(int dtype, const void* stats, int n_chunks, const void* U,
+cudaError_t launch_draft_select(int dtype, const void* entries, int n_slots, const void* U,
                                 const void* W1, const void* W2t, const int32_t* anchor,
                                 int32_t* tokens, float* logit_x, float* lse, int bs, int gamma,
                                 int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
                                 uint64_t step, cudaStream_t s) {
   if (dtype == DSPARK_F32)
     draft_select_kernel<float><<<bs, 256, 0, s>>>(
-        (const float2*)stats, n_chunks, (const float*)U, (const float*)W1, (const float*)W2t,
+        (const float4*)entries, n_slots, (const float*)U, (const float*)W1, (const float*)W2t,
         anchor, tokens, logit_x, lse, bs, gamma, V, r, k, inv_tau, greedy, seed, step);
   else {
     cudaLaunchConfig_t cfg = {};
@@ -214,7 +201,7 @@ cudaError_t launch_draft_select(int dtype, const void* stats, int n_chunks, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, draft_select_kernel<__nv_bfloat16>, (const float2*)stats, n_chunks,
+    return cudaLaunchKernelEx(&cfg, draft_select_kernel<__nv_bfloat16>, (const float4*)entries, n_slots,
                               (const __nv_bfloat16*)U, (const __nv_bfloat16*)W1, (const __nv_bfloat16*)W2t,
                               anchor, tokens, logit_x, lse, bs, gamma, V, r, k, inv_tau, greedy, seed, step);
   }

@@ -18,7 +18,12 @@
 //   warp 0    = TMA producer: W2t tiles in K-stages of 64 (evict-last: W2 is re-read by every
 //               position) and, in DRAFT, the U tile (3-D map over [bs, gamma, V], evict-first)
 //   warp 1    = TMEM owner + single-thread tcgen05.mma issuer, commits to mbarriers
-//   warps 2-5 = epilogue: tcgen05.ld of the 128 x 128 fp32 accumulator (one row per thread)
+//   warps 2-9 = epilogue, two warps per TMEM lane quarter (one request row per thread).
+//               DRAFT: the two warp sets take alternate tiles (full 128-id chunks) and keep
+//               per-row running statistics and the best chunk key in registers; each CTA
+//               writes one entry per request at the end (DraftEntry), so the select merges
+//               one entry per CTA instead of one per chunk.  DECIDE: each warp reduces 64 of
+//               a tile's 128 columns into a half-chunk entry.
 //   warps 10-11 = (DECIDE) cp.async gather of each request's U row and target row, one warp
 //               per 64-column half, so one half refills while the other is being reduced
 //   2 TMEM accumulators (256 columns) let MMA, loads and epilogue overlap.
@@ -50,10 +55,10 @@ constexpr uint32_t kUHalf = kBM * 64 * 2;        // 16 KB: one 64-column half of
 constexpr uint32_t kTmemCols = kAccBufs * kBN;   // 256
 constexpr float kLog2e = 1.4426950408889634f;
 
-// 8 epilogue warps: two per TMEM lane quarter, each reducing 64 of a row's 128 columns into
-// its own half-chunk statistics entry (no cross-warp exchange).  DRAFT: W2t ring of 5
-// K-stages (leaving room for a select block to sit beside this one on an SM).  DECIDE: 4 K-stages and two gather warps, one per 64-column half of the U and
-// target rows, each half with its own full / empty barrier pair.
+// 8 epilogue warps, two per TMEM lane quarter.  DRAFT: W2t ring of 5 K-stages (leaving room
+// for a select block to sit beside this one on an SM).  DECIDE: 4 K-stages and two gather
+// warps, one per 64-column half of the U and target rows, each half with its own full / empty
+// barrier pair.
 template <bool kDecide>
 __host__ __device__ constexpr int b_stages() { return kDecide ? 4 : 5; }
 template <bool kDecide>
@@ -70,6 +75,7 @@ struct Barriers {
   uint32_t tmem_base;
   int abort;
   int xrow[kBM];  // W1 row of each A row (-1: zero row)
+  float4 xch[kBM];  // DRAFT: warp set 1's entry of each row, merged by set 0 at the end
 };
 
 // Per-row facts of the DECIDE pass (one request per tile row).
@@ -89,10 +95,14 @@ struct Params {
   int bs, gamma, V, r, k;
   float inv_tau;
   int greedy;
-  float2* stats;
+  float2* stats;    // DECIDE: per (request, chunk) half-chunk masses
   int n_chunks;
   uint32_t* status;
   uint64_t timeout_ns;
+  // DRAFT only
+  float4* entries;  // per (request, slot): see DraftEntry
+  int n_slots;
+  uint64_t seed, step;
   // DECIDE only
   const __nv_bfloat16* U;
   const __nv_bfloat16* target;
@@ -123,6 +133,14 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// The chunk Gumbel G_c of request `req` at position k (Philox purpose 1, index c).  Kept out of
+// line: inlined into the DRAFT tile loop its Philox rounds raise register pressure there
+// enough to spill, although the loop only calls it for tiles past the ones drawn up front.
+__device__ __noinline__ float chunk_gumbel_call(uint64_t seed, uint64_t step, int req, int k, int c) {
+  const uint4 w = philox_group(seed, step, kDraftChunk, uint32_t(req), k, uint32_t(c) >> 2);
+  return gumbel_from_bits(pick_word(w, c & 3));
+}
 
 __device__ __forceinline__ void unpack8(const uint4 q, float* x) {
   x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
@@ -164,12 +182,14 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
     }
     for (int s = 0; s < kUStages; ++s) {
       tc::mbar_init(tc::smem_u32(&bar->u_full[s]), kDecide ? 32 : 1);  // DECIDE: one arrive per loader lane
-      // one arrival per epilogue warp (DECIDE: per warp of the half the stage holds)
-      tc::mbar_init(tc::smem_u32(&bar->u_empty[s]), kDecide ? kEpiThreads / 64 : kEpiThreads / 32);
+      // one arrival per epilogue warp that reads the stage: DRAFT, the warp set of tiles with
+      // this parity; DECIDE, the warps of the column half the stage holds
+      tc::mbar_init(tc::smem_u32(&bar->u_empty[s]), kEpiThreads / 64);
     }
     for (int s = 0; s < kAccBufs; ++s) {
       tc::mbar_init(tc::smem_u32(&bar->acc_full[s]), 1);
-      tc::mbar_init(tc::smem_u32(&bar->acc_empty[s]), kEpiThreads / 32);
+      // DRAFT: one warp set per accumulator buffer; DECIDE: every epilogue warp
+      tc::mbar_init(tc::smem_u32(&bar->acc_empty[s]), kDecide ? kEpiThreads / 32 : kEpiThreads / 64);
     }
     tc::mbar_init(tc::smem_u32(&bar->drain), 1);
     tc::mbar_init(tc::smem_u32(&bar->a_ready), kEpiThreads / 32);
@@ -242,6 +262,7 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
   const uint32_t tmem_base = bar->tmem_base;
   const long long deadline = tc::deadline_after_ns(p.timeout_ns);
   tc::grid_launch_dependents();  // the next kernel may start its own set-up now
+  float4 xmine = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(INT_MAX));  // DRAFT epilogue entry
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -369,30 +390,52 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
       set_status(p.status, DSPARK_ETIMEOUT);
     }
     cp_async_wait_all();  // no copy of this warp outlives the CTA
-  } else if (warp >= 2 && warp < 2 + epi_warps<kDecide>()) {
-    // ------------------------------------------------------------------ epilogue
+  } else if (!kDecide && warp >= 2 && warp < 2 + epi_warps<kDecide>()) {
+    // ------------------------------------------------------------------ DRAFT epilogue
+    // Warp set `half` (4 warps, one per TMEM lane quarter) takes the CTA's tiles t = half,
+    // half + 2, ...: accumulator buffer `half` and U stage `half` always.  A thread owns one
+    // request row and, per tile (= one 128-id chunk), reduces the chunk to its log-mass and the
+    // chunk's Gumbel key, keeping in registers the running (max, sum-exp) over its chunks and
+    // the best key seen (at temperature 0: the running max logit and its lowest index).
     const int wq = warp & 3;          // TMEM lane quarter this warp may access
     const int m = wq * 32 + lane;     // tile row = TMEM lane
-    const int half = (warp - 2) >> 2; // DRAFT: which 64 of the 128 columns this warp takes
+    const int half = (warp - 2) >> 2; // warp set
     const int grow = m0 + m;
     const float inv_tau = p.inv_tau;
     const float c2 = inv_tau * kLog2e;
-    if (!kDecide) {
-      // x_{k-1} comes from the previous kernel (the select of position k-1): everything above
-      // -- barrier set-up, TMEM, and the producer's U / W2 prefetch -- overlapped with it
-      tc::grid_dependency_wait();
-      gather_a(64, kEpiThreads, [] { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); });
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->a_ready));
+    // The chunk Gumbels (Philox purpose 1) of this row and of the set's first kGReg tiles do not
+    // depend on any logit: draw them before waiting for the previous kernel, so that the Philox
+    // rounds overlap its tail instead of the tile loop.  Later tiles draw theirs in the loop.
+    constexpr int kGReg = 8;
+    auto chunk_gumbel = [&](int c) {
+      const uint4 w = philox_group(p.seed, p.step, kDraftChunk, uint32_t(grow), p.k, uint32_t(c) >> 2);
+      return gumbel_from_bits(pick_word(w, c & 3));
+    };
+    float gk[kGReg];
+#pragma unroll
+    for (int i = 0; i < kGReg; ++i) {
+      const int t = half + 2 * i;
+      gk[i] = (!p.greedy && t < n_tiles) ? chunk_gumbel(c0 + t * cstride) : 0.f;
     }
-    int us = 0, uph = 0, ab = 0, aph = 0;
-    for (int t = 0; t < n_tiles; ++t) {
+    // x_{k-1} comes from the previous kernel (the select of position k-1): everything above
+    // -- barrier set-up, TMEM, the producer's U / W2 prefetch, the Gumbels -- overlapped with it
+    tc::grid_dependency_wait();
+    gather_a(64, kEpiThreads, [] { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); });
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->a_ready));
+
+    const uint32_t taddr = tmem_base + (uint32_t(wq * 32) << 16) + half * kBN;
+    const uint8_t* ub = sU + half * 2 * kUHalf + m * 128;
+    // running (max, sum-exp) in log2 units: run_m = max of l c2, run_s = sum of 2^(l c2 - run_m)
+    float run_m = -INFINITY, run_s = 0.f, best_key = -INFINITY;
+    int best_c = INT_MAX;
+    int ph = 0;
+    for (int t = half, i = 0; t < n_tiles; t += 2, ++i, ph ^= 1) {
       const int c = c0 + t * cstride;
       const int n0 = c * kBN;
       const int valid = min(kBN, V - n0);
-      const int ustage = kDecide ? half : us;  // DECIDE: the stage of this warp's column half
-      bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[ab]), aph, deadline, abort_flag) &&
-                tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[ustage]), uph, deadline, abort_flag);
+      bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[half]), ph, deadline, abort_flag) &&
+                tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[half]), ph, deadline, abort_flag);
       // one decision per warp before the .sync.aligned TMEM loads; warps run independently
       // (no named barrier in this loop), so a warp that gives up can hold up no other
       ok = __all_sync(0xFFFFFFFFu, ok);
@@ -402,98 +445,131 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
         break;
       }
       tc::tc_fence_after();
-      const uint32_t taddr = tmem_base + (uint32_t(wq * 32) << 16) + ab * kBN;
-      float2 part;
-      if (!kDecide) {
-        constexpr int kH = kBN / 2;  // columns per thread
-        float v[kH];
+      float v[kBN];
 #pragma unroll
-        for (int q = 0; q < kH / 32; ++q)
-          tc::tmem_ld32(taddr + half * kH + q * 32, reinterpret_cast<uint32_t*>(v + q * 32));
-        tc::tmem_ld_wait();
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[ab]));
+      for (int q = 0; q < kBN / 32; ++q) tc::tmem_ld32(taddr + q * 32, reinterpret_cast<uint32_t*>(v + q * 32));
+      tc::tmem_ld_wait();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[half]));
+#pragma unroll
+      for (int j = 0; j < kBN / 8; ++j) {  // + U_k: 16-byte groups of the two 64-column halves
+        float x[8];
+        unpack8(*reinterpret_cast<const uint4*>(ub + (j >> 3) * kUHalf + (((j & 7) ^ (m & 7)) << 4)), x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[8 * j + e] += x[e];
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->u_empty[half]));
 
-        const uint8_t* ub = sU + us * 2 * kUHalf + half * kUHalf + m * 128;
+      if (p.greedy) {
+        float best = -INFINITY;
+        int bi = INT_MAX;
 #pragma unroll
-        for (int j = 0; j < kH / 8; ++j) {
-          float x[8];
-          unpack8(*reinterpret_cast<const uint4*>(ub + ((j ^ (m & 7)) << 4)), x);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[8 * j + e] += x[e];
-        }
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->u_empty[us]));
-
-        const int vh = valid - half * kH;  // valid columns of this half (may be <= 0)
-        if (p.greedy) {
-          float best = -INFINITY;
-          int bi = INT_MAX;
-#pragma unroll
-          for (int i = 0; i < kH; ++i)
-            if (i < vh && v[i] > best) { best = v[i]; bi = i; }
-          part = make_float2(best, __int_as_float(bi == INT_MAX ? INT_MAX : n0 + half * kH + bi));
-        } else {
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int i = 0; i < kH; ++i)
-            if (i < vh) m4[i & 3] = fmaxf(m4[i & 3], v[i]);
-          const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int i = 0; i < kH; ++i)
-            if (i < vh) s4[i & 3] += exp2f((v[i] - mx) * c2);
-          part = make_float2(mx * inv_tau, (s4[0] + s4[1]) + (s4[2] + s4[3]));
-        }
+        for (int i = 0; i < kBN; ++i)
+          if (i < valid && v[i] > best) { best = v[i]; bi = i; }
+        // chunks arrive in increasing order: a strict > keeps the lowest index on ties
+        if (best > best_key) { best_key = best; best_c = n0 + bi; }
       } else {
-        // residual / bonus masses of this half row, 32 columns at a time
-        constexpr int kH = kBN / 2;
-        const RowMeta rm = meta[m];
-        const uint8_t* ub = sU + half * kUHalf + m * 128;              // U rows, this half
-        const uint8_t* tb = sU + 2 * kUHalf + half * kUHalf + m * 128; // target rows, this half
-        const int vh = valid - half * kH;
-        float R = 0.f, P = 0.f;
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int q = 0; q < kH / 32; ++q) {
-          float v[32];
-          tc::tmem_ld32(taddr + half * kH + q * 32, reinterpret_cast<uint32_t*>(v));
-          tc::tmem_ld_wait();
+        for (int i = 0; i < kBN; ++i)
+          if (i < valid) m4[i & 3] = fmaxf(m4[i & 3], v[i]);
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int j4 = 0; j4 < 4; ++j4) {
-            const int j = q * 4 + j4;  // 16-byte chunk within the half row
-            const uint32_t off = ((j ^ (m & 7)) << 4);
-            float xu[8], xt[8];
-            unpack8(*reinterpret_cast<const uint4*>(ub + off), xu);
-            unpack8(*reinterpret_cast<const uint4*>(tb + off), xt);
+        for (int i = 0; i < kBN; ++i)
+          if (i < valid) s4[i & 3] += exp2f((v[i] - mx) * c2);
+        const float sc = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        float g;
+        if (i < kGReg) {
+          g = gk[0];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int i = 8 * j + e;
-              const float pt = exp2f(fmaf(xt[e], c2, -rm.a_t));
-              const float pd = exp2f(fmaf(v[8 * j4 + e] + xu[e], c2, -rm.a_d));
-              const float w = rm.resid ? fmaxf(0.f, pt - pd) : pt;
-              if (i < vh && rm.live) {
-                R += w;
-                P += pt;
-              }
+          for (int j = 0; j + 1 < kGReg; ++j) gk[j] = gk[j + 1];
+        } else {
+          g = chunk_gumbel_call(p.seed, p.step, grow, p.k, c);
+        }
+        if (mx > -INFINITY) {
+          const float key = mx * inv_tau + logf(sc) + g;  // chunk log-mass + Gumbel
+          if (key > best_key) { best_key = key; best_c = c; }
+          const float m2 = mx * c2;
+          if (m2 > run_m) {
+            run_s = run_s * exp2f(run_m - m2) + sc;
+            run_m = m2;
+          } else {
+            run_s += sc * exp2f(m2 - run_m);
+          }
+        }
+      }
+    }
+    run_m *= 0.69314718055994531f;  // back to natural units: max of l / T
+    // the two warp sets of a lane quarter meet in shared memory after the final barrier
+    if (half == 1) bar->xch[m] = make_float4(run_m, run_s, best_key, __int_as_float(best_c));
+    xmine = make_float4(run_m, run_s, best_key, __int_as_float(best_c));
+  } else if (kDecide && warp >= 2 && warp < 2 + epi_warps<kDecide>()) {
+    // ------------------------------------------------------------------ DECIDE epilogue
+    const int wq = warp & 3;          // TMEM lane quarter this warp may access
+    const int m = wq * 32 + lane;     // tile row = TMEM lane
+    const int half = (warp - 2) >> 2; // which 64 of the 128 columns this warp takes
+    const int grow = m0 + m;
+    const float inv_tau = p.inv_tau;
+    const float c2 = inv_tau * kLog2e;
+    int uph = 0, ab = 0, aph = 0;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int c = c0 + t * cstride;
+      const int n0 = c * kBN;
+      const int valid = min(kBN, V - n0);
+      bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[ab]), aph, deadline, abort_flag) &&
+                tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[half]), uph, deadline, abort_flag);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(p.status, DSPARK_ETIMEOUT);
+        break;
+      }
+      tc::tc_fence_after();
+      const uint32_t taddr = tmem_base + (uint32_t(wq * 32) << 16) + ab * kBN;
+      // residual / bonus masses of this half row, 32 columns at a time
+      constexpr int kH = kBN / 2;
+      const RowMeta rm = meta[m];
+      const uint8_t* ub = sU + half * kUHalf + m * 128;              // U rows, this half
+      const uint8_t* tb = sU + 2 * kUHalf + half * kUHalf + m * 128; // target rows, this half
+      const int vh = valid - half * kH;
+      float R = 0.f, P = 0.f;
+#pragma unroll
+      for (int q = 0; q < kH / 32; ++q) {
+        float v[32];
+        tc::tmem_ld32(taddr + half * kH + q * 32, reinterpret_cast<uint32_t*>(v));
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int j4 = 0; j4 < 4; ++j4) {
+          const int j = q * 4 + j4;  // 16-byte chunk within the half row
+          const uint32_t off = ((j ^ (m & 7)) << 4);
+          float xu[8], xt[8];
+          unpack8(*reinterpret_cast<const uint4*>(ub + off), xu);
+          unpack8(*reinterpret_cast<const uint4*>(tb + off), xt);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int i = 8 * j + e;
+            const float pt = exp2f(fmaf(xt[e], c2, -rm.a_t));
+            const float pd = exp2f(fmaf(v[8 * j4 + e] + xu[e], c2, -rm.a_d));
+            const float w = rm.resid ? fmaxf(0.f, pt - pd) : pt;
+            if (i < vh && rm.live) {
+              R += w;
+              P += pt;
             }
           }
         }
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[ab]));
-          tc::mbar_arrive(tc::smem_u32(&bar->u_empty[half]));
-        }
-        part = make_float2(R, P);
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[ab]));
+        tc::mbar_arrive(tc::smem_u32(&bar->u_empty[half]));
       }
       if (++ab == kAccBufs) { ab = 0; aph ^= 1; }
-      if (!kDecide) {
-        if (++us == kUStages) { us = 0; uph ^= 1; }
-      } else {
-        uph ^= 1;  // DECIDE: each half's stage is refilled every tile
-      }
-      if (grow < bs) p.stats[(size_t(grow) * p.n_chunks + c) * kStatsPerChunk + half] = part;
+      uph ^= 1;  // each half's stage is refilled every tile
+      if (grow < bs) p.stats[(size_t(grow) * p.n_chunks + c) * kStatsPerChunk + half] = make_float2(R, P);
     }
   }
 
@@ -502,6 +578,15 @@ __global__ void __launch_bounds__(threads<kDecide>(), 1) stats_tc_kernel(
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem_base, kTmemCols);
+  }
+  if (!kDecide && warp >= 2 && warp < 6) {
+    // DRAFT: warp set 0 merges the other set's entry of the same row and writes the CTA's
+    // entry (request grow, slot c0) -- see DraftEntry
+    const int m = (warp & 3) * 32 + lane, grow = m0 + m;
+    const float4 o = bar->xch[m];
+    const LsePair l = lse_merge(LsePair{xmine.x, xmine.y}, LsePair{o.x, o.y});
+    const ArgMax a = better(ArgMax{xmine.z, __float_as_int(xmine.w)}, ArgMax{o.z, __float_as_int(o.w)});
+    if (grow < bs) p.entries[size_t(grow) * p.n_slots + c0] = make_float4(l.m, l.s, a.v, __int_as_float(a.i));
   }
 }
 
@@ -551,6 +636,14 @@ bool encode_w2(CUtensorMap* map, const void* W2t, int V, int r) {
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Persistent grid: one CTA per SM, a whole number of CTAs per 128-request M-tile, at most one
+// per (M-tile, chunk).  CTA b takes M-tile b % n_mt and chunks b / n_mt + j * (grid / n_mt).
+int grid_size(int bs, int n_chunks) {
+  const int n_mt = (bs + kBM - 1) / kBM;
+  const int grid = (sm_count() / n_mt) * n_mt;
+  return max(n_mt, min(grid, n_mt * n_chunks));
+}
+
 template <bool kDecide>
 cudaError_t launch(const CUtensorMap& w2, const CUtensorMap& u, const Params& prm, cudaStream_t s) {
   const size_t smem = smem_bytes<kDecide>(prm.r);
@@ -568,9 +661,7 @@ cudaError_t launch(const CUtensorMap& w2, const CUtensorMap& u, const Params& pr
       attr_set[dev] = true;
     }
   }
-  const int n_mt = (prm.bs + kBM - 1) / kBM;
-  int grid = (sm_count() / n_mt) * n_mt;
-  grid = min(grid, n_mt * prm.n_chunks);
+  const int grid = grid_size(prm.bs, prm.n_chunks);
   // programmatic dependent launch: set-up and prefetch overlap the previous kernel's tail
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -596,8 +687,9 @@ bool draft_tc_supported(int dtype, int bs, int V, int r) {
 
 cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t,
                                   const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
-                                  int V, int r, int k, float inv_tau, int greedy, void* stats,
-                                  int n_chunks, uint32_t* status, cudaStream_t s) {
+                                  int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
+                                  uint64_t step, void* entries, int n_chunks, int* n_slots,
+                                  uint32_t* status, cudaStream_t s) {
   if (!encode_fn()) return cudaErrorNotSupported;
   CUtensorMap map_w2, map_u;
   if (!encode_w2(&map_w2, W2t, V, r)) return cudaErrorInvalidValue;
@@ -618,10 +710,14 @@ cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t
   prm.bs = bs; prm.gamma = gamma; prm.V = V; prm.r = r; prm.k = k;
   prm.inv_tau = inv_tau;
   prm.greedy = greedy;
-  prm.stats = static_cast<float2*>(stats);
   prm.n_chunks = n_chunks;
   prm.status = status;
   prm.timeout_ns = g_wait_timeout_ns;
+  prm.entries = static_cast<float4*>(entries);
+  prm.n_slots = grid_size(bs, n_chunks) / ((bs + kBM - 1) / kBM);
+  prm.seed = seed;
+  prm.step = step;
+  *n_slots = prm.n_slots;
   return launch<false>(map_w2, map_u, prm, s);
 }
 

@@ -7,18 +7,20 @@
 namespace dspark {
 
 // ---- S1 draft ---------------------------------------------------------------------------
-// Per-(row, chunk) statistics of l_k = U_k + W1[x_{k-1}] W2 for one position k:
-//   temperature > 0: (max t, sum exp(t - max)) with t = l * inv_tau
-//   temperature = 0: (max l, lowest argmax as int bits)
+// Partial draws of l_k = U_k + W1[x_{k-1}] W2 for one position k: per (row, slot) a
+// DraftEntry (common.cuh) over the slot's chunks.  The CUDA-core pass has one slot per chunk
+// (n_slots = n_chunks).
 cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, const void* W2t,
                                     const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
-                                    int V, int r, int k, float inv_tau, int greedy, void* stats,
-                                    int n_chunks, cudaStream_t s);
-// Same statistics on the tensor cores (tcgen05 + TMEM + TMA), bf16 only.
+                                    int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
+                                    uint64_t step, void* entries, int n_chunks, cudaStream_t s);
+// Same on the tensor cores (tcgen05 + TMEM + TMA), bf16 only: one slot per CTA column
+// (n_slots <= n_chunks, returned).
 cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t,
                                   const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
-                                  int V, int r, int k, float inv_tau, int greedy, void* stats,
-                                  int n_chunks, uint32_t* status, cudaStream_t s);
+                                  int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
+                                  uint64_t step, void* entries, int n_chunks, int* n_slots,
+                                  uint32_t* status, cudaStream_t s);
 bool draft_tc_supported(int dtype, int bs, int V, int r);
 // Verify's decision masses on the tensor cores (bf16): per (request, chunk) the residual mass
 // sum max(0, p_t - p_d) and the target mass sum p_t of the request's deciding row.
@@ -28,8 +30,8 @@ cudaError_t launch_decision_stats_tc(const void* target, const void* U, const vo
                                      float inv_tau, void* stats, int n_chunks, uint32_t* status,
                                      cudaStream_t s);
 extern uint64_t g_wait_timeout_ns;  // deadline of device-side waits (dspark_set_wait_timeout_ns)
-// Merge the chunk statistics of one position and draw x_k.
-cudaError_t launch_draft_select(int dtype, const void* stats, int n_chunks, const void* U,
+// Merge the n_slots entries of each row of one position and draw x_k.
+cudaError_t launch_draft_select(int dtype, const void* entries, int n_slots, const void* U,
                                 const void* W1, const void* W2t, const int32_t* anchor,
                                 int32_t* tokens, float* logit_x, float* lse, int bs, int gamma,
                                 int V, int r, int k, float inv_tau, int greedy, uint64_t seed,

@@ -67,6 +67,21 @@ def test_draft_parity_full_size_sampled_rows():
         compare_draft(tg[rows], lg[rows], sg[rows], to, lo, so, mo, "bf16", greedy=temperature == 0.0)
 
 
+def test_draft_parity_long_vocabulary_sampled_rows():
+    """V = 213000 (1665 chunks, ragged last chunk) at bs = 136: a tensor-core CTA takes 22
+    chunks, more than its warp sets draw Gumbels for up front, and the second 128-request
+    M-tile is ragged."""
+    wl = I.WORKLOADS["mixed_bs256"].with_(name="long_vocab", bs=136, gamma=2, V=213000, seed=21)
+    inp = I.make_device_inputs(wl, "cuda", with_target=False, with_hidden=False)
+    rows = np.array([0, 67, 127, 128, 135])
+    for temperature in (1.0, 0.0):
+        tg, lg, sg = _draft_gpu(inp, temperature, wl.seed, 9)
+        U = to_np(inp["U"][torch.as_tensor(rows, device="cuda")])
+        to, lo, so, mo = O.draft_block(U, to_np(inp["W1"]), to_np(inp["W2t"]), to_np(inp["anchor"])[rows],
+                                       temperature, wl.seed, 9, dtype="bf16", req_ids=rows)
+        compare_draft(tg[rows], lg[rows], sg[rows], to, lo, so, mo, "bf16", greedy=temperature == 0.0)
+
+
 @pytest.mark.parametrize("name,d", [("tiny_fp32", 64), ("bf16_ragged", 4096)])
 def test_confidence_parity(name, d):
     wl = SMALL[name].with_(d=d, bs=24)
