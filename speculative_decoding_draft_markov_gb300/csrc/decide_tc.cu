@@ -1,0 +1,446 @@
+// Verify's decision masses on the tensor cores (bf16): for each request's deciding row, per
+// 64-id half chunk, the residual mass sum max(0, p_t - p_d) and the target mass sum p_t.
+//
+// DSpark technical summary, "Verification": a rejected draft token is replaced by a sample of
+// normalise(max(0, p_t - p_d)) at the rejected position, and a fully accepted block takes a
+// bonus token from p_t.  p_d there is the draft distribution softmax((U_k + W1[x_{k-1}] W2)/T)
+// at the rejected position k, so the pass recomputes those logits with one GEMM
+// [bs, r] x [r, V] (rows of requests whose decision is a bonus or absent use a zero A row).
+// No [bs, V] tensor reaches HBM: the masses are reduced in the epilogue.
+//
+// Work decomposition (one persistent CTA per SM, as in the draft pass):
+//   tile      = 128 requests (TMEM lanes) x 64 vocabulary ids (one half chunk), K = r
+//   warp 0    = TMA producer: W2t tiles [64 ids x 64 K] in a ring of K-stages (evict-last)
+//   warp 1    = TMEM owner + single-thread tcgen05.mma issuer: the r-long K loop, then four
+//               MMAs with A = the gathered U tile and B = a 64 x 64 identity, which add U
+//               into the accumulator (exact products; zero terms add nothing)
+//   warps 2-9 = epilogue, two warp sets of four (one per TMEM lane quarter); set h takes the
+//               tiles t = h, h + 2, ...: accumulator buffer h and gather stage h
+//   warps 10-13 = cp.async gather of the U rows and target rows of each tile, two warps per
+//               stage (64 rows each), so one stage refills while the other is reduced
+// Every mbarrier wait is bounded (SM cycle-counter deadline + shared abort flag); on give-up the
+// kernel records DSPARK_ETIMEOUT, waits (bounded) for its own copies / MMAs in flight, frees
+// TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_host.h"
+#include "tc_ptx.cuh"
+
+namespace dspark {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 64;                             // ids per tile: one half chunk
+constexpr int kBK = 64;                             // K per stage: one 128-byte swizzle row
+constexpr int kBStages = 8;                         // W2t K-stages (two tiles of K = 256)
+constexpr int kStages = 2;                          // (U, target) gather stages
+constexpr int kAccBufs = 2;
+constexpr int kEpiWarps = 8;
+constexpr int kGatherWarps = 4;
+constexpr int kThreads = 32 * (2 + kEpiWarps + kGatherWarps);
+constexpr uint32_t kAAtom = kBM * kBK * 2;          // 16 KB: A rows [128 x 64 K]
+constexpr uint32_t kBAtom = kBN * kBK * 2;          // 8 KB: W2t rows [64 x 64 K]
+constexpr uint32_t kRowsTile = kBM * kBN * 2;       // 16 KB: [128 rows x 64 ids] bf16
+constexpr uint32_t kStageBytes = 2 * kRowsTile;     // U tile | target tile
+constexpr uint32_t kTmemCols = 128;                 // 2 accumulators x 64 columns
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Bars {
+  uint64_t b_full[kBStages], b_empty[kBStages];
+  uint64_t s_full[kStages], s_empty[kStages];
+  uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int xrow[kBM];  // W1 row of each A row (-1: zero row)
+};
+
+// Per-row facts (one request per tile row).
+struct RowMeta {
+  long long u_off;  // element offset of U[b, kdec-1, 0] (residual rows)
+  long long t_off;  // element offset of target[pdec, 0] (live rows)
+  float a_t;        // lse_t * log2(e)
+  float a_d;        // lse_d * log2(e)
+  int resid;        // residual row (else bonus, or dead)
+  int live;         // the request has a decision
+};
+
+struct Params {
+  const __nv_bfloat16* W1;
+  const __nv_bfloat16* U;
+  const __nv_bfloat16* target;
+  const int32_t* anchor;
+  const int32_t* tokens;
+  const float* lse_d;
+  const RowStat* rs;
+  const Decision* dec;
+  int bs, gamma, V, r;
+  float inv_tau;
+  float2* stats;  // [bs][2 * n_chunks] half-chunk (R, P)
+  int n_chunks;
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+// Dynamic shared memory: A atoms | W2t ring | gather stages | identity | row facts | barriers.
+constexpr size_t kSmemBytes = 4 * size_t(kAAtom) + kBStages * size_t(kBAtom) + kStages * size_t(kStageBytes) +
+                              size_t(kBAtom) + kBM * sizeof(RowMeta) + sizeof(Bars);
+static_assert(kSmemBytes <= 232448, "dynamic shared memory beyond the 227 KB per-block limit");
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ void unpack8(const uint4 q, float* x) {
+  x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
+  x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
+                                                                 const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (tc::smem_u32(smem_raw) & 1023u) {  // the swizzled layouts need 1024-byte alignment
+    if (threadIdx.x == 0) set_status(p.status, DSPARK_EUNSUPPORTED);
+    return;
+  }
+  const int nk = p.r / kBK;
+  uint8_t* sA = smem_raw;                          // nk A atoms
+  uint8_t* sB = sA + 4 * kAAtom;                   // W2t ring
+  uint8_t* sS = sB + kBStages * kBAtom;            // gather stages: U tile | target tile
+  uint8_t* sI = sS + kStages * kStageBytes;        // identity atom [64 x 64]
+  RowMeta* meta = reinterpret_cast<RowMeta*>(sI + kBAtom);
+  Bars* bar = reinterpret_cast<Bars*>(meta + kBM);
+  volatile int* abort_flag = &bar->abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bs = p.bs, V = p.V, r = p.r;
+  const int n_mt = (bs + kBM - 1) / kBM;
+  const int m0 = (blockIdx.x % n_mt) * kBM;
+  const int cstride = gridDim.x / n_mt;
+  const int c0 = blockIdx.x / n_mt;
+  const int n_ct = (c0 < p.n_chunks) ? (p.n_chunks - c0 + cstride - 1) / cstride : 0;
+  const int n_tiles = 2 * n_ct;  // tile t: chunk c0 + (t / 2) * cstride, half t % 2
+
+  if (tid == 0) {
+    for (int s = 0; s < kBStages; ++s) {
+      tc::mbar_init(tc::smem_u32(&bar->b_full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&bar->b_empty[s]), 1);
+    }
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(tc::smem_u32(&bar->s_full[s]), 2);      // the two gather warps of the stage
+      tc::mbar_init(tc::smem_u32(&bar->s_empty[s]), 4 + 1); // the epilogue set + the U MMAs' commit
+    }
+    for (int s = 0; s < kAccBufs; ++s) {
+      tc::mbar_init(tc::smem_u32(&bar->acc_full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&bar->acc_empty[s]), 4);
+    }
+    tc::mbar_init(tc::smem_u32(&bar->drain), 1);
+    bar->abort = 0;
+    tc::fence_mbar_init();
+    tc::prefetch_tensormap(&tmap_w2);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(&bar->tmem_base), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  {  // identity B operand [64 rows n x 64 K], K-major, 128-byte swizzle
+    uint4* z = reinterpret_cast<uint4*>(sI);
+    for (int i = tid; i < int(kBAtom) / 16; i += kThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    for (int n = tid; n < kBN; n += kThreads) {
+      const int j = n >> 3, e = n & 7;
+      reinterpret_cast<uint16_t*>(sI + n * 128 + ((j ^ (n & 7)) << 4))[e] = 0x3F80u;  // bf16 1.0
+    }
+    tc::fence_proxy_async_smem();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = bar->tmem_base;
+  const long long deadline = tc::deadline_after_ns(p.timeout_ns);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    // W2t does not depend on the previous kernel: the ring fills while the others wait for it.
+    if (lane == 0) {
+      const uint64_t keep = tc::policy_evict_last();
+      int bstage = 0, bph = 0;
+      int b_issued[kBStages];
+      for (int s = 0; s < kBStages; ++s) b_issued[s] = -1;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int n0 = (c0 + (t >> 1) * cstride) * kChunk + (t & 1) * kBN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->b_empty[bstage]), bph ^ 1, deadline, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bfull = tc::smem_u32(&bar->b_full[bstage]);
+          tc::mbar_arrive_expect_tx(bfull, kBAtom);
+          tc::tma_load_2d(tc::smem_u32(sB + bstage * kBAtom), &tmap_w2, bfull, kb * kBK, n0, keep);
+          b_issued[bstage] = bph;
+          if (++bstage == kBStages) { bstage = 0; bph ^= 1; }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(p.status, DSPARK_ETIMEOUT);
+        // wait (bounded) for every copy this thread put in flight before the CTA exits
+        const long long dl = tc::deadline_after_ns(200000000ull);
+        const volatile int never = 0;
+        for (int s = 0; s < kBStages; ++s)
+          if (b_issued[s] >= 0) tc::mbar_wait_bounded(tc::smem_u32(&bar->b_full[s]), b_issued[s], dl, &never);
+      }
+    }
+    return;  // takes no part in the named barrier below
+  }
+
+  // ---------------------------------------------------------------- everyone else: row facts + A
+  tc::grid_dependency_wait();  // the decisions come from the previous kernel
+  constexpr int kRest = kThreads - 32;
+  const int rt = tid - 32;
+  for (int m = rt; m < kBM; m += kRest) {
+    RowMeta rm{0, 0, 0.f, 0.f, 0, 0};
+    int xp = -1;
+    const int grow = m0 + m;
+    if (grow < bs) {
+      const Decision d = p.dec[grow];
+      if (d.kind != kDecNone) {
+        rm.live = 1;
+        rm.t_off = (long long)d.pdec * V;
+        rm.a_t = p.rs[d.pdec].lse * kLog2e;
+        if (d.kind == kDecResidual) {
+          rm.resid = 1;
+          rm.u_off = ((long long)grow * p.gamma + d.kdec - 1) * V;
+          rm.a_d = p.lse_d[(size_t)grow * p.gamma + d.kdec - 1] * kLog2e;
+          xp = clamp_token((d.kdec == 1) ? p.anchor[grow] : p.tokens[size_t(grow) * p.gamma + d.kdec - 2], V);
+        }
+      }
+    }
+    meta[m] = rm;
+    bar->xrow[m] = xp;
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kRest) : "memory");
+  {  // A operand: W1[x] of each residual row (zero rows otherwise), 128-byte-swizzled K-major
+    const int cpr = r / 8;
+    for (int idx = rt; idx < kBM * cpr; idx += kRest) {
+      const int row = idx / cpr, ch = idx % cpr;
+      const int xp = bar->xrow[row];
+      const int kb = ch >> 3, j = ch & 7;
+      const uint32_t dst = tc::smem_u32(sA + kb * kAAtom + row * 128 + ((j ^ (row & 7)) << 4));
+      cp_async16(dst, xp >= 0 ? p.W1 + size_t(xp) * r + ch * 8 : p.W1, xp >= 0 ? 16u : 0u);
+    }
+    cp_async_wait_all();
+    tc::fence_proxy_async_smem();
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kRest) : "memory");
+
+  if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
+      int bstage = 0, bph = 0;
+      bool ok = true, issued = false;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int ab = t & 1, ph = (t >> 1) & 1;  // accumulator buffer and gather stage = t % 2
+        if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_empty[ab]), ph ^ 1, deadline, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t d = tmem_base + ab * kBN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->b_full[bstage]), bph, deadline, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t a_addr = tc::smem_u32(sA + kb * kAAtom);
+          const uint32_t b_addr = tc::smem_u32(sB + bstage * kBAtom);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc::mma_bf16(d, tc::sdesc_kmajor_sw128(a_addr + kk * 32), tc::sdesc_kmajor_sw128(b_addr + kk * 32),
+                         idesc, (kb | kk) != 0);
+          issued = true;
+          tc::mma_commit(tc::smem_u32(&bar->b_empty[bstage]));
+          if (++bstage == kBStages) { bstage = 0; bph ^= 1; }
+        }
+        if (!ok) break;
+        // D += U I (the gathered U tile of the stage; zero rows for non-residual requests)
+        if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->s_full[ab]), ph, deadline, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t u_addr = tc::smem_u32(sS + ab * kStageBytes);
+        const uint32_t i_addr = tc::smem_u32(sI);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          tc::mma_bf16(d, tc::sdesc_kmajor_sw128(u_addr + kk * 32), tc::sdesc_kmajor_sw128(i_addr + kk * 32), idesc, 1);
+        tc::mma_commit(tc::smem_u32(&bar->s_empty[ab]));
+        tc::mma_commit(tc::smem_u32(&bar->acc_full[ab]));
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(p.status, DSPARK_ETIMEOUT);
+        if (issued) {  // wait (bounded) for the MMAs already issued before TMEM is freed
+          tc::mma_commit(tc::smem_u32(&bar->drain));
+          const volatile int never = 0;
+          tc::mbar_wait_bounded(tc::smem_u32(&bar->drain), 0, tc::deadline_after_ns(200000000ull), &never);
+        }
+      }
+    }
+  } else if (warp >= 2 + kEpiWarps) {
+    // ------------------------------------------------------------------ row gather
+    // Stage s (tiles t = s, s + 2, ...) is filled by gather warps s and s + 2, rows 64 * (g >> 1)
+    // .. + 63 each: the tile's U rows (residual rows) and target rows (live rows).  The warp waits
+    // for its own copies and fences them for the tensor core before arriving.
+    const int g = warp - (2 + kEpiWarps);
+    const int s = g & 1, rbase = (g >> 1) * 64;
+    const int j = lane & 7, rsub = lane >> 3;  // 16-byte group in the 128-byte row, row within 4
+    const uint32_t su = tc::smem_u32(sS + s * kStageBytes), st = su + kRowsTile;
+    bool ok = true;
+    for (int t = s, i = 0; t < n_tiles; t += 2, ++i) {
+      if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->s_empty[s]), (i & 1) ^ 1, deadline, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const int col = (c0 + (t >> 1) * cstride) * kChunk + (t & 1) * kBN + j * 8;
+      const bool in_v = col < V;
+#pragma unroll 4
+      for (int it = 0; it < 64 / 4; ++it) {
+        const int row = rbase + it * 4 + rsub;
+        const RowMeta rm = meta[row];
+        const uint32_t off = row * 128 + ((j ^ (row & 7)) << 4);
+        const bool gu = rm.resid && in_v, gt = rm.live && in_v;
+        cp_async16(su + off, gu ? p.U + rm.u_off + col : p.U, gu ? 16u : 0u);
+        cp_async16(st + off, gt ? p.target + rm.t_off + col : p.target, gt ? 16u : 0u);
+      }
+      cp_async_wait_all();
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->s_full[s]));
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      set_status(p.status, DSPARK_ETIMEOUT);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int wq = warp & 3;           // TMEM lane quarter this warp may access
+    const int m = wq * 32 + lane;      // tile row = TMEM lane
+    const int set = (warp - 2) >> 2;   // tiles t = set, set + 2, ...
+    const int grow = m0 + m;
+    const float c2 = p.inv_tau * kLog2e;
+    const RowMeta rm = meta[m];
+    const uint32_t taddr = tmem_base + (uint32_t(wq * 32) << 16) + set * kBN;
+    const uint8_t* tb = sS + set * kStageBytes + kRowsTile + m * 128;  // this row's target values
+    for (int t = set, i = 0; t < n_tiles; t += 2, ++i) {
+      const int c = c0 + (t >> 1) * cstride;
+      const int valid = min(kBN, V - (c * kChunk + (t & 1) * kBN));  // may be <= 0 past V
+      bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[set]), i & 1, deadline, abort_flag) &&
+                tc::mbar_wait_bounded(tc::smem_u32(&bar->s_full[set]), i & 1, deadline, abort_flag);
+      // one decision per warp before the .sync.aligned TMEM loads
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(p.status, DSPARK_ETIMEOUT);
+        break;
+      }
+      tc::tc_fence_after();
+      float l[kBN];  // draft logits U + W1[x] W2 of this row (residual rows)
+      tc::tmem_ld32(taddr, reinterpret_cast<uint32_t*>(l));
+      tc::tmem_ld32(taddr + 32, reinterpret_cast<uint32_t*>(l + 32));
+      tc::tmem_ld_wait();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[set]));
+      float R = 0.f, P = 0.f;
+      if (rm.live) {
+        float R4[4] = {0.f, 0.f, 0.f, 0.f}, P4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int jj = 0; jj < kBN / 8; ++jj) {
+          float x[8];
+          unpack8(*reinterpret_cast<const uint4*>(tb + ((jj ^ (m & 7)) << 4)), x);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int q = 8 * jj + e;
+            const float pt = tc::ex2_approx(fmaf(x[e], c2, -rm.a_t));
+            const float pd = tc::ex2_approx(fmaf(l[q], c2, -rm.a_d));
+            const float w = rm.resid ? fmaxf(0.f, pt - pd) : pt;
+            if (valid == kBN || q < valid) {
+              R4[e & 3] += w;
+              P4[e & 3] += pt;
+            }
+          }
+        }
+        R = (R4[0] + R4[1]) + (R4[2] + R4[3]);
+        P = (P4[0] + P4[1]) + (P4[2] + P4[3]);
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->s_empty[set]));
+      if (grow < bs) p.stats[(size_t(grow) * p.n_chunks + c) * kStatsPerChunk + (t & 1)] = make_float2(R, P);
+    }
+  }
+
+  tc::tc_fence_before();
+  asm volatile("bar.sync 1, %0;" ::"n"(kRest) : "memory");
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decision_stats_tc(const void* target, const void* U, const void* W1, const void* W2t,
+                                     const int32_t* anchor, const int32_t* tokens, const float* lse_d,
+                                     const void* rs, const void* dec, int bs, int gamma, int V, int r,
+                                     float inv_tau, void* stats, int n_chunks, uint32_t* status,
+                                     cudaStream_t s) {
+  if (!tch::encode_fn()) return cudaErrorNotSupported;
+  if (r % kBK != 0 || r > 256) return cudaErrorInvalidValue;
+  CUtensorMap map_w2;
+  if (!tch::encode_bf16_2d(&map_w2, W2t, size_t(V), size_t(r), kBN)) return cudaErrorInvalidValue;
+  static bool smem_set[tch::kMaxDevices] = {};
+  static std::mutex smem_mu;
+  if (cudaError_t e = tch::set_smem_once(decide_tc_kernel, int(kSmemBytes), smem_set, &smem_mu)) return e;
+  Params prm{};
+  prm.W1 = static_cast<const __nv_bfloat16*>(W1);
+  prm.U = static_cast<const __nv_bfloat16*>(U);
+  prm.target = static_cast<const __nv_bfloat16*>(target);
+  prm.anchor = anchor;
+  prm.tokens = tokens;
+  prm.lse_d = lse_d;
+  prm.rs = static_cast<const RowStat*>(rs);
+  prm.dec = static_cast<const Decision*>(dec);
+  prm.bs = bs; prm.gamma = gamma; prm.V = V; prm.r = r;
+  prm.inv_tau = inv_tau;
+  prm.stats = static_cast<float2*>(stats);
+  prm.n_chunks = n_chunks;
+  prm.status = status;
+  prm.timeout_ns = g_wait_timeout_ns;
+  // programmatic dependent launch: barrier set-up, TMEM and the W2t ring overlap the previous
+  // kernel's tail
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tch::vocab_grid(bs, n_chunks));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decide_tc_kernel, map_w2, prm);
+}
+
+}  // namespace dspark

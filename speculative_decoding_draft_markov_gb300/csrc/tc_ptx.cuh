@@ -101,6 +101,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Hardware base-2 exponential (MUFU), flushing subnormal results to zero: the epilogues sum
+// terms 2^x with x <= 0 whose subnormal values do not matter next to the leading term 1.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------------------------- tcgen05
 // Allocate / free `ncols` TMEM columns (power of two >= 32); one full warp executes these.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
