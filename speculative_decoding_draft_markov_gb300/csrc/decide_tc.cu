@@ -1,5 +1,5 @@
 // Verify's decision masses on the tensor cores (bf16): for each request's deciding row, per
-// 64-id half chunk, the residual mass sum max(0, p_t - p_d) and the target mass sum p_t.
+// 128-id chunk, the residual mass sum max(0, p_t - p_d) and the target mass sum p_t.
 //
 // DSpark technical summary, "Verification": a rejected draft token is replaced by a sample of
 // normalise(max(0, p_t - p_d)) at the rejected position, and a fully accepted block takes a
@@ -9,11 +9,12 @@
 // No [bs, V] tensor reaches HBM: the masses are reduced in the epilogue.
 //
 // Work decomposition (one persistent CTA per SM, as in the draft pass):
-//   tile      = 128 requests (TMEM lanes) x 64 vocabulary ids (one half chunk), K = r
-//   warp 0    = TMA producer: W2t tiles [64 ids x 64 K] in a ring of K-stages (evict-last)
-//   warp 1    = TMEM owner + single-thread tcgen05.mma issuer: the r-long K loop, then four
-//               MMAs with A = the gathered U tile and B = a 64 x 64 identity, which add U
-//               into the accumulator (exact products; zero terms add nothing)
+//   tile      = 128 requests (TMEM lanes) x 128 vocabulary ids (one chunk), K = r
+//   A operand = W1[x] of each residual request, held in tensor memory (tcgen05.st by the
+//               first epilogue warp set; 128 columns), which leaves shared memory to two
+//               (U, target) gather stages
+//   warp 0    = TMA producer: W2t tiles [128 ids x 64 K] in a ring of K-stages (evict-last)
+//   warp 1    = TMEM owner + single-thread tcgen05.mma issuer (A from TMEM, B from smem)
 //   warps 2-9 = epilogue, two warp sets of four (one per TMEM lane quarter); set h takes the
 //               tiles t = h, h + 2, ...: accumulator buffer h and gather stage h
 //   warps 10-13 = cp.async gather of the U rows and target rows of each tile, two warps per
@@ -37,19 +38,19 @@ namespace dspark {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBN = 64;                             // ids per tile: one half chunk
+constexpr int kBN = 128;                            // ids per tile: one chunk
 constexpr int kBK = 64;                             // K per stage: one 128-byte swizzle row
-constexpr int kBStages = 8;                         // W2t K-stages (two tiles of K = 256)
+constexpr int kBStages = 4;                         // W2t K-stages (one tile of K = 256)
 constexpr int kStages = 2;                          // (U, target) gather stages
 constexpr int kAccBufs = 2;
 constexpr int kEpiWarps = 8;
-constexpr int kGatherWarps = 4;
+constexpr int kGatherWarps = 2 * kStages;           // two per stage
 constexpr int kThreads = 32 * (2 + kEpiWarps + kGatherWarps);
-constexpr uint32_t kAAtom = kBM * kBK * 2;          // 16 KB: A rows [128 x 64 K]
-constexpr uint32_t kBAtom = kBN * kBK * 2;          // 8 KB: W2t rows [64 x 64 K]
-constexpr uint32_t kRowsTile = kBM * kBN * 2;       // 16 KB: [128 rows x 64 ids] bf16
-constexpr uint32_t kStageBytes = 2 * kRowsTile;     // U tile | target tile
-constexpr uint32_t kTmemCols = 128;                 // 2 accumulators x 64 columns
+constexpr uint32_t kBAtom = kBN * kBK * 2;          // 16 KB: W2t rows [128 x 64 K]
+constexpr uint32_t kHalf = kBM * 64 * 2;            // 16 KB: [128 rows x 64 ids] bf16
+constexpr uint32_t kStageBytes = 4 * kHalf;         // U tile (two halves) | target tile (two halves)
+constexpr uint32_t kTmemCols = 512;                 // 2 accumulators x 128 + A (128) -> 512
+constexpr uint32_t kTmemA = kAccBufs * kBN;         // first column of A
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Bars {
@@ -57,9 +58,9 @@ struct Bars {
   uint64_t s_full[kStages], s_empty[kStages];
   uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
   uint64_t drain;
+  uint64_t a_ready;  // A is in TMEM (one arrival per warp of epilogue set 0)
   uint32_t tmem_base;
   int abort;
-  int xrow[kBM];  // W1 row of each A row (-1: zero row)
 };
 
 // Per-row facts (one request per tile row).
@@ -89,9 +90,9 @@ struct Params {
   uint64_t timeout_ns;
 };
 
-// Dynamic shared memory: A atoms | W2t ring | gather stages | identity | row facts | barriers.
-constexpr size_t kSmemBytes = 4 * size_t(kAAtom) + kBStages * size_t(kBAtom) + kStages * size_t(kStageBytes) +
-                              size_t(kBAtom) + kBM * sizeof(RowMeta) + sizeof(Bars);
+// Dynamic shared memory: W2t ring | gather stages | row facts | barriers.
+constexpr size_t kSmemBytes =
+    kBStages * size_t(kBAtom) + kStages * size_t(kStageBytes) + kBM * sizeof(RowMeta) + sizeof(Bars);
 static_assert(kSmemBytes <= 232448, "dynamic shared memory beyond the 227 KB per-block limit");
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
@@ -112,11 +113,9 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
     return;
   }
   const int nk = p.r / kBK;
-  uint8_t* sA = smem_raw;                          // nk A atoms
-  uint8_t* sB = sA + 4 * kAAtom;                   // W2t ring
-  uint8_t* sS = sB + kBStages * kBAtom;            // gather stages: U tile | target tile
-  uint8_t* sI = sS + kStages * kStageBytes;        // identity atom [64 x 64]
-  RowMeta* meta = reinterpret_cast<RowMeta*>(sI + kBAtom);
+  uint8_t* sB = smem_raw;                          // W2t ring
+  uint8_t* sS = sB + kBStages * kBAtom;            // gather stages
+  RowMeta* meta = reinterpret_cast<RowMeta*>(sS + kStages * kStageBytes);
   Bars* bar = reinterpret_cast<Bars*>(meta + kBM);
   volatile int* abort_flag = &bar->abort;
 
@@ -126,8 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
   const int m0 = (blockIdx.x % n_mt) * kBM;
   const int cstride = gridDim.x / n_mt;
   const int c0 = blockIdx.x / n_mt;
-  const int n_ct = (c0 < p.n_chunks) ? (p.n_chunks - c0 + cstride - 1) / cstride : 0;
-  const int n_tiles = 2 * n_ct;  // tile t: chunk c0 + (t / 2) * cstride, half t % 2
+  const int n_tiles = (c0 < p.n_chunks) ? (p.n_chunks - c0 + cstride - 1) / cstride : 0;
 
   if (tid == 0) {
     for (int s = 0; s < kBStages; ++s) {
@@ -135,14 +133,15 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
       tc::mbar_init(tc::smem_u32(&bar->b_empty[s]), 1);
     }
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(tc::smem_u32(&bar->s_full[s]), 2);      // the two gather warps of the stage
-      tc::mbar_init(tc::smem_u32(&bar->s_empty[s]), 4 + 1); // the epilogue set + the U MMAs' commit
+      tc::mbar_init(tc::smem_u32(&bar->s_full[s]), 2);   // the two gather warps of the stage
+      tc::mbar_init(tc::smem_u32(&bar->s_empty[s]), 4);  // the epilogue set of the stage
     }
     for (int s = 0; s < kAccBufs; ++s) {
       tc::mbar_init(tc::smem_u32(&bar->acc_full[s]), 1);
       tc::mbar_init(tc::smem_u32(&bar->acc_empty[s]), 4);
     }
     tc::mbar_init(tc::smem_u32(&bar->drain), 1);
+    tc::mbar_init(tc::smem_u32(&bar->a_ready), 4);
     bar->abort = 0;
     tc::fence_mbar_init();
     tc::prefetch_tensormap(&tmap_w2);
@@ -150,16 +149,6 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
   if (warp == 1) {
     tc::tmem_alloc(tc::smem_u32(&bar->tmem_base), kTmemCols);
     tc::tmem_relinquish();
-  }
-  {  // identity B operand [64 rows n x 64 K], K-major, 128-byte swizzle
-    uint4* z = reinterpret_cast<uint4*>(sI);
-    for (int i = tid; i < int(kBAtom) / 16; i += kThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
-    __syncthreads();
-    for (int n = tid; n < kBN; n += kThreads) {
-      const int j = n >> 3, e = n & 7;
-      reinterpret_cast<uint16_t*>(sI + n * 128 + ((j ^ (n & 7)) << 4))[e] = 0x3F80u;  // bf16 1.0
-    }
-    tc::fence_proxy_async_smem();
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -177,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
       for (int s = 0; s < kBStages; ++s) b_issued[s] = -1;
       bool ok = true;
       for (int t = 0; t < n_tiles && ok; ++t) {
-        const int n0 = (c0 + (t >> 1) * cstride) * kChunk + (t & 1) * kBN;
+        const int n0 = (c0 + t * cstride) * kBN;
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->b_empty[bstage]), bph ^ 1, deadline, abort_flag)) {
             ok = false;
@@ -200,16 +189,14 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
           if (b_issued[s] >= 0) tc::mbar_wait_bounded(tc::smem_u32(&bar->b_full[s]), b_issued[s], dl, &never);
       }
     }
-    return;  // takes no part in the named barrier below
+    return;  // takes no part in the named barriers below
   }
 
-  // ---------------------------------------------------------------- everyone else: row facts + A
+  // ---------------------------------------------------------------- everyone else: row facts
   tc::grid_dependency_wait();  // the decisions come from the previous kernel
   constexpr int kRest = kThreads - 32;
-  const int rt = tid - 32;
-  for (int m = rt; m < kBM; m += kRest) {
+  for (int m = tid - 32; m < kBM; m += kRest) {
     RowMeta rm{0, 0, 0.f, 0.f, 0, 0};
-    int xp = -1;
     const int grow = m0 + m;
     if (grow < bs) {
       const Decision d = p.dec[grow];
@@ -221,25 +208,10 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
           rm.resid = 1;
           rm.u_off = ((long long)grow * p.gamma + d.kdec - 1) * V;
           rm.a_d = p.lse_d[(size_t)grow * p.gamma + d.kdec - 1] * kLog2e;
-          xp = clamp_token((d.kdec == 1) ? p.anchor[grow] : p.tokens[size_t(grow) * p.gamma + d.kdec - 2], V);
         }
       }
     }
     meta[m] = rm;
-    bar->xrow[m] = xp;
-  }
-  asm volatile("bar.sync 1, %0;" ::"n"(kRest) : "memory");
-  {  // A operand: W1[x] of each residual row (zero rows otherwise), 128-byte-swizzled K-major
-    const int cpr = r / 8;
-    for (int idx = rt; idx < kBM * cpr; idx += kRest) {
-      const int row = idx / cpr, ch = idx % cpr;
-      const int xp = bar->xrow[row];
-      const int kb = ch >> 3, j = ch & 7;
-      const uint32_t dst = tc::smem_u32(sA + kb * kAAtom + row * 128 + ((j ^ (row & 7)) << 4));
-      cp_async16(dst, xp >= 0 ? p.W1 + size_t(xp) * r + ch * 8 : p.W1, xp >= 0 ? 16u : 0u);
-    }
-    cp_async_wait_all();
-    tc::fence_proxy_async_smem();
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kRest) : "memory");
 
@@ -248,9 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
       int bstage = 0, bph = 0;
-      bool ok = true, issued = false;
+      bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->a_ready), 0, deadline, abort_flag);
+      bool issued = false;
+      tc::tc_fence_after();
       for (int t = 0; t < n_tiles && ok; ++t) {
-        const int ab = t & 1, ph = (t >> 1) & 1;  // accumulator buffer and gather stage = t % 2
+        const int ab = t & 1, ph = (t >> 1) & 1;  // accumulator buffer t % 2 and its phase
         if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_empty[ab]), ph ^ 1, deadline, abort_flag)) {
           ok = false;
           break;
@@ -263,29 +237,16 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
             break;
           }
           tc::tc_fence_after();
-          const uint32_t a_addr = tc::smem_u32(sA + kb * kAAtom);
           const uint32_t b_addr = tc::smem_u32(sB + bstage * kBAtom);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            tc::mma_bf16(d, tc::sdesc_kmajor_sw128(a_addr + kk * 32), tc::sdesc_kmajor_sw128(b_addr + kk * 32),
-                         idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < kBK / 16; ++kk)  // A columns: 8 per 16 K values
+            tc::mma_bf16_ts(d, tmem_base + kTmemA + kb * (kBK / 2) + kk * 8,
+                            tc::sdesc_kmajor_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
           issued = true;
           tc::mma_commit(tc::smem_u32(&bar->b_empty[bstage]));
           if (++bstage == kBStages) { bstage = 0; bph ^= 1; }
         }
         if (!ok) break;
-        // D += U I (the gathered U tile of the stage; zero rows for non-residual requests)
-        if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->s_full[ab]), ph, deadline, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc::tc_fence_after();
-        const uint32_t u_addr = tc::smem_u32(sS + ab * kStageBytes);
-        const uint32_t i_addr = tc::smem_u32(sI);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          tc::mma_bf16(d, tc::sdesc_kmajor_sw128(u_addr + kk * 32), tc::sdesc_kmajor_sw128(i_addr + kk * 32), idesc, 1);
-        tc::mma_commit(tc::smem_u32(&bar->s_empty[ab]));
         tc::mma_commit(tc::smem_u32(&bar->acc_full[ab]));
       }
       if (!ok) {
@@ -301,31 +262,31 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
   } else if (warp >= 2 + kEpiWarps) {
     // ------------------------------------------------------------------ row gather
     // Stage s (tiles t = s, s + 2, ...) is filled by gather warps s and s + 2, rows 64 * (g >> 1)
-    // .. + 63 each: the tile's U rows (residual rows) and target rows (live rows).  The warp waits
-    // for its own copies and fences them for the tensor core before arriving.
+    // .. + 63 each: the tile's U rows (residual rows) and target rows (live rows), both halves.
+    // Only CUDA-core loads read the stages, so the warp waits for its own copies and arrives.
     const int g = warp - (2 + kEpiWarps);
     const int s = g & 1, rbase = (g >> 1) * 64;
-    const int j = lane & 7, rsub = lane >> 3;  // 16-byte group in the 128-byte row, row within 4
-    const uint32_t su = tc::smem_u32(sS + s * kStageBytes), st = su + kRowsTile;
+    const int j = lane & 7, rsub = lane >> 3;  // 16-byte group in a 128-byte half row, row within 4
+    const uint32_t su = tc::smem_u32(sS + s * kStageBytes), st = su + 2 * kHalf;
     bool ok = true;
     for (int t = s, i = 0; t < n_tiles; t += 2, ++i) {
       if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->s_empty[s]), (i & 1) ^ 1, deadline, abort_flag)) {
         ok = false;
         break;
       }
-      const int col = (c0 + (t >> 1) * cstride) * kChunk + (t & 1) * kBN + j * 8;
-      const bool in_v = col < V;
-#pragma unroll 4
-      for (int it = 0; it < 64 / 4; ++it) {
-        const int row = rbase + it * 4 + rsub;
+      const int n0 = (c0 + t * cstride) * kBN;
+#pragma unroll 2
+      for (int it = 0; it < 2 * 64 / 4; ++it) {
+        const int h = it & 1, row = rbase + (it >> 1) * 4 + rsub;
+        const int col = n0 + h * 64 + j * 8;
+        const bool in_v = col < V;
         const RowMeta rm = meta[row];
-        const uint32_t off = row * 128 + ((j ^ (row & 7)) << 4);
+        const uint32_t off = h * kHalf + row * 128 + ((j ^ (row & 7)) << 4);
         const bool gu = rm.resid && in_v, gt = rm.live && in_v;
         cp_async16(su + off, gu ? p.U + rm.u_off + col : p.U, gu ? 16u : 0u);
         cp_async16(st + off, gt ? p.target + rm.t_off + col : p.target, gt ? 16u : 0u);
       }
       cp_async_wait_all();
-      tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->s_full[s]));
     }
@@ -341,11 +302,36 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
     const int grow = m0 + m;
     const float c2 = p.inv_tau * kLog2e;
     const RowMeta rm = meta[m];
-    const uint32_t taddr = tmem_base + (uint32_t(wq * 32) << 16) + set * kBN;
-    const uint8_t* tb = sS + set * kStageBytes + kRowsTile + m * 128;  // this row's target values
+    const uint32_t lane_base = tmem_base + (uint32_t(wq * 32) << 16);
+    if (set == 0) {
+      // A operand into TMEM: this row's W1[x] (zero unless the request's decision is a
+      // residual), 64 K values (32 columns) per store
+      int xp = -1;
+      if (rm.resid) {
+        const Decision d = p.dec[grow];
+        xp = clamp_token((d.kdec == 1) ? p.anchor[grow] : p.tokens[size_t(grow) * p.gamma + d.kdec - 2], V);
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(p.W1 + size_t(xp < 0 ? 0 : xp) * r);
+      for (int kb = 0; kb < nk; ++kb) {
+        uint32_t a32[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 w = xp >= 0 ? src[kb * 8 + q] : make_uint4(0u, 0u, 0u, 0u);
+          a32[4 * q + 0] = w.x; a32[4 * q + 1] = w.y; a32[4 * q + 2] = w.z; a32[4 * q + 3] = w.w;
+        }
+        tc::tmem_st32(lane_base + kTmemA + kb * 32, a32);
+      }
+      tc::tmem_st_wait();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->a_ready));
+    }
+    const uint32_t taddr = lane_base + set * kBN;
+    const uint8_t* ub = sS + set * kStageBytes + m * 128;  // U row in the stage (+ h * kHalf)
+    const uint8_t* tb = ub + 2 * kHalf;                     // target row
     for (int t = set, i = 0; t < n_tiles; t += 2, ++i) {
-      const int c = c0 + (t >> 1) * cstride;
-      const int valid = min(kBN, V - (c * kChunk + (t & 1) * kBN));  // may be <= 0 past V
+      const int c = c0 + t * cstride;
+      const int valid = min(kBN, V - c * kBN);
       bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[set]), i & 1, deadline, abort_flag) &&
                 tc::mbar_wait_bounded(tc::smem_u32(&bar->s_full[set]), i & 1, deadline, abort_flag);
       // one decision per warp before the .sync.aligned TMEM loads
@@ -356,38 +342,46 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
         break;
       }
       tc::tc_fence_after();
-      float l[kBN];  // draft logits U + W1[x] W2 of this row (residual rows)
-      tc::tmem_ld32(taddr, reinterpret_cast<uint32_t*>(l));
-      tc::tmem_ld32(taddr + 32, reinterpret_cast<uint32_t*>(l + 32));
-      tc::tmem_ld_wait();
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[set]));
-      float R = 0.f, P = 0.f;
-      if (rm.live) {
-        float R4[4] = {0.f, 0.f, 0.f, 0.f}, P4[4] = {0.f, 0.f, 0.f, 0.f};
+      float R4[4] = {0.f, 0.f, 0.f, 0.f}, P4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int jj = 0; jj < kBN / 8; ++jj) {
-          float x[8];
-          unpack8(*reinterpret_cast<const uint4*>(tb + ((jj ^ (m & 7)) << 4)), x);
+      for (int h = 0; h < 2; ++h) {  // 64 columns at a time
+        float l[64];  // W1[x] W2 part of the draft logits (residual rows)
+        tc::tmem_ld32(taddr + h * 64, reinterpret_cast<uint32_t*>(l));
+        tc::tmem_ld32(taddr + h * 64 + 32, reinterpret_cast<uint32_t*>(l + 32));
+        tc::tmem_ld_wait();
+        if (h == 1) {
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[set]));
+        }
+        if (rm.live) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int q = 8 * jj + e;
-            const float pt = tc::ex2_approx(fmaf(x[e], c2, -rm.a_t));
-            const float pd = tc::ex2_approx(fmaf(l[q], c2, -rm.a_d));
-            const float w = rm.resid ? fmaxf(0.f, pt - pd) : pt;
-            if (valid == kBN || q < valid) {
-              R4[e & 3] += w;
-              P4[e & 3] += pt;
+          for (int jj = 0; jj < 8; ++jj) {
+            const uint32_t off = h * kHalf + ((jj ^ (m & 7)) << 4);
+            float xu[8], xt[8];
+            unpack8(*reinterpret_cast<const uint4*>(ub + off), xu);
+            unpack8(*reinterpret_cast<const uint4*>(tb + off), xt);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int q = h * 64 + 8 * jj + e;
+              const float pt = tc::ex2_approx(fmaf(xt[e], c2, -rm.a_t));
+              const float pd = tc::ex2_approx(fmaf(l[8 * jj + e] + xu[e], c2, -rm.a_d));
+              const float w = rm.resid ? fmaxf(0.f, pt - pd) : pt;
+              if (valid == kBN || q < valid) {
+                R4[e & 3] += w;
+                P4[e & 3] += pt;
+              }
             }
           }
         }
-        R = (R4[0] + R4[1]) + (R4[2] + R4[3]);
-        P = (P4[0] + P4[1]) + (P4[2] + P4[3]);
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->s_empty[set]));
-      if (grow < bs) p.stats[(size_t(grow) * p.n_chunks + c) * kStatsPerChunk + (t & 1)] = make_float2(R, P);
+      if (grow < bs) {
+        float2* e2 = p.stats + (size_t(grow) * p.n_chunks + c) * kStatsPerChunk;
+        e2[0] = make_float2((R4[0] + R4[1]) + (R4[2] + R4[3]), (P4[0] + P4[1]) + (P4[2] + P4[3]));
+        e2[1] = make_float2(0.f, 0.f);
+      }
     }
   }
 

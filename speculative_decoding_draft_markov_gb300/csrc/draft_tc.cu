@@ -13,13 +13,12 @@
 //               chunks; the gathered A operand W1[x_{k-1}] (128 x r) stays in shared memory
 //   warp 0    = TMA producer: W2t tiles in K-stages of 64 (evict-last) and the U_k tile
 //               (3-D map over [bs, gamma, V], evict-first)
-//   warp 1    = TMEM owner + single-thread tcgen05.mma issuer, commits to mbarriers.  After
-//               the K loop over r, eight more MMAs with A = the U_k tile and B = a 128 x 128
-//               identity add U_k into the accumulator (D += U_k I; every product is exact and
-//               the zero terms add nothing), so the epilogue reads finished logits.
+//   warp 1    = TMEM owner + single-thread tcgen05.mma issuer, commits to mbarriers
 //   warps 2-9 = epilogue, two warp sets of four (one warp per TMEM lane quarter, one request
 //               row per thread).  Set h takes the tiles t = h, h + 2, ... (accumulator buffer
-//               h): per full chunk it forms the chunk's log-mass and Gumbel key and keeps, in
+//               h, U stage h): it adds U_k to the accumulator row (adding U_k on the tensor
+//               core through an identity operand costs more tensor-pipe time than these adds
+//               cost issue slots), forms each chunk's log-mass and Gumbel key and keeps, in
 //               registers, the row's running (max, sum-exp) and best key.  Each CTA writes one
 //               entry per request at the end, so the select merges one entry per CTA column.
 //   2 TMEM accumulators (256 columns) let MMA, loads and epilogue overlap.
@@ -44,7 +43,7 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kBK = 64;
-constexpr int kBStages = 4;                      // W2t ring: one tile of K = 256
+constexpr int kBStages = 6;                      // W2t ring: 1.5 tiles of K = 256
 constexpr int kUStages = 2;
 constexpr int kAccBufs = 2;
 constexpr int kEpiWarps = 8;
@@ -82,11 +81,11 @@ struct Params {
   uint64_t seed, step;
 };
 
-// Dynamic shared memory: A atoms | W2t ring | U stages | identity atoms | barriers.  The buffer
-// is declared 1024-byte aligned (128-byte swizzle atoms).
+// Dynamic shared memory: A atoms | W2t ring | U stages | barriers.  The buffer is declared
+// 1024-byte aligned (128-byte swizzle atoms).
 constexpr size_t smem_bytes(int r) {
   return size_t(r / kBK) * kAtomBytes + kBStages * size_t(kAtomBytes) + kUStages * 2 * size_t(kUHalf) +
-         2 * size_t(kAtomBytes) + sizeof(Barriers);
+         sizeof(Barriers);
 }
 static_assert(smem_bytes(256) <= 232448, "dynamic shared memory beyond the 227 KB per-block limit");
 
@@ -137,8 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
   uint8_t* sA = smem_raw;                    // nk atoms
   uint8_t* sB = sA + nk * kAtomBytes;        // kBStages atoms
   uint8_t* sU = sB + kBStages * kAtomBytes;  // kUStages x 32 KB
-  uint8_t* sI = sU + kUStages * 2 * kUHalf;  // identity: 2 atoms
-  Barriers* bar = reinterpret_cast<Barriers*>(sI + 2 * kAtomBytes);
+  Barriers* bar = reinterpret_cast<Barriers*>(sU + kUStages * 2 * kUHalf);
   volatile int* abort_flag = &bar->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -156,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     }
     for (int s = 0; s < kUStages; ++s) {
       tc::mbar_init(tc::smem_u32(&bar->u_full[s]), 1);
-      tc::mbar_init(tc::smem_u32(&bar->u_empty[s]), 1);  // the commit after the U_k MMAs
+      tc::mbar_init(tc::smem_u32(&bar->u_empty[s]), kEpiWarps / 2);  // the warp set of the stage
     }
     for (int s = 0; s < kAccBufs; ++s) {
       tc::mbar_init(tc::smem_u32(&bar->acc_full[s]), 1);
@@ -172,18 +170,6 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
   if (warp == 1) {
     tc::tmem_alloc(tc::smem_u32(&bar->tmem_base), kTmemCols);
     tc::tmem_relinquish();
-  }
-  {
-    // identity B operand: atom h holds rows n = 0..127 of columns k = 64h..64h+63 of I, K-major
-    // with the 128-byte swizzle (16-byte group j of row n at position j ^ (n & 7))
-    uint4* z = reinterpret_cast<uint4*>(sI);
-    for (int i = tid; i < 2 * int(kAtomBytes) / 16; i += kThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
-    __syncthreads();
-    for (int n = tid; n < kBM; n += kThreads) {
-      const int h = n >> 6, k = n & 63, j = k >> 3, e = k & 7;
-      reinterpret_cast<uint16_t*>(sI + h * kAtomBytes + n * 128 + ((j ^ (n & 7)) << 4))[e] = 0x3F80u;  // 1.0
-    }
-    tc::fence_proxy_async_smem();
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -244,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
-      int bstage = 0, bph = 0, ab = 0, aph = 0, us = 0, uph = 0;
+      int bstage = 0, bph = 0, ab = 0, aph = 0;
       bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->a_ready), 0, deadline, abort_flag);
       bool issued = false;
       for (int t = 0; t < n_tiles && ok; ++t) {
@@ -271,23 +257,6 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
           if (++bstage == kBStages) { bstage = 0; bph ^= 1; }
         }
         if (!ok) break;
-        // D += U_k I, 64 columns of U_k (one swizzled half) at a time
-        if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[us]), uph, deadline, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc::tc_fence_after();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t u_addr = tc::smem_u32(sU + us * 2 * kUHalf + h * kUHalf);
-          const uint32_t i_addr = tc::smem_u32(sI + h * kAtomBytes);
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            tc::mma_bf16(d, tc::sdesc_kmajor_sw128(u_addr + kk * 32), tc::sdesc_kmajor_sw128(i_addr + kk * 32),
-                         idesc, 1);
-        }
-        tc::mma_commit(tc::smem_u32(&bar->u_empty[us]));
-        if (++us == kUStages) { us = 0; uph ^= 1; }
         tc::mma_commit(tc::smem_u32(&bar->acc_full[ab]));
         if (++ab == kAccBufs) { ab = 0; aph ^= 1; }
       }
@@ -352,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->a_ready));
 
     const uint32_t taddr = tmem_base + (uint32_t(wq * 32) << 16) + half * kBN;
+    const uint8_t* ub = sU + half * 2 * kUHalf + m * 128;  // this row in U stage `half`
     // running (max, sum-exp) in log2 units: run_m = max of l c2, run_s = sum of 2^(l c2 - run_m)
     float run_m = -INFINITY, run_s = 0.f, best_key = -INFINITY;
     int best_c = INT_MAX;
@@ -360,7 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
       const int c = c0 + t * cstride;
       const int n0 = c * kBN;
       const int valid = min(kBN, V - n0);
-      bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[half]), ph, deadline, abort_flag);
+      bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[half]), ph, deadline, abort_flag) &&
+                tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[half]), ph, deadline, abort_flag);
       // one decision per warp before the .sync.aligned TMEM loads; warps run independently
       // (no named barrier in this loop), so a warp that gives up can hold up no other
       ok = __all_sync(0xFFFFFFFFu, ok);
@@ -377,6 +348,16 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[half]));
+#pragma unroll
+      for (int j = 0; j < kBN / 8; ++j) {  // + U_k: 16-byte groups of the tile's two 64-column halves
+        const uint4 q = *reinterpret_cast<const uint4*>(ub + (j >> 3) * kUHalf + (((j & 7) ^ (m & 7)) << 4));
+        v[8 * j + 0] += bf16lo(q.x); v[8 * j + 1] += bf16hi(q.x);
+        v[8 * j + 2] += bf16lo(q.y); v[8 * j + 3] += bf16hi(q.y);
+        v[8 * j + 4] += bf16lo(q.z); v[8 * j + 5] += bf16hi(q.z);
+        v[8 * j + 6] += bf16lo(q.w); v[8 * j + 7] += bf16hi(q.w);
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->u_empty[half]));
 
       if (p.greedy) {
         float best = -INFINITY;
