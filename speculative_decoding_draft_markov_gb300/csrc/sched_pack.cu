@@ -94,14 +94,44 @@ cudaError_t launch_confidence(int dtype, const void* h, const void* W1, const in
 // verification, "DSpark confidence scheduling mechanism": tau counts one extra token per
 // request plus the survival of the admitted slots.
 // One block of 1024 threads.  64-bit keys (descending fp32 survival bits, then slot index
-// r * gamma + j) are sorted by a merge tree: each request's gamma keys are sorted by one
-// thread (they normally arrive sorted already, survival being non-increasing), then
-// ceil(log2 bs) levels merge pairs of runs, every key finding its output position by a binary
-// search in the partner run.  Then exact int64 fixed-point prefix sums of floor(a * 2^40),
+// r * gamma + j) are sorted by a merge tree: each request's keys form one run, sorted by one
+// thread (they normally arrive sorted already, survival being non-increasing) and padded to a
+// power of two with sentinels, then ceil(log2 bs) levels merge pairs of runs, every key
+// finding its output position by a binary search in the partner run.  Then exact int64 fixed-point prefix sums of floor(a * 2^40),
 // Theta in fp64 with one rounding per product, block reductions for the stop / argmax.
 // ---------------------------------------------------------------------------------------
 constexpr int kSchedThreads = 1024;
 constexpr int kSchedMaxSlots = 4096;
+
+// floor(a * 2^40) of a non-negative fp32 value from its bits, in integer arithmetic (the fp64
+// pipe of this part is narrow): a = (m | 2^23) 2^(e - 150), so a 2^40 = (m | 2^23) 2^(e - 110).
+// Exact for a < 2^23; zero for subnormal a (a 2^40 < 1).
+__device__ __forceinline__ long long fix40(uint32_t bits) {
+  const int e = int((bits >> 23) & 0xFFu);
+  if (e == 0) return 0;
+  const unsigned long long mm = (bits & 0x7FFFFFu) | 0x800000u;
+  const int sh = e - 110;
+  if (sh >= 0) return static_cast<long long>(mm << (sh < 22 ? sh : 22));
+  return sh <= -24 ? 0ll : static_cast<long long>(mm >> (-sh));
+}
+
+// T 2^-40 as a double for an integer 2^40 <= T < 2^53: exact, built from the bits (T has at most
+// 53 significant bits, and the scale only lowers the exponent).
+__device__ __forceinline__ double scaled_fixed(long long T) {
+  const int e = 63 - __clzll(T);  // floor(log2 T), 40 .. 52
+  const unsigned long long mant = (static_cast<unsigned long long>(T) << (52 - e)) & ((1ull << 52) - 1);
+  return __longlong_as_double(static_cast<long long>((static_cast<unsigned long long>(e + 1023 - 40) << 52) | mant));
+}
+
+// Order-preserving 64-bit integer of a non-NaN double (-0 maps with +0).
+__device__ __forceinline__ long long dkey(double x) {
+  long long b = __double_as_longlong(x);
+  if (b == static_cast<long long>(0x8000000000000000ull)) b = 0;
+  return b >= 0 ? b : (b ^ 0x7FFFFFFFFFFFFFFFll);
+}
+__device__ __forceinline__ bool dnan(double x) {
+  return (static_cast<unsigned long long>(__double_as_longlong(x)) & 0x7FFFFFFFFFFFFFFFull) > 0x7FF0000000000000ull;
+}
 
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
     const float* __restrict__ surv, int bs, int gamma, const double* __restrict__ sps, int m_max,
@@ -111,7 +141,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   __shared__ unsigned short slot[kSchedMaxSlots];
   __shared__ long long wsum[32];
   __shared__ int red_k[32];
-  __shared__ double red_t[32];
+  __shared__ long long red_v[32];
   __shared__ int win[DSPARK_MAX_BS];
   __shared__ int s_kstar;
   const int tid = threadIdx.x;
@@ -119,23 +149,36 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   unsigned long long* src = sched_buf;
   unsigned long long* dst = sched_buf + kSchedMaxSlots;
 
-  // runs of length gamma, one request per thread: written as they come, then put in order in
-  // place (insertion sort in shared memory) in the rare case a row is not already sorted
-  for (int r = tid; r < bs; r += kSchedThreads) {
+  // Power-of-two layout: request r owns the run [r gp, (r + 1) gp), gp = gamma rounded up to a
+  // power of two, over bp = bs rounded up; the padding holds sentinel keys above every real key
+  // (survival 0 has high word 0xFFFFFFFF, real slot indices are below 4096).  Runs are written
+  // as they come and put in order in place (insertion sort) in the rare case a row is not
+  // already sorted.
+  int lg_gp = 0;
+  while ((1 << lg_gp) < gamma) ++lg_gp;
+  int lg_n = lg_gp;
+  while ((1 << (lg_n - lg_gp)) < bs) ++lg_n;
+  const int gp = 1 << lg_gp, N = 1 << lg_n;
+  for (int r = tid; r < (N >> lg_gp); r += kSchedThreads) {
+    unsigned long long* run = src + (r << lg_gp);
     bool sorted = true;
     unsigned long long prev = 0;
-    for (int j = 0; j < gamma; ++j) {
-      const int e = r * gamma + j;
-      uint32_t bits = __float_as_uint(surv[e]);
-      if (bits & 0x80000000u) bits = 0u;  // -0 and negatives rank as 0
-      const unsigned long long x = (static_cast<unsigned long long>(0xFFFFFFFFu - bits) << 32) | static_cast<unsigned>(e);
+    for (int j = 0; j < gp; ++j) {
+      unsigned long long x;
+      if (r < bs && j < gamma) {
+        const int e = r * gamma + j;
+        uint32_t bits = __float_as_uint(surv[e]);
+        if (bits & 0x80000000u) bits = 0u;  // -0 and negatives rank as 0
+        x = (static_cast<unsigned long long>(0xFFFFFFFFu - bits) << 32) | static_cast<unsigned>(e);
+      } else {
+        x = (0xFFFFFFFFull << 32) | static_cast<unsigned>(kSchedMaxSlots + (r << lg_gp) + j);
+      }
       sorted = sorted && (j == 0 || x > prev);
       prev = x;
-      src[e] = x;
+      run[j] = x;
     }
     if (!sorted) {
-      unsigned long long* run = src + r * gamma;
-      for (int j = 1; j < gamma; ++j) {
+      for (int j = 1; j < gp; ++j) {
         const unsigned long long x = run[j];
         int i = j;
         while (i > 0 && run[i - 1] > x) {
@@ -148,18 +191,33 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   }
   for (int e = tid; e < DSPARK_MAX_BS; e += kSchedThreads) win[e] = 0;
   __syncthreads();
-  // merge levels: runs [i*len, min((i+1)*len, n)) pairwise into runs of 2*len
-  for (int len = gamma; len < n; len <<= 1) {
-    for (int p = tid; p < n; p += kSchedThreads) {
-      const int run = p / len, idx = p - run * len;
-      const unsigned long long x = src[p];
-      const int pbeg = (run ^ 1) * len, pend = min(pbeg + len, n);
-      int lo = pbeg, hi = max(pbeg, pend);
-      while (lo < hi) {  // keys are unique: count of partner keys below x
-        const int mid = (lo + hi) >> 1;
-        if (src[mid] < x) lo = mid + 1; else hi = mid;
+  // merge levels: runs of len = 2^lg pairwise into runs of 2 len.  Every key finds its output
+  // position from the count of keys below it in the partner run (keys are unique), by a
+  // fixed-step binary search; a thread advances its up to four keys' searches together.
+  constexpr int kItems = kSchedMaxSlots / kSchedThreads;
+  for (int lg = lg_gp; lg < lg_n; ++lg) {
+    const int len = 1 << lg;
+    unsigned long long x[kItems];
+    int pb[kItems], c[kItems];
+#pragma unroll
+    for (int q = 0; q < kItems; ++q) {
+      const int pos = tid + q * kSchedThreads;
+      x[q] = pos < N ? src[pos] : 0ull;
+      pb[q] = ((pos >> lg) ^ 1) << lg;
+      c[q] = 0;
+    }
+    for (int w = len >> 1; w >= 1; w >>= 1) {
+#pragma unroll
+      for (int q = 0; q < kItems; ++q)
+        if (tid + q * kSchedThreads < N && src[pb[q] + c[q] + w - 1] < x[q]) c[q] += w;
+    }
+#pragma unroll
+    for (int q = 0; q < kItems; ++q) {
+      const int pos = tid + q * kSchedThreads;
+      if (pos < N) {
+        if (src[pb[q] + c[q]] < x[q]) c[q] += 1;
+        dst[((pos >> (lg + 1)) << (lg + 1)) + (pos & (len - 1)) + c[q]] = x[q];
       }
-      dst[min(run, run ^ 1) * len + idx + (lo - pbeg)] = x;
     }
     __syncthreads();
     unsigned long long* t = src;
@@ -177,8 +235,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
     if (i < n) {
       const unsigned long long kv = key[i];
       slot[i] = static_cast<unsigned short>(kv & 0xFFFFFFFFu);
-      const float a = __uint_as_float(0xFFFFFFFFu - static_cast<uint32_t>(kv >> 32));
-      x = static_cast<long long>(static_cast<double>(a) * 1099511627776.0);  // floor(a * 2^40), a >= 0
+      x = fix40(0xFFFFFFFFu - static_cast<uint32_t>(kv >> 32));  // floor(a * 2^40), a >= 0
     }
     run += x;
     v[q] = run;  // inclusive within the thread
@@ -212,37 +269,46 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   __syncthreads();
 
   const int kmax = min(n, m_max - bs);
+  // Theta(K) = tau(K) sps[bs + K], tau(K) = (bs 2^40 + S_K) 2^-40 formed exactly from the bits
+  // (the integer stays below 2^53), so the one fp64 operation is the rounded product.
+  // Candidates compare as order-preserving integers of the doubles; a NaN Theta never wins
+  // and stops the early-stop scan (the host-built tables are finite and non-negative).
   auto theta = [&](int K) -> double {
-    const long long S = (K == 0) ? 0ll : static_cast<long long>(key[K - 1]);
-    const double tau = __dadd_rn(static_cast<double>(bs), __dmul_rn(static_cast<double>(S), 0x1p-40));
-    return __dmul_rn(tau, sps[bs + K]);
+    const long long T = static_cast<long long>(bs) * (1ll << 40) + ((K == 0) ? 0ll : static_cast<long long>(key[K - 1]));
+    return __dmul_rn(scaled_fixed(T), sps[bs + K]);
   };
   int cand = INT_MAX;
-  double best_t = -1.0;
+  long long best_v = LLONG_MIN;
   int best_k = INT_MAX;
   for (int K = tid; K <= kmax; K += kSchedThreads) {
     const double t0 = theta(K);
     if (mode == DSPARK_SCHED_EARLY_STOP) {
-      if (K < kmax && !(theta(K + 1) > t0)) cand = min(cand, K);
-    } else if (t0 > best_t || (t0 == best_t && K < best_k)) {
-      best_t = t0;
-      best_k = K;
+      if (K < kmax) {
+        const double t1 = theta(K + 1);
+        if (dnan(t0) || dnan(t1) || !(dkey(t1) > dkey(t0))) cand = min(cand, K);
+      }
+    } else if (!dnan(t0)) {
+      const long long v0 = dkey(t0);
+      if (v0 > best_v || (v0 == best_v && K < best_k)) {
+        best_v = v0;
+        best_k = K;
+      }
     }
   }
   // block reductions (min for early stop; argmax with lowest K for the global search)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     cand = min(cand, __shfl_xor_sync(0xFFFFFFFFu, cand, o));
-    const double ot = __shfl_xor_sync(0xFFFFFFFFu, best_t, o);
+    const long long ov = __shfl_xor_sync(0xFFFFFFFFu, best_v, o);
     const int ok = __shfl_xor_sync(0xFFFFFFFFu, best_k, o);
-    if (ot > best_t || (ot == best_t && ok < best_k)) {
-      best_t = ot;
+    if (ov > best_v || (ov == best_v && ok < best_k)) {
+      best_v = ov;
       best_k = ok;
     }
   }
   if (lane == 0) {
     red_k[warp] = (mode == DSPARK_SCHED_EARLY_STOP) ? cand : best_k;
-    red_t[warp] = best_t;
+    red_v[warp] = best_v;
   }
   __syncthreads();
   if (tid == 0) {
@@ -252,13 +318,14 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
       for (int i = 0; i < 32; ++i) ks = min(ks, red_k[i]);
       if (ks == INT_MAX) ks = kmax;
     } else {
-      double bt = red_t[0];
+      long long bv = red_v[0];
       ks = red_k[0];
       for (int i = 1; i < 32; ++i)
-        if (red_t[i] > bt || (red_t[i] == bt && red_k[i] < ks)) {
-          bt = red_t[i];
+        if (red_v[i] > bv || (red_v[i] == bv && red_k[i] < ks)) {
+          bv = red_v[i];
           ks = red_k[i];
         }
+      if (ks == INT_MAX) ks = 0;  // every Theta NaN
     }
     s_kstar = ks;
     *K_out = ks;

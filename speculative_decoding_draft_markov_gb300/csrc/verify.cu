@@ -24,7 +24,15 @@ namespace dspark {
 // Row statistics.  16-byte vector loads, per-thread online (max, sum-exp), fixed-order
 // block merge.
 // ---------------------------------------------------------------------------------------
-constexpr int kRowThreads = 512;
+constexpr int kRowThreads = 256;
+
+// Hardware base-2 exponential (relative error near 2^-22; subnormal results flush to zero: the
+// sum's leading term is 1).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 template <typename T>
 __device__ __forceinline__ int load_group(const T* row, int e, float* x);
@@ -90,29 +98,41 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
     }
     return;
   }
-  LsePair acc{-INFINITY, 0.f};
-  constexpr int kBatch = 4;  // independent 16-byte loads in flight per thread
+  // online sum in base 2: m2 = running max of x c2 (c2 = log2(e) / T), s = sum of 2^(x c2 - m2),
+  // rescaled only when a batch of kBatch * G values raises the max
+  const float c2 = inv_tau * 1.4426950408889634f;
+  float m2 = -INFINITY, s2 = 0.f;
+  constexpr int kBatch = 8;  // independent 16-byte loads in flight per thread
   for (int e0 = tid; e0 < ng; e0 += kBatch * kRowThreads) {
     float xb[kBatch][8];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int e = e0 + u * kRowThreads;
-      if (e < ng) load_group<T>(row, e, xb[u]);
-    }
+      if (e < ng) {
+        load_group<T>(row, e, xb[u]);
+      } else {
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      if (e0 + u * kRowThreads >= ng) break;
-      float gm = xb[u][0] * inv_tau;
-#pragma unroll
-      for (int q = 1; q < G; ++q) gm = fmaxf(gm, xb[u][q] * inv_tau);
-      if (gm > acc.m) {
-        acc.s = (acc.s == 0.f) ? 0.f : acc.s * expf(acc.m - gm);
-        acc.m = gm;
+        for (int q = 0; q < 8; ++q) xb[u][q] = -INFINITY;
       }
-#pragma unroll
-      for (int q = 0; q < G; ++q) acc.s += expf(xb[u][q] * inv_tau - acc.m);
     }
+    float bm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+      for (int q = 0; q < G; ++q) bm = fmaxf(bm, xb[u][q]);
+    const float bm2 = bm * c2;
+    if (bm2 > m2) {
+      s2 = (s2 == 0.f) ? 0.f : s2 * ex2_approx(m2 - bm2);
+      m2 = bm2;
+    }
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+      for (int q = 0; q < G; ++q) s4[q & 3] += ex2_approx(fmaf(xb[u][q], c2, -m2));  // 2^-inf = 0
+    s2 += (s4[0] + s4[1]) + (s4[2] + s4[3]);
   }
+  LsePair acc{m2 * 0.69314718055994531f, s2};  // natural units for the block merge
   acc = block_lse<kRowThreads>(acc, sv, ss);
   if (tid == 0) {
     RowStat o{acc.m + logf(acc.s), -INFINITY, -1, 0};

@@ -104,8 +104,11 @@ def _sched_cases():
     for (bs, gamma, seed, ties, kind) in [(4, 7, 0, False, "tiny"), (256, 7, 1, False, "mixed"),
                                           (256, 7, 2, True, "mixed"), (256, 16, 3, False, "wide"),
                                           (1, 1, 4, False, "one"), (33, 5, 5, True, "steep"),
-                                          (128, 15, 6, False, "long"), (64, 7, 7, False, "short")]:
+                                          (128, 15, 6, False, "long"), (64, 7, 7, False, "short"),
+                                          (200, 3, 8, False, "unsorted")]:
         a = I.random_survival(bs, gamma, seed, ties=ties)
+        if kind == "unsorted":  # rows not non-increasing: the per-request runs need sorting
+            a = np.random.default_rng(seed).random((bs, gamma)).astype(np.float32)
         if kind == "tiny":
             sps = O.build_sps(1.0 + 0.002 * np.arange(65), [])
         elif kind == "steep":
