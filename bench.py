@@ -49,20 +49,64 @@ def _peaks():
 
 # ------------------------------------------------------------------------------- clocks
 class ClockSampler:
+    """SM clock and clock-event reasons of the benchmark's GPU, sampled every ~2 ms by a thread
+    during the timed region: NVML read-only queries through ctypes (the device is matched by
+    PCI bus id), else `nvidia-smi -lms 200`.  Nothing is set."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
+    def __init__(self, device):
+        self.device = device
+        self.samples = []  # (sm_mhz, max_mhz, reasons bitmask)
         self.lines = []
+        self.proc = None
+        self.stop = threading.Event()
+        self.nvml = None
+
+    def _nvml_handle(self):
+        import ctypes
+        import torch
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            return None
+        props = torch.cuda.get_device_properties(self.device)
+        h = ctypes.c_void_p()
+        bus = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id, props.pci_device_id)
+        if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+            if nv.nvmlDeviceGetHandleByUUID(("GPU-" + str(props.uuid)).encode(), ctypes.byref(h)) != 0:
+                return None
+        self.reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return nv, h
+
+    def _poll(self):
+        import ctypes
+        nv, h = self.nvml
+        mhz, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if (nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and
+                    nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
+                    self.reason_fn(h, ctypes.byref(rs)) == 0):
+                self.samples.append((mhz.value, mx.value, rs.value))
+            time.sleep(0.002)
 
     def __enter__(self):
         try:
+            self.nvml = self._nvml_handle()
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return self
+        try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                ["nvidia-smi", "-i", str(self.device.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except Exception:
@@ -74,6 +118,9 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
+        self.stop.set()
+        if self.nvml is not None:
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -83,6 +130,10 @@ class ClockSampler:
 
     def summary(self):
         sm, mx, reasons = [], [], set()
+        for s_mhz, m_mhz, bits in self.samples:
+            sm.append(float(s_mhz))
+            mx.append(float(m_mhz))
+            reasons.update(n for b, n in self.REASONS.items() if bits & b)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
@@ -99,7 +150,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvml" if self.samples else "nvidia-smi"}
 
 
 # ------------------------------------------------------------------------------- CPU oracle
@@ -146,6 +197,55 @@ def cpu_baseline(n_req: int = 64, reps: int = 4):
 
 
 # ------------------------------------------------------------------------------- GPU arm
+def draft_block_bytes(bs: int, gamma: int, V: int, r: int, n_sm: int) -> int:
+    """Compulsory HBM bytes of one dspark_draft_block call (bf16), position by position.
+    Vocabulary pass: U_k [bs, V] and W2t [V, r] read once (a GEMM [bs, r] x [r, V] whose
+    operands are consumed as they stream; W2t is re-read by every position because the positions
+    are serially dependent), the gathered A rows W1[x] [bs, r], and the partial-draw entries
+    written (16 bytes per request and CTA column).  Select: the entries read back, the W1 row,
+    the 128 W2t rows and U_k values of the drawn chunk, and the three outputs."""
+    n_mt = (bs + 127) // 128
+    n_slots = (n_sm // n_mt)
+    vocab = bs * V * 2 + V * r * 2 + bs * r * 2 + bs * n_slots * 16
+    select = bs * (n_slots * 16 + r * 2 + 128 * r * 2 + 128 * 2 + 12)
+    return gamma * (vocab + select)
+
+
+def _profiled_traffic():
+    """DRAM bytes of one draft block from the committed ncu summary, or None when the draft
+    kernels' sources changed after that capture (the summary records their SHA-256)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "draft_block_mixed_bs256_dram.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.startswith("- "):
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    h = hashlib.sha256()
+    for f in ("draft_tc.cu", "draft.cu", "common.cuh", "tc_ptx.cuh", "tc_host.h"):
+        h.update(open(os.path.join(ROOT, "speculative_decoding_draft_markov_gb300", "csrc", f), "rb").read())
+    if fields.get("sources_sha256") != h.hexdigest() or "dram_bytes_per_draft_block_gamma7" not in fields:
+        return None
+    return int(fields["dram_bytes_per_draft_block_gamma7"])
+
+
+def aggregate_over_ranks(times_ms, counts, device):
+    """Replica aggregation of the timed region: the slowest rank's durations (MAX) and the work
+    of all ranks (SUM), over the default process group when one with more than one rank is up;
+    the inputs unchanged otherwise."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(x) for x in times_ms], [float(x) for x in counts]
+    t = torch.tensor([float(x) for x in times_ms], dtype=torch.float64, device=device)
+    n = torch.tensor([float(x) for x in counts], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return [float(x) for x in t.tolist()], [float(x) for x in n.tolist()]
+
+
 def run_ours(args, rank: int, world: int):
     import torch
     import torch.distributed as dist
@@ -193,7 +293,8 @@ def run_ours(args, rank: int, world: int):
             tokens_acc.add_((buf.acc_len.to(torch.int64) + 1).sum())
 
     for w in range(args.warmup):
-        step(10_000 + w, False)
+        step(10_000 + w, True)  # every op of the timed loop runs once before it (first-use set-up)
+    tokens_acc.zero_()
     st = B.dspark_read_device_status(buf.ws)
     if st != 0:
         raise RuntimeError("device status after warm-up: " + B.dspark_status_string(st))
@@ -202,7 +303,7 @@ def run_ours(args, rank: int, world: int):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev) as clk:
         t_host = time.perf_counter()
         for it in range(args.steps):
             flush.fill_(it & 0xFF)  # L2 flush, outside the timed segments
@@ -250,19 +351,14 @@ def run_ours(args, rank: int, world: int):
     e2e_ms = float(np.sum(t_e2e))
 
     # aggregate over ranks: max time, summed tokens
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-        n = torch.tensor([tokens, e2e_tokens], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dist.all_reduce(n, op=dist.ReduceOp.SUM)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
-        tokens, e2e_tokens = int(n[0]), int(n[1])
+    (total_ms, e2e_ms), (tokens, e2e_tokens) = aggregate_over_ranks([total_ms, e2e_ms], [tokens, e2e_tokens], dev)
+    tokens, e2e_tokens = int(tokens), int(e2e_tokens)
 
     hbm, bf16, peak_kind = _peaks()
-    n_chunks = (V + 127) // 128
-    draft_bytes = bs * gamma * V * 2 + V * r * 2 + bs * gamma * r * 2 + 2 * gamma * bs * n_chunks * 8
+    draft_bytes = draft_block_bytes(bs, gamma, V, r, torch.cuda.get_device_properties(dev).multi_processor_count)
     draft_ms = float(seg[:, 2].mean())
     achieved = draft_bytes / (draft_ms * 1e-3) / 1e9
+    traffic = _profiled_traffic()
     launches_per_step = 2 * gamma + 3 + (4 if tau > 0 else 2)
     return {
         "metric": METRIC,
@@ -288,8 +384,9 @@ def run_ours(args, rank: int, world: int):
         "stage_ms": {"draft": draft_ms, "conf_sched_pack": float((seg[:, 0] - seg[:, 2]).mean()),
                      "verify": float(seg[:, 1].mean())},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None,
-                     "kernel": "dspark_draft_block (all gamma positions: chunk-statistics + select launches)",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "kernel": "dspark_draft_block: gamma tensor-core vocabulary passes (draft_tc_kernel, "
+                               "the dominant kernel) + gamma selects, one C-ABI call, events around it",
                      "algorithmic_bytes": draft_bytes, "peak_kind": peak_kind},
         "e2e": {"value": e2e_tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},

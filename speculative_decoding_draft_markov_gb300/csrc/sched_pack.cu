@@ -54,9 +54,16 @@ __global__ void __launch_bounds__(512) confidence_kernel(
     const int xp = clamp_token((k == 1) ? anchor[req] : tokens[size_t(req) * gamma + k - 2], V);
     const T* hr = h + (size_t(req) * gamma + warp) * d;
     const T* wr = W1 + size_t(xp) * r;
-    float acc = 0.f;
-    for (int e = lane * 8; e < d; e += 256) acc += dot_chunk8(hr + e, w + e);
-    for (int i = lane; i < r; i += 32) acc = fmaf(w[d + i], ld_f32(wr, i), acc);
+    // four independent partial sums so that four 16-byte loads of h are in flight per lane
+    float a4[4] = {0.f, 0.f, 0.f, 0.f};
+    int e = lane * 8;
+    for (; e + 3 * 256 < d; e += 4 * 256) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a4[u] += dot_chunk8(hr + e + u * 256, w + e + u * 256);
+    }
+    for (; e < d; e += 256) a4[0] += dot_chunk8(hr + e, w + e);
+    float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+    if (lane * 8 < r) acc += dot_chunk8(wr + lane * 8, w + d + lane * 8);  // r is a multiple of 8, <= 256
     acc = warp_sum(acc);
     if (lane == 0) z[warp] = acc + b;
   }
@@ -94,10 +101,8 @@ cudaError_t launch_confidence(int dtype, const void* h, const void* W1, const in
 // verification, "DSpark confidence scheduling mechanism": tau counts one extra token per
 // request plus the survival of the admitted slots.
 // One block of 1024 threads.  64-bit keys (descending fp32 survival bits, then slot index
-// r * gamma + j) are sorted by a merge tree: each request's keys form one run, sorted by one
-// thread (they normally arrive sorted already, survival being non-increasing) and padded to a
-// power of two with sentinels, then ceil(log2 bs) levels merge pairs of runs, every key
-// finding its output position by a binary search in the partner run.  Then exact int64 fixed-point prefix sums of floor(a * 2^40),
+// r * gamma + j) are sorted by a bitonic network held in registers (shuffles for the short
+// distances, shared memory for the long ones).  Then exact int64 fixed-point prefix sums of floor(a * 2^40),
 // Theta in fp64 with one rounding per product, block reductions for the stop / argmax.
 // ---------------------------------------------------------------------------------------
 constexpr int kSchedThreads = 1024;
@@ -133,11 +138,70 @@ __device__ __forceinline__ bool dnan(double x) {
   return (static_cast<unsigned long long>(__double_as_longlong(x)) & 0x7FFFFFFFFFFFFFFFull) > 0x7FF0000000000000ull;
 }
 
+// Sort key of slot e (survival bits descending, then slot index), or a sentinel for e >= n.
+__device__ __forceinline__ unsigned long long sched_key(const float* __restrict__ surv, int e, int n) {
+  if (e >= n) return (0xFFFFFFFFull << 32) | static_cast<unsigned>(kSchedMaxSlots + e);
+  uint32_t bits = __float_as_uint(surv[e]);
+  if (bits & 0x80000000u) bits = 0u;  // -0 and negatives rank as 0
+  return (static_cast<unsigned long long>(0xFFFFFFFFu - bits) << 32) | static_cast<unsigned>(e);
+}
+
+// Ascending bitonic sort of the keys of slots 0 .. 1024 E - 1 by the 1024 threads of the block
+// into out[0 .. 1024 E).  `out` also serves as the exchange buffer of the long distances.
+template <int E>
+__device__ void bitonic_sort(const float* __restrict__ surv, int n, unsigned long long* out, int tid) {
+  constexpr int N = 1024 * E;
+  const int lane = tid & 31;
+  unsigned long long v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = sched_key(surv, tid * E + e, n);
+  for (int k = 2; k <= N; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j < E) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int f = e ^ j;
+          if (f > e) {
+            const bool up = ((tid * E + e) & k) == 0;
+            const unsigned long long lo = v[e] < v[f] ? v[e] : v[f], hi = v[e] < v[f] ? v[f] : v[e];
+            v[e] = up ? lo : hi;
+            v[f] = up ? hi : lo;
+          }
+        }
+      } else if (j < 32 * E) {
+        const int lm = j / E;  // partner lane distance
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = tid * E + e;
+          const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, v[e], lm);
+          const bool keep_min = ((i & k) == 0) == ((lane & lm) == 0);
+          v[e] = keep_min ? (v[e] < o ? v[e] : o) : (v[e] < o ? o : v[e]);
+        }
+      } else {
+        __syncthreads();  // earlier readers of `out` are done
+#pragma unroll
+        for (int e = 0; e < E; ++e) out[tid * E + e] = v[e];
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = tid * E + e;
+          const unsigned long long o = out[i ^ j];
+          const bool keep_min = ((i & k) == 0) == ((i & j) == 0);
+          v[e] = keep_min ? (v[e] < o ? v[e] : o) : (v[e] < o ? o : v[e]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < E; ++e) out[tid * E + e] = v[e];
+}
+
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
     const float* __restrict__ surv, int bs, int gamma, const double* __restrict__ sps, int m_max,
     int mode, int32_t* __restrict__ window, int32_t* __restrict__ K_out,
     double* __restrict__ theta_out) {
-  extern __shared__ unsigned long long sched_buf[];  // two runs buffers of kSchedMaxSlots keys
+  __shared__ unsigned long long sched_buf[kSchedMaxSlots];  // sorted keys, then prefix sums
   __shared__ unsigned short slot[kSchedMaxSlots];
   __shared__ long long wsum[32];
   __shared__ int red_k[32];
@@ -147,83 +211,20 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
   const int tid = threadIdx.x;
   const int n = bs * gamma;
   unsigned long long* src = sched_buf;
-  unsigned long long* dst = sched_buf + kSchedMaxSlots;
 
-  // Power-of-two layout: request r owns the run [r gp, (r + 1) gp), gp = gamma rounded up to a
-  // power of two, over bp = bs rounded up; the padding holds sentinel keys above every real key
-  // (survival 0 has high word 0xFFFFFFFF, real slot indices are below 4096).  Runs are written
-  // as they come and put in order in place (insertion sort) in the rare case a row is not
-  // already sorted.
-  int lg_gp = 0;
-  while ((1 << lg_gp) < gamma) ++lg_gp;
-  int lg_n = lg_gp;
-  while ((1 << (lg_n - lg_gp)) < bs) ++lg_n;
-  const int gp = 1 << lg_gp, N = 1 << lg_n;
-  for (int r = tid; r < (N >> lg_gp); r += kSchedThreads) {
-    unsigned long long* run = src + (r << lg_gp);
-    bool sorted = true;
-    unsigned long long prev = 0;
-    for (int j = 0; j < gp; ++j) {
-      unsigned long long x;
-      if (r < bs && j < gamma) {
-        const int e = r * gamma + j;
-        uint32_t bits = __float_as_uint(surv[e]);
-        if (bits & 0x80000000u) bits = 0u;  // -0 and negatives rank as 0
-        x = (static_cast<unsigned long long>(0xFFFFFFFFu - bits) << 32) | static_cast<unsigned>(e);
-      } else {
-        x = (0xFFFFFFFFull << 32) | static_cast<unsigned>(kSchedMaxSlots + (r << lg_gp) + j);
-      }
-      sorted = sorted && (j == 0 || x > prev);
-      prev = x;
-      run[j] = x;
-    }
-    if (!sorted) {
-      for (int j = 1; j < gp; ++j) {
-        const unsigned long long x = run[j];
-        int i = j;
-        while (i > 0 && run[i - 1] > x) {
-          run[i] = run[i - 1];
-          --i;
-        }
-        run[i] = x;
-      }
-    }
-  }
+  // Bitonic sort of the n keys padded with sentinels (above every real key: survival 0 has high
+  // word 0xFFFFFFFF, real slot indices are below 4096) to N = max(1024, 2^ceil(log2 n)) <= 4096.
+  // Thread t holds keys t E .. t E + E - 1 (E = N / 1024) in registers: exchanges at distance
+  // j < E stay in the thread, j < 32 E go through warp shuffles, longer ones through shared
+  // memory.
+  int lg_n = 10;
+  while ((1 << lg_n) < n) ++lg_n;
+  const int N = 1 << lg_n;
   for (int e = tid; e < DSPARK_MAX_BS; e += kSchedThreads) win[e] = 0;
+  if (N == 1024) bitonic_sort<1>(surv, n, src, tid);
+  else if (N == 2048) bitonic_sort<2>(surv, n, src, tid);
+  else bitonic_sort<4>(surv, n, src, tid);
   __syncthreads();
-  // merge levels: runs of len = 2^lg pairwise into runs of 2 len.  Every key finds its output
-  // position from the count of keys below it in the partner run (keys are unique), by a
-  // fixed-step binary search; a thread advances its up to four keys' searches together.
-  constexpr int kItems = kSchedMaxSlots / kSchedThreads;
-  for (int lg = lg_gp; lg < lg_n; ++lg) {
-    const int len = 1 << lg;
-    unsigned long long x[kItems];
-    int pb[kItems], c[kItems];
-#pragma unroll
-    for (int q = 0; q < kItems; ++q) {
-      const int pos = tid + q * kSchedThreads;
-      x[q] = pos < N ? src[pos] : 0ull;
-      pb[q] = ((pos >> lg) ^ 1) << lg;
-      c[q] = 0;
-    }
-    for (int w = len >> 1; w >= 1; w >>= 1) {
-#pragma unroll
-      for (int q = 0; q < kItems; ++q)
-        if (tid + q * kSchedThreads < N && src[pb[q] + c[q] + w - 1] < x[q]) c[q] += w;
-    }
-#pragma unroll
-    for (int q = 0; q < kItems; ++q) {
-      const int pos = tid + q * kSchedThreads;
-      if (pos < N) {
-        if (src[pb[q] + c[q]] < x[q]) c[q] += 1;
-        dst[((pos >> (lg + 1)) << (lg + 1)) + (pos & (len - 1)) + c[q]] = x[q];
-      }
-    }
-    __syncthreads();
-    unsigned long long* t = src;
-    src = dst;
-    dst = t;
-  }
   unsigned long long* key = src;  // sorted keys, then inclusive prefix sums
   // fixed-point values in sorted order, 4 consecutive per thread, then an exclusive block scan
   long long v[4];
@@ -341,17 +342,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
 cudaError_t launch_schedule(const float* surv, int bs, int gamma, const double* sps, int m_max,
                             int mode, int32_t* window, int32_t* K_out, double* theta_out,
                             cudaStream_t s) {
-  constexpr int kDyn = 2 * kSchedMaxSlots * sizeof(unsigned long long);  // 64 KB: opt in, once per device
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
-  schedule_kernel<<<1, kSchedThreads, kDyn, s>>>(surv, bs, gamma, sps, m_max, mode, window, K_out, theta_out);
+  schedule_kernel<<<1, kSchedThreads, 0, s>>>(surv, bs, gamma, sps, m_max, mode, window, K_out, theta_out);
   return cudaGetLastError();
 }
 
