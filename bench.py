@@ -1,10 +1,12 @@
 """Benchmark: DSpark step tokens/s at bs=256, V=151936, gamma=7 (the mixed-difficulty batch).
 
 One step = draft_block -> confidence -> schedule -> pack -> [target forward] -> verify, all
-through the C ABI on one stream.  The target forward is the caller's model and is not part
-of this path: it is a row gather here and it sits outside the timed segments; everything
-else is timed with CUDA events on the launching stream.  The L2 is flushed (256 MB write)
-between timed steps.  tokens/step = sum over requests of (accepted + 1).
+through the C ABI on one stream; the timed steps replay CUDA graphs captured from those calls
+(one graph per stage and step, each with its own step counter), the e2e steps call the API
+directly.  The target forward is the caller's model and is not part of this path: it is a row
+gather here and it sits outside the timed segments; everything else is timed with CUDA events
+on the launching stream.  The L2 is flushed (256 MB write) between timed steps.
+tokens/step = sum over requests of (accepted + 1).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -269,32 +271,50 @@ def run_ours(args, rank: int, world: int):
     tokens_acc = torch.zeros(1, dtype=torch.int64, device=dev)
     tau = wl.temperature
 
-    def step(it, timed, evs=None):
-        if evs is not None:
-            evs[0].record(stream)
+    def draft_stage(it):
         B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], tau, wl.seed, it, buf.tokens,
                              buf.logit_x, buf.lse, buf.ws)
-        if evs is not None:
-            evs[1].record(stream)
+
+    def conf_sched_pack_stage():
         B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], buf.tokens, inp["w"], inp["b"], inp["sts_T"],
                             buf.conf, buf.surv)
         B.dspark_schedule(buf.surv, sps, SCHED, buf.window, buf.K, buf.theta)
         B.dspark_pack(buf.window, inp["anchor"], buf.tokens, tiers_dev, buf.cu, buf.ids, buf.req, buf.pos,
                       buf.padded, buf.ws)
-        if evs is not None:
-            evs[2].record(stream)
-        fwd(buf)  # the caller's target forward: outside the timed segments
-        if evs is not None:
-            evs[3].record(stream)
-        S.verify(inp, buf, tau, wl.seed, it, B.DSPARK_COMPACT)
-        if evs is not None:
-            evs[4].record(stream)
-        if timed:
-            tokens_acc.add_((buf.acc_len.to(torch.int64) + 1).sum())
 
-    for w in range(args.warmup):
-        step(10_000 + w, True)  # every op of the timed loop runs once before it (first-use set-up)
+    def verify_stage(it):
+        S.verify(inp, buf, tau, wl.seed, it, B.DSPARK_COMPACT)
+
+    def count_tokens():
+        tokens_acc.add_((buf.acc_len.to(torch.int64) + 1).sum())
+
+    for w in range(args.warmup):  # eager, through the API
+        draft_stage(10_000 + w)
+        conf_sched_pack_stage()
+        fwd(buf)
+        verify_stage(10_000 + w)
+        count_tokens()  # every op of the timed loop runs once before it (first-use set-up)
     tokens_acc.zero_()
+
+    # The timed steps replay CUDA graphs of the same API calls, one per stage and step, captured
+    # here with each step's own counter (the draws differ step to step), then replayed once
+    # untimed so that the timed replays find them resident.
+    graphs = []
+    for it in range(args.steps):
+        gs = [torch.cuda.CUDAGraph() for _ in range(3)]
+        with torch.cuda.graph(gs[0]):
+            draft_stage(it)
+        with torch.cuda.graph(gs[1]):
+            conf_sched_pack_stage()
+        with torch.cuda.graph(gs[2]):
+            verify_stage(it)
+        graphs.append(gs)
+    for gs in graphs:
+        gs[0].replay()
+        gs[1].replay()
+        fwd(buf)
+        gs[2].replay()
+    torch.cuda.synchronize(dev)
     st = B.dspark_read_device_status(buf.ws)
     if st != 0:
         raise RuntimeError("device status after warm-up: " + B.dspark_status_string(st))
@@ -307,7 +327,17 @@ def run_ours(args, rank: int, world: int):
         t_host = time.perf_counter()
         for it in range(args.steps):
             flush.fill_(it & 0xFF)  # L2 flush, outside the timed segments
-            step(it, True, evs[it])
+            e, gs = evs[it], graphs[it]
+            e[0].record(stream)
+            gs[0].replay()
+            e[1].record(stream)
+            gs[1].replay()
+            e[2].record(stream)
+            fwd(buf)  # the caller's target forward: outside the timed segments
+            e[3].record(stream)
+            gs[2].replay()
+            e[4].record(stream)
+            count_tokens()
         t_host = time.perf_counter() - t_host  # host time to enqueue (the device may still run)
         torch.cuda.synchronize(dev)
     if world > 1:
@@ -377,7 +407,8 @@ def run_ours(args, rank: int, world: int):
         "config": {"workload": "mixed_bs256: bs=256, gamma=7, V=151936, r=256, d=4096, compact verify, "
                                "temperature 1, sawtooth cost table with tiers every 64 to 2048, global-argmax scheduler",
                    "global_batch": bs * world, "l2": "flushed between steps (256 MB write)",
-                   "timed": "draft+confidence+schedule+pack and verify segments; target forward excluded",
+                   "timed": "draft+confidence+schedule+pack and verify segments; target forward excluded; "
+                            "each stage of each timed step a captured CUDA graph of its API calls",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_step": tokens / args.steps / world,
         "host_enqueue_ms_per_step": t_host * 1e3 / args.steps,
