@@ -11,10 +11,6 @@
 namespace dspark {
 
 constexpr int kChunk = DSPARK_CHUNK;
-// Verify's decision statistics are kept per half chunk (64 ids): entry 2c + h covers ids
-// [128c + 64h, 128c + 64h + 64).  Passes that reduce a whole chunk at once write entry 2c and
-// a neutral entry 2c + 1.
-constexpr int kStatsPerChunk = 2;
 
 // The draft's partial draw over a set of chunks ("slot") of one request, as a float4:
 //   x, y : running (max t, sum exp(t - max)) of the tempered logits t = l / T over the slot's
@@ -41,8 +37,8 @@ enum DecisionKind : int { kDecNone = 0, kDecResidual = 1, kDecBonus = 2 };
 // ----------------------------------------------------------------------------------------
 // Workspace layout (all offsets 256-byte aligned)
 //   status   : uint32 status word (first device-detected error wins)
-//   stats    : 16 bytes per (row, chunk): the draft's entries (float4 [bs][n_slots],
-//              n_slots <= n_chunks) or verify's float2 [bs][2 * n_chunks] half-chunk masses
+//   stats    : 32 bytes per (row, chunk): the draft's entries (float4 [bs][n_slots]) or
+//              verify's DecideEntry [bs][n_slots], n_slots <= n_chunks
 //   rowstats : RowStat [bs * (gamma + 1)]  per packed target row
 //   dec      : Decision [bs]               per-request verify decision
 // ----------------------------------------------------------------------------------------
@@ -62,8 +58,22 @@ struct Decision {
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Verify's partial draw of the deciding row over a set of chunks ("slot"), 32 bytes:
+//   R, P   : sums over the slot's chunks of the residual mass max(0, p_t - p_d) and of p_t
+//   kR, cR : best residual key log R_c + G_c (Philox purpose 4, index c) and its chunk
+//   kP, cP : best target key log P_c + G_c and its chunk (the bonus draw, and the fallback of
+//            a residual with no mass); -inf / INT_MAX when empty, ties to the lowest chunk
+struct DecideEntry {
+  float R, P, kR, kP;
+  int cR, cP, pad0, pad1;
+};
+
+// The draft's scratch alone (16-byte entries, at most one per chunk).
+__host__ __device__ inline size_t draft_stats_bytes(int bs, int n_chunks) {
+  return size_t(bs) * n_chunks * sizeof(float4);
+}
 __host__ __device__ inline size_t stats_bytes(int bs, int n_chunks) {
-  return size_t(bs) * n_chunks * kStatsPerChunk * sizeof(float2);
+  return size_t(bs) * n_chunks * sizeof(DecideEntry);
 }
 
 struct WsLayout {

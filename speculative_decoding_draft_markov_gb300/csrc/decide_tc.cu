@@ -1,5 +1,7 @@
 // Verify's decision masses on the tensor cores (bf16): for each request's deciding row, per
-// 128-id chunk, the residual mass sum max(0, p_t - p_d) and the target mass sum p_t.
+// 128-id chunk, the residual mass sum max(0, p_t - p_d) and the target mass sum p_t, reduced at
+// once to per-CTA partial draws (DecideEntry, common.cuh): mass sums and the best chunk keys
+// log(mass) + Gumbel for the first level of the residual / bonus draw.
 //
 // DSpark technical summary, "Verification": a rejected draft token is replaced by a sample of
 // normalise(max(0, p_t - p_d)) at the rejected position, and a fully accepted block takes a
@@ -61,6 +63,7 @@ struct Bars {
   uint64_t a_ready;  // A is in TMEM (one arrival per warp of epilogue set 0)
   uint32_t tmem_base;
   int abort;
+  DecideEntry xch[kBM];  // warp set 1's partial draw of each row, merged by set 0 at the end
 };
 
 // Per-row facts (one request per tile row).
@@ -71,6 +74,8 @@ struct RowMeta {
   float a_d;        // lse_d * log2(e)
   int resid;        // residual row (else bonus, or dead)
   int live;         // the request has a decision
+  int kdec;         // position of the decision (Philox counter of its chunk Gumbels)
+  int pad;
 };
 
 struct Params {
@@ -84,8 +89,10 @@ struct Params {
   const Decision* dec;
   int bs, gamma, V, r;
   float inv_tau;
-  float2* stats;  // [bs][2 * n_chunks] half-chunk (R, P)
+  DecideEntry* entries;  // [bs][n_slots]: one partial draw per request and CTA column
+  int n_slots;
   int n_chunks;
+  uint64_t seed, step;
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -99,6 +106,13 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// The chunk Gumbel of a decision (Philox purpose 4, index c).  Out of line: inlined into the
+// tile loop its rounds raise register pressure there.
+__device__ __noinline__ float decide_gumbel_call(uint64_t seed, uint64_t step, int req, int kdec, int c) {
+  const uint4 w = philox_group(seed, step, kDecideChunk, uint32_t(req), kdec, uint32_t(c) >> 2);
+  return gumbel_from_bits(pick_word(w, c & 3));
+}
 
 __device__ __forceinline__ void unpack8(const uint4 q, float* x) {
   x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
@@ -155,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
   tc::tc_fence_after();
   const uint32_t tmem_base = bar->tmem_base;
   const long long deadline = tc::deadline_after_ns(p.timeout_ns);
+  DecideEntry xmine{0.f, 0.f, -INFINITY, -INFINITY, INT_MAX, INT_MAX, 0, 0};  // epilogue set 0's draw
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -196,12 +211,13 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
   tc::grid_dependency_wait();  // the decisions come from the previous kernel
   constexpr int kRest = kThreads - 32;
   for (int m = tid - 32; m < kBM; m += kRest) {
-    RowMeta rm{0, 0, 0.f, 0.f, 0, 0};
+    RowMeta rm{0, 0, 0.f, 0.f, 0, 0, 0, 0};
     const int grow = m0 + m;
     if (grow < bs) {
       const Decision d = p.dec[grow];
       if (d.kind != kDecNone) {
         rm.live = 1;
+        rm.kdec = d.kdec;
         rm.t_off = (long long)d.pdec * V;
         rm.a_t = p.rs[d.pdec].lse * kLog2e;
         if (d.kind == kDecResidual) {
@@ -329,6 +345,21 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
     const uint32_t taddr = lane_base + set * kBN;
     const uint8_t* ub = sS + set * kStageBytes + m * 128;  // U row in the stage (+ h * kHalf)
     const uint8_t* tb = ub + 2 * kHalf;                     // target row
+    // the row's partial draw over this set's chunks; the chunk Gumbels of the first kGReg tiles
+    // are drawn before the loop
+    constexpr int kGReg = 8;
+    float gk[kGReg];
+#pragma unroll
+    for (int q = 0; q < kGReg; ++q) {
+      const int t = set + 2 * q;
+      gk[q] = 0.f;
+      if (rm.live && t < n_tiles) {
+        const int c = c0 + t * cstride;
+        const uint4 w = philox_group(p.seed, p.step, kDecideChunk, uint32_t(grow), rm.kdec, uint32_t(c) >> 2);
+        gk[q] = gumbel_from_bits(pick_word(w, c & 3));
+      }
+    }
+    DecideEntry pe{0.f, 0.f, -INFINITY, -INFINITY, INT_MAX, INT_MAX, 0, 0};
     for (int t = set, i = 0; t < n_tiles; t += 2, ++i) {
       const int c = c0 + t * cstride;
       const int valid = min(kBN, V - c * kBN);
@@ -377,12 +408,29 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->s_empty[set]));
-      if (grow < bs) {
-        float2* e2 = p.stats + (size_t(grow) * p.n_chunks + c) * kStatsPerChunk;
-        e2[0] = make_float2((R4[0] + R4[1]) + (R4[2] + R4[3]), (P4[0] + P4[1]) + (P4[2] + P4[3]));
-        e2[1] = make_float2(0.f, 0.f);
+      float g;
+      if (i < kGReg) {
+        g = gk[0];
+#pragma unroll
+        for (int q = 0; q + 1 < kGReg; ++q) gk[q] = gk[q + 1];
+      } else {
+        g = rm.live ? decide_gumbel_call(p.seed, p.step, grow, rm.kdec, c) : 0.f;
+      }
+      const float R = (R4[0] + R4[1]) + (R4[2] + R4[3]), P = (P4[0] + P4[1]) + (P4[2] + P4[3]);
+      pe.R += R;
+      pe.P += P;
+      // chunks arrive in increasing order: a strict > keeps the lowest chunk on ties
+      if (R > 0.f) {
+        const float kr = logf(R) + g;
+        if (kr > pe.kR) { pe.kR = kr; pe.cR = c; }
+      }
+      if (P > 0.f) {
+        const float kp = logf(P) + g;
+        if (kp > pe.kP) { pe.kP = kp; pe.cP = c; }
       }
     }
+    if (set == 1) bar->xch[m] = pe;
+    xmine = pe;
   }
 
   tc::tc_fence_before();
@@ -391,6 +439,18 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem_base, kTmemCols);
   }
+  if (warp >= 2 && warp < 6) {
+    // warp set 0 merges the other set's partial draw of the same row and writes the CTA's
+    // entry (request grow, slot c0)
+    const int m = (warp & 3) * 32 + lane, grow = m0 + m;
+    const DecideEntry o = bar->xch[m];
+    DecideEntry e = xmine;
+    e.R += o.R;
+    e.P += o.P;
+    if (o.kR > e.kR || (o.kR == e.kR && o.cR < e.cR)) { e.kR = o.kR; e.cR = o.cR; }
+    if (o.kP > e.kP || (o.kP == e.kP && o.cP < e.cP)) { e.kP = o.kP; e.cP = o.cP; }
+    if (grow < bs) p.entries[size_t(grow) * p.n_slots + c0] = e;
+  }
 }
 
 }  // namespace
@@ -398,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
 cudaError_t launch_decision_stats_tc(const void* target, const void* U, const void* W1, const void* W2t,
                                      const int32_t* anchor, const int32_t* tokens, const float* lse_d,
                                      const void* rs, const void* dec, int bs, int gamma, int V, int r,
-                                     float inv_tau, void* stats, int n_chunks, uint32_t* status,
-                                     cudaStream_t s) {
+                                     float inv_tau, uint64_t seed, uint64_t step, void* entries,
+                                     int n_chunks, int* n_slots, uint32_t* status, cudaStream_t s) {
   if (!tch::encode_fn()) return cudaErrorNotSupported;
   if (r % kBK != 0 || r > 256) return cudaErrorInvalidValue;
   CUtensorMap map_w2;
@@ -418,14 +478,19 @@ cudaError_t launch_decision_stats_tc(const void* target, const void* U, const vo
   prm.dec = static_cast<const Decision*>(dec);
   prm.bs = bs; prm.gamma = gamma; prm.V = V; prm.r = r;
   prm.inv_tau = inv_tau;
-  prm.stats = static_cast<float2*>(stats);
+  prm.entries = static_cast<DecideEntry*>(entries);
   prm.n_chunks = n_chunks;
+  prm.seed = seed;
+  prm.step = step;
   prm.status = status;
   prm.timeout_ns = g_wait_timeout_ns;
+  const int grid = tch::vocab_grid(bs, n_chunks);
+  prm.n_slots = grid / ((bs + kBM - 1) / kBM);
+  *n_slots = prm.n_slots;
   // programmatic dependent launch: barrier set-up, TMEM and the W2t ring overlap the previous
   // kernel's tail
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(tch::vocab_grid(bs, n_chunks));
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;

@@ -74,7 +74,7 @@ extern "C" DSPARK_API int dspark_draft_block_noalloc(
 
   // the scratch this call needs: status word + 16 bytes per (request, 128-id chunk)
   const WsLayout L = ws_layout(bs, gamma, V);
-  const size_t need = L.stats + stats_bytes(bs, L.n_chunks);
+  const size_t need = L.stats + draft_stats_bytes(bs, L.n_chunks);
   if (need > kNoAllocScratchBytes) return DSPARK_EUNSUPPORTED;
 
   void* scratch = nullptr;

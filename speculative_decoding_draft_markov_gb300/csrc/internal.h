@@ -22,13 +22,14 @@ cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t
                                   uint64_t step, void* entries, int n_chunks, int* n_slots,
                                   uint32_t* status, cudaStream_t s);
 bool draft_tc_supported(int dtype, int bs, int V, int r);
-// Verify's decision masses on the tensor cores (bf16): per (request, chunk) the residual mass
-// sum max(0, p_t - p_d) and the target mass sum p_t of the request's deciding row.
+// Verify's decision masses on the tensor cores (bf16): per request and CTA column a
+// DecideEntry (common.cuh) over the column's chunks of the request's deciding row (residual
+// mass sum max(0, p_t - p_d), target mass sum p_t, best chunk keys); n_slots returned.
 cudaError_t launch_decision_stats_tc(const void* target, const void* U, const void* W1, const void* W2t,
                                      const int32_t* anchor, const int32_t* tokens, const float* lse_d,
                                      const void* rs, const void* dec, int bs, int gamma, int V, int r,
-                                     float inv_tau, void* stats, int n_chunks, uint32_t* status,
-                                     cudaStream_t s);
+                                     float inv_tau, uint64_t seed, uint64_t step, void* entries,
+                                     int n_chunks, int* n_slots, uint32_t* status, cudaStream_t s);
 extern uint64_t g_wait_timeout_ns;  // deadline of device-side waits (dspark_set_wait_timeout_ns)
 // Merge the n_slots entries of each row of one position and draw x_k.
 cudaError_t launch_draft_select(int dtype, const void* entries, int n_slots, const void* U,

@@ -217,7 +217,8 @@ __global__ void __launch_bounds__(128) decision_stats_simt_kernel(
     const T* __restrict__ target, const T* __restrict__ U, const T* __restrict__ W1,
     const T* __restrict__ W2t, const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens,
     const float* __restrict__ lse_d, const RowStat* __restrict__ rs, const Decision* __restrict__ dec,
-    int bs, int gamma, int V, int r, float inv_tau, float2* __restrict__ stats, int n_chunks) {
+    int bs, int gamma, int V, int r, float inv_tau, uint64_t seed, uint64_t step,
+    DecideEntry* __restrict__ entries, int n_chunks) {
   __shared__ float sA[RB][64];
   __shared__ float sW[kChunk][65];
   __shared__ float red[4];
@@ -272,9 +273,13 @@ __global__ void __launch_bounds__(128) decision_stats_simt_kernel(
     }
     const float R = block_sum<kChunk>(w, red);
     const float P = block_sum<kChunk>(pt, red);
-    if (tid == 0) {
-      stats[(size_t(row) * n_chunks + c) * kStatsPerChunk] = make_float2(R, P);
-      stats[(size_t(row) * n_chunks + c) * kStatsPerChunk + 1] = make_float2(0.f, 0.f);
+    if (tid == 0) {  // the chunk's entry: masses and keys log(mass) + G_c (purpose 4, index c)
+      const uint4 gw = philox_group(seed, step, kDecideChunk, uint32_t(row), d.kdec, uint32_t(c) >> 2);
+      const float g = gumbel_from_bits(pick_word(gw, c & 3));
+      DecideEntry e{R, P, -INFINITY, -INFINITY, INT_MAX, INT_MAX, 0, 0};
+      if (R > 0.f) { e.kR = logf(R) + g; e.cR = c; }
+      if (P > 0.f) { e.kP = logf(P) + g; e.cP = c; }
+      entries[size_t(row) * n_chunks + c] = e;
     }
   }
 }
@@ -287,32 +292,39 @@ __global__ void __launch_bounds__(256) decision_select_kernel(
     const T* __restrict__ target, const T* __restrict__ U, const T* __restrict__ W1,
     const T* __restrict__ W2t, const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens,
     const float* __restrict__ lse_d, const RowStat* __restrict__ rs, const Decision* __restrict__ dec,
-    const float2* __restrict__ stats, int n_chunks, int bs, int gamma, int V, int r, float inv_tau,
+    const DecideEntry* __restrict__ entries, int n_slots, int bs, int gamma, int V, int r, float inv_tau,
     uint64_t seed, uint64_t step, int32_t* __restrict__ out_tokens) {
   __shared__ float sA[256];
   __shared__ float tw[kChunk], tp[kChunk];
   __shared__ float rv[8];
   __shared__ int ri[8];
+  __shared__ int s_use_res, s_win;
   const int b = blockIdx.x, tid = threadIdx.x;
   const Decision d = dec[b];
   if (d.kind == kDecNone) return;
-  const float2* st = stats + size_t(b) * n_chunks * kStatsPerChunk;
-  float Rl = 0.f;
-  for (int c = tid; c < n_chunks; c += 256) Rl += st[2 * c].x + st[2 * c + 1].x;
-  const bool use_res = block_sum<256>(Rl, rv) > 0.f;
-  ArgMax best{-INFINITY, INT_MAX};
-  const int n_grp = (n_chunks + 3) / 4;
-  for (int g = tid; g < n_grp; g += 256) {
-    const uint4 w = philox_group(seed, step, kDecideChunk, b, d.kdec, g);
-#pragma unroll
-    for (int l = 0; l < 4; ++l) {
-      const int c = 4 * g + l;
-      if (c >= n_chunks) break;
-      const float mass = use_res ? st[2 * c].x + st[2 * c + 1].x : st[2 * c].y + st[2 * c + 1].y;
-      if (mass > 0.f) best = better(best, ArgMax{logf(mass) + gumbel_from_bits(pick_word(w, l)), c});
+  // merge the request's partial draws: total residual mass (does the residual have mass?) and
+  // the winning chunk of the residual or, without residual mass, of the target draw
+  if (tid < 32) {
+    const DecideEntry* en = entries + size_t(b) * n_slots;
+    float R = 0.f;
+    ArgMax bR{-INFINITY, INT_MAX}, bP{-INFINITY, INT_MAX};
+    for (int i = tid; i < n_slots; i += 32) {
+      const DecideEntry e = en[i];
+      R += e.R;
+      bR = better(bR, ArgMax{e.kR, e.cR});
+      bP = better(bP, ArgMax{e.kP, e.cP});
+    }
+    R = warp_sum(R);
+    bR = warp_argmax(bR);
+    bP = warp_argmax(bP);
+    if (tid == 0) {
+      s_use_res = R > 0.f;
+      s_win = (R > 0.f) ? bR.i : bP.i;
     }
   }
-  best = block_argmax<256>(best, rv, ri);
+  __syncthreads();
+  const bool use_res = s_use_res;
+  const ArgMax best{0.f, s_win};
   const int cstar = (best.i == INT_MAX) ? 0 : best.i;  // only non-finite statistics leave it unset
   const bool resid = (d.kind == kDecResidual) && use_res;
   if (resid) {
@@ -364,7 +376,7 @@ static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_
   const WsLayout L = ws_layout(bs, gamma, V);
   char* w = static_cast<char*>(ws);
   uint32_t* status = reinterpret_cast<uint32_t*>(w + L.status);
-  float2* stats = reinterpret_cast<float2*>(w + L.stats);
+  DecideEntry* entries = reinterpret_cast<DecideEntry*>(w + L.stats);
   RowStat* rs = reinterpret_cast<RowStat*>(w + L.rowstats);
   Decision* dec = reinterpret_cast<Decision*>(w + L.dec);
   verify_rows_kernel<T><<<bs * (gamma + 1), kRowThreads, 0, s>>>(target, cu, tokens, bs, gamma, V,
@@ -375,16 +387,18 @@ static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_
   if (!greedy) {
     constexpr int RB = 32;
     constexpr bool kBf16 = sizeof(T) == 2;
+    int n_slots = L.n_chunks;
     if (kBf16 && draft_tc_supported(DSPARK_BF16, bs, V, r)) {
       const cudaError_t e = launch_decision_stats_tc(target, U, W1, W2t, anchor, tokens, lse, rs, dec, bs, gamma, V,
-                                                     r, inv_tau, stats, L.n_chunks, status, s);
+                                                     r, inv_tau, seed, step, entries, L.n_chunks, &n_slots, status, s);
       if (e != cudaSuccess) return e;
     } else {
       decision_stats_simt_kernel<T, RB><<<dim3(L.n_chunks, (bs + RB - 1) / RB), kChunk, 0, s>>>(
-          target, U, W1, W2t, anchor, tokens, lse, rs, dec, bs, gamma, V, r, inv_tau, stats, L.n_chunks);
+          target, U, W1, W2t, anchor, tokens, lse, rs, dec, bs, gamma, V, r, inv_tau, seed, step, entries,
+          L.n_chunks);
     }
     decision_select_kernel<T><<<bs, 256, 0, s>>>(target, U, W1, W2t, anchor, tokens, lse, rs, dec,
-                                                 stats, L.n_chunks, bs, gamma, V, r, inv_tau, seed,
+                                                 entries, n_slots, bs, gamma, V, r, inv_tau, seed,
                                                  step, out_tokens);
   }
   return cudaGetLastError();
