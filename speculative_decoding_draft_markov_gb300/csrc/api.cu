@@ -122,10 +122,9 @@ int dspark_draft_block(const void* U, const void* W1, const void* W2t, int dtype
   const bool tc = draft_tc_supported(dtype, bs, V, r);
   if (tc && draft_fused_available(dtype, bs, gamma, V, r)) {
     // one cooperative launch for the whole block; the launch-per-stage path below otherwise
-    unsigned* gsync = reinterpret_cast<unsigned*>(w + L.status + 128);
-    int* gabort = reinterpret_cast<int*>(w + L.status + 192);
+    int* sync_words = reinterpret_cast<int*>(w + L.sync);
     const cudaError_t e = launch_draft_fused_tc(U, W1, W2t, anchor, tokens, logit_x, lse, bs, gamma, V, r, inv_tau,
-                                                greedy, seed, step, stats, L.n_chunks, status, gsync, gabort, s);
+                                                greedy, seed, step, stats, L.n_chunks, status, sync_words, s);
     if (e == cudaSuccess) return DSPARK_OK;
     cudaGetLastError();  // a launch the device could not take leaves no error behind
   }

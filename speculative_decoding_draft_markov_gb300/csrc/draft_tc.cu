@@ -419,11 +419,16 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
 
 // ===================================================================================
 // All gamma positions in one cooperative launch (every CTA resident, one per SM).  Per
-// position k the CTA runs the vocabulary pass above; then a grid barrier, the select of up to
-// two requests per CTA (one per epilogue warp set) and a second grid barrier, after which
-// every CTA gathers the W1 rows of the new tokens for position k + 1.  The producer keeps
-// streaming U_{k+1} and W2t into its rings through the barriers and the select, and the
-// kernel boundaries of the launch-per-stage path disappear.
+// position k the CTA runs the vocabulary pass above, publishes its entries (a per-CTA flag),
+// and selects up to two requests (one per epilogue warp set) as soon as the entries of every
+// CTA of the request's M-tile are published; each select publishes its token (a per-request
+// flag), and a CTA starts position k + 1 as soon as the tokens of its own 128 rows are there.
+// No grid-wide barrier: every wait is on the data it needs.  The producer keeps streaming
+// U_{k+1} and W2t into its rings meanwhile.  Flags hold the last position published (release
+// stores, acquire loads); every wait is bounded and a CTA that gives up sets `gabort`, which
+// ends the others' waits.  Write-after-read safety: a CTA overwrites its entries (position
+// k + 1) only after the tokens of its rows -- written by the selects that read those entries
+// -- are published.
 // ===================================================================================
 constexpr int kFusedBStages = 5;
 
@@ -435,7 +440,7 @@ struct SelScratch {
   float lse;
   float best;
   int win;
-  int pad;
+  int fail;  // the merge gave up waiting for the entries
 };
 
 struct FusedBarriers {
@@ -467,8 +472,9 @@ struct FusedParams {
   float4* entries;
   uint64_t seed, step;
   uint32_t* status;
-  unsigned* gsync;  // grid barrier counter (zero at launch)
-  int* gabort;      // set by a CTA that gives up in a grid barrier (zero at launch)
+  int* fslot;       // [gridDim.x]: last position whose entries the CTA published (zero at launch)
+  int* frow;        // [bs]: last position whose token the request's select published (zero)
+  int* gabort;      // set by a CTA that gives up (zero at launch)
   uint64_t timeout_ns;
 };
 
@@ -477,12 +483,6 @@ constexpr size_t fused_smem_bytes(int r) {
          sizeof(FusedBarriers);
 }
 static_assert(fused_smem_bytes(256) <= 232448, "dynamic shared memory beyond the 227 KB per-block limit");
-
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 
 // Barrier among the epilogue warps (named barrier 1) that also returns, to every thread, the OR
 // of `pred` over them: the uniform way for the warps to agree to stop.
@@ -499,19 +499,24 @@ __device__ __forceinline__ void group_barrier(int g) {  // the four warps of epi
   asm volatile("bar.sync %0, 128;" ::"r"(2 + g) : "memory");
 }
 
-// One thread per CTA: arrive on the grid counter and wait until `target` arrivals in total;
-// bounded (deadline, or another CTA's give-up).  Returns false on give-up.  The arrival is a
-// release reduction (the CTA's threads synchronised with this one before, so their writes are
-// ordered before it) and the wait an acquire load: no separate fences.
-__device__ bool grid_arrive_wait(unsigned* counter, unsigned target, int* gabort, uint64_t timeout_ns) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
-  const long long dl = tc::deadline_after_ns(timeout_ns);
-  while (ld_acquire_gpu(counter) < target) {
+__device__ __forceinline__ int ld_acquire_gpu_s32(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu_s32(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Wait until *flag >= want (acquire), bounded by `dl` and by another CTA's give-up; false on
+// give-up, which this call also announces through gabort.
+__device__ bool wait_flag(const int* flag, int want, int* gabort, long long dl) {
+  while (ld_acquire_gpu_s32(flag) < want) {
     if (*reinterpret_cast<volatile int*>(gabort)) return false;
     if (clock64() > dl) {
       atomicExch(gabort, 1);
       return false;
     }
+    __nanosleep(100);  // few polling requests: the flags' L2 lines serve other traffic too
   }
   return true;
 }
@@ -736,14 +741,28 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(const __grid_c
     };
     draw_gumbels(1);
     for (int k = 1; k <= gamma; ++k) {
-      // A operand: W1[x_{k-1}] of rows m0 .. m0 + 127 (tokens of position k - 1 come from the
-      // selects of every CTA: read through L2)
-      for (int mm = et; mm < kBM; mm += kEpiThreads) {
-        const int gr = m0 + mm;
-        bar->xrow[mm] = gr < bs ? clamp_token((k == 1) ? p.anchor[gr] : __ldcg(p.tokens + size_t(gr) * gamma + k - 2), V)
-                                : -1;
+      // A operand: W1[x_{k-1}] of rows m0 .. m0 + 127.  The tokens of position k - 1 come from
+      // the selects of other CTAs: wait for each row's flag, then read through L2.
+      bool tok_fail = false;
+      if (et < 32) {  // one warp polls the 128 rows' flags, four per lane
+        const long long dl = tc::deadline_after_ns(p.timeout_ns);
+        for (int mm = et; mm < kBM; mm += 32) {
+          const int gr = m0 + mm;
+          int xp = -1;
+          if (gr < bs) {
+            if (k == 1) {
+              xp = clamp_token(p.anchor[gr], V);
+            } else if (wait_flag(p.frow + gr, k - 1, p.gabort, dl)) {
+              xp = clamp_token(__ldcg(p.tokens + size_t(gr) * gamma + k - 2), V);
+            } else {
+              tok_fail = true;
+            }
+          }
+          bar->xrow[mm] = xp;
+        }
       }
-      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+      stop = epi_barrier_or(tok_fail);
+      if (stop) break;
       {
         const int cpr = r / 8;
         for (int idx = et; idx < kBM * cpr; idx += kEpiThreads) {
@@ -838,12 +857,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(const __grid_c
         const ArgMax a = better(ArgMax{best_key, best_c}, ArgMax{o.z, __float_as_int(o.w)});
         if (grow < bs) p.entries[size_t(grow) * p.n_slots + c0] = make_float4(l.m, l.s, a.v, __int_as_float(a.i));
       }
-      // ---- grid barrier 1: every CTA's entries of position k are written
+      // ---- publish this CTA's entries of position k
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-      bool gfail = false;
-      if (et == 0) gfail = !grid_arrive_wait(p.gsync, gridDim.x * unsigned(2 * k - 1), p.gabort, p.timeout_ns);
-      stop = epi_barrier_or(gfail);
-      if (stop) break;
+      if (et == 0) st_release_gpu_s32(p.fslot + blockIdx.x, k);
 
       // ---- select of position k: request blockIdx.x + g * gridDim.x by warp set g
       {
@@ -853,6 +869,13 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(const __grid_c
         const bool act = rq < bs;
         if (act) {
           if (gw == 0) {  // merge the request's entries: row LSE and the winner
+            // the entries of slot s come from CTA s * n_mt + (rq's M-tile): wait for them
+            const int mt = rq / kBM;
+            const long long dl = tc::deadline_after_ns(p.timeout_ns);
+            bool ok = true;
+            for (int sl = lane; sl < p.n_slots && ok; sl += 32) ok = wait_flag(p.fslot + sl * n_mt + mt, k, p.gabort, dl);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (lane == 0) S.fail = ok ? 0 : 1;
             const float4* en = p.entries + size_t(rq) * p.n_slots;
             LsePair lp{-INFINITY, 0.f};
             ArgMax best{-INFINITY, INT_MAX};
@@ -888,12 +911,15 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(const __grid_c
           }
         }
         group_barrier(g);
-        if (act && p.greedy) {
+        const bool sel_fail = act && S.fail;
+        if (sel_fail) {
+        } else if (act && p.greedy) {
           if (gt == 0) {
             const size_t out = size_t(rq) * gamma + (k - 1);
             p.tokens[out] = (S.win == INT_MAX) ? 0 : S.win;
             p.logit_x[out] = S.best;
             p.lse[out] = 0.f;
+            st_release_gpu_s32(p.frow + rq, k);  // publish x_k of the request
           }
         } else if (act) {
           const int cstar = (S.win == INT_MAX) ? 0 : S.win;
@@ -923,7 +949,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(const __grid_c
             p.tokens[out] = xk;
             p.logit_x[out] = te;
             p.lse[out] = S.lse;
-            if (k < gamma) {  // the next gather reads W1[x_k] after the grid barrier: warm L2 now
+            st_release_gpu_s32(p.frow + rq, k);  // publish x_k of the request
+            if (k < gamma) {  // the next gathers read W1[x_k]: warm L2 now
               const char* row = reinterpret_cast<const char*>(p.W1 + size_t(xk) * r);
               for (int q = 0; q < r * 2; q += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + q));
             }
@@ -932,20 +959,21 @@ __global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(const __grid_c
           group_barrier(g);  // same barrier sequence as the active groups of this CTA
           group_barrier(g);
         }
+        if (sel_fail && !p.greedy) {  // keep the group's barrier count of an active select
+          group_barrier(g);
+          group_barrier(g);
+        }
+        // a select that gave up stops the CTA (every epilogue warp agrees below)
+        if (epi_barrier_or(sel_fail)) {
+          stop = true;
+          break;
+        }
       }
-      // ---- grid barrier 2: every request's x_k is written (not needed after the last position)
-      if (k < gamma) {
-        draw_gumbels(k + 1);
-        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-        gfail = false;
-        if (et == 0) gfail = !grid_arrive_wait(p.gsync, gridDim.x * unsigned(2 * k), p.gabort, p.timeout_ns);
-        stop = epi_barrier_or(gfail);
-        if (stop) break;
-      }
+      if (k < gamma) draw_gumbels(k + 1);
     }
     if (stop) {
       *abort_flag = 1;  // the producer and the MMA issuer stop waiting
-      if (et == 0) atomicExch(p.gabort, 1);  // and so do the other CTAs at their grid barriers
+      if (et == 0) atomicExch(p.gabort, 1);  // and so do the other CTAs' flag waits
       set_status(p.status, DSPARK_ETIMEOUT);
     }
   }
@@ -1058,7 +1086,7 @@ bool draft_fused_available(int dtype, int bs, int gamma, int V, int r) {
 cudaError_t launch_draft_fused_tc(const void* U, const void* W1, const void* W2t, const int32_t* anchor,
                                   int32_t* tokens, float* logit_x, float* lse, int bs, int gamma, int V, int r,
                                   float inv_tau, int greedy, uint64_t seed, uint64_t step, void* entries,
-                                  int n_chunks, uint32_t* status, unsigned* gsync, int* gabort, cudaStream_t s) {
+                                  int n_chunks, uint32_t* status, int* sync_words, cudaStream_t s) {
   if (!tch::encode_fn()) return cudaErrorNotSupported;
   CUtensorMap map_w2, map_u;
   if (!tch::encode_bf16_2d(&map_w2, W2t, size_t(V), size_t(r), kBN)) return cudaErrorInvalidValue;
@@ -1093,11 +1121,12 @@ cudaError_t launch_draft_fused_tc(const void* U, const void* W1, const void* W2t
   prm.seed = seed;
   prm.step = step;
   prm.status = status;
-  prm.gsync = gsync;
-  prm.gabort = gabort;
+  prm.gabort = sync_words;
+  prm.fslot = sync_words + 32;
+  prm.frow = sync_words + 32 + grid;
   prm.timeout_ns = g_wait_timeout_ns;
-  if (cudaMemsetAsync(gsync, 0, sizeof(unsigned), s) != cudaSuccess) return cudaErrorUnknown;
-  if (cudaMemsetAsync(gabort, 0, sizeof(int), s) != cudaSuccess) return cudaErrorUnknown;
+  if (32 + grid + bs > kSyncWords) return cudaErrorInvalidValue;
+  if (cudaMemsetAsync(sync_words, 0, sizeof(int) * size_t(32 + grid + bs), s) != cudaSuccess) return cudaErrorUnknown;
   // cooperative: the grid barriers need every CTA resident (the launch fails otherwise)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
