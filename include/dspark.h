@@ -109,12 +109,6 @@ DSPARK_API uint64_t dspark_set_wait_timeout_ns(uint64_t ns);
 DSPARK_API int dspark_build_sps(const double* T_raw, int m_max, const int32_t* tiers, int n_tiers,
                      double* sps_out);
 
-/* Whether dspark_draft_block runs as one cooperative launch on the current device for these
- * sizes (bf16, r a multiple of 64, every CTA of the vocabulary grid resident): 1 yes, 0 no (the
- * draft then launches its kernels stage by stage, with the same results).  The page has no
- * counterpart: it is a property of this implementation, for callers and tests. */
-DSPARK_API int dspark_draft_single_launch(int dtype, int bs, int gamma, int V, int r);
-
 /* S1. Markov-head block draft ([SUMMARY] "Architecture (drafter)", Markov head and
  * left-to-right sampling).  For k = 1..gamma, per request:
  *     l_k = U[:, k-1] + W1[x_{k-1}] . W2,   W2 = W2t^T,  x_0 = anchor

@@ -29,7 +29,6 @@ _SIGS = {
     "dspark_read_device_status": (_i, [_vp, _vp]),
     "dspark_build_sps": (_i, [_vp, _i, _vp, _i, _vp]),
     "dspark_set_wait_timeout_ns": (_u64, [_u64]),
-    "dspark_draft_single_launch": (_i, [_i, _i, _i, _i, _i]),
     "dspark_draft_block": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _u64, _u64,
                                 _vp, _vp, _vp, _vp, _sz, _vp]),
     "dspark_draft_block_noalloc": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _u64, _u64,
@@ -152,11 +151,6 @@ def dspark_draft_block(U, W1, W2t, anchor, temperature, seed, step, tokens, logi
     _check(lib().dspark_draft_block(_p(U), _p(W1), _p(W2t), _dtype(U), _p(anchor), bs, gamma, V, r,
                                     float(temperature), int(seed), int(step), _p(tokens), _p(logit_x),
                                     _p(lse), _p(ws), ws.numel(), _stream(stream)), "dspark_draft_block")
-
-
-def dspark_draft_single_launch(dtype: int, bs: int, gamma: int, V: int, r: int) -> bool:
-    """Whether dspark_draft_block runs as one cooperative launch on the current device."""
-    return bool(lib().dspark_draft_single_launch(int(dtype), int(bs), int(gamma), int(V), int(r)))
 
 
 def dspark_draft_block_noalloc(U, W1, W2t, anchor, temperature, seed, step, tokens, logit_x, lse,

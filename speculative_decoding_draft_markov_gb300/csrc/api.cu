@@ -120,14 +120,6 @@ int dspark_draft_block(const void* U, const void* W1, const void* W2t, int dtype
   const int greedy = temperature == 0.f;
   const float inv_tau = greedy ? 1.f : static_cast<float>(1.0 / static_cast<double>(temperature));
   const bool tc = draft_tc_supported(dtype, bs, V, r);
-  if (tc && draft_fused_available(dtype, bs, gamma, V, r)) {
-    // one cooperative launch for the whole block; the launch-per-stage path below otherwise
-    int* sync_words = reinterpret_cast<int*>(w + L.sync);
-    const cudaError_t e = launch_draft_fused_tc(U, W1, W2t, anchor, tokens, logit_x, lse, bs, gamma, V, r, inv_tau,
-                                                greedy, seed, step, stats, L.n_chunks, status, sync_words, s);
-    if (e == cudaSuccess) return DSPARK_OK;
-    cudaGetLastError();  // a launch the device could not take leaves no error behind
-  }
   for (int k = 1; k <= gamma; ++k) {
     int n_slots = L.n_chunks;
     cudaError_t e = tc ? launch_draft_stats_tc(U, W1, W2t, anchor, tokens, bs, gamma, V, r, k, inv_tau,
@@ -140,11 +132,6 @@ int dspark_draft_block(const void* U, const void* W1, const void* W2t, int dtype
     if (e != cudaSuccess) return DSPARK_ECUDA;
   }
   return DSPARK_OK;
-}
-
-int dspark_draft_single_launch(int dtype, int bs, int gamma, int V, int r) {
-  if (!valid_dtype(dtype) || check_core(bs, gamma, V, r) != 0) return 0;
-  return draft_fused_available(dtype, bs, gamma, V, r) ? 1 : 0;
 }
 
 int dspark_confidence(const void* h, const void* W1, int dtype, const int32_t* anchor,

@@ -41,7 +41,6 @@ enum DecisionKind : int { kDecNone = 0, kDecResidual = 1, kDecBonus = 2 };
 //              verify's DecideEntry [bs][n_slots], n_slots <= n_chunks
 //   rowstats : RowStat [bs * (gamma + 1)]  per packed target row
 //   dec      : Decision [bs]               per-request verify decision
-//   sync     : int [kSyncWords]            the single-launch draft's flags
 // ----------------------------------------------------------------------------------------
 struct RowStat {
   float lse;     // log-sum-exp of the tempered target row (temperature > 0)
@@ -77,12 +76,8 @@ __host__ __device__ inline size_t stats_bytes(int bs, int n_chunks) {
   return size_t(bs) * n_chunks * sizeof(DecideEntry);
 }
 
-// Synchronisation words of the single-launch draft: an abort word, one flag per CTA and one
-// per request (zeroed by the draft before each launch).
-constexpr int kSyncWords = 2048;
-
 struct WsLayout {
-  size_t status = 0, stats = 0, rowstats = 0, dec = 0, sync = 0, total = 0;
+  size_t status = 0, stats = 0, rowstats = 0, dec = 0, total = 0;
   int n_chunks = 0;
 };
 
@@ -98,8 +93,6 @@ __host__ __device__ inline WsLayout ws_layout(int bs, int gamma, int V) {
   off += align256(size_t(bs) * (gamma + 1) * sizeof(RowStat));
   L.dec = off;
   off += align256(size_t(bs) * sizeof(Decision));
-  L.sync = off;
-  off += align256(size_t(kSyncWords) * sizeof(int));
   L.total = off;
   return L;
 }

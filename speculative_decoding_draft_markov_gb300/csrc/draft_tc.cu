@@ -416,576 +416,6 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
   }
 }
 
-
-// ===================================================================================
-// All gamma positions in one cooperative launch (every CTA resident, one per SM).  Per
-// position k the CTA runs the vocabulary pass above, publishes its entries (a per-CTA flag),
-// and selects up to two requests (one per epilogue warp set) as soon as the entries of every
-// CTA of the request's M-tile are published; each select publishes its token (a per-request
-// flag), and a CTA starts position k + 1 as soon as the tokens of its own 128 rows are there.
-// No grid-wide barrier: every wait is on the data it needs.  The producer keeps streaming
-// U_{k+1} and W2t into its rings meanwhile.  Flags hold the last position published (release
-// stores, acquire loads); every wait is bounded and a CTA that gives up sets `gabort`, which
-// ends the others' waits.  Write-after-read safety: a CTA overwrites its entries (position
-// k + 1) only after the tokens of its rows -- written by the selects that read those entries
-// -- are published.
-// ===================================================================================
-constexpr int kFusedBStages = 5;
-
-struct SelScratch {
-  float a[256];    // W1[x_{k-1}] of the request, fp32
-  float tv[kBN];   // the drawn chunk's tempered logits
-  float rv[4];
-  int ri[4];
-  float lse;
-  float best;
-  int win;
-  int fail;  // the merge gave up waiting for the entries
-};
-
-struct FusedBarriers {
-  uint64_t b_full[kFusedBStages], b_empty[kFusedBStages];
-  uint64_t u_full[kUStages], u_empty[kUStages];
-  uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
-  uint64_t drain;
-  uint64_t a_ready;  // phase k - 1: the A operand of position k is in shared memory
-  uint32_t tmem_base;
-  int abort;
-  int xrow[kBM];
-  float4 xch[kBM];
-  SelScratch sel[2];
-};
-
-struct FusedParams {
-  const __nv_bfloat16* W1;
-  const __nv_bfloat16* W2t;
-  const __nv_bfloat16* U;
-  const int32_t* anchor;
-  int32_t* tokens;
-  float* logit_x;
-  float* lse;
-  int bs, gamma, V, r;
-  float inv_tau;
-  int greedy;
-  int n_chunks;
-  int n_slots;
-  float4* entries;
-  uint64_t seed, step;
-  uint32_t* status;
-  int* fslot;       // [gridDim.x]: last position whose entries the CTA published (zero at launch)
-  int* frow;        // [bs]: last position whose token the request's select published (zero)
-  int* gabort;      // set by a CTA that gives up (zero at launch)
-  uint64_t timeout_ns;
-};
-
-constexpr size_t fused_smem_bytes(int r) {
-  return size_t(r / kBK) * kAtomBytes + kFusedBStages * size_t(kAtomBytes) + kUStages * 2 * size_t(kUHalf) +
-         sizeof(FusedBarriers);
-}
-static_assert(fused_smem_bytes(256) <= 232448, "dynamic shared memory beyond the 227 KB per-block limit");
-
-// Barrier among the epilogue warps (named barrier 1) that also returns, to every thread, the OR
-// of `pred` over them: the uniform way for the warps to agree to stop.
-__device__ __forceinline__ bool epi_barrier_or(bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"(pred ? 1u : 0u), "n"(kEpiThreads)
-      : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ void group_barrier(int g) {  // the four warps of epilogue set g
-  asm volatile("bar.sync %0, 128;" ::"r"(2 + g) : "memory");
-}
-
-__device__ __forceinline__ int ld_acquire_gpu_s32(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_gpu_s32(int* p, int v) {
-  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Wait until *flag >= want (acquire), bounded by `dl` and by another CTA's give-up; false on
-// give-up, which this call also announces through gabort.
-__device__ bool wait_flag(const int* flag, int want, int* gabort, long long dl) {
-  while (ld_acquire_gpu_s32(flag) < want) {
-    if (*reinterpret_cast<volatile int*>(gabort)) return false;
-    if (clock64() > dl) {
-      atomicExch(gabort, 1);
-      return false;
-    }
-    __nanosleep(100);  // few polling requests: the flags' L2 lines serve other traffic too
-  }
-  return true;
-}
-
-// 32 consecutive vocabulary ids v0 .. v0 + 31 of W1[x] W2t^T by one warp: lane l takes K values
-// 8l .. 8l + 7 of every id (all 32 loads issued first), then a fixed shuffle tree per id.
-__device__ __forceinline__ void dots32(const __nv_bfloat16* __restrict__ W2t, int r, int V, int v0,
-                                       const float* __restrict__ a, float* out, int lane) {
-  const bool on = lane * 8 < r;
-  float av[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) av[e] = on ? a[lane * 8 + e] : 0.f;
-  uint4 q[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const int v = v0 + j;
-    q[j] = (on && v < V) ? *reinterpret_cast<const uint4*>(W2t + size_t(v) * r + lane * 8) : make_uint4(0u, 0u, 0u, 0u);
-  }
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    float acc = bf16lo(q[j].x) * av[0];
-    acc = fmaf(bf16hi(q[j].x), av[1], acc);
-    acc = fmaf(bf16lo(q[j].y), av[2], acc);
-    acc = fmaf(bf16hi(q[j].y), av[3], acc);
-    acc = fmaf(bf16lo(q[j].z), av[4], acc);
-    acc = fmaf(bf16hi(q[j].z), av[5], acc);
-    acc = fmaf(bf16lo(q[j].w), av[6], acc);
-    acc = fmaf(bf16hi(q[j].w), av[7], acc);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-    if (lane == j) out[j] = acc;
-  }
-}
-
-__global__ void __launch_bounds__(kThreads, 1) draft_fused_kernel(const __grid_constant__ CUtensorMap tmap_w2,
-                                                                   const __grid_constant__ CUtensorMap tmap_u,
-                                                                   const FusedParams p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  if (tc::smem_u32(smem_raw) & 1023u) {
-    if (threadIdx.x == 0) {
-      set_status(p.status, DSPARK_EUNSUPPORTED);
-      atomicExch(p.gabort, 1);  // the other CTAs must not wait for this one
-    }
-    return;
-  }
-  const int nk = p.r / kBK;
-  uint8_t* sA = smem_raw;
-  uint8_t* sB = sA + nk * kAtomBytes;
-  uint8_t* sU = sB + kFusedBStages * kAtomBytes;
-  FusedBarriers* bar = reinterpret_cast<FusedBarriers*>(sU + kUStages * 2 * kUHalf);
-  volatile int* abort_flag = &bar->abort;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bs = p.bs, V = p.V, r = p.r, gamma = p.gamma;
-  const int n_mt = (bs + kBM - 1) / kBM;
-  const int m0 = (blockIdx.x % n_mt) * kBM;
-  const int cstride = gridDim.x / n_mt;
-  const int c0 = blockIdx.x / n_mt;
-  const int n_tiles = (c0 < p.n_chunks) ? (p.n_chunks - c0 + cstride - 1) / cstride : 0;
-
-  if (tid == 0) {
-    for (int s = 0; s < kFusedBStages; ++s) {
-      tc::mbar_init(tc::smem_u32(&bar->b_full[s]), 1);
-      tc::mbar_init(tc::smem_u32(&bar->b_empty[s]), 1);
-    }
-    for (int s = 0; s < kUStages; ++s) {
-      tc::mbar_init(tc::smem_u32(&bar->u_full[s]), 1);
-      tc::mbar_init(tc::smem_u32(&bar->u_empty[s]), kEpiWarps / 2);
-    }
-    for (int s = 0; s < kAccBufs; ++s) {
-      tc::mbar_init(tc::smem_u32(&bar->acc_full[s]), 1);
-      tc::mbar_init(tc::smem_u32(&bar->acc_empty[s]), kEpiWarps / 2);
-    }
-    tc::mbar_init(tc::smem_u32(&bar->drain), 1);
-    tc::mbar_init(tc::smem_u32(&bar->a_ready), kEpiWarps);
-    bar->abort = 0;
-    tc::fence_mbar_init();
-    tc::prefetch_tensormap(&tmap_w2);
-    tc::prefetch_tensormap(&tmap_u);
-  }
-  if (warp == 1) {
-    tc::tmem_alloc(tc::smem_u32(&bar->tmem_base), kTmemCols);
-    tc::tmem_relinquish();
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  const uint32_t tmem_base = bar->tmem_base;
-  // the rings' waits span every position: one timeout per position
-  const long long deadline =
-      tc::deadline_after_ns(p.timeout_ns > (1ull << 56) ? p.timeout_ns : p.timeout_ns * uint64_t(gamma + 1));
-
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t keep = tc::policy_evict_last(), stream = tc::policy_evict_first();
-      int bstage = 0, bph = 0;
-      int uuse[kUStages] = {0, 0};
-      int b_issued[kFusedBStages], u_issued[kUStages];
-      for (int s = 0; s < kFusedBStages; ++s) b_issued[s] = -1;
-      for (int s = 0; s < kUStages; ++s) u_issued[s] = -1;
-      bool ok = true;
-      for (int k = 1; k <= gamma && ok; ++k) {
-        for (int t = 0; t < n_tiles && ok; ++t) {
-          const int n0 = (c0 + t * cstride) * kBN;
-          const int us = t & 1, uph = uuse[us] & 1;
-          if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->u_empty[us]), uph ^ 1, deadline, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const uint32_t ufull = tc::smem_u32(&bar->u_full[us]);
-          tc::mbar_arrive_expect_tx(ufull, 2 * kUHalf);
-          const uint32_t ud = tc::smem_u32(sU + us * 2 * kUHalf);
-          tc::tma_load_3d(ud, &tmap_u, ufull, n0, k - 1, m0, stream);
-          tc::tma_load_3d(ud + kUHalf, &tmap_u, ufull, n0 + 64, k - 1, m0, stream);
-          u_issued[us] = uph;
-          ++uuse[us];
-          for (int kb = 0; kb < nk; ++kb) {
-            if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->b_empty[bstage]), bph ^ 1, deadline, abort_flag)) {
-              ok = false;
-              break;
-            }
-            const uint32_t bfull = tc::smem_u32(&bar->b_full[bstage]);
-            tc::mbar_arrive_expect_tx(bfull, kAtomBytes);
-            tc::tma_load_2d(tc::smem_u32(sB + bstage * kAtomBytes), &tmap_w2, bfull, kb * kBK, n0, keep);
-            b_issued[bstage] = bph;
-            if (++bstage == kFusedBStages) { bstage = 0; bph ^= 1; }
-          }
-        }
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        set_status(p.status, DSPARK_ETIMEOUT);
-        const long long dl = tc::deadline_after_ns(200000000ull);
-        const volatile int never = 0;
-        for (int s = 0; s < kFusedBStages; ++s)
-          if (b_issued[s] >= 0) tc::mbar_wait_bounded(tc::smem_u32(&bar->b_full[s]), b_issued[s], dl, &never);
-        for (int s = 0; s < kUStages; ++s)
-          if (u_issued[s] >= 0) tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[s]), u_issued[s], dl, &never);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
-      int bstage = 0, bph = 0;
-      int ause[kAccBufs] = {0, 0};
-      bool ok = true, issued = false;
-      for (int k = 1; k <= gamma && ok; ++k) {
-        if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->a_ready), (k - 1) & 1, deadline, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc::tc_fence_after();
-        for (int t = 0; t < n_tiles && ok; ++t) {
-          const int ab = t & 1, aph = ause[ab] & 1;
-          if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_empty[ab]), aph ^ 1, deadline, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc::tc_fence_after();
-          const uint32_t d = tmem_base + ab * kBN;
-          for (int kb = 0; kb < nk; ++kb) {
-            if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->b_full[bstage]), bph, deadline, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc::tc_fence_after();
-            const uint32_t a_addr = tc::smem_u32(sA + kb * kAtomBytes);
-            const uint32_t b_addr = tc::smem_u32(sB + bstage * kAtomBytes);
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-              tc::mma_bf16(d, tc::sdesc_kmajor_sw128(a_addr + kk * 32), tc::sdesc_kmajor_sw128(b_addr + kk * 32),
-                           idesc, (kb | kk) != 0);
-            issued = true;
-            tc::mma_commit(tc::smem_u32(&bar->b_empty[bstage]));
-            if (++bstage == kFusedBStages) { bstage = 0; bph ^= 1; }
-          }
-          if (!ok) break;
-          tc::mma_commit(tc::smem_u32(&bar->acc_full[ab]));
-          ++ause[ab];
-        }
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        set_status(p.status, DSPARK_ETIMEOUT);
-        if (issued) {
-          tc::mma_commit(tc::smem_u32(&bar->drain));
-          const volatile int never = 0;
-          tc::mbar_wait_bounded(tc::smem_u32(&bar->drain), 0, tc::deadline_after_ns(200000000ull), &never);
-        }
-      }
-    }
-  } else {
-    // ------------------------------------------------------------------ epilogue + select
-    const int wq = warp & 3;
-    const int m = wq * 32 + lane;
-    const int half = (warp - 2) >> 2;
-    const int grow = m0 + m;
-    const float inv_tau = p.inv_tau;
-    const float c2 = inv_tau * kLog2e;
-    const int et = tid - 64;  // 0 .. 255
-    const uint32_t taddr = tmem_base + (uint32_t(wq * 32) << 16) + half * kBN;
-    const uint8_t* ub = sU + half * 2 * kUHalf + m * 128;
-    int ause = 0;  // tiles this warp set has taken (accumulator buffer and U stage `half`)
-    bool stop = false;
-    // chunk Gumbels of a position's first kGReg tiles of the set: independent of the tokens, so
-    // those of position k + 1 are drawn while other CTAs finish the selects of position k
-    constexpr int kGReg = 8;
-    float gk[kGReg];
-    auto draw_gumbels = [&](int kk) {
-#pragma unroll
-      for (int i = 0; i < kGReg; ++i) {
-        const int t = half + 2 * i;
-        gk[i] = 0.f;
-        if (!p.greedy && t < n_tiles) {
-          const int c = c0 + t * cstride;
-          const uint4 w = philox_group(p.seed, p.step, kDraftChunk, uint32_t(grow), kk, uint32_t(c) >> 2);
-          gk[i] = gumbel_from_bits(pick_word(w, c & 3));
-        }
-      }
-    };
-    draw_gumbels(1);
-    for (int k = 1; k <= gamma; ++k) {
-      // A operand: W1[x_{k-1}] of rows m0 .. m0 + 127.  The tokens of position k - 1 come from
-      // the selects of other CTAs: wait for each row's flag, then read through L2.
-      bool tok_fail = false;
-      if (et < 32) {  // one warp polls the 128 rows' flags, four per lane
-        const long long dl = tc::deadline_after_ns(p.timeout_ns);
-        for (int mm = et; mm < kBM; mm += 32) {
-          const int gr = m0 + mm;
-          int xp = -1;
-          if (gr < bs) {
-            if (k == 1) {
-              xp = clamp_token(p.anchor[gr], V);
-            } else if (wait_flag(p.frow + gr, k - 1, p.gabort, dl)) {
-              xp = clamp_token(__ldcg(p.tokens + size_t(gr) * gamma + k - 2), V);
-            } else {
-              tok_fail = true;
-            }
-          }
-          bar->xrow[mm] = xp;
-        }
-      }
-      stop = epi_barrier_or(tok_fail);
-      if (stop) break;
-      {
-        const int cpr = r / 8;
-        for (int idx = et; idx < kBM * cpr; idx += kEpiThreads) {
-          const int row = idx / cpr, ch = idx % cpr;
-          const int xp = bar->xrow[row];
-          const int kb = ch >> 3, j = ch & 7;
-          const uint32_t dst = tc::smem_u32(sA + kb * kAtomBytes + row * 128 + ((j ^ (row & 7)) << 4));
-          cp_async16(dst, xp >= 0 ? p.W1 + size_t(xp) * r + ch * 8 : p.W1, xp >= 0 ? 16u : 0u);
-        }
-        cp_async_wait_all();
-        tc::fence_proxy_async_smem();
-      }
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->a_ready));
-
-      // ---- vocabulary pass of position k: running partial draw of this row
-      float run_m = -INFINITY, run_s = 0.f, best_key = -INFINITY;
-      int best_c = INT_MAX;
-      bool gave_up = false;
-      for (int t = half, i = 0; t < n_tiles; t += 2, ++i) {
-        const int c = c0 + t * cstride;
-        const int n0 = c * kBN;
-        const int valid = min(kBN, V - n0);
-        const int ph = ause & 1;
-        bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[half]), ph, deadline, abort_flag) &&
-                  tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[half]), ph, deadline, abort_flag);
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        if (!ok) {
-          *abort_flag = 1;
-          set_status(p.status, DSPARK_ETIMEOUT);
-          gave_up = true;
-          break;
-        }
-        ++ause;
-        tc::tc_fence_after();
-        float v[kBN];
-#pragma unroll
-        for (int q = 0; q < kBN / 32; ++q) tc::tmem_ld32(taddr + q * 32, reinterpret_cast<uint32_t*>(v + q * 32));
-        tc::tmem_ld_wait();
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[half]));
-#pragma unroll
-        for (int j = 0; j < kBN / 8; ++j) {
-          const uint4 q = *reinterpret_cast<const uint4*>(ub + (j >> 3) * kUHalf + (((j & 7) ^ (m & 7)) << 4));
-          v[8 * j + 0] += bf16lo(q.x); v[8 * j + 1] += bf16hi(q.x);
-          v[8 * j + 2] += bf16lo(q.y); v[8 * j + 3] += bf16hi(q.y);
-          v[8 * j + 4] += bf16lo(q.z); v[8 * j + 5] += bf16hi(q.z);
-          v[8 * j + 6] += bf16lo(q.w); v[8 * j + 7] += bf16hi(q.w);
-        }
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->u_empty[half]));
-        if (p.greedy) {
-          float best = -INFINITY;
-          int bi = INT_MAX;
-#pragma unroll
-          for (int q = 0; q < kBN; ++q)
-            if (q < valid && v[q] > best) { best = v[q]; bi = q; }
-          if (best > best_key) { best_key = best; best_c = n0 + bi; }
-        } else {
-          const float mx = valid == kBN ? row_max<false>(v, valid) : row_max<true>(v, valid);
-          const float sc = valid == kBN ? row_sum_exp2<false>(v, valid, mx * c2, c2)
-                                        : row_sum_exp2<true>(v, valid, mx * c2, c2);
-          float g;
-          if (i < kGReg) {
-            g = gk[0];
-#pragma unroll
-            for (int j = 0; j + 1 < kGReg; ++j) gk[j] = gk[j + 1];
-          } else {
-            g = chunk_gumbel_call(p.seed, p.step, grow, k, c);
-          }
-          if (mx > -INFINITY) {
-            const float key = mx * inv_tau + logf(sc) + g;
-            if (key > best_key) { best_key = key; best_c = c; }
-            const float m2 = mx * c2;
-            if (m2 > run_m) {
-              run_s = run_s * exp2f(run_m - m2) + sc;
-              run_m = m2;
-            } else {
-              run_s += sc * exp2f(m2 - run_m);
-            }
-          }
-        }
-      }
-      run_m *= 0.69314718055994531f;
-      if (half == 1) bar->xch[m] = make_float4(run_m, run_s, best_key, __int_as_float(best_c));
-      stop = epi_barrier_or(gave_up);
-      if (stop) break;
-      if (half == 0) {
-        const float4 o = bar->xch[m];
-        const LsePair l = lse_merge(LsePair{run_m, run_s}, LsePair{o.x, o.y});
-        const ArgMax a = better(ArgMax{best_key, best_c}, ArgMax{o.z, __float_as_int(o.w)});
-        if (grow < bs) p.entries[size_t(grow) * p.n_slots + c0] = make_float4(l.m, l.s, a.v, __int_as_float(a.i));
-      }
-      // ---- publish this CTA's entries of position k
-      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-      if (et == 0) st_release_gpu_s32(p.fslot + blockIdx.x, k);
-
-      // ---- select of position k: request blockIdx.x + g * gridDim.x by warp set g
-      {
-        const int g = half, gt = et - 128 * g, gw = gt >> 5;
-        SelScratch& S = bar->sel[g];
-        const int rq = blockIdx.x + g * gridDim.x;
-        const bool act = rq < bs;
-        if (act) {
-          if (gw == 0) {  // merge the request's entries: row LSE and the winner
-            // the entries of slot s come from CTA s * n_mt + (rq's M-tile): wait for them
-            const int mt = rq / kBM;
-            const long long dl = tc::deadline_after_ns(p.timeout_ns);
-            bool ok = true;
-            for (int sl = lane; sl < p.n_slots && ok; sl += 32) ok = wait_flag(p.fslot + sl * n_mt + mt, k, p.gabort, dl);
-            ok = __all_sync(0xFFFFFFFFu, ok);
-            if (lane == 0) S.fail = ok ? 0 : 1;
-            const float4* en = p.entries + size_t(rq) * p.n_slots;
-            LsePair lp{-INFINITY, 0.f};
-            ArgMax best{-INFINITY, INT_MAX};
-            for (int i0 = lane; i0 < p.n_slots; i0 += 32 * 5) {  // five loads in flight per lane
-              float4 e[5];
-#pragma unroll
-              for (int q = 0; q < 5; ++q)
-                e[q] = (i0 + 32 * q < p.n_slots) ? __ldcg(en + i0 + 32 * q)
-                                                 : make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(INT_MAX));
-#pragma unroll
-              for (int q = 0; q < 5; ++q) {
-                lp = lse_merge(lp, LsePair{e[q].x, e[q].y});
-                best = better(best, ArgMax{e[q].z, __float_as_int(e[q].w)});
-              }
-            }
-            lp = warp_lse(lp);
-            best = warp_argmax(best);
-            if (lane == 0) {
-              S.lse = lp.m + logf(lp.s);
-              S.best = best.v;
-              S.win = best.i;
-            }
-          } else if (!p.greedy && gw == 1) {  // the W1 row of x_{k-1}: 16 bytes per lane
-            const int xp = clamp_token((k == 1) ? p.anchor[rq] : __ldcg(p.tokens + size_t(rq) * gamma + k - 2), V);
-            if (lane * 8 < r) {
-              float x[8];
-              const uint4 q = *reinterpret_cast<const uint4*>(p.W1 + size_t(xp) * r + lane * 8);
-              x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
-              x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) S.a[lane * 8 + e] = x[e];
-            }
-          }
-        }
-        group_barrier(g);
-        const bool sel_fail = act && S.fail;
-        if (sel_fail) {
-        } else if (act && p.greedy) {
-          if (gt == 0) {
-            const size_t out = size_t(rq) * gamma + (k - 1);
-            p.tokens[out] = (S.win == INT_MAX) ? 0 : S.win;
-            p.logit_x[out] = S.best;
-            p.lse[out] = 0.f;
-            st_release_gpu_s32(p.frow + rq, k);  // publish x_k of the request
-          }
-        } else if (act) {
-          const int cstar = (S.win == INT_MAX) ? 0 : S.win;
-          const int v_own = cstar * kBN + gt;
-          const float u_v = (v_own < V) ? __bfloat162float(p.U[(size_t(rq) * gamma + (k - 1)) * V + v_own]) : 0.f;
-          dots32(p.W2t, r, V, cstar * kBN + gw * 32, S.a, S.tv + gw * 32, lane);
-          group_barrier(g);
-          const float tt = (v_own < V) ? (S.tv[gt] + u_v) * inv_tau : -INFINITY;
-          ArgMax e{-INFINITY, INT_MAX};
-          if (tt > -INFINITY) {
-            const uint4 w = philox_group(p.seed, p.step, kDraftElem, uint32_t(rq), k, uint32_t(gt) >> 2);
-            e = ArgMax{tt + gumbel_from_bits(pick_word(w, gt & 3)), gt};
-          }
-          e = warp_argmax(e);
-          if (lane == 0) { S.rv[gw] = e.v; S.ri[gw] = e.i; }
-          group_barrier(g);  // S.tv reads above are done before thread 0 reads rv / ri
-          if (gt == 0) {
-            ArgMax b2{S.rv[0], S.ri[0]};
-#pragma unroll
-            for (int w = 1; w < 4; ++w) b2 = better(b2, ArgMax{S.rv[w], S.ri[w]});
-            const int ei = (b2.i == INT_MAX) ? 0 : b2.i;
-            const float te = (cstar * kBN + ei < V) ? (S.tv[ei] + __bfloat162float(
-                                                          p.U[(size_t(rq) * gamma + (k - 1)) * V + cstar * kBN + ei])) * inv_tau
-                                                    : -INFINITY;
-            const size_t out = size_t(rq) * gamma + (k - 1);
-            const int xk = min(cstar * kBN + ei, V - 1);
-            p.tokens[out] = xk;
-            p.logit_x[out] = te;
-            p.lse[out] = S.lse;
-            st_release_gpu_s32(p.frow + rq, k);  // publish x_k of the request
-            if (k < gamma) {  // the next gathers read W1[x_k]: warm L2 now
-              const char* row = reinterpret_cast<const char*>(p.W1 + size_t(xk) * r);
-              for (int q = 0; q < r * 2; q += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + q));
-            }
-          }
-        } else if (!p.greedy) {
-          group_barrier(g);  // same barrier sequence as the active groups of this CTA
-          group_barrier(g);
-        }
-        if (sel_fail && !p.greedy) {  // keep the group's barrier count of an active select
-          group_barrier(g);
-          group_barrier(g);
-        }
-        // a select that gave up stops the CTA (every epilogue warp agrees below)
-        if (epi_barrier_or(sel_fail)) {
-          stop = true;
-          break;
-        }
-      }
-      if (k < gamma) draw_gumbels(k + 1);
-    }
-    if (stop) {
-      *abort_flag = 1;  // the producer and the MMA issuer stop waiting
-      if (et == 0) atomicExch(p.gabort, 1);  // and so do the other CTAs' flag waits
-      set_status(p.status, DSPARK_ETIMEOUT);
-    }
-  }
-
-  tc::tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc::tc_fence_after();
-    tc::tmem_dealloc(tmem_base, kTmemCols);
-  }
-}
-
 }  // namespace
 
 uint64_t g_wait_timeout_ns = 1000000000ull;  // 1 s; changed only through dspark_set_wait_timeout_ns
@@ -1044,101 +474,6 @@ cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, draft_tc_kernel, map_w2, map_u, prm);
-}
-
-
-bool draft_fused_available(int dtype, int bs, int gamma, int V, int r) {
-  if (!draft_tc_supported(dtype, bs, V, r)) return false;
-  const int n_chunks = (V + kChunk - 1) / kChunk;
-  const int grid = tch::vocab_grid(bs, n_chunks);
-  if (2 * grid < bs) return false;
-  // resident CTAs per SM for this r, queried once per device
-  static int per_sm_cache[tch::kMaxDevices][4] = {};
-  static bool smem_set[tch::kMaxDevices] = {};
-  static std::mutex mu;
-  const int dev = tch::current_device();
-  if (dev < 0 || dev >= tch::kMaxDevices) return false;
-  int per_sm;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    int& c = per_sm_cache[dev][r / kBK - 1];
-    if (c == 0) {
-      if (!smem_set[dev]) {
-        if (cudaFuncSetAttribute(draft_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(fused_smem_bytes(256))) != cudaSuccess)
-          return false;
-        smem_set[dev] = true;
-      }
-      int n = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, draft_fused_kernel, kThreads, fused_smem_bytes(r)) !=
-          cudaSuccess) {
-        cudaGetLastError();
-        return false;
-      }
-      c = n > 0 ? n : -1;
-    }
-    per_sm = c;
-  }
-  (void)gamma;
-  return per_sm >= 1 && grid <= per_sm * tch::sm_count();
-}
-
-cudaError_t launch_draft_fused_tc(const void* U, const void* W1, const void* W2t, const int32_t* anchor,
-                                  int32_t* tokens, float* logit_x, float* lse, int bs, int gamma, int V, int r,
-                                  float inv_tau, int greedy, uint64_t seed, uint64_t step, void* entries,
-                                  int n_chunks, uint32_t* status, int* sync_words, cudaStream_t s) {
-  if (!tch::encode_fn()) return cudaErrorNotSupported;
-  CUtensorMap map_w2, map_u;
-  if (!tch::encode_bf16_2d(&map_w2, W2t, size_t(V), size_t(r), kBN)) return cudaErrorInvalidValue;
-  {
-    const cuuint64_t dims[3] = {cuuint64_t(V), cuuint64_t(gamma), cuuint64_t(bs)};
-    const cuuint64_t strides[2] = {cuuint64_t(V) * 2, cuuint64_t(gamma) * V * 2};
-    const cuuint32_t box[3] = {64, 1, kBM};
-    const cuuint32_t es[3] = {1, 1, 1};
-    if (tch::encode_fn()(&map_u, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(U), dims, strides, box, es,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  if (!draft_fused_available(DSPARK_BF16, bs, gamma, V, r)) return cudaErrorNotSupported;
-  const int grid = tch::vocab_grid(bs, n_chunks);
-  const int n_mt = (bs + kBM - 1) / kBM;
-  if (2 * grid < bs) return cudaErrorNotSupported;  // two selects per CTA at most
-  FusedParams prm{};
-  prm.W1 = static_cast<const __nv_bfloat16*>(W1);
-  prm.W2t = static_cast<const __nv_bfloat16*>(W2t);
-  prm.U = static_cast<const __nv_bfloat16*>(U);
-  prm.anchor = anchor;
-  prm.tokens = tokens;
-  prm.logit_x = logit_x;
-  prm.lse = lse;
-  prm.bs = bs; prm.gamma = gamma; prm.V = V; prm.r = r;
-  prm.inv_tau = inv_tau;
-  prm.greedy = greedy;
-  prm.n_chunks = n_chunks;
-  prm.n_slots = grid / n_mt;
-  prm.entries = static_cast<float4*>(entries);
-  prm.seed = seed;
-  prm.step = step;
-  prm.status = status;
-  prm.gabort = sync_words;
-  prm.fslot = sync_words + 32;
-  prm.frow = sync_words + 32 + grid;
-  prm.timeout_ns = g_wait_timeout_ns;
-  if (32 + grid + bs > kSyncWords) return cudaErrorInvalidValue;
-  if (cudaMemsetAsync(sync_words, 0, sizeof(int) * size_t(32 + grid + bs), s) != cudaSuccess) return cudaErrorUnknown;
-  // cooperative: the grid barriers need every CTA resident (the launch fails otherwise)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = fused_smem_bytes(r);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, draft_fused_kernel, map_w2, map_u, prm);
 }
 
 }  // namespace dspark

@@ -22,13 +22,6 @@ cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t
                                   uint64_t step, void* entries, int n_chunks, int* n_slots,
                                   uint32_t* status, cudaStream_t s);
 bool draft_tc_supported(int dtype, int bs, int V, int r);
-// All gamma positions in one cooperative launch (vocabulary passes, grid barriers, selects).
-// sync_words: the workspace's kSyncWords synchronisation words (zeroed here before the launch).
-bool draft_fused_available(int dtype, int bs, int gamma, int V, int r);
-cudaError_t launch_draft_fused_tc(const void* U, const void* W1, const void* W2t, const int32_t* anchor,
-                                  int32_t* tokens, float* logit_x, float* lse, int bs, int gamma, int V, int r,
-                                  float inv_tau, int greedy, uint64_t seed, uint64_t step, void* entries,
-                                  int n_chunks, uint32_t* status, int* sync_words, cudaStream_t s);
 // Verify's decision masses on the tensor cores (bf16): per request and CTA column a
 // DecideEntry (common.cuh) over the column's chunks of the request's deciding row (residual
 // mass sum max(0, p_t - p_d), target mass sum p_t, best chunk keys); n_slots returned.
