@@ -186,7 +186,8 @@ DSPARK_API int dspark_pack(const int32_t* window, const int32_t* anchor, const i
  *     log p_t = target_row/temperature at x_k minus its log-sum-exp, log p_d = logit_x - lse,
  *     u_k the accept uniform (purpose 3, position k, index 0).  At the first rejection
  *     k* <= L_commit the token is redrawn from normalise(max(0, p_t - p_d)) (p_t if that is
- *     empty), p_d recomputed from U, W1, W2t at position k*; if no tested position up to
+ *     empty), p_d recomputed from U, W1, W2t at position k* -- or, when draft_logits is given,
+ *     p_d = exp(draft_logits[r, k*-1] / temperature - lse[r, k*-1]); if no tested position up to
  *     L_commit is rejected, a bonus token is drawn from p_t of row L_commit + 1
  *     (decision draws: purposes 4, 5 at the drawn position).
  *   temperature = 0: x_k is accepted iff it is the target argmax; the extra token is the
@@ -198,12 +199,17 @@ DSPARK_API int dspark_pack(const int32_t* window, const int32_t* anchor, const i
  *   target      device [rows, V] (dtype), rows >= cu_seqlens[bs]
  *   window      device [bs] int32 (ignored in STATIC mode, may be NULL there)
  *   tokens, logit_x, lse, anchor: the draft's outputs / inputs;  U, W1, W2t, r as in S1.
+ *   draft_logits device [bs, gamma, V] (dtype) or NULL: the draft's logits l_k of every
+ *               position, for callers that hold them (another drafter, or a caller that kept
+ *               them); lse must be their log-sum-exp at temperature (as dspark_draft_block
+ *               writes it).  Given, U, W1, W2t (may be NULL) and r are not used; NULL, U, W1,
+ *               W2t are required and p_d is recomputed.
  * Limits: as dspark_draft_block. */
 DSPARK_API int dspark_verify(const void* target, int dtype, const int32_t* cu_seqlens,
                   const int32_t* window, int mode, int bs, int gamma, int V,
                   const int32_t* anchor, const int32_t* tokens, const float* logit_x,
-                  const float* lse, const void* U, const void* W1, const void* W2t, int r,
-                  float temperature, uint64_t seed, uint64_t step,
+                  const float* lse, const void* draft_logits, const void* U, const void* W1,
+                  const void* W2t, int r, float temperature, uint64_t seed, uint64_t step,
                   int32_t* out_tokens, int32_t* acc_len, int32_t* ceiling,
                   void* ws, size_t ws_bytes, dspark_stream_t stream);
 

@@ -421,7 +421,7 @@ def pack(window, anchor, tokens, tiers, cap: int, gamma: Optional[int] = None):
 
 def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x, lse,
            U, W1, W2t, temperature: float, seed: int, step: int, dtype: str = "bf16",
-           chunk: int = CHUNK, req_ids=None):
+           chunk: int = CHUNK, req_ids=None, draft_logits=None):
     """S5: accept the longest valid prefix of each request's window, then one more token.
 
     [SUMMARY, "Abstract" and "Architecture (drafter)"]: lossless speculative decoding accepts
@@ -438,7 +438,8 @@ def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x
     residual has no mass the draw falls back to p_t; greedy (temperature 0) accepts iff
     x_k is the target argmax (lowest index) and the extra token is the target argmax.
     Draft probabilities come from logit_x - lse (the draft's outputs); the residual's draft
-    distribution p_d is recomputed from U, W1, W2 at the rejected position.
+    distribution p_d is recomputed from U, W1, W2 at the rejected position, or, when the
+    caller holds the draft's logits, taken from draft_logits [bs, gamma, V] (same dtype).
 
     target_packed row cu[r] + k - 1 holds the target logits that score position k
     (k = 1..n_r).  Returns out_tokens [bs, gamma+1] (-1 padded), acc_len [bs],
@@ -446,9 +447,12 @@ def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x
     margin [bs] (smallest decision margin among the decisions that shaped the output).
     req_ids (optional) gives each row's request index in the random streams (default: row)."""
     tgt = to_f64(target_packed, dtype)
-    Uf = to_f64(U, dtype)
-    W1f = to_f64(W1, dtype)
-    W2f = to_f64(W2t, dtype)
+    if draft_logits is None:
+        Uf = to_f64(U, dtype)
+        W1f = to_f64(W1, dtype)
+        W2f = to_f64(W2t, dtype)
+    else:
+        Df = to_f64(draft_logits, dtype)
     tokens = np.asarray(tokens, dtype=np.int64)
     bs, gamma = tokens.shape
     cu = np.asarray(cu_seqlens, dtype=np.int64)
@@ -496,7 +500,10 @@ def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x
             else:
                 t = trow(k) / temperature
                 p_t = np.exp(t - logsumexp(t))
-                d = (Uf[r, k - 1] + W1f[x[k - 1]] @ W2f.T) / temperature
+                if draft_logits is None:
+                    d = (Uf[r, k - 1] + W1f[x[k - 1]] @ W2f.T) / temperature
+                else:
+                    d = Df[r, k - 1] / temperature
                 p_d = np.exp(d - logsumexp(d))
                 res = np.maximum(0.0, p_t - p_d)
                 with np.errstate(divide="ignore"):

@@ -37,7 +37,7 @@ _SIGS = {
                                _vp, _vp, _vp]),
     "dspark_schedule": (_i, [_vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp]),
     "dspark_pack": (_i, [_vp, _vp, _vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "dspark_verify": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+    "dspark_verify": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                            _i, _f, _u64, _u64, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
@@ -188,11 +188,13 @@ def dspark_pack(window, anchor, tokens, tiers, cu_seqlens, ids, req, pos, padded
 
 
 def dspark_verify(target, cu_seqlens, window, mode, anchor, tokens, logit_x, lse, U, W1, W2t,
-                  temperature, seed, step, out_tokens, acc_len, ceiling, ws, stream=None):
+                  temperature, seed, step, out_tokens, acc_len, ceiling, ws, stream=None, draft_logits=None):
+    """draft_logits [bs, gamma, V] (optional): the draft's logits; then U, W1, W2t may be None."""
     bs, gamma = tokens.shape
     V = target.shape[1]
-    r = W1.shape[1]
+    r = W1.shape[1] if W1 is not None else 0
     _check(lib().dspark_verify(_p(target), _dtype(target), _p(cu_seqlens), _p(window), int(mode), bs, gamma,
-                               V, _p(anchor), _p(tokens), _p(logit_x), _p(lse), _p(U), _p(W1), _p(W2t), r,
+                               V, _p(anchor), _p(tokens), _p(logit_x), _p(lse), _p(draft_logits), _p(U), _p(W1),
+                               _p(W2t), r,
                                float(temperature), int(seed), int(step), _p(out_tokens), _p(acc_len),
                                _p(ceiling), _p(ws), ws.numel(), _stream(stream)), "dspark_verify")

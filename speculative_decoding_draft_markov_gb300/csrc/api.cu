@@ -178,25 +178,30 @@ int dspark_pack(const int32_t* window, const int32_t* anchor, const int32_t* tok
 
 int dspark_verify(const void* target, int dtype, const int32_t* cu_seqlens, const int32_t* window,
                   int mode, int bs, int gamma, int V, const int32_t* anchor, const int32_t* tokens,
-                  const float* logit_x, const float* lse, const void* U, const void* W1,
-                  const void* W2t, int r, float temperature, uint64_t seed, uint64_t step,
-                  int32_t* out_tokens, int32_t* acc_len, int32_t* ceiling, void* ws,
+                  const float* logit_x, const float* lse, const void* draft_logits, const void* U,
+                  const void* W1, const void* W2t, int r, float temperature, uint64_t seed,
+                  uint64_t step, int32_t* out_tokens, int32_t* acc_len, int32_t* ceiling, void* ws,
                   size_t ws_bytes, dspark_stream_t stream) {
-  if (!target || !cu_seqlens || !anchor || !tokens || !logit_x || !lse || !U || !W1 || !W2t ||
-      !out_tokens || !acc_len)
+  if (!target || !cu_seqlens || !anchor || !tokens || !logit_x || !lse || !out_tokens || !acc_len)
     return DSPARK_EINVAL;
+  if (!draft_logits && (!U || !W1 || !W2t)) return DSPARK_EINVAL;  // p_d needs one source
+  if (draft_logits) {  // U, W1, W2t and r unused
+    if (!al(draft_logits, 16)) return DSPARK_EINVAL;
+    U = W1 = W2t = nullptr;
+    r = 32;
+  }
   if (mode != DSPARK_STATIC && mode != DSPARK_COMPACT && mode != DSPARK_CAP_ACCEPT) return DSPARK_EINVAL;
   if (mode != DSPARK_STATIC && !window) return DSPARK_EINVAL;
   if (mode == DSPARK_CAP_ACCEPT && !ceiling) return DSPARK_EINVAL;
   if (!valid_dtype(dtype) || !std::isfinite(temperature) || temperature < 0.f) return DSPARK_EINVAL;
   if (int e = check_core(bs, gamma, V, r)) return e;
-  if (!al(target, 16) || !al(U, 16) || !al(W1, 16) || !al(W2t, 16)) return DSPARK_EINVAL;
+  if (!al(target, 16) || (U && !al(U, 16)) || (W1 && !al(W1, 16)) || (W2t && !al(W2t, 16))) return DSPARK_EINVAL;
   if (int e = check_ws(ws, ws_bytes, bs, gamma, V)) return e;
   const int greedy = temperature == 0.f;
   const float inv_tau = greedy ? 1.f : static_cast<float>(1.0 / static_cast<double>(temperature));
   return cuda_status(launch_verify(dtype, target, cu_seqlens, window, mode, bs, gamma, V, anchor,
-                                   tokens, logit_x, lse, U, W1, W2t, r, inv_tau, greedy, seed, step,
-                                   out_tokens, acc_len, ceiling, ws,
+                                   tokens, logit_x, lse, draft_logits, U, W1, W2t, r, inv_tau, greedy,
+                                   seed, step, out_tokens, acc_len, ceiling, ws,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -55,8 +55,9 @@ cudaError_t launch_pack(const int32_t* window, const int32_t* anchor, const int3
 cudaError_t launch_verify(int dtype, const void* target, const int32_t* cu, const int32_t* window,
                           int mode, int bs, int gamma, int V, const int32_t* anchor,
                           const int32_t* tokens, const float* logit_x, const float* lse,
-                          const void* U, const void* W1, const void* W2t, int r, float inv_tau,
-                          int greedy, uint64_t seed, uint64_t step, int32_t* out_tokens,
-                          int32_t* acc_len, int32_t* ceiling, void* ws, cudaStream_t s);
+                          const void* draft_logits, const void* U, const void* W1, const void* W2t,
+                          int r, float inv_tau, int greedy, uint64_t seed, uint64_t step,
+                          int32_t* out_tokens, int32_t* acc_len, int32_t* ceiling, void* ws,
+                          cudaStream_t s);
 
 }  // namespace dspark

@@ -11,7 +11,7 @@ namespace dspark {
 // S2.  DSpark technical summary, "Verification scheduling (system side)": the confidence
 // head is a linear projection of [h_k ; W1[x_{k-1}]] followed by a sigmoid; sequential
 // temperature scaling divides the logit by T_k; prefix survival is the running product.
-// One block per request, one warp per position; fp32 dot products in a fixed order.
+// fp32 dot products in a fixed order.
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ float dot_chunk8(const __nv_bfloat16* x, const float* w) {
   const uint4 q = *reinterpret_cast<const uint4*>(x);
@@ -41,37 +41,45 @@ __device__ __forceinline__ float dot_chunk8(const float* x, const float* w) {
   return a;
 }
 
+// One block per request; `parts` warps per position split the d-long dot product (warp q of a
+// position takes the 256-element groups q, q + parts, ...; four 16-byte loads in flight per
+// lane), then thread 0 adds the parts in order and runs the sigmoid / STS / product chain.
 template <typename T>
-__global__ void __launch_bounds__(512) confidence_kernel(
+__global__ void __launch_bounds__(1024) confidence_kernel(
     const T* __restrict__ h, const T* __restrict__ W1, const int32_t* __restrict__ anchor,
     const int32_t* __restrict__ tokens, const float* __restrict__ w, float b,
-    const float* __restrict__ sts_T, int gamma, int d, int r, int V, float* __restrict__ conf,
+    const float* __restrict__ sts_T, int gamma, int d, int r, int V, int parts, float* __restrict__ conf,
     float* __restrict__ surv) {
-  __shared__ float z[DSPARK_MAX_GAMMA];
+  __shared__ float zp[DSPARK_MAX_GAMMA * 4];
   const int req = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < gamma) {
-    const int k = warp + 1;
-    const int xp = clamp_token((k == 1) ? anchor[req] : tokens[size_t(req) * gamma + k - 2], V);
-    const T* hr = h + (size_t(req) * gamma + warp) * d;
-    const T* wr = W1 + size_t(xp) * r;
-    // four independent partial sums so that four 16-byte loads of h are in flight per lane
+  const int pos = warp / parts, part = warp - pos * parts;
+  if (pos < gamma) {
+    const int k = pos + 1;
+    const T* hr = h + (size_t(req) * gamma + pos) * d;
     float a4[4] = {0.f, 0.f, 0.f, 0.f};
-    int e = lane * 8;
-    for (; e + 3 * 256 < d; e += 4 * 256) {
+    const int stride = parts * 256;
+    int e = part * 256 + lane * 8;
+    for (; e + 3 * stride < d; e += 4 * stride) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) a4[u] += dot_chunk8(hr + e + u * 256, w + e + u * 256);
+      for (int u = 0; u < 4; ++u) a4[u] += dot_chunk8(hr + e + u * stride, w + e + u * stride);
     }
-    for (; e < d; e += 256) a4[0] += dot_chunk8(hr + e, w + e);
+    for (; e < d; e += stride) a4[0] += dot_chunk8(hr + e, w + e);
     float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
-    if (lane * 8 < r) acc += dot_chunk8(wr + lane * 8, w + d + lane * 8);  // r is a multiple of 8, <= 256
+    if (part == 0 && lane * 8 < r) {  // the W1[x_{k-1}] part of the feature (r a multiple of 8, <= 256)
+      const int xp = clamp_token((k == 1) ? anchor[req] : tokens[size_t(req) * gamma + k - 2], V);
+      acc += dot_chunk8(W1 + size_t(xp) * r + lane * 8, w + d + lane * 8);
+    }
     acc = warp_sum(acc);
-    if (lane == 0) z[warp] = acc + b;
+    if (lane == 0) zp[pos * 4 + part] = acc;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     float a = 1.f;
     for (int k = 0; k < gamma; ++k) {
-      const float c = 1.f / (1.f + expf(-z[k] / sts_T[k]));
+      float z = zp[k * 4];
+      for (int q = 1; q < parts; ++q) z += zp[k * 4 + q];
+      z += b;
+      const float c = 1.f / (1.f + expf(-z / sts_T[k]));
       a *= c;
       conf[size_t(req) * gamma + k] = c;
       surv[size_t(req) * gamma + k] = a;
@@ -83,14 +91,15 @@ cudaError_t launch_confidence(int dtype, const void* h, const void* W1, const in
                               const int32_t* tokens, const float* w, float b, const float* sts_T,
                               int bs, int gamma, int d, int r, int V, float* conf, float* surv,
                               cudaStream_t s) {
-  const int threads = 32 * gamma;
+  const int parts = gamma <= 8 ? 4 : 2;  // warps per position: at most 1024 threads
+  const int threads = 32 * parts * gamma;
   if (dtype == DSPARK_F32)
     confidence_kernel<float><<<bs, threads, 0, s>>>((const float*)h, (const float*)W1, anchor,
-                                                    tokens, w, b, sts_T, gamma, d, r, V, conf, surv);
+                                                    tokens, w, b, sts_T, gamma, d, r, V, parts, conf, surv);
   else
     confidence_kernel<__nv_bfloat16><<<bs, threads, 0, s>>>(
         (const __nv_bfloat16*)h, (const __nv_bfloat16*)W1, anchor, tokens, w, b, sts_T, gamma, d,
-        r, V, conf, surv);
+        r, V, parts, conf, surv);
   return cudaGetLastError();
 }
 

@@ -11,7 +11,8 @@
 //                   target logit of the draft token it tests -- the HBM stream over target
 //   verify_decide   one thread per request: accept tests, first rejection, commit, ceiling
 //   decision_stats  (temperature > 0) per (request, 128-id chunk): residual mass and target
-//                   mass of the deciding row, p_d recomputed from U, W1, W2
+//                   mass of the deciding row, p_d recomputed from U, W1, W2 (or read from the
+//                   caller's draft logits)
 //   decision_select (temperature > 0) one block per request: two-level Gumbel-max draw
 #include <climits>
 
@@ -287,13 +288,55 @@ __global__ void __launch_bounds__(128) decision_stats_simt_kernel(
 // ---------------------------------------------------------------------------------------
 // Decision draw: one 256-thread block per request (temperature > 0).
 // ---------------------------------------------------------------------------------------
+// ---------------------------------------------------------------------------------------
+// Decision masses from the caller's draft logits (no recompute): block = one 128-id chunk x RB
+// rows; p_d = exp(logits / T - lse_d) of the row at the decision's position.  One DecideEntry
+// per (request, chunk).
+// ---------------------------------------------------------------------------------------
+template <typename T, int RB>
+__global__ void __launch_bounds__(128) decision_stats_logits_kernel(
+    const T* __restrict__ target, const T* __restrict__ draft_logits, const float* __restrict__ lse_d,
+    const RowStat* __restrict__ rs, const Decision* __restrict__ dec, int bs, int gamma, int V, float inv_tau,
+    uint64_t seed, uint64_t step, DecideEntry* __restrict__ entries, int n_chunks) {
+  __shared__ float red[4];
+  const int c = blockIdx.x, rb = blockIdx.y * RB, tid = threadIdx.x;
+  const int v = c * kChunk + tid;
+  const bool valid = v < V;
+  for (int rr = 0; rr < RB; ++rr) {
+    const int row = rb + rr;
+    if (row >= bs) break;
+    const Decision d = dec[row];
+    if (d.kind == kDecNone) continue;  // uniform over the block
+    float pt = 0.f, w = 0.f;
+    if (valid) {
+      pt = expf(ld_f32(target, size_t(d.pdec) * V + v) * inv_tau - rs[d.pdec].lse);
+      w = pt;
+      if (d.kind == kDecResidual) {
+        const size_t drow = size_t(row) * gamma + d.kdec - 1;
+        const float pd = expf(ld_f32(draft_logits, drow * V + v) * inv_tau - lse_d[drow]);
+        w = fmaxf(0.f, pt - pd);
+      }
+    }
+    const float R = block_sum<kChunk>(w, red);
+    const float P = block_sum<kChunk>(pt, red);
+    if (tid == 0) {
+      const uint4 gw = philox_group(seed, step, kDecideChunk, uint32_t(row), d.kdec, uint32_t(c) >> 2);
+      const float g = gumbel_from_bits(pick_word(gw, c & 3));
+      DecideEntry e{R, P, -INFINITY, -INFINITY, INT_MAX, INT_MAX, 0, 0};
+      if (R > 0.f) { e.kR = logf(R) + g; e.cR = c; }
+      if (P > 0.f) { e.kP = logf(P) + g; e.cP = c; }
+      entries[size_t(row) * n_chunks + c] = e;
+    }
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) decision_select_kernel(
     const T* __restrict__ target, const T* __restrict__ U, const T* __restrict__ W1,
     const T* __restrict__ W2t, const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens,
     const float* __restrict__ lse_d, const RowStat* __restrict__ rs, const Decision* __restrict__ dec,
-    const DecideEntry* __restrict__ entries, int n_slots, int bs, int gamma, int V, int r, float inv_tau,
-    uint64_t seed, uint64_t step, int32_t* __restrict__ out_tokens) {
+    const T* __restrict__ draft_logits, const DecideEntry* __restrict__ entries, int n_slots, int bs, int gamma,
+    int V, int r, float inv_tau, uint64_t seed, uint64_t step, int32_t* __restrict__ out_tokens) {
   __shared__ float sA[256];
   __shared__ float tw[kChunk], tp[kChunk];
   __shared__ float rv[8];
@@ -327,13 +370,14 @@ __global__ void __launch_bounds__(256) decision_select_kernel(
   const ArgMax best{0.f, s_win};
   const int cstar = (best.i == INT_MAX) ? 0 : best.i;  // only non-finite statistics leave it unset
   const bool resid = (d.kind == kDecResidual) && use_res;
-  if (resid) {
+  const bool recompute = resid && draft_logits == nullptr;
+  if (recompute) {
     const int xp = clamp_token((d.kdec == 1) ? anchor[b] : tokens[size_t(b) * gamma + d.kdec - 2], V);
     for (int i = tid; i < r; i += 256) sA[i] = ld_f32(W1, size_t(xp) * r + i);
   }
   __syncthreads();
   const float lse_t = rs[d.pdec].lse;
-  if (resid) chunk_dots<T>(W2t, r, V, cstar * kChunk, sA, tw);
+  if (recompute) chunk_dots<T>(W2t, r, V, cstar * kChunk, sA, tw);
   __syncthreads();
   if (tid < kChunk) {
     const int v = cstar * kChunk + tid;
@@ -342,7 +386,9 @@ __global__ void __launch_bounds__(256) decision_select_kernel(
       pt = expf(ld_f32(target, size_t(d.pdec) * V + v) * inv_tau - lse_t);
       w = pt;
       if (resid) {
-        const float dl = (tw[tid] + ld_f32(U, (size_t(b) * gamma + d.kdec - 1) * V + v)) * inv_tau;
+        const size_t drow = size_t(b) * gamma + d.kdec - 1;
+        const float dl = draft_logits ? ld_f32(draft_logits, drow * V + v) * inv_tau
+                                      : (tw[tid] + ld_f32(U, drow * V + v)) * inv_tau;
         w = fmaxf(0.f, pt - expf(dl - lse_d[size_t(b) * gamma + d.kdec - 1]));
       }
     }
@@ -370,9 +416,10 @@ template <typename T>
 static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_t* window, int mode,
                                int bs, int gamma, int V, const int32_t* anchor,
                                const int32_t* tokens, const float* logit_x, const float* lse,
-                               const T* U, const T* W1, const T* W2t, int r, float inv_tau,
-                               int greedy, uint64_t seed, uint64_t step, int32_t* out_tokens,
-                               int32_t* acc_len, int32_t* ceiling, void* ws, cudaStream_t s) {
+                               const T* draft_logits, const T* U, const T* W1, const T* W2t, int r,
+                               float inv_tau, int greedy, uint64_t seed, uint64_t step,
+                               int32_t* out_tokens, int32_t* acc_len, int32_t* ceiling, void* ws,
+                               cudaStream_t s) {
   const WsLayout L = ws_layout(bs, gamma, V);
   char* w = static_cast<char*>(ws);
   uint32_t* status = reinterpret_cast<uint32_t*>(w + L.status);
@@ -388,7 +435,10 @@ static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_
     constexpr int RB = 32;
     constexpr bool kBf16 = sizeof(T) == 2;
     int n_slots = L.n_chunks;
-    if (kBf16 && draft_tc_supported(DSPARK_BF16, bs, V, r)) {
+    if (draft_logits) {  // p_d from the caller's draft logits: a stream over two rows per request
+      decision_stats_logits_kernel<T, RB><<<dim3(L.n_chunks, (bs + RB - 1) / RB), kChunk, 0, s>>>(
+          target, draft_logits, lse, rs, dec, bs, gamma, V, inv_tau, seed, step, entries, L.n_chunks);
+    } else if (kBf16 && draft_tc_supported(DSPARK_BF16, bs, V, r)) {
       const cudaError_t e = launch_decision_stats_tc(target, U, W1, W2t, anchor, tokens, lse, rs, dec, bs, gamma, V,
                                                      r, inv_tau, seed, step, entries, L.n_chunks, &n_slots, status, s);
       if (e != cudaSuccess) return e;
@@ -398,8 +448,8 @@ static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_
           L.n_chunks);
     }
     decision_select_kernel<T><<<bs, 256, 0, s>>>(target, U, W1, W2t, anchor, tokens, lse, rs, dec,
-                                                 entries, n_slots, bs, gamma, V, r, inv_tau, seed,
-                                                 step, out_tokens);
+                                                 draft_logits, entries, n_slots, bs, gamma, V, r, inv_tau,
+                                                 seed, step, out_tokens);
   }
   return cudaGetLastError();
 }
@@ -407,17 +457,20 @@ static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_
 cudaError_t launch_verify(int dtype, const void* target, const int32_t* cu, const int32_t* window,
                           int mode, int bs, int gamma, int V, const int32_t* anchor,
                           const int32_t* tokens, const float* logit_x, const float* lse,
-                          const void* U, const void* W1, const void* W2t, int r, float inv_tau,
-                          int greedy, uint64_t seed, uint64_t step, int32_t* out_tokens,
-                          int32_t* acc_len, int32_t* ceiling, void* ws, cudaStream_t s) {
+                          const void* draft_logits, const void* U, const void* W1, const void* W2t,
+                          int r, float inv_tau, int greedy, uint64_t seed, uint64_t step,
+                          int32_t* out_tokens, int32_t* acc_len, int32_t* ceiling, void* ws,
+                          cudaStream_t s) {
   if (dtype == DSPARK_F32)
     return verify_typed<float>((const float*)target, cu, window, mode, bs, gamma, V, anchor, tokens,
-                               logit_x, lse, (const float*)U, (const float*)W1, (const float*)W2t,
-                               r, inv_tau, greedy, seed, step, out_tokens, acc_len, ceiling, ws, s);
+                               logit_x, lse, (const float*)draft_logits, (const float*)U, (const float*)W1,
+                               (const float*)W2t, r, inv_tau, greedy, seed, step, out_tokens, acc_len,
+                               ceiling, ws, s);
   return verify_typed<__nv_bfloat16>((const __nv_bfloat16*)target, cu, window, mode, bs, gamma, V,
-                                     anchor, tokens, logit_x, lse, (const __nv_bfloat16*)U,
-                                     (const __nv_bfloat16*)W1, (const __nv_bfloat16*)W2t, r, inv_tau,
-                                     greedy, seed, step, out_tokens, acc_len, ceiling, ws, s);
+                                     anchor, tokens, logit_x, lse, (const __nv_bfloat16*)draft_logits,
+                                     (const __nv_bfloat16*)U, (const __nv_bfloat16*)W1,
+                                     (const __nv_bfloat16*)W2t, r, inv_tau, greedy, seed, step, out_tokens,
+                                     acc_len, ceiling, ws, s);
 }
 
 }  // namespace dspark

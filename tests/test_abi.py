@@ -93,12 +93,18 @@ def test_other_entry_points_host_validation(L):
     # pack: negative tier count, missing workspace
     assert L.dspark_pack(None, f, f, 4, 7, f, -1, 64, f, f, f, f, f, f, 1 << 20, None) == B.DSPARK_EINVAL
     assert L.dspark_pack(None, f, f, 4, 7, None, 0, 64, f, f, f, f, f, None, 0, None) == B.DSPARK_EWORKSPACE
-    # verify: compact without window, cap-accept without ceiling, bad mode
-    args = [f, 1, f, None, 1, 4, 7, 1024, f, f, f, f, f, f, f, 32, 1.0, 0, 0, f, f, f, f, 1 << 30, None]
+    # verify: compact without window, cap-accept without ceiling, bad mode, no source for p_d,
+    # misaligned draft logits
+    args = [f, 1, f, None, 1, 4, 7, 1024, f, f, f, f, None, f, f, f, 32, 1.0, 0, 0, f, f, f, f, 1 << 30, None]
     assert L.dspark_verify(*args) == B.DSPARK_EINVAL
-    args[3], args[4], args[21] = f, 2, None
+    args[3], args[4], args[22] = f, 2, None
     assert L.dspark_verify(*args) == B.DSPARK_EINVAL
     args[4] = 9
+    assert L.dspark_verify(*args) == B.DSPARK_EINVAL
+    args[4], args[22] = 1, f
+    args[13] = None  # neither draft logits nor U
+    assert L.dspark_verify(*args) == B.DSPARK_EINVAL
+    args[12] = f + 2  # draft logits given, not 16-byte aligned
     assert L.dspark_verify(*args) == B.DSPARK_EINVAL
 
 

@@ -231,3 +231,57 @@ def test_verify_chain_parity(name, mode, temperature):
         assert near <= 1
         total_checked += checked
     assert total_checked >= 3 * wl.bs - 3
+
+
+@pytest.mark.parametrize("name", list(VERIFY_WL))
+@pytest.mark.parametrize("mode", [O.STATIC, O.COMPACT])
+def test_verify_with_explicit_draft_logits(name, mode):
+    """dspark_verify given the draft's logits (no U / W1 / W2t): the residual's p_d comes from
+    them.  The logits here are a fresh draw (not a Markov head), with logit_x / lse taken from
+    them, so the test covers a drafter whose distribution the library never computes."""
+    wl = VERIFY_WL[name]
+    host = I.make_host_inputs(wl, with_hidden=False)
+    inp = _dev(host)
+    bs, gamma, V = wl.bs, wl.gamma, wl.V
+    rng = np.random.default_rng(77)
+    D64 = rng.normal(0.0, 3.0, size=(bs, gamma, V))
+    if wl.dtype == "bf16":
+        D_host = I.f32_to_bf16_bits(D64.astype(np.float32))
+        Df = O.to_f64(D_host, "bf16")
+        D_dev = torch.as_tensor(D_host.view(np.int16), device="cuda").view(torch.bfloat16)
+    else:
+        D_host = D64.astype(np.float32)
+        Df = D_host.astype(np.float64)
+        D_dev = torch.as_tensor(D_host, device="cuda")
+    # draft tokens drawn from softmax(D); logit_x / lse consistent with D
+    m = Df.max(-1, keepdims=True)
+    lse = (np.log(np.exp(Df - m).sum(-1)) + m[..., 0])
+    p = np.exp(Df - lse[..., None])
+    tok = np.array([[rng.choice(V, p=p[b, k] / p[b, k].sum()) for k in range(gamma)] for b in range(bs)], np.int32)
+    lx = np.take_along_axis(Df, tok[..., None].astype(np.int64), -1)[..., 0]
+    lx, lse = lx.astype(np.float32), lse.astype(np.float32)
+    win = I.random_windows(bs, gamma, 123)
+    pack_win = win if mode == O.COMPACT else None
+    cap = bs * (gamma + 1)
+    cu_o, ids_o, req_o, pos_o, pad_o = O.pack(pack_win, host["anchor"], tok, [], cap)
+    packed_o = I.gather_packed_target(host["target"], req_o, pos_o, cap)
+    checked = near = 0
+    for step in range(3):
+        out_o, acc_o, _, mv_o = O.verify(packed_o, cu_o, win, mode, host["anchor"], tok, lx, lse, None, None, None,
+                                         1.0, wl.seed, step, dtype=wl.dtype, draft_logits=D_host)
+        buf = S.StepBuffers.allocate(bs, gamma, V, cap, inp["U"].dtype)
+        buf.tokens.copy_(torch.as_tensor(tok, device="cuda"))
+        buf.logit_x.copy_(torch.as_tensor(lx, device="cuda"))
+        buf.lse.copy_(torch.as_tensor(lse, device="cuda"))
+        buf.window.copy_(torch.as_tensor(win, device="cuda"))
+        B.dspark_pack(buf.window if mode == O.COMPACT else None, inp["anchor"], buf.tokens, None, buf.cu, buf.ids,
+                      buf.req, buf.pos, buf.padded, buf.ws)
+        S.gather_target_forward(inp["target"])(buf)
+        B.dspark_verify(buf.packed, buf.cu, buf.window, mode, inp["anchor"], buf.tokens, buf.logit_x, buf.lse,
+                        None, None, None, 1.0, wl.seed, step, buf.out_tokens, buf.acc_len, buf.ceiling, buf.ws,
+                        draft_logits=D_dev)
+        assert B.dspark_read_device_status(buf.ws) == B.DSPARK_OK
+        c, n = compare_verify(buf.out_tokens.cpu().numpy(), buf.acc_len.cpu().numpy(), out_o, acc_o, mv_o)
+        checked += c
+        near += n
+    assert near <= 1 and checked >= 3 * bs - 1

@@ -6,7 +6,9 @@
 - the first committed token is distributed as p_t (lossless), also under random windows
   and in cap-accept mode (non-anticipating truncation);
 - cap-accept commits bit-identically to compact and its ceiling equals static's count;
-- greedy verification accepts exactly the argmax-matching prefix."""
+- greedy verification accepts exactly the argmax-matching prefix;
+- with the draft's logits given explicitly: the same decisions as the recompute path, full
+  acceptance when the draft equals the target, and losslessness for a non-Markov draft."""
 import numpy as np
 import pytest
 from scipy import stats
@@ -141,3 +143,70 @@ def test_verify_rejects_mismatched_packing():
     with pytest.raises(ValueError):
         O.verify(packed, cu, np.array([2, 2]), O.COMPACT, anchor, tok, lx, lse, U, W1, W2t,
                  1.0, 0, 0, dtype="f32")
+
+
+def test_explicit_draft_logits_equal_recomputed_ones():
+    """Given the draft's own logits (fp32 of U + W1[x] W2), verify decides as when it recomputes
+    them, except where a decision margin is below the fp32 rounding of the logits."""
+    U, W1, W2t, target, anchor = _setup(V=40, reps=60, seed=3, noise=1.2)
+    bs, gamma, V = U.shape
+    for step in range(4):
+        tok, lx, lse, _ = O.draft_block(U, W1, W2t, anchor, 1.0, 5, step, dtype="f32")
+        f = lambda a: a.astype(np.float64)
+        prev = np.concatenate([anchor[:, None], tok[:, :-1]], axis=1)
+        D = (f(U) + np.einsum("bkr,vr->bkv", f(W1)[prev], f(W2t))).astype(np.float32)
+        window = I.random_windows(bs, gamma, 70 + step)
+        cu, ids, req, pos, padded = O.pack(window, anchor, tok, [], cap=bs * (gamma + 1))
+        packed = I.gather_packed_target(target, req, pos, padded)
+        a = O.verify(packed, cu, window, O.COMPACT, anchor, tok, lx, lse, U, W1, W2t, 1.0, 5, step, dtype="f32")
+        b = O.verify(packed, cu, window, O.COMPACT, anchor, tok, lx, lse, None, None, None, 1.0, 5, step,
+                     dtype="f32", draft_logits=D)
+        sure = np.minimum(a[3], b[3]) > 1e-5
+        assert sure.mean() > 0.95
+        np.testing.assert_array_equal(a[0][sure], b[0][sure])
+        np.testing.assert_array_equal(a[1][sure], b[1][sure])
+
+
+def test_explicit_draft_equal_to_target_accepts_everything():
+    """p_d = p_t (the draft's logits are the target's): every tested token is accepted and the
+    extra token is the bonus draw of the next row."""
+    rng = np.random.default_rng(9)
+    bs, gamma, V = 30, 3, 24
+    target = rng.normal(0, 1.5, size=(bs, gamma + 1, V)).astype(np.float32)
+    D = target[:, :gamma].copy()
+    tok = rng.integers(0, V, size=(bs, gamma)).astype(np.int32)
+    anchor = rng.integers(0, V, size=bs).astype(np.int32)
+    f = target[:, :gamma].astype(np.float64)
+    lse = (np.log(np.exp(f - f.max(-1, keepdims=True)).sum(-1)) + f.max(-1)).astype(np.float32)
+    lx = np.take_along_axis(f, tok[..., None].astype(np.int64), -1)[..., 0].astype(np.float32)
+    cu, ids, req, pos, padded = O.pack(None, anchor, tok, [], cap=bs * (gamma + 1), gamma=gamma)
+    packed = I.gather_packed_target(target, req, pos, padded)
+    out, acc, _, _ = O.verify(packed, cu, None, O.STATIC, anchor, tok, lx, lse, None, None, None, 1.0, 2, 0,
+                              dtype="f32", draft_logits=D)
+    assert (acc == gamma).all()
+    np.testing.assert_array_equal(out[:, :gamma], tok)
+
+
+def test_explicit_draft_logits_first_committed_token_is_target_distributed():
+    """Losslessness with an arbitrary draft distribution given as logits (not a Markov head)."""
+    rng = np.random.default_rng(11)
+    V, gamma, bs = 12, 1, 400
+    t_row = rng.normal(0, 1.3, size=V)
+    d_row = rng.normal(0, 1.3, size=V)
+    target = np.broadcast_to(np.stack([t_row, rng.normal(0, 1.3, size=V)]).astype(np.float32),
+                             (bs, gamma + 1, V)).copy()
+    D = np.broadcast_to(d_row.astype(np.float32), (bs, gamma, V)).copy()
+    p_d = softmax(d_row)
+    lse_d = np.float32(np.log(np.exp(d_row - d_row.max()).sum()) + d_row.max())
+    counts = np.zeros(V)
+    for step in range(40):
+        tok = rng.choice(V, size=(bs, gamma), p=p_d).astype(np.int32)
+        lx = D[np.arange(bs)[:, None], np.arange(gamma)[None, :], tok]
+        lse = np.full((bs, gamma), lse_d, dtype=np.float32)
+        anchor = np.zeros(bs, dtype=np.int32)
+        cu, ids, req, pos, padded = O.pack(None, anchor, tok, [], cap=bs * (gamma + 1), gamma=gamma)
+        packed = I.gather_packed_target(target, req, pos, padded)
+        out, _, _, _ = O.verify(packed, cu, None, O.STATIC, anchor, tok, lx, lse, None, None, None, 1.0, 4, step,
+                                dtype="f32", draft_logits=D)
+        np.add.at(counts, out[:, 0], 1)
+    assert stats.chisquare(counts, softmax(t_row) * counts.sum()).pvalue > 1e-4
