@@ -377,6 +377,58 @@ def schedule(surv_f32, sps, mode: int = EARLY_STOP):
 
 
 # ---------------------------------------------------------------------------
+# S3 under zero-overhead scheduling -- the budget is predicted two steps back
+# ---------------------------------------------------------------------------
+
+def zos_budget(surv_f32, sps) -> int:
+    """The verify budget that step t's survival predicts for step t + 2.
+
+    [SUMMARY, "Infra"], scheduler bullet: to run under CUDA graph replay and the
+    zero-overhead (overlap) scheduler, the top-K truncation length of the current step is
+    predicted from the confidence of two steps earlier; that stale information is a causal
+    barrier, so the early-stop break is dropped and the search over the (sawtooth) SPS table
+    is global.  [SGLANG, "ZOS"]: the confidence relay reads back two steps.
+    Reading: the budget is K* of the global search (GLOBAL_ARGMAX) over that step's own
+    survival, batch size and table, exactly as `schedule` computes it."""
+    return int(schedule(surv_f32, sps, GLOBAL_ARGMAX)[1])
+
+
+def zos_select(surv_f32, K: int) -> np.ndarray:
+    """The K top-ranked slots of the current survival, as per-request window lengths.
+
+    [SUMMARY, "Infra"]: the candidates of the current step are still ranked by the latest
+    cumulative confidence.  Ranking as `schedule`: descending fp32 survival, ties to the lower
+    request, then the lower position.  K is clamped to [0, bs * gamma]."""
+    a = np.asarray(surv_f32, dtype=np.float32)
+    bs, gamma = a.shape
+    slots = sorted(((float(a[r, j]), r, j) for r in range(bs) for j in range(gamma)),
+                   key=lambda s: (-s[0], s[1], s[2]))
+    window = np.zeros(bs, dtype=np.int32)
+    for i in range(max(0, min(int(K), bs * gamma))):
+        window[slots[i][1]] += 1
+    return window
+
+
+def zos_step(surv_f32, sps, ring: list, step: int):
+    """One step of the asynchronous scheduler with a two-slot budget ring.
+
+    K_t = ring[t mod 2], the budget step t - 2 recorded; when no step recorded one (the first
+    two steps; ring entries start at -1) it is the budget of the current survival itself.
+    K_t is clamped to min(bs * gamma, m_max - bs) of the current batch, the windows are the
+    K_t top-ranked current slots, and ring[t mod 2] then receives the budget the current
+    survival predicts for step t + 2.  Returns (window, K_t); `ring` is updated in place."""
+    a = np.asarray(surv_f32, dtype=np.float32)
+    bs, gamma = a.shape
+    m_max = np.asarray(sps).size - 1
+    slot = step % 2
+    K = ring[slot] if ring[slot] >= 0 else zos_budget(a, sps)
+    K = min(K, bs * gamma, m_max - bs)
+    window = zos_select(a, K)
+    ring[slot] = zos_budget(a, sps)
+    return window, K
+
+
+# ---------------------------------------------------------------------------
 # S4 -- ragged packing
 # ---------------------------------------------------------------------------
 
