@@ -159,6 +159,28 @@ DSPARK_API int dspark_schedule(const float* surv, int bs, int gamma, const doubl
                     int mode, int32_t* window, int32_t* K_out, double* theta_out,
                     dspark_stream_t stream);
 
+/* S3 under zero-overhead (asynchronous) scheduling ([SUMMARY] "Infra", scheduler bullet;
+ * [SGLANG] "ZOS"): the verify budget of step t is predicted from the survival of step t - 2,
+ * the windows still take the top slots of step t's own survival.  Two calls per step, on a
+ * two-entry device ring of budgets (int32, set to -1 before the first step):
+ *   dspark_schedule_zos_select: K = budget_ring[step & 1]; K < 0 (nothing recorded two
+ *     steps back) means K = the GLOBAL_ARGMAX K* of surv itself.  K is clamped to
+ *     min(bs*gamma, m_max - bs); window[r] = how many of the K top-ranked slots of surv
+ *     (ranking as dspark_schedule) belong to r;  K_out = K.  budget_ring is only read.
+ *   dspark_schedule_zos_budget: budget_ring[step & 1] = the GLOBAL_ARGMAX K* of surv (as
+ *     dspark_schedule), the budget of step + 2.
+ * Ordering, the caller's: select(step) before budget(step) (both touch slot step & 1), and
+ * budget(step) before select(step + 2).  On one stream in that order this holds; the budget
+ * call may run on a second stream, off the step's critical path, joined by events.
+ *   surv, sps, m_max, window, K_out as dspark_schedule;  budget_ring device [2] int32
+ * Limits: bs * gamma <= 4096.  One thread block each; no host readback. */
+DSPARK_API int dspark_schedule_zos_select(const float* surv, int bs, int gamma, const double* sps,
+                               int m_max, const int32_t* budget_ring, uint64_t step,
+                               int32_t* window, int32_t* K_out, dspark_stream_t stream);
+DSPARK_API int dspark_schedule_zos_budget(const float* surv, int bs, int gamma, const double* sps,
+                               int m_max, int32_t* budget_ring, uint64_t step,
+                               dspark_stream_t stream);
+
 /* S4. Ragged cu_seqlens packing rounded up to a captured graph tier ([SGLANG] "Ragged verify
  * under full CUDA graphs", Fig. 2; [VLLM] "Graph Capture", "CUDA Graph Padding").
  * Request r contributes n_r = l_r + 1 rows [x_0, x_1 .. x_{l_r}] where l_r = window[r]

@@ -36,6 +36,8 @@ _SIGS = {
     "dspark_confidence": (_i, [_vp, _vp, _i, _vp, _vp, _vp, _f, _vp, _i, _i, _i, _i, _i,
                                _vp, _vp, _vp]),
     "dspark_schedule": (_i, [_vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp]),
+    "dspark_schedule_zos_select": (_i, [_vp, _i, _i, _vp, _i, _vp, _u64, _vp, _vp, _vp]),
+    "dspark_schedule_zos_budget": (_i, [_vp, _i, _i, _vp, _i, _vp, _u64, _vp]),
     "dspark_pack": (_i, [_vp, _vp, _vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dspark_verify": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                            _i, _f, _u64, _u64, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -177,6 +179,19 @@ def dspark_schedule(surv, sps, mode, window, K_out, theta_out, stream=None):
     bs, gamma = surv.shape
     _check(lib().dspark_schedule(_p(surv), bs, gamma, _p(sps), sps.numel() - 1, int(mode), _p(window),
                                  _p(K_out), _p(theta_out), _stream(stream)), "dspark_schedule")
+
+
+def dspark_schedule_zos_select(surv, sps, budget_ring, step, window, K_out, stream=None):
+    bs, gamma = surv.shape
+    _check(lib().dspark_schedule_zos_select(_p(surv), bs, gamma, _p(sps), sps.numel() - 1, _p(budget_ring),
+                                            int(step), _p(window), _p(K_out), _stream(stream)),
+           "dspark_schedule_zos_select")
+
+
+def dspark_schedule_zos_budget(surv, sps, budget_ring, step, stream=None):
+    bs, gamma = surv.shape
+    _check(lib().dspark_schedule_zos_budget(_p(surv), bs, gamma, _p(sps), sps.numel() - 1, _p(budget_ring),
+                                            int(step), _stream(stream)), "dspark_schedule_zos_budget")
 
 
 def dspark_pack(window, anchor, tokens, tiers, cu_seqlens, ids, req, pos, padded_total, ws, stream=None):

@@ -206,20 +206,31 @@ __device__ void bitonic_sort(const float* __restrict__ surv, int n, unsigned lon
   for (int e = 0; e < E; ++e) out[tid * E + e] = v[e];
 }
 
-__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
-    const float* __restrict__ surv, int bs, int gamma, const double* __restrict__ sps, int m_max,
-    int mode, int32_t* __restrict__ window, int32_t* __restrict__ K_out,
-    double* __restrict__ theta_out) {
-  __shared__ unsigned long long sched_buf[kSchedMaxSlots];  // sorted keys, then prefix sums
-  __shared__ unsigned short slot[kSchedMaxSlots];
-  __shared__ long long wsum[32];
-  __shared__ int red_k[32];
-  __shared__ long long red_v[32];
-  __shared__ int win[DSPARK_MAX_BS];
-  __shared__ int s_kstar;
+// Shared state of one scheduler block.
+struct SchedShared {
+  unsigned long long buf[kSchedMaxSlots];  // sorted keys, then prefix sums (radix histogram)
+  unsigned short slot[kSchedMaxSlots];     // slot index r * gamma + j of rank i
+  long long wsum[32];
+  long long red_v[32];
+  int red_k[32];
+  int win[DSPARK_MAX_BS];
+  int kstar;
+};
+
+// The synchronous search: ranks the slots (sh.slot), forms the fixed-point prefix sums and
+// returns K* of `mode` (also in sh.kstar); Theta(K*) goes to theta_out unless it is null.
+// Zeroes sh.win.
+__device__ int sched_search(const float* __restrict__ surv, int bs, int gamma,
+                            const double* __restrict__ sps, int m_max, int mode, SchedShared& sh,
+                            double* __restrict__ theta_out) {
   const int tid = threadIdx.x;
   const int n = bs * gamma;
-  unsigned long long* src = sched_buf;
+  unsigned long long* src = sh.buf;
+  unsigned short* slot = sh.slot;
+  long long* wsum = sh.wsum;
+  int* red_k = sh.red_k;
+  long long* red_v = sh.red_v;
+  int* win = sh.win;
 
   // Bitonic sort of the n keys padded with sentinels (above every real key: survival 0 has high
   // word 0xFFFFFFFF, real slot indices are below 4096) to N = max(1024, 2^ceil(log2 n)) <= 4096.
@@ -337,21 +348,185 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
         }
       if (ks == INT_MAX) ks = 0;  // every Theta NaN
     }
-    s_kstar = ks;
-    *K_out = ks;
-    *theta_out = theta(ks);
+    sh.kstar = ks;
+    if (theta_out) *theta_out = theta(ks);
   }
   __syncthreads();
-  const int ks = s_kstar;
-  for (int i = tid; i < ks; i += kSchedThreads) atomicAdd(&win[slot[i] / gamma], 1);
+  return sh.kstar;
+}
+
+// window[r] = how many of the first K ranked slots (sh.slot) belong to request r.
+__device__ void sched_windows(SchedShared& sh, int K, int bs, int gamma, int32_t* __restrict__ window) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i < K; i += kSchedThreads) atomicAdd(&sh.win[sh.slot[i] / gamma], 1);
   __syncthreads();
-  for (int r = tid; r < bs; r += kSchedThreads) window[r] = win[r];
+  for (int r = tid; r < bs; r += kSchedThreads) window[r] = sh.win[r];
+}
+
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
+    const float* __restrict__ surv, int bs, int gamma, const double* __restrict__ sps, int m_max,
+    int mode, int32_t* __restrict__ window, int32_t* __restrict__ K_out,
+    double* __restrict__ theta_out) {
+  __shared__ SchedShared sh;
+  const int ks = sched_search(surv, bs, gamma, sps, m_max, mode, sh, theta_out);
+  if (threadIdx.x == 0) *K_out = ks;
+  if (window) sched_windows(sh, ks, bs, gamma, window);
 }
 
 cudaError_t launch_schedule(const float* surv, int bs, int gamma, const double* sps, int m_max,
                             int mode, int32_t* window, int32_t* K_out, double* theta_out,
                             cudaStream_t s) {
   schedule_kernel<<<1, kSchedThreads, 0, s>>>(surv, bs, gamma, sps, m_max, mode, window, K_out, theta_out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------
+// S3 under zero-overhead scheduling.  DSpark technical summary, "Infra" (scheduler bullet);
+// DSpark in SGLang, "ZOS": the verify budget of step t is predicted from the confidence of
+// step t - 2, while the current candidates are still ranked by the current survival; with the
+// stale budget the search over the table is global (no early stop).
+// The budget of a step is the global search above (schedule_kernel without windows), written
+// to slot step & 1 of a two-entry device ring; the select of step t reads slot t & 1 before
+// the budget of step t overwrites it.  The select needs no prefix sums and no full order: a
+// three-pass radix selection (11, 11, 10 bits of the descending-survival key) finds the K
+// smallest keys, equal keys going to the lower slot index, as in the full ranking.
+// ---------------------------------------------------------------------------------------
+constexpr int kRadixBins = 2048;
+
+// Exclusive block-wide prefix sum of one int per thread over the 1024 threads; the block
+// total goes to *total.  `wtot` holds 32 ints of shared memory.
+__device__ __forceinline__ int block_excl_scan(int x, int* wtot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wtot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int t = wtot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, t, o);
+      if (lane >= o) t += y;
+    }
+    wtot[lane] = t;  // inclusive over warps
+  }
+  __syncthreads();
+  const int res = incl - x + (warp > 0 ? wtot[warp - 1] : 0);
+  *total = wtot[31];
+  __syncthreads();  // wtot may be reused
+  return res;
+}
+
+__global__ void __launch_bounds__(kSchedThreads) zos_select_kernel(
+    const float* __restrict__ surv, int bs, int gamma, const double* __restrict__ sps, int m_max,
+    const int32_t* __restrict__ ring, uint64_t step, int32_t* __restrict__ window,
+    int32_t* __restrict__ K_out) {
+  __shared__ SchedShared sh;
+  __shared__ int s_K, s_bin, s_before;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int n = bs * gamma;
+  const int kmax = min(n, m_max - bs);
+  if (tid == 0) s_K = ring[step & 1];
+  for (int e = tid; e < DSPARK_MAX_BS; e += kSchedThreads) sh.win[e] = 0;
+  __syncthreads();
+  if (s_K < 0) {  // no budget recorded two steps back: the global search over this survival
+    const int ks = sched_search(surv, bs, gamma, sps, m_max, DSPARK_SCHED_GLOBAL_ARGMAX, sh, nullptr);
+    if (tid == 0) *K_out = ks;
+    sched_windows(sh, ks, bs, gamma, window);
+    return;
+  }
+  const int K = min(s_K, kmax);
+
+  // Thread t holds slots t E .. t E + E - 1 (E <= 4): key = ~bits of the survival (negatives
+  // rank as 0), state 0 undecided, 1 admitted, 2 not admitted.
+  const int E = (n + kSchedThreads - 1) / kSchedThreads;
+  uint32_t key[4];
+  int st[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int i = tid * E + e;
+    key[e] = 0u;
+    st[e] = 2;
+    if (e < E && i < n) {
+      uint32_t bits = __float_as_uint(surv[i]);
+      if (bits & 0x80000000u) bits = 0u;
+      key[e] = 0xFFFFFFFFu - bits;
+      st[e] = 0;
+    }
+  }
+  int* hist = reinterpret_cast<int*>(sh.buf);  // kRadixBins ints
+  int* wtot = sh.red_k;
+  int need = K;  // undecided slots still to admit; the undecided ones number at least `need`
+  for (int pass = 0; pass < 3 && need > 0; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const uint32_t mask = pass == 2 ? 0x3FFu : 0x7FFu;
+    hist[tid] = 0;
+    hist[tid + kSchedThreads] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {  // warp-aggregated histogram of the undecided keys' digits
+      const bool live = st[e] == 0;
+      const uint32_t d = live ? ((key[e] >> shift) & mask) : 0xFFFFFFFFu;
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, d);
+      if (live && lane == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+    }
+    __syncthreads();
+    const int h0 = hist[2 * tid], h1 = hist[2 * tid + 1];
+    int total;
+    const int ex = block_excl_scan(h0 + h1, wtot, &total);
+    // the digit holding the need-th smallest undecided key
+    if (ex < need && need <= ex + h0) {
+      s_bin = 2 * tid;
+      s_before = ex;
+    } else if (ex + h0 < need && need <= ex + h0 + h1) {
+      s_bin = 2 * tid + 1;
+      s_before = ex + h0;
+    }
+    __syncthreads();
+    const uint32_t bin = static_cast<uint32_t>(s_bin);
+    need -= s_before;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (st[e] != 0) continue;
+      const uint32_t d = (key[e] >> shift) & mask;
+      st[e] = d < bin ? 1 : (d > bin ? 2 : 0);
+    }
+  }
+  // The undecided slots share one key: the first `need` of them in slot order are admitted.
+  int cnt = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) cnt += st[e] == 0;
+  int total;
+  int rank = block_excl_scan(cnt, wtot, &total);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (st[e] != 0) continue;
+    st[e] = rank < need ? 1 : 2;
+    ++rank;
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (st[e] == 1) atomicAdd(&sh.win[(tid * E + e) / gamma], 1);
+  __syncthreads();
+  for (int r = tid; r < bs; r += kSchedThreads) window[r] = sh.win[r];
+  if (tid == 0) *K_out = K;
+}
+
+cudaError_t launch_zos_select(const float* surv, int bs, int gamma, const double* sps, int m_max,
+                              const int32_t* ring, uint64_t step, int32_t* window, int32_t* K_out,
+                              cudaStream_t s) {
+  zos_select_kernel<<<1, kSchedThreads, 0, s>>>(surv, bs, gamma, sps, m_max, ring, step, window, K_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zos_budget(const float* surv, int bs, int gamma, const double* sps, int m_max,
+                              int32_t* ring, uint64_t step, cudaStream_t s) {
+  schedule_kernel<<<1, kSchedThreads, 0, s>>>(surv, bs, gamma, sps, m_max, DSPARK_SCHED_GLOBAL_ARGMAX,
+                                              nullptr, ring + (step & 1), nullptr);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,101 @@
+"""GPU parity of the asynchronous (zero-overhead) scheduler through the C ABI: the budget ring,
+the radix top-K select and the first-steps fallback, bit-exact against the oracle over
+sequences of steps, at the benchmark's sizes and at the edges (one slot, 4096 slots, ties,
+K = 0, K beyond the batch, a table shorter than the batch)."""
+import numpy as np
+import pytest
+
+from oracle import dspark_oracle as O
+from speculative_decoding_draft_markov_gb300 import binding as B
+from speculative_decoding_draft_markov_gb300 import inputs as I
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _table(bs, gamma, kind):
+    m = bs * (gamma + 1)
+    if kind == "tiny":
+        return O.build_sps(1.0 + 0.002 * np.arange(65), [])
+    if kind == "short":    # K capped by m_max - bs
+        return O.build_sps(5.0 + 0.01 * np.arange(200), list(range(16, 200, 16)) + [199])
+    if kind == "flat":     # the global search admits every slot
+        return np.ones(m + 1)
+    step = 64 if kind == "sawtooth" else 16
+    return O.build_sps(5.0 + 0.01 * np.arange(m + 1), list(range(step, m, step)) + [m])
+
+
+CASES = [(4, 7, "tiny", False), (256, 7, "sawtooth", False), (256, 7, "sawtooth", True),
+         (256, 16, "tiers16", False), (1, 1, "tiers16", False), (33, 5, "tiers16", True),
+         (128, 15, "tiers16", False), (64, 7, "short", False), (200, 3, "flat", True)]
+
+
+def _survival(bs, gamma, seed, ties, t):
+    a = I.random_survival(bs, gamma, 1000 * seed + t, ties=ties)
+    if t == 3:   # all-equal keys and zeros in one step
+        a = np.where(np.arange(gamma)[None, :] < gamma // 2, np.float32(1.0), np.float32(0.0)).repeat(bs, 0)
+        a = a.astype(np.float32)
+    return a
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_zos_sequence_bit_exact(case):
+    bs, gamma, kind, ties = CASES[case]
+    sps_h = _table(bs, gamma, kind)
+    sps = torch.as_tensor(sps_h, device="cuda")
+    ring = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    ring_o = [-1, -1]
+    win = torch.zeros(bs, dtype=torch.int32, device="cuda")
+    K = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for t in range(6):
+        a = _survival(bs, gamma, case, ties, t)
+        surv = torch.as_tensor(a, device="cuda")
+        B.dspark_schedule_zos_select(surv, sps, ring, t, win, K)
+        B.dspark_schedule_zos_budget(surv, sps, ring, t)
+        w_o, K_o = O.zos_step(a, sps_h, ring_o, t)
+        np.testing.assert_array_equal(win.cpu().numpy(), w_o)
+        assert int(K.item()) == K_o, (t, int(K.item()), K_o)
+        assert ring.cpu().tolist() == ring_o, (t, ring.cpu().tolist(), ring_o)
+
+
+@pytest.mark.parametrize("shape", [(256, 7), (256, 16), (1, 1), (37, 5), (128, 15)])
+def test_zos_select_every_budget(shape):
+    """Budgets planted in the ring: the radix select equals the oracle's top-K for each."""
+    bs, gamma = shape
+    n = bs * gamma
+    m_max = bs + n
+    sps = torch.ones(m_max + 1, dtype=torch.float64, device="cuda")
+    win = torch.zeros(bs, dtype=torch.int32, device="cuda")
+    K = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for ties in (False, True):
+        a = I.random_survival(bs, gamma, n + ties, ties=ties)
+        surv = torch.as_tensor(a, device="cuda")
+        for Kp in sorted({0, 1, 2, n // 3, n // 2, n - 1, n, n + 5}):
+            if Kp < 0:
+                continue
+            ring = torch.tensor([Kp, -1], dtype=torch.int32, device="cuda")
+            B.dspark_schedule_zos_select(surv, sps, ring, 0, win, K)
+            Ke = min(Kp, n)
+            assert int(K.item()) == Ke
+            np.testing.assert_array_equal(win.cpu().numpy(), O.zos_select(a, Ke), err_msg=f"K={Kp}")
+
+
+def test_zos_select_tie_and_sign_edge_cases():
+    bs, gamma = 64, 8
+    sps = torch.ones(bs * (gamma + 1) + 1, dtype=torch.float64, device="cuda")
+    win = torch.zeros(bs, dtype=torch.int32, device="cuda")
+    K = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rng = np.random.default_rng(5)
+    variants = [np.ones((bs, gamma), np.float32),                     # every key equal
+                np.zeros((bs, gamma), np.float32),
+                np.full((bs, gamma), -0.0, np.float32),                # ranks as 0
+                -np.sort(-rng.choice(np.float32([1.0, 0.5, 2.0 ** -30, 1e-38, 0.0]),
+                                     size=(bs, gamma)), axis=1).astype(np.float32)]
+    for a in variants:
+        surv = torch.as_tensor(a, device="cuda")
+        for Kp in (0, 1, 63, 64, 65, 300, 511, 512):
+            ring = torch.tensor([-1, Kp], dtype=torch.int32, device="cuda")
+            B.dspark_schedule_zos_select(surv, sps, ring, 1, win, K)
+            Ke = min(Kp, bs * gamma)
+            expect = O.zos_select(np.maximum(a, 0) + np.float32(0), Ke)
+            np.testing.assert_array_equal(win.cpu().numpy(), expect)
