@@ -6,7 +6,8 @@ through the C ABI on one stream; the timed steps replay CUDA graphs captured fro
 directly.  The target forward is the caller's model and is not part of this path: it is a row
 gather here and it sits outside the timed segments; everything else is timed with CUDA events
 on the launching stream.  The L2 is flushed (256 MB write) between timed steps.
-tokens/step = sum over requests of (accepted + 1).
+tokens/step = sum over requests of (accepted + 1).  The same steps are timed again under the
+asynchronous scheduler (budget from two steps back on a second stream) and reported under "zos".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -271,84 +272,107 @@ def run_ours(args, rank: int, world: int):
     tokens_acc = torch.zeros(1, dtype=torch.int64, device=dev)
     tau = wl.temperature
 
+    side = torch.cuda.Stream(dev)
+    ring = S.zos_ring(dev)
+
     def draft_stage(it):
         B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], tau, wl.seed, it, buf.tokens,
                              buf.logit_x, buf.lse, buf.ws)
 
-    def conf_sched_pack_stage():
+    def conf_sched_pack_stage(it, zos):
         B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], buf.tokens, inp["w"], inp["b"], inp["sts_T"],
                             buf.conf, buf.surv)
-        B.dspark_schedule(buf.surv, sps, SCHED, buf.window, buf.K, buf.theta)
+        if zos:
+            B.dspark_schedule_zos_select(buf.surv, sps, ring, it, buf.window, buf.K)
+        else:
+            B.dspark_schedule(buf.surv, sps, SCHED, buf.window, buf.K, buf.theta)
         B.dspark_pack(buf.window, inp["anchor"], buf.tokens, tiers_dev, buf.cu, buf.ids, buf.req, buf.pos,
                       buf.padded, buf.ws)
 
-    def verify_stage(it):
+    def verify_stage(it, zos):
+        # asynchronous scheduler: the budget for step it + 2 forks onto a second stream and
+        # runs beside the verify, joined at the end of the stage
+        if zos:
+            S.schedule_budget(buf, sps, ring, it, stream, side)
         S.verify(inp, buf, tau, wl.seed, it, B.DSPARK_COMPACT)
+        if zos:
+            S.join_budget(stream, side)
 
     def count_tokens():
         tokens_acc.add_((buf.acc_len.to(torch.int64) + 1).sum())
 
-    for w in range(args.warmup):  # eager, through the API
-        draft_stage(10_000 + w)
-        conf_sched_pack_stage()
-        fwd(buf)
-        verify_stage(10_000 + w)
-        count_tokens()  # every op of the timed loop runs once before it (first-use set-up)
-    tokens_acc.zero_()
+    def measure(zos):
+        """Warm-up, graph capture and the timed steps of one scheduler variant."""
+        for w in range(args.warmup):  # eager, through the API
+            draft_stage(10_000 + w)
+            conf_sched_pack_stage(10_000 + w, zos)
+            fwd(buf)
+            verify_stage(10_000 + w, zos)
+            count_tokens()  # every op of the timed loop runs once before it (first-use set-up)
+        tokens_acc.zero_()
 
-    # The timed steps replay CUDA graphs of the same API calls, one per stage and step, captured
-    # here with each step's own counter (the draws differ step to step), then replayed once
-    # untimed so that the timed replays find them resident.
-    graphs = []
-    for it in range(args.steps):
-        gs = [torch.cuda.CUDAGraph() for _ in range(3)]
-        with torch.cuda.graph(gs[0]):
-            draft_stage(it)
-        with torch.cuda.graph(gs[1]):
-            conf_sched_pack_stage()
-        with torch.cuda.graph(gs[2]):
-            verify_stage(it)
-        graphs.append(gs)
-    for gs in graphs:
-        gs[0].replay()
-        gs[1].replay()
-        fwd(buf)
-        gs[2].replay()
-    torch.cuda.synchronize(dev)
-    st = B.dspark_read_device_status(buf.ws)
-    if st != 0:
-        raise RuntimeError("device status after warm-up: " + B.dspark_status_string(st))
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(dev) as clk:
-        t_host = time.perf_counter()
+        # The timed steps replay CUDA graphs of the same API calls, one per stage and step,
+        # captured here with each step's own counter (the draws differ step to step), then
+        # replayed once untimed so that the timed replays find them resident.
+        graphs = []
         for it in range(args.steps):
-            flush.fill_(it & 0xFF)  # L2 flush, outside the timed segments
-            e, gs = evs[it], graphs[it]
-            e[0].record(stream)
+            gs = [torch.cuda.CUDAGraph() for _ in range(3)]
+            with torch.cuda.graph(gs[0]):
+                draft_stage(it)
+            with torch.cuda.graph(gs[1]):
+                conf_sched_pack_stage(it, zos)
+            with torch.cuda.graph(gs[2]):
+                verify_stage(it, zos)
+            graphs.append(gs)
+        for gs in graphs:
             gs[0].replay()
-            e[1].record(stream)
             gs[1].replay()
-            e[2].record(stream)
-            fwd(buf)  # the caller's target forward: outside the timed segments
-            e[3].record(stream)
+            fwd(buf)
             gs[2].replay()
-            e[4].record(stream)
-            count_tokens()
-        t_host = time.perf_counter() - t_host  # host time to enqueue (the device may still run)
         torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    seg = np.array([[e[0].elapsed_time(e[2]), e[3].elapsed_time(e[4]), e[0].elapsed_time(e[1])] for e in evs])
+        st = B.dspark_read_device_status(buf.ws)
+        if st != 0:
+            raise RuntimeError("device status after warm-up: " + B.dspark_status_string(st))
+        tokens_acc.zero_()
+
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        with ClockSampler(dev) as clk:
+            t_host = time.perf_counter()
+            for it in range(args.steps):
+                flush.fill_(it & 0xFF)  # L2 flush, outside the timed segments
+                e, gs = evs[it], graphs[it]
+                e[0].record(stream)
+                gs[0].replay()
+                e[1].record(stream)
+                gs[1].replay()
+                e[2].record(stream)
+                fwd(buf)  # the caller's target forward: outside the timed segments
+                e[3].record(stream)
+                gs[2].replay()
+                e[4].record(stream)
+                count_tokens()
+            t_host = time.perf_counter() - t_host  # host time to enqueue (the device may still run)
+            torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        seg = np.array([[e[0].elapsed_time(e[2]), e[3].elapsed_time(e[4]), e[0].elapsed_time(e[1])] for e in evs])
+        st = B.dspark_read_device_status(buf.ws)
+        if st != 0:
+            raise RuntimeError("device status after the timed steps: " + B.dspark_status_string(st))
+        tokens = int(tokens_acc.item())
+        del graphs
+        return seg, tokens, t_host, clk.summary()
+
+    seg, tokens, t_host, clocks = measure(False)
     step_ms = seg[:, 0] + seg[:, 1]
     total_ms = float(step_ms.sum())
-    tokens = int(tokens_acc.item())
-    st = B.dspark_read_device_status(buf.ws)
-    if st != 0:
-        raise RuntimeError("device status after the timed steps: " + B.dspark_status_string(st))
+    # the same steps under the asynchronous scheduler (budget from two steps back, computed on
+    # a second stream beside the verify; the select alone on the step's path)
+    zseg, ztokens, _, zclocks = measure(True)
+    ztotal_ms = float((zseg[:, 0] + zseg[:, 1]).sum())
 
     # ---- end to end through the public API with host buffers (pinned), copies inside the timing
     host_U = inp["U"].cpu().pin_memory()
@@ -381,8 +405,9 @@ def run_ours(args, rank: int, world: int):
     e2e_ms = float(np.sum(t_e2e))
 
     # aggregate over ranks: max time, summed tokens
-    (total_ms, e2e_ms), (tokens, e2e_tokens) = aggregate_over_ranks([total_ms, e2e_ms], [tokens, e2e_tokens], dev)
-    tokens, e2e_tokens = int(tokens), int(e2e_tokens)
+    (total_ms, e2e_ms, ztotal_ms), (tokens, e2e_tokens, ztokens) = aggregate_over_ranks(
+        [total_ms, e2e_ms, ztotal_ms], [tokens, e2e_tokens, ztokens], dev)
+    tokens, e2e_tokens, ztokens = int(tokens), int(e2e_tokens), int(ztokens)
 
     hbm, bf16, peak_kind = _peaks()
     draft_bytes = draft_block_bytes(bs, gamma, V, r, torch.cuda.get_device_properties(dev).multi_processor_count)
@@ -422,7 +447,15 @@ def run_ours(args, rank: int, world: int):
         "e2e": {"value": e2e_tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
+        "zos": {"value": ztokens / (ztotal_ms * 1e-3), "unit": "tokens/s", "ms_per_step": ztotal_ms / args.steps,
+                "tokens_per_step": ztokens / args.steps / world,
+                "stage_ms": {"draft": float(zseg[:, 2].mean()),
+                             "conf_sched_pack": float((zseg[:, 0] - zseg[:, 2]).mean()),
+                             "verify_with_budget": float(zseg[:, 1].mean())},
+                "scheduler": "asynchronous: budget from the survival two steps back (global search, second "
+                             "stream beside the verify), radix top-K select on the step's path",
+                "gpu_launches": (launches_per_step + 1) * args.steps, "clocks": zclocks},
     }
 
 

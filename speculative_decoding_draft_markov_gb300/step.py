@@ -2,6 +2,9 @@
 
     draft_block -> confidence -> schedule -> pack -> target_forward(packed ids) -> verify
 
+or, with the asynchronous scheduler, schedule_zos_select in place of schedule and
+schedule_zos_budget beside the target forward and the verify (a second stream).
+
 `target_forward` is the caller's model: it receives the packed batch (ids / req / pos /
 cu_seqlens / padded total, all on the device) and fills the packed target-logit rows.
 Buffers are allocated once by PyTorch; the library itself allocates nothing."""
@@ -86,15 +89,26 @@ def gather_target_forward(target_full):
     return fwd
 
 
+def zos_ring(device="cuda"):
+    """The two-entry budget ring of the asynchronous scheduler, empty (-1) before the first step."""
+    import torch
+    return torch.full((2,), -1, dtype=torch.int32, device=device)
+
+
 def draft_and_schedule(inp: dict, buf: StepBuffers, sps, temperature: float, seed: int, step: int,
                        sched_mode: int = B.DSPARK_SCHED_EARLY_STOP, mode: int = B.DSPARK_COMPACT,
-                       tiers=None, stream=None) -> None:
-    """Stages S1-S4 (everything before the target forward)."""
+                       tiers=None, stream=None, ring=None) -> None:
+    """Stages S1-S4 (everything before the target forward).  With a budget ring the scheduler
+    is the asynchronous one: the windows take the budget recorded two steps back
+    (schedule_budget records this step's)."""
     B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], temperature, seed, step,
                          buf.tokens, buf.logit_x, buf.lse, buf.ws, stream)
     B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], buf.tokens, inp["w"], inp["b"], inp["sts_T"],
                         buf.conf, buf.surv, stream)
-    B.dspark_schedule(buf.surv, sps, sched_mode, buf.window, buf.K, buf.theta, stream)
+    if ring is not None:
+        B.dspark_schedule_zos_select(buf.surv, sps, ring, step, buf.window, buf.K, stream)
+    else:
+        B.dspark_schedule(buf.surv, sps, sched_mode, buf.window, buf.K, buf.theta, stream)
     B.dspark_pack(buf.window if mode == B.DSPARK_COMPACT else None, inp["anchor"], buf.tokens, tiers,
                   buf.cu, buf.ids, buf.req, buf.pos, buf.padded, buf.ws, stream)
 
@@ -107,12 +121,36 @@ def verify(inp: dict, buf: StepBuffers, temperature: float, seed: int, step: int
                     buf.ceiling, buf.ws, stream)
 
 
+def schedule_budget(buf: StepBuffers, sps, ring, step: int, main=None, side=None) -> None:
+    """Record the budget this step's survival predicts for step + 2.  With a side stream the
+    call forks off `main` (after this step's select) and `join_budget` merges it back, so it
+    overlaps the target forward and the verify instead of sitting on the step's path."""
+    import torch
+    if side is None:
+        B.dspark_schedule_zos_budget(buf.surv, sps, ring, step, main)
+        return
+    main = main if main is not None else torch.cuda.current_stream()
+    side.wait_stream(main)
+    B.dspark_schedule_zos_budget(buf.surv, sps, ring, step, side)
+
+
+def join_budget(main=None, side=None) -> None:
+    import torch
+    if side is not None:
+        (main if main is not None else torch.cuda.current_stream()).wait_stream(side)
+
+
 def run_step(inp: dict, buf: StepBuffers, sps, target_forward: Callable[[StepBuffers], None],
              temperature: float, seed: int, step: int, mode: int = B.DSPARK_COMPACT,
-             sched_mode: int = B.DSPARK_SCHED_EARLY_STOP, tiers=None, stream=None) -> None:
-    draft_and_schedule(inp, buf, sps, temperature, seed, step, sched_mode, mode, tiers, stream)
+             sched_mode: int = B.DSPARK_SCHED_EARLY_STOP, tiers=None, stream=None, ring=None,
+             side_stream=None) -> None:
+    draft_and_schedule(inp, buf, sps, temperature, seed, step, sched_mode, mode, tiers, stream, ring)
+    if ring is not None:
+        schedule_budget(buf, sps, ring, step, stream, side_stream)
     target_forward(buf)
     verify(inp, buf, temperature, seed, step, mode, stream)
+    if ring is not None:
+        join_budget(stream, side_stream)
 
 
 def device_inputs_from_host(host: dict, device="cuda") -> dict:

@@ -99,3 +99,35 @@ def test_zos_select_tie_and_sign_edge_cases():
             Ke = min(Kp, bs * gamma)
             expect = O.zos_select(np.maximum(a, 0) + np.float32(0), Ke)
             np.testing.assert_array_equal(win.cpu().numpy(), expect)
+
+
+def test_zos_inside_the_step_with_a_second_stream():
+    """The orchestrated step (step.run_step with a ring and a side stream for the budget): over
+    five steps of the mixed workload the windows of each step equal the oracle's asynchronous
+    scheduler applied to the survival the GPU produced, with the oracle's own ring."""
+    from speculative_decoding_draft_markov_gb300 import step as S
+    dev = torch.device("cuda")
+    wl = I.WORKLOADS["mixed_bs256"]
+    inp = I.make_device_inputs(wl, dev)
+    bs, gamma, V = wl.bs, wl.gamma, wl.V
+    cap = int(I.tiers_for(wl)[-1])
+    buf = S.StepBuffers.allocate(bs, gamma, V, cap, inp["U"].dtype, dev)
+    sps = S.sps_table(inp["T_raw"], inp["tiers"], dev)
+    sps_h = sps.cpu().numpy()
+    tiers = torch.as_tensor(inp["tiers"], device=dev)
+    fwd = S.gather_target_forward(inp["target"])
+    ring, ring_o = S.zos_ring(dev), [-1, -1]
+    side = torch.cuda.Stream(dev)
+    main = torch.cuda.current_stream(dev)
+    for t in range(5):
+        S.run_step(inp, buf, sps, fwd, wl.temperature, wl.seed, t, B.DSPARK_COMPACT, tiers=tiers,
+                   stream=main, ring=ring, side_stream=side)
+        torch.cuda.synchronize(dev)
+        assert B.dspark_read_device_status(buf.ws) == B.DSPARK_OK
+        w_o, K_o = O.zos_step(buf.surv.cpu().numpy(), sps_h, ring_o, t)
+        np.testing.assert_array_equal(buf.window.cpu().numpy(), w_o)
+        assert int(buf.K.item()) == K_o
+        assert ring.cpu().tolist() == ring_o
+        # the packed layout and the verify used those windows
+        assert int(buf.cu[-1].item()) == bs + K_o
+        assert np.all(buf.acc_len.cpu().numpy() <= w_o)
