@@ -11,6 +11,9 @@ It computes, plainly and slowly, in IEEE double:
   S3 schedule      -- hardware-aware global top-B prefix scheduler
   S4 pack          -- ragged cu_seqlens packing rounded up to a captured graph tier
   S5 verify        -- rejection-sampling verification (static / compact / cap-accept, greedy)
+  zos_*            -- the asynchronous scheduler (budget predicted two steps back)
+  observe, sts_fit -- observability records (ceiling, utilisation, ECE) and the sequential
+                      temperature scaling fit
 plus the host cost-table preparation (build_sps) and the shared random-number
 contract (Philox4x32-10 uniforms, Gumbel keys, two-level Gumbel-max sampler).
 
@@ -20,7 +23,8 @@ Sources, cited by page and section:
              "Architecture (drafter)", "Verification scheduling (system side)", "Infra".
   [SGLANG]   "DSpark in SGLang" blog post (Vietnamese and Chinese translations), sections
              "Verify modes", "Ragged verify under full CUDA graphs" (Fig. 2),
-             "Cost-table profiling" (Fig. 6).
+             "Observability", "Per-request differentiation under mixed traffic" (Fig. 4),
+             "ZOS", "Cost-table profiling" (Fig. 6).
   [VLLM]     "vLLM adaptive verification with DSpark", sections "DSpark confidence
              scheduling mechanism", "Technical implementation and CUDA Graphs".
   [PHILOX]   Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
@@ -583,3 +587,134 @@ def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x
 def step_tokens(acc_len) -> int:
     """Tokens committed by one step: accepted drafts plus the one extra token per request."""
     return int(np.sum(np.asarray(acc_len, dtype=np.int64) + 1))
+
+
+# ---------------------------------------------------------------------------
+# Observability and calibration
+# ---------------------------------------------------------------------------
+
+def ece_bin(conf_f32, n_bins: int) -> np.ndarray:
+    """Equal-width bin of a score in [0, 1]: floor(a * M) in fp32 arithmetic (the decision
+    both sides take in the same precision), the last bin closed at 1, negatives in bin 0."""
+    a = np.asarray(conf_f32, dtype=np.float32)
+    b = np.floor(a * np.float32(n_bins)).astype(np.int64)
+    return np.clip(b, 0, n_bins - 1)
+
+
+def ece(conf_f32, label, n_bins: int = 10):
+    """Expected calibration error of scores against 0/1 outcomes.
+
+    [SUMMARY, "Verification scheduling", STS] and [SGLANG, "Observability"] report ECE
+    without defining it.  Reading: the textbook definition -- M equal-width bins over [0, 1];
+    ECE = sum_b (n_b / N) |mean outcome_b - mean score_b| = sum_b |sum outcome_b - sum score_b| / N.
+    Returns (ece, count[M], sum outcome[M], sum score[M]); ece = 0 when N = 0."""
+    a = np.asarray(conf_f32, dtype=np.float32).ravel()
+    y = np.asarray(label, dtype=np.int64).ravel()
+    b = ece_bin(a, n_bins)
+    cnt = np.zeros(n_bins, dtype=np.int64)
+    lab = np.zeros(n_bins, dtype=np.int64)
+    sc = np.zeros(n_bins, dtype=np.float64)
+    for i in range(a.size):
+        cnt[b[i]] += 1
+        lab[b[i]] += y[i]
+        sc[b[i]] += float(a[i])
+    N = a.size
+    e = float(np.sum(np.abs(lab - sc)) / N) if N else 0.0
+    return e, cnt, lab, sc
+
+
+def prefix_labels(window, acc_len, ceiling, gamma: int):
+    """Realised outcome of each prefix survival a_{r,k}: did positions 1..k all pass?
+
+    With a ceiling (the accepted length over the whole block: cap-accept, or static's own
+    accepted length) the outcome is [ceiling >= k] at every k.  Without one (compact) it is
+    known only where the run decided it ([SGLANG, "Observability"]: pruning hides the
+    ceiling): [acc >= k] for k <= l_r, and 0 beyond l_r when the window was rejected inside;
+    unknown beyond l_r when the whole window passed.
+    Returns (label [bs, gamma] int64, known [bs, gamma] bool)."""
+    acc = np.asarray(acc_len, dtype=np.int64)
+    bs = acc.size
+    k = np.arange(1, gamma + 1)[None, :]
+    if ceiling is not None:
+        c = np.asarray(ceiling, dtype=np.int64)[:, None]
+        return (c >= k).astype(np.int64), np.ones((bs, gamma), dtype=bool)
+    w = np.full(bs, gamma, dtype=np.int64) if window is None else np.asarray(window, dtype=np.int64)
+    label = (acc[:, None] >= k).astype(np.int64)
+    known = (k <= w[:, None]) | (acc[:, None] < w[:, None])
+    return label, known
+
+
+MAX_GAMMA = 16  # histogram length - 1 (the block-length limit of the library's interface)
+
+
+def observe(surv_f32, window, acc_len, ceiling, n_bins: int = 10) -> dict:
+    """One step's observability record ([SGLANG, "Observability"]; "Per-request
+    differentiation under mixed traffic", Fig. 4):
+      - window and accepted-length sums and histograms, and with a ceiling (cap-accept) the
+        ceiling sum / histogram and the accepted sum over those requests (utilisation);
+      - calibration: ECE bins of the prefix survival against the realised prefix outcome,
+        over the (r, k) whose outcome is known, and the same per position k.
+    window None means gamma (static)."""
+    a = np.asarray(surv_f32, dtype=np.float32)
+    bs, gamma = a.shape
+    w = np.full(bs, gamma, dtype=np.int64) if window is None else np.asarray(window, dtype=np.int64)
+    acc = np.asarray(acc_len, dtype=np.int64)
+    H = MAX_GAMMA + 1
+    st = {"steps": 1, "requests": bs, "sum_window": int(w.sum()), "sum_accepted": int(acc.sum()),
+          "window_hist": np.bincount(w, minlength=H)[:H], "accepted_hist": np.bincount(acc, minlength=H)[:H],
+          "ceiling_requests": 0, "sum_ceiling": 0, "sum_accepted_ceiling": 0,
+          "ceiling_hist": np.zeros(H, dtype=np.int64)}
+    if ceiling is not None:
+        c = np.asarray(ceiling, dtype=np.int64)
+        st.update(ceiling_requests=bs, sum_ceiling=int(c.sum()), sum_accepted_ceiling=int(acc.sum()),
+                  ceiling_hist=np.bincount(c, minlength=H)[:H])
+    label, known = prefix_labels(w, acc, ceiling, gamma)
+    _, cnt, lab, sc = ece(a[known], label[known], n_bins)
+    st.update(bin_count=cnt, bin_label=lab, bin_score=sc)
+    st["pos_count"] = known.sum(axis=0).astype(np.int64)
+    st["pos_label"] = (label * known).sum(axis=0).astype(np.int64)
+    st["pos_score"] = np.array([float(np.sum(a[known[:, k], k].astype(np.float64))) for k in range(gamma)])
+    return st
+
+
+def obs_report(st: dict) -> dict:
+    """Summary of accumulated observability records: mean window, mean accepted length, mean
+    ceiling, utilisation = accepted / ceiling (ratio of sums over the requests that carry a
+    ceiling; Fig. 4's "utilisation against the ceiling"), ECE of the survival, and per
+    position the mean survival next to the realised pass rate."""
+    n = max(st["requests"], 1)
+    nc = st["ceiling_requests"]
+    N = int(np.sum(st["bin_count"]))
+    return {"mean_window": st["sum_window"] / n, "mean_accepted": st["sum_accepted"] / n,
+            "mean_ceiling": st["sum_ceiling"] / nc if nc else float("nan"),
+            "utilisation": st["sum_accepted_ceiling"] / st["sum_ceiling"] if st["sum_ceiling"] else float("nan"),
+            "ece": float(np.sum(np.abs(st["bin_label"] - st["bin_score"])) / N) if N else 0.0,
+            "pos_mean_survival": np.where(st["pos_count"] > 0, st["pos_score"] / np.maximum(st["pos_count"], 1), np.nan),
+            "pos_pass_rate": np.where(st["pos_count"] > 0, st["pos_label"] / np.maximum(st["pos_count"], 1), np.nan)}
+
+
+def sts_fit(z, ceiling, grid, n_bins: int = 10):
+    """Sequential temperature scaling fit ([SUMMARY, "Verification scheduling", STS]): left to
+    right over the positions, a one-dimensional grid search of T_k minimising the ECE of the
+    cumulative survival prod_{i<=k} sigmoid(z_i / T_i) (earlier T fixed), against the prefix
+    outcome [ceiling >= k]; dividing a logit by T > 0 keeps each position's order.
+    Ties: the lowest grid index.  Returns (T [gamma], ece of the chosen T [gamma], ece of
+    every grid value [gamma, n_grid])."""
+    z = np.asarray(z, dtype=np.float64)
+    N, gamma = z.shape
+    grid = np.asarray(grid, dtype=np.float64)
+    c = np.asarray(ceiling, dtype=np.int64)
+    prev = np.ones(N)
+    T = np.zeros(gamma)
+    best = np.zeros(gamma)
+    table = np.zeros((gamma, grid.size))
+    for k in range(gamma):
+        y = (c >= k + 1).astype(np.int64)
+        for g in range(grid.size):
+            a = prev / (1.0 + np.exp(-z[:, k] / grid[g]))
+            table[k, g] = ece(a.astype(np.float32), y, n_bins)[0]
+        g_star = int(np.argmin(table[k]))  # first minimum
+        T[k] = grid[g_star]
+        best[k] = table[k, g_star]
+        prev = prev / (1.0 + np.exp(-z[:, k] / T[k]))
+    return T, best, table

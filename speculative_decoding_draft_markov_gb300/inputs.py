@@ -196,6 +196,24 @@ def random_survival(bs: int, gamma: int, seed: int, ties: bool = False) -> np.nd
     return -np.sort(-v, axis=1)
 
 
+def calibration_steps(N: int, gamma: int, T_true, seed: int, mu0: float = 2.5, mu_slope: float = -0.25,
+                      z_std: float = 1.5):
+    """Synthetic labelled steps for the temperature fit (no real drafter: a known law).
+
+    Confidence logits z[i, k] ~ N(mu0 + mu_slope k, z_std^2) (float32).  Position k + 1 passes,
+    given that its prefix passed, with probability 1 / (1 + exp(-z[i, k] / T_true[k])); the
+    label is the accepted prefix length (the ceiling of a full-block verification).
+    Returns (z [N, gamma] float32, ceiling [N] int32)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 104]))
+    z = (mu0 + mu_slope * np.arange(gamma)[None, :]
+         + z_std * rng.standard_normal((N, gamma))).astype(np.float32)
+    T = np.asarray(T_true, dtype=np.float64)[None, :]
+    p_pass = 1.0 / (1.0 + np.exp(-z.astype(np.float64) / T))
+    passes = rng.random((N, gamma)) < p_pass
+    ceiling = np.where(passes.all(axis=1), gamma, np.argmin(passes, axis=1)).astype(np.int32)
+    return z, ceiling
+
+
 def random_windows(bs: int, gamma: int, seed: int) -> np.ndarray:
     rng = np.random.default_rng(np.random.SeedSequence([seed, 102]))
     return rng.integers(0, gamma + 1, size=bs).astype(np.int32)
