@@ -138,11 +138,12 @@ DSPARK_API int dspark_draft_block(const void* U, const void* W1, const void* W2t
  *   tokens   device [bs, gamma] int32 (x_1..x_gamma);  anchor device [bs] int32
  *   w        device [d + r] fp32;  sts_T device [gamma] fp32, each > 0
  *   conf, surv  device [bs, gamma] fp32 out
+ *   z_logit  device [bs, gamma] fp32 out or NULL: z before STS (the input of dspark_sts_fit)
  * Limits: as dspark_draft_block, and d % 8 == 0, 8 <= d <= 65536. */
 DSPARK_API int dspark_confidence(const void* h, const void* W1, int dtype, const int32_t* anchor,
                       const int32_t* tokens, const float* w, float b, const float* sts_T,
                       int bs, int gamma, int d, int r, int V,
-                      float* conf, float* surv, dspark_stream_t stream);
+                      float* conf, float* surv, float* z_logit, dspark_stream_t stream);
 
 /* S3. Hardware-aware global top-B prefix scheduler ([SUMMARY] "Verification scheduling",
  * Algorithm 1; [VLLM] "DSpark confidence scheduling mechanism"; [SUMMARY] "Infra").
@@ -256,6 +257,72 @@ DSPARK_API int dspark_draft_block_noalloc(const void* U, const void* W1, const v
                                           float temperature, uint64_t seed, uint64_t step,
                                           int32_t* tokens, float* logit_x, float* lse,
                                           uint32_t* device_status, dspark_stream_t stream);
+
+/* Observability and calibration ([SGLANG] "Observability", "Per-request differentiation under
+ * mixed traffic" Fig. 4; [SUMMARY] "Verification scheduling", STS).
+ *
+ * The outcome of a prefix survival a_{r,k}: did positions 1..k all pass?  With a ceiling (the
+ * accepted length over the whole block: a cap-accept run's `ceiling`, or a static run's
+ * acc_len) it is [ceiling_r >= k] at every k.  Without one (compact) it is known where the run
+ * decided it: [acc_r >= k] for k <= l_r, and 0 beyond l_r when the window was rejected inside;
+ * unknown beyond l_r when the whole window passed (pruning hides the ceiling).
+ * ECE over M equal-width bins of [0, 1] (bin = floor(a * M) in fp32, clamped to [0, M-1]):
+ *     ECE = sum_b |sum of outcomes in b - sum of scores in b| / (scored pairs). */
+#define DSPARK_OBS_MAX_BINS 64
+
+/* Accumulated records (device memory, zeroed by the caller before the first record).  Score
+ * sums are fixed point: sum of floor(a * 2^32) (a in [0, 1]; exact integer sums, so records
+ * are order-independent and reproducible). */
+typedef struct {
+  int64_t steps, requests, sum_window, sum_accepted;
+  int64_t ceiling_requests, sum_ceiling, sum_accepted_ceiling, reserved;
+  int64_t window_hist[DSPARK_MAX_GAMMA + 1];    /* requests by window length l_r           */
+  int64_t accepted_hist[DSPARK_MAX_GAMMA + 1];  /* requests by accepted length             */
+  int64_t ceiling_hist[DSPARK_MAX_GAMMA + 1];   /* requests by ceiling (ceiling runs only) */
+  int64_t bin_count[DSPARK_OBS_MAX_BINS];       /* scored (r, k) pairs per bin              */
+  int64_t bin_label[DSPARK_OBS_MAX_BINS];       /* passed prefixes per bin                  */
+  int64_t bin_score_fx[DSPARK_OBS_MAX_BINS];    /* sum of floor(a * 2^32) per bin           */
+  int64_t pos_count[DSPARK_MAX_GAMMA];          /* the same three per position k            */
+  int64_t pos_label[DSPARK_MAX_GAMMA];
+  int64_t pos_score_fx[DSPARK_MAX_GAMMA];
+} dspark_obs_stats;
+
+typedef struct {
+  double mean_window, mean_accepted, mean_ceiling; /* per request; mean_ceiling NaN if none */
+  double utilisation;      /* sum accepted / sum ceiling over ceiling runs (NaN if none)     */
+  double ece;              /* of the survival against the prefix outcomes                    */
+  double pos_mean_survival[DSPARK_MAX_GAMMA], pos_pass_rate[DSPARK_MAX_GAMMA]; /* NaN if none */
+  int64_t scored;          /* (r, k) pairs with a known outcome                              */
+} dspark_obs_summary;
+
+/* Add one step's record to `stats` (device).  surv device [bs, gamma] fp32 in [0, 1];
+ * window device [bs] int32 or NULL (= gamma, static); acc_len device [bs] int32;
+ * ceiling device [bs] int32 or NULL;  1 <= n_bins <= DSPARK_OBS_MAX_BINS.
+ * Device check (status word via ws, EINVAL): window, acc_len or ceiling outside [0, gamma],
+ * acc_len > window, or acc_len > ceiling; the step is then not recorded.  One thread block. */
+DSPARK_API int dspark_observe(const float* surv, const int32_t* window, const int32_t* acc_len,
+                   const int32_t* ceiling, int bs, int gamma, int n_bins,
+                   dspark_obs_stats* stats, void* ws, size_t ws_bytes, dspark_stream_t stream);
+
+/* Host: the summary of a host copy of accumulated records.  EINVAL on NULL or bad n_bins. */
+DSPARK_API int dspark_obs_report(const dspark_obs_stats* stats, int n_bins, dspark_obs_summary* out);
+
+/* Sequential temperature scaling fit ([SUMMARY] "Verification scheduling", STS): for
+ * k = 1..gamma in order, T_k = the grid value minimising the ECE of
+ *     a_{i,k} = prod_{j<k} sigmoid(z[i, j] / T_j) * sigmoid(z[i, k] / T)      (fp32)
+ * against [ceiling_i >= k] over the N labelled prefixes (earlier T_j fixed; ties: the lowest
+ * grid index).  ECE per grid value from exact fixed-point sums, in fp64.
+ *   z        device [N, gamma] fp32: confidence logits before STS (dspark_confidence z_logit)
+ *   ceiling  device [N] int32 in [0, gamma]: accepted prefix length over the whole block
+ *   grid     device [n_grid] fp32 temperatures, each > 0 (1 <= n_grid <= 1024)
+ *   T_out    device [gamma] fp32 out;  ece_out device [gamma] fp64 out (ECE at the chosen T)
+ *   ws       device scratch of dspark_sts_fit_workspace_bytes(n_grid, n_bins) bytes
+ * Limits: 1 <= N <= 2^30, 1 <= gamma <= DSPARK_MAX_GAMMA, 1 <= n_bins <= DSPARK_OBS_MAX_BINS.
+ * 3 gamma launches, all asynchronous. */
+DSPARK_API size_t dspark_sts_fit_workspace_bytes(int n_grid, int n_bins);
+DSPARK_API int dspark_sts_fit(const float* z, const int32_t* ceiling, int N, int gamma,
+                   const float* grid, int n_grid, int n_bins, float* T_out, double* ece_out,
+                   void* ws, size_t ws_bytes, dspark_stream_t stream);
 
 #ifdef __cplusplus
 }

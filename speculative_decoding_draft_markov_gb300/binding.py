@@ -34,11 +34,15 @@ _SIGS = {
     "dspark_draft_block_noalloc": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _u64, _u64,
                                         _vp, _vp, _vp, _vp, _vp]),
     "dspark_confidence": (_i, [_vp, _vp, _i, _vp, _vp, _vp, _f, _vp, _i, _i, _i, _i, _i,
-                               _vp, _vp, _vp]),
+                               _vp, _vp, _vp, _vp]),
     "dspark_schedule": (_i, [_vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp]),
     "dspark_schedule_zos_select": (_i, [_vp, _i, _i, _vp, _i, _vp, _u64, _vp, _vp, _vp]),
     "dspark_schedule_zos_budget": (_i, [_vp, _i, _i, _vp, _i, _vp, _u64, _vp]),
     "dspark_pack": (_i, [_vp, _vp, _vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dspark_observe": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _sz, _vp]),
+    "dspark_obs_report": (_i, [_vp, _i, _vp]),
+    "dspark_sts_fit_workspace_bytes": (_sz, [_i, _i]),
+    "dspark_sts_fit": (_i, [_vp, _vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "dspark_verify": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                            _i, _f, _u64, _u64, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
@@ -167,12 +171,12 @@ def dspark_draft_block_noalloc(U, W1, W2t, anchor, temperature, seed, step, toke
            "dspark_draft_block_noalloc")
 
 
-def dspark_confidence(h, W1, anchor, tokens, w, b, sts_T, conf, surv, stream=None):
+def dspark_confidence(h, W1, anchor, tokens, w, b, sts_T, conf, surv, stream=None, z_logit=None):
     bs, gamma, d = h.shape
     V, r = W1.shape
     _check(lib().dspark_confidence(_p(h), _p(W1), _dtype(h), _p(anchor), _p(tokens), _p(w), float(b),
-                                   _p(sts_T), bs, gamma, d, r, V, _p(conf), _p(surv), _stream(stream)),
-           "dspark_confidence")
+                                   _p(sts_T), bs, gamma, d, r, V, _p(conf), _p(surv), _p(z_logit),
+                                   _stream(stream)), "dspark_confidence")
 
 
 def dspark_schedule(surv, sps, mode, window, K_out, theta_out, stream=None):
@@ -213,3 +217,77 @@ def dspark_verify(target, cu_seqlens, window, mode, anchor, tokens, logit_x, lse
                                _p(W2t), r,
                                float(temperature), int(seed), int(step), _p(out_tokens), _p(acc_len),
                                _p(ceiling), _p(ws), ws.numel(), _stream(stream)), "dspark_verify")
+
+
+# ----------------------------------------------------------------------------- observability
+
+DSPARK_OBS_MAX_BINS = 64
+_H = DSPARK_MAX_GAMMA + 1
+
+
+class ObsStats(ctypes.Structure):
+    """dspark_obs_stats (include/dspark.h), field for field."""
+    _fields_ = [(n, ctypes.c_int64) for n in ("steps", "requests", "sum_window", "sum_accepted",
+                                               "ceiling_requests", "sum_ceiling", "sum_accepted_ceiling",
+                                               "reserved")] + \
+               [("window_hist", ctypes.c_int64 * _H), ("accepted_hist", ctypes.c_int64 * _H),
+                ("ceiling_hist", ctypes.c_int64 * _H),
+                ("bin_count", ctypes.c_int64 * DSPARK_OBS_MAX_BINS), ("bin_label", ctypes.c_int64 * DSPARK_OBS_MAX_BINS),
+                ("bin_score_fx", ctypes.c_int64 * DSPARK_OBS_MAX_BINS),
+                ("pos_count", ctypes.c_int64 * DSPARK_MAX_GAMMA), ("pos_label", ctypes.c_int64 * DSPARK_MAX_GAMMA),
+                ("pos_score_fx", ctypes.c_int64 * DSPARK_MAX_GAMMA)]
+
+
+class ObsSummary(ctypes.Structure):
+    """dspark_obs_summary (include/dspark.h)."""
+    _fields_ = [(n, ctypes.c_double) for n in ("mean_window", "mean_accepted", "mean_ceiling", "utilisation",
+                                                "ece")] + \
+               [("pos_mean_survival", ctypes.c_double * DSPARK_MAX_GAMMA),
+                ("pos_pass_rate", ctypes.c_double * DSPARK_MAX_GAMMA), ("scored", ctypes.c_int64)]
+
+
+def alloc_obs_stats(device="cuda"):
+    """Zeroed device records (an int64 tensor laid out as dspark_obs_stats)."""
+    import torch
+    return torch.zeros(ctypes.sizeof(ObsStats) // 8, dtype=torch.int64, device=device)
+
+
+def obs_stats_from(stats) -> ObsStats:
+    """Host copy of device records as the C structure."""
+    host = stats.detach().cpu().numpy().astype(np.int64)
+    out = ObsStats()
+    ctypes.memmove(ctypes.addressof(out), host.ctypes.data, ctypes.sizeof(ObsStats))
+    return out
+
+
+def dspark_observe(surv, window, acc_len, ceiling, n_bins, stats, ws, stream=None):
+    bs, gamma = surv.shape
+    _check(lib().dspark_observe(_p(surv), _p(window), _p(acc_len), _p(ceiling), bs, gamma, int(n_bins), _p(stats),
+                                _p(ws), ws.numel() * ws.element_size(), _stream(stream)), "dspark_observe")
+
+
+def dspark_obs_report(stats, n_bins) -> dict:
+    """The host summary of device (or host ObsStats) records, as a dict."""
+    st = stats if isinstance(stats, ObsStats) else obs_stats_from(stats)
+    out = ObsSummary()
+    _check(lib().dspark_obs_report(ctypes.addressof(st), int(n_bins), ctypes.addressof(out)), "dspark_obs_report")
+    return {"mean_window": out.mean_window, "mean_accepted": out.mean_accepted, "mean_ceiling": out.mean_ceiling,
+            "utilisation": out.utilisation, "ece": out.ece, "scored": out.scored,
+            "pos_mean_survival": list(out.pos_mean_survival), "pos_pass_rate": list(out.pos_pass_rate)}
+
+
+def dspark_sts_fit_workspace_bytes(n_grid: int, n_bins: int) -> int:
+    return int(lib().dspark_sts_fit_workspace_bytes(int(n_grid), int(n_bins)))
+
+
+def dspark_sts_fit(z, ceiling, grid, n_bins, T_out, ece_out, ws=None, stream=None):
+    """Sequential temperature scaling fit on labelled steps (device tensors); allocates its
+    scratch with PyTorch when `ws` is None."""
+    import torch
+    N, gamma = z.shape
+    n_grid = grid.numel()
+    nbytes = dspark_sts_fit_workspace_bytes(n_grid, n_bins)
+    if ws is None:
+        ws = torch.empty(max(nbytes, 8), dtype=torch.uint8, device=z.device)
+    _check(lib().dspark_sts_fit(_p(z), _p(ceiling), N, gamma, _p(grid), n_grid, int(n_bins), _p(T_out), _p(ece_out),
+                                _p(ws), ws.numel() * ws.element_size(), _stream(stream)), "dspark_sts_fit")

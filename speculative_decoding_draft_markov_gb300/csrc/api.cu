@@ -136,7 +136,7 @@ int dspark_draft_block(const void* U, const void* W1, const void* W2t, int dtype
 
 int dspark_confidence(const void* h, const void* W1, int dtype, const int32_t* anchor,
                       const int32_t* tokens, const float* w, float b, const float* sts_T, int bs,
-                      int gamma, int d, int r, int V, float* conf, float* surv,
+                      int gamma, int d, int r, int V, float* conf, float* surv, float* z_logit,
                       dspark_stream_t stream) {
   if (!h || !W1 || !anchor || !tokens || !w || !sts_T || !conf || !surv) return DSPARK_EINVAL;
   if (!valid_dtype(dtype) || !std::isfinite(b)) return DSPARK_EINVAL;
@@ -144,10 +144,10 @@ int dspark_confidence(const void* h, const void* W1, int dtype, const int32_t* a
   if (d < 8 || d % 8 != 0) return DSPARK_EINVAL;
   if (d > 65536) return DSPARK_EUNSUPPORTED;
   if (!al(h, 16) || !al(W1, 16) || !al(w, 16) || !al(anchor, 4) || !al(tokens, 4) ||
-      !al(sts_T, 4) || !al(conf, 4) || !al(surv, 4))
+      !al(sts_T, 4) || !al(conf, 4) || !al(surv, 4) || !al(z_logit, 4))
     return DSPARK_EINVAL;
   return cuda_status(launch_confidence(dtype, h, W1, anchor, tokens, w, b, sts_T, bs, gamma, d, r, V,
-                                       conf, surv, reinterpret_cast<cudaStream_t>(stream)));
+                                       conf, surv, z_logit, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int dspark_schedule(const float* surv, int bs, int gamma, const double* sps, int m_max, int mode,
@@ -225,6 +225,68 @@ int dspark_verify(const void* target, int dtype, const int32_t* cu_seqlens, cons
                                    tokens, logit_x, lse, draft_logits, U, W1, W2t, r, inv_tau, greedy,
                                    seed, step, out_tokens, acc_len, ceiling, ws,
                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dspark_observe(const float* surv, const int32_t* window, const int32_t* acc_len,
+                   const int32_t* ceiling, int bs, int gamma, int n_bins, dspark_obs_stats* stats,
+                   void* ws, size_t ws_bytes, dspark_stream_t stream) {
+  if (!surv || !acc_len || !stats) return DSPARK_EINVAL;
+  if (bs < 1 || gamma < 1 || n_bins < 1 || n_bins > DSPARK_OBS_MAX_BINS) return DSPARK_EINVAL;
+  if (bs > DSPARK_MAX_BS || gamma > DSPARK_MAX_GAMMA) return DSPARK_EUNSUPPORTED;
+  if (!al(surv, 4) || !al(window, 4) || !al(acc_len, 4) || !al(ceiling, 4) || !al(stats, 8))
+    return DSPARK_EINVAL;
+  if (!ws || !al(ws, 256) || ws_bytes < 256) return DSPARK_EWORKSPACE;
+  return cuda_status(launch_observe(surv, window, acc_len, ceiling, bs, gamma, n_bins, stats,
+                                    static_cast<uint32_t*>(ws), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dspark_obs_report(const dspark_obs_stats* st, int n_bins, dspark_obs_summary* out) {
+  if (!st || !out || n_bins < 1 || n_bins > DSPARK_OBS_MAX_BINS) return DSPARK_EINVAL;
+  const double nan = std::nan("");
+  std::memset(out, 0, sizeof(*out));
+  const double n = st->requests > 0 ? static_cast<double>(st->requests) : 1.0;
+  out->mean_window = static_cast<double>(st->sum_window) / n;
+  out->mean_accepted = static_cast<double>(st->sum_accepted) / n;
+  out->mean_ceiling = st->ceiling_requests > 0
+                          ? static_cast<double>(st->sum_ceiling) / static_cast<double>(st->ceiling_requests)
+                          : nan;
+  out->utilisation = st->sum_ceiling > 0
+                         ? static_cast<double>(st->sum_accepted_ceiling) / static_cast<double>(st->sum_ceiling)
+                         : nan;
+  int64_t scored = 0;
+  double num = 0.0;
+  for (int b = 0; b < n_bins; ++b) {
+    scored += st->bin_count[b];
+    // |passed 2^32 - score sum| exact in integers, then scaled
+    const int64_t d = static_cast<int64_t>(static_cast<uint64_t>(st->bin_label[b]) << 32) - st->bin_score_fx[b];
+    num += static_cast<double>(d < 0 ? -d : d);
+  }
+  out->scored = scored;
+  out->ece = scored > 0 ? std::ldexp(num, -32) / static_cast<double>(scored) : 0.0;
+  for (int k = 0; k < DSPARK_MAX_GAMMA; ++k) {
+    const int64_t c = st->pos_count[k];
+    out->pos_mean_survival[k] = c > 0 ? std::ldexp(static_cast<double>(st->pos_score_fx[k]), -32) / c : nan;
+    out->pos_pass_rate[k] = c > 0 ? static_cast<double>(st->pos_label[k]) / c : nan;
+  }
+  return DSPARK_OK;
+}
+
+size_t dspark_sts_fit_workspace_bytes(int n_grid, int n_bins) {
+  if (n_grid < 1 || n_grid > 1024 || n_bins < 1 || n_bins > DSPARK_OBS_MAX_BINS) return 0;
+  return sts_fit_ws_bytes(n_grid, n_bins);
+}
+
+int dspark_sts_fit(const float* z, const int32_t* ceiling, int N, int gamma, const float* grid,
+                   int n_grid, int n_bins, float* T_out, double* ece_out, void* ws, size_t ws_bytes,
+                   dspark_stream_t stream) {
+  if (!z || !ceiling || !grid || !T_out || !ece_out) return DSPARK_EINVAL;
+  if (N < 1 || N > (1 << 30) || gamma < 1 || n_grid < 1 || n_bins < 1 || n_bins > DSPARK_OBS_MAX_BINS)
+    return DSPARK_EINVAL;
+  if (gamma > DSPARK_MAX_GAMMA || n_grid > 1024) return DSPARK_EUNSUPPORTED;
+  if (!al(z, 4) || !al(ceiling, 4) || !al(grid, 4) || !al(T_out, 4) || !al(ece_out, 8)) return DSPARK_EINVAL;
+  if (!ws || !al(ws, 8) || ws_bytes < sts_fit_ws_bytes(n_grid, n_bins)) return DSPARK_EWORKSPACE;
+  return cuda_status(launch_sts_fit(z, ceiling, N, gamma, grid, n_grid, n_bins, T_out, ece_out, ws,
+                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(1024) confidence_kernel(
     const T* __restrict__ h, const T* __restrict__ W1, const int32_t* __restrict__ anchor,
     const int32_t* __restrict__ tokens, const float* __restrict__ w, float b,
     const float* __restrict__ sts_T, int gamma, int d, int r, int V, int parts, float* __restrict__ conf,
-    float* __restrict__ surv) {
+    float* __restrict__ surv, float* __restrict__ z_out) {
   __shared__ float zp[DSPARK_MAX_GAMMA * 4];
   const int req = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pos = warp / parts, part = warp - pos * parts;
@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(1024) confidence_kernel(
       float z = zp[k * 4];
       for (int q = 1; q < parts; ++q) z += zp[k * 4 + q];
       z += b;
+      if (z_out) z_out[size_t(req) * gamma + k] = z;  // the logit before STS (calibration input)
       const float c = 1.f / (1.f + expf(-z / sts_T[k]));
       a *= c;
       conf[size_t(req) * gamma + k] = c;
@@ -90,16 +91,16 @@ __global__ void __launch_bounds__(1024) confidence_kernel(
 cudaError_t launch_confidence(int dtype, const void* h, const void* W1, const int32_t* anchor,
                               const int32_t* tokens, const float* w, float b, const float* sts_T,
                               int bs, int gamma, int d, int r, int V, float* conf, float* surv,
-                              cudaStream_t s) {
+                              float* z_out, cudaStream_t s) {
   const int parts = gamma <= 8 ? 4 : 2;  // warps per position: at most 1024 threads
   const int threads = 32 * parts * gamma;
   if (dtype == DSPARK_F32)
     confidence_kernel<float><<<bs, threads, 0, s>>>((const float*)h, (const float*)W1, anchor,
-                                                    tokens, w, b, sts_T, gamma, d, r, V, parts, conf, surv);
+                                                    tokens, w, b, sts_T, gamma, d, r, V, parts, conf, surv, z_out);
   else
     confidence_kernel<__nv_bfloat16><<<bs, threads, 0, s>>>(
         (const __nv_bfloat16*)h, (const __nv_bfloat16*)W1, anchor, tokens, w, b, sts_T, gamma, d,
-        r, V, parts, conf, surv);
+        r, V, parts, conf, surv, z_out);
   return cudaGetLastError();
 }
 

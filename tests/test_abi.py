@@ -85,7 +85,20 @@ def test_draft_host_validation(L):
 def test_other_entry_points_host_validation(L):
     f = FAKE
     # confidence: d not a multiple of 8
-    assert L.dspark_confidence(f, f, 1, f, f, f, 0.0, f, 4, 7, 60, 32, 1024, f, f, None) == B.DSPARK_EINVAL
+    assert L.dspark_confidence(f, f, 1, f, f, f, 0.0, f, 4, 7, 60, 32, 1024, f, f, None, None) == B.DSPARK_EINVAL
+    assert L.dspark_confidence(f, f, 1, f, f, f, 0.0, f, 4, 7, 64, 32, 1024, f, f, f + 2, None) == B.DSPARK_EINVAL
+    # observability: bad bin count, missing stats, missing workspace
+    assert L.dspark_observe(f, None, f, None, 4, 7, 0, f, f, 1 << 20, None) == B.DSPARK_EINVAL
+    assert L.dspark_observe(f, None, f, None, 4, 7, 65, f, f, 1 << 20, None) == B.DSPARK_EINVAL
+    assert L.dspark_observe(f, None, f, None, 4, 7, 10, None, f, 1 << 20, None) == B.DSPARK_EINVAL
+    assert L.dspark_observe(f, None, f, None, 4, 7, 10, f, None, 0, None) == B.DSPARK_EWORKSPACE
+    # temperature fit: sizes, grid too long, workspace too small
+    assert L.dspark_sts_fit_workspace_bytes(64, 10) == 64 * 3 * 10 * 8
+    assert L.dspark_sts_fit_workspace_bytes(0, 10) == 0 and L.dspark_sts_fit_workspace_bytes(8, 65) == 0
+    assert L.dspark_sts_fit(f, f, 0, 7, f, 8, 10, f, f, f, 1 << 20, None) == B.DSPARK_EINVAL
+    assert L.dspark_sts_fit(f, f, 100, 17, f, 8, 10, f, f, f, 1 << 20, None) == B.DSPARK_EUNSUPPORTED
+    assert L.dspark_sts_fit(f, f, 100, 7, f, 2000, 10, f, f, f, 1 << 30, None) == B.DSPARK_EUNSUPPORTED
+    assert L.dspark_sts_fit(f, f, 100, 7, f, 8, 10, f, f, f, 16, None) == B.DSPARK_EWORKSPACE
     # schedule: m_max < bs, bad mode, too many slots
     assert L.dspark_schedule(f, 4, 7, f, 3, 0, f, f, f, None) == B.DSPARK_EINVAL
     assert L.dspark_schedule(f, 4, 7, f, 64, 5, f, f, f, None) == B.DSPARK_EINVAL
@@ -134,3 +147,62 @@ def test_build_sps_matches_oracle(L):
         B.dspark_build_sps(np.array([1.0, -1.0]), np.zeros(0, np.int32))
     with pytest.raises(B.DSparkError):
         B.dspark_build_sps(np.ones(10), np.array([4, 4], np.int32))
+
+
+def test_obs_structures_match_the_header(tmp_path):
+    """The binding's ctypes structures have the C layout (sizes and field offsets)."""
+    import ctypes
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = ["steps", "sum_accepted_ceiling", "window_hist", "ceiling_hist", "bin_count", "bin_score_fx",
+              "pos_count", "pos_score_fx"]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"dspark.h\"\nint main(void){\n"
+                   'printf("%zu %zu\\n", sizeof(dspark_obs_stats), sizeof(dspark_obs_summary));\n'
+                   + "".join(f'printf("%zu\\n", offsetof(dspark_obs_stats, {f}));\n' for f in fields)
+                   + 'printf("%zu %zu\\n", offsetof(dspark_obs_summary, pos_pass_rate), offsetof(dspark_obs_summary, scored));\n'
+                   + "return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I" + os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    got = [int(x) for x in out]
+    assert got[0] == ctypes.sizeof(B.ObsStats) and got[1] == ctypes.sizeof(B.ObsSummary)
+    assert got[2:2 + len(fields)] == [getattr(B.ObsStats, f).offset for f in fields]
+    assert got[-2:] == [B.ObsSummary.pos_pass_rate.offset, B.ObsSummary.scored.offset]
+
+
+def test_obs_report_matches_oracle(L):
+    """The host report of the C library on records made from the oracle's observe()."""
+    rng = np.random.default_rng(4)
+    bs, gamma, M = 32, 7, 12
+    st = B.ObsStats()
+    recs = []
+    for t in range(3):
+        surv = I.random_survival(bs, gamma, 50 + t)
+        ceiling = rng.integers(0, gamma + 1, bs)
+        window = rng.integers(0, gamma + 1, bs)
+        acc = np.minimum(ceiling, window)
+        recs.append(O.observe(surv, window, acc, ceiling if t != 1 else None, M))
+    tot = {k: sum(r[k] for r in recs) for k in recs[0]}
+    for k in ("steps", "requests", "sum_window", "sum_accepted", "ceiling_requests", "sum_ceiling",
+              "sum_accepted_ceiling"):
+        setattr(st, k, int(tot[k]))
+    for k in ("window_hist", "accepted_hist", "ceiling_hist"):
+        getattr(st, k)[:] = [int(v) for v in tot[k]]
+    st.bin_count[:M] = [int(v) for v in tot["bin_count"]]
+    st.bin_label[:M] = [int(v) for v in tot["bin_label"]]
+    st.bin_score_fx[:M] = [int(round(v * 2.0 ** 32)) for v in tot["bin_score"]]
+    st.pos_count[:gamma] = [int(v) for v in tot["pos_count"]]
+    st.pos_label[:gamma] = [int(v) for v in tot["pos_label"]]
+    st.pos_score_fx[:gamma] = [int(round(v * 2.0 ** 32)) for v in tot["pos_score"]]
+    got = B.dspark_obs_report(st, M)
+    ref = O.obs_report(tot)
+    for k in ("mean_window", "mean_accepted", "mean_ceiling", "utilisation", "ece"):
+        assert got[k] == pytest.approx(ref[k], rel=1e-9, abs=1e-9), k
+    np.testing.assert_allclose(got["pos_mean_survival"][:gamma], ref["pos_mean_survival"], rtol=1e-9)
+    np.testing.assert_allclose(got["pos_pass_rate"][:gamma], ref["pos_pass_rate"], rtol=1e-12)
+    assert all(np.isnan(got["pos_pass_rate"][gamma:]))
+    assert got["scored"] == int(np.sum(tot["bin_count"]))
