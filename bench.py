@@ -409,6 +409,8 @@ def run_ours(args, rank: int, world: int):
         [total_ms, e2e_ms, ztotal_ms], [tokens, e2e_tokens, ztokens], dev)
     tokens, e2e_tokens, ztokens = int(tokens), int(e2e_tokens), int(ztokens)
 
+    obs = measure_observability(args, inp, buf, tau, wl, dev, stream, tiers_dev, fwd)
+
     hbm, bf16, peak_kind = _peaks()
     draft_bytes = draft_block_bytes(bs, gamma, V, r, torch.cuda.get_device_properties(dev).multi_processor_count)
     draft_ms = float(seg[:, 2].mean())
@@ -448,6 +450,7 @@ def run_ours(args, rank: int, world: int):
                 "d2h_bytes_per_step": bo},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
+        "observability": obs,
         "zos": {"value": ztokens / (ztotal_ms * 1e-3), "unit": "tokens/s", "ms_per_step": ztotal_ms / args.steps,
                 "tokens_per_step": ztokens / args.steps / world,
                 "stage_ms": {"draft": float(zseg[:, 2].mean()),
@@ -457,6 +460,73 @@ def run_ours(args, rank: int, world: int):
                              "stream beside the verify), radix top-K select on the step's path",
                 "gpu_launches": (launches_per_step + 1) * args.steps, "clocks": zclocks},
     }
+
+
+def measure_observability(args, inp, buf, tau, wl, dev, stream, tiers_dev, fwd):
+    """Observability and calibration beside the step: one cap-accept verification of the last
+    drafted block exposes the ceiling; dspark_observe records it (timed per call with events);
+    the temperature fit runs on 2^20 synthetic labelled prefixes drawn from a known law
+    (7 positions, 64 grid temperatures, 15 bins), timed after one untimed fit."""
+    import torch
+
+    from speculative_decoding_draft_markov_gb300 import binding as B
+    from speculative_decoding_draft_markov_gb300 import inputs as I
+    from speculative_decoding_draft_markov_gb300 import step as S
+    n_bins = 15
+    gamma = wl.gamma
+    # cap-accept verifies the whole block: static packing of the last drafted block, the
+    # stand-in target forward, then the verification with the scheduler's windows
+    B.dspark_pack(None, inp["anchor"], buf.tokens, tiers_dev, buf.cu, buf.ids, buf.req, buf.pos, buf.padded,
+                  buf.ws)
+    fwd(buf)
+    S.verify(inp, buf, tau, wl.seed, 30_000, B.DSPARK_CAP_ACCEPT)
+    stats = B.alloc_obs_stats(dev)
+    B.dspark_observe(buf.surv, buf.window, buf.acc_len, buf.ceiling, n_bins, stats, buf.ws)
+    torch.cuda.synchronize(dev)
+    # device time per call: a CUDA graph of `reps` back-to-back calls, replayed once untimed
+    # (eager calls from Python would time the host's launch rate instead)
+    reps = 20
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            B.dspark_observe(buf.surv, buf.window, buf.acc_len, buf.ceiling, n_bins, stats, buf.ws)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    stats.zero_()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    observe_us = e0.elapsed_time(e1) * 1e3 / reps
+    st = B.dspark_read_device_status(buf.ws)
+    if st != 0:
+        raise RuntimeError("device status after dspark_observe: " + B.dspark_status_string(st))
+    rep = B.dspark_obs_report(stats, n_bins)
+
+    N = 1 << 20
+    T_true = [1.5, 1.8, 1.2, 2.0, 1.4, 1.1, 1.7]
+    z_h, c_h = I.calibration_steps(N, gamma, T_true[:gamma], seed=77, mu0=3.0, mu_slope=-0.1)
+    z, c = torch.as_tensor(z_h, device=dev), torch.as_tensor(c_h, device=dev)
+    grid = torch.linspace(0.5, 3.65, 64, device=dev, dtype=torch.float32)
+    T = torch.zeros(gamma, dtype=torch.float32, device=dev)
+    ece = torch.zeros(gamma, dtype=torch.float64, device=dev)
+    ws = torch.empty(B.dspark_sts_fit_workspace_bytes(64, n_bins), dtype=torch.uint8, device=dev)
+    B.dspark_sts_fit(z, c, grid, n_bins, T, ece, ws)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    B.dspark_sts_fit(z, c, grid, n_bins, T, ece, ws)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return {"observe_us_per_step": observe_us,
+            "record": {"calls": reps, "verify": "cap-accept (ceiling exposed, commits as compact)",
+                       "mean_window": rep["mean_window"], "mean_accepted": rep["mean_accepted"],
+                       "mean_ceiling": rep["mean_ceiling"], "utilisation": rep["utilisation"],
+                       "ece": rep["ece"], "bins": n_bins},
+            "sts_fit": {"ms": e0.elapsed_time(e1), "prefixes": N, "positions": gamma, "grid": 64,
+                        "bins": n_bins, "T_true": T_true[:gamma],
+                        "T_fit": [round(float(x), 4) for x in T.tolist()],
+                        "ece": [round(float(x), 5) for x in ece.tolist()]}}
 
 
 def run_reference(args):
@@ -490,6 +560,9 @@ def run_profile_case(args):
     build.build()
     dev = torch.device("cuda", 0)
     wl = I.WORKLOADS[WORKLOAD].with_(gamma=args.gamma)
+    if args.profile_case == "observe":
+        run_observe_case(args, dev)
+        return
     inp = I.make_device_inputs(wl, dev, with_hidden=args.profile_case != "draft",
                                with_target=args.profile_case != "draft")
     bs, gamma, V = wl.bs, wl.gamma, wl.V
@@ -522,6 +595,49 @@ def run_profile_case(args):
         sys.exit(1)
 
 
+def run_observe_case(args, dev):
+    """Observability and calibration kernels on their own: 3 + 20 dspark_observe calls of a
+    bs 256, gamma 7 record (cap-accept, 15 bins; the 20 as one CUDA graph) and one
+    dspark_sts_fit on 2^18 labelled prefixes (7 positions, 64 grid values, 15 bins)."""
+    import torch
+
+    from speculative_decoding_draft_markov_gb300 import binding as B
+    from speculative_decoding_draft_markov_gb300 import inputs as I
+    bs, gamma, n_bins = 256, 7, 15
+    surv = torch.as_tensor(I.random_survival(bs, gamma, 1), device=dev)
+    rng = np.random.default_rng(0)
+    ceil = torch.as_tensor(rng.integers(0, gamma + 1, bs).astype(np.int32), device=dev)
+    win = torch.as_tensor(rng.integers(0, gamma + 1, bs).astype(np.int32), device=dev)
+    acc = torch.minimum(ceil, win).contiguous()
+    stats = B.alloc_obs_stats(dev)
+    ws = B.alloc_workspace(bs, gamma, 1024, dev)
+    for _ in range(3):
+        B.dspark_observe(surv, win, acc, ceil, n_bins, stats, ws)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(20):
+            B.dspark_observe(surv, win, acc, ceil, n_bins, stats, ws)
+    N = 1 << 18
+    z, c = I.calibration_steps(N, gamma, [1.5] * gamma, seed=1)
+    z, c = torch.as_tensor(z, device=dev), torch.as_tensor(c, device=dev)
+    grid = torch.linspace(0.5, 3.65, 64, device=dev)
+    T = torch.zeros(gamma, device=dev)
+    e = torch.zeros(gamma, dtype=torch.float64, device=dev)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    ev[0].record()
+    g.replay()
+    ev[1].record()
+    B.dspark_sts_fit(z, c, grid, n_bins, T, e)
+    ev[2].record()
+    torch.cuda.synchronize()
+    st = B.dspark_read_device_status(ws)
+    print(json.dumps({"case": "observe", "observe_us_per_call": ev[0].elapsed_time(ev[1]) * 1e3 / 20,
+                      "sts_fit_ms_2e18": ev[1].elapsed_time(ev[2]), "status": B.dspark_status_string(st)}))
+    if st != 0:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -529,7 +645,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["draft", "verify"], default=None,
+    ap.add_argument("--profile-case", choices=["draft", "verify", "observe"], default=None,
                     help="run one stage of the workload (small gamma) for an ncu capture; no JSON contract")
     ap.add_argument("--gamma", type=int, default=2, help="block length of --profile-case")
     args = ap.parse_args()

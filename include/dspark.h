@@ -311,7 +311,8 @@ DSPARK_API int dspark_obs_report(const dspark_obs_stats* stats, int n_bins, dspa
  * k = 1..gamma in order, T_k = the grid value minimising the ECE of
  *     a_{i,k} = prod_{j<k} sigmoid(z[i, j] / T_j) * sigmoid(z[i, k] / T)      (fp32)
  * against [ceiling_i >= k] over the N labelled prefixes (earlier T_j fixed; ties: the lowest
- * grid index).  ECE per grid value from exact fixed-point sums, in fp64.
+ * grid index).  The scores use the fast exponential (relative error ~1e-6: they are only
+ * binned); the ECE of each grid value comes from exact integer sums of floor(a 2^24), in fp64.
  *   z        device [N, gamma] fp32: confidence logits before STS (dspark_confidence z_logit)
  *   ceiling  device [N] int32 in [0, gamma]: accepted prefix length over the whole block
  *   grid     device [n_grid] fp32 temperatures, each > 0 (1 <= n_grid <= 1024)

@@ -10,8 +10,9 @@
 // cumulative survival.
 //
 // observe_kernel: one block adds one step's record (sums, histograms, ECE bins of the
-// survival against the prefix outcomes) to a device dspark_obs_stats with integer atomics.
-// STS fit, per position k: sts_bins_kernel (grid values x sample slices) accumulates the ECE
+// survival against the prefix outcomes) to a device dspark_obs_stats with integer atomics
+// (exact, so the records do not depend on the order of the additions).
+// STS fit, per position k: sts_bins_kernel (sample slices x grid chunks) accumulates the ECE
 // bins of every grid temperature, sts_pick_kernel takes the grid value of least ECE.
 #include "common.cuh"
 #include "internal.h"
@@ -51,44 +52,75 @@ __device__ __forceinline__ void add64(int64_t* dst, unsigned long long v) {
 // ---------------------------------------------------------------------------------------
 // One step's record.  Outcome of a_{r,k}: with a ceiling [c_r >= k] everywhere; without, known
 // for k <= l_r ([acc_r >= k]) and, when the window was rejected inside (acc_r < l_r), 0 beyond.
+// Every warp owns a private slice of shared sums (slots 0 .. n_bins-1: score bins;
+// DSPARK_OBS_MAX_BINS + k - 1: positions) filled with plain 32-bit shared atomics; the score
+// is split in 16-bit halves so that the 32-bit sums stay exact (<= 4096 scores per call).  The
+// slices are added up in a fixed order at the end.
 // ---------------------------------------------------------------------------------------
+constexpr int kObsWarps = kObsThreads / 32;
+constexpr int kObsSlots = DSPARK_OBS_MAX_BINS + DSPARK_MAX_GAMMA;
+
 __global__ void __launch_bounds__(kObsThreads) observe_kernel(
     const float* __restrict__ surv, const int32_t* __restrict__ window,
     const int32_t* __restrict__ acc_len, const int32_t* __restrict__ ceiling, int bs, int gamma,
     int n_bins, dspark_obs_stats* __restrict__ st, uint32_t* __restrict__ status) {
-  __shared__ unsigned int s_cnt[DSPARK_OBS_MAX_BINS + DSPARK_MAX_GAMMA];
-  __shared__ unsigned int s_lab[DSPARK_OBS_MAX_BINS + DSPARK_MAX_GAMMA];
-  __shared__ unsigned long long s_sc[DSPARK_OBS_MAX_BINS + DSPARK_MAX_GAMMA];
-  __shared__ unsigned int s_hist[3][kHist];
-  __shared__ unsigned int s_sum[3];
+  __shared__ unsigned s_part[kObsWarps][4][kObsSlots];  // count, passed, score lo, score hi
+  __shared__ unsigned s_hist[3][kHist];
+  __shared__ unsigned s_sum[3];
   __shared__ int s_bad;
-  const int tid = threadIdx.x;
-  constexpr int kSlots = DSPARK_OBS_MAX_BINS + DSPARK_MAX_GAMMA;
-  for (int i = tid; i < kSlots; i += kObsThreads) {
-    s_cnt[i] = 0u;
-    s_lab[i] = 0u;
-    s_sc[i] = 0ull;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = bs * gamma;
+
+  // every global read first (elements tid + j * 1024, j < 4, then this thread's request), so
+  // that their latencies overlap each other and the shared-memory set-up
+  float a[4];
+  int wk[4], acck[4], ck[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = tid + j * kObsThreads;
+    a[j] = 0.f;
+    wk[j] = acck[j] = ck[j] = 0;
+    if (e < n) {
+      const int r = e / gamma;
+      a[j] = surv[e];
+      wk[j] = window ? window[r] : gamma;
+      acck[j] = acc_len[r];
+      ck[j] = ceiling ? ceiling[r] : 0;
+    }
   }
+  int w = 0, acc = 0, c = 0;
+  if (tid < bs) {
+    w = window ? window[tid] : gamma;
+    acc = acc_len[tid];
+    c = ceiling ? ceiling[tid] : 0;
+  }
+  for (int i = tid; i < kObsWarps * 4 * kObsSlots; i += kObsThreads) (&s_part[0][0][0])[i] = 0u;
   if (tid < 3 * kHist) (&s_hist[0][0])[tid] = 0u;
   if (tid < 3) s_sum[tid] = 0u;
   if (tid == 0) s_bad = 0;
   __syncthreads();
 
-  for (int r = tid; r < bs; r += kObsThreads) {
-    const int w = window ? window[r] : gamma, acc = acc_len[r], c = ceiling ? ceiling[r] : 0;
-    const bool bad = w < 0 || w > gamma || acc < 0 || acc > w ||
-                     (ceiling && (c < 0 || c > gamma || acc > c));
-    if (bad) {
-      s_bad = 1;
-      continue;
+  // per request: checks, sums and histograms (bs <= 256: warps 0..7)
+  if (tid < ((bs + 31) & ~31)) {
+    bool ok = false;
+    if (tid < bs) {
+      const bool bad = w < 0 || w > gamma || acc < 0 || acc > w ||
+                       (ceiling && (c < 0 || c > gamma || acc > c));
+      if (bad) s_bad = 1;
+      ok = !bad;
     }
-    atomicAdd(&s_sum[0], unsigned(w));
-    atomicAdd(&s_sum[1], unsigned(acc));
-    atomicAdd(&s_hist[0][w], 1u);
-    atomicAdd(&s_hist[1][acc], 1u);
-    if (ceiling) {
-      atomicAdd(&s_sum[2], unsigned(c));
-      atomicAdd(&s_hist[2][c], 1u);
+    const unsigned sw = __reduce_add_sync(0xFFFFFFFFu, ok ? unsigned(w) : 0u);
+    const unsigned sa = __reduce_add_sync(0xFFFFFFFFu, ok ? unsigned(acc) : 0u);
+    const unsigned sc = __reduce_add_sync(0xFFFFFFFFu, ok ? unsigned(c) : 0u);
+    if (lane == 0) {
+      atomicAdd(&s_sum[0], sw);
+      atomicAdd(&s_sum[1], sa);
+      atomicAdd(&s_sum[2], sc);
+    }
+    if (ok) {
+      atomicAdd(&s_hist[0][w], 1u);
+      atomicAdd(&s_hist[1][acc], 1u);
+      if (ceiling) atomicAdd(&s_hist[2][c], 1u);
     }
   }
   __syncthreads();
@@ -97,47 +129,63 @@ __global__ void __launch_bounds__(kObsThreads) observe_kernel(
     return;
   }
 
-  const int n = bs * gamma;
-  for (int e = tid; e < n; e += kObsThreads) {
-    const int r = e / gamma, k = e - r * gamma + 1;
-    const int w = window ? window[r] : gamma, acc = acc_len[r];
-    int label;
-    bool known = true;
+  unsigned* cnt = s_part[warp][0];
+  unsigned* lab = s_part[warp][1];
+  unsigned* lo = s_part[warp][2];
+  unsigned* hi = s_part[warp][3];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = tid + j * kObsThreads;
+    if (e >= n) break;
+    const int k = e - (e / gamma) * gamma + 1;
+    unsigned passed;
     if (ceiling) {
-      label = ceiling[r] >= k;
+      passed = ck[j] >= k;
     } else {
-      label = acc >= k;
-      known = k <= w || acc < w;
+      passed = acck[j] >= k;
+      if (!(k <= wk[j] || acck[j] < wk[j])) continue;  // outcome unknown: the whole window passed
     }
-    if (!known) continue;
-    const float a = surv[e];
-    const unsigned long long fx = fix32(a);
-    const int b = score_bin(a, n_bins), p = DSPARK_OBS_MAX_BINS + (k - 1);
-    atomicAdd(&s_cnt[b], 1u);
-    atomicAdd(&s_cnt[p], 1u);
-    if (label) {
-      atomicAdd(&s_lab[b], 1u);
-      atomicAdd(&s_lab[p], 1u);
+    const unsigned long long fx = fix32(a[j]);
+    const unsigned flo = static_cast<unsigned>(fx & 0xFFFFu), fhi = static_cast<unsigned>(fx >> 16);
+    const int b = score_bin(a[j], n_bins), p = DSPARK_OBS_MAX_BINS + k - 1;
+    atomicAdd(&cnt[b], 1u);
+    atomicAdd(&cnt[p], 1u);
+    if (passed) {
+      atomicAdd(&lab[b], 1u);
+      atomicAdd(&lab[p], 1u);
     }
-    atomicAdd(&s_sc[b], fx);
-    atomicAdd(&s_sc[p], fx);
+    atomicAdd(&lo[b], flo);
+    atomicAdd(&lo[p], flo);
+    atomicAdd(&hi[b], fhi);
+    atomicAdd(&hi[p], fhi);
   }
   __syncthreads();
 
-  if (tid < n_bins) {
-    add64(&st->bin_count[tid], s_cnt[tid]);
-    add64(&st->bin_label[tid], s_lab[tid]);
-    add64(&st->bin_score_fx[tid], s_sc[tid]);
-  } else if (tid >= DSPARK_OBS_MAX_BINS && tid < DSPARK_OBS_MAX_BINS + gamma) {
-    const int k = tid - DSPARK_OBS_MAX_BINS;
-    add64(&st->pos_count[k], s_cnt[tid]);
-    add64(&st->pos_label[k], s_lab[tid]);
-    add64(&st->pos_score_fx[k], s_sc[tid]);
-  } else if (tid >= 128 && tid < 128 + 3 * kHist) {
-    const int h = (tid - 128) / kHist, i = (tid - 128) % kHist;
+  // each (array, slot) summed over the warps in a fixed order by its own thread, the halves of
+  // the score recombined through shared memory, then the 64-bit accumulators
+  unsigned long long* s_tot = reinterpret_cast<unsigned long long*>(&s_part[0][0][0]);  // reuses warp 0..
+  unsigned long long tot = 0;
+  const int q = tid / kObsSlots, i = tid - q * kObsSlots;  // array q < 4, slot i
+  const bool used = q < 4 && (i < n_bins || (i >= DSPARK_OBS_MAX_BINS && i < DSPARK_OBS_MAX_BINS + gamma));
+  if (used)
+    for (int wv = 0; wv < kObsWarps; ++wv) tot += s_part[wv][q][i];
+  __syncthreads();
+  if (used) s_tot[q * kObsSlots + i] = tot;
+  __syncthreads();
+  if (used && q < 3) {
+    unsigned long long v = tot;
+    if (q == 2) v = (s_tot[3 * kObsSlots + i] << 16) + tot;  // hi 2^16 + lo
+    if (i < n_bins) {
+      add64(q == 0 ? &st->bin_count[i] : (q == 1 ? &st->bin_label[i] : &st->bin_score_fx[i]), v);
+    } else {
+      const int k = i - DSPARK_OBS_MAX_BINS;
+      add64(q == 0 ? &st->pos_count[k] : (q == 1 ? &st->pos_label[k] : &st->pos_score_fx[k]), v);
+    }
+  } else if (tid >= 512 && tid < 512 + 3 * kHist) {
+    const int h = (tid - 512) / kHist, hi_i = (tid - 512) % kHist;
     int64_t* dst = h == 0 ? st->window_hist : (h == 1 ? st->accepted_hist : st->ceiling_hist);
-    add64(&dst[i], s_hist[h][i]);
-  } else if (tid == 256) {
+    add64(&dst[hi_i], s_hist[h][hi_i]);
+  } else if (tid == 600) {
     add64(&st->steps, 1ull);
     add64(&st->requests, static_cast<unsigned long long>(bs));
     add64(&st->sum_window, s_sum[0]);
@@ -160,64 +208,78 @@ cudaError_t launch_observe(const float* surv, const int32_t* window, const int32
 
 // ---------------------------------------------------------------------------------------
 // STS fit.  Accumulators per grid value g: [g][0][b] scored count, [g][1][b] passed prefixes,
-// [g][2][b] sum of floor(a 2^32).  Warp-aggregated: lanes of one bin add once through the lane
-// with the lowest index (the score split in 16-bit halves so that the warp sums stay exact).
+// [g][2][b] sum of floor(a 2^24) (the fit's internal quantum; the ECE it gives is within
+// 2^-24 of the exact one).  Block (x, y) takes samples [x S, x S + S) (S <= 2^15) and the grid
+// values of chunk y.  A warp loads 32 samples at a time (prefix product a_{k-1} with the fixed
+// temperatures, logit z_k, outcome) and then walks them one by one: the sample is broadcast
+// and lane l bins it for grid values l, l + 32, ...; so the lanes of an atomic never share a
+// slot.  Shared sums are 32-bit (score in 12-bit halves), flushed to 64-bit at the end.
 // ---------------------------------------------------------------------------------------
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+constexpr int kStsChunkBins = 2048;      // grid values x bins held in shared memory per block
+constexpr int kStsMaxSamples = 1 << 15;  // samples per block: the 32-bit shared sums stay exact
+
+// sigmoid(x) with the fast exponential and division intrinsics (relative error ~1e-6: the fit
+// only bins the scores)
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
 __global__ void __launch_bounds__(kStsThreads) sts_bins_kernel(
     const float* __restrict__ z, const int32_t* __restrict__ ceiling, int N, int gamma, int k,
-    const float* __restrict__ grid, const float* __restrict__ T_fixed, int n_bins,
-    unsigned long long* __restrict__ acc) {
-  __shared__ unsigned int s_cnt[DSPARK_OBS_MAX_BINS], s_lab[DSPARK_OBS_MAX_BINS];
-  __shared__ unsigned long long s_sc[DSPARK_OBS_MAX_BINS];
-  __shared__ float s_T[DSPARK_MAX_GAMMA];
-  const int tid = threadIdx.x, lane = tid & 31, g = blockIdx.x;
-  if (tid < DSPARK_OBS_MAX_BINS) {
-    s_cnt[tid] = 0u;
-    s_lab[tid] = 0u;
-    s_sc[tid] = 0ull;
-  }
-  if (tid < k) s_T[tid] = T_fixed[tid];
+    const float* __restrict__ grid, int n_grid, const float* __restrict__ T_fixed, int n_bins,
+    int per_block, unsigned long long* __restrict__ acc) {
+  __shared__ unsigned s_cnt[kStsChunkBins], s_lab[kStsChunkBins], s_lo[kStsChunkBins], s_hi[kStsChunkBins];
+  __shared__ float s_invT[DSPARK_MAX_GAMMA];
+  __shared__ float s_inv[kStsChunkBins];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per_chunk = kStsChunkBins / n_bins;
+  const int g0 = blockIdx.y * per_chunk;
+  const int ng = min(per_chunk, n_grid - g0);
+  for (int i = tid; i < ng * n_bins; i += kStsThreads) s_cnt[i] = s_lab[i] = s_lo[i] = s_hi[i] = 0u;
+  for (int i = tid; i < ng; i += kStsThreads) s_inv[i] = 1.f / grid[g0 + i];
+  if (tid < k) s_invT[tid] = 1.f / T_fixed[tid];
   __syncthreads();
-  const float Tg = grid[g];
-  const int stride = gridDim.y * kStsThreads;
-  for (int base = blockIdx.y * kStsThreads; base < N; base += stride) {  // uniform per warp
-    const int i = base + tid;
-    const bool live = i < N;
-    unsigned int b = 0xFFFFFFFFu, lab = 0u, lo = 0u, hi = 0u;
-    if (live) {
+  const float fM = static_cast<float>(n_bins);
+  const int i0 = blockIdx.x * per_block, i1 = min(N, i0 + per_block);
+  for (int base = i0 + warp * 32; base < i1; base += kStsThreads) {
+    const int i = base + lane;
+    float prev = 0.f, zk = 0.f;
+    unsigned passed = 0u;
+    if (i < i1) {
       const float* zi = z + size_t(i) * gamma;
-      float a = 1.f;
-      for (int j = 0; j < k; ++j) a *= sigmoid_f(zi[j] / s_T[j]);
-      a *= sigmoid_f(zi[k] / Tg);
-      b = static_cast<unsigned int>(score_bin(a, n_bins));
-      lab = ceiling[i] >= k + 1 ? 1u : 0u;
-      const unsigned long long fx = fix32(a);  // <= 2^32
-      lo = static_cast<unsigned int>(fx & 0xFFFFu);
-      hi = static_cast<unsigned int>(fx >> 16);
+      prev = 1.f;
+      for (int j = 0; j < k; ++j) prev *= sigmoid_fast(zi[j] * s_invT[j]);
+      zk = zi[k];
+      passed = ceiling[i] >= k + 1 ? 1u : 0u;
     }
-    const unsigned peers = __match_any_sync(0xFFFFFFFFu, b);
-    const unsigned n_peer = __popc(peers);
-    const unsigned sum_lab = __reduce_add_sync(peers, lab);
-    const unsigned sum_lo = __reduce_add_sync(peers, lo);
-    const unsigned sum_hi = __reduce_add_sync(peers, hi);
-    if (live && lane == __ffs(peers) - 1) {
-      atomicAdd(&s_cnt[b], n_peer);
-      if (sum_lab) atomicAdd(&s_lab[b], sum_lab);
-      atomicAdd(&s_sc[b], (static_cast<unsigned long long>(sum_hi) << 16) + sum_lo);
+    const int cnt_s = min(32, i1 - base);
+    for (int s = 0; s < cnt_s; ++s) {  // uniform per warp
+      const float p = __shfl_sync(0xFFFFFFFFu, prev, s);
+      const float zz = __shfl_sync(0xFFFFFFFFu, zk, s);
+      const unsigned ps = __shfl_sync(0xFFFFFFFFu, passed, s);
+      for (int g = lane; g < ng; g += 32) {
+        const float a = p * sigmoid_fast(zz * s_inv[g]);
+        const float xb = floorf(a * fM);
+        const int b = xb >= fM - 1.f ? n_bins - 1 : (xb >= 0.f ? static_cast<int>(xb) : 0);
+        const unsigned fx = static_cast<unsigned>(a * 16777216.f);  // floor(a 2^24), a in [0, 1]
+        const int slot = g * n_bins + b;
+        atomicAdd(&s_cnt[slot], 1u);
+        if (ps) atomicAdd(&s_lab[slot], 1u);
+        atomicAdd(&s_lo[slot], fx & 0xFFFu);
+        atomicAdd(&s_hi[slot], fx >> 12);
+      }
     }
   }
   __syncthreads();
-  if (tid < n_bins) {
+  for (int i = tid; i < ng * n_bins; i += kStsThreads) {
+    const int g = g0 + i / n_bins, b = i % n_bins;
     unsigned long long* row = acc + size_t(g) * 3 * n_bins;
-    if (s_cnt[tid]) atomicAdd(&row[tid], static_cast<unsigned long long>(s_cnt[tid]));
-    if (s_lab[tid]) atomicAdd(&row[n_bins + tid], static_cast<unsigned long long>(s_lab[tid]));
-    if (s_sc[tid]) atomicAdd(&row[2 * n_bins + tid], s_sc[tid]);
+    if (s_cnt[i]) atomicAdd(&row[b], static_cast<unsigned long long>(s_cnt[i]));
+    if (s_lab[i]) atomicAdd(&row[n_bins + b], static_cast<unsigned long long>(s_lab[i]));
+    const unsigned long long sc = (static_cast<unsigned long long>(s_hi[i]) << 12) + s_lo[i];
+    if (sc) atomicAdd(&row[2 * n_bins + b], sc);
   }
 }
 
-// ECE of every grid value from the integer sums (|passed 2^32 - score sum| exact in int64,
+// ECE of every grid value from the integer sums (|passed 2^24 - score sum| exact in int64,
 // then fp64 in bin order), and the least one (lowest grid index on ties).
 __global__ void __launch_bounds__(kStsThreads) sts_pick_kernel(
     const unsigned long long* __restrict__ acc, int n_grid, int n_bins, int N, int k,
@@ -227,10 +289,10 @@ __global__ void __launch_bounds__(kStsThreads) sts_pick_kernel(
     const unsigned long long* row = acc + size_t(g) * 3 * n_bins;
     double num = 0.0;
     for (int b = 0; b < n_bins; ++b) {
-      const long long d = static_cast<long long>(row[n_bins + b] << 32) - static_cast<long long>(row[2 * n_bins + b]);
+      const long long d = static_cast<long long>(row[n_bins + b] << 24) - static_cast<long long>(row[2 * n_bins + b]);
       num += static_cast<double>(d < 0 ? -d : d);
     }
-    s_e[g] = num * 0x1p-32 / static_cast<double>(N);
+    s_e[g] = num * 0x1p-24 / static_cast<double>(N);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -248,16 +310,20 @@ cudaError_t launch_sts_fit(const float* z, const int32_t* ceiling, int N, int ga
                            int n_grid, int n_bins, float* T_out, double* ece_out, void* ws,
                            cudaStream_t s) {
   unsigned long long* acc = static_cast<unsigned long long*>(ws);
-  const int want = 8 * tch::sm_count();  // blocks in flight across the grid values
-  int slices = (want + n_grid - 1) / n_grid;
-  const int max_slices = (N + kStsThreads - 1) / kStsThreads;
-  slices = slices < 1 ? 1 : (slices > max_slices ? max_slices : slices);
-  if (slices > 65535) slices = 65535;
+  const int per_chunk = kStsChunkBins / n_bins;
+  const int chunks = (n_grid + per_chunk - 1) / per_chunk;
+  // about four blocks per SM in all, at most 2^15 samples per block, whole warps of samples
+  const int want = 4 * tch::sm_count();
+  long long per = (static_cast<long long>(N) * chunks + want - 1) / want;
+  per = ((per + kStsThreads - 1) / kStsThreads) * kStsThreads;
+  if (per < kStsThreads) per = kStsThreads;
+  if (per > kStsMaxSamples) per = kStsMaxSamples;
+  const int slices = static_cast<int>((N + per - 1) / per);
   for (int k = 0; k < gamma; ++k) {
     cudaError_t e = cudaMemsetAsync(acc, 0, sts_fit_ws_bytes(n_grid, n_bins), s);
     if (e != cudaSuccess) return e;
-    sts_bins_kernel<<<dim3(n_grid, slices), kStsThreads, 0, s>>>(z, ceiling, N, gamma, k, grid, T_out,
-                                                                 n_bins, acc);
+    sts_bins_kernel<<<dim3(slices, chunks), kStsThreads, 0, s>>>(z, ceiling, N, gamma, k, grid, n_grid, T_out,
+                                                                 n_bins, static_cast<int>(per), acc);
     sts_pick_kernel<<<1, kStsThreads, 0, s>>>(acc, n_grid, n_bins, N, k, grid, T_out, ece_out);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
