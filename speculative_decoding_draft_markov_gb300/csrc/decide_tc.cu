@@ -19,8 +19,9 @@
 //   warp 1    = TMEM owner + single-thread tcgen05.mma issuer (A from TMEM, B from smem)
 //   warps 2-9 = epilogue, two warp sets of four (one per TMEM lane quarter); set h takes the
 //               tiles t = h, h + 2, ...: accumulator buffer h and gather stage h
-//   warps 10-13 = cp.async gather of the U rows and target rows of each tile, two warps per
-//               stage (64 rows each), so one stage refills while the other is reduced
+//   warps 10-13 = cp.async gather of the U rows and target rows of each tile by half tile: a
+//               ring of four half-tile slots (two per epilogue set), one warp per slot, each
+//               slot refilled as soon as its half is reduced
 // Every mbarrier wait is bounded (SM cycle-counter deadline + shared abort flag); on give-up the
 // kernel records DSPARK_ETIMEOUT, waits (bounded) for its own copies / MMAs in flight, frees
 // TMEM and returns.
@@ -42,22 +43,22 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBN = 128;                            // ids per tile: one chunk
 constexpr int kBK = 64;                             // K per stage: one 128-byte swizzle row
-constexpr int kBStages = 4;                         // W2t K-stages (one tile of K = 256)
-constexpr int kStages = 2;                          // (U, target) gather stages
+constexpr int kBStages = 5;                         // W2t K-stages (1.25 tiles of K = 256)
+constexpr int kSlots = 4;                           // (U, target) half-tile gather slots
 constexpr int kAccBufs = 2;
 constexpr int kEpiWarps = 8;
-constexpr int kGatherWarps = 2 * kStages;           // two per stage
+constexpr int kGatherWarps = kSlots;                // one per slot
 constexpr int kThreads = 32 * (2 + kEpiWarps + kGatherWarps);
 constexpr uint32_t kBAtom = kBN * kBK * 2;          // 16 KB: W2t rows [128 x 64 K]
 constexpr uint32_t kHalf = kBM * 64 * 2;            // 16 KB: [128 rows x 64 ids] bf16
-constexpr uint32_t kStageBytes = 4 * kHalf;         // U tile (two halves) | target tile (two halves)
+constexpr uint32_t kSlotBytes = 2 * kHalf;          // U half tile | target half tile
 constexpr uint32_t kTmemCols = 512;                 // 2 accumulators x 128 + A (128) -> 512
 constexpr uint32_t kTmemA = kAccBufs * kBN;         // first column of A
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Bars {
   uint64_t b_full[kBStages], b_empty[kBStages];
-  uint64_t s_full[kStages], s_empty[kStages];
+  uint64_t s_full[kSlots], s_empty[kSlots];
   uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
   uint64_t drain;
   uint64_t a_ready;  // A is in TMEM (one arrival per warp of epilogue set 0)
@@ -68,8 +69,8 @@ struct Bars {
 
 // Per-row facts (one request per tile row).
 struct RowMeta {
-  long long u_off;  // element offset of U[b, kdec-1, 0] (residual rows)
-  long long t_off;  // element offset of target[pdec, 0] (live rows)
+  int u_row;        // row b * gamma + kdec - 1 of U viewed as [bs * gamma, V] (residual rows; else 0)
+  int t_row;        // packed target row pdec (live rows; else 0)
   float a_t;        // lse_t * log2(e)
   float a_d;        // lse_d * log2(e)
   int resid;        // residual row (else bonus, or dead)
@@ -97,9 +98,9 @@ struct Params {
   uint64_t timeout_ns;
 };
 
-// Dynamic shared memory: W2t ring | gather stages | row facts | barriers.
+// Dynamic shared memory: W2t ring | gather slots | row facts | barriers.
 constexpr size_t kSmemBytes =
-    kBStages * size_t(kBAtom) + kStages * size_t(kStageBytes) + kBM * sizeof(RowMeta) + sizeof(Bars);
+    kBStages * size_t(kBAtom) + kSlots * size_t(kSlotBytes) + kBM * sizeof(RowMeta) + sizeof(Bars);
 static_assert(kSmemBytes <= 232448, "dynamic shared memory beyond the 227 KB per-block limit");
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
@@ -128,8 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
   }
   const int nk = p.r / kBK;
   uint8_t* sB = smem_raw;                          // W2t ring
-  uint8_t* sS = sB + kBStages * kBAtom;            // gather stages
-  RowMeta* meta = reinterpret_cast<RowMeta*>(sS + kStages * kStageBytes);
+  uint8_t* sS = sB + kBStages * kBAtom;            // gather slots
+  RowMeta* meta = reinterpret_cast<RowMeta*>(sS + kSlots * kSlotBytes);
   Bars* bar = reinterpret_cast<Bars*>(meta + kBM);
   volatile int* abort_flag = &bar->abort;
 
@@ -146,9 +147,9 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
       tc::mbar_init(tc::smem_u32(&bar->b_full[s]), 1);
       tc::mbar_init(tc::smem_u32(&bar->b_empty[s]), 1);
     }
-    for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(tc::smem_u32(&bar->s_full[s]), 2);   // the two gather warps of the stage
-      tc::mbar_init(tc::smem_u32(&bar->s_empty[s]), 4);  // the epilogue set of the stage
+    for (int s = 0; s < kSlots; ++s) {
+      tc::mbar_init(tc::smem_u32(&bar->s_full[s]), 1);   // the slot's gather warp
+      tc::mbar_init(tc::smem_u32(&bar->s_empty[s]), 4);  // the epilogue set of the slot
     }
     for (int s = 0; s < kAccBufs; ++s) {
       tc::mbar_init(tc::smem_u32(&bar->acc_full[s]), 1);
@@ -218,11 +219,11 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
       if (d.kind != kDecNone) {
         rm.live = 1;
         rm.kdec = d.kdec;
-        rm.t_off = (long long)d.pdec * V;
+        rm.t_row = d.pdec;
         rm.a_t = p.rs[d.pdec].lse * kLog2e;
         if (d.kind == kDecResidual) {
           rm.resid = 1;
-          rm.u_off = ((long long)grow * p.gamma + d.kdec - 1) * V;
+          rm.u_row = grow * p.gamma + d.kdec - 1;
           rm.a_d = p.lse_d[(size_t)grow * p.gamma + d.kdec - 1] * kLog2e;
         }
       }
@@ -277,34 +278,33 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
     }
   } else if (warp >= 2 + kEpiWarps) {
     // ------------------------------------------------------------------ row gather
-    // Stage s (tiles t = s, s + 2, ...) is filled by gather warps s and s + 2, rows 64 * (g >> 1)
-    // .. + 63 each: the tile's U rows (residual rows) and target rows (live rows), both halves.
-    // Only CUDA-core loads read the stages, so the warp waits for its own copies and arrives.
-    const int g = warp - (2 + kEpiWarps);
-    const int s = g & 1, rbase = (g >> 1) * 64;
-    const int j = lane & 7, rsub = lane >> 3;  // 16-byte group in a 128-byte half row, row within 4
-    const uint32_t su = tc::smem_u32(sS + s * kStageBytes), st = su + 2 * kHalf;
+    // Warp g fills slot g: half h = g & 1 of the tiles t with t & 1 == g >> 1 -- the U rows of
+    // the residual requests and the target rows of the live ones (zero otherwise), 64 ids from
+    // column (chunk) * 128 + 64 h.  Only CUDA-core loads read the slots, so the warp waits for
+    // its own copies and arrives.
+    const int sl = warp - (2 + kEpiWarps), h = sl & 1;
+    const int j = lane & 7, rsub = lane >> 3;  // 16-byte group in a 128-byte row, row within 4
+    const uint32_t su = tc::smem_u32(sS + sl * kSlotBytes), st = su + kHalf;
     bool ok = true;
-    for (int t = s, i = 0; t < n_tiles; t += 2, ++i) {
-      if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->s_empty[s]), (i & 1) ^ 1, deadline, abort_flag)) {
+    for (int t = sl >> 1, i = 0; t < n_tiles; t += 2, ++i) {
+      if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->s_empty[sl]), (i & 1) ^ 1, deadline, abort_flag)) {
         ok = false;
         break;
       }
-      const int n0 = (c0 + t * cstride) * kBN;
-#pragma unroll 2
-      for (int it = 0; it < 2 * 64 / 4; ++it) {
-        const int h = it & 1, row = rbase + (it >> 1) * 4 + rsub;
-        const int col = n0 + h * 64 + j * 8;
-        const bool in_v = col < V;
+      const int col = (c0 + t * cstride) * kBN + h * 64 + j * 8;
+      const bool in_v = col < V;
+#pragma unroll 4
+      for (int it = 0; it < kBM / 4; ++it) {
+        const int row = it * 4 + rsub;
         const RowMeta rm = meta[row];
-        const uint32_t off = h * kHalf + row * 128 + ((j ^ (row & 7)) << 4);
+        const uint32_t off = row * 128 + ((j ^ (row & 7)) << 4);
         const bool gu = rm.resid && in_v, gt = rm.live && in_v;
-        cp_async16(su + off, gu ? p.U + rm.u_off + col : p.U, gu ? 16u : 0u);
-        cp_async16(st + off, gt ? p.target + rm.t_off + col : p.target, gt ? 16u : 0u);
+        cp_async16(su + off, gu ? p.U + (size_t)rm.u_row * V + col : p.U, gu ? 16u : 0u);
+        cp_async16(st + off, gt ? p.target + (size_t)rm.t_row * V + col : p.target, gt ? 16u : 0u);
       }
       cp_async_wait_all();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->s_full[s]));
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->s_full[sl]));
     }
     if (!ok) {
       *abort_flag = 1;
@@ -343,8 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
       if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->a_ready));
     }
     const uint32_t taddr = lane_base + set * kBN;
-    const uint8_t* ub = sS + set * kStageBytes + m * 128;  // U row in the stage (+ h * kHalf)
-    const uint8_t* tb = ub + 2 * kHalf;                     // target row
+    const uint8_t* ub0 = sS + (2 * set) * kSlotBytes + m * 128;  // U row in slot 2 set + h (+ h slots)
     // the row's partial draw over this set's chunks; the chunk Gumbels of the first kGReg tiles
     // are drawn before the loop
     constexpr int kGReg = 8;
@@ -363,8 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
     for (int t = set, i = 0; t < n_tiles; t += 2, ++i) {
       const int c = c0 + t * cstride;
       const int valid = min(kBN, V - c * kBN);
-      bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[set]), i & 1, deadline, abort_flag) &&
-                tc::mbar_wait_bounded(tc::smem_u32(&bar->s_full[set]), i & 1, deadline, abort_flag);
+      bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[set]), i & 1, deadline, abort_flag);
       // one decision per warp before the .sync.aligned TMEM loads
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) {
@@ -376,6 +374,17 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
       float R4[4] = {0.f, 0.f, 0.f, 0.f}, P4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int h = 0; h < 2; ++h) {  // 64 columns at a time
+        const int sl = 2 * set + h;
+        // one decision per warp before the .sync.aligned TMEM loads
+        if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait_bounded(tc::smem_u32(&bar->s_full[sl]), i & 1, deadline,
+                                                           abort_flag))) {
+          *abort_flag = 1;
+          set_status(p.status, DSPARK_ETIMEOUT);
+          ok = false;
+          break;
+        }
+        const uint8_t* ub = ub0 + h * kSlotBytes;  // U row of this half
+        const uint8_t* tb = ub + kHalf;            // target row of this half
         float l[64];  // W1[x] W2 part of the draft logits (residual rows)
         tc::tmem_ld32(taddr + h * 64, reinterpret_cast<uint32_t*>(l));
         tc::tmem_ld32(taddr + h * 64 + 32, reinterpret_cast<uint32_t*>(l + 32));
@@ -388,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
         if (rm.live) {
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            const uint32_t off = h * kHalf + ((jj ^ (m & 7)) << 4);
+            const uint32_t off = (jj ^ (m & 7)) << 4;
             float xu[8], xt[8];
             unpack8(*reinterpret_cast<const uint4*>(ub + off), xu);
             unpack8(*reinterpret_cast<const uint4*>(tb + off), xt);
@@ -405,9 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
             }
           }
         }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->s_empty[sl]));
       }
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->s_empty[set]));
+      if (!ok) break;
       float g;
       if (i < kGReg) {
         g = gk[0];
