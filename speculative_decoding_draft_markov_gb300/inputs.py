@@ -45,10 +45,17 @@ CHUNK = 128  # vocabulary chunk width of the two-level sampler (part of the samp
 # ---------------------------------------------------------------------------
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float32 values to bf16 (round to nearest, ties to even); returns uint16 bit patterns."""
-    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    rounded = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
-    return rounded.astype(np.uint16)
+    """Round float32 values to bf16 (round to nearest, ties to even); returns uint16 bit patterns.
+
+    bits + 0x7FFF + (bit 16), then the high 16 bits, taken through a little-endian uint16 view
+    (numpy's integer shifts are slow on some builds)."""
+    b = np.ascontiguousarray(x, dtype=np.float32).reshape(-1).view(np.uint32)
+    half = b.view(np.uint16)
+    if half.size and not np.little_endian:
+        raise RuntimeError("big-endian hosts are not supported")
+    lsb = (half[1::2] & np.uint16(1)).astype(np.uint32)
+    rounded = b + np.uint32(0x7FFF) + lsb  # wraps only for negative NaN patterns
+    return np.ascontiguousarray(rounded.view(np.uint16)[1::2]).reshape(np.shape(x))
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:

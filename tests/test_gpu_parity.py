@@ -217,6 +217,9 @@ def _verify_chain(wl, temperature, mode, windows_seed, step=0):
 VERIFY_WL = {
     "tiny_fp32": I.WORKLOADS["tiny_fp32"].with_(bs=12),
     "bf16_ragged": SMALL["bf16_ragged"].with_(bs=16, gamma=5, sigmas=(0.3, 1.0, 3.0)),
+    # two request tiles (the second ragged), the longest block, a ragged last vocabulary chunk
+    "bf16_two_mtiles_g16": SMALL["bf16_two_mtiles"].with_(name="bf16_two_mtiles_g16", bs=200, gamma=16,
+                                                          sigmas=(0.3, 1.0, 3.0)),
 }
 
 
