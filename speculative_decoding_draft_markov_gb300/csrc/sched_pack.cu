@@ -13,39 +13,53 @@ namespace dspark {
 // temperature scaling divides the logit by T_k; prefix survival is the running product.
 // fp32 dot products in a fixed order.
 // ---------------------------------------------------------------------------------------
-__device__ __forceinline__ float dot_chunk8(const __nv_bfloat16* x, const float* w) {
-  const uint4 q = *reinterpret_cast<const uint4*>(x);
-  const float4 w0 = *reinterpret_cast<const float4*>(w);
-  const float4 w1 = *reinterpret_cast<const float4*>(w + 4);
-  float a = bf16lo(q.x) * w0.x;
-  a = fmaf(bf16hi(q.x), w0.y, a);
-  a = fmaf(bf16lo(q.y), w0.z, a);
-  a = fmaf(bf16hi(q.y), w0.w, a);
-  a = fmaf(bf16lo(q.z), w1.x, a);
-  a = fmaf(bf16hi(q.z), w1.y, a);
-  a = fmaf(bf16lo(q.w), w1.z, a);
-  a = fmaf(bf16hi(q.w), w1.w, a);
-  return a;
+// One 8-element group of a feature row: loaded as 16 bytes of bf16 (or two 16-byte halves of
+// fp32), then dotted with w read from memory at the time of use.
+template <typename T>
+__device__ __forceinline__ void load_hgroup(const T* x, uint4* q) {
+  if constexpr (sizeof(T) == 2) {
+    q[0] = *reinterpret_cast<const uint4*>(x);
+  } else {
+    q[0] = *reinterpret_cast<const uint4*>(x);
+    q[1] = *reinterpret_cast<const uint4*>(x + 4);
+  }
 }
-__device__ __forceinline__ float dot_chunk8(const float* x, const float* w) {
-  const float4 x0 = *reinterpret_cast<const float4*>(x), x1 = *reinterpret_cast<const float4*>(x + 4);
-  const float4 w0 = *reinterpret_cast<const float4*>(w), w1 = *reinterpret_cast<const float4*>(w + 4);
-  float a = x0.x * w0.x;
-  a = fmaf(x0.y, w0.y, a);
-  a = fmaf(x0.z, w0.z, a);
-  a = fmaf(x0.w, w0.w, a);
-  a = fmaf(x1.x, w1.x, a);
-  a = fmaf(x1.y, w1.y, a);
-  a = fmaf(x1.z, w1.z, a);
-  a = fmaf(x1.w, w1.w, a);
-  return a;
+template <typename T>
+__device__ __forceinline__ float dot_hgroup(const uint4* q, const float* __restrict__ w) {
+  const float4 w0 = __ldg(reinterpret_cast<const float4*>(w));
+  const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + 4));
+  if constexpr (sizeof(T) == 2) {
+    float a = bf16lo(q[0].x) * w0.x;
+    a = fmaf(bf16hi(q[0].x), w0.y, a);
+    a = fmaf(bf16lo(q[0].y), w0.z, a);
+    a = fmaf(bf16hi(q[0].y), w0.w, a);
+    a = fmaf(bf16lo(q[0].z), w1.x, a);
+    a = fmaf(bf16hi(q[0].z), w1.y, a);
+    a = fmaf(bf16lo(q[0].w), w1.z, a);
+    a = fmaf(bf16hi(q[0].w), w1.w, a);
+    return a;
+  } else {
+    float a = __uint_as_float(q[0].x) * w0.x;
+    a = fmaf(__uint_as_float(q[0].y), w0.y, a);
+    a = fmaf(__uint_as_float(q[0].z), w0.z, a);
+    a = fmaf(__uint_as_float(q[0].w), w0.w, a);
+    a = fmaf(__uint_as_float(q[1].x), w1.x, a);
+    a = fmaf(__uint_as_float(q[1].y), w1.y, a);
+    a = fmaf(__uint_as_float(q[1].z), w1.z, a);
+    a = fmaf(__uint_as_float(q[1].w), w1.w, a);
+    return a;
+  }
 }
 
-// One block per request; `parts` warps per position split the d-long dot product (warp q of a
-// position takes the 256-element groups q, q + parts, ...; four 16-byte loads in flight per
-// lane), then thread 0 adds the parts in order and runs the sigmoid / STS / product chain.
+// One block per request; `parts` warps per position split the d-long dot product: warp q of a
+// position takes the 256-element groups q, q + parts, ...  A lane issues the h loads of up to
+// kHLoads groups at once (one memory round trip for d <= 256 parts kHLoads) and reads w when it
+// uses it (every warp of the block reads the same w).  Thread 0 then adds the parts in order
+// and runs the sigmoid / STS / product chain.
+constexpr int kHLoads = 8;
+
 template <typename T>
-__global__ void __launch_bounds__(1024) confidence_kernel(
+__global__ void __launch_bounds__(512) confidence_kernel(
     const T* __restrict__ h, const T* __restrict__ W1, const int32_t* __restrict__ anchor,
     const int32_t* __restrict__ tokens, const float* __restrict__ w, float b,
     const float* __restrict__ sts_T, int gamma, int d, int r, int V, int parts, float* __restrict__ conf,
@@ -55,19 +69,30 @@ __global__ void __launch_bounds__(1024) confidence_kernel(
   const int pos = warp / parts, part = warp - pos * parts;
   if (pos < gamma) {
     const int k = pos + 1;
+    // the W1[x_{k-1}] part of the feature (r a multiple of 8, <= 256): its row index first
+    int xp = 0;
+    if (part == 0 && lane * 8 < r)
+      xp = clamp_token((k == 1) ? anchor[req] : tokens[size_t(req) * gamma + k - 2], V);
     const T* hr = h + (size_t(req) * gamma + pos) * d;
-    float a4[4] = {0.f, 0.f, 0.f, 0.f};
     const int stride = parts * 256;
-    int e = part * 256 + lane * 8;
-    for (; e + 3 * stride < d; e += 4 * stride) {
+    float acc = 0.f;
+    for (int e0 = part * 256 + lane * 8; e0 < d; e0 += kHLoads * stride) {
+      uint4 q[kHLoads][sizeof(T) == 4 ? 2 : 1];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) a4[u] += dot_chunk8(hr + e + u * stride, w + e + u * stride);
+      for (int u = 0; u < kHLoads; ++u) {
+        const int e = e0 + u * stride;
+        if (e < d) load_hgroup<T>(hr + e, q[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < kHLoads; ++u) {
+        const int e = e0 + u * stride;
+        if (e < d) acc += dot_hgroup<T>(q[u], w + e);
+      }
     }
-    for (; e < d; e += stride) a4[0] += dot_chunk8(hr + e, w + e);
-    float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
-    if (part == 0 && lane * 8 < r) {  // the W1[x_{k-1}] part of the feature (r a multiple of 8, <= 256)
-      const int xp = clamp_token((k == 1) ? anchor[req] : tokens[size_t(req) * gamma + k - 2], V);
-      acc += dot_chunk8(W1 + size_t(xp) * r + lane * 8, w + d + lane * 8);
+    if (part == 0 && lane * 8 < r) {
+      uint4 qa[sizeof(T) == 4 ? 2 : 1];
+      load_hgroup<T>(W1 + size_t(xp) * r + lane * 8, qa);
+      acc += dot_hgroup<T>(qa, w + d + lane * 8);
     }
     acc = warp_sum(acc);
     if (lane == 0) zp[pos * 4 + part] = acc;
@@ -92,7 +117,7 @@ cudaError_t launch_confidence(int dtype, const void* h, const void* W1, const in
                               const int32_t* tokens, const float* w, float b, const float* sts_T,
                               int bs, int gamma, int d, int r, int V, float* conf, float* surv,
                               float* z_out, cudaStream_t s) {
-  const int parts = gamma <= 8 ? 4 : 2;  // warps per position: at most 1024 threads
+  const int parts = gamma <= 8 ? 2 : 1;  // warps per position: at most 512 threads, two blocks per SM
   const int threads = 32 * parts * gamma;
   if (dtype == DSPARK_F32)
     confidence_kernel<float><<<bs, threads, 0, s>>>((const float*)h, (const float*)W1, anchor,
