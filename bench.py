@@ -563,13 +563,28 @@ def run_profile_case(args):
     if args.profile_case == "observe":
         run_observe_case(args, dev)
         return
+    if args.profile_case == "schedule":
+        wl = I.WORKLOADS[WORKLOAD]
     inp = I.make_device_inputs(wl, dev, with_hidden=args.profile_case != "draft",
-                               with_target=args.profile_case != "draft")
+                               with_target=args.profile_case not in ("draft", "schedule"))
     bs, gamma, V = wl.bs, wl.gamma, wl.V
     cap = bs * (gamma + 1)
     buf = S.StepBuffers.allocate(bs, gamma, V, cap, inp["U"].dtype, dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    if args.profile_case == "draft":
+    if args.profile_case == "schedule":
+        # the benchmark's scheduler input: one drafted block's survival, its sawtooth table
+        sps = S.sps_table(inp["T_raw"], inp["tiers"], dev)
+        B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], wl.temperature, wl.seed, 0,
+                             buf.tokens, buf.logit_x, buf.lse, buf.ws)
+        B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], buf.tokens, inp["w"], inp["b"], inp["sts_T"],
+                            buf.conf, buf.surv)
+        ring = S.zos_ring(dev)
+        ring.fill_(200)
+
+        def run(it):
+            B.dspark_schedule(buf.surv, sps, SCHED, buf.window, buf.K, buf.theta)
+            B.dspark_schedule_zos_select(buf.surv, sps, ring, it, buf.window, buf.K)
+    elif args.profile_case == "draft":
         def run(it):
             B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], wl.temperature, wl.seed, it,
                                  buf.tokens, buf.logit_x, buf.lse, buf.ws)
@@ -645,7 +660,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["draft", "verify", "observe"], default=None,
+    ap.add_argument("--profile-case", choices=["draft", "verify", "observe", "schedule"], default=None,
                     help="run one stage of the workload (small gamma) for an ncu capture; no JSON contract")
     ap.add_argument("--gamma", type=int, default=2, help="block length of --profile-case")
     args = ap.parse_args()

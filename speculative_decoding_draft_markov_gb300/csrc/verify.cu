@@ -57,15 +57,19 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
     int bs, int gamma, int V, float inv_tau, int greedy, RowStat* __restrict__ rs, uint32_t* status) {
   __shared__ float sv[kRowThreads / 32], ss[kRowThreads / 32];
   __shared__ int si[kRowThreads / 32];
+  __shared__ int s_cu[DSPARK_MAX_BS + 1];
   const int p = blockIdx.x, tid = threadIdx.x;
-  const int M = cu[bs];
+  // cu_seqlens in one coalesced read, then the row's request by binary search in shared memory
+  for (int i = tid; i <= bs; i += kRowThreads) s_cu[i] = cu[i];
+  __syncthreads();
+  const int M = s_cu[bs];
   if (p >= M) return;
   int lo = 0, hi = bs;  // cu[lo] <= p < cu[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (cu[mid] <= p) lo = mid; else hi = mid;
+    if (s_cu[mid] <= p) lo = mid; else hi = mid;
   }
-  const int r = lo, j = p - cu[r], n_r = cu[r + 1] - cu[r];
+  const int r = lo, j = p - s_cu[r], n_r = s_cu[r + 1] - s_cu[r];
   const T* row = target + size_t(p) * V;
   constexpr int G = sizeof(T) == 2 ? 8 : 4;
   const int ng = V / G;

@@ -105,19 +105,28 @@ def _sched_cases():
                                           (256, 7, 2, True, "mixed"), (256, 16, 3, False, "wide"),
                                           (1, 1, 4, False, "one"), (33, 5, 5, True, "steep"),
                                           (128, 15, 6, False, "long"), (64, 7, 7, False, "short"),
-                                          (200, 3, 8, False, "unsorted")]:
+                                          (200, 3, 8, False, "unsorted"),
+                                          # above 1024 slots the search first sorts the top 1024 only:
+                                          # cases where that settles it and cases where it must fall back
+                                          (205, 5, 9, True, "tiers16"), (256, 5, 10, False, "flat"),
+                                          (256, 8, 11, False, "const"), (129, 8, 12, False, "mixed"),
+                                          (256, 4, 13, False, "unsorted")]:
         a = I.random_survival(bs, gamma, seed, ties=ties)
         if kind == "unsorted":  # rows not non-increasing: the per-request runs need sorting
             a = np.random.default_rng(seed).random((bs, gamma)).astype(np.float32)
+        if kind == "const":     # every key equal: the slot order decides
+            a = np.full((bs, gamma), 0.5, dtype=np.float32)
         if kind == "tiny":
             sps = O.build_sps(1.0 + 0.002 * np.arange(65), [])
         elif kind == "steep":
             sps = O.build_sps(1.0 + 0.5 * np.arange(bs * (gamma + 1) + 1), [])
         elif kind == "short":   # table shorter than bs + bs*gamma: K is capped by m_max
             sps = O.build_sps(5.0 + 0.01 * np.arange(200), list(range(16, 200, 16)) + [199])
+        elif kind == "flat":    # constant step time: the global search admits every slot
+            sps = O.build_sps(np.full(bs * (gamma + 1) + 1, 5.0), [])
         else:
             m = bs * (gamma + 1)
-            step = 64 if kind == "mixed" else 16
+            step = 64 if kind in ("mixed", "const") else 16
             sps = O.build_sps(5.0 + 0.01 * np.arange(m + 1), list(range(step, m, step)) + [m])
         cases.append((a, sps))
     return cases
