@@ -174,17 +174,30 @@ __global__ void __launch_bounds__(128) verify_decide_kernel(
     dec[r] = Decision{0, 0, kDecNone, 0};
     return;
   }
+  // every tested position's facts are read before the first test (one round trip, not one per
+  // position), then the tests run in order up to the first rejection
+  const int c0 = cu[r];
+  RowStat st[DSPARK_MAX_GAMMA];
+  int xk[DSPARK_MAX_GAMMA];
+  float lpd[DSPARK_MAX_GAMMA];
+#pragma unroll
+  for (int k = 0; k < DSPARK_MAX_GAMMA; ++k) {
+    if (k < L_test) {
+      st[k] = rs[c0 + k];
+      xk[k] = tokens[size_t(r) * gamma + k];
+      lpd[k] = greedy ? 0.f : logit_x[size_t(r) * gamma + k] - lse[size_t(r) * gamma + k];
+    }
+  }
   int first = 0;
-  for (int k = 1; k <= L_test; ++k) {
-    const RowStat s = rs[cu[r] + k - 1];
-    const int x = tokens[size_t(r) * gamma + k - 1];
+#pragma unroll
+  for (int k = 1; k <= DSPARK_MAX_GAMMA; ++k) {
+    if (k > L_test) break;
     bool ok;
     if (greedy) {
-      ok = (s.argmax == x);
+      ok = (st[k - 1].argmax == xk[k - 1]);
     } else {
-      const float lp_t = s.tx - s.lse;
-      const float lp_d = logit_x[size_t(r) * gamma + k - 1] - lse[size_t(r) * gamma + k - 1];
-      const float ratio = expf(lp_t - lp_d);
+      const float lp_t = st[k - 1].tx - st[k - 1].lse;
+      const float ratio = expf(lp_t - lpd[k - 1]);
       const float u = bits_to_uniform(philox_group(seed, step, kAccept, r, k, 0).x);
       ok = u < ratio;
     }
