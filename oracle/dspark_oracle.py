@@ -30,8 +30,8 @@ Sources, cited by page and section:
   [PHILOX]   Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
              SC'11 -- the Philox4x32 round function, multipliers and Weyl key schedule.
 
-Where the pages are silent the reading taken is stated at the function; the design doc
-lists every reading.  Every function here is pinned by tests under tests/
+Where the pages are silent the reading taken is stated at the function.  Every
+function here is pinned by tests under tests/
 (test_oracle_*.py) against closed forms, brute force, distributional tests and an
 independent library Philox.
 """

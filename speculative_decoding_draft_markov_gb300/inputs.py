@@ -7,8 +7,8 @@ conversion to bf16, the cost curve T(M) of each workload (an input table),
 and the row gather that stands in for the target model's forward pass over
 the packed verify batch.
 
-Workloads (shapes and laws as the benchmark configurations state them; the
-readings where they are silent are listed in the design doc):
+Workloads (shapes of the models and batches the pages evaluate on; the value laws
+are seeded synthetic stand-ins for their data):
 
   tiny_fp32    bs=4,   gamma=7,  V=1024,   r=32,  d=64,   fp32
   qwen3_4b     bs=64,  gamma=7,  V=151936, r=256, d=2560, bf16

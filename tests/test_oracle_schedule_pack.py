@@ -215,7 +215,7 @@ def test_pack_layout_and_static():
     cu_s, ids_s, _, _, padded_s = O.pack(None, anchor, tokens, [], cap=64)
     np.testing.assert_array_equal(cu_s, np.arange(bs + 1) * (gamma + 1))
     # the static layout of the bs=256, gamma=7 workload fills the largest capture exactly
-    c = json.load(open(os.path.join(GOLDEN, "survey_constants.json")))["max_capture"]
+    c = json.load(open(os.path.join(GOLDEN, "page_constants.json")))["max_capture"]
     wl = I.WORKLOADS["mixed_bs256"]
     assert (wl.gamma + 1) * wl.bs == c["value"] == I.tiers_for(wl)[-1]
 
