@@ -29,6 +29,7 @@
 #include <cudaTypedefs.h>
 
 #include <climits>
+#include <type_traits>
 #include <mutex>
 
 #include "common.cuh"
@@ -342,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->a_ready));
     }
+    const float neg_at = -rm.a_t, neg_ad = rm.resid ? -rm.a_d : -INFINITY;
     const uint32_t taddr = lane_base + set * kBN;
     const uint8_t* ub0 = sS + (2 * set) * kSlotBytes + m * 128;  // U row in slot 2 set + h (+ h slots)
     // the row's partial draw over this set's chunks; the chunk Gumbels of the first kGReg tiles
@@ -395,24 +397,29 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
           if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[set]));
         }
         if (rm.live) {
+          // w = max(0, p_t - p_d); a bonus row's p_d offset is -inf, so p_d = 0 and w = p_t.
+          // Full chunks take no per-element bound check.
+          auto half_sums = [&](auto full) {
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const uint32_t off = (jj ^ (m & 7)) << 4;
-            float xu[8], xt[8];
-            unpack8(*reinterpret_cast<const uint4*>(ub + off), xu);
-            unpack8(*reinterpret_cast<const uint4*>(tb + off), xt);
+            for (int jj = 0; jj < 8; ++jj) {
+              const uint32_t off = (jj ^ (m & 7)) << 4;
+              float xu[8], xt[8];
+              unpack8(*reinterpret_cast<const uint4*>(ub + off), xu);
+              unpack8(*reinterpret_cast<const uint4*>(tb + off), xt);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int q = h * 64 + 8 * jj + e;
-              const float pt = tc::ex2_approx(fmaf(xt[e], c2, -rm.a_t));
-              const float pd = tc::ex2_approx(fmaf(l[8 * jj + e] + xu[e], c2, -rm.a_d));
-              const float w = rm.resid ? fmaxf(0.f, pt - pd) : pt;
-              if (valid == kBN || q < valid) {
-                R4[e & 3] += w;
-                P4[e & 3] += pt;
+              for (int e = 0; e < 8; ++e) {
+                const float pt = tc::ex2_approx(fmaf(xt[e], c2, neg_at));
+                const float pd = tc::ex2_approx(fmaf(l[8 * jj + e] + xu[e], c2, neg_ad));
+                const float w = fmaxf(0.f, pt - pd);
+                if (decltype(full)::value || h * 64 + 8 * jj + e < valid) {
+                  R4[e & 3] += w;
+                  P4[e & 3] += pt;
+                }
               }
             }
-          }
+          };
+          if (valid == kBN) half_sums(std::true_type{});
+          else half_sums(std::false_type{});
         }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->s_empty[sl]));
