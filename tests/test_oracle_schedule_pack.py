@@ -237,3 +237,28 @@ def test_scheduler_does_not_admit_a_slot_with_zero_gain():
         win, K, th, theta = O.schedule(a, sps, mode)
         assert theta[0] == theta[1] == 1.5
         assert K == 0 and win[0] == 0
+
+
+def test_pruning_is_a_large_batch_effect():
+    """[SGLANG, "A preliminary look at dynamic vs static scheduling", Fig. 3]: at batch 1 the
+    verify step barely slows with more tokens, so pruning saves little; as concurrency rises the
+    dynamic budget prunes, and (two workloads of different acceptance) more so where acceptance
+    is low.  With the sweep's cost curve (5 ms + 0.01 ms per token, graph tiers every 16) the
+    global search admits every slot at bs 1, and its admitted fraction falls with the batch and
+    with the acceptance level."""
+    fracs = {"high": [], "low": []}
+    for bs in I.DSV4_BATCHES:
+        wl = I.dsv4(bs)
+        sps = O.build_sps(I.cost_curve_ms(wl), I.tiers_for(wl))
+        for name, cmean in (("high", 0.9), ("low", 0.6)):
+            rng = np.random.default_rng(bs)
+            c = np.clip(rng.normal(cmean, 0.05, (bs, wl.gamma)), 0.01, 0.999).astype(np.float32)
+            a = np.cumprod(c, axis=1).astype(np.float32)
+            _, K, _, _ = O.schedule(a, sps, O.GLOBAL_ARGMAX)
+            fracs[name].append(K / (bs * wl.gamma))
+    for name in fracs:
+        assert fracs[name][0] == 1.0                                   # bs 1: nothing pruned
+        assert all(x >= y for x, y in zip(fracs[name], fracs[name][1:]))  # more pruning with load
+    assert fracs["high"][-1] > 0.75 and fracs["low"][-1] < 0.35        # bs 256
+    assert all(lo <= hi for lo, hi in zip(fracs["low"], fracs["high"]))
+    assert fracs["low"][-1] < fracs["high"][-1] - 0.4
