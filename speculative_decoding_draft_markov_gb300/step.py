@@ -10,12 +10,30 @@ cu_seqlens / padded total, all on the device) and fills the packed target-logit 
 Buffers are allocated once by PyTorch; the library itself allocates nothing."""
 from __future__ import annotations
 
+import contextlib
 import dataclasses
+import os
 from typing import Callable, Optional
 
 import numpy as np
 
 from . import binding as B
+
+# NVTX ranges around the stages (for a timeline profiler) when DSPARK_NVTX=1; off by default
+_NVTX = os.environ.get("DSPARK_NVTX", "0") == "1"
+
+
+@contextlib.contextmanager
+def stage(name: str):
+    if not _NVTX:
+        yield
+        return
+    import torch
+    torch.cuda.nvtx.range_push(name)
+    try:
+        yield
+    finally:
+        torch.cuda.nvtx.range_pop()
 
 
 @dataclasses.dataclass
@@ -144,11 +162,15 @@ def run_step(inp: dict, buf: StepBuffers, sps, target_forward: Callable[[StepBuf
              temperature: float, seed: int, step: int, mode: int = B.DSPARK_COMPACT,
              sched_mode: int = B.DSPARK_SCHED_EARLY_STOP, tiers=None, stream=None, ring=None,
              side_stream=None) -> None:
-    draft_and_schedule(inp, buf, sps, temperature, seed, step, sched_mode, mode, tiers, stream, ring)
+    with stage("dspark.draft_confidence_schedule_pack"):
+        draft_and_schedule(inp, buf, sps, temperature, seed, step, sched_mode, mode, tiers, stream, ring)
     if ring is not None:
-        schedule_budget(buf, sps, ring, step, stream, side_stream)
-    target_forward(buf)
-    verify(inp, buf, temperature, seed, step, mode, stream)
+        with stage("dspark.schedule_budget"):
+            schedule_budget(buf, sps, ring, step, stream, side_stream)
+    with stage("dspark.target_forward"):
+        target_forward(buf)
+    with stage("dspark.verify"):
+        verify(inp, buf, temperature, seed, step, mode, stream)
     if ring is not None:
         join_budget(stream, side_stream)
 

@@ -206,3 +206,12 @@ def test_obs_report_matches_oracle(L):
     np.testing.assert_allclose(got["pos_pass_rate"][:gamma], ref["pos_pass_rate"], rtol=1e-12)
     assert all(np.isnan(got["pos_pass_rate"][gamma:]))
     assert got["scored"] == int(np.sum(tot["bin_count"]))
+
+
+def test_stage_ranges_are_inert_by_default():
+    """The NVTX stage ranges of step.py cost nothing unless DSPARK_NVTX=1."""
+    from speculative_decoding_draft_markov_gb300 import step as S
+    ran = []
+    with S.stage("x"):
+        ran.append(1)
+    assert ran == [1] and S._NVTX is False
