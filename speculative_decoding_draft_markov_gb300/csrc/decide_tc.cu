@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
 
   // ---------------------------------------------------------------- everyone else: row facts
   tc::grid_dependency_wait();  // the decisions come from the previous kernel
+  tc::grid_launch_dependents();  // the decision select may be scheduled (it waits for this grid)
   constexpr int kRest = kThreads - 32;
   for (int m = tid - 32; m < kBM; m += kRest) {
     RowMeta rm{0, 0, 0.f, 0.f, 0, 0, 0, 0};

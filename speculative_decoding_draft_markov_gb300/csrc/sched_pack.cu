@@ -4,6 +4,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "pdl.h"
 
 namespace dspark {
 
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(512) confidence_kernel(
     const float* __restrict__ sts_T, int gamma, int d, int r, int V, int parts, float* __restrict__ conf,
     float* __restrict__ surv, float* __restrict__ z_out) {
   __shared__ float zp[DSPARK_MAX_GAMMA * 4];
+  pdl_enter();
   const int req = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pos = warp / parts, part = warp - pos * parts;
   if (pos < gamma) {
@@ -120,13 +122,10 @@ cudaError_t launch_confidence(int dtype, const void* h, const void* W1, const in
   const int parts = gamma <= 8 ? 2 : 1;  // warps per position: at most 512 threads, two blocks per SM
   const int threads = 32 * parts * gamma;
   if (dtype == DSPARK_F32)
-    confidence_kernel<float><<<bs, threads, 0, s>>>((const float*)h, (const float*)W1, anchor,
-                                                    tokens, w, b, sts_T, gamma, d, r, V, parts, conf, surv, z_out);
-  else
-    confidence_kernel<__nv_bfloat16><<<bs, threads, 0, s>>>(
-        (const __nv_bfloat16*)h, (const __nv_bfloat16*)W1, anchor, tokens, w, b, sts_T, gamma, d,
-        r, V, parts, conf, surv, z_out);
-  return cudaGetLastError();
+    return launch_pdl(confidence_kernel<float>, dim3(bs), dim3(threads), 0, s, (const float*)h, (const float*)W1,
+                      anchor, tokens, w, b, sts_T, gamma, d, r, V, parts, conf, surv, z_out);
+  return launch_pdl(confidence_kernel<__nv_bfloat16>, dim3(bs), dim3(threads), 0, s, (const __nv_bfloat16*)h,
+                    (const __nv_bfloat16*)W1, anchor, tokens, w, b, sts_T, gamma, d, r, V, parts, conf, surv, z_out);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -394,6 +393,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
     int mode, int32_t* __restrict__ window, int32_t* __restrict__ K_out,
     double* __restrict__ theta_out) {
   __shared__ SchedShared sh;
+  pdl_enter();
   const int ks = sched_search(surv, bs, gamma, sps, m_max, mode, sh, theta_out);
   if (threadIdx.x == 0) *K_out = ks;
   if (window) sched_windows(sh, ks, bs, gamma, window);
@@ -402,8 +402,8 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
 cudaError_t launch_schedule(const float* surv, int bs, int gamma, const double* sps, int m_max,
                             int mode, int32_t* window, int32_t* K_out, double* theta_out,
                             cudaStream_t s) {
-  schedule_kernel<<<1, kSchedThreads, 0, s>>>(surv, bs, gamma, sps, m_max, mode, window, K_out, theta_out);
-  return cudaGetLastError();
+  return launch_pdl(schedule_kernel, dim3(1), dim3(kSchedThreads), 0, s, surv, bs, gamma, sps, m_max, mode, window,
+                    K_out, theta_out);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -453,6 +453,7 @@ __global__ void __launch_bounds__(kSchedThreads) zos_select_kernel(
     int32_t* __restrict__ K_out) {
   __shared__ SchedShared sh;
   __shared__ int s_K, s_bin, s_before;
+  pdl_enter();
   const int tid = threadIdx.x, lane = tid & 31;
   const int n = bs * gamma;
   const int kmax = min(n, m_max - bs);
@@ -545,15 +546,15 @@ __global__ void __launch_bounds__(kSchedThreads) zos_select_kernel(
 cudaError_t launch_zos_select(const float* surv, int bs, int gamma, const double* sps, int m_max,
                               const int32_t* ring, uint64_t step, int32_t* window, int32_t* K_out,
                               cudaStream_t s) {
-  zos_select_kernel<<<1, kSchedThreads, 0, s>>>(surv, bs, gamma, sps, m_max, ring, step, window, K_out);
-  return cudaGetLastError();
+  return launch_pdl(zos_select_kernel, dim3(1), dim3(kSchedThreads), 0, s, surv, bs, gamma, sps, m_max, ring, step,
+                    window, K_out);
 }
 
 cudaError_t launch_zos_budget(const float* surv, int bs, int gamma, const double* sps, int m_max,
                               int32_t* ring, uint64_t step, cudaStream_t s) {
-  schedule_kernel<<<1, kSchedThreads, 0, s>>>(surv, bs, gamma, sps, m_max, DSPARK_SCHED_GLOBAL_ARGMAX,
-                                              nullptr, ring + (step & 1), nullptr);
-  return cudaGetLastError();
+  return launch_pdl(schedule_kernel, dim3(1), dim3(kSchedThreads), 0, s, surv, bs, gamma, sps, m_max,
+                    int(DSPARK_SCHED_GLOBAL_ARGMAX), static_cast<int32_t*>(nullptr), ring + (step & 1),
+                    static_cast<double*>(nullptr));
 }
 
 // ---------------------------------------------------------------------------------------
@@ -569,6 +570,7 @@ __global__ void __launch_bounds__(DSPARK_MAX_BS) pack_kernel(
     uint32_t* status) {
   __shared__ int wsum[DSPARK_MAX_BS / 32];
   __shared__ int s_padded, s_M, s_bad;
+  pdl_enter();
   const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
   if (r == 0) s_bad = 0;
   __syncthreads();
@@ -638,9 +640,8 @@ cudaError_t launch_pack(const int32_t* window, const int32_t* anchor, const int3
                         int bs, int gamma, const int32_t* tiers, int n_tiers, int cap,
                         int32_t* cu, int32_t* ids, int32_t* req, int32_t* pos, int32_t* padded,
                         uint32_t* status, cudaStream_t s) {
-  pack_kernel<<<1, DSPARK_MAX_BS, 0, s>>>(window, anchor, tokens, bs, gamma, tiers, n_tiers, cap,
-                                          cu, ids, req, pos, padded, status);
-  return cudaGetLastError();
+  return launch_pdl(pack_kernel, dim3(1), dim3(DSPARK_MAX_BS), 0, s, window, anchor, tokens, bs, gamma, tiers,
+                    n_tiers, cap, cu, ids, req, pos, padded, status);
 }
 
 }  // namespace dspark

@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "pdl.h"
 
 namespace dspark {
 
@@ -58,6 +59,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
   __shared__ float sv[kRowThreads / 32], ss[kRowThreads / 32];
   __shared__ int si[kRowThreads / 32];
   __shared__ int s_cu[DSPARK_MAX_BS + 1];
+  pdl_enter();
   const int p = blockIdx.x, tid = threadIdx.x;
   // cu_seqlens in one coalesced read, then the row's request by binary search in shared memory
   for (int i = tid; i <= bs; i += kRowThreads) s_cu[i] = cu[i];
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(128) verify_decide_kernel(
     const float* __restrict__ lse, const RowStat* __restrict__ rs, int greedy, uint64_t seed,
     uint64_t step, int32_t* __restrict__ out_tokens, int32_t* __restrict__ acc_len,
     int32_t* __restrict__ ceiling, Decision* __restrict__ dec, uint32_t* status) {
+  pdl_enter();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= bs) return;
   int32_t* out = out_tokens + size_t(r) * (gamma + 1);
@@ -359,6 +362,7 @@ __global__ void __launch_bounds__(256) decision_select_kernel(
   __shared__ float rv[8];
   __shared__ int ri[8];
   __shared__ int s_use_res, s_win;
+  pdl_enter();
   const int b = blockIdx.x, tid = threadIdx.x;
   const Decision d = dec[b];
   if (d.kind == kDecNone) return;
@@ -443,11 +447,13 @@ static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_
   DecideEntry* entries = reinterpret_cast<DecideEntry*>(w + L.stats);
   RowStat* rs = reinterpret_cast<RowStat*>(w + L.rowstats);
   Decision* dec = reinterpret_cast<Decision*>(w + L.dec);
-  verify_rows_kernel<T><<<bs * (gamma + 1), kRowThreads, 0, s>>>(target, cu, tokens, bs, gamma, V,
-                                                                  inv_tau, greedy, rs, status);
-  verify_decide_kernel<<<(bs + 127) / 128, 128, 0, s>>>(cu, window, mode, bs, gamma, tokens,
-                                                         logit_x, lse, rs, greedy, seed, step,
-                                                         out_tokens, acc_len, ceiling, dec, status);
+  cudaError_t le = launch_pdl(verify_rows_kernel<T>, dim3(bs * (gamma + 1)), dim3(kRowThreads), 0, s, target, cu,
+                              tokens, bs, gamma, V, inv_tau, greedy, rs, status);
+  if (le != cudaSuccess) return le;
+  le = launch_pdl(verify_decide_kernel, dim3((bs + 127) / 128), dim3(128), 0, s, cu, window, mode, bs, gamma, tokens,
+                  logit_x, lse, static_cast<const RowStat*>(rs), greedy, seed, step, out_tokens, acc_len, ceiling, dec,
+                  status);
+  if (le != cudaSuccess) return le;
   if (!greedy) {
     constexpr int RB = 32;
     constexpr bool kBf16 = sizeof(T) == 2;
@@ -464,9 +470,11 @@ static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_
           target, U, W1, W2t, anchor, tokens, lse, rs, dec, bs, gamma, V, r, inv_tau, seed, step, entries,
           L.n_chunks);
     }
-    decision_select_kernel<T><<<bs, 256, 0, s>>>(target, U, W1, W2t, anchor, tokens, lse, rs, dec,
-                                                 draft_logits, entries, n_slots, bs, gamma, V, r, inv_tau,
-                                                 seed, step, out_tokens);
+    le = launch_pdl(decision_select_kernel<T>, dim3(bs), dim3(256), 0, s, target, U, W1, W2t, anchor, tokens, lse,
+                    static_cast<const RowStat*>(rs), static_cast<const Decision*>(dec), draft_logits,
+                    static_cast<const DecideEntry*>(entries), n_slots, bs, gamma, V, r, inv_tau, seed, step,
+                    out_tokens);
+    if (le != cudaSuccess) return le;
   }
   return cudaGetLastError();
 }
