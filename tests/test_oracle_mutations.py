@@ -1,0 +1,52 @@
+"""Planted mistakes: each one, put into a copy of the oracle, must make one of its pins fail.
+
+Opt-in (DSPARK_MUTATION=1; each case runs a pytest subprocess on a copy of oracle/, tests/ and
+the package, a few minutes in all).  A mistake that no pin catches would mean the oracle could
+be wrong in that way unnoticed; every case here is caught.  The mutations are planted in the
+oracle only, on the CPU."""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# name -> (text in oracle/dspark_oracle.py, its replacement, the pins that must catch it)
+MUTS = {
+ "ratio_inverted": ("ratio = math.exp(lp_t - lp_d)", "ratio = math.exp(lp_d - lp_t)", "tests/test_oracle_verify.py::test_monte_carlo_acceptance_equals_one_minus_tv"),
+ "residual_flipped": ("res = np.maximum(0.0, p_t - p_d)", "res = np.maximum(0.0, p_d - p_t)", "tests/test_oracle_verify.py::test_first_committed_token_is_target_distributed"),
+ "bias_wrong_token": ("x_prev = tokens[:, k - 1].astype(np.int64)", "x_prev = x_prev", "tests/test_oracle_sampling.py::test_draft_joint_distribution_of_first_two_tokens"),
+ "conf_x_index": ("np.asarray(tokens, dtype=np.int64)[:, :gamma - 1]], axis=1)", "np.asarray(tokens, dtype=np.int64)[:, 1:gamma]], axis=1)", "tests/test_oracle_schedule_pack.py::test_confidence_feature_indexing"),
+ "philox_round": ("c = [hi1 ^ c[1] ^ np.uint64(ka), lo1, hi0 ^ c[3] ^ np.uint64(kb), lo0]", "c = [hi0 ^ c[1] ^ np.uint64(ka), lo1, hi1 ^ c[3] ^ np.uint64(kb), lo0]", "tests/test_oracle_philox.py::test_philox_matches_triton_library_implementation"),
+ "sched_nonstrict": ("if not theta[K + 1] > theta[K]:", "if theta[K + 1] < theta[K]:", "tests/test_oracle_schedule_pack.py"),
+ "chunk_mass_max": ("safe_m + np.log(np.exp(blocks - safe_m[:, None]).sum(axis=1))", "safe_m", "tests/test_oracle_sampling.py::test_two_level_sampler_chunk_marginal_is_chunk_mass"),
+ "zos_wrong_slot": ("    slot = step % 2\n", "    slot = (step + 1) % 2\n", "tests/test_oracle_zos.py"),
+ "zos_budget_early_stop": ("return int(schedule(surv_f32, sps, GLOBAL_ARGMAX)[1])", "return int(schedule(surv_f32, sps, EARLY_STOP)[1])", "tests/test_oracle_zos.py"),
+ "zos_tie_order": ("slots = sorted(((float(a[r, j]), r, j) for r in range(bs) for j in range(gamma)),\n                   key=lambda s: (-s[0], s[1], s[2]))", "slots = sorted(((float(a[r, j]), r, j) for r in range(bs) for j in range(gamma)),\n                   key=lambda s: (-s[0], -s[1], s[2]))", "tests/test_oracle_zos.py"),
+ "zos_no_clamp": ("    K = min(K, bs * gamma, m_max - bs)\n", "    K = min(K, bs * gamma)\n", "tests/test_oracle_zos.py"),
+ "ece_per_bin_norm": ("    e = float(np.sum(np.abs(lab - sc)) / N) if N else 0.0", "    e = float(np.sum(np.abs(lab - sc)) / max(int(cnt.max()), 1)) if N else 0.0", "tests/test_oracle_observe.py"),
+ "ece_round_bins": ("    b = np.floor(a * np.float32(n_bins)).astype(np.int64)", "    b = np.round(a * np.float32(n_bins)).astype(np.int64)", "tests/test_oracle_observe.py"),
+ "labels_strict": ("        return (c >= k).astype(np.int64), np.ones((bs, gamma), dtype=bool)", "        return (c > k).astype(np.int64), np.ones((bs, gamma), dtype=bool)", "tests/test_oracle_observe.py"),
+ "labels_known_window_only": ("    known = (k <= w[:, None]) | (acc[:, None] < w[:, None])", "    known = (k <= w[:, None])", "tests/test_oracle_observe.py"),
+ "util_inverted": ('st["sum_accepted_ceiling"] / st["sum_ceiling"] if st["sum_ceiling"]', 'st["sum_ceiling"] / st["sum_accepted_ceiling"] if st["sum_ceiling"]', "tests/test_oracle_observe.py"),
+ "sts_label_offby1": ("        y = (c >= k + 1).astype(np.int64)", "        y = (c >= k).astype(np.int64)", "tests/test_oracle_observe.py"),
+ "sts_no_carry": ("        prev = prev / (1.0 + np.exp(-z[:, k] / T[k]))", "        prev = prev", "tests/test_oracle_observe.py"),
+ "sts_argmax": ("        g_star = int(np.argmin(table[k]))  # first minimum", "        g_star = int(np.argmax(table[k]))", "tests/test_oracle_observe.py"),
+}
+
+
+@pytest.mark.skipif(os.environ.get("DSPARK_MUTATION") != "1", reason="opt-in: DSPARK_MUTATION=1")
+@pytest.mark.parametrize("name", list(MUTS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    a, b, pins = MUTS[name]
+    src = open(os.path.join(ROOT, "oracle", "dspark_oracle.py")).read()
+    assert a in src, "the mutated text is no longer in the oracle"
+    for d in ("oracle", "tests", "speculative_decoding_draft_markov_gb300"):
+        shutil.copytree(os.path.join(ROOT, d), tmp_path / d, ignore=shutil.ignore_patterns("lib", "*.so", "__pycache__"))
+    (tmp_path / "oracle" / "dspark_oracle.py").write_text(src.replace(a, b))
+    env = dict(os.environ, DSPARK_MUTATION="0")
+    p = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", "-m", "not gpu", pins],
+                       capture_output=True, text=True, cwd=tmp_path, env=env, timeout=900)
+    assert p.returncode != 0, f"planted mistake {name!r} passed every pin in {pins}"
