@@ -108,6 +108,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 // The chunk Gumbel of a decision (Philox purpose 4, index c).  Out of line: inlined into the
 // tile loop its rounds raise register pressure there.
@@ -304,6 +305,19 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
         cp_async16(su + off, gu ? p.U + (size_t)rm.u_row * V + col : p.U, gu ? 16u : 0u);
         cp_async16(st + off, gt ? p.target + (size_t)rm.t_row * V + col : p.target, gt ? 16u : 0u);
       }
+      // the rows of this slot's next fill (tile t + 2) into L2 while this one completes: one
+      // prefetch per 128-byte row segment, lane = row within a group of 32
+      if (t + 2 < n_tiles) {
+        const int ncol = (c0 + (t + 2) * cstride) * kBN + h * 64;
+        if (ncol < V) {
+#pragma unroll
+          for (int q = 0; q < kBM / 32; ++q) {
+            const RowMeta rm = meta[q * 32 + lane];
+            if (rm.resid) prefetch_l2(p.U + (size_t)rm.u_row * V + ncol);
+            if (rm.live) prefetch_l2(p.target + (size_t)rm.t_row * V + ncol);
+          }
+        }
+      }
       cp_async_wait_all();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->s_full[sl]));
@@ -375,8 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
       }
       tc::tc_fence_after();
       float R4[4] = {0.f, 0.f, 0.f, 0.f}, P4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {  // 64 columns at a time
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {  // 64 columns at a time (one copy of the code for both)
         const int sl = 2 * set + h;
         // one decision per warp before the .sync.aligned TMEM loads
         if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait_bounded(tc::smem_u32(&bar->s_full[sl]), i & 1, deadline,
