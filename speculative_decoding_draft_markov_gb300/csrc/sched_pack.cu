@@ -71,10 +71,14 @@ __global__ void __launch_bounds__(512) confidence_kernel(
   const int pos = warp / parts, part = warp - pos * parts;
   if (pos < gamma) {
     const int k = pos + 1;
-    // the W1[x_{k-1}] part of the feature (r a multiple of 8, <= 256): its row index first
-    int xp = 0;
-    if (part == 0 && lane * 8 < r)
-      xp = clamp_token((k == 1) ? anchor[req] : tokens[size_t(req) * gamma + k - 2], V);
+    // the W1[x_{k-1}] part of the feature (r a multiple of 8, <= 256): its row is read first,
+    // so that its two round trips (token id, then row) overlap the h loads below
+    const bool has_w1 = part == 0 && lane * 8 < r;
+    uint4 qa[sizeof(T) == 4 ? 2 : 1];
+    if (has_w1) {
+      const int xp = clamp_token((k == 1) ? anchor[req] : tokens[size_t(req) * gamma + k - 2], V);
+      load_hgroup<T>(W1 + size_t(xp) * r + lane * 8, qa);
+    }
     const T* hr = h + (size_t(req) * gamma + pos) * d;
     const int stride = parts * 256;
     float acc = 0.f;
@@ -91,11 +95,7 @@ __global__ void __launch_bounds__(512) confidence_kernel(
         if (e < d) acc += dot_hgroup<T>(q[u], w + e);
       }
     }
-    if (part == 0 && lane * 8 < r) {
-      uint4 qa[sizeof(T) == 4 ? 2 : 1];
-      load_hgroup<T>(W1 + size_t(xp) * r + lane * 8, qa);
-      acc += dot_hgroup<T>(qa, w + d + lane * 8);
-    }
+    if (has_w1) acc += dot_hgroup<T>(qa, w + d + lane * 8);
     acc = warp_sum(acc);
     if (lane == 0) zp[pos * 4 + part] = acc;
   }
