@@ -42,7 +42,8 @@ from typing import Optional
 
 import numpy as np
 
-CHUNK = 128
+CHUNK = 128        # ids per chunk of verify's draws (residual and bonus)
+DRAFT_CHUNK = 64   # ids per chunk of the draft's draws
 
 # Philox purposes (counter word 3, bits 24..31)
 P_DRAFT_CHUNK = 1
@@ -214,7 +215,7 @@ def markov_logits(U_k: np.ndarray, W1: np.ndarray, W2t: np.ndarray, x_prev: np.n
 
 
 def draft_block(U, W1, W2t, anchor, temperature: float, seed: int, step: int,
-                dtype: str = "bf16", chunk: int = CHUNK, req_ids=None):
+                dtype: str = "bf16", chunk: int = DRAFT_CHUNK, req_ids=None):
     """S1: draw x_1..x_gamma left to right from p_k(v) = softmax(U_k(v) + B_k(v)).
 
     [SUMMARY, "Architecture (drafter)"]: the parallel backbone yields U_1..U_gamma in one pass
@@ -222,7 +223,8 @@ def draft_block(U, W1, W2t, anchor, temperature: float, seed: int, step: int,
     the causal per-position distributions left to right; per-token probabilities stay exact
     softmax values, which rejection sampling needs.
     Readings: x_0 = anchor feeds B_1; the sampling temperature divides the logits; at
-    temperature 0 the draw is the argmax (lowest index on ties).
+    temperature 0 the draw is the argmax (lowest index on ties); the two-level draw uses
+    chunks of DRAFT_CHUNK = 64 ids (the law is exactly softmax for any chunk width).
 
     Returns tokens [bs, gamma] int32, logit_x [bs, gamma] (tempered logit of the drawn
     token; raw logit at temperature 0), lse [bs, gamma] (log-sum-exp of the tempered
