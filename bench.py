@@ -206,11 +206,12 @@ def draft_block_bytes(bs: int, gamma: int, V: int, r: int, n_sm: int) -> int:
     operands are consumed as they stream; W2t is re-read by every position because the positions
     are serially dependent), the gathered A rows W1[x] [bs, r], and the partial-draw entries
     written (16 bytes per request and CTA column).  Select: the entries read back, the W1 row,
-    the 128 W2t rows and U_k values of the drawn chunk, and the three outputs."""
+    the 64 W2t rows and U_k values of the drawn draft chunk, and the three outputs."""
     n_mt = (bs + 127) // 128
     n_slots = (n_sm // n_mt)
     vocab = bs * V * 2 + V * r * 2 + bs * r * 2 + bs * n_slots * 16
-    select = bs * (n_slots * 16 + r * 2 + 128 * r * 2 + 128 * 2 + 12)
+    chunk = 64  # ids per draft chunk
+    select = bs * (n_slots * 16 + r * 2 + chunk * r * 2 + chunk * 2 + 12)
     return gamma * (vocab + select)
 
 
@@ -229,6 +230,7 @@ def _profiled_traffic():
     h = hashlib.sha256()
     for f in ("draft_tc.cu", "draft.cu", "common.cuh", "tc_ptx.cuh", "tc_host.h"):
         h.update(open(os.path.join(ROOT, "speculative_decoding_draft_markov_gb300", "csrc", f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "dspark.h"), "rb").read())
     if fields.get("sources_sha256") != h.hexdigest() or "dram_bytes_per_draft_block_gamma7" not in fields:
         return None
     return int(fields["dram_bytes_per_draft_block_gamma7"])

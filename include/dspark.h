@@ -33,8 +33,10 @@
  *     key, 2 draft entry key, 3 accept uniform, 4 decision chunk key, 5 decision entry key.
  *     A uniform is ((word >> 9) + 0.5) * 2^-23.  A step is reproducible from (seed, step).
  *   - Sampling: a categorical draw over the vocabulary uses the two-level Gumbel-max rule:
- *     chunks of DSPARK_CHUNK consecutive ids get key log(mass) + Gumbel; the best chunk is
- *     drawn, then an id inside it by Gumbel-max over its log-weights.  Ties: lowest index.
+ *     chunks of consecutive ids get key log(mass) + Gumbel; the best chunk is drawn, then an
+ *     id inside it by Gumbel-max over its log-weights.  Ties: lowest index.  The draft's draws
+ *     use chunks of DSPARK_DRAFT_CHUNK ids, the verification's of DSPARK_CHUNK ids (the law
+ *     is exactly the softmax for any chunk width; the width fixes which random words are used).
  */
 #ifndef DSPARK_H
 #define DSPARK_H
@@ -72,7 +74,8 @@ typedef enum { DSPARK_SCHED_EARLY_STOP = 0, DSPARK_SCHED_GLOBAL_ARGMAX = 1 } dsp
 
 #define DSPARK_MAX_BS 256     /* requests per step                                   */
 #define DSPARK_MAX_GAMMA 16   /* draft block length                                  */
-#define DSPARK_CHUNK 128      /* vocabulary chunk width of the two-level sampler     */
+#define DSPARK_CHUNK 128      /* chunk width of the verification's two-level draws   */
+#define DSPARK_DRAFT_CHUNK 64 /* chunk width of the draft's two-level draws          */
 
 /* Human-readable name of a status code (static string, never NULL). */
 DSPARK_API const char* dspark_status_string(int status);

@@ -18,7 +18,7 @@ DSPARK_OK, DSPARK_EINVAL, DSPARK_EUNSUPPORTED, DSPARK_ECUDA, DSPARK_ETIMEOUT, DS
 DSPARK_F32, DSPARK_BF16 = 0, 1
 DSPARK_STATIC, DSPARK_COMPACT, DSPARK_CAP_ACCEPT = 0, 1, 2
 DSPARK_SCHED_EARLY_STOP, DSPARK_SCHED_GLOBAL_ARGMAX = 0, 1
-DSPARK_MAX_BS, DSPARK_MAX_GAMMA, DSPARK_CHUNK = 256, 16, 128
+DSPARK_MAX_BS, DSPARK_MAX_GAMMA, DSPARK_CHUNK, DSPARK_DRAFT_CHUNK = 256, 16, 128, 64
 
 _vp, _i, _f, _u64, _sz, _d = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t, ctypes.c_double
 

@@ -121,14 +121,14 @@ int dspark_draft_block(const void* U, const void* W1, const void* W2t, int dtype
   const float inv_tau = greedy ? 1.f : static_cast<float>(1.0 / static_cast<double>(temperature));
   const bool tc = draft_tc_supported(dtype, bs, V, r);
   for (int k = 1; k <= gamma; ++k) {
-    int n_slots = L.n_chunks;
+    int n_slots = n_draft_chunks(V);  // the CUDA-core pass: one slot per draft chunk
     cudaError_t e = tc ? launch_draft_stats_tc(U, W1, W2t, anchor, tokens, bs, gamma, V, r, k, inv_tau,
                                                greedy, seed, step, stats, L.n_chunks, &n_slots, status, s)
                        : launch_draft_stats_simt(dtype, U, W1, W2t, anchor, tokens, bs, gamma, V, r, k,
-                                                 inv_tau, greedy, seed, step, stats, L.n_chunks, s);
+                                                 inv_tau, greedy, seed, step, stats, n_slots, s);
     if (e != cudaSuccess) return DSPARK_ECUDA;
     e = launch_draft_select(dtype, stats, n_slots, U, W1, W2t, anchor, tokens, logit_x, lse, bs,
-                            gamma, V, r, k, inv_tau, greedy, seed, step, s);
+                            gamma, V, r, k, inv_tau, greedy, seed, step, status, s);
     if (e != cudaSuccess) return DSPARK_ECUDA;
   }
   return DSPARK_OK;

@@ -10,14 +10,17 @@
 
 namespace dspark {
 
-constexpr int kChunk = DSPARK_CHUNK;
+constexpr int kChunk = DSPARK_CHUNK;          // ids per chunk of verify's draws
+constexpr int kDraftIds = DSPARK_DRAFT_CHUNK;  // ids per chunk of the draft's draws
+static_assert(kChunk == 2 * kDraftIds, "a verify-width vocabulary tile holds two draft chunks");
 
 // The draft's partial draw over a set of chunks ("slot") of one request, as a float4:
 //   x, y : running (max t, sum exp(t - max)) of the tempered logits t = l / T over the slot's
 //          chunks (-inf, 0 when empty; unused at temperature 0)
-//   z    : best key -- temperature > 0: max over the slot's chunks of the chunk's log-mass
-//          plus its Gumbel (Philox purpose 1, index c); temperature 0: the max logit
-//   w    : int bits of the argmax of z -- the chunk index (T > 0) or the token id (T = 0);
+//   z    : best key -- temperature > 0: max over the slot's draft chunks (kDraftIds ids each)
+//          of the chunk's log-mass plus its Gumbel (Philox purpose 1, index c); temperature 0:
+//          the max logit
+//   w    : int bits of the argmax of z -- the draft chunk index (T > 0) or the token id (T = 0);
 //          INT_MAX when empty.  Ties go to the lowest index.
 // The select merges a request's entries: LSE from (x, y), winner = argmax (z, lowest w).
 // Slots never share a chunk, so the merged winner is the two-level draw's chunk.
@@ -68,9 +71,11 @@ struct DecideEntry {
   int cR, cP, pad0, pad1;
 };
 
-// The draft's scratch alone (16-byte entries, at most one per chunk).
-__host__ __device__ inline size_t draft_stats_bytes(int bs, int n_chunks) {
-  return size_t(bs) * n_chunks * sizeof(float4);
+// The draft's scratch alone (16-byte entries, at most one per draft chunk).  The stats region
+// of the workspace (32 bytes per verify chunk) holds it: n_draft_chunks <= 2 n_chunks.
+__host__ __device__ inline int n_draft_chunks(int V) { return (V + kDraftIds - 1) / kDraftIds; }
+__host__ __device__ inline size_t draft_stats_bytes(int bs, int n_slots) {
+  return size_t(bs) * n_slots * sizeof(float4);
 }
 __host__ __device__ inline size_t stats_bytes(int bs, int n_chunks) {
   return size_t(bs) * n_chunks * sizeof(DecideEntry);
@@ -156,12 +161,13 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ----------------------------------------------------------------------------------------
-// Dot products W2t[v] . a for the 128 ids v0 .. v0+127 of one sampler chunk, by a 256-thread
-// block: warp w takes ids v0 + 16w .. v0 + 16w + 15, lane l the K slice [8l, 8l + 8).  All 16
-// rows' loads are issued before any arithmetic; fixed summation order.  out[i] (shared memory)
-// receives the dot of id v0 + i, 0 for ids >= V.  Requires r % 8 == 0 and r <= 256.
+// Dot products W2t[v] . a for the 8 NW ids v0 .. v0 + 8 NW - 1 of one sampler chunk (NW = 16:
+// a verify chunk of 128 ids; NW = 8: a draft chunk of 64), by a 256-thread block: warp w takes
+// ids v0 + NW w .. + NW - 1, lane l the K slice [8l, 8l + 8).  All NW rows' loads are issued
+// before any arithmetic; fixed summation order.  out[i] (shared memory) receives the dot of id
+// v0 + i, 0 for ids >= V.  Requires r % 8 == 0 and r <= 256.
 // ----------------------------------------------------------------------------------------
-template <typename T>
+template <typename T, int NW = 16>
 __device__ __forceinline__ void chunk_dots(const T* __restrict__ W2t, int r, int V, int v0,
                                            const float* __restrict__ a, float* out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -169,17 +175,17 @@ __device__ __forceinline__ void chunk_dots(const T* __restrict__ W2t, int r, int
   float av[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) av[e] = on ? a[lane * 8 + e] : 0.f;
-  float part[16];
+  float part[NW];
   if constexpr (sizeof(T) == 2) {
-    uint4 q[16];
+    uint4 q[NW];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int v = v0 + warp * 16 + j;
+    for (int j = 0; j < NW; ++j) {
+      const int v = v0 + warp * NW + j;
       q[j] = (on && v < V) ? *reinterpret_cast<const uint4*>(W2t + size_t(v) * r + lane * 8)
                            : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < NW; ++j) {
       float acc = bf16lo(q[j].x) * av[0];
       acc = fmaf(bf16hi(q[j].x), av[1], acc);
       acc = fmaf(bf16lo(q[j].y), av[2], acc);
@@ -192,8 +198,8 @@ __device__ __forceinline__ void chunk_dots(const T* __restrict__ W2t, int r, int
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int v = v0 + warp * 16 + j;
+    for (int j = 0; j < NW; ++j) {
+      const int v = v0 + warp * NW + j;
       float acc = 0.f;
       if (on && v < V) {
         const float4 x0 = *reinterpret_cast<const float4*>(W2t + size_t(v) * r + lane * 8);
@@ -211,11 +217,11 @@ __device__ __forceinline__ void chunk_dots(const T* __restrict__ W2t, int r, int
     }
   }
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int j = 0; j < NW; ++j) {
     float t = part[j];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
-    if (lane == j) out[warp * 16 + j] = t;
+    if (lane == j) out[warp * NW + j] = t;
   }
 }
 

@@ -13,22 +13,52 @@
 namespace dspark {
 
 // ---------------------------------------------------------------------------------------
-// CUDA-core statistics pass.  Block = 128 threads = one 128-id chunk = one slot; RB rows per
-// block.  Serves fp32 inputs (exact fp32 FMA) and small problems; bf16 at scale uses the
-// tensor-core pass in draft_tc.cu.
+// CUDA-core statistics pass.  Block = 128 threads = one 128-id vocabulary tile = two draft
+// chunks (threads 0..63 and 64..127), each its own slot; RB rows per block.  Serves fp32
+// inputs (exact fp32 FMA) and small problems; bf16 at scale uses the tensor-core pass in
+// draft_tc.cu.
 // ---------------------------------------------------------------------------------------
+
+// Reductions over each 64-thread half of a 128-thread block (warps 2q, 2q + 1); every thread
+// of half q returns its half's result.  Fixed order: warp tree, then warp 2q before 2q + 1.
+__device__ __forceinline__ float half_max(float v, float* scratch) {
+  v = warp_max(v);
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) scratch[w] = v;
+  __syncthreads();
+  return fmaxf(scratch[w & ~1], scratch[w | 1]);
+}
+__device__ __forceinline__ float half_sum(float v, float* scratch) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) scratch[w] = v;
+  __syncthreads();
+  return scratch[w & ~1] + scratch[w | 1];
+}
+__device__ __forceinline__ ArgMax half_argmax(ArgMax a, float* sv, int* si) {
+  a = warp_argmax(a);
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) { sv[w] = a.v; si[w] = a.i; }
+  __syncthreads();
+  return better(ArgMax{sv[w & ~1], si[w & ~1]}, ArgMax{sv[w | 1], si[w | 1]});
+}
+
 template <typename T, int RB>
 __global__ void __launch_bounds__(128) draft_stats_simt_kernel(
     const T* __restrict__ U, const T* __restrict__ W1, const T* __restrict__ W2t,
     const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens, int bs, int gamma,
     int V, int r, int k, float inv_tau, int greedy, uint64_t seed, uint64_t step,
-    float4* __restrict__ entries, int n_chunks) {
+    float4* __restrict__ entries, int n_slots) {
   __shared__ float sA[RB][64];
   __shared__ float sW[kChunk][65];
   __shared__ float red[4];
   __shared__ int redi[4];
   const int c = blockIdx.x, rb = blockIdx.y * RB, tid = threadIdx.x;
   const int v = c * kChunk + tid;
+  const int cc = 2 * c + (tid >> 6);  // this thread's draft chunk
   float acc[RB];
 #pragma unroll
   for (int rr = 0; rr < RB; ++rr) acc[rr] = 0.f;
@@ -58,24 +88,25 @@ __global__ void __launch_bounds__(128) draft_stats_simt_kernel(
   }
 
   const bool valid = v < V;
+  const bool writer = (tid & 63) == 0 && cc < n_slots;
 #pragma unroll
   for (int rr = 0; rr < RB; ++rr) {
     const int row = rb + rr;
     if (row >= bs) break;  // uniform over the block
     const float l = valid ? acc[rr] + ld_f32(U, (size_t(row) * gamma + (k - 1)) * V + v) : 0.f;
-    float4* out = entries + size_t(row) * n_chunks + c;
+    float4* out = entries + size_t(row) * n_slots + cc;
     if (greedy) {
-      const ArgMax am = block_argmax<kChunk>(ArgMax{valid ? l : -INFINITY, valid ? v : INT_MAX}, red, redi);
-      if (tid == 0) *out = make_float4(-INFINITY, 0.f, am.v, __int_as_float(am.i));
+      const ArgMax am = half_argmax(ArgMax{valid ? l : -INFINITY, valid ? v : INT_MAX}, red, redi);
+      if (writer) *out = make_float4(-INFINITY, 0.f, am.v, __int_as_float(am.i));
     } else {
       const float t = valid ? l * inv_tau : -INFINITY;
-      const float m = block_max<kChunk>(t, red);
-      const float s = block_sum<kChunk>(valid ? expf(t - m) : 0.f, red);
-      if (tid == 0) {
+      const float m = half_max(t, red);
+      const float s = half_sum(valid ? expf(t - m) : 0.f, red);
+      if (writer) {
         float4 e = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(INT_MAX));
-        if (m > -INFINITY) {  // chunk key: log-mass + Gumbel (purpose 1, index c)
-          const uint4 w = philox_group(seed, step, kDraftChunk, uint32_t(row), k, uint32_t(c) >> 2);
-          e = make_float4(m, s, m + logf(s) + gumbel_from_bits(pick_word(w, c & 3)), __int_as_float(c));
+        if (m > -INFINITY) {  // chunk key: log-mass + Gumbel (purpose 1, index cc)
+          const uint4 w = philox_group(seed, step, kDraftChunk, uint32_t(row), k, uint32_t(cc) >> 2);
+          e = make_float4(m, s, m + logf(s) + gumbel_from_bits(pick_word(w, cc & 3)), __int_as_float(cc));
         }
         *out = e;
       }
@@ -86,19 +117,20 @@ __global__ void __launch_bounds__(128) draft_stats_simt_kernel(
 // ---------------------------------------------------------------------------------------
 // Select pass: one 256-thread block per row.  Warp 0 merges the row's entries: the row LSE
 // from the (max, sum-exp) pairs, and the winner = argmax of the keys (lowest index on ties).
-//   temperature > 0: the winner is the chunk c* of the first Gumbel level; its 128 logits are
-//   recomputed (fixed-order fp32 dot products) and the entry key t_v + G'_v (purpose 2,
-//   index v - 128 c*) picks x_k.
+//   temperature > 0: the winner is the draft chunk c* of the first Gumbel level; its 64 logits
+//   are recomputed (fixed-order fp32 dot products) and the entry key t_v + G'_v (purpose 2,
+//   index v - 64 c*) picks x_k.
 //   temperature = 0: the winner is x_k itself (lowest-index argmax).
 // ---------------------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(256) draft_select_kernel(
+__global__ void __launch_bounds__(256, 1) draft_select_kernel(
     const float4* __restrict__ entries, int n_slots, const T* __restrict__ U,
     const T* __restrict__ W1, const T* __restrict__ W2t, const int32_t* __restrict__ anchor,
     int32_t* __restrict__ tokens, float* __restrict__ logit_x, float* __restrict__ lse, int bs,
-    int gamma, int V, int r, int k, float inv_tau, int greedy, uint64_t seed, uint64_t step) {
+    int gamma, int V, int r, int k, float inv_tau, int greedy, uint64_t seed, uint64_t step,
+    uint32_t* status) {
   __shared__ float sA[256];
-  __shared__ float tv[kChunk];
+  __shared__ float tv[kDraftIds];
   __shared__ float rv[8];
   __shared__ int ri[8];
   __shared__ float s_lse, s_best;
@@ -141,17 +173,23 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
     }
     return;
   }
-  const int cstar = (s_win == INT_MAX) ? 0 : s_win;  // only non-finite statistics leave it unset
+  // only non-finite statistics leave the winner unset; a winner outside the vocabulary means the
+  // entries were not written by this position's statistics pass (it gave up): report, use 0
+  int cstar = (s_win == INT_MAX) ? 0 : s_win;
+  if (cstar < 0 || cstar >= n_draft_chunks(V)) {
+    if (tid == 0) set_status(status, DSPARK_EINVAL);
+    cstar = 0;
+  }
   // the U values of the chosen chunk load together with its W2t rows
   float u_v = 0.f;
-  const int v_own = cstar * kChunk + tid;
-  if (tid < kChunk && v_own < V) u_v = ld_f32(U, (size_t(b) * gamma + (k - 1)) * V + v_own);
-  chunk_dots<T>(W2t, r, V, cstar * kChunk, sA, tv);
+  const int v_own = cstar * kDraftIds + tid;
+  if (tid < kDraftIds && v_own < V) u_v = ld_f32(U, (size_t(b) * gamma + (k - 1)) * V + v_own);
+  chunk_dots<T, kDraftIds / 8>(W2t, r, V, cstar * kDraftIds, sA, tv);
   __syncthreads();
-  if (tid < kChunk) tv[tid] = (v_own < V) ? (tv[tid] + u_v) * inv_tau : -INFINITY;
+  if (tid < kDraftIds) tv[tid] = (v_own < V) ? (tv[tid] + u_v) * inv_tau : -INFINITY;
   __syncthreads();
   ArgMax e{-INFINITY, INT_MAX};
-  if (tid < kChunk) {
+  if (tid < kDraftIds) {
     const uint4 w = philox_group(seed, step, kDraftElem, b, k, tid >> 2);
     const float t = tv[tid];
     if (t > -INFINITY) e = ArgMax{t + gumbel_from_bits(pick_word(w, tid & 3)), tid};
@@ -159,7 +197,7 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
   e = block_argmax<256>(e, rv, ri);
   if (tid == 0) {
     const int ei = (e.i == INT_MAX) ? 0 : e.i;
-    tokens[out] = min(cstar * kChunk + ei, V - 1);
+    tokens[out] = min(cstar * kDraftIds + ei, V - 1);
     logit_x[out] = tv[ei];
     lse[out] = s_lse;
   }
@@ -168,17 +206,17 @@ __global__ void __launch_bounds__(256) draft_select_kernel(
 cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, const void* W2t,
                                     const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
                                     int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
-                                    uint64_t step, void* entries, int n_chunks, cudaStream_t s) {
+                                    uint64_t step, void* entries, int n_slots, cudaStream_t s) {
   constexpr int RB = 32;
-  dim3 grid(n_chunks, (bs + RB - 1) / RB);
+  dim3 grid((V + kChunk - 1) / kChunk, (bs + RB - 1) / RB);
   if (dtype == DSPARK_F32)
     draft_stats_simt_kernel<float, RB><<<grid, kChunk, 0, s>>>(
         (const float*)U, (const float*)W1, (const float*)W2t, anchor, tokens, bs, gamma, V, r, k,
-        inv_tau, greedy, seed, step, (float4*)entries, n_chunks);
+        inv_tau, greedy, seed, step, (float4*)entries, n_slots);
   else
     draft_stats_simt_kernel<__nv_bfloat16, RB><<<grid, kChunk, 0, s>>>(
         (const __nv_bfloat16*)U, (const __nv_bfloat16*)W1, (const __nv_bfloat16*)W2t, anchor,
-        tokens, bs, gamma, V, r, k, inv_tau, greedy, seed, step, (float4*)entries, n_chunks);
+        tokens, bs, gamma, V, r, k, inv_tau, greedy, seed, step, (float4*)entries, n_slots);
   return cudaGetLastError();
 }
 
@@ -186,11 +224,11 @@ cudaError_t launch_draft_select(int dtype, const void* entries, int n_slots, con
                                 const void* W1, const void* W2t, const int32_t* anchor,
                                 int32_t* tokens, float* logit_x, float* lse, int bs, int gamma,
                                 int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
-                                uint64_t step, cudaStream_t s) {
+                                uint64_t step, uint32_t* status, cudaStream_t s) {
   if (dtype == DSPARK_F32)
     draft_select_kernel<float><<<bs, 256, 0, s>>>(
         (const float4*)entries, n_slots, (const float*)U, (const float*)W1, (const float*)W2t,
-        anchor, tokens, logit_x, lse, bs, gamma, V, r, k, inv_tau, greedy, seed, step);
+        anchor, tokens, logit_x, lse, bs, gamma, V, r, k, inv_tau, greedy, seed, step, status);
   else {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(bs);
@@ -203,7 +241,8 @@ cudaError_t launch_draft_select(int dtype, const void* entries, int n_slots, con
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, draft_select_kernel<__nv_bfloat16>, (const float4*)entries, n_slots,
                               (const __nv_bfloat16*)U, (const __nv_bfloat16*)W1, (const __nv_bfloat16*)W2t,
-                              anchor, tokens, logit_x, lse, bs, gamma, V, r, k, inv_tau, greedy, seed, step);
+                              anchor, tokens, logit_x, lse, bs, gamma, V, r, k, inv_tau, greedy, seed, step,
+                              status);
   }
   return cudaGetLastError();
 }

@@ -72,9 +72,9 @@ extern "C" DSPARK_API int dspark_draft_block_noalloc(
       !aligned(tokens, 4) || !aligned(logit_x, 4) || !aligned(lse, 4) || !aligned(device_status, 4))
     return DSPARK_EINVAL;
 
-  // the scratch this call needs: status word + 16 bytes per (request, 128-id chunk)
+  // the scratch this call needs: status word + 16 bytes per (request, draft chunk)
   const WsLayout L = ws_layout(bs, gamma, V);
-  const size_t need = L.stats + draft_stats_bytes(bs, L.n_chunks);
+  const size_t need = L.stats + draft_stats_bytes(bs, n_draft_chunks(V));
   if (need > kNoAllocScratchBytes) return DSPARK_EUNSUPPORTED;
 
   void* scratch = nullptr;
@@ -90,14 +90,14 @@ extern "C" DSPARK_API int dspark_draft_block_noalloc(
   const float inv_tau = greedy ? 1.f : static_cast<float>(1.0 / static_cast<double>(temperature));
   const bool tc = draft_tc_supported(dtype, bs, V, r);
   for (int k = 1; k <= gamma; ++k) {
-    int n_slots = L.n_chunks;
+    int n_slots = n_draft_chunks(V);  // the CUDA-core pass: one slot per draft chunk
     cudaError_t e = tc ? launch_draft_stats_tc(U, W1, W2t, anchor, tokens, bs, gamma, V, r, k, inv_tau, greedy,
                                                seed, step, stats, L.n_chunks, &n_slots, status, s)
                        : launch_draft_stats_simt(dtype, U, W1, W2t, anchor, tokens, bs, gamma, V, r, k, inv_tau,
-                                                 greedy, seed, step, stats, L.n_chunks, s);
+                                                 greedy, seed, step, stats, n_slots, s);
     if (e != cudaSuccess) return DSPARK_ECUDA;
     e = launch_draft_select(dtype, stats, n_slots, U, W1, W2t, anchor, tokens, logit_x, lse, bs, gamma, V, r,
-                            k, inv_tau, greedy, seed, step, s);
+                            k, inv_tau, greedy, seed, step, status, s);
     if (e != cudaSuccess) return DSPARK_ECUDA;
   }
   return DSPARK_OK;

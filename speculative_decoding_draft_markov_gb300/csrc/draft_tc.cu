@@ -8,7 +8,7 @@
 // partial draws (DraftEntry, common.cuh).
 //
 // Work decomposition:
-//   tile      = 128 requests (TMEM lanes) x 128 vocabulary ids (= one sampler chunk), K = r
+//   tile      = 128 requests (TMEM lanes) x 128 vocabulary ids (= two 64-id draft chunks), K = r
 //   CTA       = persistent, one per SM; fixed 128-request M-tile, strided over vocabulary
 //               chunks; the gathered A operand W1[x_{k-1}] (128 x r) stays in shared memory
 //   warp 0    = TMA producer: W2t tiles in K-stages of 64 (evict-last) and the U_k tile
@@ -18,8 +18,9 @@
 //               row per thread).  Set h takes the tiles t = h, h + 2, ... (accumulator buffer
 //               h, U stage h): it adds U_k to the accumulator row (adding U_k on the tensor
 //               core through an identity operand costs more tensor-pipe time than these adds
-//               cost issue slots), forms each chunk's log-mass and Gumbel key and keeps, in
-//               registers, the row's running (max, sum-exp) and best key.  Each CTA writes one
+//               cost issue slots), forms the log-mass and Gumbel key of each of the tile's two
+//               draft chunks and keeps, in registers, the row's running (max, sum-exp) and
+//               best key.  Each CTA writes one
 //               entry per request at the end, so the select merges one entry per CTA column.
 //   2 TMEM accumulators (256 columns) let MMA, loads and epilogue overlap.
 // Every mbarrier wait is bounded (SM cycle-counter deadline + shared abort flag); on give-up the
@@ -42,6 +43,7 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
+static_assert(kBN == 2 * kDraftIds, "the epilogue splits a tile into two draft chunks");
 constexpr int kBK = 64;
 constexpr int kBStages = 6;                      // W2t ring: 1.5 tiles of K = 256
 constexpr int kUStages = 2;
@@ -94,30 +96,35 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// The chunk Gumbel G_c of request `req` at position k (Philox purpose 1, index c).  Kept out of
-// line: inlined into the tile loop its Philox rounds raise register pressure there enough to
-// spill, although the loop only calls it for tiles past the ones drawn up front.
-__device__ __noinline__ float chunk_gumbel_call(uint64_t seed, uint64_t step, int req, int k, int c) {
-  const uint4 w = philox_group(seed, step, kDraftChunk, uint32_t(req), k, uint32_t(c) >> 2);
-  return gumbel_from_bits(pick_word(w, c & 3));
+// The Gumbels G_{2c}, G_{2c+1} of the two draft chunks of vocabulary tile c, request `req`,
+// position k (Philox purpose 1): both sit in counter group c / 2, words 2 (c & 1) and + 1.
+__device__ __forceinline__ float2 tile_gumbels(uint64_t seed, uint64_t step, int req, int k, int c) {
+  const uint4 w = philox_group(seed, step, kDraftChunk, uint32_t(req), k, uint32_t(c) >> 1);
+  return (c & 1) ? make_float2(gumbel_from_bits(w.z), gumbel_from_bits(w.w))
+                 : make_float2(gumbel_from_bits(w.x), gumbel_from_bits(w.y));
+}
+// Kept out of line for the tile loop: inlined there its Philox rounds raise register pressure
+// enough to spill, although the loop only calls it for tiles past the ones drawn up front.
+__device__ __noinline__ float2 tile_gumbels_call(uint64_t seed, uint64_t step, int req, int k, int c) {
+  return tile_gumbels(seed, step, req, k, c);
 }
 
-// Max of the first `valid` of 128 values (all of them when !kRagged), four independent chains.
+// Max of the first `valid` of kDraftIds values (all of them when !kRagged), four chains.
 template <bool kRagged>
 __device__ __forceinline__ float row_max(const float* v, int valid) {
   float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-  for (int i = 0; i < kBN; ++i)
+  for (int i = 0; i < kDraftIds; ++i)
     if (!kRagged || i < valid) m4[i & 3] = fmaxf(m4[i & 3], v[i]);
   return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
-// sum over the first `valid` values of 2^(v c2 - mc2), mc2 = max * c2 (each term <= 1), with the
-// hardware base-2 exponential (relative error near 2^-22) and eight independent chains.
+// sum over the first `valid` of kDraftIds values of 2^(v c2 - mc2), mc2 = max * c2 (each term
+// <= 1), with the hardware base-2 exponential (relative error near 2^-22), eight chains.
 template <bool kRagged>
 __device__ __forceinline__ float row_sum_exp2(const float* v, int valid, float mc2, float c2) {
   float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int i = 0; i < kBN; ++i) {
+  for (int i = 0; i < kDraftIds; ++i) {
     const float e = tc::ex2_approx(fmaf(v[i], c2, -mc2));
     if (!kRagged || i < valid) s8[i & 7] += e;
   }
@@ -281,17 +288,13 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     // The chunk Gumbels (Philox purpose 1) of this row and of the set's first kGReg tiles do not
     // depend on any logit: draw them before waiting for the previous kernel, so that the Philox
     // rounds overlap its tail instead of the tile loop.  Later tiles draw theirs in the loop.
-    constexpr int kGReg = 8;
-    float gk[kGReg];
+    constexpr int kGReg = 6;
+    float2 gk[kGReg];
 #pragma unroll
     for (int i = 0; i < kGReg; ++i) {
       const int t = half + 2 * i;
-      gk[i] = 0.f;
-      if (!p.greedy && t < n_tiles) {
-        const int c = c0 + t * cstride;
-        const uint4 w = philox_group(p.seed, p.step, kDraftChunk, uint32_t(grow), p.k, uint32_t(c) >> 2);
-        gk[i] = gumbel_from_bits(pick_word(w, c & 3));
-      }
+      gk[i] = make_float2(0.f, 0.f);
+      if (!p.greedy && t < n_tiles) gk[i] = tile_gumbels(p.seed, p.step, grow, p.k, c0 + t * cstride);
     }
     // x_{k-1} comes from the previous kernel (the select of position k-1): everything above
     // -- barrier set-up, TMEM, the producer's U / W2 prefetch, the Gumbels -- overlapped with it
@@ -368,27 +371,34 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
         // chunks arrive in increasing order: a strict > keeps the lowest index on ties
         if (best > best_key) { best_key = best; best_c = n0 + bi; }
       } else {
-        // only the last chunk of a vocabulary that is not a multiple of 128 is ragged
-        const float mx = valid == kBN ? row_max<false>(v, valid) : row_max<true>(v, valid);
-        const float sc = valid == kBN ? row_sum_exp2<false>(v, valid, mx * c2, c2)
-                                      : row_sum_exp2<true>(v, valid, mx * c2, c2);
-        float g;
+        float2 g;
         if (i < kGReg) {
           g = gk[0];
 #pragma unroll
           for (int j = 0; j + 1 < kGReg; ++j) gk[j] = gk[j + 1];
         } else {
-          g = chunk_gumbel_call(p.seed, p.step, grow, p.k, c);
+          g = tile_gumbels_call(p.seed, p.step, grow, p.k, c);
         }
-        if (mx > -INFINITY) {
-          const float key = mx * inv_tau + logf(sc) + g;  // chunk log-mass + Gumbel
-          if (key > best_key) { best_key = key; best_c = c; }
-          const float m2 = mx * c2;
-          if (m2 > run_m) {
-            run_s = run_s * exp2f(run_m - m2) + sc;
-            run_m = m2;
-          } else {
-            run_s += sc * exp2f(m2 - run_m);
+        // the tile's draft chunks 2c (ids 0..63) and 2c + 1 (ids 64..127), in that order; only
+        // the last tile of a vocabulary that is not a multiple of 128 is ragged
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float* vq = v + q * kDraftIds;
+          const int vl = valid - q * kDraftIds;
+          const bool full = vl >= kDraftIds;
+          const float mx = full ? row_max<false>(vq, vl) : row_max<true>(vq, vl);
+          if (mx > -INFINITY) {
+            const float sc = full ? row_sum_exp2<false>(vq, vl, mx * c2, c2)
+                                  : row_sum_exp2<true>(vq, vl, mx * c2, c2);
+            const float key = mx * inv_tau + logf(sc) + (q ? g.y : g.x);  // log-mass + Gumbel
+            if (key > best_key) { best_key = key; best_c = 2 * c + q; }
+            const float m2 = mx * c2;
+            if (m2 > run_m) {
+              run_s = run_s * exp2f(run_m - m2) + sc;
+              run_m = m2;
+            } else {
+              run_s += sc * exp2f(m2 - run_m);
+            }
           }
         }
       }

@@ -8,14 +8,14 @@ namespace dspark {
 
 // ---- S1 draft ---------------------------------------------------------------------------
 // Partial draws of l_k = U_k + W1[x_{k-1}] W2 for one position k: per (row, slot) a
-// DraftEntry (common.cuh) over the slot's chunks.  The CUDA-core pass has one slot per chunk
-// (n_slots = n_chunks).
+// DraftEntry (common.cuh) over the slot's draft chunks.  The CUDA-core pass has one slot per
+// draft chunk (n_slots = n_draft_chunks(V)).
 cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, const void* W2t,
                                     const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
                                     int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
-                                    uint64_t step, void* entries, int n_chunks, cudaStream_t s);
+                                    uint64_t step, void* entries, int n_slots, cudaStream_t s);
 // Same on the tensor cores (tcgen05 + TMEM + TMA), bf16 only: one slot per CTA column
-// (n_slots <= n_chunks, returned).
+// (n_slots <= n_chunks 128-id tiles, returned).
 cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t,
                                   const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
                                   int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
@@ -36,7 +36,7 @@ cudaError_t launch_draft_select(int dtype, const void* entries, int n_slots, con
                                 const void* W1, const void* W2t, const int32_t* anchor,
                                 int32_t* tokens, float* logit_x, float* lse, int bs, int gamma,
                                 int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
-                                uint64_t step, cudaStream_t s);
+                                uint64_t step, uint32_t* status, cudaStream_t s);
 
 // ---- S2 / S3 / S4 -----------------------------------------------------------------------
 cudaError_t launch_confidence(int dtype, const void* h, const void* W1, const int32_t* anchor,

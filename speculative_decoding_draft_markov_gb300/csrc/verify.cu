@@ -351,12 +351,13 @@ __global__ void __launch_bounds__(128) decision_stats_logits_kernel(
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256) decision_select_kernel(
+__global__ void __launch_bounds__(256, 1) decision_select_kernel(
     const T* __restrict__ target, const T* __restrict__ U, const T* __restrict__ W1,
     const T* __restrict__ W2t, const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens,
     const float* __restrict__ lse_d, const RowStat* __restrict__ rs, const Decision* __restrict__ dec,
     const T* __restrict__ draft_logits, const DecideEntry* __restrict__ entries, int n_slots, int bs, int gamma,
-    int V, int r, float inv_tau, uint64_t seed, uint64_t step, int32_t* __restrict__ out_tokens) {
+    int V, int r, float inv_tau, uint64_t seed, uint64_t step, int32_t* __restrict__ out_tokens,
+    uint32_t* status) {
   __shared__ float sA[256];
   __shared__ float tw[kChunk], tp[kChunk];
   __shared__ float rv[8];
@@ -388,8 +389,13 @@ __global__ void __launch_bounds__(256) decision_select_kernel(
   }
   __syncthreads();
   const bool use_res = s_use_res;
-  const ArgMax best{0.f, s_win};
-  const int cstar = (best.i == INT_MAX) ? 0 : best.i;  // only non-finite statistics leave it unset
+  // only non-finite statistics leave the winner unset; a winner outside the vocabulary means the
+  // entries were not written by this call's statistics pass (it gave up): report, use 0
+  int cstar = (s_win == INT_MAX) ? 0 : s_win;
+  if (cstar < 0 || cstar >= (V + kChunk - 1) / kChunk) {
+    if (tid == 0) set_status(status, DSPARK_EINVAL);
+    cstar = 0;
+  }
   const bool resid = (d.kind == kDecResidual) && use_res;
   const bool recompute = resid && draft_logits == nullptr;
   if (recompute) {
@@ -473,7 +479,7 @@ static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_
     le = launch_pdl(decision_select_kernel<T>, dim3(bs), dim3(256), 0, s, target, U, W1, W2t, anchor, tokens, lse,
                     static_cast<const RowStat*>(rs), static_cast<const Decision*>(dec), draft_logits,
                     static_cast<const DecideEntry*>(entries), n_slots, bs, gamma, V, r, inv_tau, seed, step,
-                    out_tokens);
+                    out_tokens, status);
     if (le != cudaSuccess) return le;
   }
   return cudaGetLastError();

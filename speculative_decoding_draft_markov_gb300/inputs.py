@@ -37,7 +37,6 @@ from typing import Sequence
 
 import numpy as np
 
-CHUNK = 128  # vocabulary chunk width of the two-level sampler (part of the sampling contract)
 
 
 # ---------------------------------------------------------------------------

@@ -149,6 +149,17 @@ def test_build_sps_matches_oracle(L):
         B.dspark_build_sps(np.ones(10), np.array([4, 4], np.int32))
 
 
+def test_constants_match_the_header_and_the_oracle():
+    """The binding's size and chunk constants are the header's; the chunk widths are the ones
+    the oracle's draws use (the chunk width fixes which random words a draw consumes)."""
+    src = open(HEADER).read()
+    defs = {k: int(v) for k, v in re.findall(r"#define\s+(DSPARK_\w+)\s+(\d+)\b", src)}
+    for name in ("DSPARK_MAX_BS", "DSPARK_MAX_GAMMA", "DSPARK_CHUNK", "DSPARK_DRAFT_CHUNK"):
+        assert getattr(B, name) == defs[name], name
+    assert defs["DSPARK_CHUNK"] == O.CHUNK and defs["DSPARK_DRAFT_CHUNK"] == O.DRAFT_CHUNK
+    assert defs["DSPARK_MAX_GAMMA"] == O.MAX_GAMMA
+
+
 def test_obs_structures_match_the_header(tmp_path):
     """The binding's ctypes structures have the C layout (sizes and field offsets)."""
     import ctypes

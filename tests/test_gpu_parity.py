@@ -1,6 +1,7 @@
 """GPU parity: every stage through the C ABI against the oracle on the same seeded inputs.
 
-Small cases span several 128-id chunks with a ragged tail; the full-size case uses the
+Small cases span several 128-id vocabulary tiles (two 64-id draft chunks each) with a ragged
+tail, including tails that end in either half of a tile; the full-size case uses the
 bs=256, gamma=7, V=151936 workload and checks sampled requests one by one."""
 import numpy as np
 import pytest
@@ -36,6 +37,9 @@ SMALL = {
     "tiny_fp32": I.WORKLOADS["tiny_fp32"],
     "bf16_ragged": I.WORKLOADS["qwen3_4b"].with_(name="bf16_ragged", bs=5, gamma=3, V=2000, d=64, seed=11),
     "bf16_r64": I.WORKLOADS["qwen3_4b"].with_(name="bf16_r64", bs=9, gamma=4, V=1032, r=64, d=64, seed=12),
+    # r = 32 takes the CUDA-core statistics pass in bf16; V = 1000 ends 40 ids into a draft chunk
+    "bf16_r32_simt": I.WORKLOADS["qwen3_4b"].with_(name="bf16_r32_simt", bs=7, gamma=3, V=1000, r=32, d=64,
+                                                   seed=14),
     "bf16_two_mtiles": I.WORKLOADS["qwen3_4b"].with_(name="bf16_two_mtiles", bs=200, gamma=2, V=3000, r=128,
                                                      d=64, seed=13),
 }
@@ -68,9 +72,9 @@ def test_draft_parity_full_size_sampled_rows():
 
 
 def test_draft_parity_long_vocabulary_sampled_rows():
-    """V = 213000 (1665 chunks, ragged last chunk) at bs = 136: a tensor-core CTA takes 22
-    chunks, more than its warp sets draw Gumbels for up front, and the second 128-request
-    M-tile is ragged."""
+    """V = 213000 (1665 vocabulary tiles, ragged last tile) at bs = 136: a tensor-core CTA
+    takes 22 tiles, more than its warp sets draw Gumbels for up front, and the second
+    128-request M-tile is ragged."""
     wl = I.WORKLOADS["mixed_bs256"].with_(name="long_vocab", bs=136, gamma=2, V=213000, seed=21)
     inp = I.make_device_inputs(wl, "cuda", with_target=False, with_hidden=False)
     rows = np.array([0, 67, 127, 128, 135])
