@@ -15,7 +15,8 @@ It computes, plainly and slowly, in IEEE double:
   observe, sts_fit -- observability records (ceiling, utilisation, ECE) and the sequential
                       temperature scaling fit
 plus the host cost-table preparation (build_sps) and the shared random-number
-contract (Philox4x32-10 uniforms, Gumbel keys, two-level Gumbel-max sampler).
+contract (Philox4x32-10 uniforms, Gumbel keys, the two-level samplers: Gumbel-max over
+chunks, then inverse CDF (draft) or Gumbel-max (verification) inside the drawn chunk).
 
 Sources, cited by page and section:
   [SUMMARY]  "DSpark: Confidence-Scheduled Speculative Decoding with Semi-Autoregressive
@@ -201,6 +202,45 @@ def two_level_gumbel(logw: np.ndarray, seed: int, step: int, req: int, pos: int,
     return lo + j, min(_top2_gap(Kc), _top2_gap(ke))
 
 
+def inverse_cdf(w: np.ndarray, u: float):
+    """Inverse-CDF draw from non-negative weights w (not all zero) with one uniform u in (0, 1):
+    with partial sums C_j = w_0 + ... + w_j and S = C_last, the first j with C_j > u S, so that
+    j is drawn with probability w_j / S (zero weights are never drawn).  Returns (j, margin),
+    margin = the distance of u S to the partial sums on either side of the decision, over S."""
+    w = np.asarray(w, dtype=np.float64)
+    C = np.cumsum(w)
+    S = C[-1]
+    t = u * S
+    j = int(np.argmax(C > t))
+    lo = C[j - 1] if j > 0 else 0.0
+    return j, float(min(t - lo, C[j] - t) / S)
+
+
+def two_level_cdf(logw: np.ndarray, seed: int, step: int, req: int, pos: int,
+                  purpose_chunk: int, purpose_elem: int, chunk: int = DRAFT_CHUNK):
+    """Exact draw of v with probability proportional to exp(logw[v]): a chunk by Gumbel-max over
+    the chunks' log-masses, then an id inside the chunk by inverse CDF.
+
+    Level 1 as in two_level_gumbel (chunk key L_c + G_c, purpose_chunk, index c).  Level 2: one
+    uniform u (purpose_elem, index 0) and the chunk's weights w_i = exp(logw[v_i] - m), m the
+    chunk's largest log-weight; the id is inverse_cdf(w, u).  Given the chunk, an id is drawn in
+    proportion to exp(logw), so the product is exact.  Returns (v, margin), margin = the smaller
+    of the level-1 top-two key gap and the level-2 distance to a partial-sum boundary."""
+    logw = np.asarray(logw, dtype=np.float64)
+    n = logw.size
+    L = chunk_log_mass(logw, chunk)
+    nc = L.size
+    Kc = L + gumbel(uniform(seed, step, purpose_chunk, req, pos, np.arange(nc)))
+    if not np.any(np.isfinite(Kc)):
+        raise ValueError("two_level_cdf: no entry with positive weight")
+    c = _first_argmax(Kc)
+    lo, hi = c * chunk, min(n, (c + 1) * chunk)
+    seg = logw[lo:hi]
+    u = float(uniform(seed, step, purpose_elem, req, pos, np.array([0]))[0])
+    j, m2 = inverse_cdf(np.exp(seg - np.max(seg)), u)
+    return lo + j, min(_top2_gap(Kc), m2)
+
+
 # ---------------------------------------------------------------------------
 # S1 -- Markov-head block draft
 # ---------------------------------------------------------------------------
@@ -223,8 +263,9 @@ def draft_block(U, W1, W2t, anchor, temperature: float, seed: int, step: int,
     the causal per-position distributions left to right; per-token probabilities stay exact
     softmax values, which rejection sampling needs.
     Readings: x_0 = anchor feeds B_1; the sampling temperature divides the logits; at
-    temperature 0 the draw is the argmax (lowest index on ties); the two-level draw uses
-    chunks of DRAFT_CHUNK = 64 ids (the law is exactly softmax for any chunk width).
+    temperature 0 the draw is the argmax (lowest index on ties); the draw is two_level_cdf
+    over chunks of DRAFT_CHUNK = 64 ids: a chunk by Gumbel-max over chunk masses, then an id by
+    inverse CDF inside it (the law is exactly softmax for any chunk width).
 
     Returns tokens [bs, gamma] int32, logit_x [bs, gamma] (tempered logit of the drawn
     token; raw logit at temperature 0), lse [bs, gamma] (log-sum-exp of the tempered
@@ -250,7 +291,7 @@ def draft_block(U, W1, W2t, anchor, temperature: float, seed: int, step: int,
             else:
                 t = ell[r] / temperature
                 rid = r if req_ids is None else int(req_ids[r])
-                v, mg = two_level_gumbel(t, seed, step, rid, k, P_DRAFT_CHUNK, P_DRAFT_ELEM, chunk)
+                v, mg = two_level_cdf(t, seed, step, rid, k, P_DRAFT_CHUNK, P_DRAFT_ELEM, chunk)
                 tokens[r, k - 1] = v
                 logit_x[r, k - 1] = t[v]
                 lse[r, k - 1] = logsumexp(t)

@@ -1,6 +1,10 @@
 """Pins of the oracle's samplers and of S1 (Markov block draft).
 
 - the two-level Gumbel sampler draws exactly from softmax (chi-square, ragged chunks);
+- the inverse-CDF step takes hand-computed ids on boundary and zero-weight cases, and the map
+  u -> id partitions (0, 1) into intervals of length w_j / S (brute force over a fine u grid);
+- the two-level chunk + inverse-CDF sampler of the draft draws exactly from softmax, its chunk
+  marginal is the chunk mass, and its level-2 uniform is the element purpose's word 0;
 - Markov logits equal a brute-force triple loop;
 - the drafted joint distribution of (x_1, x_2) is p_1(x_1) p_2(x_2 | x_1) with the bias of
   position 2 taken from x_1 (catches an off-by-one in the conditioning token);
@@ -44,6 +48,68 @@ def test_two_level_sampler_chunk_marginal_is_chunk_mass():
         counts[v // chunk] += 1
     assert _chi2_ok(counts, mass)
     np.testing.assert_allclose(np.exp(O.chunk_log_mass(logw, chunk)), np.exp(logw).reshape(5, 8).sum(1), rtol=1e-12)
+
+
+def test_inverse_cdf_by_hand():
+    # w = [1, 1, 2]: partial sums 1, 2, 4 (S = 4); the first j with C_j > u S
+    w = [1.0, 1.0, 2.0]
+    assert O.inverse_cdf(w, 0.1)[0] == 0      # u S = 0.4 < 1
+    assert O.inverse_cdf(w, 0.25)[0] == 1     # u S = 1 = C_0: not > , so the next id
+    assert O.inverse_cdf(w, 0.3)[0] == 1      # 1.2
+    assert O.inverse_cdf(w, 0.5)[0] == 2      # 2 = C_1
+    assert O.inverse_cdf(w, 0.99)[0] == 2
+    j, m = O.inverse_cdf(w, 0.3)
+    assert abs(m - 0.05) < 1e-12              # min(1.2 - 1, 2 - 1.2) / 4
+    # zero weights are never drawn
+    z = [0.0, 1.0, 0.0, 1.0]
+    assert O.inverse_cdf(z, 0.2)[0] == 1 and O.inverse_cdf(z, 0.7)[0] == 3
+    assert O.inverse_cdf([0.0, 0.0, 5.0], 0.01)[0] == 2
+
+
+def test_inverse_cdf_partitions_the_unit_interval():
+    rng = np.random.default_rng(12)
+    w = rng.exponential(size=9)
+    w[4] = 0.0
+    n = 200_000
+    us = (np.arange(n) + 0.5) / n
+    ids = np.array([O.inverse_cdf(w, u)[0] for u in us])
+    assert np.all(np.diff(ids) >= 0)          # monotone in u
+    frac = np.bincount(ids, minlength=9) / n
+    np.testing.assert_allclose(frac, w / w.sum(), atol=2.0 / n)
+
+
+def test_chunk_cdf_sampler_matches_softmax_with_ragged_chunks():
+    rng = np.random.default_rng(13)
+    logw = rng.normal(0, 1.5, size=13)
+    logw[6] = -np.inf
+    p = softmax(np.where(np.isfinite(logw), logw, -1e300))
+    counts = np.zeros(13)
+    for s in range(30000):
+        v, _ = O.two_level_cdf(logw, 9, s, 0, 1, O.P_DRAFT_CHUNK, O.P_DRAFT_ELEM, chunk=4)
+        counts[v] += 1
+    assert counts[6] == 0
+    assert _chi2_ok(counts, p)
+
+
+def test_chunk_cdf_sampler_levels():
+    rng = np.random.default_rng(14)
+    logw = rng.normal(0, 2.0, size=40)
+    chunk = 8
+    mass = softmax(logw).reshape(5, 8).sum(axis=1)
+    counts = np.zeros(5)
+    for s in range(20000):
+        v, _ = O.two_level_cdf(logw, 2, s, 1, 3, O.P_DRAFT_CHUNK, O.P_DRAFT_ELEM, chunk=chunk)
+        counts[v // chunk] += 1
+    assert _chi2_ok(counts, mass)
+    # inside the drawn chunk, the id is the inverse CDF of the element purpose's word 0
+    for s in range(50):
+        v, _ = O.two_level_cdf(logw, 2, s, 1, 3, O.P_DRAFT_CHUNK, O.P_DRAFT_ELEM, chunk=chunk)
+        c = v // chunk
+        u = O.uniform(2, s, O.P_DRAFT_ELEM, 1, 3, np.array([0]))[0]
+        seg = logw[c * chunk:(c + 1) * chunk]
+        p_in = np.exp(seg - seg.max())
+        edges = np.concatenate([[0.0], np.cumsum(p_in)]) / p_in.sum()
+        assert edges[v % chunk] <= u < edges[v % chunk + 1]
 
 
 def test_markov_logits_brute_force():
