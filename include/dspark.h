@@ -30,13 +30,16 @@
  *   - No exception or abort crosses the ABI.
  *   - Random numbers: Philox4x32-10 keyed by `seed`, counter (index >> 2, request, step low
  *     32 bits, purpose << 24 | position << 16 | step bits 32..47).  Purposes: 1 draft chunk
- *     key, 2 draft entry key, 3 accept uniform, 4 decision chunk key, 5 decision entry key.
+ *     key, 2 draft in-chunk uniform (index 0), 3 accept uniform, 4 decision chunk key,
+ *     5 decision entry key.
  *     A uniform is ((word >> 9) + 0.5) * 2^-23.  A step is reproducible from (seed, step).
- *   - Sampling: a categorical draw over the vocabulary uses the two-level Gumbel-max rule:
- *     chunks of consecutive ids get key log(mass) + Gumbel; the best chunk is drawn, then an
- *     id inside it by Gumbel-max over its log-weights.  Ties: lowest index.  The draft's draws
- *     use chunks of DSPARK_DRAFT_CHUNK ids, the verification's of DSPARK_CHUNK ids (the law
- *     is exactly the softmax for any chunk width; the width fixes which random words are used).
+ *   - Sampling: a categorical draw over the vocabulary is two-level: chunks of consecutive ids
+ *     get key log(mass) + Gumbel and the best chunk is drawn; then the id inside it.  The draft
+ *     (chunks of DSPARK_DRAFT_CHUNK ids) takes the id by inverse CDF: the first id whose
+ *     partial sum of the chunk's weights exceeds u times their total, u its in-chunk uniform.
+ *     The verification (chunks of DSPARK_CHUNK ids) takes it by Gumbel-max over the chunk's
+ *     log-weights.  Ties: lowest index.  Both laws are exactly the softmax for any chunk
+ *     width; the width fixes which random words are used.
  */
 #ifndef DSPARK_H
 #define DSPARK_H

@@ -118,8 +118,8 @@ __global__ void __launch_bounds__(128) draft_stats_simt_kernel(
 // Select pass: one 256-thread block per row.  Warp 0 merges the row's entries: the row LSE
 // from the (max, sum-exp) pairs, and the winner = argmax of the keys (lowest index on ties).
 //   temperature > 0: the winner is the draft chunk c* of the first Gumbel level; its 64 logits
-//   are recomputed (fixed-order fp32 dot products) and the entry key t_v + G'_v (purpose 2,
-//   index v - 64 c*) picks x_k.
+//   are recomputed (fixed-order fp32 dot products) and an inverse-CDF draw over them with the
+//   row's uniform (purpose 2, index 0) picks x_k.
 //   temperature = 0: the winner is x_k itself (lowest-index argmax).
 // ---------------------------------------------------------------------------------------
 template <typename T>
@@ -131,8 +131,6 @@ __global__ void __launch_bounds__(256, 1) draft_select_kernel(
     uint32_t* status) {
   __shared__ float sA[256];
   __shared__ float tv[kDraftIds];
-  __shared__ float rv[8];
-  __shared__ int ri[8];
   __shared__ float s_lse, s_best;
   __shared__ int s_win;
   const int b = blockIdx.x, tid = threadIdx.x;
@@ -188,18 +186,37 @@ __global__ void __launch_bounds__(256, 1) draft_select_kernel(
   __syncthreads();
   if (tid < kDraftIds) tv[tid] = (v_own < V) ? (tv[tid] + u_v) * inv_tau : -INFINITY;
   __syncthreads();
-  ArgMax e{-INFINITY, INT_MAX};
-  if (tid < kDraftIds) {
-    const uint4 w = philox_group(seed, step, kDraftElem, b, k, tid >> 2);
-    const float t = tv[tid];
-    if (t > -INFINITY) e = ArgMax{t + gumbel_from_bits(pick_word(w, tid & 3)), tid};
-  }
-  e = block_argmax<256>(e, rv, ri);
-  if (tid == 0) {
-    const int ei = (e.i == INT_MAX) ? 0 : e.i;
-    tokens[out] = min(cstar * kDraftIds + ei, V - 1);
-    logit_x[out] = tv[ei];
-    lse[out] = s_lse;
+  // the id inside the chunk by inverse CDF (warp 0, two offsets a lane: lane and lane + 32): the
+  // first offset whose partial sum of exp(t - max) exceeds u times the total, u the row's
+  // uniform of Philox purpose 2, index 0; should rounding leave every partial sum at or below
+  // it, the last id with a finite logit
+  if (tid < 32) {
+    const float a0 = tv[tid], a1 = tv[tid + 32];
+    const float mc = warp_max(fmaxf(a0, a1));
+    const float w0 = a0 > -INFINITY ? expf(a0 - mc) : 0.f, w1 = a1 > -INFINITY ? expf(a1 - mc) : 0.f;
+    float c0 = w0, c1 = w1;  // inclusive scans over offsets 0..31 and 32..63
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y0 = __shfl_up_sync(0xFFFFFFFFu, c0, o), y1 = __shfl_up_sync(0xFFFFFFFFu, c1, o);
+      if (tid >= o) { c0 += y0; c1 += y1; }
+    }
+    c1 += __shfl_sync(0xFFFFFFFFu, c0, 31);
+    const float total = __shfl_sync(0xFFFFFFFFu, c1, 31);
+    const float u = bits_to_uniform(philox_group(seed, step, kDraftElem, b, k, 0).x);
+    const float tgt = u * total;
+    const unsigned hit0 = __ballot_sync(0xFFFFFFFFu, w0 > 0.f && c0 > tgt);
+    const unsigned hit1 = __ballot_sync(0xFFFFFFFFu, w1 > 0.f && c1 > tgt);
+    const unsigned pos0 = __ballot_sync(0xFFFFFFFFu, w0 > 0.f), pos1 = __ballot_sync(0xFFFFFFFFu, w1 > 0.f);
+    int ei;
+    if (hit0) ei = __ffs(hit0) - 1;
+    else if (hit1) ei = 32 + __ffs(hit1) - 1;
+    else if (pos1) ei = 32 + 31 - __clz(pos1);
+    else ei = pos0 ? 31 - __clz(pos0) : 0;
+    if (tid == 0) {
+      tokens[out] = min(cstar * kDraftIds + ei, V - 1);
+      logit_x[out] = tv[ei];
+      lse[out] = s_lse;
+    }
   }
 }
 
