@@ -141,10 +141,11 @@ __global__ void __launch_bounds__(256, 1) draft_select_kernel(
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const size_t out = size_t(b) * gamma + (k - 1);
 
-  // the W1 row of x_{k-1} does not depend on the draw: fetch it first
-  if (!greedy) {
+  // the W1 row of x_{k-1} does not depend on the draw: warps 1..7 fetch it while warp 0 merges
+  // the entries, so that neither waits for the other's loads
+  if (!greedy && tid >= 32) {
     const int xp = clamp_token((k == 1) ? anchor[b] : tokens[size_t(b) * gamma + k - 2], V);
-    for (int i = tid; i < r; i += 256) sA[i] = ld_f32(W1, size_t(xp) * r + i);
+    for (int i = tid - 32; i < r; i += 224) sA[i] = ld_f32(W1, size_t(xp) * r + i);
   }
   if (tid < 32) {
     LsePair lp{-INFINITY, 0.f};
