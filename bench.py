@@ -3,9 +3,10 @@
 One step = draft_block -> confidence -> schedule -> pack -> [target forward] -> verify, all
 through the C ABI on one stream; the timed steps replay CUDA graphs captured from those calls
 (one graph per stage and step, each with its own step counter), the e2e steps call the API
-directly.  The target forward is the caller's model and is not part of this path: it is a row
-gather here and it sits outside the timed segments; everything else is timed with CUDA events
-on the launching stream.  The L2 is flushed (256 MB write) between timed steps.
+directly.  The target forward is the caller's model and is not part of this path: in the timed
+steps it is a device row gather outside the timed segments; in the e2e steps it copies the
+step's packed rows from host memory, inside the timing.  Everything else is timed with CUDA
+events on the launching stream.  The L2 is flushed (256 MB write) between timed steps.
 tokens/step = sum over requests of (accepted + 1).  The same steps are timed again under the
 asynchronous scheduler (budget from two steps back on a second stream) and reported under "zos".
 
@@ -377,19 +378,31 @@ def run_ours(args, rank: int, world: int):
     ztotal_ms = float((zseg[:, 0] + zseg[:, 1]).sum())
 
     # ---- end to end through the public API with host buffers (pinned), copies inside the timing.
-    # Every step copies its own inputs host -> device and reads its result back; the inputs are
-    # double-buffered so that the copy of step t + 1 (a second stream) runs while step t computes.
-    # The timed region holds every copy and every step; each step's inputs (1.18 GB) exceed L2.
-    host = {k: inp[k].cpu().pin_memory() for k in ("U", "h", "anchor", "target")}
+    # Every step copies its own inputs host -> device and reads its result back.  U, h and the
+    # anchors are double-buffered, so that the copy of step t + 1 (a second stream) runs while
+    # step t computes.  The target logits stay in host memory as the target model's output for
+    # every (request, position); each step's target forward reads back the packed layout
+    # (cu_seqlens) and copies exactly the rows that step verifies (dspark_copy_packed_rows_async).
+    # The timed region holds every copy and every step; each step's inputs exceed L2.
+    host = {k: inp[k].cpu().pin_memory() for k in ("U", "h", "anchor")}
+    host_target = inp["target"].cpu().pin_memory()
+    cu_host = torch.empty(bs + 1, dtype=torch.int32).pin_memory()
+    target_rows = []
+
+    def host_target_forward(b):
+        cu_host.copy_(b.cu, non_blocking=True)
+        stream.synchronize()  # the packed layout is known once the pack has run
+        B.dspark_copy_packed_rows_async(b.packed, host_target, cu_host, stream)
+        target_rows.append(int(cu_host[bs]))
+
     inps = [inp, dict(inp)]
     for k in host:
         inps[1][k] = torch.empty_like(inp[k])
-    fwds = [fwd, S.gather_target_forward(inps[1]["target"])]
+    fwds = [host_target_forward, host_target_forward]
     e2e_steps = max(2, min(args.steps, 10))
     outs = [torch.empty((bs, gamma + 1), dtype=torch.int32).pin_memory() for _ in range(e2e_steps)]
     accs = [torch.empty(bs, dtype=torch.int32).pin_memory() for _ in range(e2e_steps)]
-    bi = sum(t.numel() * t.element_size() for t in host.values())
-    bo = outs[0].numel() * 4 + accs[0].numel() * 4
+    bo = outs[0].numel() * 4 + accs[0].numel() * 4 + cu_host.numel() * 4
     cstream = torch.cuda.Stream(dev)
     copied = [torch.cuda.Event() for _ in range(2)]
     released = [torch.cuda.Event() for _ in range(2)]
@@ -420,6 +433,8 @@ def run_ours(args, rank: int, world: int):
     e1.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     e2e_tokens = sum(int((a.to(torch.int64) + 1).sum()) for a in accs)
+    row_bytes = host_target[0, 0].numel() * host_target.element_size()
+    bi = sum(t.numel() * t.element_size() for t in host.values()) + int(np.mean(target_rows)) * row_bytes
 
     # aggregate over ranks: max time, summed tokens
     (total_ms, e2e_ms, ztotal_ms), (tokens, e2e_tokens, ztokens) = aggregate_over_ranks(
@@ -465,8 +480,10 @@ def run_ours(args, rank: int, world: int):
                      "algorithmic_bytes": draft_bytes, "peak_kind": peak_kind},
         "e2e": {"value": e2e_tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "steps": e2e_steps,
-                "note": "inputs copied from pinned host memory every step on a second stream, one step "
-                        "ahead (double-buffered); host-to-device copies run at ~210 GB/s on this box"},
+                "note": "U, h, anchors copied from pinned host memory every step on a second stream, one step "
+                        "ahead (double-buffered); the target forward copies the step's packed target rows "
+                        "from pinned host memory after the pack (cu_seqlens read back); host-to-device "
+                        "copies run at ~210 GB/s on this box"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "observability": obs,

@@ -115,10 +115,25 @@ DSPARK_API uint64_t dspark_set_wait_timeout_ns(uint64_t ns);
 DSPARK_API int dspark_build_sps(const double* T_raw, int m_max, const int32_t* tiers, int n_tiers,
                      double* sps_out);
 
+/* Host helper for a caller whose target-model logits sit in host memory (a host-side target
+ * model, a replay of recorded logits): enqueue the host-to-device copies of exactly the rows a
+ * packed verify batch reads ([SGLANG] "Ragged verify under full CUDA graphs": request r's
+ * tested positions 0 .. n_r - 1 occupy packed rows cu[r] .. cu[r+1] - 1).
+ *   packed     device [>= cu[bs], row_bytes]   destination rows (dspark_verify's `target`)
+ *   rows       host   [bs, rows_per_req, row_bytes]  request r's candidate rows 0 .. rows_per_req-1
+ *              (pinned memory for asynchronous copies)
+ *   cu         host   [bs + 1] int32, the cu_seqlens that dspark_pack wrote (read back by the
+ *              caller): one cudaMemcpyAsync per request with n_r = cu[r+1] - cu[r] > 0 rows
+ * Returns DSPARK_EINVAL on null pointers, row_bytes or rows_per_req < 1, decreasing cu or
+ * n_r > rows_per_req (nothing is enqueued then), DSPARK_ECUDA when a copy fails to enqueue. */
+DSPARK_API int dspark_copy_packed_rows_async(void* packed, const void* rows, size_t row_bytes, int bs,
+                                             int rows_per_req, const int32_t* cu, dspark_stream_t stream);
+
 /* S1. Markov-head block draft ([SUMMARY] "Architecture (drafter)", Markov head and
  * left-to-right sampling).  For k = 1..gamma, per request:
  *     l_k = U[:, k-1] + W1[x_{k-1}] . W2,   W2 = W2t^T,  x_0 = anchor
- *     temperature > 0:  x_k ~ softmax(l_k / temperature)  (two-level Gumbel-max, purposes 1, 2)
+ *     temperature > 0:  x_k ~ softmax(l_k / temperature)  (chunk by Gumbel-max, id by inverse
+ *                       CDF; purposes 1, 2)
  *                       logit_x = l_k[x_k] / temperature,  lse = logsumexp(l_k / temperature)
  *     temperature = 0:  x_k = argmax l_k (lowest index),  logit_x = l_k[x_k],  lse = 0
  *   U        device [bs, gamma, V]  base logits U_1..U_gamma of the parallel backbone

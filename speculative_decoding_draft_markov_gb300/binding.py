@@ -28,6 +28,7 @@ _SIGS = {
     "dspark_workspace_init": (_i, [_vp, _sz, _vp]),
     "dspark_read_device_status": (_i, [_vp, _vp]),
     "dspark_build_sps": (_i, [_vp, _i, _vp, _i, _vp]),
+    "dspark_copy_packed_rows_async": (_i, [_vp, _vp, _sz, _i, _i, _vp, _vp]),
     "dspark_set_wait_timeout_ns": (_u64, [_u64]),
     "dspark_draft_block": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _u64, _u64,
                                 _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -147,6 +148,21 @@ def dspark_build_sps(T_raw, tiers) -> np.ndarray:
     _check(lib().dspark_build_sps(T.ctypes.data, T.size - 1, t.ctypes.data if t.size else None,
                                   t.size, out.ctypes.data), "dspark_build_sps")
     return out
+
+
+def dspark_copy_packed_rows_async(packed, rows_host, cu_host, stream=None) -> None:
+    """Enqueue the host-to-device copies of the rows a packed batch reads: request r's rows
+    0 .. n_r - 1 of rows_host [bs, rows_per_req, ...] (pinned CPU tensor) into packed rows
+    cu[r] .. cu[r+1] - 1 of `packed` (device); cu_host is the batch's cu_seqlens on the host."""
+    if rows_host.is_cuda or not cu_host.device.type == "cpu":
+        raise ValueError("rows_host and cu_host must be host tensors")
+    cu = cu_host.contiguous()
+    if cu.dtype.itemsize != 4:
+        raise ValueError("cu_host must be int32")
+    bs, rpr = rows_host.shape[0], rows_host.shape[1]
+    row_bytes = rows_host[0, 0].numel() * rows_host.element_size()
+    _check(lib().dspark_copy_packed_rows_async(_p(packed), _p(rows_host), row_bytes, bs, rpr, cu.data_ptr(),
+                                               _stream(stream)), "dspark_copy_packed_rows_async")
 
 
 # ----------------------------------------------------------------------------- the path

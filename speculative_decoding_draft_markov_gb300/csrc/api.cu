@@ -75,6 +75,26 @@ uint64_t dspark_set_wait_timeout_ns(uint64_t ns) {
   return old;
 }
 
+int dspark_copy_packed_rows_async(void* packed, const void* rows, size_t row_bytes, int bs, int rows_per_req,
+                                  const int32_t* cu, dspark_stream_t stream) {
+  if (!packed || !rows || !cu || row_bytes < 1 || rows_per_req < 1 || bs < 1) return DSPARK_EINVAL;
+  for (int r = 0; r < bs; ++r) {  // validate everything before the first copy is enqueued
+    const int n = cu[r + 1] - cu[r];
+    if (cu[r] < 0 || n < 0 || n > rows_per_req) return DSPARK_EINVAL;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* dst = static_cast<char*>(packed);
+  const char* src = static_cast<const char*>(rows);
+  for (int r = 0; r < bs; ++r) {
+    const int n = cu[r + 1] - cu[r];
+    if (n == 0) continue;
+    if (cudaMemcpyAsync(dst + size_t(cu[r]) * row_bytes, src + size_t(r) * rows_per_req * row_bytes,
+                        size_t(n) * row_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return DSPARK_ECUDA;
+  }
+  return DSPARK_OK;
+}
+
 int dspark_build_sps(const double* T_raw, int m_max, const int32_t* tiers, int n_tiers,
                      double* sps_out) {
   if (!T_raw || !sps_out || m_max < 0 || n_tiers < 0 || (n_tiers > 0 && !tiers)) return DSPARK_EINVAL;

@@ -128,6 +128,21 @@ def test_other_entry_points_host_validation(L):
     assert L.dspark_verify(*args) == B.DSPARK_EINVAL
 
 
+def test_copy_packed_rows_host_validation(L):
+    """Bad arguments are refused on the host before any copy is enqueued."""
+    f = FAKE
+    cu = np.array([0, 3, 3, 9], dtype=np.int32)      # 3 requests: 3, 0, 6 rows
+    p = cu.ctypes.data
+    assert L.dspark_copy_packed_rows_async(None, f, 64, 3, 8, p, None) == B.DSPARK_EINVAL
+    assert L.dspark_copy_packed_rows_async(f, None, 64, 3, 8, p, None) == B.DSPARK_EINVAL
+    assert L.dspark_copy_packed_rows_async(f, f, 64, 3, 8, None, None) == B.DSPARK_EINVAL
+    assert L.dspark_copy_packed_rows_async(f, f, 0, 3, 8, p, None) == B.DSPARK_EINVAL
+    assert L.dspark_copy_packed_rows_async(f, f, 64, 3, 0, p, None) == B.DSPARK_EINVAL
+    assert L.dspark_copy_packed_rows_async(f, f, 64, 3, 5, p, None) == B.DSPARK_EINVAL   # 6 rows > 5
+    bad = np.array([0, 4, 2, 5], dtype=np.int32)     # decreasing
+    assert L.dspark_copy_packed_rows_async(f, f, 64, 3, 8, bad.ctypes.data, None) == B.DSPARK_EINVAL
+
+
 def test_build_sps_matches_oracle(L):
     g = json.load(open(os.path.join(ROOT, "tests", "golden", "tier_padding.json")))
     rng = np.random.default_rng(0)
