@@ -1,5 +1,5 @@
 // S1 -- Markov-head block draft: per-position chunk statistics (CUDA-core path) and the
-// per-row merge + two-level Gumbel-max draw.
+// per-row merge + two-level draw (a chunk by Gumbel-max, the id inside it by inverse CDF).
 //
 // DSpark technical summary, "Architecture (drafter)": the sequential Markov head adds the
 // rank-r bias W1[x_{k-1}] W2 to the backbone's base logits U_k and samples left to right.
