@@ -34,6 +34,13 @@ MUTS = {
  "sts_label_offby1": ("        y = (c >= k + 1).astype(np.int64)", "        y = (c >= k).astype(np.int64)", "tests/test_oracle_observe.py"),
  "sts_no_carry": ("        prev = prev / (1.0 + np.exp(-z[:, k] / T[k]))", "        prev = prev", "tests/test_oracle_observe.py"),
  "sts_argmax": ("        g_star = int(np.argmin(table[k]))  # first minimum", "        g_star = int(np.argmax(table[k]))", "tests/test_oracle_observe.py"),
+ "cdf_nonstrict": ("    j = int(np.argmax(C > t))", "    j = int(np.argmax(C >= t))", "tests/test_oracle_sampling.py::test_inverse_cdf_by_hand"),
+ "cdf_reversed_sums": ("    C = np.cumsum(w)\n", "    C = np.cumsum(w[::-1])\n", "tests/test_oracle_sampling.py::test_inverse_cdf_by_hand"),
+ "cdf_wrong_uniform": ("    u = float(uniform(seed, step, purpose_elem, req, pos, np.array([0]))[0])",
+                       "    u = float(uniform(seed, step, purpose_elem, req, pos, np.array([1]))[0])",
+                       "tests/test_oracle_sampling.py::test_chunk_cdf_sampler_levels"),
+ "cdf_chunk_offset_dropped": ("    return lo + j, min(_top2_gap(Kc), m2)", "    return j, min(_top2_gap(Kc), m2)",
+                              "tests/test_oracle_sampling.py::test_chunk_cdf_sampler_matches_softmax_with_ragged_chunks"),
 }
 
 
