@@ -123,7 +123,9 @@ DSPARK_API int dspark_build_sps(const double* T_raw, int m_max, const int32_t* t
  *   rows       host   [bs, rows_per_req, row_bytes]  request r's candidate rows 0 .. rows_per_req-1
  *              (pinned memory for asynchronous copies)
  *   cu         host   [bs + 1] int32, the cu_seqlens that dspark_pack wrote (read back by the
- *              caller): one cudaMemcpyAsync per request with n_r = cu[r+1] - cu[r] > 0 rows
+ *              caller); request r contributes n_r = cu[r+1] - cu[r] rows.  Consecutive requests
+ *              with the same n_r > 0 are one strided copy (cudaMemcpy2DAsync), a lone one a
+ *              cudaMemcpyAsync.
  * Returns DSPARK_EINVAL on null pointers, row_bytes or rows_per_req < 1, decreasing cu or
  * n_r > rows_per_req (nothing is enqueued then), DSPARK_ECUDA when a copy fails to enqueue. */
 DSPARK_API int dspark_copy_packed_rows_async(void* packed, const void* rows, size_t row_bytes, int bs,

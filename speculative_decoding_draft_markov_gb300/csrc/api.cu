@@ -85,12 +85,23 @@ int dspark_copy_packed_rows_async(void* packed, const void* rows, size_t row_byt
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* dst = static_cast<char*>(packed);
   const char* src = static_cast<const char*>(rows);
-  for (int r = 0; r < bs; ++r) {
+  const size_t spitch = size_t(rows_per_req) * row_bytes;
+  // consecutive requests with the same row count n are one strided copy: their packed rows are
+  // contiguous (n rows each), their host rows sit rows_per_req rows apart
+  for (int r = 0; r < bs;) {
     const int n = cu[r + 1] - cu[r];
-    if (n == 0) continue;
-    if (cudaMemcpyAsync(dst + size_t(cu[r]) * row_bytes, src + size_t(r) * rows_per_req * row_bytes,
-                        size_t(n) * row_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-      return DSPARK_ECUDA;
+    int e = r + 1;
+    while (e < bs && cu[e + 1] - cu[e] == n) ++e;
+    if (n > 0) {
+      const size_t width = size_t(n) * row_bytes;
+      const cudaError_t ce =
+          (e - r == 1) ? cudaMemcpyAsync(dst + size_t(cu[r]) * row_bytes, src + size_t(r) * spitch, width,
+                                         cudaMemcpyHostToDevice, s)
+                       : cudaMemcpy2DAsync(dst + size_t(cu[r]) * row_bytes, width, src + size_t(r) * spitch, spitch,
+                                           width, size_t(e - r), cudaMemcpyHostToDevice, s);
+      if (ce != cudaSuccess) return DSPARK_ECUDA;
+    }
+    r = e;
   }
   return DSPARK_OK;
 }

@@ -31,3 +31,21 @@ def test_copied_rows_equal_the_gather():
     B.dspark_copy_packed_rows_async(buf.packed, host, cu)
     torch.cuda.synchronize()
     assert torch.equal(buf.packed[:M], want[:M])
+
+
+def test_runs_of_equal_row_counts():
+    """Hand-made packings with runs of equal row counts (strided copies), lone requests and
+    empty ones: every packed row holds its request's row."""
+    bs, rpr, V = 12, 6, 200
+    host = torch.randn(bs, rpr, V).to(torch.bfloat16).pin_memory()
+    for counts in ([1, 1, 1, 3, 3, 0, 0, 2, 1, 1, 6, 6], [2] * 12, [0, 4, 1, 4, 1, 0, 5, 5, 5, 1, 0, 3]):
+        n = torch.tensor(counts, dtype=torch.int32)
+        cu = torch.zeros(bs + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(n, 0)
+        M = int(cu[-1])
+        packed = torch.zeros((M + 3, V), dtype=torch.bfloat16, device="cuda")
+        B.dspark_copy_packed_rows_async(packed, host, cu)
+        torch.cuda.synchronize()
+        want = torch.cat([host[r, :counts[r]] for r in range(bs)]) if M else host[:0, 0]
+        assert torch.equal(packed[:M].cpu(), want)
+        assert not packed[M:].any()
