@@ -154,11 +154,12 @@ def dspark_copy_packed_rows_async(packed, rows_host, cu_host, stream=None) -> No
     """Enqueue the host-to-device copies of the rows a packed batch reads: request r's rows
     0 .. n_r - 1 of rows_host [bs, rows_per_req, ...] (pinned CPU tensor) into packed rows
     cu[r] .. cu[r+1] - 1 of `packed` (device); cu_host is the batch's cu_seqlens on the host."""
-    if rows_host.is_cuda or not cu_host.device.type == "cpu":
+    import torch
+    if rows_host.is_cuda or cu_host.device.type != "cpu":
         raise ValueError("rows_host and cu_host must be host tensors")
+    if cu_host.dtype != torch.int32 or cu_host.numel() != rows_host.shape[0] + 1:
+        raise ValueError("cu_host must be int32 with one entry per request plus one")
     cu = cu_host.contiguous()
-    if cu.dtype.itemsize != 4:
-        raise ValueError("cu_host must be int32")
     bs, rpr = rows_host.shape[0], rows_host.shape[1]
     row_bytes = rows_host[0, 0].numel() * rows_host.element_size()
     _check(lib().dspark_copy_packed_rows_async(_p(packed), _p(rows_host), row_bytes, bs, rpr, cu.data_ptr(),
