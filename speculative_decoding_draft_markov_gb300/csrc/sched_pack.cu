@@ -181,10 +181,15 @@ __device__ __forceinline__ unsigned long long sched_key(const float* __restrict_
 }
 
 // Ascending bitonic sort of the keys of slots 0 .. 1024 E - 1 by the 1024 threads of the block
-// into out[0 .. 1024 E).  `out` also serves as the exchange buffer of the long distances.
+// into out[0 .. 1024 E).  `out` also serves as the exchange buffer of the long distances; when
+// it holds two such buffers (2 N <= kSchedMaxSlots) consecutive exchanges alternate between
+// them, so that an exchange needs one barrier instead of two (a thread writes one buffer only
+// after every thread has passed the barrier of the exchange that used the other).
 template <int E>
 __device__ void bitonic_sort(const float* __restrict__ surv, int n, unsigned long long* out, int tid) {
   constexpr int N = 1024 * E;
+  constexpr bool kTwoBuffers = 2 * N <= kSchedMaxSlots;
+  int ex = 0;  // exchanges through shared memory so far
   const int lane = tid & 31;
   unsigned long long v[E];
 #pragma unroll
@@ -212,17 +217,19 @@ __device__ void bitonic_sort(const float* __restrict__ surv, int n, unsigned lon
           v[e] = keep_min ? (v[e] < o ? v[e] : o) : (v[e] < o ? o : v[e]);
         }
       } else {
-        __syncthreads();  // earlier readers of `out` are done
+        unsigned long long* xb = (kTwoBuffers && (ex & 1)) ? out + N : out;
+        if (!kTwoBuffers) __syncthreads();  // earlier readers of `out` are done
 #pragma unroll
-        for (int e = 0; e < E; ++e) out[tid * E + e] = v[e];
+        for (int e = 0; e < E; ++e) xb[tid * E + e] = v[e];
         __syncthreads();
 #pragma unroll
         for (int e = 0; e < E; ++e) {
           const int i = tid * E + e;
-          const unsigned long long o = out[i ^ j];
+          const unsigned long long o = xb[i ^ j];
           const bool keep_min = ((i & k) == 0) == ((i & j) == 0);
           v[e] = keep_min ? (v[e] < o ? v[e] : o) : (v[e] < o ? o : v[e]);
         }
+        ++ex;
       }
     }
   }
