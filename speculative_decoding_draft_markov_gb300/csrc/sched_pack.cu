@@ -313,7 +313,7 @@ __device__ int sched_search(const float* __restrict__ surv, int bs, int gamma,
   }
   __syncthreads();
   const long long base = (incl - run) + (warp > 0 ? wsum[warp - 1] : 0ll);
-  __syncthreads();
+  // each thread overwrites only the keys it read itself: no barrier needed before
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int i = tid * 4 + q;
