@@ -179,20 +179,24 @@ __global__ void __launch_bounds__(256, 1) draft_select_kernel(
     if (tid == 0) set_status(status, DSPARK_EINVAL);
     cstar = 0;
   }
-  // the U values of the chosen chunk load together with its W2t rows
-  float u_v = 0.f;
-  const int v_own = cstar * kDraftIds + tid;
-  if (tid < kDraftIds && v_own < V) u_v = ld_f32(U, (size_t(b) * gamma + (k - 1)) * V + v_own);
+  // the U values of the chosen chunk (warp 0: offsets lane and lane + 32) load together with its
+  // W2t rows
+  const int v0 = cstar * kDraftIds + tid, v1 = v0 + 32;
+  const size_t urow = (size_t(b) * gamma + (k - 1)) * V;
+  float u0 = 0.f, u1 = 0.f;
+  if (tid < 32) {
+    if (v0 < V) u0 = ld_f32(U, urow + v0);
+    if (v1 < V) u1 = ld_f32(U, urow + v1);
+  }
   chunk_dots<T, kDraftIds / 8>(W2t, r, V, cstar * kDraftIds, sA, tv);
-  __syncthreads();
-  if (tid < kDraftIds) tv[tid] = (v_own < V) ? (tv[tid] + u_v) * inv_tau : -INFINITY;
   __syncthreads();
   // the id inside the chunk by inverse CDF (warp 0, two offsets a lane: lane and lane + 32): the
   // first offset whose partial sum of exp(t - max) exceeds u times the total, u the row's
   // uniform of Philox purpose 2, index 0; should rounding leave every partial sum at or below
   // it, the last id with a finite logit
   if (tid < 32) {
-    const float a0 = tv[tid], a1 = tv[tid + 32];
+    const float a0 = v0 < V ? (tv[tid] + u0) * inv_tau : -INFINITY;
+    const float a1 = v1 < V ? (tv[tid + 32] + u1) * inv_tau : -INFINITY;
     const float mc = warp_max(fmaxf(a0, a1));
     const float w0 = a0 > -INFINITY ? expf(a0 - mc) : 0.f, w1 = a1 > -INFINITY ? expf(a1 - mc) : 0.f;
     float c0 = w0, c1 = w1;  // inclusive scans over offsets 0..31 and 32..63
@@ -213,9 +217,10 @@ __global__ void __launch_bounds__(256, 1) draft_select_kernel(
     else if (hit1) ei = 32 + __ffs(hit1) - 1;
     else if (pos1) ei = 32 + 31 - __clz(pos1);
     else ei = pos0 ? 31 - __clz(pos0) : 0;
+    const float te = __shfl_sync(0xFFFFFFFFu, (ei & 32) ? a1 : a0, ei & 31);  // tempered logit of x_k
     if (tid == 0) {
       tokens[out] = min(cstar * kDraftIds + ei, V - 1);
-      logit_x[out] = tv[ei];
+      logit_x[out] = te;
       lse[out] = s_lse;
     }
   }
