@@ -290,10 +290,11 @@ def run_ours(args, rank: int, world: int):
                             buf.conf, buf.surv)
         if zos:
             B.dspark_schedule_zos_select(buf.surv, sps, ring, it, buf.window, buf.K)
-        else:
-            B.dspark_schedule(buf.surv, sps, SCHED, buf.window, buf.K, buf.theta)
-        B.dspark_pack(buf.window, inp["anchor"], buf.tokens, tiers_dev, buf.cu, buf.ids, buf.req, buf.pos,
-                      buf.padded, buf.ws)
+            B.dspark_pack(buf.window, inp["anchor"], buf.tokens, tiers_dev, buf.cu, buf.ids, buf.req, buf.pos,
+                          buf.padded, buf.ws)
+        else:  # the synchronous scheduler and the pack of its windows in one launch
+            B.dspark_schedule_pack(buf.surv, sps, SCHED, buf.window, buf.K, buf.theta, inp["anchor"], buf.tokens,
+                                   tiers_dev, buf.cu, buf.ids, buf.req, buf.pos, buf.padded, buf.ws)
 
     def verify_stage(it, zos):
         # asynchronous scheduler: the budget for step it + 2 forks onto a second stream and
@@ -451,7 +452,9 @@ def run_ours(args, rank: int, world: int):
     draft_ms = float(seg[:, 2].mean())
     achieved = draft_bytes / (draft_ms * 1e-3) / 1e9
     traffic = _profiled_traffic()
-    launches_per_step = 2 * gamma + 3 + (4 if tau > 0 else 2)
+    # per step: gamma vocabulary passes + gamma selects, confidence, schedule+pack (one launch),
+    # verify rows, decide, and at temperature > 0 the decision statistics and select
+    launches_per_step = 2 * gamma + 2 + (4 if tau > 0 else 2)
     return {
         "metric": METRIC,
         "value": tokens / (total_ms * 1e-3),
@@ -497,7 +500,7 @@ def run_ours(args, rank: int, world: int):
                              "verify_with_budget": float(zseg[:, 1].mean())},
                 "scheduler": "asynchronous: budget from the survival two steps back (global search, second "
                              "stream beside the verify), radix top-K select on the step's path",
-                "gpu_launches": (launches_per_step + 1) * args.steps, "clocks": zclocks},
+                "gpu_launches": (launches_per_step + 2) * args.steps, "clocks": zclocks},
     }
 
 

@@ -222,6 +222,16 @@ DSPARK_API int dspark_pack(const int32_t* window, const int32_t* anchor, const i
                 int32_t* cu_seqlens, int32_t* ids, int32_t* req, int32_t* pos,
                 int32_t* padded_total, void* ws, size_t ws_bytes, dspark_stream_t stream);
 
+/* S3 then S4 in one launch: exactly dspark_schedule (window required) followed by dspark_pack
+ * of the windows it wrote, with the arguments, outputs and errors of both; one kernel boundary
+ * fewer on the step's path. */
+DSPARK_API int dspark_schedule_pack(const float* surv, int bs, int gamma, const double* sps, int m_max,
+                                    int mode, int32_t* window, int32_t* K_out, double* theta_out,
+                                    const int32_t* anchor, const int32_t* tokens, const int32_t* tiers,
+                                    int n_tiers, int cap, int32_t* cu_seqlens, int32_t* ids, int32_t* req,
+                                    int32_t* pos, int32_t* padded_total, void* ws, size_t ws_bytes,
+                                    dspark_stream_t stream);
+
 /* S5. Rejection-sampling verification ([SUMMARY] "Abstract", "Architecture (drafter)";
  * [SGLANG] "Verify modes").  Per request r, with l_r = window[r]:
  *   tested positions  L_test   = l_r (COMPACT) or gamma (STATIC, CAP_ACCEPT)

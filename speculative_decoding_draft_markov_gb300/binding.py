@@ -40,6 +40,8 @@ _SIGS = {
     "dspark_schedule_zos_select": (_i, [_vp, _i, _i, _vp, _i, _vp, _u64, _vp, _vp, _vp]),
     "dspark_schedule_zos_budget": (_i, [_vp, _i, _i, _vp, _i, _vp, _u64, _vp]),
     "dspark_pack": (_i, [_vp, _vp, _vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dspark_schedule_pack": (_i, [_vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp,
+                                  _vp, _vp, _vp, _sz, _vp]),
     "dspark_observe": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "dspark_obs_report": (_i, [_vp, _i, _vp]),
     "dspark_sts_fit_workspace_bytes": (_sz, [_i, _i]),
@@ -221,6 +223,17 @@ def dspark_pack(window, anchor, tokens, tiers, cu_seqlens, ids, req, pos, padded
     _check(lib().dspark_pack(_p(window), _p(anchor), _p(tokens), bs, gamma, _p(tiers) if n_t else None, n_t,
                              ids.numel(), _p(cu_seqlens), _p(ids), _p(req), _p(pos), _p(padded_total),
                              _p(ws), ws.numel(), _stream(stream)), "dspark_pack")
+
+
+def dspark_schedule_pack(surv, sps, mode, window, K_out, theta_out, anchor, tokens, tiers, cu_seqlens, ids, req,
+                         pos, padded_total, ws, stream=None):
+    """dspark_schedule then dspark_pack of its windows, in one launch."""
+    bs, gamma = surv.shape
+    n_t = 0 if tiers is None else tiers.numel()
+    _check(lib().dspark_schedule_pack(_p(surv), bs, gamma, _p(sps), sps.numel() - 1, mode, _p(window), _p(K_out),
+                                      _p(theta_out), _p(anchor), _p(tokens), _p(tiers) if n_t else None, n_t,
+                                      ids.numel(), _p(cu_seqlens), _p(ids), _p(req), _p(pos), _p(padded_total),
+                                      _p(ws), ws.numel(), _stream(stream)), "dspark_schedule_pack")
 
 
 def dspark_verify(target, cu_seqlens, window, mode, anchor, tokens, logit_x, lse, U, W1, W2t,

@@ -229,6 +229,26 @@ int dspark_pack(const int32_t* window, const int32_t* anchor, const int32_t* tok
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int dspark_schedule_pack(const float* surv, int bs, int gamma, const double* sps, int m_max, int mode,
+                         int32_t* window, int32_t* K_out, double* theta_out, const int32_t* anchor,
+                         const int32_t* tokens, const int32_t* tiers, int n_tiers, int cap, int32_t* cu_seqlens,
+                         int32_t* ids, int32_t* req, int32_t* pos, int32_t* padded_total, void* ws,
+                         size_t ws_bytes, dspark_stream_t stream) {
+  // the argument checks of dspark_schedule and of dspark_pack
+  if (!surv || !sps || !window || !K_out || !theta_out) return DSPARK_EINVAL;
+  if (bs < 1 || gamma < 1 || m_max < bs) return DSPARK_EINVAL;
+  if (mode != DSPARK_SCHED_EARLY_STOP && mode != DSPARK_SCHED_GLOBAL_ARGMAX) return DSPARK_EINVAL;
+  if (bs > DSPARK_MAX_BS || gamma > DSPARK_MAX_GAMMA || bs * gamma > 4096) return DSPARK_EUNSUPPORTED;
+  if (!al(surv, 4) || !al(sps, 8) || !al(window, 4) || !al(K_out, 4) || !al(theta_out, 8))
+    return DSPARK_EINVAL;
+  if (!anchor || !tokens || !cu_seqlens || !ids || !req || !pos || !padded_total) return DSPARK_EINVAL;
+  if (n_tiers < 0 || (n_tiers > 0 && !tiers) || cap < 1) return DSPARK_EINVAL;
+  if (!ws || !al(ws, 256) || ws_bytes < 256) return DSPARK_EWORKSPACE;
+  return cuda_status(launch_schedule_pack(surv, bs, gamma, sps, m_max, mode, window, K_out, theta_out, anchor,
+                                          tokens, tiers, n_tiers, cap, cu_seqlens, ids, req, pos, padded_total,
+                                          static_cast<uint32_t*>(ws), reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int dspark_verify(const void* target, int dtype, const int32_t* cu_seqlens, const int32_t* window,
                   int mode, int bs, int gamma, int V, const int32_t* anchor, const int32_t* tokens,
                   const float* logit_x, const float* lse, const void* draft_logits, const void* U,

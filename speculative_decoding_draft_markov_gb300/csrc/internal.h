@@ -61,6 +61,12 @@ cudaError_t launch_pack(const int32_t* window, const int32_t* anchor, const int3
                         int bs, int gamma, const int32_t* tiers, int n_tiers, int cap,
                         int32_t* cu, int32_t* ids, int32_t* req, int32_t* pos, int32_t* padded,
                         uint32_t* status, cudaStream_t s);
+// S3 and S4 in one launch (the scheduler's block packs the windows it writes).
+cudaError_t launch_schedule_pack(const float* surv, int bs, int gamma, const double* sps, int m_max, int mode,
+                                 int32_t* window, int32_t* K_out, double* theta_out, const int32_t* anchor,
+                                 const int32_t* tokens, const int32_t* tiers, int n_tiers, int cap, int32_t* cu,
+                                 int32_t* ids, int32_t* req, int32_t* pos, int32_t* padded, uint32_t* status,
+                                 cudaStream_t s);
 
 // ---- S5 verify --------------------------------------------------------------------------
 cudaError_t launch_verify(int dtype, const void* target, const int32_t* cu, const int32_t* window,

@@ -569,15 +569,15 @@ cudaError_t launch_zos_budget(const float* surv, int bs, int gamma, const double
 // packed front to back into a cu_seqlens buffer and the total is rounded up to the nearest
 // captured tier.  One block; thread r owns request r.
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(DSPARK_MAX_BS) pack_kernel(
-    const int32_t* __restrict__ window, const int32_t* __restrict__ anchor,
-    const int32_t* __restrict__ tokens, int bs, int gamma, const int32_t* __restrict__ tiers,
-    int n_tiers, int cap, int32_t* __restrict__ cu, int32_t* __restrict__ ids,
-    int32_t* __restrict__ req, int32_t* __restrict__ pos, int32_t* __restrict__ padded_out,
-    uint32_t* status) {
-  __shared__ int wsum[DSPARK_MAX_BS / 32];
+// The pack of one block of any size (a multiple of 32, at least bs threads; every thread takes
+// part in the barriers): request r is thread r.
+__device__ void pack_block(const int32_t* __restrict__ window, const int32_t* __restrict__ anchor,
+                           const int32_t* __restrict__ tokens, int bs, int gamma, const int32_t* __restrict__ tiers,
+                           int n_tiers, int cap, int32_t* __restrict__ cu, int32_t* __restrict__ ids,
+                           int32_t* __restrict__ req, int32_t* __restrict__ pos, int32_t* __restrict__ padded_out,
+                           uint32_t* status) {
+  __shared__ int wsum[32];
   __shared__ int s_padded, s_M, s_bad;
-  pdl_enter();
   const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
   if (r == 0) s_bad = 0;
   __syncthreads();
@@ -643,12 +643,48 @@ __global__ void __launch_bounds__(DSPARK_MAX_BS) pack_kernel(
   }
 }
 
+__global__ void __launch_bounds__(DSPARK_MAX_BS) pack_kernel(
+    const int32_t* __restrict__ window, const int32_t* __restrict__ anchor,
+    const int32_t* __restrict__ tokens, int bs, int gamma, const int32_t* __restrict__ tiers,
+    int n_tiers, int cap, int32_t* __restrict__ cu, int32_t* __restrict__ ids,
+    int32_t* __restrict__ req, int32_t* __restrict__ pos, int32_t* __restrict__ padded_out,
+    uint32_t* status) {
+  pdl_enter();
+  pack_block(window, anchor, tokens, bs, gamma, tiers, n_tiers, cap, cu, ids, req, pos, padded_out, status);
+}
+
+// S3 then S4 in one block: the windows the search writes are packed by the same block (one launch
+// and one kernel boundary fewer per step than schedule_kernel + pack_kernel).
+__global__ void __launch_bounds__(kSchedThreads) schedule_pack_kernel(
+    const float* __restrict__ surv, int bs, int gamma, const double* __restrict__ sps, int m_max, int mode,
+    int32_t* __restrict__ window, int32_t* __restrict__ K_out, double* __restrict__ theta_out,
+    const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens, const int32_t* __restrict__ tiers,
+    int n_tiers, int cap, int32_t* __restrict__ cu, int32_t* __restrict__ ids, int32_t* __restrict__ req,
+    int32_t* __restrict__ pos, int32_t* __restrict__ padded_out, uint32_t* status) {
+  __shared__ SchedShared sh;
+  pdl_enter();
+  const int ks = sched_search(surv, bs, gamma, sps, m_max, mode, sh, theta_out);
+  if (threadIdx.x == 0) *K_out = ks;
+  sched_windows(sh, ks, bs, gamma, window);
+  __syncthreads();  // the block's window writes are visible to the block
+  pack_block(window, anchor, tokens, bs, gamma, tiers, n_tiers, cap, cu, ids, req, pos, padded_out, status);
+}
+
 cudaError_t launch_pack(const int32_t* window, const int32_t* anchor, const int32_t* tokens,
                         int bs, int gamma, const int32_t* tiers, int n_tiers, int cap,
                         int32_t* cu, int32_t* ids, int32_t* req, int32_t* pos, int32_t* padded,
                         uint32_t* status, cudaStream_t s) {
   return launch_pdl(pack_kernel, dim3(1), dim3(DSPARK_MAX_BS), 0, s, window, anchor, tokens, bs, gamma, tiers,
                     n_tiers, cap, cu, ids, req, pos, padded, status);
+}
+
+cudaError_t launch_schedule_pack(const float* surv, int bs, int gamma, const double* sps, int m_max, int mode,
+                                 int32_t* window, int32_t* K_out, double* theta_out, const int32_t* anchor,
+                                 const int32_t* tokens, const int32_t* tiers, int n_tiers, int cap, int32_t* cu,
+                                 int32_t* ids, int32_t* req, int32_t* pos, int32_t* padded, uint32_t* status,
+                                 cudaStream_t s) {
+  return launch_pdl(schedule_pack_kernel, dim3(1), dim3(kSchedThreads), 0, s, surv, bs, gamma, sps, m_max, mode,
+                    window, K_out, theta_out, anchor, tokens, tiers, n_tiers, cap, cu, ids, req, pos, padded, status);
 }
 
 }  // namespace dspark

@@ -123,6 +123,10 @@ def draft_and_schedule(inp: dict, buf: StepBuffers, sps, temperature: float, see
                          buf.tokens, buf.logit_x, buf.lse, buf.ws, stream)
     B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], buf.tokens, inp["w"], inp["b"], inp["sts_T"],
                         buf.conf, buf.surv, stream)
+    if ring is None and mode == B.DSPARK_COMPACT:  # the windows are the packing: one launch for both
+        B.dspark_schedule_pack(buf.surv, sps, sched_mode, buf.window, buf.K, buf.theta, inp["anchor"], buf.tokens,
+                               tiers, buf.cu, buf.ids, buf.req, buf.pos, buf.padded, buf.ws, stream)
+        return
     if ring is not None:
         B.dspark_schedule_zos_select(buf.surv, sps, ring, step, buf.window, buf.K, stream)
     else:

@@ -128,6 +128,18 @@ def test_other_entry_points_host_validation(L):
     assert L.dspark_verify(*args) == B.DSPARK_EINVAL
 
 
+def test_schedule_pack_host_validation(L):
+    f = FAKE
+    assert L.dspark_schedule_pack(None, 4, 7, f, 64, 1, f, f, f, f, f, None, 0, 64, f, f, f, f, f, f, 1 << 20,
+                                  None) == B.DSPARK_EINVAL
+    assert L.dspark_schedule_pack(f, 4, 7, f, 64, 5, f, f, f, f, f, None, 0, 64, f, f, f, f, f, f, 1 << 20,
+                                  None) == B.DSPARK_EINVAL          # unknown mode
+    assert L.dspark_schedule_pack(f, 4, 7, f, 64, 1, f, f, f, f, f, None, 0, 64, f, f, f, f, f, None, 0,
+                                  None) == B.DSPARK_EWORKSPACE
+    assert L.dspark_schedule_pack(f, 300, 7, f, 4000, 1, f, f, f, f, f, None, 0, 64, f, f, f, f, f, f, 1 << 20,
+                                  None) == B.DSPARK_EUNSUPPORTED
+
+
 def test_copy_packed_rows_host_validation(L):
     """Bad arguments are refused on the host before any copy is enqueued."""
     f = FAKE

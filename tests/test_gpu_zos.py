@@ -131,3 +131,36 @@ def test_zos_inside_the_step_with_a_second_stream():
         # the packed layout and the verify used those windows
         assert int(buf.cu[-1].item()) == bs + K_o
         assert np.all(buf.acc_len.cpu().numpy() <= w_o)
+
+
+@pytest.mark.parametrize("sched_mode", [0, 1])
+def test_fused_schedule_pack_equals_the_two_calls(sched_mode):
+    """dspark_schedule_pack writes exactly what dspark_schedule followed by dspark_pack write."""
+    wl = I.WORKLOADS["qwen3_4b"].with_(name="fused_sched", bs=77, gamma=6, V=2048, d=64, seed=41)
+    dev = torch.device("cuda")
+    bs, gamma = wl.bs, wl.gamma
+    surv = torch.as_tensor(I.random_survival(bs, gamma, 9), device=dev)
+    tokens = torch.as_tensor(I.random_tokens(bs, gamma, wl.V, 3), device=dev)
+    anchor = torch.arange(bs, dtype=torch.int32, device=dev)
+    tiers = torch.as_tensor(np.arange(32, bs * (gamma + 1) + 32, 32, dtype=np.int32), device=dev)
+    T = 1.0 + 0.01 * np.arange(bs * (gamma + 1) + 1)
+    sps = torch.as_tensor(O.build_sps(T, list(range(32, bs * (gamma + 1) + 32, 32))), device=dev)
+    cap = int(tiers[-1])
+    outs = []
+    for fused in (False, True):
+        ws = B.alloc_workspace(bs, gamma, wl.V)
+        win = torch.zeros(bs, dtype=torch.int32, device=dev)
+        K = torch.zeros(1, dtype=torch.int32, device=dev)
+        th = torch.zeros(1, dtype=torch.float64, device=dev)
+        cu = torch.zeros(bs + 1, dtype=torch.int32, device=dev)
+        ids, req, pos = (torch.full((cap,), -7, dtype=torch.int32, device=dev) for _ in range(3))
+        pad = torch.zeros(1, dtype=torch.int32, device=dev)
+        if fused:
+            B.dspark_schedule_pack(surv, sps, sched_mode, win, K, th, anchor, tokens, tiers, cu, ids, req, pos, pad, ws)
+        else:
+            B.dspark_schedule(surv, sps, sched_mode, win, K, th)
+            B.dspark_pack(win, anchor, tokens, tiers, cu, ids, req, pos, pad, ws)
+        assert B.dspark_read_device_status(ws) == B.DSPARK_OK
+        outs.append([t.cpu() for t in (win, K, th, cu, ids, req, pos, pad)])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
