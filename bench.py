@@ -1,22 +1,29 @@
-"""Benchmark: DSpark step tokens/s at bs=256, V=151936, gamma=7 (the mixed-difficulty batch).
+"""Benchmark: DSpark step tokens/s at bs=256, V=151936, gamma=7 (the mixed-difficulty batch),
+then the pages' other workloads.
 
 One step = draft_block -> confidence -> schedule -> pack -> [target forward] -> verify, all
 through the C ABI on one stream; the timed steps replay CUDA graphs captured from those calls
 (one graph per stage and step, each with its own step counter), the e2e steps call the API
-directly.  The target forward is the caller's model and is not part of this path: in the timed
-steps it is a device row gather outside the timed segments; in the e2e steps it copies the
-step's packed rows from host memory, inside the timing.  Everything else is timed with CUDA
-events on the launching stream.  The L2 is flushed (256 MB write) between timed steps.
-tokens/step = sum over requests of (accepted + 1).  The same steps are timed again under the
-asynchronous scheduler (budget from two steps back on a second stream) and reported under "zos".
+directly with host buffers.  The target forward is the caller's model and is not part of this
+path: in the timed steps it is a device row gather outside the timed segments; in the e2e steps
+it copies the step's packed rows from host memory, inside the timing.  Everything else is timed
+with CUDA events on the launching stream.  The L2 is flushed (256 MB write) before every timed
+step.  tokens/step = sum over requests of (accepted + 1); `value` = tokens of all K timed steps /
+their summed time, `value_median` the same at the median step.  Rooflines per stage: the
+draft against HBM (U, W2 once, the gathered W1 rows) and the tensor pipe (2 bs gamma r V flops),
+the verification against HBM (the packed target rows, and at temperature > 0 one U row per
+request and W2 for the recompute of p_d).  The same steps are timed again under the
+asynchronous scheduler ("zos"), and every further configuration gets its own result under
+"configs" (Qwen3-4B-shaped bs 64; the DeepSeek-V4-shaped sweep bs 1..256 with static and compact
+budgets; the long block at temperature 1 and greedy).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload all|none|NAME]
 
 --gpus N > 1 runs under torchrun: one independent replica per GPU (the path has no
 cross-request exchange that needs a collective), barrier + max-over-ranks timing; value is
 the tokens of all ranks / that time ("scaling": "weak").
---impl reference times the CPU oracle (plain numpy, fp64) on bounded samples of the same
-workload."""
+--impl reference times the CPU oracle (plain numpy, fp64; draft and verify over the host cores
+in worker processes) on bounded samples of the same workload."""
 from __future__ import annotations
 
 import argparse
@@ -156,88 +163,133 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm), "source": "nvml" if self.samples else "nvidia-smi"}
 
-
 # ------------------------------------------------------------------------------- CPU oracle
-_SAMPLE_CACHE = {}
-
-
-def _oracle_sample(n_req: int, step: int, wl_name: str = WORKLOAD):
-    """Run the oracle's full step on the first n_req requests of the workload (host inputs).
-    Returns (tokens, seconds).  Inputs are generated (once per sample size) before the clock starts."""
+def _oracle_steps(wl_name: str, n_req: int, steps, mode_name: str = "compact", sched: int = SCHED):
+    """The oracle's full step (draft, confidence, schedule, pack, verify) on the first n_req
+    requests of a workload, on every host core (oracle.pool: one worker per core, requests in
+    slices).  Host inputs are generated and the pool started before the clock; each step's
+    (tokens, seconds) is returned."""
     from oracle import dspark_oracle as O
+    from oracle import pool as OP
     from speculative_decoding_draft_markov_gb300 import inputs as I
     wl = I.WORKLOADS[wl_name].with_(bs=n_req)
-    if n_req not in _SAMPLE_CACHE:
-        h = I.make_host_inputs(wl)
-        _SAMPLE_CACHE[n_req] = (h, O.build_sps(h["T_raw"], h["tiers"]))
-    host, sps = _SAMPLE_CACHE[n_req]
-    t0 = time.perf_counter()
-    tok, lx, lse, _ = O.draft_block(host["U"], host["W1"], host["W2t"], host["anchor"], wl.temperature, wl.seed, step)
-    _, surv, _ = O.confidence(host["h"], host["W1"], host["anchor"], tok, host["w"], host["b"], host["sts_T"])
-    win, K, _, _ = O.schedule(surv.astype(np.float32), sps, SCHED)
-    cap = wl.bs * (wl.gamma + 1)
-    cu, ids, req, pos, padded = O.pack(win, host["anchor"], tok, host["tiers"], max(cap, int(host["tiers"][-1])))
-    packed = I.gather_packed_target(host["target"], req, pos, int(cu[-1]))
-    _, acc, _, _ = O.verify(packed, cu, win, O.COMPACT, host["anchor"], tok, lx, lse, host["U"], host["W1"],
-                            host["W2t"], wl.temperature, wl.seed, step)
-    dt = time.perf_counter() - t0
-    return O.step_tokens(acc), dt
+    h = I.make_host_inputs(wl)
+    sps = O.build_sps(h["T_raw"], h["tiers"])
+    mode = {"compact": O.COMPACT, "static": O.STATIC}[mode_name]
+    per = max(1, -(-n_req // OP.workers()))
+    out = []
+    with OP.pool(h["W1"], h["W2t"], wl.dtype) as p:
+        for s in steps:
+            t0 = time.perf_counter()
+            (tok, lx, lse, _), _ = OP.draft_all(p, h["U"], h["anchor"], wl.temperature, wl.seed, s, per=per)
+            if mode == O.COMPACT:
+                _, surv, _ = O.confidence(h["h"], h["W1"], h["anchor"], tok, h["w"], h["b"], h["sts_T"],
+                                          dtype=wl.dtype)
+                win, _, _, _ = O.schedule(surv.astype(np.float32), sps, sched)
+                cu, _, _, _, _ = O.pack(win, h["anchor"], tok, h["tiers"], max(n_req * (wl.gamma + 1),
+                                                                                 int(h["tiers"][-1])))
+            else:
+                win = np.full(n_req, wl.gamma, dtype=np.int32)
+            (_, acc, _, _), _ = OP.verify_all(p, h["target"], h["U"], win, mode, h["anchor"], tok,
+                                              lx.astype(np.float32), lse.astype(np.float32), wl.temperature,
+                                              wl.seed, s, per=per)
+            out.append((O.step_tokens(acc), time.perf_counter() - t0))
+    return out, OP.workers()
 
 
-def cpu_baseline(n_req: int = 64, reps: int = 4):
-    """Time the oracle in a child process limited to one BLAS/OpenMP thread."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = ("import sys, json; sys.path.insert(0, %r); import bench; "
-            "r = [bench._oracle_sample(%d, s) for s in range(%d)]; print(json.dumps(r))" % (ROOT, n_req, reps))
-    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
-    if out.returncode != 0:
-        return {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle", "error": out.stderr[-300:]}
-    res = json.loads(out.stdout.strip().splitlines()[-1])
+def cpu_baseline(n_req: int = 128, steps: int = 3):
+    """The oracle, as it stands, on every host core: a bounded sample of the workload."""
+    try:
+        res, cores = _oracle_steps(WORKLOAD, n_req, range(steps))
+    except Exception as e:  # reported, never fatal for the GPU line
+        return {"value": None, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                "error": repr(e)[-300:]}
     tok = sum(r[0] for r in res)
     sec = sum(r[1] for r in res)
-    return {"value": tok / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n_req} of the 256 requests, full V=151936, gamma=7, all five stages, {reps} step(s); "
-                      f"{tok} tokens in {sec:.1f} s"}
+    return {"value": tok / sec, "unit": "tokens/s", "cores": cores, "nproc": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {n_req} of the 256 requests of mixed_bs256 (full V=151936, gamma=7), all five "
+                      f"stages (oracle draft and verify in {cores} worker processes, one BLAS thread each), "
+                      f"{steps} steps: {tok} tokens in {sec:.1f} s"}
 
 
-# ------------------------------------------------------------------------------- GPU arm
-def draft_block_bytes(bs: int, gamma: int, V: int, r: int, n_sm: int) -> int:
-    """Compulsory HBM bytes of one dspark_draft_block call (bf16), position by position.
-    Vocabulary pass: U_k [bs, V] and W2t [V, r] read once (a GEMM [bs, r] x [r, V] whose
-    operands are consumed as they stream; W2t is re-read by every position because the positions
-    are serially dependent), the gathered A rows W1[x] [bs, r], and the partial-draw entries
-    written (16 bytes per request and CTA column).  Select: the entries read back, the W1 row,
-    the 64 W2t rows and U_k values of the drawn draft chunk, and the three outputs."""
-    n_mt = (bs + 127) // 128
-    n_slots = (n_sm // n_mt)
-    vocab = bs * V * 2 + V * r * 2 + bs * r * 2 + bs * n_slots * 16
-    chunk = 64  # ids per draft chunk
-    select = bs * (n_slots * 16 + r * 2 + chunk * r * 2 + chunk * 2 + 12)
-    return gamma * (vocab + select)
+# ------------------------------------------------------------------------------- rooflines
+# Algorithmic bytes and flops per call, as the hot-path scope table counts them.
+
+def draft_bytes(bs: int, gamma: int, V: int, r: int, esize: int = 2) -> int:
+    """One dspark_draft_block call: U [bs, gamma, V] read once, W2 [r, V] read once, and the
+    gamma x bs gathered W1 rows.  Re-reads of W2 by later positions (it does not stay in L2)
+    are traffic, reported beside this, not algorithmic bytes."""
+    return bs * gamma * V * esize + V * r * esize + bs * gamma * r * esize
 
 
-def _profiled_traffic():
-    """DRAM bytes of one draft block from the committed ncu summary, or None when the draft
-    kernels' sources changed after that capture (the summary records their SHA-256)."""
+def draft_flops(bs: int, gamma: int, V: int, r: int) -> int:
+    return 2 * bs * gamma * r * V
+
+
+def verify_bytes(rows: float, bs: int, V: int, r: int, greedy: bool, esize: int = 2) -> float:
+    """One dspark_verify call: every packed target row once; at temperature > 0 the decision
+    pass's recompute of p_d adds one U row per request and W2 once (the deciding target rows are
+    counted as L2 re-reads)."""
+    b = rows * V * esize
+    if not greedy:
+        b += bs * V * esize + V * r * esize
+    return b
+
+
+def _sources_sha(files):
     import hashlib
-    path = os.path.join(ROOT, "profiles", "draft_block_mixed_bs256_dram.md")
-    if not os.path.exists(path):
-        return None
-    fields = {}
-    for line in open(path):
-        if ":" in line and line.startswith("- "):
-            k, v = line[2:].split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
     h = hashlib.sha256()
-    for f in ("draft_tc.cu", "draft.cu", "common.cuh", "tc_ptx.cuh", "tc_host.h"):
+    for f in files:
         h.update(open(os.path.join(ROOT, "speculative_decoding_draft_markov_gb300", "csrc", f), "rb").read())
     # of the header, the constants (the kernels' sizes and chunk widths), not its documentation
     for line in open(os.path.join(ROOT, "include", "dspark.h"), "rb"):
         if line.startswith(b"#define"):
             h.update(line)
-    if fields.get("sources_sha256") != h.hexdigest() or "dram_bytes_per_draft_block_gamma7" not in fields:
+    return h.hexdigest()
+
+
+def _profiled_traffic(name: str):
+    """DRAM bytes per call of a stage from its committed ncu summary (profiles/<name>.json), or
+    None when the kernels' sources changed after that capture (the summary records their
+    SHA-256)."""
+    path = os.path.join(ROOT, "profiles", name + ".json")
+    if not os.path.exists(path):
         return None
-    return int(fields["dram_bytes_per_draft_block_gamma7"])
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("sources_sha256") != _sources_sha(d.get("sources", [])):
+        return None
+    return d.get("dram_bytes_per_call")
+
+
+DRAFT_SOURCES = ["draft_tc.cu", "draft.cu", "common.cuh", "tc_ptx.cuh", "tc_host.h"]
+VERIFY_SOURCES = ["verify.cu", "decide_tc.cu", "common.cuh", "tc_ptx.cuh", "tc_host.h"]
+
+
+def rooflines(wl, stage_ms, rows, tau, profile_key=None):
+    hbm, bf16, peak_kind = _peaks()
+    bs, gamma, V, r = wl.bs, wl.gamma, wl.V, wl.r
+    db = draft_bytes(bs, gamma, V, r)
+    dflop = draft_flops(bs, gamma, V, r)
+    dsec = stage_ms["draft"] * 1e-3
+    traffic = _profiled_traffic(f"draft_block_{profile_key}_dram") if profile_key else None
+    vb = verify_bytes(rows, bs, V, r, tau == 0.0)
+    vsec = stage_ms["verify"] * 1e-3
+    vtraffic = _profiled_traffic(f"verify_{profile_key}_dram") if profile_key else None
+    return {
+        "bound": "hbm", "achieved": db / dsec / 1e9, "peak": hbm, "unit": "GB/s", "frac": db / dsec / 1e9 / hbm,
+        "traffic": traffic, "traffic_over_algorithmic": (traffic / db) if traffic else None,
+        "kernel": "dspark_draft_block (gamma tensor-core vocabulary passes, draft_tc_kernel the dominant kernel, "
+                  "+ gamma selects): one C-ABI call, CUDA events around it in the timed steps",
+        "algorithmic_bytes": db, "peak_kind": peak_kind,
+        "tensor": {"achieved": dflop / dsec / 1e12, "peak": bf16, "unit": "TFLOP/s",
+                   "frac": dflop / dsec / 1e12 / bf16, "flops": dflop},
+        "verify": {"bound": "hbm", "achieved": vb / vsec / 1e9, "peak": hbm, "unit": "GB/s",
+                   "frac": vb / vsec / 1e9 / hbm, "algorithmic_bytes": vb, "packed_rows": rows,
+                   "traffic": vtraffic,
+                   "kernel": "dspark_verify (row statistics over the packed target rows, accept scan, and at "
+                             "temperature > 0 the tensor-core decision pass and its select), events around it"},
+    }
 
 
 def aggregate_over_ranks(times_ms, counts, device):
@@ -255,140 +307,159 @@ def aggregate_over_ranks(times_ms, counts, device):
     return [float(x) for x in t.tolist()], [float(x) for x in n.tolist()]
 
 
-def run_ours(args, rank: int, world: int):
-    import torch
-    import torch.distributed as dist
+# ------------------------------------------------------------------------------- GPU arm
+class Path:
+    """One workload's device inputs, buffers and the three stages of its step through the API.
 
-    from speculative_decoding_draft_markov_gb300 import binding as B
-    from speculative_decoding_draft_markov_gb300 import inputs as I
-    from speculative_decoding_draft_markov_gb300 import step as S
+    mode: "compact" (confidence, global scheduler + pack, compact verify) or "static" (pack of
+    the whole block, static verify); tau: sampling temperature (0 = greedy)."""
 
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    wl = I.WORKLOADS[WORKLOAD].with_(seed=I.WORKLOADS[WORKLOAD].seed + 1000 * rank)
-    bs, gamma, V, r = wl.bs, wl.gamma, wl.V, wl.r
-    inp = I.make_device_inputs(wl, dev)
-    cap = int(I.tiers_for(wl)[-1])
-    buf = S.StepBuffers.allocate(bs, gamma, V, cap, inp["U"].dtype, dev)
-    sps = S.sps_table(inp["T_raw"], inp["tiers"], dev)
-    tiers_dev = torch.as_tensor(inp["tiers"], device=dev)
-    fwd = S.gather_target_forward(inp["target"])
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    tokens_acc = torch.zeros(1, dtype=torch.int64, device=dev)
-    tau = wl.temperature
+    def __init__(self, wl, dev, mode="compact", tau=None, sched=SCHED):
+        import torch
 
-    side = torch.cuda.Stream(dev)
-    ring = S.zos_ring(dev)
+        from speculative_decoding_draft_markov_gb300 import binding as B
+        from speculative_decoding_draft_markov_gb300 import inputs as I
+        from speculative_decoding_draft_markov_gb300 import step as S
+        self.B, self.S = B, S
+        self.wl, self.dev, self.mode, self.sched = wl, dev, mode, sched
+        self.tau = wl.temperature if tau is None else tau
+        self.inp = I.make_device_inputs(wl, dev)
+        self.cap = int(I.tiers_for(wl)[-1]) if len(I.tiers_for(wl)) else wl.bs * (wl.gamma + 1)
+        self.cap = max(self.cap, wl.bs * (wl.gamma + 1))
+        self.buf = S.StepBuffers.allocate(wl.bs, wl.gamma, wl.V, self.cap, self.inp["U"].dtype, dev)
+        self.sps = S.sps_table(self.inp["T_raw"], self.inp["tiers"], dev)
+        self.tiers = torch.as_tensor(self.inp["tiers"], device=dev) if len(self.inp["tiers"]) else None
+        self.fwd = S.gather_target_forward(self.inp["target"])
+        self.ring = S.zos_ring(dev)
+        self.vmode = B.DSPARK_COMPACT if mode == "compact" else B.DSPARK_STATIC
+        self.launches = 2 * wl.gamma + (2 if mode == "compact" else 1) + (4 if self.tau > 0 else 2)
 
-    def draft_stage(it):
-        B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], tau, wl.seed, it, buf.tokens,
-                             buf.logit_x, buf.lse, buf.ws)
+    def draft(self, it):
+        inp, buf = self.inp, self.buf
+        self.B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], self.tau, self.wl.seed, it,
+                                  buf.tokens, buf.logit_x, buf.lse, buf.ws)
 
-    def conf_sched_pack_stage(it, zos):
+    def sched_pack(self, it, zos=False):
+        B, inp, buf = self.B, self.inp, self.buf
+        if self.mode == "static":
+            B.dspark_pack(None, inp["anchor"], buf.tokens, self.tiers, buf.cu, buf.ids, buf.req, buf.pos, buf.padded,
+                          buf.ws)
+            return
         B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], buf.tokens, inp["w"], inp["b"], inp["sts_T"],
                             buf.conf, buf.surv)
         if zos:
-            B.dspark_schedule_zos_select(buf.surv, sps, ring, it, buf.window, buf.K)
-            B.dspark_pack(buf.window, inp["anchor"], buf.tokens, tiers_dev, buf.cu, buf.ids, buf.req, buf.pos,
+            B.dspark_schedule_zos_select(buf.surv, self.sps, self.ring, it, buf.window, buf.K, buf.ws)
+            B.dspark_pack(buf.window, inp["anchor"], buf.tokens, self.tiers, buf.cu, buf.ids, buf.req, buf.pos,
                           buf.padded, buf.ws)
         else:  # the synchronous scheduler and the pack of its windows in one launch
-            B.dspark_schedule_pack(buf.surv, sps, SCHED, buf.window, buf.K, buf.theta, inp["anchor"], buf.tokens,
-                                   tiers_dev, buf.cu, buf.ids, buf.req, buf.pos, buf.padded, buf.ws)
+            B.dspark_schedule_pack(buf.surv, self.sps, self.sched, buf.window, buf.K, buf.theta, inp["anchor"],
+                                   buf.tokens, self.tiers, buf.cu, buf.ids, buf.req, buf.pos, buf.padded, buf.ws)
 
-    def verify_stage(it, zos):
+    def verify(self, it, zos=False, stream=None, side=None):
         # asynchronous scheduler: the budget for step it + 2 forks onto a second stream and
         # runs beside the verify, joined at the end of the stage
         if zos:
-            S.schedule_budget(buf, sps, ring, it, stream, side)
-        S.verify(inp, buf, tau, wl.seed, it, B.DSPARK_COMPACT)
+            self.S.schedule_budget(self.buf, self.sps, self.ring, it, stream, side)
+        self.S.verify(self.inp, self.buf, self.tau, self.wl.seed, it, self.vmode)
         if zos:
-            S.join_budget(stream, side)
+            self.S.join_budget(stream, side)
 
-    def count_tokens():
-        tokens_acc.add_((buf.acc_len.to(torch.int64) + 1).sum())
 
-    def measure(zos):
-        """Warm-up, graph capture and the timed steps of one scheduler variant."""
-        for w in range(args.warmup):  # eager, through the API
-            draft_stage(10_000 + w)
-            conf_sched_pack_stage(10_000 + w, zos)
-            fwd(buf)
-            verify_stage(10_000 + w, zos)
-            count_tokens()  # every op of the timed loop runs once before it (first-use set-up)
-        tokens_acc.zero_()
+def time_steps(path, steps, warmup, zos=False, world=1):
+    """Warm-up, graph capture and the timed steps of one path.  The timed steps replay CUDA
+    graphs of the API calls (one per stage and step, each with its own step counter); the L2 is
+    flushed (256 MB write) before every step, outside the timed segments, and the stand-in target
+    forward runs outside them too.  Returns per-step segment times [steps, 3] (draft + sched/pack,
+    verify, draft alone) in ms, tokens, packed rows and admitted slots summed over the steps, the
+    host enqueue time and the clock record."""
+    import torch
+    import torch.distributed as dist
+    B, buf, dev = path.B, path.buf, path.dev
+    stream = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev) if zos else None
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    acc = torch.zeros(3, dtype=torch.int64, device=dev)  # tokens, packed rows, admitted slots
 
-        # The timed steps replay CUDA graphs of the same API calls, one per stage and step,
-        # captured here with each step's own counter (the draws differ step to step), then
-        # replayed once untimed so that the timed replays find them resident.
-        graphs = []
-        for it in range(args.steps):
-            gs = [torch.cuda.CUDAGraph() for _ in range(3)]
-            with torch.cuda.graph(gs[0]):
-                draft_stage(it)
-            with torch.cuda.graph(gs[1]):
-                conf_sched_pack_stage(it, zos)
-            with torch.cuda.graph(gs[2]):
-                verify_stage(it, zos)
-            graphs.append(gs)
-        for gs in graphs:
+    def count():
+        acc[0].add_((buf.acc_len.to(torch.int64) + 1).sum())
+        acc[1].add_(buf.cu[-1].to(torch.int64))
+        acc[2].add_(buf.K[0].to(torch.int64))
+
+    if zos:
+        path.ring.fill_(-1)
+    for w in range(warmup):  # eager, through the API: every op of the timed loop runs once before it
+        path.draft(10_000 + w)
+        path.sched_pack(10_000 + w, zos)
+        path.fwd(buf)
+        path.verify(10_000 + w, zos, stream, side)
+        count()
+    graphs = []
+    for it in range(steps):
+        gs = [torch.cuda.CUDAGraph() for _ in range(3)]
+        with torch.cuda.graph(gs[0]):
+            path.draft(it)
+        with torch.cuda.graph(gs[1]):
+            path.sched_pack(it, zos)
+        with torch.cuda.graph(gs[2]):
+            path.verify(it, zos, torch.cuda.current_stream(dev), side)
+        graphs.append(gs)
+    for gs in graphs:  # once untimed, so that the timed replays find the graphs resident
+        gs[0].replay()
+        gs[1].replay()
+        path.fwd(buf)
+        gs[2].replay()
+    torch.cuda.synchronize(dev)
+    st = B.dspark_read_device_status(buf.ws)
+    if st != 0:
+        raise RuntimeError(f"{path.wl.name}: device status after warm-up: " + B.dspark_status_string(st))
+    acc.zero_()
+    buf.K.zero_()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev) as clk:
+        t_host = time.perf_counter()
+        for it in range(steps):
+            flush.fill_(it & 0xFF)  # L2 flush, outside the timed segments
+            e, gs = evs[it], graphs[it]
+            e[0].record(stream)
             gs[0].replay()
+            e[1].record(stream)
             gs[1].replay()
-            fwd(buf)
+            e[2].record(stream)
+            path.fwd(buf)  # the caller's target forward: outside the timed segments
+            e[3].record(stream)
             gs[2].replay()
+            e[4].record(stream)
+            count()
+        t_host = time.perf_counter() - t_host  # host time to enqueue (the device may still run)
         torch.cuda.synchronize(dev)
-        st = B.dspark_read_device_status(buf.ws)
-        if st != 0:
-            raise RuntimeError("device status after warm-up: " + B.dspark_status_string(st))
-        tokens_acc.zero_()
+    if world > 1:
+        dist.barrier()
+    seg = np.array([[e[0].elapsed_time(e[2]), e[3].elapsed_time(e[4]), e[0].elapsed_time(e[1])] for e in evs])
+    st = B.dspark_read_device_status(buf.ws)
+    if st != 0:
+        raise RuntimeError(f"{path.wl.name}: device status after the timed steps: " + B.dspark_status_string(st))
+    tokens, rows, slots = (int(x) for x in acc.tolist())
+    del graphs
+    return seg, tokens, rows, slots, t_host, clk.summary()
 
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-        with ClockSampler(dev) as clk:
-            t_host = time.perf_counter()
-            for it in range(args.steps):
-                flush.fill_(it & 0xFF)  # L2 flush, outside the timed segments
-                e, gs = evs[it], graphs[it]
-                e[0].record(stream)
-                gs[0].replay()
-                e[1].record(stream)
-                gs[1].replay()
-                e[2].record(stream)
-                fwd(buf)  # the caller's target forward: outside the timed segments
-                e[3].record(stream)
-                gs[2].replay()
-                e[4].record(stream)
-                count_tokens()
-            t_host = time.perf_counter() - t_host  # host time to enqueue (the device may still run)
-            torch.cuda.synchronize(dev)
-        if world > 1:
-            dist.barrier()
-        seg = np.array([[e[0].elapsed_time(e[2]), e[3].elapsed_time(e[4]), e[0].elapsed_time(e[1])] for e in evs])
-        st = B.dspark_read_device_status(buf.ws)
-        if st != 0:
-            raise RuntimeError("device status after the timed steps: " + B.dspark_status_string(st))
-        tokens = int(tokens_acc.item())
-        del graphs
-        return seg, tokens, t_host, clk.summary()
 
-    seg, tokens, t_host, clocks = measure(False)
-    step_ms = seg[:, 0] + seg[:, 1]
-    total_ms = float(step_ms.sum())
-    # the same steps under the asynchronous scheduler (budget from two steps back, computed on
-    # a second stream beside the verify; the select alone on the step's path)
-    zseg, ztokens, _, zclocks = measure(True)
-    ztotal_ms = float((zseg[:, 0] + zseg[:, 1]).sum())
-
-    # ---- end to end through the public API with host buffers (pinned), copies inside the timing.
-    # Every step copies its own inputs host -> device and reads its result back.  U, h and the
-    # anchors are double-buffered, so that the copy of step t + 1 (a second stream) runs while
-    # step t computes.  The target logits stay in host memory as the target model's output for
-    # every (request, position); each step's target forward reads back the packed layout
-    # (cu_seqlens) and copies exactly the rows that step verifies (dspark_copy_packed_rows_async).
-    # The timed region holds every copy and every step; each step's inputs exceed L2.
-    host = {k: inp[k].cpu().pin_memory() for k in ("U", "h", "anchor")}
+def time_e2e(path, steps):
+    """The same step end to end through the public API with host buffers (pinned), every copy
+    inside the timing: U, h and the anchors of each step copied host -> device on a second stream
+    one step ahead (double-buffered); the target logits of every (request, position) stay in
+    pinned host memory (the target model's output) and each step's target forward reads the packed
+    layout back (cu_seqlens, after the pack) and copies exactly the rows that step verifies
+    (dspark_copy_packed_rows_async); out_tokens and acc_len come back every step.  Returns
+    (tokens/s, h2d bytes per step, d2h bytes per step, steps)."""
+    import torch
+    B, S, buf, inp, wl, dev = path.B, path.S, path.buf, path.inp, path.wl, path.dev
+    bs, gamma = wl.bs, wl.gamma
+    stream = torch.cuda.current_stream(dev)
+    keys = ("U", "h", "anchor") if path.mode == "compact" else ("U", "anchor")
+    host = {k: inp[k].cpu().pin_memory() for k in keys}
     host_target = inp["target"].cpu().pin_memory()
     cu_host = torch.empty(bs + 1, dtype=torch.int32).pin_memory()
     target_rows = []
@@ -402,10 +473,8 @@ def run_ours(args, rank: int, world: int):
     inps = [inp, dict(inp)]
     for k in host:
         inps[1][k] = torch.empty_like(inp[k])
-    fwds = [host_target_forward, host_target_forward]
-    e2e_steps = max(2, min(args.steps, 10))
-    outs = [torch.empty((bs, gamma + 1), dtype=torch.int32).pin_memory() for _ in range(e2e_steps)]
-    accs = [torch.empty(bs, dtype=torch.int32).pin_memory() for _ in range(e2e_steps)]
+    outs = [torch.empty((bs, gamma + 1), dtype=torch.int32).pin_memory() for _ in range(steps)]
+    accs = [torch.empty(bs, dtype=torch.int32).pin_memory() for _ in range(steps)]
     bo = outs[0].numel() * 4 + accs[0].numel() * 4 + cu_host.numel() * 4
     cstream = torch.cuda.Stream(dev)
     copied = [torch.cuda.Event() for _ in range(2)]
@@ -424,45 +493,109 @@ def run_ours(args, rank: int, world: int):
     e0.record(stream)
     cstream.wait_stream(stream)
     issue_copy(0)
-    for it in range(e2e_steps):
-        if it + 1 < e2e_steps:
+    for it in range(steps):
+        if it + 1 < steps:
             issue_copy(it + 1)
         stream.wait_event(copied[it % 2])
-        S.run_step(inps[it % 2], buf, sps, fwds[it % 2], tau, wl.seed, 20_000 + it, B.DSPARK_COMPACT, SCHED,
-                   tiers=tiers_dev)
+        S.run_step(inps[it % 2], buf, path.sps, host_target_forward, path.tau, wl.seed, 20_000 + it, path.vmode,
+                   path.sched, tiers=path.tiers)
         released[it % 2].record(stream)
         outs[it].copy_(buf.out_tokens, non_blocking=True)
         accs[it].copy_(buf.acc_len, non_blocking=True)
     e1.record(stream)
     e1.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    e2e_tokens = sum(int((a.to(torch.int64) + 1).sum()) for a in accs)
+    ms = e0.elapsed_time(e1)
+    tokens = sum(int((a.to(torch.int64) + 1).sum()) for a in accs)
     row_bytes = host_target[0, 0].numel() * host_target.element_size()
     bi = sum(t.numel() * t.element_size() for t in host.values()) + int(np.mean(target_rows)) * row_bytes
+    st = B.dspark_read_device_status(buf.ws)
+    if st != 0:
+        raise RuntimeError(f"{wl.name}: device status after the end-to-end steps: " + B.dspark_status_string(st))
+    del host, host_target
+    return tokens / (ms * 1e-3), bi, bo, steps, ms
 
-    # aggregate over ranks: max time, summed tokens
-    (total_ms, e2e_ms, ztotal_ms), (tokens, e2e_tokens, ztokens) = aggregate_over_ranks(
-        [total_ms, e2e_ms, ztotal_ms], [tokens, e2e_tokens, ztokens], dev)
-    tokens, e2e_tokens, ztokens = int(tokens), int(e2e_tokens), int(ztokens)
 
-    obs = measure_observability(args, inp, buf, tau, wl, dev, stream, tiers_dev, fwd)
-
-    hbm, bf16, peak_kind = _peaks()
-    draft_bytes = draft_block_bytes(bs, gamma, V, r, torch.cuda.get_device_properties(dev).multi_processor_count)
-    draft_ms = float(seg[:, 2].mean())
-    achieved = draft_bytes / (draft_ms * 1e-3) / 1e9
-    traffic = _profiled_traffic()
-    # per step: gamma vocabulary passes + gamma selects, confidence, schedule+pack (one launch),
-    # verify rows, decide, and at temperature > 0 the decision statistics and select
-    launches_per_step = 2 * gamma + 2 + (4 if tau > 0 else 2)
+def measure(path, steps, warmup, e2e_steps, profile_key=None, world=1):
+    """Device-timed steps, end-to-end steps and the rooflines of one path, as a result dict."""
+    seg, tokens, rows, slots, t_host, clocks = time_steps(path, steps, warmup, world=world)
+    step_ms = seg[:, 0] + seg[:, 1]
+    (total_ms,), (tokens_all,) = aggregate_over_ranks([float(step_ms.sum())], [tokens], path.dev)
+    stage_ms = {"draft": float(seg[:, 2].mean()), "conf_sched_pack": float((seg[:, 0] - seg[:, 2]).mean()),
+                "verify": float(seg[:, 1].mean())}
+    e2e_v, bi, bo, e_steps, e_ms = time_e2e(path, e2e_steps)
+    (e_ms_all,), (e2e_tok,) = aggregate_over_ranks([e_ms], [e2e_v * e_ms * 1e-3], path.dev)
+    wl = path.wl
     return {
+        "value": tokens_all / (total_ms * 1e-3), "unit": "tokens/s", "steps": steps, "ms_per_step": total_ms / steps,
+        "median_ms_per_step": float(np.median(step_ms)),
+        "value_median": tokens / steps / (float(np.median(step_ms)) * 1e-3),
+        "tokens_per_step": tokens / steps, "packed_rows_per_step": rows / steps,
+        "admitted_slots_per_step": slots / steps if path.mode == "compact" else wl.bs * wl.gamma,
+        "stage_ms": stage_ms, "host_enqueue_ms_per_step": t_host * 1e3 / steps,
+        "roofline": rooflines(wl, stage_ms, rows / steps, path.tau, profile_key),
+        "e2e": {"value": e2e_tok / (e_ms_all * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo, "steps": e_steps},
+        "gpu_launches": path.launches * steps, "clocks": clocks,
+    }
+
+
+def config_lines(args, dev):
+    """Every other configuration of the pages' workloads, one result each: Qwen3-4B-shaped (bs 64,
+    compact), the DeepSeek-V4-shaped sweep (bs 1..256, static and compact budgets) and the long
+    block (bs 128, gamma 15, temperature 1 and greedy)."""
+    import gc
+
+    import torch
+
+    from speculative_decoding_draft_markov_gb300 import inputs as I
+    runs = [("qwen3_4b", I.WORKLOADS["qwen3_4b"], "compact", None)]
+    for b in I.DSV4_BATCHES:
+        for mode in ("static", "compact"):
+            runs.append((f"dsv4_bs{b}_{mode}", I.dsv4(b), mode, None))
+    runs += [("long_block_t1", I.WORKLOADS["long_block"], "compact", 1.0),
+             ("long_block_greedy", I.WORKLOADS["long_block"], "compact", 0.0)]
+    out = []
+    for name, wl, mode, tau in runs:
+        if args.workload not in ("all", name, wl.name):
+            continue
+        path = Path(wl, dev, mode, tau)
+        r = measure(path, args.config_steps, args.warmup, 4)
+        r = {"workload": name, "bs": wl.bs, "gamma": wl.gamma, "V": wl.V, "r": wl.r, "d": wl.d, "mode": mode,
+             "temperature": path.tau, "scheduler": "global-argmax" if mode == "compact" else "none (whole block)",
+             **r}
+        out.append(r)
+        del path
+        gc.collect()
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, rank: int, world: int):
+    import torch
+
+    from speculative_decoding_draft_markov_gb300 import inputs as I
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl = I.WORKLOADS[WORKLOAD].with_(seed=I.WORKLOADS[WORKLOAD].seed + 1000 * rank)
+    path = Path(wl, dev, "compact")
+    head = measure(path, args.steps, args.warmup, max(2, min(args.steps, 10)), profile_key=WORKLOAD, world=world)
+    # the same steps under the asynchronous scheduler (budget from two steps back, computed on a
+    # second stream beside the verify; the select alone on the step's path)
+    zseg, ztokens, _, _, _, zclocks = time_steps(path, args.steps, args.warmup, zos=True, world=world)
+    (ztotal_ms,), (ztokens,) = aggregate_over_ranks([float((zseg[:, 0] + zseg[:, 1]).sum())], [ztokens], dev)
+    obs = measure_observability(args, path.inp, path.buf, path.tau, wl, dev, torch.cuda.current_stream(dev),
+                                path.tiers, path.fwd)
+    res = {
         "metric": METRIC,
-        "value": tokens / (total_ms * 1e-3),
+        "value": head["value"],
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": total_ms / args.steps,
+        "ms_per_step": head["ms_per_step"],
+        "median_ms_per_step": head["median_ms_per_step"],
+        "value_median": head["value_median"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -471,27 +604,22 @@ def run_ours(args, rank: int, world: int):
                 "sigma 0.5/1/2 by thirds)",
         "config": {"workload": "mixed_bs256: bs=256, gamma=7, V=151936, r=256, d=4096, compact verify, "
                                "temperature 1, sawtooth cost table with tiers every 64 to 2048, global-argmax scheduler",
-                   "global_batch": bs * world, "l2": "flushed between steps (256 MB write)",
+                   "global_batch": wl.bs * world, "l2": "flushed between steps (256 MB write)",
                    "timed": "draft+confidence+schedule+pack and verify segments; target forward excluded; "
                             "each stage of each timed step a captured CUDA graph of its API calls",
                    "parallelism": f"replicas x{world}"},
-        "tokens_per_step": tokens / args.steps / world,
-        "host_enqueue_ms_per_step": t_host * 1e3 / args.steps,
-        "stage_ms": {"draft": draft_ms, "conf_sched_pack": float((seg[:, 0] - seg[:, 2]).mean()),
-                     "verify": float(seg[:, 1].mean())},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": traffic,
-                     "kernel": "dspark_draft_block: gamma tensor-core vocabulary passes (draft_tc_kernel, "
-                               "the dominant kernel) + gamma selects, one C-ABI call, events around it",
-                     "algorithmic_bytes": draft_bytes, "peak_kind": peak_kind},
-        "e2e": {"value": e2e_tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
-                "d2h_bytes_per_step": bo, "steps": e2e_steps,
-                "note": "U, h, anchors copied from pinned host memory every step on a second stream, one step "
-                        "ahead (double-buffered); the target forward copies the step's packed target rows "
-                        "from pinned host memory after the pack (cu_seqlens read back); host-to-device "
-                        "copies run at ~210 GB/s on this box"},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
+        "tokens_per_step": head["tokens_per_step"] / world,
+        "packed_rows_per_step": head["packed_rows_per_step"],
+        "admitted_slots_per_step": head["admitted_slots_per_step"],
+        "host_enqueue_ms_per_step": head["host_enqueue_ms_per_step"],
+        "stage_ms": head["stage_ms"],
+        "roofline": head["roofline"],
+        "e2e": dict(head["e2e"], note="U, h, anchors copied from pinned host memory every step on a second stream, "
+                                      "one step ahead (double-buffered); the target forward copies the step's "
+                                      "packed target rows from pinned host memory after the pack (cu_seqlens read "
+                                      "back)"),
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
         "observability": obs,
         "zos": {"value": ztokens / (ztotal_ms * 1e-3), "unit": "tokens/s", "ms_per_step": ztotal_ms / args.steps,
                 "tokens_per_step": ztokens / args.steps / world,
@@ -500,8 +628,15 @@ def run_ours(args, rank: int, world: int):
                              "verify_with_budget": float(zseg[:, 1].mean())},
                 "scheduler": "asynchronous: budget from the survival two steps back (global search, second "
                              "stream beside the verify), radix top-K select on the step's path",
-                "gpu_launches": (launches_per_step + 2) * args.steps, "clocks": zclocks},
+                "gpu_launches": (path.launches + 2) * args.steps, "clocks": zclocks},
     }
+    del path
+    if not args.no_configs:
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        res["configs"] = config_lines(args, dev)
+    return res
 
 
 def measure_observability(args, inp, buf, tau, wl, dev, stream, tiers_dev, fwd):
@@ -572,21 +707,22 @@ def measure_observability(args, inp, buf, tau, wl, dev, stream, tiers_dev, fwd):
 
 
 def run_reference(args):
-    """The CPU oracle as the reference arm: each step is a bounded sample of the workload."""
-    n_req = 4
-    toks, secs = 0, 0.0
-    for s in range(args.warmup + args.steps):
-        t, dt = _oracle_sample(n_req, s)
-        if s >= args.warmup:
-            toks += t
-            secs += dt
+    """The CPU oracle as the reference arm, on every host core: each step is a bounded sample of
+    the workload (its first 32 requests, full vocabulary, all five stages)."""
+    n_req = 32
+    res, cores = _oracle_steps(WORKLOAD, n_req, range(args.warmup + args.steps))
+    res = res[args.warmup:]
+    toks = sum(r[0] for r in res)
+    secs = sum(r[1] for r in res)
     v = toks / secs
     return {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "median_ms_per_step": float(np.median([r[1] for r in res])) * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": "mixed_bs256 sample: first 4 of the 256 requests, full V=151936, gamma=7"},
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{n_req} requests per step, {args.steps} timed steps"},
+            "config": {"workload": f"mixed_bs256 sample: first {n_req} of the 256 requests, full V=151936, gamma=7"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "nproc": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{n_req} requests per step (oracle draft and verify in {cores} worker "
+                                       f"processes), {args.steps} timed steps after {args.warmup} warm-up steps"},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -624,8 +760,8 @@ def run_profile_case(args):
         ring.fill_(200)
 
         def run(it):
-            B.dspark_schedule(buf.surv, sps, SCHED, buf.window, buf.K, buf.theta)
-            B.dspark_schedule_zos_select(buf.surv, sps, ring, it, buf.window, buf.K)
+            B.dspark_schedule(buf.surv, sps, SCHED, buf.window, buf.K, buf.theta, buf.ws)
+            B.dspark_schedule_zos_select(buf.surv, sps, ring, it, buf.window, buf.K, buf.ws)
     elif args.profile_case == "draft":
         def run(it):
             B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], wl.temperature, wl.seed, it,
@@ -698,10 +834,14 @@ def run_observe_case(args, dev):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="all",
+                    help="the configurations measured after the headline one: all (default), none, or one name "
+                         "(qwen3_4b, dsv4_bs<b>_<static|compact>, long_block_t1, long_block_greedy)")
+    ap.add_argument("--config-steps", type=int, default=20, help="timed steps of each further configuration")
     ap.add_argument("--profile-case", choices=["draft", "verify", "observe", "schedule"], default=None,
                     help="run one stage of the workload (small gamma) for an ncu capture; no JSON contract")
     ap.add_argument("--gamma", type=int, default=2, help="block length of --profile-case")
@@ -710,6 +850,7 @@ def main():
         run_profile_case(args)
         return
     args.warmup = max(args.warmup, 3)
+    args.no_configs = args.workload == "none"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -176,12 +176,17 @@ DSPARK_API int dspark_confidence(const void* h, const void* W1, int dtype, const
  * EARLY_STOP: K* = first K with Theta(K+1) <= Theta(K) (else the last K);
  * GLOBAL_ARGMAX: K* = smallest K maximising Theta.  window[r] = admitted slots of r.
  *   surv     device [bs, gamma] fp32, non-increasing along each row, in [0, 1]
- *   sps      device [m_max + 1] fp64 (dspark_build_sps), m_max >= bs
+ *   sps      device [m_max + 1] fp64 (dspark_build_sps), m_max >= bs; the entries the search
+ *            reads, sps[bs .. bs + Kmax], must be finite, >= 0 and non-increasing in M
  *   window   device [bs] int32 out;  K_out device int32 out;  theta_out device fp64 out
+ *   ws       the step's workspace (>= 256 bytes); only its status word is used, updated
+ *            atomically, so a call on another stream may share it.
+ * Device error (status word, EINVAL): a table entry the search reads that is negative, not
+ * finite, or above the entry before it (the outputs are still written, from the table as given).
  * Limits: bs * gamma <= 4096.  One thread block; no host readback. */
 DSPARK_API int dspark_schedule(const float* surv, int bs, int gamma, const double* sps, int m_max,
                     int mode, int32_t* window, int32_t* K_out, double* theta_out,
-                    dspark_stream_t stream);
+                    void* ws, size_t ws_bytes, dspark_stream_t stream);
 
 /* S3 under zero-overhead (asynchronous) scheduling ([SUMMARY] "Infra", scheduler bullet;
  * [SGLANG] "ZOS"): the verify budget of step t is predicted from the survival of step t - 2,
@@ -196,14 +201,16 @@ DSPARK_API int dspark_schedule(const float* surv, int bs, int gamma, const doubl
  * Ordering, the caller's: select(step) before budget(step) (both touch slot step & 1), and
  * budget(step) before select(step + 2).  On one stream in that order this holds; the budget
  * call may run on a second stream, off the step's critical path, joined by events.
- *   surv, sps, m_max, window, K_out as dspark_schedule;  budget_ring device [2] int32
+ *   surv, sps, m_max, window, K_out, ws as dspark_schedule (the table check applies whenever
+ *   the global search runs);  budget_ring device [2] int32
  * Limits: bs * gamma <= 4096.  One thread block each; no host readback. */
 DSPARK_API int dspark_schedule_zos_select(const float* surv, int bs, int gamma, const double* sps,
                                int m_max, const int32_t* budget_ring, uint64_t step,
-                               int32_t* window, int32_t* K_out, dspark_stream_t stream);
-DSPARK_API int dspark_schedule_zos_budget(const float* surv, int bs, int gamma, const double* sps,
-                               int m_max, int32_t* budget_ring, uint64_t step,
+                               int32_t* window, int32_t* K_out, void* ws, size_t ws_bytes,
                                dspark_stream_t stream);
+DSPARK_API int dspark_schedule_zos_budget(const float* surv, int bs, int gamma, const double* sps,
+                               int m_max, int32_t* budget_ring, uint64_t step, void* ws,
+                               size_t ws_bytes, dspark_stream_t stream);
 
 /* S4. Ragged cu_seqlens packing rounded up to a captured graph tier ([SGLANG] "Ragged verify
  * under full CUDA graphs", Fig. 2; [VLLM] "Graph Capture", "CUDA Graph Padding").
@@ -215,16 +222,16 @@ DSPARK_API int dspark_schedule_zos_budget(const float* surv, int bs, int gamma, 
  *   tiers    device [n_tiers] int32 strictly increasing;  cap = rows of ids/req/pos
  *   cu_seqlens device [bs+1] int32 out;  ids, req, pos device [cap] int32 out
  *   padded_total device [1] int32 out (-1 on a device-side error)
- * Device errors (status word, EINVAL): l_r outside [0, gamma], M beyond the largest tier,
- * padded > cap. */
+ * Device errors (status word, EINVAL; padded_total = -1, no rows written): l_r outside
+ * [0, gamma], tiers not positive and strictly increasing, M beyond the largest tier, padded > cap. */
 DSPARK_API int dspark_pack(const int32_t* window, const int32_t* anchor, const int32_t* tokens,
                 int bs, int gamma, const int32_t* tiers, int n_tiers, int cap,
                 int32_t* cu_seqlens, int32_t* ids, int32_t* req, int32_t* pos,
                 int32_t* padded_total, void* ws, size_t ws_bytes, dspark_stream_t stream);
 
 /* S3 then S4 in one launch: exactly dspark_schedule (window required) followed by dspark_pack
- * of the windows it wrote, with the arguments, outputs and errors of both; one kernel boundary
- * fewer on the step's path. */
+ * of the windows it wrote, with the arguments, outputs and errors of both (device checks of the
+ * table and of the tiers included); one kernel boundary fewer on the step's path. */
 DSPARK_API int dspark_schedule_pack(const float* surv, int bs, int gamma, const double* sps, int m_max,
                                     int mode, int32_t* window, int32_t* K_out, double* theta_out,
                                     const int32_t* anchor, const int32_t* tokens, const int32_t* tiers,
@@ -276,10 +283,13 @@ DSPARK_API int dspark_verify(const void* target, int dtype, const int32_t* cu_se
  * fixes its device footprint at start-up and forbids later allocation.  Same computation,
  * arguments and limits as dspark_draft_block, without ws / ws_bytes; it allocates nothing.
  *   Scratch: a fixed 8 MiB array inside the library (every GPU that loads the library holds it
- *   until exit).  Sizes whose scratch (256 B + bs * ceil(V / 128) * 16 B) exceeds it are rejected
- *   with DSPARK_EUNSUPPORTED -- e.g. bs = 256 allows V up to about 262,000.
+ *   until exit).  A call needs 256 B + bs * n * 16 B of it, n = ceil(V / 128) on the tensor-core
+ *   pass (bf16 with r = 64, 128 or 256) and n = ceil(V / 64) on the CUDA-core pass (fp32, or
+ *   r = 32); sizes needing more are rejected with DSPARK_EUNSUPPORTED.  At bs = 256 that allows
+ *   V <= 262,016 on the tensor-core pass and V <= 131,008 on the CUDA-core pass.
  *   The first call on a device looks up the array's device address (once per device, with that
- *   device current); make that first call before any stream capture.
+ *   device current); make that first call before any stream capture.  The address is kept for
+ *   the life of the process: cudaDeviceReset between calls is not supported.
  *   All calls share the array and it keeps the last call's contents: calls whose work can
  *   overlap on the GPU (other streams, other host threads) race and must be serialised.
  *   device_status: device uint32 or NULL.  If given, device-side errors (a wait timeout) are

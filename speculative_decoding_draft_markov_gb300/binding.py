@@ -36,9 +36,9 @@ _SIGS = {
                                         _vp, _vp, _vp, _vp, _vp]),
     "dspark_confidence": (_i, [_vp, _vp, _i, _vp, _vp, _vp, _f, _vp, _i, _i, _i, _i, _i,
                                _vp, _vp, _vp, _vp]),
-    "dspark_schedule": (_i, [_vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp]),
-    "dspark_schedule_zos_select": (_i, [_vp, _i, _i, _vp, _i, _vp, _u64, _vp, _vp, _vp]),
-    "dspark_schedule_zos_budget": (_i, [_vp, _i, _i, _vp, _i, _vp, _u64, _vp]),
+    "dspark_schedule": (_i, [_vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dspark_schedule_zos_select": (_i, [_vp, _i, _i, _vp, _i, _vp, _u64, _vp, _vp, _vp, _sz, _vp]),
+    "dspark_schedule_zos_budget": (_i, [_vp, _i, _i, _vp, _i, _vp, _u64, _vp, _sz, _vp]),
     "dspark_pack": (_i, [_vp, _vp, _vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dspark_schedule_pack": (_i, [_vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp,
                                   _vp, _vp, _vp, _sz, _vp]),
@@ -198,23 +198,24 @@ def dspark_confidence(h, W1, anchor, tokens, w, b, sts_T, conf, surv, stream=Non
                                    _stream(stream)), "dspark_confidence")
 
 
-def dspark_schedule(surv, sps, mode, window, K_out, theta_out, stream=None):
+def dspark_schedule(surv, sps, mode, window, K_out, theta_out, ws, stream=None):
     bs, gamma = surv.shape
     _check(lib().dspark_schedule(_p(surv), bs, gamma, _p(sps), sps.numel() - 1, int(mode), _p(window),
-                                 _p(K_out), _p(theta_out), _stream(stream)), "dspark_schedule")
+                                 _p(K_out), _p(theta_out), _p(ws), ws.numel(), _stream(stream)), "dspark_schedule")
 
 
-def dspark_schedule_zos_select(surv, sps, budget_ring, step, window, K_out, stream=None):
+def dspark_schedule_zos_select(surv, sps, budget_ring, step, window, K_out, ws, stream=None):
     bs, gamma = surv.shape
     _check(lib().dspark_schedule_zos_select(_p(surv), bs, gamma, _p(sps), sps.numel() - 1, _p(budget_ring),
-                                            int(step), _p(window), _p(K_out), _stream(stream)),
+                                            int(step), _p(window), _p(K_out), _p(ws), ws.numel(), _stream(stream)),
            "dspark_schedule_zos_select")
 
 
-def dspark_schedule_zos_budget(surv, sps, budget_ring, step, stream=None):
+def dspark_schedule_zos_budget(surv, sps, budget_ring, step, ws, stream=None):
     bs, gamma = surv.shape
     _check(lib().dspark_schedule_zos_budget(_p(surv), bs, gamma, _p(sps), sps.numel() - 1, _p(budget_ring),
-                                            int(step), _stream(stream)), "dspark_schedule_zos_budget")
+                                            int(step), _p(ws), ws.numel(), _stream(stream)),
+           "dspark_schedule_zos_budget")
 
 
 def dspark_pack(window, anchor, tokens, tiers, cu_seqlens, ids, req, pos, padded_total, ws, stream=None):

@@ -182,37 +182,42 @@ int dspark_confidence(const void* h, const void* W1, int dtype, const int32_t* a
 }
 
 int dspark_schedule(const float* surv, int bs, int gamma, const double* sps, int m_max, int mode,
-                    int32_t* window, int32_t* K_out, double* theta_out, dspark_stream_t stream) {
+                    int32_t* window, int32_t* K_out, double* theta_out, void* ws, size_t ws_bytes,
+                    dspark_stream_t stream) {
   if (!surv || !sps || !window || !K_out || !theta_out) return DSPARK_EINVAL;
   if (bs < 1 || gamma < 1 || m_max < bs) return DSPARK_EINVAL;
   if (mode != DSPARK_SCHED_EARLY_STOP && mode != DSPARK_SCHED_GLOBAL_ARGMAX) return DSPARK_EINVAL;
   if (bs > DSPARK_MAX_BS || gamma > DSPARK_MAX_GAMMA || bs * gamma > 4096) return DSPARK_EUNSUPPORTED;
   if (!al(surv, 4) || !al(sps, 8) || !al(window, 4) || !al(K_out, 4) || !al(theta_out, 8))
     return DSPARK_EINVAL;
+  if (!ws || !al(ws, 256) || ws_bytes < 256) return DSPARK_EWORKSPACE;
   return cuda_status(launch_schedule(surv, bs, gamma, sps, m_max, mode, window, K_out, theta_out,
-                                     reinterpret_cast<cudaStream_t>(stream)));
+                                     static_cast<uint32_t*>(ws), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int dspark_schedule_zos_select(const float* surv, int bs, int gamma, const double* sps, int m_max,
                                const int32_t* budget_ring, uint64_t step, int32_t* window,
-                               int32_t* K_out, dspark_stream_t stream) {
+                               int32_t* K_out, void* ws, size_t ws_bytes, dspark_stream_t stream) {
   if (!surv || !sps || !budget_ring || !window || !K_out) return DSPARK_EINVAL;
   if (bs < 1 || gamma < 1 || m_max < bs) return DSPARK_EINVAL;
   if (bs > DSPARK_MAX_BS || gamma > DSPARK_MAX_GAMMA || bs * gamma > 4096) return DSPARK_EUNSUPPORTED;
   if (!al(surv, 4) || !al(sps, 8) || !al(budget_ring, 4) || !al(window, 4) || !al(K_out, 4))
     return DSPARK_EINVAL;
+  if (!ws || !al(ws, 256) || ws_bytes < 256) return DSPARK_EWORKSPACE;
   return cuda_status(launch_zos_select(surv, bs, gamma, sps, m_max, budget_ring, step, window, K_out,
-                                       reinterpret_cast<cudaStream_t>(stream)));
+                                       static_cast<uint32_t*>(ws), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int dspark_schedule_zos_budget(const float* surv, int bs, int gamma, const double* sps, int m_max,
-                               int32_t* budget_ring, uint64_t step, dspark_stream_t stream) {
+                               int32_t* budget_ring, uint64_t step, void* ws, size_t ws_bytes,
+                               dspark_stream_t stream) {
   if (!surv || !sps || !budget_ring) return DSPARK_EINVAL;
   if (bs < 1 || gamma < 1 || m_max < bs) return DSPARK_EINVAL;
   if (bs > DSPARK_MAX_BS || gamma > DSPARK_MAX_GAMMA || bs * gamma > 4096) return DSPARK_EUNSUPPORTED;
   if (!al(surv, 4) || !al(sps, 8) || !al(budget_ring, 4)) return DSPARK_EINVAL;
+  if (!ws || !al(ws, 256) || ws_bytes < 256) return DSPARK_EWORKSPACE;
   return cuda_status(launch_zos_budget(surv, bs, gamma, sps, m_max, budget_ring, step,
-                                       reinterpret_cast<cudaStream_t>(stream)));
+                                       static_cast<uint32_t*>(ws), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int dspark_pack(const int32_t* window, const int32_t* anchor, const int32_t* tokens, int bs,

@@ -65,6 +65,7 @@ struct Bars {
   uint64_t a_ready;  // A is in TMEM (one arrival per warp of epilogue set 0)
   uint32_t tmem_base;
   int abort;
+  int mma_pending;   // the issuer's MMAs that nobody has waited for (set by the issuing thread)
   DecideEntry xch[kBM];  // warp set 1's partial draw of each row, merged by set 0 at the end
 };
 
@@ -122,6 +123,20 @@ __device__ __forceinline__ void unpack8(const uint4 q, float* x) {
   x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
 }
 
+// Warp 1 at the end of the kernel: free the tensor memory.  An epilogue that gave up has not
+// waited for every accumulator, so then the MMAs still in flight are waited for (bounded) first.
+// Out of line: it takes no registers from the kernel's loops.
+__device__ __noinline__ void free_tmem(Bars* bar, uint32_t tmem_base, int lane) {
+  if (lane == 0 && bar->mma_pending && bar->abort) {
+    tc::mma_commit(tc::smem_u32(&bar->drain));
+    const volatile int never = 0;
+    tc::mbar_wait_bounded(tc::smem_u32(&bar->drain), 0, tc::deadline_after_ns(200000000ull), &never);
+  }
+  __syncwarp();
+  tc::tc_fence_after();
+  tc::tmem_dealloc(tmem_base, kTmemCols);
+}
+
 __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
                                                                  const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -160,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
     tc::mbar_init(tc::smem_u32(&bar->drain), 1);
     tc::mbar_init(tc::smem_u32(&bar->a_ready), 4);
     bar->abort = 0;
+    bar->mma_pending = 0;
     tc::fence_mbar_init();
     tc::prefetch_tensormap(&tmap_w2);
   }
@@ -277,6 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
           const volatile int never = 0;
           tc::mbar_wait_bounded(tc::smem_u32(&bar->drain), 0, tc::deadline_after_ns(200000000ull), &never);
         }
+      } else {
+        bar->mma_pending = issued;  // complete only once the epilogue has consumed every accumulator
       }
     }
   } else if (warp >= 2 + kEpiWarps) {
@@ -467,10 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
 
   tc::tc_fence_before();
   asm volatile("bar.sync 1, %0;" ::"n"(kRest) : "memory");
-  if (warp == 1) {
-    tc::tc_fence_after();
-    tc::tmem_dealloc(tmem_base, kTmemCols);
-  }
+  if (warp == 1) free_tmem(bar, tmem_base, lane);
   if (warp >= 2 && warp < 6) {
     // warp set 0 merges the other set's partial draw of the same row and writes the CTA's
     // entry (request grow, slot c0)

@@ -14,6 +14,9 @@
 // the first call of this entry point on a device performs that lookup, so that first call
 // should come before any stream capture.
 //
+// The device address is cached per device for the life of the process: a cudaDeviceReset
+// between calls destroys the context the address belongs to, and is not supported.
+//
 // Every call shares the one array and the last call's contents stay in it.  The status word
 // is cleared at the start of each call (when the caller does not pass its own); the chunk
 // statistics need no clearing (each position writes all of them before reading any).  Calls
@@ -72,9 +75,12 @@ extern "C" DSPARK_API int dspark_draft_block_noalloc(
       !aligned(tokens, 4) || !aligned(logit_x, 4) || !aligned(lse, 4) || !aligned(device_status, 4))
     return DSPARK_EINVAL;
 
-  // the scratch this call needs: status word + 16 bytes per (request, draft chunk)
+  // The scratch this call needs: the status word, then 16 bytes per (request, slot) of the
+  // pass that will run.  The tensor-core pass (bf16, r a multiple of 64) writes one slot per
+  // CTA column, at most one per 128-id tile; the CUDA-core pass one per 64-id draft chunk.
   const WsLayout L = ws_layout(bs, gamma, V);
-  const size_t need = L.stats + draft_stats_bytes(bs, n_draft_chunks(V));
+  const bool tc = draft_tc_supported(dtype, bs, V, r);
+  const size_t need = L.stats + draft_stats_bytes(bs, tc ? L.n_chunks : n_draft_chunks(V));
   if (need > kNoAllocScratchBytes) return DSPARK_EUNSUPPORTED;
 
   void* scratch = nullptr;
@@ -88,7 +94,6 @@ extern "C" DSPARK_API int dspark_draft_block_noalloc(
 
   const int greedy = temperature == 0.f;
   const float inv_tau = greedy ? 1.f : static_cast<float>(1.0 / static_cast<double>(temperature));
-  const bool tc = draft_tc_supported(dtype, bs, V, r);
   for (int k = 1; k <= gamma; ++k) {
     int n_slots = n_draft_chunks(V);  // the CUDA-core pass: one slot per draft chunk
     cudaError_t e = tc ? launch_draft_stats_tc(U, W1, W2t, anchor, tokens, bs, gamma, V, r, k, inv_tau, greedy,

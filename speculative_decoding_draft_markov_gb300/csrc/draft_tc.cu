@@ -64,6 +64,7 @@ struct Barriers {
   uint64_t a_ready;  // the A operand is in shared memory (one arrival per epilogue warp)
   uint32_t tmem_base;
   int abort;
+  int mma_pending;   // the issuer's MMAs that nobody has waited for (set by the issuing thread)
   int xrow[kBM];     // W1 row of each A row (-1: zero row)
   float4 xch[kBM];   // warp set 1's entry of each row, merged by set 0 at the end
 };
@@ -131,6 +132,20 @@ __device__ __forceinline__ float row_sum_exp2(const float* v, int valid, float m
   return ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
 }
 
+// Warp 1 at the end of the kernel: free the tensor memory.  An epilogue that gave up has not
+// waited for every accumulator, so then the MMAs still in flight are waited for (bounded) first.
+// Out of line: it takes no registers from the kernel's loops.
+__device__ __noinline__ void free_tmem(Barriers* bar, uint32_t tmem_base, int lane) {
+  if (lane == 0 && bar->mma_pending && bar->abort) {
+    tc::mma_commit(tc::smem_u32(&bar->drain));
+    const volatile int never = 0;
+    tc::mbar_wait_bounded(tc::smem_u32(&bar->drain), 0, tc::deadline_after_ns(200000000ull), &never);
+  }
+  __syncwarp();
+  tc::tc_fence_after();
+  tc::tmem_dealloc(tmem_base, kTmemCols);
+}
+
 __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
                                                                 const __grid_constant__ CUtensorMap tmap_u,
                                                                 const Params p) {
@@ -170,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     tc::mbar_init(tc::smem_u32(&bar->drain), 1);
     tc::mbar_init(tc::smem_u32(&bar->a_ready), kEpiWarps);
     bar->abort = 0;
+    bar->mma_pending = 0;
     tc::fence_mbar_init();
     tc::prefetch_tensormap(&tmap_w2);
     tc::prefetch_tensormap(&tmap_u);
@@ -275,6 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
           const volatile int never = 0;
           tc::mbar_wait_bounded(tc::smem_u32(&bar->drain), 0, tc::deadline_after_ns(200000000ull), &never);
         }
+      } else {
+        bar->mma_pending = issued;  // complete only once the epilogue has consumed every accumulator
       }
     }
   } else {
@@ -411,10 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
 
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
-    tc::tc_fence_after();
-    tc::tmem_dealloc(tmem_base, kTmemCols);
-  }
+  if (warp == 1) free_tmem(bar, tmem_base, lane);
   if (warp >= 2 && warp < 6) {
     // warp set 0 merges the other set's entry of the same row and writes the CTA's entry
     // (request grow, slot c0)

@@ -45,10 +45,10 @@ cudaError_t launch_confidence(int dtype, const void* h, const void* W1, const in
                               float* z_out, cudaStream_t s);
 cudaError_t launch_schedule(const float* surv, int bs, int gamma, const double* sps, int m_max,
                             int mode, int32_t* window, int32_t* K_out, double* theta_out,
-                            cudaStream_t s);
+                            uint32_t* status, cudaStream_t s);
 cudaError_t launch_zos_select(const float* surv, int bs, int gamma, const double* sps, int m_max,
                               const int32_t* ring, uint64_t step, int32_t* window, int32_t* K_out,
-                              cudaStream_t s);
+                              uint32_t* status, cudaStream_t s);
 cudaError_t launch_observe(const float* surv, const int32_t* window, const int32_t* acc_len,
                            const int32_t* ceiling, int bs, int gamma, int n_bins, void* stats,
                            uint32_t* status, cudaStream_t s);
@@ -56,7 +56,7 @@ size_t sts_fit_ws_bytes(int n_grid, int n_bins);
 cudaError_t launch_sts_fit(const float* z, const int32_t* ceiling, int N, int gamma, const float* grid,
                            int n_grid, int n_bins, float* T_out, double* ece_out, void* ws, cudaStream_t s);
 cudaError_t launch_zos_budget(const float* surv, int bs, int gamma, const double* sps, int m_max,
-                              int32_t* ring, uint64_t step, cudaStream_t s);
+                              int32_t* ring, uint64_t step, uint32_t* status, cudaStream_t s);
 cudaError_t launch_pack(const int32_t* window, const int32_t* anchor, const int32_t* tokens,
                         int bs, int gamma, const int32_t* tiers, int n_tiers, int cap,
                         int32_t* cu, int32_t* ids, int32_t* req, int32_t* pos, int32_t* padded,

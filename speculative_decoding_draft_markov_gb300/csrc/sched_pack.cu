@@ -254,7 +254,7 @@ struct SchedShared {
 // Zeroes sh.win.
 __device__ int sched_search(const float* __restrict__ surv, int bs, int gamma,
                             const double* __restrict__ sps, int m_max, int mode, SchedShared& sh,
-                            double* __restrict__ theta_out) {
+                            double* __restrict__ theta_out, uint32_t* status) {
   const int tid = threadIdx.x;
   const int n = bs * gamma;
   unsigned long long* src = sh.buf;
@@ -333,7 +333,13 @@ __device__ int sched_search(const float* __restrict__ surv, int bs, int gamma,
   int cand = INT_MAX;
   long long best_v = LLONG_MIN;
   int best_k = INT_MAX;
+  bool bad_table = false;
   for (int K = tid; K <= kmax; K += kSchedThreads) {
+    // the table entries the search reads must be finite, non-negative and non-increasing in M
+    // (dspark_build_sps makes them so); a table that is not is reported, the search still runs
+    const double s0 = sps[bs + K];
+    if (!(s0 >= 0.0) || dnan(s0) || s0 > 1.7976931348623157e308 || (K < kmax && !(sps[bs + K + 1] <= s0)))
+      bad_table = true;
     const double t0 = theta(K);
     if (mode == DSPARK_SCHED_EARLY_STOP) {
       if (K < kmax) {
@@ -359,6 +365,7 @@ __device__ int sched_search(const float* __restrict__ surv, int bs, int gamma,
       best_k = ok;
     }
   }
+  if (__any_sync(0xFFFFFFFFu, bad_table) && lane == 0) set_status(status, DSPARK_EINVAL);
   if (lane == 0) {
     red_k[warp] = (mode == DSPARK_SCHED_EARLY_STOP) ? cand : best_k;
     red_v[warp] = best_v;
@@ -398,19 +405,19 @@ __device__ void sched_windows(SchedShared& sh, int K, int bs, int gamma, int32_t
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(
     const float* __restrict__ surv, int bs, int gamma, const double* __restrict__ sps, int m_max,
     int mode, int32_t* __restrict__ window, int32_t* __restrict__ K_out,
-    double* __restrict__ theta_out) {
+    double* __restrict__ theta_out, uint32_t* status) {
   __shared__ SchedShared sh;
   pdl_enter();
-  const int ks = sched_search(surv, bs, gamma, sps, m_max, mode, sh, theta_out);
+  const int ks = sched_search(surv, bs, gamma, sps, m_max, mode, sh, theta_out, status);
   if (threadIdx.x == 0) *K_out = ks;
   if (window) sched_windows(sh, ks, bs, gamma, window);
 }
 
 cudaError_t launch_schedule(const float* surv, int bs, int gamma, const double* sps, int m_max,
                             int mode, int32_t* window, int32_t* K_out, double* theta_out,
-                            cudaStream_t s) {
+                            uint32_t* status, cudaStream_t s) {
   return launch_pdl(schedule_kernel, dim3(1), dim3(kSchedThreads), 0, s, surv, bs, gamma, sps, m_max, mode, window,
-                    K_out, theta_out);
+                    K_out, theta_out, status);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -457,7 +464,7 @@ __device__ __forceinline__ int block_excl_scan(int x, int* wtot, int* total) {
 __global__ void __launch_bounds__(kSchedThreads) zos_select_kernel(
     const float* __restrict__ surv, int bs, int gamma, const double* __restrict__ sps, int m_max,
     const int32_t* __restrict__ ring, uint64_t step, int32_t* __restrict__ window,
-    int32_t* __restrict__ K_out) {
+    int32_t* __restrict__ K_out, uint32_t* status) {
   __shared__ SchedShared sh;
   __shared__ int s_K, s_bin, s_before;
   pdl_enter();
@@ -468,7 +475,7 @@ __global__ void __launch_bounds__(kSchedThreads) zos_select_kernel(
   for (int e = tid; e < DSPARK_MAX_BS; e += kSchedThreads) sh.win[e] = 0;
   __syncthreads();
   if (s_K < 0) {  // no budget recorded two steps back: the global search over this survival
-    const int ks = sched_search(surv, bs, gamma, sps, m_max, DSPARK_SCHED_GLOBAL_ARGMAX, sh, nullptr);
+    const int ks = sched_search(surv, bs, gamma, sps, m_max, DSPARK_SCHED_GLOBAL_ARGMAX, sh, nullptr, status);
     if (tid == 0) *K_out = ks;
     sched_windows(sh, ks, bs, gamma, window);
     return;
@@ -552,16 +559,16 @@ __global__ void __launch_bounds__(kSchedThreads) zos_select_kernel(
 
 cudaError_t launch_zos_select(const float* surv, int bs, int gamma, const double* sps, int m_max,
                               const int32_t* ring, uint64_t step, int32_t* window, int32_t* K_out,
-                              cudaStream_t s) {
+                              uint32_t* status, cudaStream_t s) {
   return launch_pdl(zos_select_kernel, dim3(1), dim3(kSchedThreads), 0, s, surv, bs, gamma, sps, m_max, ring, step,
-                    window, K_out);
+                    window, K_out, status);
 }
 
 cudaError_t launch_zos_budget(const float* surv, int bs, int gamma, const double* sps, int m_max,
-                              int32_t* ring, uint64_t step, cudaStream_t s) {
+                              int32_t* ring, uint64_t step, uint32_t* status, cudaStream_t s) {
   return launch_pdl(schedule_kernel, dim3(1), dim3(kSchedThreads), 0, s, surv, bs, gamma, sps, m_max,
                     int(DSPARK_SCHED_GLOBAL_ARGMAX), static_cast<int32_t*>(nullptr), ring + (step & 1),
-                    static_cast<double*>(nullptr));
+                    static_cast<double*>(nullptr), status);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -571,7 +578,7 @@ cudaError_t launch_zos_budget(const float* surv, int bs, int gamma, const double
 // ---------------------------------------------------------------------------------------
 // The pack of one block of any size (a multiple of 32, at least bs threads; every thread takes
 // part in the barriers): request r is thread r.
-__device__ void pack_block(const int32_t* __restrict__ window, const int32_t* __restrict__ anchor,
+__device__ void pack_block(const int32_t* window, const int32_t* __restrict__ anchor,
                            const int32_t* __restrict__ tokens, int bs, int gamma, const int32_t* __restrict__ tiers,
                            int n_tiers, int cap, int32_t* __restrict__ cu, int32_t* __restrict__ ids,
                            int32_t* __restrict__ req, int32_t* __restrict__ pos, int32_t* __restrict__ padded_out,
@@ -581,6 +588,9 @@ __device__ void pack_block(const int32_t* __restrict__ window, const int32_t* __
   const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
   if (r == 0) s_bad = 0;
   __syncthreads();
+  // the tiers must be positive and strictly increasing (the search below takes the first >= M)
+  for (int i = r; i < n_tiers; i += blockDim.x)
+    if (tiers[i] <= (i > 0 ? tiers[i - 1] : 0)) atomicExch(&s_bad, 1);
   int l = 0;
   if (r < bs) {
     l = window ? window[r] : gamma;
@@ -663,11 +673,13 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_pack_kernel(
     int32_t* __restrict__ pos, int32_t* __restrict__ padded_out, uint32_t* status) {
   __shared__ SchedShared sh;
   pdl_enter();
-  const int ks = sched_search(surv, bs, gamma, sps, m_max, mode, sh, theta_out);
+  const int ks = sched_search(surv, bs, gamma, sps, m_max, mode, sh, theta_out, status);
   if (threadIdx.x == 0) *K_out = ks;
   sched_windows(sh, ks, bs, gamma, window);
-  __syncthreads();  // the block's window writes are visible to the block
-  pack_block(window, anchor, tokens, bs, gamma, tiers, n_tiers, cap, cu, ids, req, pos, padded_out, status);
+  __syncthreads();
+  // the pack reads the windows from shared memory (sh.win, complete after the barrier in
+  // sched_windows), not back from the global copy this block has just written
+  pack_block(sh.win, anchor, tokens, bs, gamma, tiers, n_tiers, cap, cu, ids, req, pos, padded_out, status);
 }
 
 cudaError_t launch_pack(const int32_t* window, const int32_t* anchor, const int32_t* tokens,

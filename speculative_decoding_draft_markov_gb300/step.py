@@ -118,9 +118,14 @@ def draft_and_schedule(inp: dict, buf: StepBuffers, sps, temperature: float, see
                        tiers=None, stream=None, ring=None) -> None:
     """Stages S1-S4 (everything before the target forward).  With a budget ring the scheduler
     is the asynchronous one: the windows take the budget recorded two steps back
-    (schedule_budget records this step's)."""
+    (schedule_budget records this step's).  STATIC verification tests the whole block, so it
+    needs no windows: the draft is packed as it is, without confidence or scheduler."""
     B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], temperature, seed, step,
                          buf.tokens, buf.logit_x, buf.lse, buf.ws, stream)
+    if mode == B.DSPARK_STATIC and ring is None:
+        B.dspark_pack(None, inp["anchor"], buf.tokens, tiers, buf.cu, buf.ids, buf.req, buf.pos, buf.padded,
+                      buf.ws, stream)
+        return
     B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], buf.tokens, inp["w"], inp["b"], inp["sts_T"],
                         buf.conf, buf.surv, stream)
     if ring is None and mode == B.DSPARK_COMPACT:  # the windows are the packing: one launch for both
@@ -128,9 +133,9 @@ def draft_and_schedule(inp: dict, buf: StepBuffers, sps, temperature: float, see
                                tiers, buf.cu, buf.ids, buf.req, buf.pos, buf.padded, buf.ws, stream)
         return
     if ring is not None:
-        B.dspark_schedule_zos_select(buf.surv, sps, ring, step, buf.window, buf.K, stream)
+        B.dspark_schedule_zos_select(buf.surv, sps, ring, step, buf.window, buf.K, buf.ws, stream)
     else:
-        B.dspark_schedule(buf.surv, sps, sched_mode, buf.window, buf.K, buf.theta, stream)
+        B.dspark_schedule(buf.surv, sps, sched_mode, buf.window, buf.K, buf.theta, buf.ws, stream)
     B.dspark_pack(buf.window if mode == B.DSPARK_COMPACT else None, inp["anchor"], buf.tokens, tiers,
                   buf.cu, buf.ids, buf.req, buf.pos, buf.padded, buf.ws, stream)
 
@@ -149,11 +154,11 @@ def schedule_budget(buf: StepBuffers, sps, ring, step: int, main=None, side=None
     overlaps the target forward and the verify instead of sitting on the step's path."""
     import torch
     if side is None:
-        B.dspark_schedule_zos_budget(buf.surv, sps, ring, step, main)
+        B.dspark_schedule_zos_budget(buf.surv, sps, ring, step, buf.ws, main)
         return
     main = main if main is not None else torch.cuda.current_stream()
     side.wait_stream(main)
-    B.dspark_schedule_zos_budget(buf.surv, sps, ring, step, side)
+    B.dspark_schedule_zos_budget(buf.surv, sps, ring, step, buf.ws, side)
 
 
 def join_budget(main=None, side=None) -> None:

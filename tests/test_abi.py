@@ -99,17 +99,22 @@ def test_other_entry_points_host_validation(L):
     assert L.dspark_sts_fit(f, f, 100, 17, f, 8, 10, f, f, f, 1 << 20, None) == B.DSPARK_EUNSUPPORTED
     assert L.dspark_sts_fit(f, f, 100, 7, f, 2000, 10, f, f, f, 1 << 30, None) == B.DSPARK_EUNSUPPORTED
     assert L.dspark_sts_fit(f, f, 100, 7, f, 8, 10, f, f, f, 16, None) == B.DSPARK_EWORKSPACE
-    # schedule: m_max < bs, bad mode, too many slots
-    assert L.dspark_schedule(f, 4, 7, f, 3, 0, f, f, f, None) == B.DSPARK_EINVAL
-    assert L.dspark_schedule(f, 4, 7, f, 64, 5, f, f, f, None) == B.DSPARK_EINVAL
-    assert L.dspark_schedule(f, 256, 17, f, 9000, 0, f, f, f, None) == B.DSPARK_EUNSUPPORTED
-    # asynchronous scheduler: no ring, m_max < bs, too many slots
-    assert L.dspark_schedule_zos_select(f, 4, 7, f, 64, None, 0, f, f, None) == B.DSPARK_EINVAL
-    assert L.dspark_schedule_zos_select(f, 4, 7, f, 3, f, 0, f, f, None) == B.DSPARK_EINVAL
-    assert L.dspark_schedule_zos_select(f, 256, 17, f, 9000, f, 0, f, f, None) == B.DSPARK_EUNSUPPORTED
-    assert L.dspark_schedule_zos_budget(f, 4, 7, f, 64, None, 0, None) == B.DSPARK_EINVAL
-    assert L.dspark_schedule_zos_budget(f, 0, 7, f, 64, f, 0, None) == B.DSPARK_EINVAL
-    assert L.dspark_schedule_zos_budget(f, 4, 7, f, 64, f + 2, 0, None) == B.DSPARK_EINVAL
+    # schedule: m_max < bs, bad mode, too many slots, no / small / misaligned workspace
+    assert L.dspark_schedule(f, 4, 7, f, 3, 0, f, f, f, f, 256, None) == B.DSPARK_EINVAL
+    assert L.dspark_schedule(f, 4, 7, f, 64, 5, f, f, f, f, 256, None) == B.DSPARK_EINVAL
+    assert L.dspark_schedule(f, 256, 17, f, 9000, 0, f, f, f, f, 256, None) == B.DSPARK_EUNSUPPORTED
+    assert L.dspark_schedule(f, 4, 7, f, 64, 0, f, f, f, None, 256, None) == B.DSPARK_EWORKSPACE
+    assert L.dspark_schedule(f, 4, 7, f, 64, 0, f, f, f, f, 255, None) == B.DSPARK_EWORKSPACE
+    assert L.dspark_schedule(f, 4, 7, f, 64, 0, f, f, f, f + 16, 256, None) == B.DSPARK_EWORKSPACE
+    # asynchronous scheduler: no ring, m_max < bs, too many slots, no workspace
+    assert L.dspark_schedule_zos_select(f, 4, 7, f, 64, None, 0, f, f, f, 256, None) == B.DSPARK_EINVAL
+    assert L.dspark_schedule_zos_select(f, 4, 7, f, 3, f, 0, f, f, f, 256, None) == B.DSPARK_EINVAL
+    assert L.dspark_schedule_zos_select(f, 256, 17, f, 9000, f, 0, f, f, f, 256, None) == B.DSPARK_EUNSUPPORTED
+    assert L.dspark_schedule_zos_select(f, 4, 7, f, 64, f, 0, f, f, None, 0, None) == B.DSPARK_EWORKSPACE
+    assert L.dspark_schedule_zos_budget(f, 4, 7, f, 64, None, 0, f, 256, None) == B.DSPARK_EINVAL
+    assert L.dspark_schedule_zos_budget(f, 0, 7, f, 64, f, 0, f, 256, None) == B.DSPARK_EINVAL
+    assert L.dspark_schedule_zos_budget(f, 4, 7, f, 64, f + 2, 0, f, 256, None) == B.DSPARK_EINVAL
+    assert L.dspark_schedule_zos_budget(f, 4, 7, f, 64, f, 0, None, 0, None) == B.DSPARK_EWORKSPACE
     # pack: negative tier count, missing workspace
     assert L.dspark_pack(None, f, f, 4, 7, f, -1, 64, f, f, f, f, f, f, 1 << 20, None) == B.DSPARK_EINVAL
     assert L.dspark_pack(None, f, f, 4, 7, None, 0, 64, f, f, f, f, f, None, 0, None) == B.DSPARK_EWORKSPACE

@@ -63,14 +63,14 @@ def test_step_entry_points_keep_their_bounds(shape):
     _check(conf, surv, z)
     sps = S.sps_table(inp["T_raw"], inp["tiers"], dev)
     win, K, th = Guarded((bs,), torch.int32), Guarded((1,), torch.int32), Guarded((1,), torch.float64)
-    B.dspark_schedule(surv.t, sps, B.DSPARK_SCHED_GLOBAL_ARGMAX, win.t, K.t, th.t)
+    B.dspark_schedule(surv.t, sps, B.DSPARK_SCHED_GLOBAL_ARGMAX, win.t, K.t, th.t, ws.t)
     _check(win, K, th)
     ring = Guarded((2,), torch.int32)
     ring.t.fill_(-1)
     win2, K2 = Guarded((bs,), torch.int32), Guarded((1,), torch.int32)
     for step in range(3):
-        B.dspark_schedule_zos_select(surv.t, sps, ring.t, step, win2.t, K2.t)
-        B.dspark_schedule_zos_budget(surv.t, sps, ring.t, step)
+        B.dspark_schedule_zos_select(surv.t, sps, ring.t, step, win2.t, K2.t, ws.t)
+        B.dspark_schedule_zos_budget(surv.t, sps, ring.t, step, ws.t)
     _check(ring, win2, K2)
     cap = bs * (gamma + 1)
     tiers = torch.as_tensor(inp["tiers"], device=dev) if len(inp["tiers"]) else None

@@ -100,7 +100,8 @@ def test_confidence_parity(name, d):
                                host["sts_T"], dtype=wl.dtype)
     tol = TOL[wl.dtype]
     np.testing.assert_allclose(conf.cpu().numpy(), c_o, rtol=tol, atol=0)
-    np.testing.assert_allclose(surv.cpu().numpy(), a_o, rtol=tol * wl.gamma, atol=0)
+    # survival: a product of gamma confidences, held to the same relative tolerance as each one
+    np.testing.assert_allclose(surv.cpu().numpy(), a_o, rtol=tol, atol=0)
 
 
 def _sched_cases():
@@ -143,7 +144,10 @@ def test_schedule_bit_exact(mode):
         win = torch.zeros(bs, dtype=torch.int32, device="cuda")
         K = torch.zeros(1, dtype=torch.int32, device="cuda")
         th = torch.zeros(1, dtype=torch.float64, device="cuda")
-        B.dspark_schedule(torch.as_tensor(a, device="cuda"), torch.as_tensor(sps, device="cuda"), mode, win, K, th)
+        ws = B.alloc_workspace(bs, gamma, 1024)
+        B.dspark_schedule(torch.as_tensor(a, device="cuda"), torch.as_tensor(sps, device="cuda"), mode, win, K, th,
+                          ws)
+        assert B.dspark_read_device_status(ws) == B.DSPARK_OK
         w_o, K_o, th_o, _ = O.schedule(a, sps, mode)
         np.testing.assert_array_equal(win.cpu().numpy(), w_o)
         assert int(K.item()) == K_o
@@ -185,6 +189,48 @@ def test_pack_device_errors_and_recovery():
     assert B.dspark_read_device_status(ws) == B.DSPARK_EINVAL
     B.dspark_pack(t([1] * bs), anchor, tokens, t([8, 16]), cu, ids, req, pos, padded, ws)      # fine again
     assert B.dspark_read_device_status(ws) == B.DSPARK_OK and padded.item() == 16
+    # tiers not strictly increasing (a repeat, a decrease) or not positive
+    for bad in ([8, 8, 16], [16, 8, 32], [0, 16], [-4, 16]):
+        padded.fill_(7)
+        B.dspark_pack(t([1] * bs), anchor, tokens, t(bad), cu, ids, req, pos, padded, ws)
+        assert B.dspark_read_device_status(ws) == B.DSPARK_EINVAL, bad
+        assert padded.item() == -1
+
+
+def test_schedule_rejects_a_table_that_increases():
+    """A cost table whose entries rise with M (or are negative / not finite) is reported by every
+    scheduler entry point that searches it; a table from dspark_build_sps never is."""
+    bs, gamma = 16, 4
+    a = I.random_survival(bs, gamma, 3)
+    surv = torch.as_tensor(a, device="cuda")
+    m = bs * (gamma + 1)
+    good = O.build_sps(5.0 + 0.01 * np.arange(m + 1), [])
+    t = lambda x: torch.as_tensor(np.asarray(x, dtype=np.int32), device="cuda")
+    win = torch.zeros(bs, dtype=torch.int32, device="cuda")
+    K = torch.zeros(1, dtype=torch.int32, device="cuda")
+    th = torch.zeros(1, dtype=torch.float64, device="cuda")
+    cu = torch.zeros(bs + 1, dtype=torch.int32, device="cuda")
+    ids, req, pos = (torch.zeros(m, dtype=torch.int32, device="cuda") for _ in range(3))
+    padded = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = B.alloc_workspace(bs, gamma, 1024)
+    anchor, tokens = t(np.arange(bs)), t(np.zeros((bs, gamma)))
+    bads = []
+    for where, val in ((bs + 3, 1.0), (bs, -1.0), (bs + 7, np.inf), (bs + 1, np.nan)):
+        b = good.copy()
+        b[where] = val if val != 1.0 else b[where - 1] * 1.001  # one entry above the one before
+        bads.append(b)
+    for sps_h, expect in [(good, B.DSPARK_OK)] + [(b, B.DSPARK_EINVAL) for b in bads]:
+        sps = torch.as_tensor(sps_h, device="cuda")
+        B.dspark_schedule(surv, sps, B.DSPARK_SCHED_GLOBAL_ARGMAX, win, K, th, ws)
+        assert B.dspark_read_device_status(ws) == expect
+        B.dspark_schedule_pack(surv, sps, B.DSPARK_SCHED_EARLY_STOP, win, K, th, anchor, tokens, None, cu, ids, req,
+                               pos, padded, ws)
+        assert B.dspark_read_device_status(ws) == expect
+        ring = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+        B.dspark_schedule_zos_select(surv, sps, ring, 0, win, K, ws)   # empty ring: the global search
+        assert B.dspark_read_device_status(ws) == expect
+        B.dspark_schedule_zos_budget(surv, sps, ring, 0, ws)
+        assert B.dspark_read_device_status(ws) == expect
 
 
 def _verify_chain(wl, temperature, mode, windows_seed, step=0):
@@ -238,7 +284,7 @@ VERIFY_WL = {
 
 @pytest.mark.parametrize("name", list(VERIFY_WL))
 @pytest.mark.parametrize("mode", [O.STATIC, O.COMPACT, O.CAP_ACCEPT])
-@pytest.mark.parametrize("temperature", [1.0, 0.0])
+@pytest.mark.parametrize("temperature", [1.0, 0.7, 0.0])
 def test_verify_chain_parity(name, mode, temperature):
     wl = VERIFY_WL[name]
     total_checked = 0
@@ -251,7 +297,8 @@ def test_verify_chain_parity(name, mode, temperature):
 
 @pytest.mark.parametrize("name", list(VERIFY_WL))
 @pytest.mark.parametrize("mode", [O.STATIC, O.COMPACT])
-def test_verify_with_explicit_draft_logits(name, mode):
+@pytest.mark.parametrize("temperature", [1.0, 0.7])
+def test_verify_with_explicit_draft_logits(name, mode, temperature):
     """dspark_verify given the draft's logits (no U / W1 / W2t): the residual's p_d comes from
     them.  The logits here are a fresh draw (not a Markov head), with logit_x / lse taken from
     them, so the test covers a drafter whose distribution the library never computes."""
@@ -269,12 +316,13 @@ def test_verify_with_explicit_draft_logits(name, mode):
         D_host = D64.astype(np.float32)
         Df = D_host.astype(np.float64)
         D_dev = torch.as_tensor(D_host, device="cuda")
-    # draft tokens drawn from softmax(D); logit_x / lse consistent with D
-    m = Df.max(-1, keepdims=True)
-    lse = (np.log(np.exp(Df - m).sum(-1)) + m[..., 0])
-    p = np.exp(Df - lse[..., None])
+    # draft tokens drawn from softmax(D / T); logit_x / lse consistent with D at temperature T
+    Dt = Df / temperature
+    m = Dt.max(-1, keepdims=True)
+    lse = (np.log(np.exp(Dt - m).sum(-1)) + m[..., 0])
+    p = np.exp(Dt - lse[..., None])
     tok = np.array([[rng.choice(V, p=p[b, k] / p[b, k].sum()) for k in range(gamma)] for b in range(bs)], np.int32)
-    lx = np.take_along_axis(Df, tok[..., None].astype(np.int64), -1)[..., 0]
+    lx = np.take_along_axis(Dt, tok[..., None].astype(np.int64), -1)[..., 0]
     lx, lse = lx.astype(np.float32), lse.astype(np.float32)
     win = I.random_windows(bs, gamma, 123)
     pack_win = win if mode == O.COMPACT else None
@@ -284,7 +332,7 @@ def test_verify_with_explicit_draft_logits(name, mode):
     checked = near = 0
     for step in range(3):
         out_o, acc_o, _, mv_o = O.verify(packed_o, cu_o, win, mode, host["anchor"], tok, lx, lse, None, None, None,
-                                         1.0, wl.seed, step, dtype=wl.dtype, draft_logits=D_host)
+                                         temperature, wl.seed, step, dtype=wl.dtype, draft_logits=D_host)
         buf = S.StepBuffers.allocate(bs, gamma, V, cap, inp["U"].dtype)
         buf.tokens.copy_(torch.as_tensor(tok, device="cuda"))
         buf.logit_x.copy_(torch.as_tensor(lx, device="cuda"))
@@ -294,8 +342,8 @@ def test_verify_with_explicit_draft_logits(name, mode):
                       buf.req, buf.pos, buf.padded, buf.ws)
         S.gather_target_forward(inp["target"])(buf)
         B.dspark_verify(buf.packed, buf.cu, buf.window, mode, inp["anchor"], buf.tokens, buf.logit_x, buf.lse,
-                        None, None, None, 1.0, wl.seed, step, buf.out_tokens, buf.acc_len, buf.ceiling, buf.ws,
-                        draft_logits=D_dev)
+                        None, None, None, temperature, wl.seed, step, buf.out_tokens, buf.acc_len, buf.ceiling,
+                        buf.ws, draft_logits=D_dev)
         assert B.dspark_read_device_status(buf.ws) == B.DSPARK_OK
         c, n = compare_verify(buf.out_tokens.cpu().numpy(), buf.acc_len.cpu().numpy(), out_o, acc_o, mv_o)
         checked += c

@@ -59,7 +59,8 @@ def test_workload_full_size(name, wl, modes, temperature):
                         buf.conf, buf.surv)
     c_o, a_o, _ = O.confidence(to_np(inp["h"][t_rows]), W1, anchor[rows], to_np(buf.tokens)[rows],
                                to_np(inp["w"]), inp["b"], to_np(inp["sts_T"]))
-    np.testing.assert_allclose(to_np(buf.conf)[rows], c_o, rtol=TOL["bf16"], atol=1e-6)
+    np.testing.assert_allclose(to_np(buf.conf)[rows], c_o, rtol=TOL["bf16"], atol=0)
+    np.testing.assert_allclose(to_np(buf.surv)[rows], a_o, rtol=TOL["bf16"], atol=0)
 
     # S4 + S5 with generator windows, every mode of the workload
     win = I.random_windows(bs, gamma, wl.seed + 7)

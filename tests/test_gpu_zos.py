@@ -13,6 +13,11 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 
+def _WS():
+    """A status-word workspace for the scheduler calls (they use only its first word)."""
+    return torch.zeros(256, dtype=torch.uint8, device="cuda")
+
+
 def _table(bs, gamma, kind):
     m = bs * (gamma + 1)
     if kind == "tiny":
@@ -50,8 +55,8 @@ def test_zos_sequence_bit_exact(case):
     for t in range(6):
         a = _survival(bs, gamma, case, ties, t)
         surv = torch.as_tensor(a, device="cuda")
-        B.dspark_schedule_zos_select(surv, sps, ring, t, win, K)
-        B.dspark_schedule_zos_budget(surv, sps, ring, t)
+        B.dspark_schedule_zos_select(surv, sps, ring, t, win, K, _WS())
+        B.dspark_schedule_zos_budget(surv, sps, ring, t, _WS())
         w_o, K_o = O.zos_step(a, sps_h, ring_o, t)
         np.testing.assert_array_equal(win.cpu().numpy(), w_o)
         assert int(K.item()) == K_o, (t, int(K.item()), K_o)
@@ -74,7 +79,7 @@ def test_zos_select_every_budget(shape):
             if Kp < 0:
                 continue
             ring = torch.tensor([Kp, -1], dtype=torch.int32, device="cuda")
-            B.dspark_schedule_zos_select(surv, sps, ring, 0, win, K)
+            B.dspark_schedule_zos_select(surv, sps, ring, 0, win, K, _WS())
             Ke = min(Kp, n)
             assert int(K.item()) == Ke
             np.testing.assert_array_equal(win.cpu().numpy(), O.zos_select(a, Ke), err_msg=f"K={Kp}")
@@ -95,7 +100,7 @@ def test_zos_select_tie_and_sign_edge_cases():
         surv = torch.as_tensor(a, device="cuda")
         for Kp in (0, 1, 63, 64, 65, 300, 511, 512):
             ring = torch.tensor([-1, Kp], dtype=torch.int32, device="cuda")
-            B.dspark_schedule_zos_select(surv, sps, ring, 1, win, K)
+            B.dspark_schedule_zos_select(surv, sps, ring, 1, win, K, _WS())
             Ke = min(Kp, bs * gamma)
             expect = O.zos_select(np.maximum(a, 0) + np.float32(0), Ke)
             np.testing.assert_array_equal(win.cpu().numpy(), expect)
@@ -158,7 +163,7 @@ def test_fused_schedule_pack_equals_the_two_calls(sched_mode):
         if fused:
             B.dspark_schedule_pack(surv, sps, sched_mode, win, K, th, anchor, tokens, tiers, cu, ids, req, pos, pad, ws)
         else:
-            B.dspark_schedule(surv, sps, sched_mode, win, K, th)
+            B.dspark_schedule(surv, sps, sched_mode, win, K, th, ws)
             B.dspark_pack(win, anchor, tokens, tiers, cu, ids, req, pos, pad, ws)
         assert B.dspark_read_device_status(ws) == B.DSPARK_OK
         outs.append([t.cpu() for t in (win, K, th, cu, ids, req, pos, pad)])

@@ -43,23 +43,26 @@ def _run_step(U, W1, W2t, target, anchor, window, mode, step, tau=1.0, seed=5):
     return tok, out, acc, ceil
 
 
-def test_monte_carlo_acceptance_equals_one_minus_tv():
+@pytest.mark.parametrize("tau", [1.0, 0.7])
+def test_monte_carlo_acceptance_equals_one_minus_tv(tau):
+    """At temperature tau both distributions are the tempered softmaxes: p_d = softmax(l / tau),
+    p_t = softmax(t / tau), and the acceptance is 1 - TV between them."""
     U, W1, W2t, target, anchor = _setup()
     bs, gamma, V = U.shape
     f = lambda a: a.astype(np.float64)
-    pd1 = softmax(f(U[0, 0]) + f(W1[anchor[0]]) @ f(W2t).T)
-    pt1 = softmax(f(target[0, 0]))
-    pt2 = softmax(f(target[0, 1]))
+    pd1 = softmax((f(U[0, 0]) + f(W1[anchor[0]]) @ f(W2t).T) / tau)
+    pt1 = softmax(f(target[0, 0]) / tau)
+    pt2 = softmax(f(target[0, 1]) / tau)
     acc1 = 1.0 - 0.5 * np.abs(pd1 - pt1).sum()
     # P(accept 2 | accept 1) = sum_x1 min(pd1, pt1)(x1) / acc1 * (1 - TV(pd2(.|x1), pt2))
     cond = 0.0
     for x1 in range(V):
-        pd2 = softmax(f(U[0, 1]) + f(W1[x1]) @ f(W2t).T)
+        pd2 = softmax((f(U[0, 1]) + f(W1[x1]) @ f(W2t).T) / tau)
         cond += min(pd1[x1], pt1[x1]) / acc1 * (1.0 - 0.5 * np.abs(pd2 - pt2).sum())
     window = np.full(bs, gamma, dtype=np.int32)
     n1 = n2 = n = 0
     for step in range(60):
-        _, _, acc, _ = _run_step(U, W1, W2t, target, anchor, window, O.COMPACT, step)
+        _, _, acc, _ = _run_step(U, W1, W2t, target, anchor, window, O.COMPACT, step, tau=tau)
         n += bs
         n1 += int(np.sum(acc >= 1))
         n2 += int(np.sum(acc >= 2))
@@ -69,18 +72,40 @@ def test_monte_carlo_acceptance_equals_one_minus_tv():
     assert abs(p21 - cond) < 4 * np.sqrt(cond * (1 - cond) / n1)
 
 
+@pytest.mark.parametrize("tau", [1.0, 0.7])
 @pytest.mark.parametrize("mode", ["compact_random", "static", "cap_accept"])
-def test_first_committed_token_is_target_distributed(mode):
+def test_first_committed_token_is_target_distributed(mode, tau):
+    """Lossless at any temperature: the first committed token follows softmax(t / tau) -- through
+    an accepted draft token, the residual after a rejection, or the bonus after an empty or
+    fully accepted window."""
     U, W1, W2t, target, anchor = _setup(seed=1, noise=1.5)
     bs, gamma, V = U.shape
-    pt1 = softmax(target[0, 0].astype(np.float64))
+    pt1 = softmax(target[0, 0].astype(np.float64) / tau)
     counts = np.zeros(V)
     for step in range(60):
         window = I.random_windows(bs, gamma, 1000 + step)
         m = {"compact_random": O.COMPACT, "static": O.STATIC, "cap_accept": O.CAP_ACCEPT}[mode]
-        _, out, _, _ = _run_step(U, W1, W2t, target, anchor, window, m, step)
+        _, out, _, _ = _run_step(U, W1, W2t, target, anchor, window, m, step, tau=tau)
         np.add.at(counts, out[:, 0], 1)
     assert stats.chisquare(counts, pt1 * counts.sum()).pvalue > 1e-4
+
+
+@pytest.mark.parametrize("tau", [0.7, 1.6])
+def test_second_committed_token_given_first_accepted_is_target_distributed(tau):
+    """Given that x_1 was accepted, the next committed token follows the target's row 2 at the
+    same temperature (accepted x_2, residual at position 2, or the bonus of a one-token window),
+    so every position's tempering is exercised."""
+    U, W1, W2t, target, anchor = _setup(seed=6, noise=0.8, reps=300)
+    bs, gamma, V = U.shape
+    pt2 = softmax(target[0, 1].astype(np.float64) / tau)
+    counts = np.zeros(V)
+    for step in range(40):
+        window = np.where(I.random_windows(bs, gamma, 500 + step) > 0, gamma, 1).astype(np.int32)
+        tok, out, acc, _ = _run_step(U, W1, W2t, target, anchor, window, O.COMPACT, step, tau=tau)
+        sel = acc >= 1
+        np.add.at(counts, out[sel, 1], 1)
+    assert counts.sum() > 3000
+    assert stats.chisquare(counts, pt2 * counts.sum()).pvalue > 1e-4
 
 
 def test_cap_accept_commits_like_compact_and_exposes_static_ceiling():

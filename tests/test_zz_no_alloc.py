@@ -5,7 +5,9 @@ whose device footprint is fixed at start-up) have no workspace to hand over, so 
 point takes its scratch from a fixed array inside the library.  These tests call it through
 the C ABI and check it against dspark_draft_block (same kernels, caller-owned workspace) on
 two calls in a row -- the second call finds the first call's contents still in the shared
-array -- and check that sizes beyond the array are refused.  This file is collected last."""
+array -- at the mixed-difficulty batch's shape (bs 256, V 151936, also against the oracle)
+and at the largest vocabulary each pass accepts, and check that one step beyond is refused.
+This file is collected last."""
 import ctypes
 
 import numpy as np
@@ -15,7 +17,8 @@ from speculative_decoding_draft_markov_gb300 import binding as B
 from speculative_decoding_draft_markov_gb300 import build as BUILD
 from speculative_decoding_draft_markov_gb300 import inputs as I
 from speculative_decoding_draft_markov_gb300 import step as S
-from tests.parity import TOL
+from oracle import dspark_oracle as O
+from tests.parity import TOL, compare_draft, to_np
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -57,20 +60,85 @@ def test_noalloc_draft_matches_workspace_draft_on_two_calls(name):
         np.testing.assert_array_equal(got[0].cpu().numpy(), ref[0].cpu().numpy())
         for g, rf in zip(got[1:], ref[1:]):
             np.testing.assert_allclose(g.cpu().numpy(), rf.cpu().numpy(), rtol=tol, atol=tol)
-    # the library's own status word path (device_status = NULL) also works
+    # the library's own status word path (device_status = NULL): same outputs as the workspace draft
+    _compare_with_workspace_draft(L, U, W1, W2t, anchor, 1.0, wl.seed, 5, ws, None, tol)
+
+
+def _compare_with_workspace_draft(L, U, W1, W2t, anchor, temperature, seed, step, ws, status, tol):
+    """One allocation-free call against dspark_draft_block on the same inputs."""
+    bs, gamma, V = U.shape
+    r = W1.shape[1]
+    dt = B.DSPARK_F32 if U.dtype == torch.float32 else B.DSPARK_BF16
+    stream = torch.cuda.current_stream().cuda_stream
+    ref = [torch.zeros((bs, gamma), dtype=t, device="cuda") for t in (torch.int32, torch.float32, torch.float32)]
+    got = [torch.full((bs, gamma), -5, dtype=t, device="cuda") for t in (torch.int32, torch.float32, torch.float32)]
+    B.dspark_draft_block(U, W1, W2t, anchor, temperature, seed, step, *ref, ws)
     rc = L.dspark_draft_block_noalloc(_ptr(U), _ptr(W1), _ptr(W2t), dt, _ptr(anchor), bs, gamma, V, r,
-                                      ctypes.c_float(1.0), wl.seed, 5, _ptr(got[0]), _ptr(got[1]), _ptr(got[2]),
-                                      None, ctypes.c_void_p(stream))
-    assert rc == B.DSPARK_OK
+                                      ctypes.c_float(temperature), seed, step, _ptr(got[0]), _ptr(got[1]),
+                                      _ptr(got[2]), _ptr(status), ctypes.c_void_p(stream))
+    assert rc == B.DSPARK_OK, B.dspark_status_string(rc)
     torch.cuda.synchronize()
     assert B.dspark_read_device_status(ws) == B.DSPARK_OK
+    if status is not None:
+        assert int(status.item()) == 0
+    np.testing.assert_array_equal(got[0].cpu().numpy(), ref[0].cpu().numpy())
+    for g, rf in zip(got[1:], ref[1:]):
+        np.testing.assert_allclose(g.cpu().numpy(), rf.cpu().numpy(), rtol=tol, atol=tol)
+    return got
 
 
-def test_noalloc_rejects_sizes_beyond_its_scratch():
+# Largest vocabulary each pass accepts at bs = 256: 256 B + 256 * n * 16 B <= 8 MiB gives n <= 2047,
+# i.e. ceil(V / 128) <= 2047 on the tensor-core pass and ceil(V / 64) <= 2047 on the CUDA-core pass.
+V_MAX_TC, V_MAX_SIMT = 2047 * 128, 2047 * 64
+
+
+def test_noalloc_headline_shape_against_oracle_rows():
+    """bs = 256, V = 151936 in bf16 (the mixed-difficulty batch) is accepted, equals the workspace
+    draft, and its sampled requests equal the oracle's draws."""
+    BUILD.build()
+    L = B.lib()
+    wl = I.WORKLOADS["mixed_bs256"].with_(name="noalloc_full", gamma=2, seed=33)
+    inp = I.make_device_inputs(wl, "cuda", with_target=False, with_hidden=False)
+    bs, gamma, V = wl.bs, wl.gamma, wl.V
+    ws = B.alloc_workspace(bs, gamma, V)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _compare_with_workspace_draft(L, inp["U"], inp["W1"], inp["W2t"], inp["anchor"], 1.0, wl.seed, 2, ws,
+                                        status, TOL["bf16"])
+    rows = np.array([0, 100, 255])
+    U = to_np(inp["U"][torch.as_tensor(rows, device="cuda")])
+    to, lo, so, mo = O.draft_block(U, to_np(inp["W1"]), to_np(inp["W2t"]), to_np(inp["anchor"])[rows], 1.0,
+                                   wl.seed, 2, dtype="bf16", req_ids=rows)
+    g = [to_np(x)[rows] for x in got]
+    checked, near = compare_draft(g[0], g[1], g[2], to, lo, so, mo, "bf16")
+    assert near <= 1 and checked >= (len(rows) - near) * gamma
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", V_MAX_TC), ("f32", V_MAX_SIMT)])
+def test_noalloc_at_the_exact_limit(dtype, V):
+    """The largest accepted vocabulary at bs = 256 on each pass runs and equals the workspace draft."""
+    BUILD.build()
+    L = B.lib()
+    bs, gamma, r = 256, 1, 256 if dtype == "bf16" else 32
+    g = torch.Generator(device="cuda")
+    g.manual_seed(34)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    U = (torch.randn((bs, gamma, V), device="cuda", generator=g) * 3.0).to(tdt)
+    W1 = (torch.randn((V, r), device="cuda", generator=g) * 0.05).to(tdt)
+    W2t = (torch.randn((V, r), device="cuda", generator=g) * 0.05).to(tdt)
+    anchor = torch.randint(0, V, (bs,), device="cuda", generator=g, dtype=torch.int64).to(torch.int32)
+    ws = B.alloc_workspace(bs, gamma, V)
+    _compare_with_workspace_draft(L, U, W1, W2t, anchor, 1.0, 34, 0, ws, None, TOL[dtype])
+
+
+@pytest.mark.parametrize("dtype,V,r", [("bf16", V_MAX_TC + 8, 256), ("f32", V_MAX_SIMT + 8, 32),
+                                       ("bf16", V_MAX_SIMT + 8, 32), ("bf16", 1 << 23, 256)])
+def test_noalloc_rejects_sizes_beyond_its_scratch(dtype, V, r):
+    """One vocabulary step past each pass's limit at bs = 256 is refused before anything runs (the
+    bf16 r = 32 case takes the CUDA-core pass, hence its limit)."""
     BUILD.build()
     L = B.lib()
     fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the size check comes first
-    # bs = 256 and V = 2^23 need 256 * 65536 * 8 bytes of statistics, far beyond the array
-    rc = L.dspark_draft_block_noalloc(fake, fake, fake, B.DSPARK_BF16, fake, 256, 7, 1 << 23, 256,
+    dt = B.DSPARK_BF16 if dtype == "bf16" else B.DSPARK_F32
+    rc = L.dspark_draft_block_noalloc(fake, fake, fake, dt, fake, 256, 7, V, r,
                                       ctypes.c_float(1.0), 0, 0, fake, fake, fake, None, None)
     assert rc == B.DSPARK_EUNSUPPORTED
