@@ -767,8 +767,12 @@ def run_profile_case(args):
             B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], wl.temperature, wl.seed, it,
                                  buf.tokens, buf.logit_x, buf.lse, buf.ws)
     else:
-        sps = S.sps_table(I.cost_curve_ms(wl.with_(tier_max=cap)), np.zeros(0, np.int32), dev)
-        S.draft_and_schedule(inp, buf, sps, wl.temperature, wl.seed, 0, SCHED)
+        # the benchmark's own packing: its cost table and graph tiers, the global scheduler
+        cap = max(cap, int(inp["tiers"][-1]))
+        buf = S.StepBuffers.allocate(bs, gamma, V, cap, inp["U"].dtype, dev)
+        sps = S.sps_table(inp["T_raw"], inp["tiers"], dev)
+        S.draft_and_schedule(inp, buf, sps, wl.temperature, wl.seed, 0, SCHED,
+                             tiers=torch.as_tensor(inp["tiers"], device=dev))
         S.gather_target_forward(inp["target"])(buf)
 
         def run(it):
@@ -783,7 +787,7 @@ def run_profile_case(args):
     torch.cuda.synchronize()
     st = B.dspark_read_device_status(buf.ws)
     print(json.dumps({"case": args.profile_case, "gamma": gamma, "ms_per_call": ev[0].elapsed_time(ev[1]) / args.steps,
-                      "status": B.dspark_status_string(st)}))
+                      "packed_rows": int(buf.cu[-1].item()), "status": B.dspark_status_string(st)}))
     if st != 0:
         sys.exit(1)
 

@@ -7,6 +7,7 @@ none of the method's arithmetic.
 
 It computes, plainly and slowly, in IEEE double:
   S1 draft_block   -- Markov sequential head, left-to-right sampling
+     rnn_draft_block -- the same with the RNN sequential head (gated recurrent state)
   S2 confidence    -- confidence head + sequential temperature scaling + prefix survival
   S3 schedule      -- hardware-aware global top-B prefix scheduler
   S4 pack          -- ragged cu_seqlens packing rounded up to a captured graph tier
@@ -283,21 +284,87 @@ def draft_block(U, W1, W2t, anchor, temperature: float, seed: int, step: int,
     for k in range(1, gamma + 1):
         ell = markov_logits(U[:, k - 1], W1, W2t, x_prev)
         for r in range(bs):
-            if temperature == 0.0:
-                v = _first_argmax(ell[r])
-                tokens[r, k - 1] = v
-                logit_x[r, k - 1] = ell[r, v]
-                margin[r, k - 1] = _top2_gap(ell[r])
-            else:
-                t = ell[r] / temperature
-                rid = r if req_ids is None else int(req_ids[r])
-                v, mg = two_level_cdf(t, seed, step, rid, k, P_DRAFT_CHUNK, P_DRAFT_ELEM, chunk)
-                tokens[r, k - 1] = v
-                logit_x[r, k - 1] = t[v]
-                lse[r, k - 1] = logsumexp(t)
-                margin[r, k - 1] = mg
+            rid = r if req_ids is None else int(req_ids[r])
+            tokens[r, k - 1], logit_x[r, k - 1], lse[r, k - 1], margin[r, k - 1] = \
+                _draw_position(ell[r], temperature, seed, step, rid, k, chunk)
         x_prev = tokens[:, k - 1].astype(np.int64)
     return tokens, logit_x, lse, margin
+
+
+def _draw_position(ell_row, temperature: float, seed: int, step: int, rid: int, k: int, chunk: int):
+    """The draw of one request at position k from its logits l_k (the draft's sampling rule):
+    temperature 0 -> the argmax (lowest index); else two_level_cdf of l_k / temperature.
+    Returns (token, logit_x, lse, margin) as draft_block reports them."""
+    if temperature == 0.0:
+        v = _first_argmax(ell_row)
+        return v, ell_row[v], 0.0, _top2_gap(ell_row)
+    t = ell_row / temperature
+    v, mg = two_level_cdf(t, seed, step, rid, k, P_DRAFT_CHUNK, P_DRAFT_ELEM, chunk)
+    return v, t[v], logsumexp(t), mg
+
+
+# ---------------------------------------------------------------------------
+# S1 with the RNN sequential head
+# ---------------------------------------------------------------------------
+
+def round_bf16(x) -> np.ndarray:
+    """Round to the nearest bf16 value, ties to even, returned in float64: with x = m 2^e and
+    0.5 <= |m| < 1, keep 8 significant bits of m (bf16 has a 7-bit stored mantissa)."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.round(m * 256.0) / 256.0, e)  # np.round: half to even
+
+
+def rnn_state_step(e, s_prev, Wg, bg, dtype: str = "bf16"):
+    """One update of the RNN head's gated recurrent state.
+
+    [SUMMARY, "Architecture (drafter)", RNN head]: the head keeps a gated recurrent state s_k
+    across the whole block, so position k sees the full prefix history.  The pages give no
+    equations; reading (the plainest gated recurrence over the Markov head's inputs):
+        g_k = sigmoid([e_k ; s_{k-1}] Wg + b_g)        (Wg: [2r, r], b_g: [r])
+        s_k = g_k * s_{k-1} + (1 - g_k) * e_k           (s_0 = 0, e_k = W1[x_{k-1}])
+    and the state is held in the head's parameter precision: rounded to bf16 after every
+    update when the head is bf16 (the tensor cores read it as an operand).  A closed gate
+    (g = 0) gives s_k = e_k, the Markov head; an open gate (g = 1) keeps s_k = 0.
+    Inputs are float64 arrays ([n, r] e and s_prev); returns s_k [n, r]."""
+    z = np.concatenate([e, s_prev], axis=1) @ Wg + bg[None, :]
+    with np.errstate(over="ignore"):
+        g = 1.0 / (1.0 + np.exp(-z))
+    s = g * s_prev + (1.0 - g) * e
+    return round_bf16(s) if dtype == "bf16" else s
+
+
+def rnn_draft_block(U, W1, W2t, Wg, bg, anchor, temperature: float, seed: int, step: int,
+                    dtype: str = "bf16", chunk: int = DRAFT_CHUNK, req_ids=None):
+    """S1 with the RNN head: p_k(v) = softmax(U_k(v) + B_k(v)), B_k = s_k W2 with the gated
+    recurrent state s_k of rnn_state_step (W2 = W2t^T, the Markov head's projection), drawn
+    left to right with the draft's sampling rule and random streams (as draft_block).
+    Wg, W1, W2t, U in `dtype`; bg float32 [r].  Returns tokens, logit_x, lse, margin (as
+    draft_block) and states [bs, gamma, r] (float64 values of the bf16 / fp32 state s_k)."""
+    U = to_f64(U, dtype)
+    W1 = to_f64(W1, dtype)
+    W2t = to_f64(W2t, dtype)
+    Wg = to_f64(Wg, dtype)
+    bg = np.asarray(bg, dtype=np.float64)
+    bs, gamma, V = U.shape
+    r = W1.shape[1]
+    tokens = np.zeros((bs, gamma), dtype=np.int32)
+    logit_x = np.zeros((bs, gamma))
+    lse = np.zeros((bs, gamma))
+    margin = np.zeros((bs, gamma))
+    states = np.zeros((bs, gamma, r))
+    s = np.zeros((bs, r))
+    x_prev = np.asarray(anchor, dtype=np.int64).copy()
+    for k in range(1, gamma + 1):
+        s = rnn_state_step(W1[x_prev], s, Wg, bg, dtype)
+        states[:, k - 1] = s
+        ell = U[:, k - 1] + s @ W2t.T
+        for r_ in range(bs):
+            rid = r_ if req_ids is None else int(req_ids[r_])
+            tokens[r_, k - 1], logit_x[r_, k - 1], lse[r_, k - 1], margin[r_, k - 1] = \
+                _draw_position(ell[r_], temperature, seed, step, rid, k, chunk)
+        x_prev = tokens[:, k - 1].astype(np.int64)
+    return tokens, logit_x, lse, margin, states
 
 
 # ---------------------------------------------------------------------------
@@ -520,7 +587,7 @@ def pack(window, anchor, tokens, tiers, cap: int, gamma: Optional[int] = None):
 
 def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x, lse,
            U, W1, W2t, temperature: float, seed: int, step: int, dtype: str = "bf16",
-           chunk: int = CHUNK, req_ids=None, draft_logits=None):
+           chunk: int = CHUNK, req_ids=None, draft_logits=None, draft_states=None):
     """S5: accept the longest valid prefix of each request's window, then one more token.
 
     [SUMMARY, "Abstract" and "Architecture (drafter)"]: lossless speculative decoding accepts
@@ -539,6 +606,8 @@ def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x
     Draft probabilities come from logit_x - lse (the draft's outputs); the residual's draft
     distribution p_d is recomputed from U, W1, W2 at the rejected position, or, when the
     caller holds the draft's logits, taken from draft_logits [bs, gamma, V] (same dtype).
+    With the RNN head the low-rank factor of position k is the state s_k, not W1[x_{k-1}]:
+    draft_states [bs, gamma, r] (the states rnn_draft_block returns) then replaces the lookup.
 
     target_packed row cu[r] + k - 1 holds the target logits that score position k
     (k = 1..n_r).  Returns out_tokens [bs, gamma+1] (-1 padded), acc_len [bs],
@@ -600,7 +669,8 @@ def verify(target_packed, cu_seqlens, window, mode: int, anchor, tokens, logit_x
                 t = trow(k) / temperature
                 p_t = np.exp(t - logsumexp(t))
                 if draft_logits is None:
-                    d = (Uf[r, k - 1] + W1f[x[k - 1]] @ W2f.T) / temperature
+                    a_row = W1f[x[k - 1]] if draft_states is None else np.asarray(draft_states[r][k - 1], np.float64)
+                    d = (Uf[r, k - 1] + a_row @ W2f.T) / temperature
                 else:
                     d = Df[r, k - 1] / temperature
                 p_d = np.exp(d - logsumexp(d))

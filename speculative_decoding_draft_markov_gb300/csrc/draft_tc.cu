@@ -10,10 +10,15 @@
 // Work decomposition:
 //   tile      = 128 requests (TMEM lanes) x 128 vocabulary ids (= two 64-id draft chunks), K = r
 //   CTA       = persistent, one per SM; fixed 128-request M-tile, strided over vocabulary
-//               chunks; the gathered A operand W1[x_{k-1}] (128 x r) stays in shared memory
-//   warp 0    = TMA producer: W2t tiles in K-stages of 64 (evict-last) and the U_k tile
-//               (3-D map over [bs, gamma, V], evict-first)
-//   warp 1    = TMEM owner + single-thread tcgen05.mma issuer, commits to mbarriers
+//               chunks; the gathered A operand W1[x_{k-1}] (128 x r) stays in tensor memory
+//               (written once by the epilogue warps with tcgen05.st), which leaves the shared
+//               memory to the operand rings
+//   warp 0    = TMA producer: W2t tiles in K-stages of 64 (evict-last: W2t is re-read by every
+//               position and stays in L2) and the U_k tiles (3-D map over [bs, gamma, V],
+//               evict-first) in a four-deep ring: U is the stream that DRAM serves, so each SM
+//               keeps up to 64 KB of it in flight
+//   warp 1    = TMEM owner + single-thread tcgen05.mma issuer (A from TMEM, B from shared
+//               memory), commits to mbarriers
 //   warps 2-9 = epilogue, two warp sets of four (one warp per TMEM lane quarter, one request
 //               row per thread).  Set h takes the tiles t = h, h + 2, ... (accumulator buffer
 //               h, U stage h): it adds U_k to the accumulator row (adding U_k on the tensor
@@ -22,7 +27,7 @@
 //               draft chunks and keeps, in registers, the row's running (max, sum-exp) and
 //               best key.  Each CTA writes one
 //               entry per request at the end, so the select merges one entry per CTA column.
-//   2 TMEM accumulators (256 columns) let MMA, loads and epilogue overlap.
+//   2 TMEM accumulators (256 columns) let MMA, loads and epilogue overlap; A takes 128 more.
 // Every mbarrier wait is bounded (SM cycle-counter deadline + shared abort flag); on give-up the
 // kernel records DSPARK_ETIMEOUT, waits (bounded) for its own copies / MMAs in flight,
 // frees TMEM and returns.
@@ -46,14 +51,15 @@ constexpr int kBN = 128;
 static_assert(kBN == 2 * kDraftIds, "the epilogue splits a tile into two draft chunks");
 constexpr int kBK = 64;
 constexpr int kBStages = 6;                      // W2t ring: 1.5 tiles of K = 256
-constexpr int kUStages = 2;
+constexpr int kUStages = 4;                      // U_k ring: two tiles ahead per epilogue set
 constexpr int kAccBufs = 2;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr uint32_t kAtomBytes = kBM * kBK * 2;   // 16 KB: 128 rows x 128 bytes
 constexpr uint32_t kUHalf = kBM * 64 * 2;        // 16 KB: one 64-column half of a 128 x 128 bf16 tile
-constexpr uint32_t kTmemCols = kAccBufs * kBN;   // 256
+constexpr uint32_t kTmemA = kAccBufs * kBN;      // first TMEM column of A (256)
+constexpr uint32_t kTmemCols = 512;              // 2 accumulators x 128 + A (up to 128) -> 512
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Barriers {
@@ -61,11 +67,10 @@ struct Barriers {
   uint64_t u_full[kUStages], u_empty[kUStages];
   uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
   uint64_t drain;
-  uint64_t a_ready;  // the A operand is in shared memory (one arrival per epilogue warp)
+  uint64_t a_ready;  // the A operand is in tensor memory (one arrival per epilogue warp)
   uint32_t tmem_base;
   int abort;
   int mma_pending;   // the issuer's MMAs that nobody has waited for (set by the issuing thread)
-  int xrow[kBM];     // W1 row of each A row (-1: zero row)
   float4 xch[kBM];   // warp set 1's entry of each row, merged by set 0 at the end
 };
 
@@ -84,18 +89,10 @@ struct Params {
   uint64_t seed, step;
 };
 
-// Dynamic shared memory: A atoms | W2t ring | U stages | barriers.  The buffer is declared
-// 1024-byte aligned (128-byte swizzle atoms).
-constexpr size_t smem_bytes(int r) {
-  return size_t(r / kBK) * kAtomBytes + kBStages * size_t(kAtomBytes) + kUStages * 2 * size_t(kUHalf) +
-         sizeof(Barriers);
-}
-static_assert(smem_bytes(256) <= 232448, "dynamic shared memory beyond the 227 KB per-block limit");
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Dynamic shared memory: W2t ring | U stages | barriers.  The buffer is declared 1024-byte
+// aligned (128-byte swizzle atoms).
+constexpr size_t kSmemBytes = kBStages * size_t(kAtomBytes) + kUStages * 2 * size_t(kUHalf) + sizeof(Barriers);
+static_assert(kSmemBytes <= 232448, "dynamic shared memory beyond the 227 KB per-block limit");
 
 // The Gumbels G_{2c}, G_{2c+1} of the two draft chunks of vocabulary tile c, request `req`,
 // position k (Philox purpose 1): both sit in counter group c / 2, words 2 (c & 1) and + 1.
@@ -155,8 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     return;
   }
   const int nk = p.r / kBK;
-  uint8_t* sA = smem_raw;                    // nk atoms
-  uint8_t* sB = sA + nk * kAtomBytes;        // kBStages atoms
+  uint8_t* sB = smem_raw;                    // kBStages atoms
   uint8_t* sU = sB + kBStages * kAtomBytes;  // kUStages x 32 KB
   Barriers* bar = reinterpret_cast<Barriers*>(sU + kUStages * 2 * kUHalf);
   volatile int* abort_flag = &bar->abort;
@@ -269,12 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
             break;
           }
           tc::tc_fence_after();
-          const uint32_t a_addr = tc::smem_u32(sA + kb * kAtomBytes);
           const uint32_t b_addr = tc::smem_u32(sB + bstage * kAtomBytes);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            tc::mma_bf16(d, tc::sdesc_kmajor_sw128(a_addr + kk * 32), tc::sdesc_kmajor_sw128(b_addr + kk * 32),
-                         idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < kBK / 16; ++kk)  // A columns: 8 per 16 K values
+            tc::mma_bf16_ts(d, tmem_base + kTmemA + kb * (kBK / 2) + kk * 8,
+                            tc::sdesc_kmajor_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
           issued = true;
           tc::mma_commit(tc::smem_u32(&bar->b_empty[bstage]));
           if (++bstage == kBStages) { bstage = 0; bph ^= 1; }
@@ -317,32 +312,41 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     // x_{k-1} comes from the previous kernel (the select of position k-1): everything above
     // -- barrier set-up, TMEM, the producer's U / W2 prefetch, the Gumbels -- overlapped with it
     tc::grid_dependency_wait();
+    const uint32_t lane_base = tmem_base + (uint32_t(wq * 32) << 16);
     {
-      // A operand: rows m0..m0+127 of W1[x_{k-1}] in the 128-byte-swizzled K-major layout.
-      // Token ids first, then every 16-byte row chunk as an independent cp.async.
-      const int et = tid - 64;
-      for (int mm = et; mm < kBM; mm += kEpiThreads) {
-        const int gr = m0 + mm;
-        bar->xrow[mm] = gr < bs ? clamp_token((p.k == 1) ? p.anchor[gr] : p.tokens[size_t(gr) * p.gamma + p.k - 2], V)
-                                : -1;
+      // A operand into tensor memory: this row's W1[x_{k-1}] (a zero row past the batch), 64 K
+      // values (32 columns) per store.  Both warp sets of a lane quarter write it, set 0 the
+      // first half of K and set 1 the second, each issuing all of its loads before its stores
+      // (one round trip for the gather).
+      const int xp = grow < bs
+          ? clamp_token((p.k == 1) ? p.anchor[grow] : p.tokens[size_t(grow) * p.gamma + p.k - 2], V) : -1;
+      const uint4* src = reinterpret_cast<const uint4*>(p.W1 + size_t(xp < 0 ? 0 : xp) * r);
+      const int kb_lo = half ? (nk + 1) / 2 : 0, kb_hi = half ? nk : (nk + 1) / 2;  // warp-uniform
+      uint4 w[2][8];
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          w[j][q] = (xp >= 0 && kb_lo + j < kb_hi) ? src[(kb_lo + j) * 8 + q] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (kb_lo + j < kb_hi) {
+          uint32_t a32[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            a32[4 * q + 0] = w[j][q].x; a32[4 * q + 1] = w[j][q].y;
+            a32[4 * q + 2] = w[j][q].z; a32[4 * q + 3] = w[j][q].w;
+          }
+          tc::tmem_st32(lane_base + kTmemA + (kb_lo + j) * 32, a32);
+        }
       }
-      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-      const int cpr = r / 8;  // 16-byte chunks per row
-      for (int idx = et; idx < kBM * cpr; idx += kEpiThreads) {
-        const int row = idx / cpr, ch = idx % cpr;
-        const int xp = bar->xrow[row];
-        const int kb = ch >> 3, j = ch & 7;
-        const uint32_t dst = tc::smem_u32(sA + kb * kAtomBytes + row * 128 + ((j ^ (row & 7)) << 4));
-        cp_async16(dst, xp >= 0 ? p.W1 + size_t(xp) * r + ch * 8 : p.W1, xp >= 0 ? 16u : 0u);
-      }
-      cp_async_wait_all();
-      tc::fence_proxy_async_smem();
+      tc::tmem_st_wait();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->a_ready));
     }
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->a_ready));
 
-    const uint32_t taddr = tmem_base + (uint32_t(wq * 32) << 16) + half * kBN;
-    const uint8_t* ub = sU + half * 2 * kUHalf + m * 128;  // this row in U stage `half`
+    const uint32_t taddr = lane_base + half * kBN;
     // running (max, sum-exp) in log2 units: run_m = max of l c2, run_s = sum of 2^(l c2 - run_m)
     float run_m = -INFINITY, run_s = 0.f, best_key = -INFINITY;
     int best_c = INT_MAX;
@@ -351,8 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
       const int c = c0 + t * cstride;
       const int n0 = c * kBN;
       const int valid = min(kBN, V - n0);
+      // U stage of tile t: t mod kUStages (always one of this set's two), phase t / kUStages
+      const int us = t % kUStages;
+      const uint8_t* ub = sU + us * 2 * kUHalf + m * 128;  // this row in U stage us
       bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[half]), ph, deadline, abort_flag) &&
-                tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[half]), ph, deadline, abort_flag);
+                tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[us]), (t / kUStages) & 1, deadline, abort_flag);
       // one decision per warp before the .sync.aligned TMEM loads; warps run independently
       // (no named barrier in this loop), so a warp that gives up can hold up no other
       ok = __all_sync(0xFFFFFFFFu, ok);
@@ -378,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
         v[8 * j + 6] += bf16lo(q.w); v[8 * j + 7] += bf16hi(q.w);
       }
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->u_empty[half]));
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->u_empty[us]));
 
       if (p.greedy) {
         float best = -INFINITY;
@@ -470,7 +477,7 @@ cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t
   }
   static bool smem_set[tch::kMaxDevices] = {};
   static std::mutex smem_mu;
-  if (cudaError_t e = tch::set_smem_once(draft_tc_kernel, int(smem_bytes(256)), smem_set, &smem_mu)) return e;
+  if (cudaError_t e = tch::set_smem_once(draft_tc_kernel, int(kSmemBytes), smem_set, &smem_mu)) return e;
   const int grid = tch::vocab_grid(bs, n_chunks);
   Params prm{};
   prm.W1 = static_cast<const __nv_bfloat16*>(W1);
@@ -491,7 +498,7 @@ cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes(r);
+  cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

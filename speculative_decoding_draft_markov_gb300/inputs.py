@@ -28,6 +28,7 @@ Tensors produced (layouts are the library's):
   sts_T   [gamma] f32         per-position STS temperatures T_k = 1 + 0.1 k
   T_raw   [m_max + 1] f64     profiled step time in ms for M verify tokens
   tiers   [n] int32           captured graph totals (strictly increasing)
+  Wg, bg  [2r, r], [r]        RNN head gate weights and bias (with_rnn only)
 """
 from __future__ import annotations
 
@@ -145,7 +146,7 @@ def cost_curve_ms(wl: Workload) -> np.ndarray:
 # Host (numpy) generator
 # ---------------------------------------------------------------------------
 
-_TAGS = {"U": 1, "Ux": 2, "W1": 3, "W2t": 4, "anchor": 5, "noise": 6, "h": 7, "w": 8}
+_TAGS = {"U": 1, "Ux": 2, "W1": 3, "W2t": 4, "anchor": 5, "noise": 6, "h": 7, "w": 8, "Wg": 9, "bg": 10}
 
 
 def _rng(seed: int, tag: str, extra: int = 0) -> np.random.Generator:
@@ -158,8 +159,17 @@ def _as_dtype(x32: np.ndarray, dtype: str) -> np.ndarray:
     return f32_to_bf16_bits(x32)
 
 
-def make_host_inputs(wl: Workload, with_target: bool = True, with_hidden: bool = True) -> dict:
-    """All inputs of one step as numpy arrays (bf16 tensors as uint16 bit patterns)."""
+def rnn_gate_std(wl: Workload) -> float:
+    """Std of the RNN head's gate weights Wg [2r, r]: the gate pre-activation [e ; s] Wg has
+    unit variance when e and s have the weights' std (w_std)."""
+    return 1.0 / (wl.w_std * math.sqrt(2 * wl.r))
+
+
+def make_host_inputs(wl: Workload, with_target: bool = True, with_hidden: bool = True,
+                     with_rnn: bool = False) -> dict:
+    """All inputs of one step as numpy arrays (bf16 tensors as uint16 bit patterns).
+    with_rnn adds the RNN head's gate weights: Wg [2r, r] ~ N(0, rnn_gate_std^2) in the
+    workload's dtype and bg [r] ~ N(0, 1) float32."""
     bs, g, V, r, d = wl.bs, wl.gamma, wl.V, wl.r, wl.d
     s = wl.seed
     U32 = (_rng(s, "U").standard_normal((bs, g, V), dtype=np.float32) * np.float32(wl.u_std))
@@ -177,6 +187,10 @@ def make_host_inputs(wl: Workload, with_target: bool = True, with_hidden: bool =
     if with_hidden:
         out["h"] = _as_dtype(_rng(s, "h").standard_normal((bs, g, d), dtype=np.float32), wl.dtype)
         out["w"] = (_rng(s, "w").standard_normal(d + r) / math.sqrt(d + r)).astype(np.float32)
+    if with_rnn:
+        out["Wg"] = _as_dtype(_rng(s, "Wg").standard_normal((2 * r, r), dtype=np.float32)
+                              * np.float32(rnn_gate_std(wl)), wl.dtype)
+        out["bg"] = _rng(s, "bg").standard_normal(r).astype(np.float32)
     if with_target:
         # target row j (scoring the token at j+1) = base logits of that position + noise;
         # row gamma (the bonus row) takes an extra independent base-logit draw.
@@ -246,7 +260,8 @@ def gather_packed_target(target: np.ndarray, req: np.ndarray, pos: np.ndarray, r
 # Device (torch) generator for full-size workloads
 # ---------------------------------------------------------------------------
 
-def make_device_inputs(wl: Workload, device, with_target: bool = True, with_hidden: bool = True) -> dict:
+def make_device_inputs(wl: Workload, device, with_target: bool = True, with_hidden: bool = True,
+                       with_rnn: bool = False) -> dict:
     """Same recipe as make_host_inputs, drawn on the device with torch's seeded generator.
 
     The draws differ bit-wise from the numpy ones (another generator) but follow the same
@@ -282,6 +297,9 @@ def make_device_inputs(wl: Workload, device, with_target: bool = True, with_hidd
     if with_hidden:
         out["h"] = normal((bs, g, d), 1.0, "h").to(tdt)
         out["w"] = normal((d + r,), 1.0 / math.sqrt(d + r), "w")
+    if with_rnn:
+        out["Wg"] = normal((2 * r, r), rnn_gate_std(wl), "Wg").to(tdt)
+        out["bg"] = normal((r,), 1.0, "bg")
     if with_target:
         sig = torch.tensor(sigma_per_request(bs, wl.sigmas), dtype=torch.float32, device=device)
         target = torch.empty((bs, g + 1, V), device=device, dtype=tdt)

@@ -43,6 +43,14 @@ MUTS = {
  "sts_label_offby1": ("        y = (c >= k + 1).astype(np.int64)", "        y = (c >= k).astype(np.int64)", "tests/test_oracle_observe.py"),
  "sts_no_carry": ("        prev = prev / (1.0 + np.exp(-z[:, k] / T[k]))", "        prev = prev", "tests/test_oracle_observe.py"),
  "sts_argmax": ("        g_star = int(np.argmin(table[k]))  # first minimum", "        g_star = int(np.argmax(table[k]))", "tests/test_oracle_observe.py"),
+ "rnn_gate_swapped": ("    s = g * s_prev + (1.0 - g) * e\n", "    s = (1.0 - g) * s_prev + g * e\n",
+                      "tests/test_oracle_rnn.py::test_closed_gate_is_the_markov_head"),
+ "rnn_state_not_carried": ("        s = rnn_state_step(W1[x_prev], s, Wg, bg, dtype)",
+                           "        s = rnn_state_step(W1[x_prev], np.zeros_like(s), Wg, bg, dtype)",
+                           "tests/test_oracle_rnn.py::test_joint_law_of_the_first_three_tokens"),
+ "rnn_verify_markov_row": ("a_row = W1f[x[k - 1]] if draft_states is None else np.asarray(draft_states[r][k - 1], np.float64)",
+                           "a_row = W1f[x[k - 1]]",
+                           "tests/test_oracle_rnn.py::test_rnn_draft_first_committed_token_is_target_distributed"),
  "cdf_nonstrict": ("    j = int(np.argmax(C > t))", "    j = int(np.argmax(C >= t))", "tests/test_oracle_sampling.py::test_inverse_cdf_by_hand"),
  "cdf_reversed_sums": ("    C = np.cumsum(w)\n", "    C = np.cumsum(w[::-1])\n", "tests/test_oracle_sampling.py::test_inverse_cdf_by_hand"),
  "cdf_wrong_uniform": ("    u = float(uniform(seed, step, purpose_elem, req, pos, np.array([0]))[0])",
