@@ -314,7 +314,7 @@ class Path:
     mode: "compact" (confidence, global scheduler + pack, compact verify) or "static" (pack of
     the whole block, static verify); tau: sampling temperature (0 = greedy)."""
 
-    def __init__(self, wl, dev, mode="compact", tau=None, sched=SCHED):
+    def __init__(self, wl, dev, mode="compact", tau=None, sched=SCHED, rnn=False):
         import torch
 
         from speculative_decoding_draft_markov_gb300 import binding as B
@@ -323,7 +323,9 @@ class Path:
         self.B, self.S = B, S
         self.wl, self.dev, self.mode, self.sched = wl, dev, mode, sched
         self.tau = wl.temperature if tau is None else tau
-        self.inp = I.make_device_inputs(wl, dev)
+        self.inp = I.make_device_inputs(wl, dev, with_rnn=rnn)
+        self.states = (torch.empty((wl.bs, wl.gamma, wl.r), dtype=self.inp["U"].dtype, device=dev)
+                       if rnn else None)
         self.cap = int(I.tiers_for(wl)[-1]) if len(I.tiers_for(wl)) else wl.bs * (wl.gamma + 1)
         self.cap = max(self.cap, wl.bs * (wl.gamma + 1))
         self.buf = S.StepBuffers.allocate(wl.bs, wl.gamma, wl.V, self.cap, self.inp["U"].dtype, dev)
@@ -332,10 +334,15 @@ class Path:
         self.fwd = S.gather_target_forward(self.inp["target"])
         self.ring = S.zos_ring(dev)
         self.vmode = B.DSPARK_COMPACT if mode == "compact" else B.DSPARK_STATIC
-        self.launches = 2 * wl.gamma + (2 if mode == "compact" else 1) + (4 if self.tau > 0 else 2)
+        self.launches = (3 if rnn else 2) * wl.gamma + (2 if mode == "compact" else 1) + (4 if self.tau > 0 else 2)
 
     def draft(self, it):
         inp, buf = self.inp, self.buf
+        if self.states is not None:  # the RNN sequential head
+            self.B.dspark_draft_block_rnn(inp["U"], inp["W1"], inp["W2t"], inp["Wg"], inp["bg"], inp["anchor"],
+                                          self.tau, self.wl.seed, it, buf.tokens, buf.logit_x, buf.lse, self.states,
+                                          buf.ws)
+            return
         self.B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], self.tau, self.wl.seed, it,
                                   buf.tokens, buf.logit_x, buf.lse, buf.ws)
 
@@ -360,7 +367,7 @@ class Path:
         # runs beside the verify, joined at the end of the stage
         if zos:
             self.S.schedule_budget(self.buf, self.sps, self.ring, it, stream, side)
-        self.S.verify(self.inp, self.buf, self.tau, self.wl.seed, it, self.vmode)
+        self.S.verify(self.inp, self.buf, self.tau, self.wl.seed, it, self.vmode, states=self.states)
         if zos:
             self.S.join_budget(stream, side)
 
@@ -631,6 +638,24 @@ def run_ours(args, rank: int, world: int):
                 "gpu_launches": (path.launches + 2) * args.steps, "clocks": zclocks},
     }
     del path
+    # the same step with the RNN sequential head (device-timed; the draft adds one state-update
+    # launch per position and verify recomputes p_d from the states)
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+    rpath = Path(wl, dev, "compact", rnn=True)
+    rseg, rtokens, rrows, _, _, rclocks = time_steps(rpath, args.steps, args.warmup, world=world)
+    (rtotal_ms,), (rtokens,) = aggregate_over_ranks([float((rseg[:, 0] + rseg[:, 1]).sum())], [rtokens], dev)
+    rstage = {"draft": float(rseg[:, 2].mean()), "conf_sched_pack": float((rseg[:, 0] - rseg[:, 2]).mean()),
+              "verify": float(rseg[:, 1].mean())}
+    rroof = rooflines(wl, rstage, rrows / args.steps, rpath.tau)
+    res["rnn"] = {"value": rtokens / (rtotal_ms * 1e-3), "unit": "tokens/s", "ms_per_step": rtotal_ms / args.steps,
+                  "tokens_per_step": rtokens / args.steps / world, "stage_ms": rstage,
+                  "draft_frac_hbm": rroof["frac"], "verify_frac_hbm": rroof["verify"]["frac"],
+                  "head": "RNN sequential head: gated recurrent state s_k (bf16), bias s_k W2; one state-update "
+                          "launch per position before the vocabulary pass",
+                  "gpu_launches": rpath.launches * args.steps, "clocks": rclocks}
+    del rpath
     if not args.no_configs:
         import gc
         gc.collect()

@@ -152,6 +152,26 @@ DSPARK_API int dspark_draft_block(const void* U, const void* W1, const void* W2t
                        int32_t* tokens, float* logit_x, float* lse,
                        void* ws, size_t ws_bytes, dspark_stream_t stream);
 
+/* S1 with the RNN sequential head ([SUMMARY] "Architecture (drafter)", RNN head: a gated
+ * recurrent state s_k carried across the block, so each position sees the whole prefix).  The
+ * pages give no equations; this library's reading, per request:
+ *     e_k = W1[x_{k-1}]  (x_0 = anchor),   s_0 = 0
+ *     g_k = sigmoid([e_k ; s_{k-1}] Wg + bg)                 Wg [2r, r], bg [r]
+ *     s_k = g_k * s_{k-1} + (1 - g_k) * e_k                  held in `dtype` (bf16: rounded to
+ *                                                             nearest even after each update)
+ *     l_k = U[:, k-1] + s_k . W2,  then the draw exactly as dspark_draft_block (same random
+ *     streams, outputs and temperature rule).  A closed gate (g = 0) is the Markov head.
+ *   Wg       device [2r, r] (dtype), row j < r multiplies e_k[j], row r + j multiplies s_{k-1}[j]
+ *   bg       device [r] fp32
+ *   states   device [bs, gamma, r] (dtype) out: s_1 .. s_gamma (dspark_verify's draft_states)
+ *   other arguments, limits and errors as dspark_draft_block.
+ * One extra small launch per position (the state update: a [bs, 2r] x [2r, r] GEMM). */
+DSPARK_API int dspark_draft_block_rnn(const void* U, const void* W1, const void* W2t, const void* Wg,
+                                      const float* bg, int dtype, const int32_t* anchor, int bs, int gamma,
+                                      int V, int r, float temperature, uint64_t seed, uint64_t step,
+                                      int32_t* tokens, float* logit_x, float* lse, void* states, void* ws,
+                                      size_t ws_bytes, dspark_stream_t stream);
+
 /* S2. Confidence head, sequential temperature scaling and prefix survival ([SUMMARY]
  * "Verification scheduling": confidence head, STS, prefix survival):
  *     z_{r,k} = w[0:d] . h[r, k-1] + w[d:d+r] . W1[x_{r,k-1}] + b      (x_0 = anchor)
@@ -265,14 +285,18 @@ DSPARK_API int dspark_schedule_pack(const float* surv, int bs, int gamma, const 
  *   draft_logits device [bs, gamma, V] (dtype) or NULL: the draft's logits l_k of every
  *               position, for callers that hold them (another drafter, or a caller that kept
  *               them); lse must be their log-sum-exp at temperature (as dspark_draft_block
- *               writes it).  Given, U, W1, W2t (may be NULL) and r are not used; NULL, U, W1,
- *               W2t are required and p_d is recomputed.
+ *               writes it).  Given, U, W1, W2t (may be NULL), draft_states and r are not used;
+ *               NULL, U, W1, W2t are required and p_d is recomputed.
+ *   draft_states device [bs, gamma, r] (dtype) or NULL: the RNN head's states s_k
+ *               (dspark_draft_block_rnn); the recompute of p_d at position k* then takes
+ *               U[:, k*-1] + s_k* . W2 instead of the Markov head's U + W1[x_{k*-1}] . W2.
  * Limits: as dspark_draft_block. */
 DSPARK_API int dspark_verify(const void* target, int dtype, const int32_t* cu_seqlens,
                   const int32_t* window, int mode, int bs, int gamma, int V,
                   const int32_t* anchor, const int32_t* tokens, const float* logit_x,
-                  const float* lse, const void* draft_logits, const void* U, const void* W1,
-                  const void* W2t, int r, float temperature, uint64_t seed, uint64_t step,
+                  const float* lse, const void* draft_logits, const void* draft_states,
+                  const void* U, const void* W1, const void* W2t, int r, float temperature,
+                  uint64_t seed, uint64_t step,
                   int32_t* out_tokens, int32_t* acc_len, int32_t* ceiling,
                   void* ws, size_t ws_bytes, dspark_stream_t stream);
 

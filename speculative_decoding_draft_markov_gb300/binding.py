@@ -34,6 +34,8 @@ _SIGS = {
                                 _vp, _vp, _vp, _vp, _sz, _vp]),
     "dspark_draft_block_noalloc": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _u64, _u64,
                                         _vp, _vp, _vp, _vp, _vp]),
+    "dspark_draft_block_rnn": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _u64, _u64,
+                                    _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dspark_confidence": (_i, [_vp, _vp, _i, _vp, _vp, _vp, _f, _vp, _i, _i, _i, _i, _i,
                                _vp, _vp, _vp, _vp]),
     "dspark_schedule": (_i, [_vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -46,7 +48,7 @@ _SIGS = {
     "dspark_obs_report": (_i, [_vp, _i, _vp]),
     "dspark_sts_fit_workspace_bytes": (_sz, [_i, _i]),
     "dspark_sts_fit": (_i, [_vp, _vp, _i, _i, _vp, _i, _i, _vp, _vp, _vp, _sz, _vp]),
-    "dspark_verify": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+    "dspark_verify": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                            _i, _f, _u64, _u64, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
@@ -190,6 +192,17 @@ def dspark_draft_block_noalloc(U, W1, W2t, anchor, temperature, seed, step, toke
            "dspark_draft_block_noalloc")
 
 
+def dspark_draft_block_rnn(U, W1, W2t, Wg, bg, anchor, temperature, seed, step, tokens, logit_x, lse, states, ws,
+                           stream=None):
+    """The block draft with the RNN head: Wg [2r, r] (U's dtype), bg [r] fp32; writes the
+    recurrent states s_1..s_gamma into states [bs, gamma, r] (U's dtype)."""
+    bs, gamma, V = U.shape
+    r = W1.shape[1]
+    _check(lib().dspark_draft_block_rnn(_p(U), _p(W1), _p(W2t), _p(Wg), _p(bg), _dtype(U), _p(anchor), bs, gamma, V,
+                                        r, float(temperature), int(seed), int(step), _p(tokens), _p(logit_x), _p(lse),
+                                        _p(states), _p(ws), ws.numel(), _stream(stream)), "dspark_draft_block_rnn")
+
+
 def dspark_confidence(h, W1, anchor, tokens, w, b, sts_T, conf, surv, stream=None, z_logit=None):
     bs, gamma, d = h.shape
     V, r = W1.shape
@@ -238,13 +251,16 @@ def dspark_schedule_pack(surv, sps, mode, window, K_out, theta_out, anchor, toke
 
 
 def dspark_verify(target, cu_seqlens, window, mode, anchor, tokens, logit_x, lse, U, W1, W2t,
-                  temperature, seed, step, out_tokens, acc_len, ceiling, ws, stream=None, draft_logits=None):
-    """draft_logits [bs, gamma, V] (optional): the draft's logits; then U, W1, W2t may be None."""
+                  temperature, seed, step, out_tokens, acc_len, ceiling, ws, stream=None, draft_logits=None,
+                  draft_states=None):
+    """draft_logits [bs, gamma, V] (optional): the draft's logits; then U, W1, W2t may be None.
+    draft_states [bs, gamma, r] (optional): the RNN head's states (dspark_draft_block_rnn)."""
     bs, gamma = tokens.shape
     V = target.shape[1]
     r = W1.shape[1] if W1 is not None else 0
     _check(lib().dspark_verify(_p(target), _dtype(target), _p(cu_seqlens), _p(window), int(mode), bs, gamma,
-                               V, _p(anchor), _p(tokens), _p(logit_x), _p(lse), _p(draft_logits), _p(U), _p(W1),
+                               V, _p(anchor), _p(tokens), _p(logit_x), _p(lse), _p(draft_logits),
+                               _p(draft_states), _p(U), _p(W1),
                                _p(W2t), r,
                                float(temperature), int(seed), int(step), _p(out_tokens), _p(acc_len),
                                _p(ceiling), _p(ws), ws.numel(), _stream(stream)), "dspark_verify")

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libdspark.so")
-SOURCES = ["api.cu", "draft.cu", "draft_tc.cu", "decide_tc.cu", "sched_pack.cu", "verify.cu", "draft_noalloc.cu",
+SOURCES = ["api.cu", "draft.cu", "draft_tc.cu", "decide_tc.cu", "sched_pack.cu", "verify.cu", "draft_noalloc.cu", "rnn.cu",
            "observe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

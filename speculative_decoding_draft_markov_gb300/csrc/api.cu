@@ -132,18 +132,16 @@ int dspark_build_sps(const double* T_raw, int m_max, const int32_t* tiers, int n
   return DSPARK_OK;
 }
 
-int dspark_draft_block(const void* U, const void* W1, const void* W2t, int dtype,
-                       const int32_t* anchor, int bs, int gamma, int V, int r, float temperature,
-                       uint64_t seed, uint64_t step, int32_t* tokens, float* logit_x, float* lse,
-                       void* ws, size_t ws_bytes, dspark_stream_t stream) {
-  if (!U || !W1 || !W2t || !anchor || !tokens || !logit_x || !lse) return DSPARK_EINVAL;
-  if (!valid_dtype(dtype) || !std::isfinite(temperature) || temperature < 0.f) return DSPARK_EINVAL;
-  if (int e = check_core(bs, gamma, V, r)) return e;
-  if (!al(U, 16) || !al(W1, 16) || !al(W2t, 16) || !al(anchor, 4) || !al(tokens, 4) ||
-      !al(logit_x, 4) || !al(lse, 4))
-    return DSPARK_EINVAL;
-  if (int e = check_ws(ws, ws_bytes, bs, gamma, V)) return e;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+}  // extern "C"
+
+namespace {
+
+// The gamma positions of a block draft, left to right: per position the RNN head's state update
+// (states non-null), the vocabulary pass (tensor cores or CUDA cores) and the select.
+int draft_positions(int dtype, const void* U, const void* W1, const void* W2t, const void* Wg, const float* bg,
+                    void* states, const int32_t* anchor, int bs, int gamma, int V, int r, float temperature,
+                    uint64_t seed, uint64_t step, int32_t* tokens, float* logit_x, float* lse, void* ws,
+                    cudaStream_t s) {
   const WsLayout L = ws_layout(bs, gamma, V);
   char* w = static_cast<char*>(ws);
   void* stats = w + L.stats;
@@ -152,17 +150,58 @@ int dspark_draft_block(const void* U, const void* W1, const void* W2t, int dtype
   const float inv_tau = greedy ? 1.f : static_cast<float>(1.0 / static_cast<double>(temperature));
   const bool tc = draft_tc_supported(dtype, bs, V, r);
   for (int k = 1; k <= gamma; ++k) {
+    if (states && launch_rnn_state(dtype, W1, Wg, bg, anchor, tokens, states, bs, gamma, V, r, k, s) != cudaSuccess)
+      return DSPARK_ECUDA;
     int n_slots = n_draft_chunks(V);  // the CUDA-core pass: one slot per draft chunk
-    cudaError_t e = tc ? launch_draft_stats_tc(U, W1, W2t, anchor, tokens, bs, gamma, V, r, k, inv_tau,
+    cudaError_t e = tc ? launch_draft_stats_tc(U, W1, W2t, states, anchor, tokens, bs, gamma, V, r, k, inv_tau,
                                                greedy, seed, step, stats, L.n_chunks, &n_slots, status, s)
-                       : launch_draft_stats_simt(dtype, U, W1, W2t, anchor, tokens, bs, gamma, V, r, k,
+                       : launch_draft_stats_simt(dtype, U, W1, W2t, states, anchor, tokens, bs, gamma, V, r, k,
                                                  inv_tau, greedy, seed, step, stats, n_slots, s);
     if (e != cudaSuccess) return DSPARK_ECUDA;
-    e = launch_draft_select(dtype, stats, n_slots, U, W1, W2t, anchor, tokens, logit_x, lse, bs,
+    e = launch_draft_select(dtype, stats, n_slots, U, W1, W2t, states, anchor, tokens, logit_x, lse, bs,
                             gamma, V, r, k, inv_tau, greedy, seed, step, status, s);
     if (e != cudaSuccess) return DSPARK_ECUDA;
   }
   return DSPARK_OK;
+}
+
+int check_draft_args(const void* U, const void* W1, const void* W2t, int dtype, const int32_t* anchor, int bs,
+                     int gamma, int V, int r, float temperature, const int32_t* tokens, const float* logit_x,
+                     const float* lse) {
+  if (!U || !W1 || !W2t || !anchor || !tokens || !logit_x || !lse) return DSPARK_EINVAL;
+  if (!valid_dtype(dtype) || !std::isfinite(temperature) || temperature < 0.f) return DSPARK_EINVAL;
+  if (int e = check_core(bs, gamma, V, r)) return e;
+  if (!al(U, 16) || !al(W1, 16) || !al(W2t, 16) || !al(anchor, 4) || !al(tokens, 4) ||
+      !al(logit_x, 4) || !al(lse, 4))
+    return DSPARK_EINVAL;
+  return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dspark_draft_block(const void* U, const void* W1, const void* W2t, int dtype,
+                       const int32_t* anchor, int bs, int gamma, int V, int r, float temperature,
+                       uint64_t seed, uint64_t step, int32_t* tokens, float* logit_x, float* lse,
+                       void* ws, size_t ws_bytes, dspark_stream_t stream) {
+  if (int e = check_draft_args(U, W1, W2t, dtype, anchor, bs, gamma, V, r, temperature, tokens, logit_x, lse))
+    return e;
+  if (int e = check_ws(ws, ws_bytes, bs, gamma, V)) return e;
+  return draft_positions(dtype, U, W1, W2t, nullptr, nullptr, nullptr, anchor, bs, gamma, V, r, temperature, seed,
+                         step, tokens, logit_x, lse, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dspark_draft_block_rnn(const void* U, const void* W1, const void* W2t, const void* Wg, const float* bg,
+                           int dtype, const int32_t* anchor, int bs, int gamma, int V, int r, float temperature,
+                           uint64_t seed, uint64_t step, int32_t* tokens, float* logit_x, float* lse,
+                           void* states, void* ws, size_t ws_bytes, dspark_stream_t stream) {
+  if (int e = check_draft_args(U, W1, W2t, dtype, anchor, bs, gamma, V, r, temperature, tokens, logit_x, lse))
+    return e;
+  if (!Wg || !bg || !states || !al(Wg, 16) || !al(bg, 16) || !al(states, 16)) return DSPARK_EINVAL;
+  if (int e = check_ws(ws, ws_bytes, bs, gamma, V)) return e;
+  return draft_positions(dtype, U, W1, W2t, Wg, bg, states, anchor, bs, gamma, V, r, temperature, seed, step,
+                         tokens, logit_x, lse, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int dspark_confidence(const void* h, const void* W1, int dtype, const int32_t* anchor,
@@ -256,18 +295,19 @@ int dspark_schedule_pack(const float* surv, int bs, int gamma, const double* sps
 
 int dspark_verify(const void* target, int dtype, const int32_t* cu_seqlens, const int32_t* window,
                   int mode, int bs, int gamma, int V, const int32_t* anchor, const int32_t* tokens,
-                  const float* logit_x, const float* lse, const void* draft_logits, const void* U,
-                  const void* W1, const void* W2t, int r, float temperature, uint64_t seed,
+                  const float* logit_x, const float* lse, const void* draft_logits, const void* draft_states,
+                  const void* U, const void* W1, const void* W2t, int r, float temperature, uint64_t seed,
                   uint64_t step, int32_t* out_tokens, int32_t* acc_len, int32_t* ceiling, void* ws,
                   size_t ws_bytes, dspark_stream_t stream) {
   if (!target || !cu_seqlens || !anchor || !tokens || !logit_x || !lse || !out_tokens || !acc_len)
     return DSPARK_EINVAL;
   if (!draft_logits && (!U || !W1 || !W2t)) return DSPARK_EINVAL;  // p_d needs one source
-  if (draft_logits) {  // U, W1, W2t and r unused
+  if (draft_logits) {  // U, W1, W2t, draft_states and r unused
     if (!al(draft_logits, 16)) return DSPARK_EINVAL;
-    U = W1 = W2t = nullptr;
+    U = W1 = W2t = draft_states = nullptr;
     r = 32;
   }
+  if (draft_states && !al(draft_states, 16)) return DSPARK_EINVAL;
   if (mode != DSPARK_STATIC && mode != DSPARK_COMPACT && mode != DSPARK_CAP_ACCEPT) return DSPARK_EINVAL;
   if (mode != DSPARK_STATIC && !window) return DSPARK_EINVAL;
   if (mode == DSPARK_CAP_ACCEPT && !ceiling) return DSPARK_EINVAL;
@@ -278,7 +318,7 @@ int dspark_verify(const void* target, int dtype, const int32_t* cu_seqlens, cons
   const int greedy = temperature == 0.f;
   const float inv_tau = greedy ? 1.f : static_cast<float>(1.0 / static_cast<double>(temperature));
   return cuda_status(launch_verify(dtype, target, cu_seqlens, window, mode, bs, gamma, V, anchor,
-                                   tokens, logit_x, lse, draft_logits, U, W1, W2t, r, inv_tau, greedy,
+                                   tokens, logit_x, lse, draft_logits, U, W1, W2t, draft_states, r, inv_tau, greedy,
                                    seed, step, out_tokens, acc_len, ceiling, ws,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -110,6 +110,17 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t code) {
 // can never address outside W1 (the kernels that own a status word also report it).
 __device__ __forceinline__ int clamp_token(int x, int V) { return x < 0 ? 0 : (x >= V ? V - 1 : x); }
 
+// The row of the draft's low-rank factor that multiplies W2 at position k of request b: the
+// Markov head's lookup W1[x_{k-1}] (x_0 = the anchor), or, with the RNN head, its recurrent
+// state s_k, row (b, k - 1) of states [bs, gamma, r].
+template <typename T>
+__device__ __forceinline__ const T* factor_row(const T* W1, const T* states, const int32_t* anchor,
+                                               const int32_t* tokens, int b, int k, int gamma, int V, int r) {
+  if (states) return states + (size_t(b) * gamma + (k - 1)) * r;
+  const int xp = clamp_token((k == 1) ? anchor[b] : tokens[size_t(b) * gamma + k - 2], V);
+  return W1 + size_t(xp) * r;
+}
+
 // ----------------------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): per round
 //   (c0, c1, c2, c3) <- (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0))

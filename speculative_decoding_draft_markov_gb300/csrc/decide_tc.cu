@@ -83,6 +83,7 @@ struct RowMeta {
 
 struct Params {
   const __nv_bfloat16* W1;
+  const __nv_bfloat16* states;  // RNN head: the draft's states s_k [bs, gamma, r] (A rows); else null
   const __nv_bfloat16* U;
   const __nv_bfloat16* target;
   const int32_t* anchor;
@@ -354,14 +355,12 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
     const RowMeta rm = meta[m];
     const uint32_t lane_base = tmem_base + (uint32_t(wq * 32) << 16);
     if (set == 0) {
-      // A operand into TMEM: this row's W1[x] (zero unless the request's decision is a
-      // residual), 64 K values (32 columns) per store
-      int xp = -1;
-      if (rm.resid) {
-        const Decision d = p.dec[grow];
-        xp = clamp_token((d.kdec == 1) ? p.anchor[grow] : p.tokens[size_t(grow) * p.gamma + d.kdec - 2], V);
-      }
-      const uint4* src = reinterpret_cast<const uint4*>(p.W1 + size_t(xp < 0 ? 0 : xp) * r);
+      // A operand into TMEM: this row's factor at the deciding position -- W1[x] (Markov head)
+      // or the state s_k (RNN head); zero unless the request's decision is a residual -- 64 K
+      // values (32 columns) per store
+      const int xp = rm.resid ? 0 : -1;  // -1: a zero row
+      const uint4* src = reinterpret_cast<const uint4*>(
+          rm.resid ? factor_row(p.W1, p.states, p.anchor, p.tokens, grow, rm.kdec, p.gamma, V, r) : p.W1);
       for (int kb = 0; kb < nk; ++kb) {
         uint32_t a32[32];
 #pragma unroll
@@ -503,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
 }  // namespace
 
 cudaError_t launch_decision_stats_tc(const void* target, const void* U, const void* W1, const void* W2t,
-                                     const int32_t* anchor, const int32_t* tokens, const float* lse_d,
+                                     const void* states, const int32_t* anchor, const int32_t* tokens, const float* lse_d,
                                      const void* rs, const void* dec, int bs, int gamma, int V, int r,
                                      float inv_tau, uint64_t seed, uint64_t step, void* entries,
                                      int n_chunks, int* n_slots, uint32_t* status, cudaStream_t s) {
@@ -516,6 +515,7 @@ cudaError_t launch_decision_stats_tc(const void* target, const void* U, const vo
   if (cudaError_t e = tch::set_smem_once(decide_tc_kernel, int(kSmemBytes), smem_set, &smem_mu)) return e;
   Params prm{};
   prm.W1 = static_cast<const __nv_bfloat16*>(W1);
+  prm.states = static_cast<const __nv_bfloat16*>(states);
   prm.U = static_cast<const __nv_bfloat16*>(U);
   prm.target = static_cast<const __nv_bfloat16*>(target);
   prm.anchor = anchor;

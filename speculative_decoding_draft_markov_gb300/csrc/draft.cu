@@ -48,7 +48,7 @@ __device__ __forceinline__ ArgMax half_argmax(ArgMax a, float* sv, int* si) {
 
 template <typename T, int RB>
 __global__ void __launch_bounds__(128) draft_stats_simt_kernel(
-    const T* __restrict__ U, const T* __restrict__ W1, const T* __restrict__ W2t,
+    const T* __restrict__ U, const T* __restrict__ W1, const T* __restrict__ W2t, const T* __restrict__ states,
     const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens, int bs, int gamma,
     int V, int r, int k, float inv_tau, int greedy, uint64_t seed, uint64_t step,
     float4* __restrict__ entries, int n_slots) {
@@ -68,10 +68,7 @@ __global__ void __launch_bounds__(128) draft_stats_simt_kernel(
     for (int e = tid; e < RB * sl; e += kChunk) {
       const int rr = e / sl, ii = e % sl, row = rb + rr;
       float val = 0.f;
-      if (row < bs) {
-        const int xp = clamp_token((k == 1) ? anchor[row] : tokens[row * gamma + k - 2], V);
-        val = ld_f32(W1, size_t(xp) * r + i0 + ii);
-      }
+      if (row < bs) val = ld_f32(factor_row(W1, states, anchor, tokens, row, k, gamma, V, r), i0 + ii);
       sA[rr][ii] = val;
     }
     for (int e = tid; e < kChunk * sl; e += kChunk) {
@@ -125,8 +122,9 @@ __global__ void __launch_bounds__(128) draft_stats_simt_kernel(
 template <typename T>
 __global__ void __launch_bounds__(256, 1) draft_select_kernel(
     const float4* __restrict__ entries, int n_slots, const T* __restrict__ U,
-    const T* __restrict__ W1, const T* __restrict__ W2t, const int32_t* __restrict__ anchor,
-    int32_t* __restrict__ tokens, float* __restrict__ logit_x, float* __restrict__ lse, int bs,
+    const T* __restrict__ W1, const T* __restrict__ W2t, const T* __restrict__ states,
+    const int32_t* __restrict__ anchor, int32_t* __restrict__ tokens, float* __restrict__ logit_x,
+    float* __restrict__ lse, int bs,
     int gamma, int V, int r, int k, float inv_tau, int greedy, uint64_t seed, uint64_t step,
     uint32_t* status) {
   __shared__ float sA[256];
@@ -141,11 +139,11 @@ __global__ void __launch_bounds__(256, 1) draft_select_kernel(
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const size_t out = size_t(b) * gamma + (k - 1);
 
-  // the W1 row of x_{k-1} does not depend on the draw: warps 1..7 fetch it while warp 0 merges
-  // the entries, so that neither waits for the other's loads
+  // the factor row (W1[x_{k-1}], or the RNN state s_k) does not depend on the draw: warps 1..7
+  // fetch it while warp 0 merges the entries, so that neither waits for the other's loads
   if (!greedy && tid >= 32) {
-    const int xp = clamp_token((k == 1) ? anchor[b] : tokens[size_t(b) * gamma + k - 2], V);
-    for (int i = tid - 32; i < r; i += 224) sA[i] = ld_f32(W1, size_t(xp) * r + i);
+    const T* arow = factor_row(W1, states, anchor, tokens, b, k, gamma, V, r);
+    for (int i = tid - 32; i < r; i += 224) sA[i] = ld_f32(arow, i);
   }
   if (tid < 32) {
     LsePair lp{-INFINITY, 0.f};
@@ -226,7 +224,7 @@ __global__ void __launch_bounds__(256, 1) draft_select_kernel(
   }
 }
 
-cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, const void* W2t,
+cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, const void* W2t, const void* states,
                                     const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
                                     int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
                                     uint64_t step, void* entries, int n_slots, cudaStream_t s) {
@@ -234,23 +232,24 @@ cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, co
   dim3 grid((V + kChunk - 1) / kChunk, (bs + RB - 1) / RB);
   if (dtype == DSPARK_F32)
     draft_stats_simt_kernel<float, RB><<<grid, kChunk, 0, s>>>(
-        (const float*)U, (const float*)W1, (const float*)W2t, anchor, tokens, bs, gamma, V, r, k,
+        (const float*)U, (const float*)W1, (const float*)W2t, (const float*)states, anchor, tokens, bs, gamma, V, r, k,
         inv_tau, greedy, seed, step, (float4*)entries, n_slots);
   else
     draft_stats_simt_kernel<__nv_bfloat16, RB><<<grid, kChunk, 0, s>>>(
-        (const __nv_bfloat16*)U, (const __nv_bfloat16*)W1, (const __nv_bfloat16*)W2t, anchor,
+        (const __nv_bfloat16*)U, (const __nv_bfloat16*)W1, (const __nv_bfloat16*)W2t, (const __nv_bfloat16*)states,
+        anchor,
         tokens, bs, gamma, V, r, k, inv_tau, greedy, seed, step, (float4*)entries, n_slots);
   return cudaGetLastError();
 }
 
 cudaError_t launch_draft_select(int dtype, const void* entries, int n_slots, const void* U,
-                                const void* W1, const void* W2t, const int32_t* anchor,
+                                const void* W1, const void* W2t, const void* states, const int32_t* anchor,
                                 int32_t* tokens, float* logit_x, float* lse, int bs, int gamma,
                                 int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
                                 uint64_t step, uint32_t* status, cudaStream_t s) {
   if (dtype == DSPARK_F32)
     draft_select_kernel<float><<<bs, 256, 0, s>>>(
-        (const float4*)entries, n_slots, (const float*)U, (const float*)W1, (const float*)W2t,
+        (const float4*)entries, n_slots, (const float*)U, (const float*)W1, (const float*)W2t, (const float*)states,
         anchor, tokens, logit_x, lse, bs, gamma, V, r, k, inv_tau, greedy, seed, step, status);
   else {
     cudaLaunchConfig_t cfg = {};
@@ -264,7 +263,7 @@ cudaError_t launch_draft_select(int dtype, const void* entries, int n_slots, con
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, draft_select_kernel<__nv_bfloat16>, (const float4*)entries, n_slots,
                               (const __nv_bfloat16*)U, (const __nv_bfloat16*)W1, (const __nv_bfloat16*)W2t,
-                              anchor, tokens, logit_x, lse, bs, gamma, V, r, k, inv_tau, greedy, seed, step,
+                              (const __nv_bfloat16*)states, anchor, tokens, logit_x, lse, bs, gamma, V, r, k, inv_tau, greedy, seed, step,
                               status);
   }
   return cudaGetLastError();

@@ -96,12 +96,12 @@ extern "C" DSPARK_API int dspark_draft_block_noalloc(
   const float inv_tau = greedy ? 1.f : static_cast<float>(1.0 / static_cast<double>(temperature));
   for (int k = 1; k <= gamma; ++k) {
     int n_slots = n_draft_chunks(V);  // the CUDA-core pass: one slot per draft chunk
-    cudaError_t e = tc ? launch_draft_stats_tc(U, W1, W2t, anchor, tokens, bs, gamma, V, r, k, inv_tau, greedy,
+    cudaError_t e = tc ? launch_draft_stats_tc(U, W1, W2t, nullptr, anchor, tokens, bs, gamma, V, r, k, inv_tau, greedy,
                                                seed, step, stats, L.n_chunks, &n_slots, status, s)
-                       : launch_draft_stats_simt(dtype, U, W1, W2t, anchor, tokens, bs, gamma, V, r, k, inv_tau,
+                       : launch_draft_stats_simt(dtype, U, W1, W2t, nullptr, anchor, tokens, bs, gamma, V, r, k, inv_tau,
                                                  greedy, seed, step, stats, n_slots, s);
     if (e != cudaSuccess) return DSPARK_ECUDA;
-    e = launch_draft_select(dtype, stats, n_slots, U, W1, W2t, anchor, tokens, logit_x, lse, bs, gamma, V, r,
+    e = launch_draft_select(dtype, stats, n_slots, U, W1, W2t, nullptr, anchor, tokens, logit_x, lse, bs, gamma, V, r,
                             k, inv_tau, greedy, seed, step, status, s);
     if (e != cudaSuccess) return DSPARK_ECUDA;
   }

@@ -76,6 +76,7 @@ struct Barriers {
 
 struct Params {
   const __nv_bfloat16* W1;
+  const __nv_bfloat16* states;  // RNN head: the states s_k [bs, gamma, r] (A rows); else null
   const int32_t* anchor;
   const int32_t* tokens;
   int bs, gamma, V, r, k;
@@ -314,13 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     tc::grid_dependency_wait();
     const uint32_t lane_base = tmem_base + (uint32_t(wq * 32) << 16);
     {
-      // A operand into tensor memory: this row's W1[x_{k-1}] (a zero row past the batch), 64 K
+      // A operand into tensor memory: this row's W1[x_{k-1}] (Markov head) or s_k (RNN head)
+      // (a zero row past the batch), 64 K
       // values (32 columns) per store.  Both warp sets of a lane quarter write it, set 0 the
       // first half of K and set 1 the second, each issuing all of its loads before its stores
       // (one round trip for the gather).
-      const int xp = grow < bs
-          ? clamp_token((p.k == 1) ? p.anchor[grow] : p.tokens[size_t(grow) * p.gamma + p.k - 2], V) : -1;
-      const uint4* src = reinterpret_cast<const uint4*>(p.W1 + size_t(xp < 0 ? 0 : xp) * r);
+      const int xp = grow < bs ? 0 : -1;  // -1: a zero row past the batch
+      const uint4* src = reinterpret_cast<const uint4*>(
+          grow < bs ? factor_row(p.W1, p.states, p.anchor, p.tokens, grow, p.k, p.gamma, V, r) : p.W1);
       const int kb_lo = half ? (nk + 1) / 2 : 0, kb_hi = half ? nk : (nk + 1) / 2;  // warp-uniform
       uint4 w[2][8];
 #pragma unroll
@@ -457,7 +459,7 @@ bool draft_tc_supported(int dtype, int bs, int V, int r) {
          tch::encode_fn() != nullptr;
 }
 
-cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t,
+cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t, const void* states,
                                   const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
                                   int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
                                   uint64_t step, void* entries, int n_chunks, int* n_slots,
@@ -481,6 +483,7 @@ cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t
   const int grid = tch::vocab_grid(bs, n_chunks);
   Params prm{};
   prm.W1 = static_cast<const __nv_bfloat16*>(W1);
+  prm.states = static_cast<const __nv_bfloat16*>(states);
   prm.anchor = anchor;
   prm.tokens = tokens;
   prm.bs = bs; prm.gamma = gamma; prm.V = V; prm.r = r; prm.k = k;

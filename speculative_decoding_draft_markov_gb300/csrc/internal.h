@@ -7,16 +7,17 @@
 namespace dspark {
 
 // ---- S1 draft ---------------------------------------------------------------------------
-// Partial draws of l_k = U_k + W1[x_{k-1}] W2 for one position k: per (row, slot) a
+// Partial draws of l_k = U_k + A_k W2 for one position k, A_k = W1[x_{k-1}] (Markov head) or
+// the RNN head's state s_k (`states` non-null, [bs, gamma, r]): per (row, slot) a
 // DraftEntry (common.cuh) over the slot's draft chunks.  The CUDA-core pass has one slot per
 // draft chunk (n_slots = n_draft_chunks(V)).
 cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, const void* W2t,
-                                    const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
+                                    const void* states, const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
                                     int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
                                     uint64_t step, void* entries, int n_slots, cudaStream_t s);
 // Same on the tensor cores (tcgen05 + TMEM + TMA), bf16 only: one slot per CTA column
 // (n_slots <= n_chunks 128-id tiles, returned).
-cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t,
+cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t, const void* states,
                                   const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
                                   int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
                                   uint64_t step, void* entries, int n_chunks, int* n_slots,
@@ -26,17 +27,23 @@ bool draft_tc_supported(int dtype, int bs, int V, int r);
 // DecideEntry (common.cuh) over the column's chunks of the request's deciding row (residual
 // mass sum max(0, p_t - p_d), target mass sum p_t, best chunk keys); n_slots returned.
 cudaError_t launch_decision_stats_tc(const void* target, const void* U, const void* W1, const void* W2t,
-                                     const int32_t* anchor, const int32_t* tokens, const float* lse_d,
+                                     const void* states, const int32_t* anchor, const int32_t* tokens, const float* lse_d,
                                      const void* rs, const void* dec, int bs, int gamma, int V, int r,
                                      float inv_tau, uint64_t seed, uint64_t step, void* entries,
                                      int n_chunks, int* n_slots, uint32_t* status, cudaStream_t s);
 extern uint64_t g_wait_timeout_ns;  // deadline of device-side waits (dspark_set_wait_timeout_ns)
 // Merge the n_slots entries of each row of one position and draw x_k.
 cudaError_t launch_draft_select(int dtype, const void* entries, int n_slots, const void* U,
-                                const void* W1, const void* W2t, const int32_t* anchor,
+                                const void* W1, const void* W2t, const void* states, const int32_t* anchor,
                                 int32_t* tokens, float* logit_x, float* lse, int bs, int gamma,
                                 int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
                                 uint64_t step, uint32_t* status, cudaStream_t s);
+
+// RNN head: the recurrent states s_k of position k for every request (states [bs, gamma, r]),
+// from s_{k-1} and W1[x_{k-1}] (x_0 = anchor, s_0 = 0).
+cudaError_t launch_rnn_state(int dtype, const void* W1, const void* Wg, const float* bg, const int32_t* anchor,
+                             const int32_t* tokens, void* states, int bs, int gamma, int V, int r, int k,
+                             cudaStream_t s);
 
 // ---- S2 / S3 / S4 -----------------------------------------------------------------------
 cudaError_t launch_confidence(int dtype, const void* h, const void* W1, const int32_t* anchor,
@@ -73,7 +80,7 @@ cudaError_t launch_verify(int dtype, const void* target, const int32_t* cu, cons
                           int mode, int bs, int gamma, int V, const int32_t* anchor,
                           const int32_t* tokens, const float* logit_x, const float* lse,
                           const void* draft_logits, const void* U, const void* W1, const void* W2t,
-                          int r, float inv_tau, int greedy, uint64_t seed, uint64_t step,
+                          const void* states, int r, float inv_tau, int greedy, uint64_t seed, uint64_t step,
                           int32_t* out_tokens, int32_t* acc_len, int32_t* ceiling, void* ws,
                           cudaStream_t s);
 

@@ -236,9 +236,9 @@ __global__ void __launch_bounds__(128) verify_decide_kernel(
 template <typename T, int RB>
 __global__ void __launch_bounds__(128) decision_stats_simt_kernel(
     const T* __restrict__ target, const T* __restrict__ U, const T* __restrict__ W1,
-    const T* __restrict__ W2t, const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens,
-    const float* __restrict__ lse_d, const RowStat* __restrict__ rs, const Decision* __restrict__ dec,
-    int bs, int gamma, int V, int r, float inv_tau, uint64_t seed, uint64_t step,
+    const T* __restrict__ W2t, const T* __restrict__ states, const int32_t* __restrict__ anchor,
+    const int32_t* __restrict__ tokens, const float* __restrict__ lse_d, const RowStat* __restrict__ rs,
+    const Decision* __restrict__ dec, int bs, int gamma, int V, int r, float inv_tau, uint64_t seed, uint64_t step,
     DecideEntry* __restrict__ entries, int n_chunks) {
   __shared__ float sA[RB][64];
   __shared__ float sW[kChunk][65];
@@ -255,10 +255,8 @@ __global__ void __launch_bounds__(128) decision_stats_simt_kernel(
       float val = 0.f;
       if (row < bs) {
         const Decision d = dec[row];
-        if (d.kind == kDecResidual) {
-          const int xp = clamp_token((d.kdec == 1) ? anchor[row] : tokens[size_t(row) * gamma + d.kdec - 2], V);
-          val = ld_f32(W1, size_t(xp) * r + i0 + ii);
-        }
+        if (d.kind == kDecResidual)
+          val = ld_f32(factor_row(W1, states, anchor, tokens, row, d.kdec, gamma, V, r), i0 + ii);
       }
       sA[rr][ii] = val;
     }
@@ -353,9 +351,10 @@ __global__ void __launch_bounds__(128) decision_stats_logits_kernel(
 template <typename T>
 __global__ void __launch_bounds__(256, 1) decision_select_kernel(
     const T* __restrict__ target, const T* __restrict__ U, const T* __restrict__ W1,
-    const T* __restrict__ W2t, const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens,
-    const float* __restrict__ lse_d, const RowStat* __restrict__ rs, const Decision* __restrict__ dec,
-    const T* __restrict__ draft_logits, const DecideEntry* __restrict__ entries, int n_slots, int bs, int gamma,
+    const T* __restrict__ W2t, const T* __restrict__ states, const int32_t* __restrict__ anchor,
+    const int32_t* __restrict__ tokens, const float* __restrict__ lse_d, const RowStat* __restrict__ rs,
+    const Decision* __restrict__ dec, const T* __restrict__ draft_logits, const DecideEntry* __restrict__ entries,
+    int n_slots, int bs, int gamma,
     int V, int r, float inv_tau, uint64_t seed, uint64_t step, int32_t* __restrict__ out_tokens,
     uint32_t* status) {
   __shared__ float sA[256];
@@ -399,8 +398,8 @@ __global__ void __launch_bounds__(256, 1) decision_select_kernel(
   const bool resid = (d.kind == kDecResidual) && use_res;
   const bool recompute = resid && draft_logits == nullptr;
   if (recompute) {
-    const int xp = clamp_token((d.kdec == 1) ? anchor[b] : tokens[size_t(b) * gamma + d.kdec - 2], V);
-    for (int i = tid; i < r; i += 256) sA[i] = ld_f32(W1, size_t(xp) * r + i);
+    const T* arow = factor_row(W1, states, anchor, tokens, b, d.kdec, gamma, V, r);
+    for (int i = tid; i < r; i += 256) sA[i] = ld_f32(arow, i);
   }
   __syncthreads();
   const float lse_t = rs[d.pdec].lse;
@@ -443,7 +442,8 @@ template <typename T>
 static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_t* window, int mode,
                                int bs, int gamma, int V, const int32_t* anchor,
                                const int32_t* tokens, const float* logit_x, const float* lse,
-                               const T* draft_logits, const T* U, const T* W1, const T* W2t, int r,
+                               const T* draft_logits, const T* U, const T* W1, const T* W2t, const T* states,
+                               int r,
                                float inv_tau, int greedy, uint64_t seed, uint64_t step,
                                int32_t* out_tokens, int32_t* acc_len, int32_t* ceiling, void* ws,
                                cudaStream_t s) {
@@ -468,15 +468,17 @@ static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_
       decision_stats_logits_kernel<T, RB><<<dim3(L.n_chunks, (bs + RB - 1) / RB), kChunk, 0, s>>>(
           target, draft_logits, lse, rs, dec, bs, gamma, V, inv_tau, seed, step, entries, L.n_chunks);
     } else if (kBf16 && draft_tc_supported(DSPARK_BF16, bs, V, r)) {
-      const cudaError_t e = launch_decision_stats_tc(target, U, W1, W2t, anchor, tokens, lse, rs, dec, bs, gamma, V,
+      const cudaError_t e = launch_decision_stats_tc(target, U, W1, W2t, states, anchor, tokens, lse, rs, dec, bs,
+                                                     gamma, V,
                                                      r, inv_tau, seed, step, entries, L.n_chunks, &n_slots, status, s);
       if (e != cudaSuccess) return e;
     } else {
       decision_stats_simt_kernel<T, RB><<<dim3(L.n_chunks, (bs + RB - 1) / RB), kChunk, 0, s>>>(
-          target, U, W1, W2t, anchor, tokens, lse, rs, dec, bs, gamma, V, r, inv_tau, seed, step, entries,
+          target, U, W1, W2t, states, anchor, tokens, lse, rs, dec, bs, gamma, V, r, inv_tau, seed, step, entries,
           L.n_chunks);
     }
-    le = launch_pdl(decision_select_kernel<T>, dim3(bs), dim3(256), 0, s, target, U, W1, W2t, anchor, tokens, lse,
+    le = launch_pdl(decision_select_kernel<T>, dim3(bs), dim3(256), 0, s, target, U, W1, W2t, states, anchor, tokens,
+                    lse,
                     static_cast<const RowStat*>(rs), static_cast<const Decision*>(dec), draft_logits,
                     static_cast<const DecideEntry*>(entries), n_slots, bs, gamma, V, r, inv_tau, seed, step,
                     out_tokens, status);
@@ -489,18 +491,18 @@ cudaError_t launch_verify(int dtype, const void* target, const int32_t* cu, cons
                           int mode, int bs, int gamma, int V, const int32_t* anchor,
                           const int32_t* tokens, const float* logit_x, const float* lse,
                           const void* draft_logits, const void* U, const void* W1, const void* W2t,
-                          int r, float inv_tau, int greedy, uint64_t seed, uint64_t step,
+                          const void* states, int r, float inv_tau, int greedy, uint64_t seed, uint64_t step,
                           int32_t* out_tokens, int32_t* acc_len, int32_t* ceiling, void* ws,
                           cudaStream_t s) {
   if (dtype == DSPARK_F32)
     return verify_typed<float>((const float*)target, cu, window, mode, bs, gamma, V, anchor, tokens,
                                logit_x, lse, (const float*)draft_logits, (const float*)U, (const float*)W1,
-                               (const float*)W2t, r, inv_tau, greedy, seed, step, out_tokens, acc_len,
+                               (const float*)W2t, (const float*)states, r, inv_tau, greedy, seed, step, out_tokens, acc_len,
                                ceiling, ws, s);
   return verify_typed<__nv_bfloat16>((const __nv_bfloat16*)target, cu, window, mode, bs, gamma, V,
                                      anchor, tokens, logit_x, lse, (const __nv_bfloat16*)draft_logits,
                                      (const __nv_bfloat16*)U, (const __nv_bfloat16*)W1,
-                                     (const __nv_bfloat16*)W2t, r, inv_tau, greedy, seed, step, out_tokens,
+                                     (const __nv_bfloat16*)W2t, (const __nv_bfloat16*)states, r, inv_tau, greedy, seed, step, out_tokens,
                                      acc_len, ceiling, ws, s);
 }
 

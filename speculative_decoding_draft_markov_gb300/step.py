@@ -141,11 +141,11 @@ def draft_and_schedule(inp: dict, buf: StepBuffers, sps, temperature: float, see
 
 
 def verify(inp: dict, buf: StepBuffers, temperature: float, seed: int, step: int,
-           mode: int = B.DSPARK_COMPACT, stream=None) -> None:
-    """Stage S5 on the packed target rows in buf.packed."""
+           mode: int = B.DSPARK_COMPACT, stream=None, states=None) -> None:
+    """Stage S5 on the packed target rows in buf.packed (states: the RNN head's, if it drafted)."""
     B.dspark_verify(buf.packed, buf.cu, buf.window, mode, inp["anchor"], buf.tokens, buf.logit_x, buf.lse,
                     inp["U"], inp["W1"], inp["W2t"], temperature, seed, step, buf.out_tokens, buf.acc_len,
-                    buf.ceiling, buf.ws, stream)
+                    buf.ceiling, buf.ws, stream, draft_states=states)
 
 
 def schedule_budget(buf: StepBuffers, sps, ring, step: int, main=None, side=None) -> None:

@@ -120,17 +120,39 @@ def test_other_entry_points_host_validation(L):
     assert L.dspark_pack(None, f, f, 4, 7, None, 0, 64, f, f, f, f, f, None, 0, None) == B.DSPARK_EWORKSPACE
     # verify: compact without window, cap-accept without ceiling, bad mode, no source for p_d,
     # misaligned draft logits
-    args = [f, 1, f, None, 1, 4, 7, 1024, f, f, f, f, None, f, f, f, 32, 1.0, 0, 0, f, f, f, f, 1 << 30, None]
+    args = [f, 1, f, None, 1, 4, 7, 1024, f, f, f, f, None, None, f, f, f, 32, 1.0, 0, 0, f, f, f, f, 1 << 30, None]
     assert L.dspark_verify(*args) == B.DSPARK_EINVAL
-    args[3], args[4], args[22] = f, 2, None
+    args[3], args[4], args[23] = f, 2, None
     assert L.dspark_verify(*args) == B.DSPARK_EINVAL
     args[4] = 9
     assert L.dspark_verify(*args) == B.DSPARK_EINVAL
-    args[4], args[22] = 1, f
-    args[13] = None  # neither draft logits nor U
+    args[4], args[23] = 1, f
+    args[13] = f + 8  # RNN states given, not 16-byte aligned
+    assert L.dspark_verify(*args) == B.DSPARK_EINVAL
+    args[13] = None
+    args[14] = None  # neither draft logits nor U
     assert L.dspark_verify(*args) == B.DSPARK_EINVAL
     args[12] = f + 2  # draft logits given, not 16-byte aligned
     assert L.dspark_verify(*args) == B.DSPARK_EINVAL
+
+
+def test_rnn_draft_host_validation(L):
+    f = FAKE
+    base = dict(U=f, W1=f, W2t=f, Wg=f, bg=f, dtype=1, anchor=f, bs=4, gamma=7, V=1024, r=32,
+                temperature=ctypes.c_float(1.0), seed=0, step=0, tokens=f, logit_x=f, lse=f, states=f, ws=f,
+                ws_bytes=1 << 30, stream=None)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        return L.dspark_draft_block_rnn(*a.values())
+    assert call(Wg=None) == B.DSPARK_EINVAL
+    assert call(bg=None) == B.DSPARK_EINVAL
+    assert call(states=None) == B.DSPARK_EINVAL
+    assert call(states=f + 4) == B.DSPARK_EINVAL
+    assert call(bs=300) == B.DSPARK_EUNSUPPORTED
+    assert call(r=48) == B.DSPARK_EUNSUPPORTED
+    assert call(ws=None) == B.DSPARK_EWORKSPACE
 
 
 def test_schedule_pack_host_validation(L):

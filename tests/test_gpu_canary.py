@@ -110,3 +110,33 @@ def test_temperature_fit_keeps_its_bounds():
     B.dspark_sts_fit(torch.as_tensor(z, device="cuda"), torch.as_tensor(c, device="cuda"), grid, n_bins, T.t, e.t,
                      ws=ws.t)
     _check(T, e, ws)
+
+
+@pytest.mark.parametrize("shape", ["small", "bench"])
+def test_rnn_head_keeps_its_bounds(shape):
+    """The RNN head's draft (states written position by position) and verify reading them."""
+    wl = (I.WORKLOADS["qwen3_4b"].with_(name="canary_rnn", bs=5, gamma=3, V=2000, d=64, seed=22) if shape == "small"
+          else I.WORKLOADS["mixed_bs256"])
+    dev = torch.device("cuda")
+    inp = I.make_device_inputs(wl, dev, with_hidden=False, with_rnn=True)
+    bs, gamma, V, r = wl.bs, wl.gamma, wl.V, wl.r
+    ws = _ws(bs, gamma, V)
+    tok, lx, lse = Guarded((bs, gamma), torch.int32), Guarded((bs, gamma), torch.float32), \
+        Guarded((bs, gamma), torch.float32)
+    st = Guarded((bs, gamma, r), inp["U"].dtype)
+    B.dspark_draft_block_rnn(inp["U"], inp["W1"], inp["W2t"], inp["Wg"], inp["bg"], inp["anchor"], 1.0, 3, 4, tok.t,
+                             lx.t, lse.t, st.t, ws.t)
+    _check(ws, tok, lx, lse, st)
+    assert B.dspark_read_device_status(ws.t) == B.DSPARK_OK
+    cap = bs * (gamma + 1)
+    cu, padded = Guarded((bs + 1,), torch.int32), Guarded((1,), torch.int32)
+    ids, req, pos = (Guarded((cap,), torch.int32) for _ in range(3))
+    B.dspark_pack(None, inp["anchor"], tok.t, None, cu.t, ids.t, req.t, pos.t, padded.t, ws.t)
+    g1 = gamma + 1
+    idx = torch.where(req.t >= 0, req.t * g1 + pos.t, torch.zeros_like(req.t)).long()
+    packed = torch.index_select(inp["target"].view(bs * g1, V), 0, idx)
+    out, acc = Guarded((bs, gamma + 1), torch.int32), Guarded((bs,), torch.int32)
+    B.dspark_verify(packed, cu.t, None, B.DSPARK_STATIC, inp["anchor"], tok.t, lx.t, lse.t, inp["U"], inp["W1"],
+                    inp["W2t"], 1.0, 5, 6, out.t, acc.t, None, ws.t, draft_states=st.t)
+    _check(out, acc, ws, st)
+    assert B.dspark_read_device_status(ws.t) == B.DSPARK_OK
