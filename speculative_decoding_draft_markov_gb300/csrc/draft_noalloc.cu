@@ -3,7 +3,7 @@
 // another framework's device-memory pool (a cudaMalloc there would bypass the host
 // framework's allocator and its accounting), or a service that fixes its device footprint at
 // start-up and forbids any later allocation.  Such a caller still passes every input and
-// output buffer; only the draft's scratch (one status word and the per-(request, chunk)
+// output buffer; only the draft's scratch (one status word and the per-(request, slot)
 // statistics of one position) comes from a fixed array that is part of the library image.
 //
 // The array below is a file-scope __device__ variable: every GPU on which the library is
@@ -77,10 +77,11 @@ extern "C" DSPARK_API int dspark_draft_block_noalloc(
 
   // The scratch this call needs: the status word, then 16 bytes per (request, slot) of the
   // pass that will run.  The tensor-core pass (bf16, r a multiple of 64) writes one slot per
-  // CTA column, at most one per 128-id tile; the CUDA-core pass one per 64-id draft chunk.
+  // CTA column (at most one per SM and per 256-id tile); the CUDA-core pass one per 64-id draft
+  // chunk.
   const WsLayout L = ws_layout(bs, gamma, V);
   const bool tc = draft_tc_supported(dtype, bs, V, r);
-  const size_t need = L.stats + draft_stats_bytes(bs, tc ? L.n_chunks : n_draft_chunks(V));
+  const size_t need = L.stats + draft_stats_bytes(bs, tc ? draft_tc_slots(bs, V) : n_draft_chunks(V));
   if (need > kNoAllocScratchBytes) return DSPARK_EUNSUPPORTED;
 
   void* scratch = nullptr;

@@ -16,13 +16,16 @@ cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, co
                                     int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
                                     uint64_t step, void* entries, int n_slots, cudaStream_t s);
 // Same on the tensor cores (tcgen05 + TMEM + TMA), bf16 only: one slot per CTA column
-// (n_slots <= n_chunks 128-id tiles, returned).
+// (n_slots = draft_tc_slots(bs, V), returned).
 cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t, const void* states,
                                   const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
                                   int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
                                   uint64_t step, void* entries, int n_chunks, int* n_slots,
                                   uint32_t* status, cudaStream_t s);
 bool draft_tc_supported(int dtype, int bs, int V, int r);
+// Slots (entries per request) the tensor-core pass writes: one per CTA column (at most one per
+// SM, and per 256-id vocabulary tile).
+int draft_tc_slots(int bs, int V);
 // Verify's decision masses on the tensor cores (bf16): per request and CTA column a
 // DecideEntry (common.cuh) over the column's chunks of the request's deciding row (residual
 // mass sum max(0, p_t - p_d), target mass sum p_t, best chunk keys); n_slots returned.
