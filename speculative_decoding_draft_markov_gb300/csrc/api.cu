@@ -137,7 +137,8 @@ int dspark_build_sps(const double* T_raw, int m_max, const int32_t* tiers, int n
 namespace {
 
 // The gamma positions of a block draft, left to right: per position the RNN head's state update
-// (states non-null), the vocabulary pass (tensor cores or CUDA cores) and the select.
+// (states non-null), the vocabulary pass (tensor cores or CUDA cores) and the select.  The
+// tensor-core pass runs the select itself, and for the Markov head all positions in one launch.
 int draft_positions(int dtype, const void* U, const void* W1, const void* W2t, const void* Wg, const float* bg,
                     void* states, const int32_t* anchor, int bs, int gamma, int V, int r, float temperature,
                     uint64_t seed, uint64_t step, int32_t* tokens, float* logit_x, float* lse, void* ws,
@@ -149,17 +150,27 @@ int draft_positions(int dtype, const void* U, const void* W1, const void* W2t, c
   const int greedy = temperature == 0.f;
   const float inv_tau = greedy ? 1.f : static_cast<float>(1.0 / static_cast<double>(temperature));
   const bool tc = draft_tc_supported(dtype, bs, V, r);
+  uint32_t* ctl = reinterpret_cast<uint32_t*>(w + L.status + 64);
+  if (tc && !states)  // the Markov head: every position in one persistent launch
+    return launch_draft_tc(U, W1, W2t, nullptr, anchor, tokens, logit_x, lse, bs, gamma, V, r, 1, gamma, inv_tau,
+                           greedy, seed, step, stats, ctl, status, s) == cudaSuccess
+               ? DSPARK_OK
+               : DSPARK_ECUDA;
   for (int k = 1; k <= gamma; ++k) {
     if (states && launch_rnn_state(dtype, W1, Wg, bg, anchor, tokens, states, bs, gamma, V, r, k, s) != cudaSuccess)
       return DSPARK_ECUDA;
-    int n_slots = n_draft_chunks(V);  // the CUDA-core pass: one slot per draft chunk
-    cudaError_t e = tc ? launch_draft_stats_tc(U, W1, W2t, states, anchor, tokens, bs, gamma, V, r, k, inv_tau,
-                                               greedy, seed, step, stats, L.n_chunks, &n_slots, status, s)
-                       : launch_draft_stats_simt(dtype, U, W1, W2t, states, anchor, tokens, bs, gamma, V, r, k,
-                                                 inv_tau, greedy, seed, step, stats, n_slots, s);
-    if (e != cudaSuccess) return DSPARK_ECUDA;
-    e = launch_draft_select(dtype, stats, n_slots, U, W1, W2t, states, anchor, tokens, logit_x, lse, bs,
-                            gamma, V, r, k, inv_tau, greedy, seed, step, status, s);
+    cudaError_t e;
+    if (tc) {
+      e = launch_draft_tc(U, W1, W2t, states, anchor, tokens, logit_x, lse, bs, gamma, V, r, k, k, inv_tau, greedy,
+                          seed, step, stats, ctl, status, s);
+    } else {
+      const int n_slots = n_draft_chunks(V);  // the CUDA-core pass: one slot per draft chunk
+      e = launch_draft_stats_simt(dtype, U, W1, W2t, states, anchor, tokens, bs, gamma, V, r, k, inv_tau, greedy,
+                                  seed, step, stats, n_slots, s);
+      if (e == cudaSuccess)
+        e = launch_draft_select(dtype, stats, n_slots, U, W1, W2t, states, anchor, tokens, logit_x, lse, bs, gamma,
+                                V, r, k, inv_tau, greedy, seed, step, status, s);
+    }
     if (e != cudaSuccess) return DSPARK_ECUDA;
   }
   return DSPARK_OK;

@@ -172,16 +172,17 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ----------------------------------------------------------------------------------------
-// Dot products W2t[v] . a for the 8 NW ids v0 .. v0 + 8 NW - 1 of one sampler chunk (NW = 16:
-// a verify chunk of 128 ids; NW = 8: a draft chunk of 64), by a 256-thread block: warp w takes
-// ids v0 + NW w .. + NW - 1, lane l the K slice [8l, 8l + 8).  All NW rows' loads are issued
-// before any arithmetic; fixed summation order.  out[i] (shared memory) receives the dot of id
-// v0 + i, 0 for ids >= V.  Requires r % 8 == 0 and r <= 256.
+// Dot products W2t[v] . a for the NG NW ids v0 .. v0 + NG NW - 1 of one sampler chunk, by a
+// group of NG warps (gt = the thread's index in the group): warp w takes ids v0 + NW w ..
+// + NW - 1, lane l the K slice [8l, 8l + 8).  (8 warps x NW = 16: a verify chunk of 128 ids;
+// 8 x 8 or 4 x 16: a draft chunk of 64.)  All NW rows' loads are issued before any arithmetic;
+// fixed summation order.  out[i] (shared memory) receives the dot of id v0 + i, 0 for ids >= V.
+// Requires r % 8 == 0 and r <= 256.
 // ----------------------------------------------------------------------------------------
 template <typename T, int NW = 16>
 __device__ __forceinline__ void chunk_dots(const T* __restrict__ W2t, int r, int V, int v0,
-                                           const float* __restrict__ a, float* out) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+                                           const float* __restrict__ a, float* out, int gt) {
+  const int warp = gt >> 5, lane = gt & 31;
   const bool on = lane * 8 < r;
   float av[8];
 #pragma unroll

@@ -8,6 +8,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "draft_select.cuh"
 #include "internal.h"
 
 namespace dspark {
@@ -112,12 +113,9 @@ __global__ void __launch_bounds__(128) draft_stats_simt_kernel(
 }
 
 // ---------------------------------------------------------------------------------------
-// Select pass: one 256-thread block per row.  Warp 0 merges the row's entries: the row LSE
-// from the (max, sum-exp) pairs, and the winner = argmax of the keys (lowest index on ties).
-//   temperature > 0: the winner is the draft chunk c* of the first Gumbel level; its 64 logits
-//   are recomputed (fixed-order fp32 dot products) and an inverse-CDF draw over them with the
-//   row's uniform (purpose 2, index 0) picks x_k.
-//   temperature = 0: the winner is x_k itself (lowest-index argmax).
+// Select pass: one 256-thread block per row runs select_row (draft_select.cuh): warp 0 merges
+// the row's entries -- the row LSE from the (max, sum-exp) pairs, the winner = argmax of the
+// keys (lowest index on ties) -- and, at temperature > 0, draws x_k inside the winning chunk.
 // ---------------------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(256, 1) draft_select_kernel(
@@ -127,101 +125,13 @@ __global__ void __launch_bounds__(256, 1) draft_select_kernel(
     float* __restrict__ lse, int bs,
     int gamma, int V, int r, int k, float inv_tau, int greedy, uint64_t seed, uint64_t step,
     uint32_t* status) {
-  __shared__ float sA[256];
-  __shared__ float tv[kDraftIds];
-  __shared__ float s_lse, s_best;
-  __shared__ int s_win;
-  const int b = blockIdx.x, tid = threadIdx.x;
-  const float4* en = entries + size_t(b) * n_slots;
+  __shared__ SelectScratch sm;
   // launched as a programmatic dependent of the statistics pass: wait for it to complete, then
   // let the next position's statistics kernel start its set-up
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const size_t out = size_t(b) * gamma + (k - 1);
-
-  // the factor row (W1[x_{k-1}], or the RNN state s_k) does not depend on the draw: warps 1..7
-  // fetch it while warp 0 merges the entries, so that neither waits for the other's loads
-  if (!greedy && tid >= 32) {
-    const T* arow = factor_row(W1, states, anchor, tokens, b, k, gamma, V, r);
-    for (int i = tid - 32; i < r; i += 224) sA[i] = ld_f32(arow, i);
-  }
-  if (tid < 32) {
-    LsePair lp{-INFINITY, 0.f};
-    ArgMax best{-INFINITY, INT_MAX};
-    for (int i = tid; i < n_slots; i += 32) {
-      const float4 e = en[i];
-      lp = lse_merge(lp, LsePair{e.x, e.y});
-      best = better(best, ArgMax{e.z, __float_as_int(e.w)});
-    }
-    lp = warp_lse(lp);
-    best = warp_argmax(best);
-    if (tid == 0) {
-      s_lse = lp.m + logf(lp.s);
-      s_best = best.v;
-      s_win = best.i;
-    }
-  }
-  __syncthreads();
-  if (greedy) {
-    if (tid == 0) {
-      tokens[out] = (s_win == INT_MAX) ? 0 : s_win;
-      logit_x[out] = s_best;
-      lse[out] = 0.f;
-    }
-    return;
-  }
-  // only non-finite statistics leave the winner unset; a winner outside the vocabulary means the
-  // entries were not written by this position's statistics pass (it gave up): report, use 0
-  int cstar = (s_win == INT_MAX) ? 0 : s_win;
-  if (cstar < 0 || cstar >= n_draft_chunks(V)) {
-    if (tid == 0) set_status(status, DSPARK_EINVAL);
-    cstar = 0;
-  }
-  // the U values of the chosen chunk (warp 0: offsets lane and lane + 32) load together with its
-  // W2t rows
-  const int v0 = cstar * kDraftIds + tid, v1 = v0 + 32;
-  const size_t urow = (size_t(b) * gamma + (k - 1)) * V;
-  float u0 = 0.f, u1 = 0.f;
-  if (tid < 32) {
-    if (v0 < V) u0 = ld_f32(U, urow + v0);
-    if (v1 < V) u1 = ld_f32(U, urow + v1);
-  }
-  chunk_dots<T, kDraftIds / 8>(W2t, r, V, cstar * kDraftIds, sA, tv);
-  __syncthreads();
-  // the id inside the chunk by inverse CDF (warp 0, two offsets a lane: lane and lane + 32): the
-  // first offset whose partial sum of exp(t - max) exceeds u times the total, u the row's
-  // uniform of Philox purpose 2, index 0; should rounding leave every partial sum at or below
-  // it, the last id with a finite logit
-  if (tid < 32) {
-    const float a0 = v0 < V ? (tv[tid] + u0) * inv_tau : -INFINITY;
-    const float a1 = v1 < V ? (tv[tid + 32] + u1) * inv_tau : -INFINITY;
-    const float mc = warp_max(fmaxf(a0, a1));
-    const float w0 = a0 > -INFINITY ? expf(a0 - mc) : 0.f, w1 = a1 > -INFINITY ? expf(a1 - mc) : 0.f;
-    float c0 = w0, c1 = w1;  // inclusive scans over offsets 0..31 and 32..63
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y0 = __shfl_up_sync(0xFFFFFFFFu, c0, o), y1 = __shfl_up_sync(0xFFFFFFFFu, c1, o);
-      if (tid >= o) { c0 += y0; c1 += y1; }
-    }
-    c1 += __shfl_sync(0xFFFFFFFFu, c0, 31);
-    const float total = __shfl_sync(0xFFFFFFFFu, c1, 31);
-    const float u = bits_to_uniform(philox_group(seed, step, kDraftElem, b, k, 0).x);
-    const float tgt = u * total;
-    const unsigned hit0 = __ballot_sync(0xFFFFFFFFu, w0 > 0.f && c0 > tgt);
-    const unsigned hit1 = __ballot_sync(0xFFFFFFFFu, w1 > 0.f && c1 > tgt);
-    const unsigned pos0 = __ballot_sync(0xFFFFFFFFu, w0 > 0.f), pos1 = __ballot_sync(0xFFFFFFFFu, w1 > 0.f);
-    int ei;
-    if (hit0) ei = __ffs(hit0) - 1;
-    else if (hit1) ei = 32 + __ffs(hit1) - 1;
-    else if (pos1) ei = 32 + 31 - __clz(pos1);
-    else ei = pos0 ? 31 - __clz(pos0) : 0;
-    const float te = __shfl_sync(0xFFFFFFFFu, (ei & 32) ? a1 : a0, ei & 31);  // tempered logit of x_k
-    if (tid == 0) {
-      tokens[out] = min(cstar * kDraftIds + ei, V - 1);
-      logit_x[out] = te;
-      lse[out] = s_lse;
-    }
-  }
+  select_row<T, 8>(blockIdx.x, threadIdx.x, entries, n_slots, U, W1, W2t, states, anchor, tokens, logit_x, lse,
+                   gamma, V, r, k, inv_tau, greedy, seed, step, status, &sm, [] { __syncthreads(); });
 }
 
 cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, const void* W2t, const void* states,

@@ -19,7 +19,9 @@
 //
 // Every call shares the one array and the last call's contents stay in it.  The status word
 // is cleared at the start of each call (when the caller does not pass its own); the chunk
-// statistics need no clearing (each position writes all of them before reading any).  Calls
+// statistics need no clearing (each position writes all of them before reading any); the
+// tensor-core pass's grid-barrier words (64 bytes after the status word) start at zero, as the
+// array does, and every launch leaves them at zero.  Calls
 // whose work can overlap on the GPU -- on different streams, or from several host threads --
 // race on the array and must be serialised by the caller.
 #include <cmath>
@@ -95,15 +97,19 @@ extern "C" DSPARK_API int dspark_draft_block_noalloc(
 
   const int greedy = temperature == 0.f;
   const float inv_tau = greedy ? 1.f : static_cast<float>(1.0 / static_cast<double>(temperature));
+  if (tc)  // every position in one persistent launch (grid barrier words beside the status word)
+    return launch_draft_tc(U, W1, W2t, nullptr, anchor, tokens, logit_x, lse, bs, gamma, V, r, 1, gamma, inv_tau,
+                           greedy, seed, step, stats, reinterpret_cast<uint32_t*>(w + L.status + 64), status, s) ==
+                   cudaSuccess
+               ? DSPARK_OK
+               : DSPARK_ECUDA;
+  const int n_slots = n_draft_chunks(V);  // the CUDA-core pass: one slot per draft chunk
   for (int k = 1; k <= gamma; ++k) {
-    int n_slots = n_draft_chunks(V);  // the CUDA-core pass: one slot per draft chunk
-    cudaError_t e = tc ? launch_draft_stats_tc(U, W1, W2t, nullptr, anchor, tokens, bs, gamma, V, r, k, inv_tau, greedy,
-                                               seed, step, stats, L.n_chunks, &n_slots, status, s)
-                       : launch_draft_stats_simt(dtype, U, W1, W2t, nullptr, anchor, tokens, bs, gamma, V, r, k, inv_tau,
-                                                 greedy, seed, step, stats, n_slots, s);
-    if (e != cudaSuccess) return DSPARK_ECUDA;
-    e = launch_draft_select(dtype, stats, n_slots, U, W1, W2t, nullptr, anchor, tokens, logit_x, lse, bs, gamma, V, r,
-                            k, inv_tau, greedy, seed, step, status, s);
+    cudaError_t e = launch_draft_stats_simt(dtype, U, W1, W2t, nullptr, anchor, tokens, bs, gamma, V, r, k, inv_tau,
+                                            greedy, seed, step, stats, n_slots, s);
+    if (e == cudaSuccess)
+      e = launch_draft_select(dtype, stats, n_slots, U, W1, W2t, nullptr, anchor, tokens, logit_x, lse, bs, gamma, V,
+                              r, k, inv_tau, greedy, seed, step, status, s);
     if (e != cudaSuccess) return DSPARK_ECUDA;
   }
   return DSPARK_OK;

@@ -4,8 +4,16 @@
 // DSpark technical summary, "Architecture (drafter)": the Markov head's bias for position k
 // is W1[x_{k-1}] W2 (rank r = 256), added to the backbone's base logits U_k over the full
 // vocabulary.  Per position this is a GEMM [bs, r] x [r, V] consumed at once by a sampler:
-// one launch per position k computes l = U_k + A_k W2 (A_k = W1[x_{k-1}], or the RNN head's
-// state s_k) and reduces it to per-request partial draws (DraftEntry, common.cuh).
+// l = U_k + A_k W2 (A_k = W1[x_{k-1}], or the RNN head's state s_k), reduced to per-request
+// partial draws (DraftEntry, common.cuh), which the select step (draft_select.cuh) merges into
+// x_k.  x_k is the next position's A row, so the positions run strictly left to right.
+//
+// One persistent launch runs positions k_first .. k_last (all gamma of them for the Markov head;
+// one at a time for the RNN head, whose state update runs between launches).  Between positions
+// the CTAs meet at a grid barrier (a cooperative launch, so that every CTA is resident), run the
+// select of the requests assigned to them, and meet again before the next position's A gather.
+// Compared with a launch per pass this removes two kernel boundaries per position, and the TMA
+// producers run on into the next position's W2t / U tiles while the select runs.
 //
 // What paces the pass on this part is the issue of tcgen05.mma instructions: measured, an
 // issuing loop that also waits on its operand barriers sustains one MMA per ~180 SM cycles
@@ -13,28 +21,43 @@
 // instruction is made as wide as the tensor core allows, N = 256: a tile of 128 requests x
 // 256 vocabulary ids is 16 MMAs (K = 256), half the instructions per logit of N = 128.
 //
+// The second bound is how fast W2t reaches shared memory: every position streams all of W2t
+// from L2 (where it stays), so a CTA needs as many bytes in flight as the L2 round trip times
+// the tensor core's consumption.  Hence the A operand lives in tensor memory, not shared memory,
+// and the freed space lets the U_k tiles (streamed from HBM, with its longer latency) be loaded
+// two tiles ahead beside a three-deep W2t ring.
+//
 // Work decomposition:
 //   tile      = 128 requests (TMEM lanes) x 256 vocabulary ids (= four 64-id draft chunks),
-//               K = r; the accumulator is 256 TMEM columns, two of them (512 columns) let the
-//               MMA of the next tile overlap the epilogue of this one
+//               K = r; the accumulator is TMEM columns 0-255, the A operand columns 256-383
 //   CTA       = persistent, one per SM; fixed 128-request M-tile, strided over vocabulary
-//               tiles; the gathered A operand (W1[x_{k-1}], or s_k) stays in shared memory
-//   warp 0    = TMA producer: W2t K-stages [256 ids x 64 K] (32 KB, a three-deep ring,
-//               evict-last: every position re-reads W2t and it stays in L2), then the two
-//               halves of the U_k tile (3-D map over [bs, gamma, V], evict-first)
-//   warp 1    = TMEM owner + single-thread tcgen05.mma issuer, commits to mbarriers
-//   warps 2-9 = epilogue, two warp sets of four (one warp per TMEM lane quarter, one request
-//               row per thread).  Set h takes columns 128 h .. 128 h + 127 of every tile (the
-//               tile's draft chunks 2h and 2h + 1) and U half h: it adds U_k to its 128
-//               accumulator values (adding U_k on the tensor core through an identity operand
-//               costs more tensor-pipe time than these adds cost issue slots), forms each
-//               chunk's log-mass and Gumbel key and keeps, in registers, the row's running
-//               (max, sum-exp) and best key.  The two sets merge through shared memory at the
-//               end and write one entry per request, so the select merges one entry per CTA
-//               column.
-// Every mbarrier wait is bounded (SM cycle-counter deadline + shared abort flag); on give-up the
-// kernel records DSPARK_ETIMEOUT, waits (bounded) for its own copies / MMAs in flight,
-// frees TMEM and returns.
+//               tiles; the gathered A operand (W1[x_{k-1}], or s_k) is written once into tensor
+//               memory by the epilogue warps (tcgen05.st)
+//   warp 0    = TMA producer of W2t K-stages [256 ids x 64 K] (32 KB, a three-deep ring,
+//               evict-last: every position re-reads W2t and it stays in L2)
+//   warp 18   = TMA producer of the two halves of the U_k tile (3-D map over [bs, gamma, V],
+//               evict-first; two buffers per half), on its own so that U never waits behind a
+//               W2t stage
+//   warp 1    = TMEM owner + single-thread tcgen05.mma issuer, commits to mbarriers; the next
+//               tile's MMAs start once both epilogue sets have read the accumulator into
+//               registers (a single accumulator: its readout is short next to the tile)
+//   warps 2-17 = epilogue, four warp sets of four (one warp per TMEM lane quarter, one request
+//               row per thread).  Set s takes columns 64 s .. 64 s + 63 of every tile -- the
+//               tile's draft chunk 4c + s -- and the matching 64-id box of U: it adds U_k to its
+//               64 accumulator values (adding U_k on the tensor core through an identity operand
+//               costs more tensor-pipe time than these adds cost issue slots), forms the chunk's
+//               log-mass and Gumbel key and keeps, in registers, the row's running (max,
+//               sum-exp) and best key.  Four sets rather than two: the per-element work is a
+//               chain of dependent ALU / MUFU operations, and with two warps per scheduler most
+//               issue slots went unused.  After a position the sets merge through spare TMEM
+//               columns (shared memory is full) and set 0 writes one entry per request, so the
+//               select merges one entry per CTA column.
+//   select    = the epilogue warps as two groups of eight, one request each (request
+//               blockIdx + (2 j + group) * gridDim)
+// Every mbarrier and grid-barrier wait is bounded (SM cycle-counter deadline + shared abort flag,
+// and a grid-wide abort word); on give-up the kernel records DSPARK_ETIMEOUT, waits (bounded) for
+// its own copies / MMAs in flight, frees TMEM and returns.  The grid barrier's words live in the
+// workspace's status block; the last CTA to leave zeroes them for the next launch.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -42,6 +65,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "draft_select.cuh"
 #include "internal.h"
 #include "tc_host.h"
 #include "tc_ptx.cuh"
@@ -52,73 +76,71 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBN = 256;                          // ids per tile
-constexpr int kHalfN = kBN / 2;                   // ids per epilogue set (two draft chunks)
-static_assert(kHalfN == 2 * kDraftIds, "an epilogue set takes two draft chunks of a tile");
+constexpr int kHalfN = kBN / 2;                   // ids per U half (two draft chunks)
+static_assert(kBN == 4 * kDraftIds, "a tile is four draft chunks, one per epilogue set");
 constexpr int kBK = 64;                           // K per stage: one 128-byte swizzle row
 constexpr int kBStages = 3;                       // W2t ring of 32 KB stages
-constexpr int kAccBufs = 2;
-constexpr int kEpiWarps = 8;
+constexpr int kUDepth = 2;                        // U buffers per epilogue set (tiles ahead)
+constexpr int kEpiSets = 4;                       // warp sets of four warps, one draft chunk each
+constexpr int kEpiWarps = 4 * kEpiSets;
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr uint32_t kAAtom = kBM * kBK * 2;        // 16 KB: A rows [128 x 64 K]
+constexpr int kUWarp = 2 + kEpiWarps;             // warp 18: the U producer
+constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr uint32_t kBStage = kBN * kBK * 2;       // 32 KB: W2t rows [256 x 64 K]
 constexpr uint32_t kUBox = kBM * 64 * 2;          // 16 KB: U [128 rows x 64 ids]
 constexpr uint32_t kUHalfTile = 2 * kUBox;        // 32 KB: one epilogue set's 128 ids
-constexpr uint32_t kTmemCols = kAccBufs * kBN;    // 512
+constexpr uint32_t kTmemA = kBN;                  // A: columns 256 .. 256 + r / 2 - 1 (bf16 pairs)
+constexpr uint32_t kTmemX = kTmemA + 128;         // 384 + 4 s: warp set s's entry, merged by set 0
+constexpr uint32_t kTmemCols = 512;               // allocation: a power of two >= 256 + 128
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Barriers {
   uint64_t b_full[kBStages], b_empty[kBStages];
-  uint64_t u_full[2], u_empty[2];  // U half h (one per epilogue set)
-  uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
+  uint64_t u_full[2][kUDepth], u_empty[2][kUDepth];  // U half h (epilogue sets 2h, 2h + 1), buffer j
+  uint64_t acc_full, acc_empty;
   uint64_t drain;
-  uint64_t a_ready;  // the A operand is in shared memory (one arrival per epilogue warp)
+  uint64_t a_ready;  // the A operand is in tensor memory (one arrival per epilogue warp)
   uint32_t tmem_base;
   int abort;
   int mma_pending;   // the issuer's MMAs that nobody has waited for (set by the issuing thread)
-  int xrow[kBM];     // row of the factor table for each A row (-1: zero row)
-  float4 xch[kBM];   // warp set 1's entry of each row, merged by set 0 at the end
+  int bail;          // the epilogue's shared decision after a grid barrier (1: stop)
+  SelectScratch sel[2];  // the two select groups' scratch
 };
 
 struct Params {
+  const __nv_bfloat16* U;
   const __nv_bfloat16* W1;
+  const __nv_bfloat16* W2t;
   const __nv_bfloat16* states;  // RNN head: the states s_k [bs, gamma, r] (A rows); else null
   const int32_t* anchor;
-  const int32_t* tokens;
-  int bs, gamma, V, r, k;
+  int32_t* tokens;
+  float* logit_x;
+  float* lse;
+  int bs, gamma, V, r, k_first, k_last;
   float inv_tau;
   int greedy;
   int n_tiles;      // 256-id vocabulary tiles
   uint32_t* status;
+  uint32_t* ctl;    // grid barrier: ctl[0] arrivals, ctl[kCtlAbort] abort, ctl[kCtlExit] exits
   uint64_t timeout_ns;
   float4* entries;  // per (request, slot): DraftEntry
   int n_slots;
   uint64_t seed, step;
 };
 
-// Dynamic shared memory: A atoms | W2t ring | U halves | barriers.  The buffer is declared
-// 1024-byte aligned (128-byte swizzle atoms).
-constexpr size_t smem_bytes(int r) {
-  return size_t(r / kBK) * kAAtom + kBStages * size_t(kBStage) + 2 * size_t(kUHalfTile) + sizeof(Barriers);
-}
-static_assert(smem_bytes(256) <= 232448, "dynamic shared memory beyond the 227 KB per-block limit");
+constexpr int kCtlAbort = 16, kCtlExit = 32;  // words of the grid barrier block (64 bytes apart)
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Dynamic shared memory: W2t ring | U halves | barriers.  The buffer is declared 1024-byte
+// aligned (128-byte swizzle atoms).
+constexpr size_t kSmemBytes = kBStages * size_t(kBStage) + 2 * kUDepth * size_t(kUHalfTile) + sizeof(Barriers);
+static_assert(kSmemBytes <= 232448, "dynamic shared memory beyond the 227 KB per-block limit");
 
-// The Gumbels of set h's two draft chunks 4c + 2h, 4c + 2h + 1 of vocabulary tile c, request
-// `req`, position k (Philox purpose 1, indices = chunk ids): counter group c, words 2h, 2h + 1.
-__device__ __forceinline__ float2 tile_gumbels(uint64_t seed, uint64_t step, int req, int k, int c, int h) {
-  const uint4 w = philox_group(seed, step, kDraftChunk, uint32_t(req), k, uint32_t(c));
-  return h ? make_float2(gumbel_from_bits(w.z), gumbel_from_bits(w.w))
-           : make_float2(gumbel_from_bits(w.x), gumbel_from_bits(w.y));
-}
-// Kept out of line for the tile loop: inlined there its Philox rounds raise register pressure
-// enough to spill, although the loop only calls it for tiles past the ones drawn up front.
-__device__ __noinline__ float2 tile_gumbels_call(uint64_t seed, uint64_t step, int req, int k, int c, int h) {
-  return tile_gumbels(seed, step, req, k, c, h);
+// The Gumbel of draft chunk 4c + s (warp set s's chunk of vocabulary tile c), request `req`,
+// position k (Philox purpose 1, index = the chunk id): counter group c, word s.  Out of line:
+// called in the tile loop before the accumulator wait (when few registers are live), its
+// Philox rounds add nothing to the loop's register pressure.
+__device__ __noinline__ float chunk_gumbel_call(uint64_t seed, uint64_t step, int req, int k, int c, int s) {
+  return gumbel_from_bits(pick_word(philox_group(seed, step, kDraftChunk, uint32_t(req), k, uint32_t(c)), s));
 }
 
 // Max of the first `valid` of kDraftIds values (all of them when !kRagged), four chains.
@@ -141,6 +163,65 @@ __device__ __forceinline__ float row_sum_exp2(const float* v, int valid, float m
     if (!kRagged || i < valid) s8[i & 7] += e;
   }
   return ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// The epilogue warps' named barrier (id 1, 256 threads); the producers and the MMA warp run on.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
+
+// One thread per CTA: arrive at grid barrier number `idx` (0, 1, ...) of this launch and wait
+// (bounded) until every CTA has arrived.  Release / acquire at GPU scope around the counter, so
+// what the CTA wrote before the barrier (fenced by the caller's CTA barrier) is visible to the
+// CTAs after it.  Returns false on give-up: the deadline, the CTA's own abort flag, or the
+// grid-wide abort word (which it then sets, so that the other CTAs stop waiting too).
+__device__ __noinline__ bool grid_arrive_wait(uint32_t* ctl, int idx, long long deadline, const volatile int* abort,
+                                              uint32_t* status) {
+  volatile uint32_t* gabort = ctl + kCtlAbort;
+  if (*abort) {
+    *gabort = 1u;
+    __threadfence();
+    return false;
+  }
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctl) : "memory");
+  const uint32_t target = uint32_t(idx + 1) * gridDim.x;
+  while (ld_acquire_gpu(ctl) < target) {
+    if (*gabort) return false;
+    if (clock64() > deadline) {
+      set_status(status, DSPARK_ETIMEOUT);
+      *gabort = 1u;
+      __threadfence();
+      return false;
+    }
+  }
+  return true;
+}
+
+// The epilogue's grid barrier: CTA barrier, one thread arrives and waits, CTA barrier.  Returns
+// the shared decision to stop (uniform across the epilogue warps: bar->bail is written only
+// between the two CTA barriers and read right after the second).
+__device__ __forceinline__ bool epi_grid_barrier(Barriers* bar, uint32_t* ctl, int idx, int et, long long deadline,
+                                                 uint32_t* status) {
+  epi_sync();
+  if (et == 0) bar->bail = grid_arrive_wait(ctl, idx, deadline, &bar->abort, status) ? 0 : 1;
+  epi_sync();
+  return bar->bail != 0;
+}
+
+// The select of position k for this CTA's requests: the epilogue's 512 threads (et) as two
+// groups of eight warps, group g taking requests blockIdx + (2 j + g) gridDim.  Out of line: its
+// registers are not added to the tile loop's.
+template <typename P>
+__device__ __noinline__ void select_requests(const P& p, int k, int et, SelectScratch* sm) {
+  const int grp = et >> 8, gt = et & 255;
+  for (int b = blockIdx.x + grp * int(gridDim.x); b < p.bs; b += 2 * int(gridDim.x))
+    select_row<__nv_bfloat16, 8>(b, gt, p.entries, p.n_slots, p.U, p.W1, p.W2t, p.states, p.anchor, p.tokens,
+                                 p.logit_x, p.lse, p.gamma, p.V, p.r, k, p.inv_tau, p.greedy, p.seed, p.step,
+                                 p.status, sm, [grp] { asm volatile("bar.sync %0, 256;" ::"r"(2 + grp) : "memory"); },
+                                 p.states == nullptr && k < p.k_last);
 }
 
 // Warp 1 at the end of the kernel: free the tensor memory.  An epilogue that gave up has not
@@ -166,14 +247,14 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     return;
   }
   const int nk = p.r / kBK;
-  uint8_t* sA = smem_raw;                    // nk atoms
-  uint8_t* sB = sA + nk * kAAtom;            // kBStages x 32 KB
-  uint8_t* sU = sB + kBStages * kBStage;     // 2 x 32 KB (U half of each epilogue set)
-  Barriers* bar = reinterpret_cast<Barriers*>(sU + 2 * kUHalfTile);
+  uint8_t* sB = smem_raw;                    // kBStages x 32 KB
+  uint8_t* sU = sB + kBStages * kBStage;     // [2 halves][kUDepth] x 32 KB
+  Barriers* bar = reinterpret_cast<Barriers*>(sU + 2 * kUDepth * kUHalfTile);
   volatile int* abort_flag = &bar->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bs = p.bs, V = p.V, r = p.r;
+  const int npos = p.k_last - p.k_first + 1;
   const int n_mt = (bs + kBM - 1) / kBM;
   const int m0 = (blockIdx.x % n_mt) * kBM;
   const int cstride = gridDim.x / n_mt;
@@ -186,17 +267,18 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
       tc::mbar_init(tc::smem_u32(&bar->b_empty[s]), 1);
     }
     for (int h = 0; h < 2; ++h) {
-      tc::mbar_init(tc::smem_u32(&bar->u_full[h]), 1);
-      tc::mbar_init(tc::smem_u32(&bar->u_empty[h]), kEpiWarps / 2);  // the warp set of the half
+      for (int j = 0; j < kUDepth; ++j) {
+        tc::mbar_init(tc::smem_u32(&bar->u_full[h][j]), 1);
+        tc::mbar_init(tc::smem_u32(&bar->u_empty[h][j]), 8);  // the two warp sets of the half
+      }
     }
-    for (int s = 0; s < kAccBufs; ++s) {
-      tc::mbar_init(tc::smem_u32(&bar->acc_full[s]), 1);
-      tc::mbar_init(tc::smem_u32(&bar->acc_empty[s]), kEpiWarps);  // both sets read every tile
-    }
+    tc::mbar_init(tc::smem_u32(&bar->acc_full), 1);
+    tc::mbar_init(tc::smem_u32(&bar->acc_empty), kEpiWarps);  // every set reads every tile
     tc::mbar_init(tc::smem_u32(&bar->drain), 1);
     tc::mbar_init(tc::smem_u32(&bar->a_ready), kEpiWarps);
     bar->abort = 0;
     bar->mma_pending = 0;
+    bar->bail = 0;
     tc::fence_mbar_init();
     tc::prefetch_tensormap(&tmap_w2);
     tc::prefetch_tensormap(&tmap_u);
@@ -211,21 +293,18 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
   const uint32_t tmem_base = bar->tmem_base;
   const long long deadline = tc::deadline_after_ns(p.timeout_ns);
   tc::grid_launch_dependents();  // the next kernel may start its own set-up now
-  float4 xmine = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(INT_MAX));  // epilogue entry
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
-    // U_k and W2t do not depend on the previous kernel: the rings fill while it finishes.
-    // Per tile: its W2t K-stages first (paced by the MMA), then the two U halves (paced by the
-    // epilogue sets, one tile deep).
+    // ------------------------------------------------------------------ W2t producer
+    // W2t does not depend on the previous kernel: the ring fills while it finishes.
     if (lane == 0) {
-      const uint64_t keep = tc::policy_evict_last(), stream = tc::policy_evict_first();
+      const uint64_t keep = tc::policy_evict_last();
       int bstage = 0, bph = 0;
-      int b_issued[kBStages], u_issued[2] = {-1, -1};
+      int b_issued[kBStages];
       for (int s = 0; s < kBStages; ++s) b_issued[s] = -1;
       bool ok = true;
-      for (int t = 0; t < n_tiles && ok; ++t) {
-        const int n0 = (c0 + t * cstride) * kBN;
+      for (int T = 0; T < npos * n_tiles && ok; ++T) {  // the same tiles at every position
+        const int n0 = (c0 + (T % n_tiles) * cstride) * kBN;
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->b_empty[bstage]), bph ^ 1, deadline, abort_flag)) {
             ok = false;
@@ -237,18 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
           b_issued[bstage] = bph;
           if (++bstage == kBStages) { bstage = 0; bph ^= 1; }
         }
-        for (int h = 0; h < 2 && ok; ++h) {
-          if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->u_empty[h]), (t & 1) ^ 1, deadline, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const uint32_t ufull = tc::smem_u32(&bar->u_full[h]);
-          tc::mbar_arrive_expect_tx(ufull, kUHalfTile);
-          const uint32_t ud = tc::smem_u32(sU + h * kUHalfTile);
-          tc::tma_load_3d(ud, &tmap_u, ufull, n0 + h * kHalfN, p.k - 1, m0, stream);
-          tc::tma_load_3d(ud + kUBox, &tmap_u, ufull, n0 + h * kHalfN + 64, p.k - 1, m0, stream);
-          u_issued[h] = t & 1;
-        }
       }
       if (!ok) {
         *abort_flag = 1;
@@ -258,43 +325,83 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
         const volatile int never = 0;
         for (int s = 0; s < kBStages; ++s)
           if (b_issued[s] >= 0) tc::mbar_wait_bounded(tc::smem_u32(&bar->b_full[s]), b_issued[s], dl, &never);
+      }
+    }
+  } else if (warp == kUWarp) {
+    // ------------------------------------------------------------------ U producer
+    // U_k does not depend on the previous kernel either.  Per tile the two halves, each paced
+    // by its epilogue set (one tile deep).
+    if (lane == 0) {
+      const uint64_t stream = tc::policy_evict_first();
+      int u_issued[2][kUDepth];
+      for (int h = 0; h < 2; ++h)
+        for (int j = 0; j < kUDepth; ++j) u_issued[h][j] = -1;
+      bool ok = true;
+      for (int T = 0; T < npos * n_tiles && ok; ++T) {  // tile T % n_tiles of position T / n_tiles
+        const int n0 = (c0 + (T % n_tiles) * cstride) * kBN;
+        const int k = p.k_first + T / n_tiles;
+        for (int h = 0; h < 2 && ok; ++h) {
+          const int j = T % kUDepth, ph = (T / kUDepth) & 1;
+          if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->u_empty[h][j]), ph ^ 1, deadline, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t ufull = tc::smem_u32(&bar->u_full[h][j]);
+          tc::mbar_arrive_expect_tx(ufull, kUHalfTile);
+          const uint32_t ud = tc::smem_u32(sU + (h * kUDepth + j) * kUHalfTile);
+          tc::tma_load_3d(ud, &tmap_u, ufull, n0 + h * kHalfN, k - 1, m0, stream);
+          tc::tma_load_3d(ud + kUBox, &tmap_u, ufull, n0 + h * kHalfN + 64, k - 1, m0, stream);
+          u_issued[h][j] = ph;
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(p.status, DSPARK_ETIMEOUT);
+        const long long dl = tc::deadline_after_ns(200000000ull);
+        const volatile int never = 0;
         for (int h = 0; h < 2; ++h)
-          if (u_issued[h] >= 0) tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[h]), u_issued[h], dl, &never);
+          for (int j = 0; j < kUDepth; ++j)
+            if (u_issued[h][j] >= 0)
+              tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[h][j]), u_issued[h][j], dl, &never);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
-      int bstage = 0, bph = 0, ab = 0, aph = 0;
-      bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->a_ready), 0, deadline, abort_flag);
+      int bstage = 0, bph = 0;
+      bool ok = true;
       bool issued = false;
-      for (int t = 0; t < n_tiles && ok; ++t) {
-        if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_empty[ab]), aph ^ 1, deadline, abort_flag)) {
+      for (int T = 0; T < npos * n_tiles && ok; ++T) {
+        // each position's A operand is written by the epilogue once it has read the previous
+        // position's last accumulator (so every MMA that read the old A has completed)
+        if (T % n_tiles == 0 &&
+            !tc::mbar_wait_bounded(tc::smem_u32(&bar->a_ready), (T / n_tiles) & 1, deadline, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_empty), (T & 1) ^ 1, deadline, abort_flag)) {
           ok = false;
           break;
         }
         tc::tc_fence_after();
-        const uint32_t d = tmem_base + ab * kBN;
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->b_full[bstage]), bph, deadline, abort_flag)) {
             ok = false;
             break;
           }
           tc::tc_fence_after();
-          const uint32_t a_addr = tc::smem_u32(sA + kb * kAAtom);
           const uint32_t b_addr = tc::smem_u32(sB + bstage * kBStage);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            tc::mma_bf16(d, tc::sdesc_kmajor_sw128(a_addr + kk * 32), tc::sdesc_kmajor_sw128(b_addr + kk * 32),
-                         idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < kBK / 16; ++kk)  // A: 8 TMEM columns (16 bf16) per K step
+            tc::mma_bf16_ts(tmem_base, tmem_base + kTmemA + kb * (kBK / 2) + kk * 8,
+                            tc::sdesc_kmajor_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
           issued = true;
           tc::mma_commit(tc::smem_u32(&bar->b_empty[bstage]));
           if (++bstage == kBStages) { bstage = 0; bph ^= 1; }
         }
         if (!ok) break;
-        tc::mma_commit(tc::smem_u32(&bar->acc_full[ab]));
-        if (++ab == kAccBufs) { ab = 0; aph ^= 1; }
+        tc::mma_commit(tc::smem_u32(&bar->acc_full));
       }
       if (!ok) {
         *abort_flag = 1;
@@ -310,124 +417,124 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     }
   } else {
     // ------------------------------------------------------------------ epilogue
+    const int et = tid - 64;          // 0 .. 511
     const int wq = warp & 3;          // TMEM lane quarter this warp may access
     const int m = wq * 32 + lane;     // tile row = TMEM lane
-    const int half = (warp - 2) >> 2; // warp set: columns 128 half .. 128 half + 127 of each tile
+    const int set = (warp - 2) >> 2;  // warp set: columns 64 set .. 64 set + 63 of each tile
     const int grow = m0 + m;
     const float inv_tau = p.inv_tau;
     const float c2 = inv_tau * kLog2e;
-    // The chunk Gumbels (Philox purpose 1) of this row and of the first kGReg tiles do not
-    // depend on any logit: draw them before waiting for the previous kernel, so that the Philox
-    // rounds overlap its tail instead of the tile loop.  Later tiles draw theirs in the loop.
-    constexpr int kGReg = 6;
-    float2 gk[kGReg];
-#pragma unroll
-    for (int i = 0; i < kGReg; ++i) {
-      gk[i] = make_float2(0.f, 0.f);
-      if (!p.greedy && i < n_tiles) gk[i] = tile_gumbels(p.seed, p.step, grow, p.k, c0 + i * cstride, half);
-    }
-    // x_{k-1} comes from the previous kernel (the select of position k-1): everything above
-    // -- barrier set-up, TMEM, the producer's U / W2 prefetch, the Gumbels -- overlapped with it
+    const uint32_t lane_base = tmem_base + (uint32_t(wq * 32) << 16);
+    const uint32_t taddr = lane_base + set * kDraftIds;
+    const int uh = set >> 1;  // the U half holding this set's 64-id box (box set & 1 of it)
+    const uint8_t* ub0 = sU + uh * kUDepth * kUHalfTile + (set & 1) * kUBox + m * 128;  // this row, buffer 0
+    // x_0 (the anchors) and the first position's inputs come from earlier kernels: everything
+    // above -- barrier set-up, TMEM, the producers' U / W2 prefetch -- overlapped with them
     tc::grid_dependency_wait();
-    {
-      // A operand: rows m0..m0+127 of the factor -- W1[x_{k-1}] (Markov head) or s_k (RNN head)
-      // -- in the 128-byte-swizzled K-major layout.  Row indices first, then every 16-byte row
-      // chunk as an independent cp.async.
-      const __nv_bfloat16* base = p.states ? p.states : p.W1;
-      const int et = tid - 64;
-      for (int mm = et; mm < kBM; mm += kEpiThreads) {
-        const int gr = m0 + mm;
-        int idx = -1;
-        if (gr < bs)
-          idx = p.states ? gr * p.gamma + p.k - 1
-                         : clamp_token((p.k == 1) ? p.anchor[gr] : p.tokens[size_t(gr) * p.gamma + p.k - 2], V);
-        bar->xrow[mm] = idx;
-      }
-      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-      const int cpr = r / 8;  // 16-byte chunks per row
-      for (int idx = et; idx < kBM * cpr; idx += kEpiThreads) {
-        const int row = idx / cpr, ch = idx % cpr;
-        const int xp = bar->xrow[row];
-        const int kb = ch >> 3, j = ch & 7;
-        const uint32_t dst = tc::smem_u32(sA + kb * kAAtom + row * 128 + ((j ^ (row & 7)) << 4));
-        cp_async16(dst, xp >= 0 ? base + size_t(xp) * r + ch * 8 : base, xp >= 0 ? 16u : 0u);
-      }
-      cp_async_wait_all();
-      tc::fence_proxy_async_smem();
-    }
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->a_ready));
-
-    const uint32_t taddr = tmem_base + (uint32_t(wq * 32) << 16) + half * kHalfN;
-    const uint8_t* ub = sU + half * kUHalfTile + m * 128;  // this row in U half `half`
-    // running (max, sum-exp) in log2 units: run_m = max of l c2, run_s = sum of 2^(l c2 - run_m)
-    float run_m = -INFINITY, run_s = 0.f, best_key = -INFINITY;
-    int best_c = INT_MAX;
-    for (int t = 0; t < n_tiles; ++t) {
-      const int c = c0 + t * cstride;
-      const int n0 = c * kBN + half * kHalfN;  // this set's first id
-      const int valid = min(kHalfN, V - n0);   // <= 0: this set's half lies past the vocabulary
-      const int ab = t & 1;
-      bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full[ab]), (t >> 1) & 1, deadline, abort_flag) &&
-                tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[half]), t & 1, deadline, abort_flag);
-      // one decision per warp before the .sync.aligned TMEM loads; warps run independently
-      // (no named barrier in this loop), so a warp that gives up can hold up no other
-      ok = __all_sync(0xFFFFFFFFu, ok);
-      if (!ok) {
-        *abort_flag = 1;
-        set_status(p.status, DSPARK_ETIMEOUT);
-        break;
-      }
-      tc::tc_fence_after();
-      float v[kHalfN];
+    int T = 0;  // tiles consumed so far, over all positions (accumulator / U ring phases)
+    for (int pi = 0; pi < npos; ++pi) {
+      const int k = p.k_first + pi;
+      {
+        // A operand into tensor memory: this row's W1[x_{k-1}] (Markov head) or s_k (RNN head)
+        // (a zero row past the batch).  The four warp sets of a lane quarter share the row, set s
+        // its K values [s r / 4, (s + 1) r / 4) (r / 8 columns of bf16 pairs), all of its loads
+        // issued before its stores (one round trip for the gather).  Every MMA that read the
+        // previous position's A has completed: this thread has waited for the accumulator of
+        // that position's last tile.
+        const bool live = grow < bs;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            live ? factor_row(p.W1, p.states, p.anchor, p.tokens, grow, k, p.gamma, V, r) : p.W1);
+        const int nq = r / 32;  // 16-byte pieces of the set's K range: 2, 4 or 8
+        uint4 w[8];
 #pragma unroll
-      for (int q = 0; q < kHalfN / 32; ++q)
-        tc::tmem_ld32(taddr + ab * kBN + q * 32, reinterpret_cast<uint32_t*>(v + q * 32));
-      tc::tmem_ld_wait();
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->acc_empty[ab]));
+        for (int q = 0; q < 8; ++q)
+          w[q] = (live && q < nq) ? src[set * nq + q] : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int j = 0; j < kHalfN / 8; ++j) {  // + U_k: 16-byte groups of the half's two 64-id boxes
-        const uint4 q = *reinterpret_cast<const uint4*>(ub + (j >> 3) * kUBox + (((j & 7) ^ (m & 7)) << 4));
-        v[8 * j + 0] += bf16lo(q.x); v[8 * j + 1] += bf16hi(q.x);
-        v[8 * j + 2] += bf16lo(q.y); v[8 * j + 3] += bf16hi(q.y);
-        v[8 * j + 4] += bf16lo(q.z); v[8 * j + 5] += bf16hi(q.z);
-        v[8 * j + 6] += bf16lo(q.w); v[8 * j + 7] += bf16hi(q.w);
-      }
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->u_empty[half]));
-
-      if (p.greedy) {
-        float best = -INFINITY;
-        int bi = INT_MAX;
-#pragma unroll
-        for (int q = 0; q < kHalfN; ++q)
-          if (q < valid && v[q] > best) { best = v[q]; bi = q; }
-        // chunks arrive in increasing order: a strict > keeps the lowest index on ties
-        if (best > best_key) { best_key = best; best_c = n0 + bi; }
-      } else {
-        float2 g;
-        if (t < kGReg) {
-          g = gk[0];
-#pragma unroll
-          for (int j = 0; j + 1 < kGReg; ++j) gk[j] = gk[j + 1];
-        } else {
-          g = tile_gumbels_call(p.seed, p.step, grow, p.k, c, half);
+        for (int q = 0; q < 8; q += 2) {
+          if (q < nq) {
+            const uint32_t a8[8] = {w[q].x, w[q].y, w[q].z, w[q].w, w[q + 1].x, w[q + 1].y, w[q + 1].z, w[q + 1].w};
+            tc::tmem_st8(lane_base + kTmemA + set * (r / 8) + q * 4, a8);
+          }
         }
-        // the set's draft chunks 4c + 2h (ids 0..63 of its half) and 4c + 2h + 1, in that order;
-        // only the last tile of a vocabulary that is not a multiple of 256 is ragged
+        tc::tmem_st_wait();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->a_ready));
+      }
+
+      // running (max, sum-exp) in log2 units: run_m = max of l c2, run_s = sum of 2^(l c2 - run_m)
+      float run_m = -INFINITY, run_s = 0.f, best_key = -INFINITY;
+      int best_c = INT_MAX;
+      for (int t = 0; t < n_tiles; ++t, ++T) {
+        const int c = c0 + t * cstride;
+        const int n0 = c * kBN + set * kDraftIds;  // this set's first id: draft chunk 4c + set
+        const int valid = min(kDraftIds, V - n0);  // <= 0: the chunk lies past the vocabulary
+        // the chunk's Gumbel (Philox purpose 1) depends on no logit: drawn before the wait for
+        // the accumulator, while the tile's MMAs run
+        const float g = p.greedy ? 0.f : chunk_gumbel_call(p.seed, p.step, grow, k, c, set);
+        bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_full), T & 1, deadline, abort_flag);
+        // one decision per warp before the .sync.aligned TMEM loads; warps run independently
+        // (no named barrier in this loop), so a warp that gives up can hold up no other
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) {
+          *abort_flag = 1;
+          set_status(p.status, DSPARK_ETIMEOUT);
+          break;
+        }
+        tc::tc_fence_after();
+        float v[kDraftIds];
+        tc::tmem_ld32(taddr, reinterpret_cast<uint32_t*>(v));
+        tc::tmem_ld32(taddr + 32, reinterpret_cast<uint32_t*>(v + 32));
+        tc::tmem_ld_wait();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->acc_empty));  // the next tile's MMAs may start
+        const int uj = T % kUDepth;
+        ok = __all_sync(0xFFFFFFFFu, tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[uh][uj]),
+                                                           (T / kUDepth) & 1, deadline, abort_flag));
+        if (!ok) {
+          *abort_flag = 1;
+          set_status(p.status, DSPARK_ETIMEOUT);
+          break;
+        }
+        const uint8_t* ub = ub0 + uj * kUHalfTile;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const float* vq = v + q * kDraftIds;
-          const int vl = valid - q * kDraftIds;
-          const bool full = vl >= kDraftIds;
-          const float mx = full ? row_max<false>(vq, vl) : row_max<true>(vq, vl);
+        for (int j = 0; j < kDraftIds / 8; ++j) {  // + U_k: the box's 16-byte groups of this row
+          const uint4 q = *reinterpret_cast<const uint4*>(ub + ((j ^ (m & 7)) << 4));
+          v[8 * j + 0] += bf16lo(q.x); v[8 * j + 1] += bf16hi(q.x);
+          v[8 * j + 2] += bf16lo(q.y); v[8 * j + 3] += bf16hi(q.y);
+          v[8 * j + 4] += bf16lo(q.z); v[8 * j + 5] += bf16hi(q.z);
+          v[8 * j + 6] += bf16lo(q.w); v[8 * j + 7] += bf16hi(q.w);
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->u_empty[uh][uj]));
+
+        if (p.greedy) {
+          // eight independent (max, first index) chains over offsets q = j (mod 8), merged with
+          // the lowest offset on ties; a strict > inside a chain keeps its lowest offset
+          float b8[8];
+          int i8[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) { b8[j] = -INFINITY; i8[j] = INT_MAX; }
+#pragma unroll
+          for (int q = 0; q < kDraftIds; ++q)
+            if (q < valid && v[q] > b8[q & 7]) { b8[q & 7] = v[q]; i8[q & 7] = q; }
+          float best = b8[0];
+          int bi = i8[0];
+#pragma unroll
+          for (int j = 1; j < 8; ++j)
+            if (b8[j] > best || (b8[j] == best && i8[j] < bi)) { best = b8[j]; bi = i8[j]; }
+          // chunks arrive in increasing order: a strict > keeps the lowest index on ties
+          if (best > best_key) { best_key = best; best_c = n0 + bi; }
+        } else {
+          // only the last tile of a vocabulary that is not a multiple of 256 is ragged
+          const bool full = valid >= kDraftIds;
+          const float mx = full ? row_max<false>(v, valid) : row_max<true>(v, valid);
           if (mx > -INFINITY) {
-            const float sc = full ? row_sum_exp2<false>(vq, vl, mx * c2, c2)
-                                  : row_sum_exp2<true>(vq, vl, mx * c2, c2);
-            const float key = mx * inv_tau + logf(sc) + (q ? g.y : g.x);  // log-mass + Gumbel
-            if (key > best_key) { best_key = key; best_c = 4 * c + 2 * half + q; }
+            const float sc = full ? row_sum_exp2<false>(v, valid, mx * c2, c2)
+                                  : row_sum_exp2<true>(v, valid, mx * c2, c2);
+            const float key = mx * inv_tau + logf(sc) + g;  // log-mass + Gumbel
+            if (key > best_key) { best_key = key; best_c = 4 * c + set; }
             const float m2 = mx * c2;
             if (m2 > run_m) {
               run_s = run_s * exp2f(run_m - m2) + sc;
@@ -438,25 +545,61 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
           }
         }
       }
+      run_m *= 0.69314718055994531f;  // back to natural units: max of l / T
+      // The four sets' entries of a row meet in TMEM columns 384 + 4 s; set 0 merges them in set
+      // order and writes the CTA's entry (request grow, slot c0).  Within a tile a lower set's
+      // chunk comes first, so on equal keys the lower chunk wins, as the merge's lowest-index
+      // rule gives.  (A warp that gave up above still passes every barrier below; the grid
+      // barrier then stops the whole epilogue.)
+      {
+        const uint32_t e4[4] = {__float_as_uint(run_m), __float_as_uint(run_s), __float_as_uint(best_key),
+                                uint32_t(best_c)};
+        tc::tmem_st4(lane_base + kTmemX + 4 * set, e4);
+        tc::tmem_st_wait();
+      }
+      tc::tc_fence_before();
+      epi_sync();
+      tc::tc_fence_after();
+      if (set == 0) {
+        uint32_t x[16];
+        tc::tmem_ld16(lane_base + kTmemX, x);
+        tc::tmem_ld_wait();
+        LsePair l{__uint_as_float(x[0]), __uint_as_float(x[1])};
+        ArgMax a{__uint_as_float(x[2]), int(x[3])};
+#pragma unroll
+        for (int q = 1; q < kEpiSets; ++q) {
+          l = lse_merge(l, LsePair{__uint_as_float(x[4 * q]), __uint_as_float(x[4 * q + 1])});
+          a = better(a, ArgMax{__uint_as_float(x[4 * q + 2]), int(x[4 * q + 3])});
+        }
+        if (grow < bs) p.entries[size_t(grow) * p.n_slots + c0] = make_float4(l.m, l.s, a.v, __int_as_float(a.i));
+      }
+      // every CTA's entries of position k are written: the select of k, two requests at a time
+      if (epi_grid_barrier(bar, p.ctl, 2 * pi, et, deadline, p.status)) {
+        *abort_flag = 1;
+        break;
+      }
+      select_requests(p, k, et, &bar->sel[et >> 8]);
+      // x_k of every request is written before any CTA gathers the next position's A rows
+      if (pi + 1 < npos && epi_grid_barrier(bar, p.ctl, 2 * pi + 1, et, deadline, p.status)) {
+        *abort_flag = 1;
+        break;
+      }
     }
-    run_m *= 0.69314718055994531f;  // back to natural units: max of l / T
-    // the two warp sets of a lane quarter meet in shared memory after the final barrier
-    if (half == 1) bar->xch[m] = make_float4(run_m, run_s, best_key, __int_as_float(best_c));
-    xmine = make_float4(run_m, run_s, best_key, __int_as_float(best_c));
   }
 
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) free_tmem(bar, tmem_base, lane);
-  if (warp >= 2 && warp < 6) {
-    // warp set 0 merges the other set's entry of the same row and writes the CTA's entry
-    // (request grow, slot c0); within a tile set 0's chunks come first, so on equal keys its
-    // (lower) chunk wins, as the merge's lowest-index rule gives
-    const int m = (warp & 3) * 32 + lane, grow = m0 + m;
-    const float4 o = bar->xch[m];
-    const LsePair l = lse_merge(LsePair{xmine.x, xmine.y}, LsePair{o.x, o.y});
-    const ArgMax a = better(ArgMax{xmine.z, __float_as_int(xmine.w)}, ArgMax{o.z, __float_as_int(o.w)});
-    if (grow < bs) p.entries[size_t(grow) * p.n_slots + c0] = make_float4(l.m, l.s, a.v, __int_as_float(a.i));
+  if (tid == 0) {
+    // the last CTA out zeroes the grid barrier's words for the next launch (which touches them
+    // only after its grid-dependency wait, i.e. after this grid has completed)
+    __threadfence();
+    if (atomicAdd(p.ctl + kCtlExit, 1u) == gridDim.x - 1) {
+      p.ctl[0] = 0u;
+      p.ctl[kCtlAbort] = 0u;
+      __threadfence();
+      p.ctl[kCtlExit] = 0u;
+    }
   }
 }
 
@@ -474,13 +617,12 @@ int draft_tc_slots(int bs, int V) {
   return tch::vocab_grid(bs, (V + kBN - 1) / kBN) / n_mt;
 }
 
-cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t, const void* states,
-                                  const int32_t* anchor, const int32_t* tokens, int bs, int gamma,
-                                  int V, int r, int k, float inv_tau, int greedy, uint64_t seed,
-                                  uint64_t step, void* entries, int n_chunks, int* n_slots,
-                                  uint32_t* status, cudaStream_t s) {
-  (void)n_chunks;
+cudaError_t launch_draft_tc(const void* U, const void* W1, const void* W2t, const void* states, const int32_t* anchor,
+                            int32_t* tokens, float* logit_x, float* lse, int bs, int gamma, int V, int r, int k_first,
+                            int k_last, float inv_tau, int greedy, uint64_t seed, uint64_t step, void* entries,
+                            uint32_t* ctl, uint32_t* status, cudaStream_t s) {
   if (!tch::encode_fn()) return cudaErrorNotSupported;
+  if (k_first < 1 || k_last < k_first || k_last > gamma) return cudaErrorInvalidValue;
   CUtensorMap map_w2, map_u;
   if (!tch::encode_bf16_2d(&map_w2, W2t, size_t(V), size_t(r), kBN)) return cudaErrorInvalidValue;
   {
@@ -495,36 +637,45 @@ cudaError_t launch_draft_stats_tc(const void* U, const void* W1, const void* W2t
   }
   static bool smem_set[tch::kMaxDevices] = {};
   static std::mutex smem_mu;
-  if (cudaError_t e = tch::set_smem_once(draft_tc_kernel, int(smem_bytes(256)), smem_set, &smem_mu)) return e;
+  if (cudaError_t e = tch::set_smem_once(draft_tc_kernel, int(kSmemBytes), smem_set, &smem_mu)) return e;
   const int n_tiles = (V + kBN - 1) / kBN;
-  const int grid = tch::vocab_grid(bs, n_tiles);
+  const int grid = tch::vocab_grid(bs, n_tiles);  // at most one CTA per SM: all resident together
   Params prm{};
+  prm.U = static_cast<const __nv_bfloat16*>(U);
   prm.W1 = static_cast<const __nv_bfloat16*>(W1);
+  prm.W2t = static_cast<const __nv_bfloat16*>(W2t);
   prm.states = static_cast<const __nv_bfloat16*>(states);
   prm.anchor = anchor;
   prm.tokens = tokens;
-  prm.bs = bs; prm.gamma = gamma; prm.V = V; prm.r = r; prm.k = k;
+  prm.logit_x = logit_x;
+  prm.lse = lse;
+  prm.bs = bs; prm.gamma = gamma; prm.V = V; prm.r = r;
+  prm.k_first = k_first; prm.k_last = k_last;
   prm.inv_tau = inv_tau;
   prm.greedy = greedy;
   prm.n_tiles = n_tiles;
   prm.status = status;
+  prm.ctl = ctl;
   prm.timeout_ns = g_wait_timeout_ns;
   prm.entries = static_cast<float4*>(entries);
   prm.n_slots = grid / ((bs + kBM - 1) / kBM);
   prm.seed = seed;
   prm.step = step;
-  *n_slots = prm.n_slots;
-  // programmatic dependent launch: set-up and prefetch overlap the previous kernel's tail
+  // cooperative: the CTAs wait on one another at the grid barriers, so the launch must make them
+  // all resident; programmatic dependent launch: set-up and prefetch overlap the previous
+  // kernel's tail
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes(r);
+  cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, draft_tc_kernel, map_w2, map_u, prm);
 }
 

@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(256, 1) decision_select_kernel(
   }
   __syncthreads();
   const float lse_t = rs[d.pdec].lse;
-  if (recompute) chunk_dots<T>(W2t, r, V, cstar * kChunk, sA, tw);
+  if (recompute) chunk_dots<T>(W2t, r, V, cstar * kChunk, sA, tw, threadIdx.x);
   __syncthreads();
   if (tid < kChunk) {
     const int v = cstar * kChunk + tid;
