@@ -24,8 +24,8 @@
 // The second bound is how fast W2t reaches shared memory: every position streams all of W2t
 // from L2 (where it stays), so a CTA needs as many bytes in flight as the L2 round trip times
 // the tensor core's consumption.  Hence the A operand lives in tensor memory, not shared memory,
-// and the freed space lets the U_k tiles (streamed from HBM, with its longer latency) be loaded
-// two tiles ahead beside a three-deep W2t ring.
+// and the freed space holds a W2t ring of one whole tile (so the next tile's operands are in
+// flight while this tile's MMAs run) beside a ring of U_k boxes 1.5 tiles deep.
 //
 // Work decomposition:
 //   tile      = 128 requests (TMEM lanes) x 256 vocabulary ids (= four 64-id draft chunks),
@@ -33,11 +33,11 @@
 //   CTA       = persistent, one per SM; fixed 128-request M-tile, strided over vocabulary
 //               tiles; the gathered A operand (W1[x_{k-1}], or s_k) is written once into tensor
 //               memory by the epilogue warps (tcgen05.st)
-//   warp 0    = TMA producer of W2t K-stages [256 ids x 64 K] (32 KB, a three-deep ring,
+//   warp 0    = TMA producer of W2t K-stages [256 ids x 64 K] (32 KB, a four-deep ring,
 //               evict-last: every position re-reads W2t and it stays in L2)
-//   warp 18   = TMA producer of the two halves of the U_k tile (3-D map over [bs, gamma, V],
-//               evict-first; two buffers per half), on its own so that U never waits behind a
-//               W2t stage
+//   warp 18   = TMA producer of the U_k tile's four 64-id boxes (3-D map over [bs, gamma, V],
+//               evict-first; a ring of six 16 KB boxes), on its own so that U never waits
+//               behind a W2t stage
 //   warp 1    = TMEM owner + single-thread tcgen05.mma issuer, commits to mbarriers; the next
 //               tile's MMAs start once both epilogue sets have read the accumulator into
 //               registers (a single accumulator: its readout is short next to the tile)
@@ -76,11 +76,10 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBN = 256;                          // ids per tile
-constexpr int kHalfN = kBN / 2;                   // ids per U half (two draft chunks)
 static_assert(kBN == 4 * kDraftIds, "a tile is four draft chunks, one per epilogue set");
 constexpr int kBK = 64;                           // K per stage: one 128-byte swizzle row
-constexpr int kBStages = 3;                       // W2t ring of 32 KB stages
-constexpr int kUDepth = 2;                        // U buffers per epilogue set (tiles ahead)
+constexpr int kBStages = 4;                       // W2t ring of 32 KB stages: one whole tile
+constexpr int kUSlots = 6;                        // U ring of 64-id boxes: 1.5 tiles
 constexpr int kEpiSets = 4;                       // warp sets of four warps, one draft chunk each
 constexpr int kEpiWarps = 4 * kEpiSets;
 constexpr int kEpiThreads = 32 * kEpiWarps;
@@ -88,7 +87,6 @@ constexpr int kUWarp = 2 + kEpiWarps;             // warp 18: the U producer
 constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr uint32_t kBStage = kBN * kBK * 2;       // 32 KB: W2t rows [256 x 64 K]
 constexpr uint32_t kUBox = kBM * 64 * 2;          // 16 KB: U [128 rows x 64 ids]
-constexpr uint32_t kUHalfTile = 2 * kUBox;        // 32 KB: one epilogue set's 128 ids
 constexpr uint32_t kTmemA = kBN;                  // A: columns 256 .. 256 + r / 2 - 1 (bf16 pairs)
 constexpr uint32_t kTmemX = kTmemA + 128;         // 384 + 4 s: warp set s's entry, merged by set 0
 constexpr uint32_t kTmemCols = 512;               // allocation: a power of two >= 256 + 128
@@ -96,7 +94,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct Barriers {
   uint64_t b_full[kBStages], b_empty[kBStages];
-  uint64_t u_full[2][kUDepth], u_empty[2][kUDepth];  // U half h (epilogue sets 2h, 2h + 1), buffer j
+  uint64_t u_full[kUSlots], u_empty[kUSlots];  // U box q = 4 T + s (tile T, set s) in slot q % kUSlots
   uint64_t acc_full, acc_empty;
   uint64_t drain;
   uint64_t a_ready;  // the A operand is in tensor memory (one arrival per epilogue warp)
@@ -132,7 +130,7 @@ constexpr int kCtlAbort = 16, kCtlExit = 32;  // words of the grid barrier block
 
 // Dynamic shared memory: W2t ring | U halves | barriers.  The buffer is declared 1024-byte
 // aligned (128-byte swizzle atoms).
-constexpr size_t kSmemBytes = kBStages * size_t(kBStage) + 2 * kUDepth * size_t(kUHalfTile) + sizeof(Barriers);
+constexpr size_t kSmemBytes = kBStages * size_t(kBStage) + kUSlots * size_t(kUBox) + sizeof(Barriers);
 static_assert(kSmemBytes <= 232448, "dynamic shared memory beyond the 227 KB per-block limit");
 
 // The Gumbel of draft chunk 4c + s (warp set s's chunk of vocabulary tile c), request `req`,
@@ -248,8 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
   }
   const int nk = p.r / kBK;
   uint8_t* sB = smem_raw;                    // kBStages x 32 KB
-  uint8_t* sU = sB + kBStages * kBStage;     // [2 halves][kUDepth] x 32 KB
-  Barriers* bar = reinterpret_cast<Barriers*>(sU + 2 * kUDepth * kUHalfTile);
+  uint8_t* sU = sB + kBStages * kBStage;     // kUSlots x 16 KB
+  Barriers* bar = reinterpret_cast<Barriers*>(sU + kUSlots * kUBox);
   volatile int* abort_flag = &bar->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -266,11 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
       tc::mbar_init(tc::smem_u32(&bar->b_full[s]), 1);
       tc::mbar_init(tc::smem_u32(&bar->b_empty[s]), 1);
     }
-    for (int h = 0; h < 2; ++h) {
-      for (int j = 0; j < kUDepth; ++j) {
-        tc::mbar_init(tc::smem_u32(&bar->u_full[h][j]), 1);
-        tc::mbar_init(tc::smem_u32(&bar->u_empty[h][j]), 8);  // the two warp sets of the half
-      }
+    for (int j = 0; j < kUSlots; ++j) {
+      tc::mbar_init(tc::smem_u32(&bar->u_full[j]), 1);
+      tc::mbar_init(tc::smem_u32(&bar->u_empty[j]), 4);  // the four warps of the box's set
     }
     tc::mbar_init(tc::smem_u32(&bar->acc_full), 1);
     tc::mbar_init(tc::smem_u32(&bar->acc_empty), kEpiWarps);  // every set reads every tile
@@ -329,29 +325,26 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     }
   } else if (warp == kUWarp) {
     // ------------------------------------------------------------------ U producer
-    // U_k does not depend on the previous kernel either.  Per tile the two halves, each paced
-    // by its epilogue set (one tile deep).
+    // U_k does not depend on the previous kernel either.  Per tile its four 64-id boxes, box s
+    // paced by epilogue set s, through a ring of kUSlots boxes.
     if (lane == 0) {
       const uint64_t stream = tc::policy_evict_first();
-      int u_issued[2][kUDepth];
-      for (int h = 0; h < 2; ++h)
-        for (int j = 0; j < kUDepth; ++j) u_issued[h][j] = -1;
+      int u_issued[kUSlots];
+      for (int j = 0; j < kUSlots; ++j) u_issued[j] = -1;
       bool ok = true;
       for (int T = 0; T < npos * n_tiles && ok; ++T) {  // tile T % n_tiles of position T / n_tiles
         const int n0 = (c0 + (T % n_tiles) * cstride) * kBN;
         const int k = p.k_first + T / n_tiles;
-        for (int h = 0; h < 2 && ok; ++h) {
-          const int j = T % kUDepth, ph = (T / kUDepth) & 1;
-          if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->u_empty[h][j]), ph ^ 1, deadline, abort_flag)) {
+        for (int sb = 0; sb < kEpiSets; ++sb) {
+          const int q = kEpiSets * T + sb, j = q % kUSlots, ph = (q / kUSlots) & 1;
+          if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->u_empty[j]), ph ^ 1, deadline, abort_flag)) {
             ok = false;
             break;
           }
-          const uint32_t ufull = tc::smem_u32(&bar->u_full[h][j]);
-          tc::mbar_arrive_expect_tx(ufull, kUHalfTile);
-          const uint32_t ud = tc::smem_u32(sU + (h * kUDepth + j) * kUHalfTile);
-          tc::tma_load_3d(ud, &tmap_u, ufull, n0 + h * kHalfN, k - 1, m0, stream);
-          tc::tma_load_3d(ud + kUBox, &tmap_u, ufull, n0 + h * kHalfN + 64, k - 1, m0, stream);
-          u_issued[h][j] = ph;
+          const uint32_t ufull = tc::smem_u32(&bar->u_full[j]);
+          tc::mbar_arrive_expect_tx(ufull, kUBox);
+          tc::tma_load_3d(tc::smem_u32(sU + j * kUBox), &tmap_u, ufull, n0 + sb * kDraftIds, k - 1, m0, stream);
+          u_issued[j] = ph;
         }
       }
       if (!ok) {
@@ -359,10 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
         set_status(p.status, DSPARK_ETIMEOUT);
         const long long dl = tc::deadline_after_ns(200000000ull);
         const volatile int never = 0;
-        for (int h = 0; h < 2; ++h)
-          for (int j = 0; j < kUDepth; ++j)
-            if (u_issued[h][j] >= 0)
-              tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[h][j]), u_issued[h][j], dl, &never);
+        for (int j = 0; j < kUSlots; ++j)
+          if (u_issued[j] >= 0) tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[j]), u_issued[j], dl, &never);
       }
     }
   } else if (warp == 1) {
@@ -426,8 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     const float c2 = inv_tau * kLog2e;
     const uint32_t lane_base = tmem_base + (uint32_t(wq * 32) << 16);
     const uint32_t taddr = lane_base + set * kDraftIds;
-    const int uh = set >> 1;  // the U half holding this set's 64-id box (box set & 1 of it)
-    const uint8_t* ub0 = sU + uh * kUDepth * kUHalfTile + (set & 1) * kUBox + m * 128;  // this row, buffer 0
+    const uint8_t* urow = sU + m * 128;  // this row in U slot 0
     // x_0 (the anchors) and the first position's inputs come from earlier kernels: everything
     // above -- barrier set-up, TMEM, the producers' U / W2 prefetch -- overlapped with them
     tc::grid_dependency_wait();
@@ -489,15 +479,15 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->acc_empty));  // the next tile's MMAs may start
-        const int uj = T % kUDepth;
-        ok = __all_sync(0xFFFFFFFFu, tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[uh][uj]),
-                                                           (T / kUDepth) & 1, deadline, abort_flag));
+        const int uq = kEpiSets * T + set, uj = uq % kUSlots;  // this set's U box of the tile
+        ok = __all_sync(0xFFFFFFFFu, tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[uj]), (uq / kUSlots) & 1,
+                                                           deadline, abort_flag));
         if (!ok) {
           *abort_flag = 1;
           set_status(p.status, DSPARK_ETIMEOUT);
           break;
         }
-        const uint8_t* ub = ub0 + uj * kUHalfTile;
+        const uint8_t* ub = urow + uj * kUBox;
 #pragma unroll
         for (int j = 0; j < kDraftIds / 8; ++j) {  // + U_k: the box's 16-byte groups of this row
           const uint4 q = *reinterpret_cast<const uint4*>(ub + ((j ^ (m & 7)) << 4));
@@ -507,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
           v[8 * j + 6] += bf16lo(q.w); v[8 * j + 7] += bf16hi(q.w);
         }
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->u_empty[uh][uj]));
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->u_empty[uj]));
 
         if (p.greedy) {
           // eight independent (max, first index) chains over offsets q = j (mod 8), merged with
