@@ -262,7 +262,7 @@ def _profiled_traffic(name: str):
     return d.get("dram_bytes_per_call")
 
 
-DRAFT_SOURCES = ["draft_tc.cu", "draft.cu", "common.cuh", "tc_ptx.cuh", "tc_host.h"]
+DRAFT_SOURCES = ["draft_tc.cu", "draft.cu", "draft_select.cuh", "common.cuh", "tc_ptx.cuh", "tc_host.h"]
 VERIFY_SOURCES = ["verify.cu", "decide_tc.cu", "common.cuh", "tc_ptx.cuh", "tc_host.h"]
 
 
@@ -279,8 +279,8 @@ def rooflines(wl, stage_ms, rows, tau, profile_key=None):
     return {
         "bound": "hbm", "achieved": db / dsec / 1e9, "peak": hbm, "unit": "GB/s", "frac": db / dsec / 1e9 / hbm,
         "traffic": traffic, "traffic_over_algorithmic": (traffic / db) if traffic else None,
-        "kernel": "dspark_draft_block (gamma tensor-core vocabulary passes, draft_tc_kernel the dominant kernel, "
-                  "+ gamma selects): one C-ABI call, CUDA events around it in the timed steps",
+        "kernel": "dspark_draft_block: one persistent cooperative draft_tc_kernel launch over all gamma positions "
+                  "(vocabulary passes + in-kernel selects); one C-ABI call, CUDA events around it in the timed steps",
         "algorithmic_bytes": db, "peak_kind": peak_kind,
         "tensor": {"achieved": dflop / dsec / 1e12, "peak": bf16, "unit": "TFLOP/s",
                    "frac": dflop / dsec / 1e12 / bf16, "flops": dflop},
