@@ -217,8 +217,9 @@ def cpu_baseline(n_req: int = 128, steps: int = 3):
 
 def draft_bytes(bs: int, gamma: int, V: int, r: int, esize: int = 2) -> int:
     """One dspark_draft_block call: U [bs, gamma, V] read once, W2 [r, V] read once, and the
-    gamma x bs gathered W1 rows.  Re-reads of W2 by later positions (it does not stay in L2)
-    are traffic, reported beside this, not algorithmic bytes."""
+    gamma x bs gathered W1 rows.  Any re-read of W2 from DRAM by a later position (it stays in
+    L2 inside the persistent draft kernel, mostly) is traffic, reported beside this, not
+    algorithmic bytes."""
     return bs * gamma * V * esize + V * r * esize + bs * gamma * r * esize
 
 

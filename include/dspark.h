@@ -310,9 +310,9 @@ DSPARK_API int dspark_verify(const void* target, int dtype, const int32_t* cu_se
  *   until exit).  A call needs 256 B + bs * n * 16 B of it, n = the CTA columns of the
  *   tensor-core pass (bf16 with r = 64, 128 or 256; at most the SM count, fewer when bs > 128
  *   or when V has fewer 256-id tiles) and n = ceil(V / 64) on the CUDA-core pass (fp32, or
- *   r = 32); sizes needing more are rejected with DSPARK_EUNSUPPORTED.  At bs = 256 every V the
- *   library accepts fits the tensor-core pass (256 x 152 x 16 B = 0.6 MB at most on a 152-SM
- *   GB300); the CUDA-core pass allows V <= 131,008.
+ *   r = 32); sizes needing more are rejected with DSPARK_EUNSUPPORTED.  Every V the library
+ *   accepts fits the tensor-core pass (at most 128 x 152 or 256 x 76 slots of 16 B, 0.3 MB, on
+ *   a 152-SM GB300); at bs = 256 the CUDA-core pass allows V <= 131,008.
  *   The first call on a device looks up the array's device address (once per device, with that
  *   device current); make that first call before any stream capture.  The address is kept for
  *   the life of the process: cudaDeviceReset between calls is not supported.

@@ -42,6 +42,10 @@ SMALL = {
                                                    seed=14),
     "bf16_two_mtiles": I.WORKLOADS["qwen3_4b"].with_(name="bf16_two_mtiles", bs=200, gamma=2, V=3000, r=128,
                                                      d=64, seed=13),
+    # the tensor-core pass runs all positions in one persistent launch: the longest block the
+    # ABI allows (16 positions, 31 grid barriers) and a single position (no barrier between)
+    "bf16_gamma16": I.WORKLOADS["qwen3_4b"].with_(name="bf16_gamma16", bs=150, gamma=16, V=2600, d=64, seed=15),
+    "bf16_gamma1": I.WORKLOADS["qwen3_4b"].with_(name="bf16_gamma1", bs=33, gamma=1, V=1800, d=64, seed=16),
 }
 
 
