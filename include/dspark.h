@@ -93,7 +93,11 @@ DSPARK_API size_t dspark_workspace_bytes(int bs, int gamma, int V);
 DSPARK_API int dspark_workspace_init(void* ws, size_t ws_bytes, dspark_stream_t stream);
 
 /* Synchronise `stream`, return the status recorded by device-side checks since the last
- * read (DSPARK_OK if none) and clear it.  The only call that waits for the device. */
+ * read (DSPARK_OK if none) and clear it.  The only call that waits for the device.
+ * Diagnostics: when a device-side wait of a tensor-core kernel gives up (DSPARK_ETIMEOUT),
+ * the first such wait since dspark_workspace_init is recorded in the workspace's 32-bit words
+ * 4, 5, 6: the wait's site code, the CTA index and the site's progress counter (tile, box,
+ * position or barrier number).  They are not cleared by this call. */
 DSPARK_API int dspark_read_device_status(void* ws, dspark_stream_t stream);
 
 /* Diagnostics: deadline, in nanoseconds from a kernel's start, of every device-side wait in

@@ -151,9 +151,10 @@ int draft_positions(int dtype, const void* U, const void* W1, const void* W2t, c
   const float inv_tau = greedy ? 1.f : static_cast<float>(1.0 / static_cast<double>(temperature));
   const bool tc = draft_tc_supported(dtype, bs, V, r);
   uint32_t* ctl = reinterpret_cast<uint32_t*>(w + L.status + 64);
+  uint32_t* diag = reinterpret_cast<uint32_t*>(w + L.status + 16);
   if (tc && !states)  // the Markov head: every position in one persistent launch
     return launch_draft_tc(U, W1, W2t, nullptr, anchor, tokens, logit_x, lse, bs, gamma, V, r, 1, gamma, inv_tau,
-                           greedy, seed, step, stats, ctl, status, s) == cudaSuccess
+                           greedy, seed, step, stats, ctl, status, diag, s) == cudaSuccess
                ? DSPARK_OK
                : DSPARK_ECUDA;
   for (int k = 1; k <= gamma; ++k) {
@@ -162,7 +163,7 @@ int draft_positions(int dtype, const void* U, const void* W1, const void* W2t, c
     cudaError_t e;
     if (tc) {
       e = launch_draft_tc(U, W1, W2t, states, anchor, tokens, logit_x, lse, bs, gamma, V, r, k, k, inv_tau, greedy,
-                          seed, step, stats, ctl, status, s);
+                          seed, step, stats, ctl, status, diag, s);
     } else {
       const int n_slots = n_draft_chunks(V);  // the CUDA-core pass: one slot per draft chunk
       e = launch_draft_stats_simt(dtype, U, W1, W2t, states, anchor, tokens, bs, gamma, V, r, k, inv_tau, greedy,

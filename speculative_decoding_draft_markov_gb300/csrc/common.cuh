@@ -106,6 +106,17 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t code) {
   if (status) atomicCAS(status, 0u, code);
 }
 
+// A device-side wait that gave up: DSPARK_ETIMEOUT in the status word and, for the first one
+// since the record was cleared, where (diag[0] = the wait's site code, diag[1] = the CTA,
+// diag[2] = the site's progress counter: tile, position or barrier number).  diag may be null.
+__device__ __forceinline__ void note_timeout(uint32_t* status, uint32_t* diag, uint32_t site, uint32_t info) {
+  set_status(status, DSPARK_ETIMEOUT);
+  if (diag && atomicCAS(diag, 0u, site) == 0u) {
+    diag[1] = blockIdx.x;
+    diag[2] = info;
+  }
+}
+
 // Token ids read from device memory index weight rows: clamp into [0, V) so that bad data
 // can never address outside W1 (the kernels that own a status word also report it).
 __device__ __forceinline__ int clamp_token(int x, int V) { return x < 0 ? 0 : (x >= V ? V - 1 : x); }

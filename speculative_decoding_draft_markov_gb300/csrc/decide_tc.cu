@@ -98,6 +98,7 @@ struct Params {
   int n_chunks;
   uint64_t seed, step;
   uint32_t* status;
+  uint32_t* diag;  // where a wait gave up (note_timeout)
   uint64_t timeout_ns;
 };
 
@@ -200,11 +201,13 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
       int b_issued[kBStages];
       for (int s = 0; s < kBStages; ++s) b_issued[s] = -1;
       bool ok = true;
+      uint32_t fail_info = 0;
       for (int t = 0; t < n_tiles && ok; ++t) {
         const int n0 = (c0 + t * cstride) * kBN;
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->b_empty[bstage]), bph ^ 1, deadline, abort_flag)) {
             ok = false;
+            fail_info = uint32_t(t);
             break;
           }
           const uint32_t bfull = tc::smem_u32(&bar->b_full[bstage]);
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
       }
       if (!ok) {
         *abort_flag = 1;
-        set_status(p.status, DSPARK_ETIMEOUT);
+        note_timeout(p.status, p.diag, 11u, fail_info);
         // wait (bounded) for every copy this thread put in flight before the CTA exits
         const long long dl = tc::deadline_after_ns(200000000ull);
         const volatile int never = 0;
@@ -258,12 +261,15 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
       constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
       int bstage = 0, bph = 0;
       bool ok = tc::mbar_wait_bounded(tc::smem_u32(&bar->a_ready), 0, deadline, abort_flag);
+      uint32_t fail_site = 12u, fail_info = 0;
       bool issued = false;
       tc::tc_fence_after();
       for (int t = 0; t < n_tiles && ok; ++t) {
         const int ab = t & 1, ph = (t >> 1) & 1;  // accumulator buffer t % 2 and its phase
         if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_empty[ab]), ph ^ 1, deadline, abort_flag)) {
           ok = false;
+          fail_site = 13u;
+          fail_info = uint32_t(t);
           break;
         }
         tc::tc_fence_after();
@@ -271,6 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->b_full[bstage]), bph, deadline, abort_flag)) {
             ok = false;
+            fail_site = 14u;
+            fail_info = uint32_t(t) | (uint32_t(kb) << 24);
             break;
           }
           tc::tc_fence_after();
@@ -288,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
       }
       if (!ok) {
         *abort_flag = 1;
-        set_status(p.status, DSPARK_ETIMEOUT);
+        note_timeout(p.status, p.diag, fail_site, fail_info);
         if (issued) {  // wait (bounded) for the MMAs already issued before TMEM is freed
           tc::mma_commit(tc::smem_u32(&bar->drain));
           const volatile int never = 0;
@@ -308,9 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
     const int j = lane & 7, rsub = lane >> 3;  // 16-byte group in a 128-byte row, row within 4
     const uint32_t su = tc::smem_u32(sS + sl * kSlotBytes), st = su + kHalf;
     bool ok = true;
+    uint32_t fail_info = 0;
     for (int t = sl >> 1, i = 0; t < n_tiles; t += 2, ++i) {
       if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->s_empty[sl]), (i & 1) ^ 1, deadline, abort_flag)) {
         ok = false;
+        fail_info = uint32_t(t) | (uint32_t(sl) << 24);
         break;
       }
       const int col = (c0 + t * cstride) * kBN + h * 64 + j * 8;
@@ -343,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
     }
     if (!ok) {
       *abort_flag = 1;
-      set_status(p.status, DSPARK_ETIMEOUT);
+      if (lane == 0) note_timeout(p.status, p.diag, 15u, fail_info);
     }
   } else {
     // ------------------------------------------------------------------ epilogue
@@ -401,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) {
         *abort_flag = 1;
-        set_status(p.status, DSPARK_ETIMEOUT);
+        if (lane == 0) note_timeout(p.status, p.diag, 16u, uint32_t(t) | (uint32_t(warp) << 24));
         break;
       }
       tc::tc_fence_after();
@@ -413,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
         if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait_bounded(tc::smem_u32(&bar->s_full[sl]), i & 1, deadline,
                                                            abort_flag))) {
           *abort_flag = 1;
-          set_status(p.status, DSPARK_ETIMEOUT);
+          if (lane == 0) note_timeout(p.status, p.diag, 17u, uint32_t(t) | (uint32_t(sl) << 24));
           ok = false;
           break;
         }
@@ -530,6 +540,7 @@ cudaError_t launch_decision_stats_tc(const void* target, const void* U, const vo
   prm.seed = seed;
   prm.step = step;
   prm.status = status;
+  prm.diag = status ? status + 4 : nullptr;  // the workspace status block's words 4 .. 6
   prm.timeout_ns = g_wait_timeout_ns;
   const int grid = tch::vocab_grid(bs, n_chunks);
   prm.n_slots = grid / ((bs + kBM - 1) / kBM);

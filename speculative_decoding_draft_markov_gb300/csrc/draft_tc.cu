@@ -119,6 +119,7 @@ struct Params {
   int greedy;
   int n_tiles;      // 256-id vocabulary tiles
   uint32_t* status;
+  uint32_t* diag;   // where a wait gave up (note_timeout)
   uint32_t* ctl;    // grid barrier: ctl[0] arrivals, ctl[kCtlAbort] abort, ctl[kCtlExit] exits
   uint64_t timeout_ns;
   float4* entries;  // per (request, slot): DraftEntry
@@ -177,7 +178,7 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n
 // CTAs after it.  Returns false on give-up: the deadline, the CTA's own abort flag, or the
 // grid-wide abort word (which it then sets, so that the other CTAs stop waiting too).
 __device__ __noinline__ bool grid_arrive_wait(uint32_t* ctl, int idx, long long deadline, const volatile int* abort,
-                                              uint32_t* status) {
+                                              uint32_t* status, uint32_t* diag) {
   volatile uint32_t* gabort = ctl + kCtlAbort;
   if (*abort) {
     *gabort = 1u;
@@ -189,7 +190,7 @@ __device__ __noinline__ bool grid_arrive_wait(uint32_t* ctl, int idx, long long 
   while (ld_acquire_gpu(ctl) < target) {
     if (*gabort) return false;
     if (clock64() > deadline) {
-      set_status(status, DSPARK_ETIMEOUT);
+      note_timeout(status, diag, 8u, uint32_t(idx) | (ld_acquire_gpu(ctl) << 8));
       *gabort = 1u;
       __threadfence();
       return false;
@@ -202,9 +203,9 @@ __device__ __noinline__ bool grid_arrive_wait(uint32_t* ctl, int idx, long long 
 // the shared decision to stop (uniform across the epilogue warps: bar->bail is written only
 // between the two CTA barriers and read right after the second).
 __device__ __forceinline__ bool epi_grid_barrier(Barriers* bar, uint32_t* ctl, int idx, int et, long long deadline,
-                                                 uint32_t* status) {
+                                                 uint32_t* status, uint32_t* diag) {
   epi_sync();
-  if (et == 0) bar->bail = grid_arrive_wait(ctl, idx, deadline, &bar->abort, status) ? 0 : 1;
+  if (et == 0) bar->bail = grid_arrive_wait(ctl, idx, deadline, &bar->abort, status, diag) ? 0 : 1;
   epi_sync();
   return bar->bail != 0;
 }
@@ -299,11 +300,13 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
       int b_issued[kBStages];
       for (int s = 0; s < kBStages; ++s) b_issued[s] = -1;
       bool ok = true;
+      uint32_t fail_info = 0;
       for (int T = 0; T < npos * n_tiles && ok; ++T) {  // the same tiles at every position
         const int n0 = (c0 + (T % n_tiles) * cstride) * kBN;
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->b_empty[bstage]), bph ^ 1, deadline, abort_flag)) {
             ok = false;
+            fail_info = uint32_t(T);
             break;
           }
           const uint32_t bfull = tc::smem_u32(&bar->b_full[bstage]);
@@ -315,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
       }
       if (!ok) {
         *abort_flag = 1;
-        set_status(p.status, DSPARK_ETIMEOUT);
+        note_timeout(p.status, p.diag, 1u, fail_info);
         // wait (bounded) for every copy this thread put in flight before the CTA exits
         const long long dl = tc::deadline_after_ns(200000000ull);
         const volatile int never = 0;
@@ -332,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
       int u_issued[kUSlots];
       for (int j = 0; j < kUSlots; ++j) u_issued[j] = -1;
       bool ok = true;
+      uint32_t fail_info = 0;
       for (int T = 0; T < npos * n_tiles && ok; ++T) {  // tile T % n_tiles of position T / n_tiles
         const int n0 = (c0 + (T % n_tiles) * cstride) * kBN;
         const int k = p.k_first + T / n_tiles;
@@ -339,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
           const int q = kEpiSets * T + sb, j = q % kUSlots, ph = (q / kUSlots) & 1;
           if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->u_empty[j]), ph ^ 1, deadline, abort_flag)) {
             ok = false;
+            fail_info = uint32_t(q);
             break;
           }
           const uint32_t ufull = tc::smem_u32(&bar->u_full[j]);
@@ -349,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
       }
       if (!ok) {
         *abort_flag = 1;
-        set_status(p.status, DSPARK_ETIMEOUT);
+        note_timeout(p.status, p.diag, 2u, fail_info);
         const long long dl = tc::deadline_after_ns(200000000ull);
         const volatile int never = 0;
         for (int j = 0; j < kUSlots; ++j)
@@ -363,22 +368,29 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
       int bstage = 0, bph = 0;
       bool ok = true;
       bool issued = false;
+      uint32_t fail_site = 0, fail_info = 0;
       for (int T = 0; T < npos * n_tiles && ok; ++T) {
         // each position's A operand is written by the epilogue once it has read the previous
         // position's last accumulator (so every MMA that read the old A has completed)
         if (T % n_tiles == 0 &&
             !tc::mbar_wait_bounded(tc::smem_u32(&bar->a_ready), (T / n_tiles) & 1, deadline, abort_flag)) {
           ok = false;
+          fail_site = 3u;
+          fail_info = uint32_t(T);
           break;
         }
         if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->acc_empty), (T & 1) ^ 1, deadline, abort_flag)) {
           ok = false;
+          fail_site = 4u;
+          fail_info = uint32_t(T);
           break;
         }
         tc::tc_fence_after();
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait_bounded(tc::smem_u32(&bar->b_full[bstage]), bph, deadline, abort_flag)) {
             ok = false;
+            fail_site = 5u;
+            fail_info = uint32_t(T) | (uint32_t(kb) << 24);
             break;
           }
           tc::tc_fence_after();
@@ -396,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
       }
       if (!ok) {
         *abort_flag = 1;
-        set_status(p.status, DSPARK_ETIMEOUT);
+        note_timeout(p.status, p.diag, fail_site, fail_info);
         if (issued) {  // wait (bounded) for the MMAs already issued before TMEM is freed
           tc::mma_commit(tc::smem_u32(&bar->drain));
           const volatile int never = 0;
@@ -468,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) {
           *abort_flag = 1;
-          set_status(p.status, DSPARK_ETIMEOUT);
+          if (lane == 0) note_timeout(p.status, p.diag, 6u, uint32_t(T) | (uint32_t(warp) << 24));
           break;
         }
         tc::tc_fence_after();
@@ -479,12 +491,20 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bar->acc_empty));  // the next tile's MMAs may start
-        const int uq = kEpiSets * T + set, uj = uq % kUSlots;  // this set's U box of the tile
-        ok = __all_sync(0xFFFFFFFFu, tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[uj]), (uq / kUSlots) & 1,
-                                                           deadline, abort_flag));
+        // This set's U box of the tile: box uq, the un-th use of slot uj.  The slot's previous box
+        // (uq - kUSlots) belongs to another set, which may still be waiting for it or reading it:
+        // a parity wait on u_full alone could then see that older phase's parity and pass early.
+        // So first wait until the previous box has been consumed (u_empty, phase un - 1): u_full
+        // is then at most one phase behind, and its parity wait is unambiguous.  (The slot's box
+        // before that, uq - 2 kUSlots, is this set's own of three tiles back, long consumed.)
+        const int uq = kEpiSets * T + set, uj = uq % kUSlots, un = uq / kUSlots;
+        ok = (un == 0 || tc::mbar_wait_bounded(tc::smem_u32(&bar->u_empty[uj]), (un - 1) & 1, deadline,
+                                               abort_flag)) &&
+             tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[uj]), un & 1, deadline, abort_flag);
+        ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) {
           *abort_flag = 1;
-          set_status(p.status, DSPARK_ETIMEOUT);
+          if (lane == 0) note_timeout(p.status, p.diag, 7u, uint32_t(T) | (uint32_t(warp) << 24));
           break;
         }
         const uint8_t* ub = urow + uj * kUBox;
@@ -564,13 +584,13 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
         if (grow < bs) p.entries[size_t(grow) * p.n_slots + c0] = make_float4(l.m, l.s, a.v, __int_as_float(a.i));
       }
       // every CTA's entries of position k are written: the select of k, two requests at a time
-      if (epi_grid_barrier(bar, p.ctl, 2 * pi, et, deadline, p.status)) {
+      if (epi_grid_barrier(bar, p.ctl, 2 * pi, et, deadline, p.status, p.diag)) {
         *abort_flag = 1;
         break;
       }
       select_requests(p, k, et, &bar->sel[et >> 8]);
       // x_k of every request is written before any CTA gathers the next position's A rows
-      if (pi + 1 < npos && epi_grid_barrier(bar, p.ctl, 2 * pi + 1, et, deadline, p.status)) {
+      if (pi + 1 < npos && epi_grid_barrier(bar, p.ctl, 2 * pi + 1, et, deadline, p.status, p.diag)) {
         *abort_flag = 1;
         break;
       }
@@ -610,7 +630,7 @@ int draft_tc_slots(int bs, int V) {
 cudaError_t launch_draft_tc(const void* U, const void* W1, const void* W2t, const void* states, const int32_t* anchor,
                             int32_t* tokens, float* logit_x, float* lse, int bs, int gamma, int V, int r, int k_first,
                             int k_last, float inv_tau, int greedy, uint64_t seed, uint64_t step, void* entries,
-                            uint32_t* ctl, uint32_t* status, cudaStream_t s) {
+                            uint32_t* ctl, uint32_t* status, uint32_t* diag, cudaStream_t s) {
   if (!tch::encode_fn()) return cudaErrorNotSupported;
   if (k_first < 1 || k_last < k_first || k_last > gamma) return cudaErrorInvalidValue;
   CUtensorMap map_w2, map_u;
@@ -645,6 +665,7 @@ cudaError_t launch_draft_tc(const void* U, const void* W1, const void* W2t, cons
   prm.greedy = greedy;
   prm.n_tiles = n_tiles;
   prm.status = status;
+  prm.diag = diag;
   prm.ctl = ctl;
   prm.timeout_ns = g_wait_timeout_ns;
   prm.entries = static_cast<float4*>(entries);

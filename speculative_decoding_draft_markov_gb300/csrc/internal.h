@@ -18,11 +18,12 @@ cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, co
 // The tensor-core pass (tcgen05 + TMEM + TMA), bf16 only, positions k_first .. k_last in one
 // persistent cooperative launch that also runs each position's select (tokens, logit_x, lse
 // written): one entry slot per CTA column (draft_tc_slots(bs, V) of them).  ctl: the grid
-// barrier's words (the workspace status block + 64 bytes; 192 bytes, zero between calls).
+// barrier's words (the workspace status block + 64 bytes; 192 bytes, zero between calls);
+// diag: three words recording the first wait that gave up (note_timeout), or null.
 cudaError_t launch_draft_tc(const void* U, const void* W1, const void* W2t, const void* states, const int32_t* anchor,
                             int32_t* tokens, float* logit_x, float* lse, int bs, int gamma, int V, int r, int k_first,
                             int k_last, float inv_tau, int greedy, uint64_t seed, uint64_t step, void* entries,
-                            uint32_t* ctl, uint32_t* status, cudaStream_t s);
+                            uint32_t* ctl, uint32_t* status, uint32_t* diag, cudaStream_t s);
 bool draft_tc_supported(int dtype, int bs, int V, int r);
 // Slots (entries per request) the tensor-core pass writes: one per CTA column (at most one per
 // SM, and per 256-id vocabulary tile).
