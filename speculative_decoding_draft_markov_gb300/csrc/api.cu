@@ -138,7 +138,8 @@ namespace {
 
 // The gamma positions of a block draft, left to right: per position the RNN head's state update
 // (states non-null), the vocabulary pass (tensor cores or CUDA cores) and the select.  The
-// tensor-core pass runs the select itself, and for the Markov head all positions in one launch.
+// tensor-core pass runs every position in one launch, with the selects and, for the RNN head,
+// the state updates after the first inside it.
 int draft_positions(int dtype, const void* U, const void* W1, const void* W2t, const void* Wg, const float* bg,
                     void* states, const int32_t* anchor, int bs, int gamma, int V, int r, float temperature,
                     uint64_t seed, uint64_t step, int32_t* tokens, float* logit_x, float* lse, void* ws,
@@ -152,26 +153,21 @@ int draft_positions(int dtype, const void* U, const void* W1, const void* W2t, c
   const bool tc = draft_tc_supported(dtype, bs, V, r);
   uint32_t* ctl = reinterpret_cast<uint32_t*>(w + L.status + 64);
   uint32_t* diag = reinterpret_cast<uint32_t*>(w + L.status + 16);
-  if (tc && !states)  // the Markov head: every position in one persistent launch
-    return launch_draft_tc(U, W1, W2t, nullptr, anchor, tokens, logit_x, lse, bs, gamma, V, r, 1, gamma, inv_tau,
-                           greedy, seed, step, stats, ctl, status, diag, s) == cudaSuccess
+  if (tc)  // every position in one persistent launch, the RNN head's state updates inside it
+    return launch_draft_tc(U, W1, W2t, states, states ? Wg : nullptr, states ? bg : nullptr, anchor, tokens, logit_x,
+                           lse, bs, gamma, V, r, 1, gamma, inv_tau, greedy, seed, step, stats, ctl, status, diag,
+                           s) == cudaSuccess
                ? DSPARK_OK
                : DSPARK_ECUDA;
   for (int k = 1; k <= gamma; ++k) {
     if (states && launch_rnn_state(dtype, W1, Wg, bg, anchor, tokens, states, bs, gamma, V, r, k, s) != cudaSuccess)
       return DSPARK_ECUDA;
-    cudaError_t e;
-    if (tc) {
-      e = launch_draft_tc(U, W1, W2t, states, anchor, tokens, logit_x, lse, bs, gamma, V, r, k, k, inv_tau, greedy,
-                          seed, step, stats, ctl, status, diag, s);
-    } else {
-      const int n_slots = n_draft_chunks(V);  // the CUDA-core pass: one slot per draft chunk
-      e = launch_draft_stats_simt(dtype, U, W1, W2t, states, anchor, tokens, bs, gamma, V, r, k, inv_tau, greedy,
-                                  seed, step, stats, n_slots, s);
-      if (e == cudaSuccess)
-        e = launch_draft_select(dtype, stats, n_slots, U, W1, W2t, states, anchor, tokens, logit_x, lse, bs, gamma,
-                                V, r, k, inv_tau, greedy, seed, step, status, s);
-    }
+    const int n_slots = n_draft_chunks(V);  // the CUDA-core pass: one slot per draft chunk
+    cudaError_t e = launch_draft_stats_simt(dtype, U, W1, W2t, states, anchor, tokens, bs, gamma, V, r, k, inv_tau,
+                                            greedy, seed, step, stats, n_slots, s);
+    if (e == cudaSuccess)
+      e = launch_draft_select(dtype, stats, n_slots, U, W1, W2t, states, anchor, tokens, logit_x, lse, bs, gamma, V,
+                              r, k, inv_tau, greedy, seed, step, status, s);
     if (e != cudaSuccess) return DSPARK_ECUDA;
   }
   return DSPARK_OK;

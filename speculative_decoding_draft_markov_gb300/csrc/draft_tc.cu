@@ -8,8 +8,10 @@
 // partial draws (DraftEntry, common.cuh), which the select step (draft_select.cuh) merges into
 // x_k.  x_k is the next position's A row, so the positions run strictly left to right.
 //
-// One persistent launch runs positions k_first .. k_last (all gamma of them for the Markov head;
-// one at a time for the RNN head, whose state update runs between launches).  Between positions
+// One persistent launch runs positions k_first .. k_last (all gamma of them).  With the RNN
+// head, the epilogue first computes every request's first state s_1 (one more grid barrier), and
+// the group that draws x_k updates that request's recurrent state to s_{k+1} before the next
+// position.  Between positions
 // the CTAs meet at a grid barrier (a cooperative launch, so that every CTA is resident), run the
 // select of the requests assigned to them, and meet again before the next position's A gather.
 // Compared with a launch per pass this removes two kernel boundaries per position, and the TMA
@@ -110,6 +112,8 @@ struct Params {
   const __nv_bfloat16* W1;
   const __nv_bfloat16* W2t;
   const __nv_bfloat16* states;  // RNN head: the states s_k [bs, gamma, r] (A rows); else null
+  const __nv_bfloat16* Wg;      // RNN head: gate weights [2r, r]; the kernel updates the states
+  const float* bg;              // RNN head: gate bias [r]
   const int32_t* anchor;
   int32_t* tokens;
   float* logit_x;
@@ -213,14 +217,84 @@ __device__ __forceinline__ bool epi_grid_barrier(Barriers* bar, uint32_t* ctl, i
 // The select of position k for this CTA's requests: the epilogue's 512 threads (et) as two
 // groups of eight warps, group g taking requests blockIdx + (2 j + g) gridDim.  Out of line: its
 // registers are not added to the tile loop's.
+// RNN head, the state of position k + 1 of request b from the x_k just drawn, by the 256 threads
+// of a select group (gt = thread):
+//   g = sigmoid([e ; s_k] Wg + b_g),  e = W1[x_k],  s_{k+1} = g s_k + (1 - g) e,
+// in fp32, rounded to bf16 (nearest even).  Warp w of the group takes input rows
+// [w 2r / 8, (w + 1) 2r / 8) -- all of e (w < 4) or all of s_k -- and lane l the output columns
+// 8l .. 8l + 7 (16-byte loads of each Wg row), sixteen rows in flight at a time; the warps'
+// partial sums meet in the group's scratch in warp order, so the summation order is fixed.  s_k
+// comes from this kernel (or, for the first position, from the update kernel before it): plain
+// loads.
+template <typename P, typename GroupSync>
+__device__ __forceinline__ void rnn_next_state(const P& p, int b, int k, int gt, float* red, GroupSync group_sync) {
+  const int r = p.r, rows = r / 4;  // 2r / 8 input rows per warp
+  const int w = gt >> 5, lane = gt & 31;
+  // k = 0: the first state, from the anchor and s_0 = 0
+  const int x = clamp_token(k == 0 ? p.anchor[b] : p.tokens[size_t(b) * p.gamma + k - 1], p.V);
+  const __nv_bfloat16* sk = k == 0 ? nullptr : p.states + (size_t(b) * p.gamma + k - 1) * r;
+  const int j0 = w * rows;  // first input row of this warp
+  const __nv_bfloat16* in = j0 < r ? p.W1 + size_t(x) * r + j0 : sk + (j0 - r);
+  const bool on = lane * 8 < r;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int jb = 0; jb < rows && in != nullptr && !(k == 0 && j0 >= r); jb += 16) {  // rows: a multiple of 16
+    uint4 wq[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      wq[u] = on ? __ldg(reinterpret_cast<const uint4*>(p.Wg + size_t(j0 + jb + u) * r) + lane)
+                 : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 iq0 = *reinterpret_cast<const uint4*>(in + jb), iq1 = *reinterpret_cast<const uint4*>(in + jb + 8);
+    const float xin[16] = {bf16lo(iq0.x), bf16hi(iq0.x), bf16lo(iq0.y), bf16hi(iq0.y),
+                           bf16lo(iq0.z), bf16hi(iq0.z), bf16lo(iq0.w), bf16hi(iq0.w),
+                           bf16lo(iq1.x), bf16hi(iq1.x), bf16lo(iq1.y), bf16hi(iq1.y),
+                           bf16lo(iq1.z), bf16hi(iq1.z), bf16lo(iq1.w), bf16hi(iq1.w)};
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      acc[0] = fmaf(xin[u], bf16lo(wq[u].x), acc[0]); acc[1] = fmaf(xin[u], bf16hi(wq[u].x), acc[1]);
+      acc[2] = fmaf(xin[u], bf16lo(wq[u].y), acc[2]); acc[3] = fmaf(xin[u], bf16hi(wq[u].y), acc[3]);
+      acc[4] = fmaf(xin[u], bf16lo(wq[u].z), acc[4]); acc[5] = fmaf(xin[u], bf16hi(wq[u].z), acc[5]);
+      acc[6] = fmaf(xin[u], bf16lo(wq[u].w), acc[6]); acc[7] = fmaf(xin[u], bf16hi(wq[u].w), acc[7]);
+    }
+  }
+  for (int ww = 0; ww < 8; ++ww) {  // red[c] = sum over warps 0 .. 7 in order
+    if (w == ww && on) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) red[lane * 8 + c] = (ww == 0 ? 0.f : red[lane * 8 + c]) + acc[c];
+    }
+    group_sync();
+  }
+  if (gt < r) {
+    const float g = 1.f / (1.f + expf(-(p.bg[gt] + red[gt])));
+    const float ei = __bfloat162float(p.W1[size_t(x) * r + gt]);
+    const float si = k == 0 ? 0.f : __bfloat162float(sk[gt]);
+    const_cast<__nv_bfloat16*>(p.states)[(size_t(b) * p.gamma + k) * r + gt] =
+        __float2bfloat16_rn(g * si + (1.f - g) * ei);
+  }
+}
+
+// RNN head: the first state s_1 of this CTA's requests (blockIdx + (2 j + group) gridDim), before
+// the first position.  Out of line, like the select.
+template <typename P>
+__device__ __noinline__ void rnn_first_states(const P& p, int et, SelectScratch* sm) {
+  const int grp = et >> 8, gt = et & 255;
+  auto group_sync = [grp] { asm volatile("bar.sync %0, 256;" ::"r"(2 + grp) : "memory"); };
+  for (int b = blockIdx.x + grp * int(gridDim.x); b < p.bs; b += 2 * int(gridDim.x))
+    rnn_next_state(p, b, 0, gt, sm->a, group_sync);
+}
+
 template <typename P>
 __device__ __noinline__ void select_requests(const P& p, int k, int et, SelectScratch* sm) {
   const int grp = et >> 8, gt = et & 255;
-  for (int b = blockIdx.x + grp * int(gridDim.x); b < p.bs; b += 2 * int(gridDim.x))
+  auto group_sync = [grp] { asm volatile("bar.sync %0, 256;" ::"r"(2 + grp) : "memory"); };
+  for (int b = blockIdx.x + grp * int(gridDim.x); b < p.bs; b += 2 * int(gridDim.x)) {
     select_row<__nv_bfloat16, 8>(b, gt, p.entries, p.n_slots, p.U, p.W1, p.W2t, p.states, p.anchor, p.tokens,
                                  p.logit_x, p.lse, p.gamma, p.V, p.r, k, p.inv_tau, p.greedy, p.seed, p.step,
-                                 p.status, sm, [grp] { asm volatile("bar.sync %0, 256;" ::"r"(2 + grp) : "memory"); },
-                                 p.states == nullptr && k < p.k_last);
+                                 p.status, sm, group_sync, p.states == nullptr && k < p.k_last);
+    if (p.Wg && k < p.k_last) {  // the RNN head's next state, from the token just drawn
+      group_sync();              // x_k (written by the group's thread 0) is visible to the group
+      rnn_next_state(p, b, k, gt, sm->a, group_sync);
+    }
+  }
 }
 
 // Warp 1 at the end of the kernel: free the tensor memory.  An epilogue that gave up has not
@@ -433,8 +507,17 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     // x_0 (the anchors) and the first position's inputs come from earlier kernels: everything
     // above -- barrier set-up, TMEM, the producers' U / W2 prefetch -- overlapped with them
     tc::grid_dependency_wait();
-    int T = 0;  // tiles consumed so far, over all positions (accumulator / U ring phases)
-    for (int pi = 0; pi < npos; ++pi) {
+    int T = 0;     // tiles consumed so far, over all positions (accumulator / U ring phases)
+    int nbar = 0;  // grid barriers passed so far
+    bool stop = false;
+    if (p.Wg && p.k_first == 1) {  // RNN head: every request's first state before position 1
+      rnn_first_states(p, et, &bar->sel[et >> 8]);
+      if (epi_grid_barrier(bar, p.ctl, nbar++, et, deadline, p.status, p.diag)) {
+        *abort_flag = 1;
+        stop = true;
+      }
+    }
+    for (int pi = 0; pi < npos && !stop; ++pi) {
       const int k = p.k_first + pi;
       {
         // A operand into tensor memory: this row's W1[x_{k-1}] (Markov head) or s_k (RNN head)
@@ -584,13 +667,13 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
         if (grow < bs) p.entries[size_t(grow) * p.n_slots + c0] = make_float4(l.m, l.s, a.v, __int_as_float(a.i));
       }
       // every CTA's entries of position k are written: the select of k, two requests at a time
-      if (epi_grid_barrier(bar, p.ctl, 2 * pi, et, deadline, p.status, p.diag)) {
+      if (epi_grid_barrier(bar, p.ctl, nbar++, et, deadline, p.status, p.diag)) {
         *abort_flag = 1;
         break;
       }
       select_requests(p, k, et, &bar->sel[et >> 8]);
       // x_k of every request is written before any CTA gathers the next position's A rows
-      if (pi + 1 < npos && epi_grid_barrier(bar, p.ctl, 2 * pi + 1, et, deadline, p.status, p.diag)) {
+      if (pi + 1 < npos && epi_grid_barrier(bar, p.ctl, nbar++, et, deadline, p.status, p.diag)) {
         *abort_flag = 1;
         break;
       }
@@ -627,12 +710,14 @@ int draft_tc_slots(int bs, int V) {
   return tch::vocab_grid(bs, (V + kBN - 1) / kBN) / n_mt;
 }
 
-cudaError_t launch_draft_tc(const void* U, const void* W1, const void* W2t, const void* states, const int32_t* anchor,
+cudaError_t launch_draft_tc(const void* U, const void* W1, const void* W2t, const void* states, const void* Wg,
+                            const float* bg, const int32_t* anchor,
                             int32_t* tokens, float* logit_x, float* lse, int bs, int gamma, int V, int r, int k_first,
                             int k_last, float inv_tau, int greedy, uint64_t seed, uint64_t step, void* entries,
                             uint32_t* ctl, uint32_t* status, uint32_t* diag, cudaStream_t s) {
   if (!tch::encode_fn()) return cudaErrorNotSupported;
   if (k_first < 1 || k_last < k_first || k_last > gamma) return cudaErrorInvalidValue;
+  if ((Wg != nullptr) != (states != nullptr && bg != nullptr)) return cudaErrorInvalidValue;
   CUtensorMap map_w2, map_u;
   if (!tch::encode_bf16_2d(&map_w2, W2t, size_t(V), size_t(r), kBN)) return cudaErrorInvalidValue;
   {
@@ -655,6 +740,8 @@ cudaError_t launch_draft_tc(const void* U, const void* W1, const void* W2t, cons
   prm.W1 = static_cast<const __nv_bfloat16*>(W1);
   prm.W2t = static_cast<const __nv_bfloat16*>(W2t);
   prm.states = static_cast<const __nv_bfloat16*>(states);
+  prm.Wg = static_cast<const __nv_bfloat16*>(Wg);
+  prm.bg = bg;
   prm.anchor = anchor;
   prm.tokens = tokens;
   prm.logit_x = logit_x;

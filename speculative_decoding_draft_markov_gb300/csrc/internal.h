@@ -19,8 +19,11 @@ cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, co
 // persistent cooperative launch that also runs each position's select (tokens, logit_x, lse
 // written): one entry slot per CTA column (draft_tc_slots(bs, V) of them).  ctl: the grid
 // barrier's words (the workspace status block + 64 bytes; 192 bytes, zero between calls);
-// diag: three words recording the first wait that gave up (note_timeout), or null.
-cudaError_t launch_draft_tc(const void* U, const void* W1, const void* W2t, const void* states, const int32_t* anchor,
+// diag: three words recording the first wait that gave up (note_timeout), or null.  RNN head:
+// states, Wg, bg non-null; the kernel writes s_1 .. s_{k_last} when k_first = 1 (else
+// states[:, k_first - 1] must already hold s_{k_first}, and it writes the states after it).
+cudaError_t launch_draft_tc(const void* U, const void* W1, const void* W2t, const void* states, const void* Wg,
+                            const float* bg, const int32_t* anchor,
                             int32_t* tokens, float* logit_x, float* lse, int bs, int gamma, int V, int r, int k_first,
                             int k_last, float inv_tau, int greedy, uint64_t seed, uint64_t step, void* entries,
                             uint32_t* ctl, uint32_t* status, uint32_t* diag, cudaStream_t s);
