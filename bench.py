@@ -267,10 +267,11 @@ DRAFT_SOURCES = ["draft_tc.cu", "draft.cu", "draft_select.cuh", "common.cuh", "t
 VERIFY_SOURCES = ["verify.cu", "decide_tc.cu", "common.cuh", "tc_ptx.cuh", "tc_host.h"]
 
 
-def rooflines(wl, stage_ms, rows, tau, profile_key=None):
+def rooflines(wl, stage_ms, rows, tau, profile_key=None, conf_in_draft=False):
     hbm, bf16, peak_kind = _peaks()
     bs, gamma, V, r = wl.bs, wl.gamma, wl.V, wl.r
-    db = draft_bytes(bs, gamma, V, r)
+    # with the confidence head inside the draft's launch its h rows count with the draft's bytes
+    db = draft_bytes(bs, gamma, V, r) + (bs * gamma * wl.d * 2 if conf_in_draft else 0)
     dflop = draft_flops(bs, gamma, V, r)
     dsec = stage_ms["draft"] * 1e-3
     traffic = _profiled_traffic(f"draft_block_{profile_key}_dram") if profile_key else None
@@ -280,8 +281,10 @@ def rooflines(wl, stage_ms, rows, tau, profile_key=None):
     return {
         "bound": "hbm", "achieved": db / dsec / 1e9, "peak": hbm, "unit": "GB/s", "frac": db / dsec / 1e9 / hbm,
         "traffic": traffic, "traffic_over_algorithmic": (traffic / db) if traffic else None,
-        "kernel": "dspark_draft_block: one persistent cooperative draft_tc_kernel launch over all gamma positions "
-                  "(vocabulary passes + in-kernel selects); one C-ABI call, CUDA events around it in the timed steps",
+        "kernel": ("dspark_draft_confidence_block" if conf_in_draft else "dspark_draft_block")
+                  + ": one persistent cooperative draft_tc_kernel launch over all gamma positions (vocabulary "
+                  "passes + in-kernel selects" + (" + the confidence head" if conf_in_draft else "") +
+                  "); one C-ABI call, CUDA events around it in the timed steps",
         "algorithmic_bytes": db, "peak_kind": peak_kind,
         "tensor": {"achieved": dflop / dsec / 1e12, "peak": bf16, "unit": "TFLOP/s",
                    "frac": dflop / dsec / 1e12 / bf16, "flops": dflop},
@@ -335,7 +338,15 @@ class Path:
         self.fwd = S.gather_target_forward(self.inp["target"])
         self.ring = S.zos_ring(dev)
         self.vmode = B.DSPARK_COMPACT if mode == "compact" else B.DSPARK_STATIC
-        self.launches = (3 if rnn else 2) * wl.gamma + (2 if mode == "compact" else 1) + (4 if self.tau > 0 else 2)
+        # the Markov head's compact step computes the confidence inside the draft's launch
+        # (dspark_draft_confidence_block); the RNN head's step runs it as its own launch
+        self.fused = mode == "compact" and not rnn
+        tc = self.inp["U"].dtype == torch.bfloat16 and wl.r in (64, 128, 256)
+        draft_l = 1 if tc else (3 if rnn else 2) * wl.gamma
+        conf_l = 0 if (mode != "compact" or self.fused) else 1
+        # launches of one synchronous-scheduler step (the asynchronous one adds two: its
+        # select + pack in place of the fused schedule+pack, and the budget search)
+        self.launches = draft_l + conf_l + 1 + (4 if self.tau > 0 else 2)
 
     def draft(self, it):
         inp, buf = self.inp, self.buf
@@ -343,6 +354,11 @@ class Path:
             self.B.dspark_draft_block_rnn(inp["U"], inp["W1"], inp["W2t"], inp["Wg"], inp["bg"], inp["anchor"],
                                           self.tau, self.wl.seed, it, buf.tokens, buf.logit_x, buf.lse, self.states,
                                           buf.ws)
+            return
+        if self.fused:
+            self.B.dspark_draft_confidence_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], self.tau,
+                                                 self.wl.seed, it, buf.tokens, buf.logit_x, buf.lse, inp["h"],
+                                                 inp["w"], inp["b"], inp["sts_T"], buf.conf, buf.surv, buf.ws)
             return
         self.B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], self.tau, self.wl.seed, it,
                                   buf.tokens, buf.logit_x, buf.lse, buf.ws)
@@ -353,8 +369,9 @@ class Path:
             B.dspark_pack(None, inp["anchor"], buf.tokens, self.tiers, buf.cu, buf.ids, buf.req, buf.pos, buf.padded,
                           buf.ws)
             return
-        B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], buf.tokens, inp["w"], inp["b"], inp["sts_T"],
-                            buf.conf, buf.surv)
+        if not self.fused:
+            B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], buf.tokens, inp["w"], inp["b"], inp["sts_T"],
+                                buf.conf, buf.surv)
         if zos:
             B.dspark_schedule_zos_select(buf.surv, self.sps, self.ring, it, buf.window, buf.K, buf.ws)
             B.dspark_pack(buf.window, inp["anchor"], buf.tokens, self.tiers, buf.cu, buf.ids, buf.req, buf.pos,
@@ -528,7 +545,7 @@ def measure(path, steps, warmup, e2e_steps, profile_key=None, world=1):
     seg, tokens, rows, slots, t_host, clocks = time_steps(path, steps, warmup, world=world)
     step_ms = seg[:, 0] + seg[:, 1]
     (total_ms,), (tokens_all,) = aggregate_over_ranks([float(step_ms.sum())], [tokens], path.dev)
-    stage_ms = {"draft": float(seg[:, 2].mean()), "conf_sched_pack": float((seg[:, 0] - seg[:, 2]).mean()),
+    stage_ms = {"draft": float(seg[:, 2].mean()), "sched_pack": float((seg[:, 0] - seg[:, 2]).mean()),
                 "verify": float(seg[:, 1].mean())}
     e2e_v, bi, bo, e_steps, e_ms = time_e2e(path, e2e_steps)
     (e_ms_all,), (e2e_tok,) = aggregate_over_ranks([e_ms], [e2e_v * e_ms * 1e-3], path.dev)
@@ -540,7 +557,7 @@ def measure(path, steps, warmup, e2e_steps, profile_key=None, world=1):
         "tokens_per_step": tokens / steps, "packed_rows_per_step": rows / steps,
         "admitted_slots_per_step": slots / steps if path.mode == "compact" else wl.bs * wl.gamma,
         "stage_ms": stage_ms, "host_enqueue_ms_per_step": t_host * 1e3 / steps,
-        "roofline": rooflines(wl, stage_ms, rows / steps, path.tau, profile_key),
+        "roofline": rooflines(wl, stage_ms, rows / steps, path.tau, profile_key, conf_in_draft=path.fused),
         "e2e": {"value": e2e_tok / (e_ms_all * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "steps": e_steps},
         "gpu_launches": path.launches * steps, "clocks": clocks,
@@ -632,7 +649,7 @@ def run_ours(args, rank: int, world: int):
         "zos": {"value": ztokens / (ztotal_ms * 1e-3), "unit": "tokens/s", "ms_per_step": ztotal_ms / args.steps,
                 "tokens_per_step": ztokens / args.steps / world,
                 "stage_ms": {"draft": float(zseg[:, 2].mean()),
-                             "conf_sched_pack": float((zseg[:, 0] - zseg[:, 2]).mean()),
+                             "sched_pack": float((zseg[:, 0] - zseg[:, 2]).mean()),
                              "verify_with_budget": float(zseg[:, 1].mean())},
                 "scheduler": "asynchronous: budget from the survival two steps back (global search, second "
                              "stream beside the verify), radix top-K select on the step's path",

@@ -6,6 +6,7 @@
  *
  *   dspark_draft_block -> dspark_confidence -> dspark_schedule -> dspark_pack
  *       -> [the caller's target forward over the packed batch] -> dspark_verify
+ * (dspark_draft_confidence_block does the first two in one call).
  *
  * Sources, cited by page and section:
  *   [SUMMARY] "DSpark: Confidence-Scheduled Speculative Decoding with Semi-Autoregressive
@@ -156,6 +157,21 @@ DSPARK_API int dspark_draft_block(const void* U, const void* W1, const void* W2t
                        int32_t* tokens, float* logit_x, float* lse,
                        void* ws, size_t ws_bytes, dspark_stream_t stream);
 
+/* S1 and S2 in one call: the outputs of dspark_draft_block followed by dspark_confidence on the
+ * drafted tokens, bit for bit.  On the tensor-core pass (bf16, r = 64, 128 or 256) the confidence
+ * of position k is computed inside the draft's launch as soon as x_{k-1} is drawn, so it finishes
+ * under the draft's own time; otherwise the two run as their own launches.
+ *   draft arguments   as dspark_draft_block
+ *   h, d, w, b, sts_T, conf, surv, z_logit   as dspark_confidence (h in `dtype`)
+ * Limits and errors: those of both calls. */
+DSPARK_API int dspark_draft_confidence_block(const void* U, const void* W1, const void* W2t, int dtype,
+                       const int32_t* anchor, int bs, int gamma, int V, int r,
+                       float temperature, uint64_t seed, uint64_t step,
+                       int32_t* tokens, float* logit_x, float* lse,
+                       const void* h, int d, const float* w, float b, const float* sts_T,
+                       float* conf, float* surv, float* z_logit,
+                       void* ws, size_t ws_bytes, dspark_stream_t stream);
+
 /* S1 with the RNN sequential head ([SUMMARY] "Architecture (drafter)", RNN head: a gated
  * recurrent state s_k carried across the block, so each position sees the whole prefix).  The
  * pages give no equations; this library's reading, per request:
@@ -169,7 +185,8 @@ DSPARK_API int dspark_draft_block(const void* U, const void* W1, const void* W2t
  *   bg       device [r] fp32
  *   states   device [bs, gamma, r] (dtype) out: s_1 .. s_gamma (dspark_verify's draft_states)
  *   other arguments, limits and errors as dspark_draft_block.
- * One extra small launch per position (the state update: a [bs, 2r] x [2r, r] GEMM). */
+ * bf16 with r = 64, 128 or 256: the state updates run inside the draft's one launch; otherwise one
+ * extra small launch per position (the state update: a [bs, 2r] x [2r, r] GEMM). */
 DSPARK_API int dspark_draft_block_rnn(const void* U, const void* W1, const void* W2t, const void* Wg,
                                       const float* bg, int dtype, const int32_t* anchor, int bs, int gamma,
                                       int V, int r, float temperature, uint64_t seed, uint64_t step,

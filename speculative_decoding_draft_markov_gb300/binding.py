@@ -32,6 +32,8 @@ _SIGS = {
     "dspark_set_wait_timeout_ns": (_u64, [_u64]),
     "dspark_draft_block": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _u64, _u64,
                                 _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dspark_draft_confidence_block": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _u64, _u64,
+                                           _vp, _vp, _vp, _vp, _i, _vp, _f, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dspark_draft_block_noalloc": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _u64, _u64,
                                         _vp, _vp, _vp, _vp, _vp]),
     "dspark_draft_block_rnn": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _f, _u64, _u64,
@@ -178,6 +180,20 @@ def dspark_draft_block(U, W1, W2t, anchor, temperature, seed, step, tokens, logi
     _check(lib().dspark_draft_block(_p(U), _p(W1), _p(W2t), _dtype(U), _p(anchor), bs, gamma, V, r,
                                     float(temperature), int(seed), int(step), _p(tokens), _p(logit_x),
                                     _p(lse), _p(ws), ws.numel(), _stream(stream)), "dspark_draft_block")
+
+
+def dspark_draft_confidence_block(U, W1, W2t, anchor, temperature, seed, step, tokens, logit_x, lse, h, w, b, sts_T,
+                                  conf, surv, ws, stream=None, z_logit=None):
+    """dspark_draft_block then dspark_confidence on the drafted tokens, as one call (the confidence
+    computed inside the draft's launch on the tensor-core pass)."""
+    bs, gamma, V = U.shape
+    r = W1.shape[1]
+    d = h.shape[2]
+    _check(lib().dspark_draft_confidence_block(_p(U), _p(W1), _p(W2t), _dtype(U), _p(anchor), bs, gamma, V, r,
+                                               float(temperature), int(seed), int(step), _p(tokens), _p(logit_x),
+                                               _p(lse), _p(h), d, _p(w), float(b), _p(sts_T), _p(conf), _p(surv),
+                                               _p(z_logit), _p(ws), ws.numel(), _stream(stream)),
+           "dspark_draft_confidence_block")
 
 
 def dspark_draft_block_noalloc(U, W1, W2t, anchor, temperature, seed, step, tokens, logit_x, lse,

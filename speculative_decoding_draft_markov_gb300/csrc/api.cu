@@ -143,7 +143,7 @@ namespace {
 int draft_positions(int dtype, const void* U, const void* W1, const void* W2t, const void* Wg, const float* bg,
                     void* states, const int32_t* anchor, int bs, int gamma, int V, int r, float temperature,
                     uint64_t seed, uint64_t step, int32_t* tokens, float* logit_x, float* lse, void* ws,
-                    cudaStream_t s) {
+                    cudaStream_t s, const ConfArgs* cf = nullptr) {
   const WsLayout L = ws_layout(bs, gamma, V);
   char* w = static_cast<char*>(ws);
   void* stats = w + L.stats;
@@ -154,7 +154,7 @@ int draft_positions(int dtype, const void* U, const void* W1, const void* W2t, c
   uint32_t* ctl = reinterpret_cast<uint32_t*>(w + L.status + 64);
   uint32_t* diag = reinterpret_cast<uint32_t*>(w + L.status + 16);
   if (tc)  // every position in one persistent launch, the RNN head's state updates inside it
-    return launch_draft_tc(U, W1, W2t, states, states ? Wg : nullptr, states ? bg : nullptr, anchor, tokens, logit_x,
+    return launch_draft_tc(U, W1, W2t, states, states ? Wg : nullptr, states ? bg : nullptr, cf, anchor, tokens, logit_x,
                            lse, bs, gamma, V, r, 1, gamma, inv_tau, greedy, seed, step, stats, ctl, status, diag,
                            s) == cudaSuccess
                ? DSPARK_OK
@@ -170,6 +170,9 @@ int draft_positions(int dtype, const void* U, const void* W1, const void* W2t, c
                               r, k, inv_tau, greedy, seed, step, status, s);
     if (e != cudaSuccess) return DSPARK_ECUDA;
   }
+  if (cf && launch_confidence(dtype, cf->h, W1, anchor, tokens, cf->w, cf->b, cf->sts_T, bs, gamma, cf->d, r, V,
+                              cf->conf, cf->surv, cf->z_logit, s) != cudaSuccess)
+    return DSPARK_ECUDA;
   return DSPARK_OK;
 }
 
@@ -198,6 +201,24 @@ int dspark_draft_block(const void* U, const void* W1, const void* W2t, int dtype
   if (int e = check_ws(ws, ws_bytes, bs, gamma, V)) return e;
   return draft_positions(dtype, U, W1, W2t, nullptr, nullptr, nullptr, anchor, bs, gamma, V, r, temperature, seed,
                          step, tokens, logit_x, lse, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dspark_draft_confidence_block(const void* U, const void* W1, const void* W2t, int dtype, const int32_t* anchor,
+                                  int bs, int gamma, int V, int r, float temperature, uint64_t seed, uint64_t step,
+                                  int32_t* tokens, float* logit_x, float* lse, const void* h, int d, const float* w,
+                                  float b, const float* sts_T, float* conf, float* surv, float* z_logit, void* ws,
+                                  size_t ws_bytes, dspark_stream_t stream) {
+  if (int e = check_draft_args(U, W1, W2t, dtype, anchor, bs, gamma, V, r, temperature, tokens, logit_x, lse))
+    return e;
+  if (!h || !w || !sts_T || !conf || !surv || !std::isfinite(b)) return DSPARK_EINVAL;
+  if (d < 8 || d % 8 != 0) return DSPARK_EINVAL;
+  if (d > 65536) return DSPARK_EUNSUPPORTED;
+  if (!al(h, 16) || !al(w, 16) || !al(sts_T, 4) || !al(conf, 4) || !al(surv, 4) || !al(z_logit, 4))
+    return DSPARK_EINVAL;
+  if (int e = check_ws(ws, ws_bytes, bs, gamma, V)) return e;
+  const ConfArgs cf{h, w, b, sts_T, d, conf, surv, z_logit};
+  return draft_positions(dtype, U, W1, W2t, nullptr, nullptr, nullptr, anchor, bs, gamma, V, r, temperature, seed,
+                         step, tokens, logit_x, lse, ws, reinterpret_cast<cudaStream_t>(stream), &cf);
 }
 
 int dspark_draft_block_rnn(const void* U, const void* W1, const void* W2t, const void* Wg, const float* bg,

@@ -98,9 +98,10 @@ extern "C" DSPARK_API int dspark_draft_block_noalloc(
   const int greedy = temperature == 0.f;
   const float inv_tau = greedy ? 1.f : static_cast<float>(1.0 / static_cast<double>(temperature));
   if (tc)  // every position in one persistent launch (grid barrier words beside the status word)
-    return launch_draft_tc(U, W1, W2t, nullptr, nullptr, nullptr, anchor, tokens, logit_x, lse, bs, gamma, V, r, 1,
-                           gamma, inv_tau, greedy, seed, step, stats, reinterpret_cast<uint32_t*>(w + L.status + 64),
-                           status, reinterpret_cast<uint32_t*>(w + L.status + 16), s) ==
+    return launch_draft_tc(U, W1, W2t, nullptr, nullptr, nullptr, nullptr, anchor, tokens, logit_x, lse, bs, gamma, V,
+                           r, 1, gamma, inv_tau, greedy, seed, step, stats,
+                           reinterpret_cast<uint32_t*>(w + L.status + 64), status,
+                           reinterpret_cast<uint32_t*>(w + L.status + 16), s) ==
                    cudaSuccess
                ? DSPARK_OK
                : DSPARK_ECUDA;

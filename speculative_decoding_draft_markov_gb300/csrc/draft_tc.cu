@@ -56,6 +56,9 @@
 //               select merges one entry per CTA column.
 //   select    = the epilogue warps as two groups of eight, one request each (request
 //               blockIdx + (2 j + group) * gridDim)
+//   warp 19   = the confidence head when the call asks for it: position k's confidence and
+//               survival of the requests blockIdx + j gridDim, as soon as x_{k-1} is readable,
+//               so that it finishes under the draft's own time
 // Every mbarrier and grid-barrier wait is bounded (SM cycle-counter deadline + shared abort flag,
 // and a grid-wide abort word); on give-up the kernel records DSPARK_ETIMEOUT, waits (bounded) for
 // its own copies / MMAs in flight, frees TMEM and returns.  The grid barrier's words live in the
@@ -67,6 +70,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "confidence.cuh"
 #include "draft_select.cuh"
 #include "internal.h"
 #include "tc_host.h"
@@ -86,7 +90,8 @@ constexpr int kEpiSets = 4;                       // warp sets of four warps, on
 constexpr int kEpiWarps = 4 * kEpiSets;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kUWarp = 2 + kEpiWarps;             // warp 18: the U producer
-constexpr int kThreads = 32 * (3 + kEpiWarps);
+constexpr int kConfWarp = 3 + kEpiWarps;          // warp 19: the confidence head (when asked for)
+constexpr int kThreads = 32 * (4 + kEpiWarps);
 constexpr uint32_t kBStage = kBN * kBK * 2;       // 32 KB: W2t rows [256 x 64 K]
 constexpr uint32_t kUBox = kBM * 64 * 2;          // 16 KB: U [128 rows x 64 ids]
 constexpr uint32_t kTmemA = kBN;                  // A: columns 256 .. 256 + r / 2 - 1 (bf16 pairs)
@@ -104,6 +109,7 @@ struct Barriers {
   int abort;
   int mma_pending;   // the issuer's MMAs that nobody has waited for (set by the issuing thread)
   int bail;          // the epilogue's shared decision after a grid barrier (1: stop)
+  uint32_t tok_pos;  // positions whose x_{k-1} every CTA can read (release / acquire; conf warp)
   SelectScratch sel[2];  // the two select groups' scratch
 };
 
@@ -114,6 +120,14 @@ struct Params {
   const __nv_bfloat16* states;  // RNN head: the states s_k [bs, gamma, r] (A rows); else null
   const __nv_bfloat16* Wg;      // RNN head: gate weights [2r, r]; the kernel updates the states
   const float* bg;              // RNN head: gate bias [r]
+  const __nv_bfloat16* h;       // confidence head: h [bs, gamma, d], or null (no confidence here)
+  const float* wconf;           // [d + r]
+  const float* sts_T;           // [gamma]
+  float* conf;                  // [bs, gamma] out
+  float* surv;                  // [bs, gamma] out
+  float* z_logit;               // [bs, gamma] out or null
+  float bconf;
+  int d;
   const int32_t* anchor;
   int32_t* tokens;
   float* logit_x;
@@ -217,6 +231,56 @@ __device__ __forceinline__ bool epi_grid_barrier(Barriers* bar, uint32_t* ctl, i
 // The select of position k for this CTA's requests: the epilogue's 512 threads (et) as two
 // groups of eight warps, group g taking requests blockIdx + (2 j + g) gridDim.  Out of line: its
 // registers are not added to the tile loop's.
+__device__ __forceinline__ void st_release_cta(uint32_t* a, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(tc::smem_u32(a)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* a) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(tc::smem_u32(a)) : "memory");
+  return v;
+}
+
+// The confidence head, computed by one warp of each CTA while the draft runs: for position k
+// (once every CTA can read x_{k-1}) and the requests blockIdx + j gridDim, the logit
+// z = w [h_k ; W1[x_{k-1}]] + b in the confidence kernel's order (confidence.cuh), then
+// c = sigmoid(z / T_k) and the survival a_k = a_{k-1} c -- the same bits as dspark_confidence.
+// tok_pos (set by the epilogue after each position's tokens are visible grid-wide) counts the
+// positions whose feature rows are ready.  Returns false if a wait gave up.
+template <typename P>
+__device__ __noinline__ bool confidence_warp(const P& p, const uint32_t* tok_pos, int npos, long long deadline,
+                                             const volatile int* abort, int lane) {
+  const int parts = conf_parts(p.gamma);
+  for (int pi = 0; pi < npos; ++pi) {
+    const int k = p.k_first + pi;
+    while (ld_acquire_cta(tok_pos) <= uint32_t(pi)) {
+      if (*abort) return false;
+      if (clock64() > deadline) {
+        if (lane == 0) note_timeout(p.status, p.diag, 9u, uint32_t(k));
+        return false;
+      }
+      __nanosleep(256);
+    }
+    for (int b = blockIdx.x; b < p.bs; b += gridDim.x) {
+      const int xp = clamp_token(k == 1 ? p.anchor[b] : p.tokens[size_t(b) * p.gamma + k - 2], p.V);
+      const __nv_bfloat16* hr = p.h + (size_t(b) * p.gamma + k - 1) * p.d;
+      const __nv_bfloat16* w1row = p.W1 + size_t(xp) * p.r;
+      float z = warp_sum(conf_part<__nv_bfloat16>(hr, w1row, p.wconf, p.d, p.r, 0, parts, lane));
+      for (int q = 1; q < parts; ++q) z += warp_sum(conf_part<__nv_bfloat16>(hr, w1row, p.wconf, p.d, p.r, q, parts, lane));
+      z += p.bconf;
+      if (lane == 0) {
+        const size_t o = size_t(b) * p.gamma + k - 1;
+        if (p.z_logit) p.z_logit[o] = z;
+        const float c = 1.f / (1.f + expf(-z / p.sts_T[k - 1]));
+        const float a = (k == 1 ? 1.f : p.surv[o - 1]) * c;
+        p.conf[o] = c;
+        p.surv[o] = a;
+      }
+      __syncwarp();
+    }
+  }
+  return true;
+}
+
 // RNN head, the state of position k + 1 of request b from the x_k just drawn, by the 256 threads
 // of a select group (gt = thread):
 //   g = sigmoid([e ; s_k] Wg + b_g),  e = W1[x_k],  s_{k+1} = g s_k + (1 - g) e,
@@ -350,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     bar->abort = 0;
     bar->mma_pending = 0;
     bar->bail = 0;
+    bar->tok_pos = 0u;
     tc::fence_mbar_init();
     tc::prefetch_tensormap(&tmap_w2);
     tc::prefetch_tensormap(&tmap_u);
@@ -435,6 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
           if (u_issued[j] >= 0) tc::mbar_wait_bounded(tc::smem_u32(&bar->u_full[j]), u_issued[j], dl, &never);
       }
     }
+  } else if (warp == kConfWarp) {
+    // ------------------------------------------------------------------ confidence head
+    if (p.h && !confidence_warp(p, &bar->tok_pos, npos, deadline, abort_flag, lane)) *abort_flag = 1;
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -507,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
     // x_0 (the anchors) and the first position's inputs come from earlier kernels: everything
     // above -- barrier set-up, TMEM, the producers' U / W2 prefetch -- overlapped with them
     tc::grid_dependency_wait();
+    if (et == 0) st_release_cta(&bar->tok_pos, 1u);  // x_0 (the anchors) are readable
     int T = 0;     // tiles consumed so far, over all positions (accumulator / U ring phases)
     int nbar = 0;  // grid barriers passed so far
     bool stop = false;
@@ -677,6 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_tc_kernel(const __grid_cons
         *abort_flag = 1;
         break;
       }
+      if (et == 0) st_release_cta(&bar->tok_pos, uint32_t(pi + 2));  // x_k is readable grid-wide
     }
   }
 
@@ -711,13 +781,14 @@ int draft_tc_slots(int bs, int V) {
 }
 
 cudaError_t launch_draft_tc(const void* U, const void* W1, const void* W2t, const void* states, const void* Wg,
-                            const float* bg, const int32_t* anchor,
+                            const float* bg, const ConfArgs* cf, const int32_t* anchor,
                             int32_t* tokens, float* logit_x, float* lse, int bs, int gamma, int V, int r, int k_first,
                             int k_last, float inv_tau, int greedy, uint64_t seed, uint64_t step, void* entries,
                             uint32_t* ctl, uint32_t* status, uint32_t* diag, cudaStream_t s) {
   if (!tch::encode_fn()) return cudaErrorNotSupported;
   if (k_first < 1 || k_last < k_first || k_last > gamma) return cudaErrorInvalidValue;
   if ((Wg != nullptr) != (states != nullptr && bg != nullptr)) return cudaErrorInvalidValue;
+  if (cf && (k_first != 1 || k_last != gamma || !cf->h)) return cudaErrorInvalidValue;
   CUtensorMap map_w2, map_u;
   if (!tch::encode_bf16_2d(&map_w2, W2t, size_t(V), size_t(r), kBN)) return cudaErrorInvalidValue;
   {
@@ -742,6 +813,16 @@ cudaError_t launch_draft_tc(const void* U, const void* W1, const void* W2t, cons
   prm.states = static_cast<const __nv_bfloat16*>(states);
   prm.Wg = static_cast<const __nv_bfloat16*>(Wg);
   prm.bg = bg;
+  if (cf) {
+    prm.h = static_cast<const __nv_bfloat16*>(cf->h);
+    prm.wconf = cf->w;
+    prm.sts_T = cf->sts_T;
+    prm.conf = cf->conf;
+    prm.surv = cf->surv;
+    prm.z_logit = cf->z_logit;
+    prm.bconf = cf->b;
+    prm.d = cf->d;
+  }
   prm.anchor = anchor;
   prm.tokens = tokens;
   prm.logit_x = logit_x;

@@ -22,8 +22,19 @@ cudaError_t launch_draft_stats_simt(int dtype, const void* U, const void* W1, co
 // diag: three words recording the first wait that gave up (note_timeout), or null.  RNN head:
 // states, Wg, bg non-null; the kernel writes s_1 .. s_{k_last} when k_first = 1 (else
 // states[:, k_first - 1] must already hold s_{k_first}, and it writes the states after it).
+// cf: the confidence head to compute while drafting (bf16, k_first = 1), or null.
+struct ConfArgs {  // the confidence head's inputs and outputs, as dspark_confidence takes them
+  const void* h;
+  const float* w;
+  float b;
+  const float* sts_T;
+  int d;
+  float* conf;
+  float* surv;
+  float* z_logit;
+};
 cudaError_t launch_draft_tc(const void* U, const void* W1, const void* W2t, const void* states, const void* Wg,
-                            const float* bg, const int32_t* anchor,
+                            const float* bg, const ConfArgs* cf, const int32_t* anchor,
                             int32_t* tokens, float* logit_x, float* lse, int bs, int gamma, int V, int r, int k_first,
                             int k_last, float inv_tau, int greedy, uint64_t seed, uint64_t step, void* entries,
                             uint32_t* ctl, uint32_t* status, uint32_t* diag, cudaStream_t s);

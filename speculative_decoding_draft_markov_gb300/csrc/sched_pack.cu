@@ -3,6 +3,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "confidence.cuh"
 #include "internal.h"
 #include "pdl.h"
 
@@ -14,51 +15,9 @@ namespace dspark {
 // temperature scaling divides the logit by T_k; prefix survival is the running product.
 // fp32 dot products in a fixed order.
 // ---------------------------------------------------------------------------------------
-// One 8-element group of a feature row: loaded as 16 bytes of bf16 (or two 16-byte halves of
-// fp32), then dotted with w read from memory at the time of use.
-template <typename T>
-__device__ __forceinline__ void load_hgroup(const T* x, uint4* q) {
-  if constexpr (sizeof(T) == 2) {
-    q[0] = *reinterpret_cast<const uint4*>(x);
-  } else {
-    q[0] = *reinterpret_cast<const uint4*>(x);
-    q[1] = *reinterpret_cast<const uint4*>(x + 4);
-  }
-}
-template <typename T>
-__device__ __forceinline__ float dot_hgroup(const uint4* q, const float* __restrict__ w) {
-  const float4 w0 = __ldg(reinterpret_cast<const float4*>(w));
-  const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + 4));
-  if constexpr (sizeof(T) == 2) {
-    float a = bf16lo(q[0].x) * w0.x;
-    a = fmaf(bf16hi(q[0].x), w0.y, a);
-    a = fmaf(bf16lo(q[0].y), w0.z, a);
-    a = fmaf(bf16hi(q[0].y), w0.w, a);
-    a = fmaf(bf16lo(q[0].z), w1.x, a);
-    a = fmaf(bf16hi(q[0].z), w1.y, a);
-    a = fmaf(bf16lo(q[0].w), w1.z, a);
-    a = fmaf(bf16hi(q[0].w), w1.w, a);
-    return a;
-  } else {
-    float a = __uint_as_float(q[0].x) * w0.x;
-    a = fmaf(__uint_as_float(q[0].y), w0.y, a);
-    a = fmaf(__uint_as_float(q[0].z), w0.z, a);
-    a = fmaf(__uint_as_float(q[0].w), w0.w, a);
-    a = fmaf(__uint_as_float(q[1].x), w1.x, a);
-    a = fmaf(__uint_as_float(q[1].y), w1.y, a);
-    a = fmaf(__uint_as_float(q[1].z), w1.z, a);
-    a = fmaf(__uint_as_float(q[1].w), w1.w, a);
-    return a;
-  }
-}
-
-// One block per request; `parts` warps per position split the d-long dot product: warp q of a
-// position takes the 256-element groups q, q + parts, ...  A lane issues the h loads of up to
-// kHLoads groups at once (one memory round trip for d <= 256 parts kHLoads) and reads w when it
-// uses it (every warp of the block reads the same w).  Thread 0 then adds the parts in order
-// and runs the sigmoid / STS / product chain.
-constexpr int kHLoads = 8;
-
+// One block per request; conf_parts(gamma) warps per position split the logit (confidence.cuh:
+// conf_part, the order shared with the persistent draft kernel).  Thread 0 then adds the parts in
+// order and runs the sigmoid / STS / product chain.
 template <typename T>
 __global__ void __launch_bounds__(512) confidence_kernel(
     const T* __restrict__ h, const T* __restrict__ W1, const int32_t* __restrict__ anchor,
@@ -71,32 +30,10 @@ __global__ void __launch_bounds__(512) confidence_kernel(
   const int pos = warp / parts, part = warp - pos * parts;
   if (pos < gamma) {
     const int k = pos + 1;
-    // the W1[x_{k-1}] part of the feature (r a multiple of 8, <= 256): its row is read first,
-    // so that its two round trips (token id, then row) overlap the h loads below
-    const bool has_w1 = part == 0 && lane * 8 < r;
-    uint4 qa[sizeof(T) == 4 ? 2 : 1];
-    if (has_w1) {
-      const int xp = clamp_token((k == 1) ? anchor[req] : tokens[size_t(req) * gamma + k - 2], V);
-      load_hgroup<T>(W1 + size_t(xp) * r + lane * 8, qa);
-    }
-    const T* hr = h + (size_t(req) * gamma + pos) * d;
-    const int stride = parts * 256;
-    float acc = 0.f;
-    for (int e0 = part * 256 + lane * 8; e0 < d; e0 += kHLoads * stride) {
-      uint4 q[kHLoads][sizeof(T) == 4 ? 2 : 1];
-#pragma unroll
-      for (int u = 0; u < kHLoads; ++u) {
-        const int e = e0 + u * stride;
-        if (e < d) load_hgroup<T>(hr + e, q[u]);
-      }
-#pragma unroll
-      for (int u = 0; u < kHLoads; ++u) {
-        const int e = e0 + u * stride;
-        if (e < d) acc += dot_hgroup<T>(q[u], w + e);
-      }
-    }
-    if (has_w1) acc += dot_hgroup<T>(qa, w + d + lane * 8);
-    acc = warp_sum(acc);
+    const T* w1row = nullptr;
+    if (part == 0 && lane * 8 < r)
+      w1row = W1 + size_t(clamp_token((k == 1) ? anchor[req] : tokens[size_t(req) * gamma + k - 2], V)) * r;
+    const float acc = warp_sum(conf_part<T>(h + (size_t(req) * gamma + pos) * d, w1row, w, d, r, part, parts, lane));
     if (lane == 0) zp[pos * 4 + part] = acc;
   }
   __syncthreads();
@@ -119,7 +56,7 @@ cudaError_t launch_confidence(int dtype, const void* h, const void* W1, const in
                               const int32_t* tokens, const float* w, float b, const float* sts_T,
                               int bs, int gamma, int d, int r, int V, float* conf, float* surv,
                               float* z_out, cudaStream_t s) {
-  const int parts = gamma <= 8 ? 2 : 1;  // warps per position: at most 512 threads, two blocks per SM
+  const int parts = conf_parts(gamma);  // warps per position: at most 512 threads, two blocks per SM
   const int threads = 32 * parts * gamma;
   if (dtype == DSPARK_F32)
     return launch_pdl(confidence_kernel<float>, dim3(bs), dim3(threads), 0, s, (const float*)h, (const float*)W1,

@@ -120,14 +120,16 @@ def draft_and_schedule(inp: dict, buf: StepBuffers, sps, temperature: float, see
     is the asynchronous one: the windows take the budget recorded two steps back
     (schedule_budget records this step's).  STATIC verification tests the whole block, so it
     needs no windows: the draft is packed as it is, without confidence or scheduler."""
-    B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], temperature, seed, step,
-                         buf.tokens, buf.logit_x, buf.lse, buf.ws, stream)
     if mode == B.DSPARK_STATIC and ring is None:
+        B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], temperature, seed, step,
+                             buf.tokens, buf.logit_x, buf.lse, buf.ws, stream)
         B.dspark_pack(None, inp["anchor"], buf.tokens, tiers, buf.cu, buf.ids, buf.req, buf.pos, buf.padded,
                       buf.ws, stream)
         return
-    B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], buf.tokens, inp["w"], inp["b"], inp["sts_T"],
-                        buf.conf, buf.surv, stream)
+    # the draft and the confidence head in one call (one launch on the tensor-core pass)
+    B.dspark_draft_confidence_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], temperature, seed, step,
+                                    buf.tokens, buf.logit_x, buf.lse, inp["h"], inp["w"], inp["b"], inp["sts_T"],
+                                    buf.conf, buf.surv, buf.ws, stream)
     if ring is None and mode == B.DSPARK_COMPACT:  # the windows are the packing: one launch for both
         B.dspark_schedule_pack(buf.surv, sps, sched_mode, buf.window, buf.K, buf.theta, inp["anchor"], buf.tokens,
                                tiers, buf.cu, buf.ids, buf.req, buf.pos, buf.padded, buf.ws, stream)

@@ -82,6 +82,27 @@ def test_draft_host_validation(L):
     assert _draft(L, ws_bytes=16) == B.DSPARK_EWORKSPACE
 
 
+def _draft_conf(L, **kw):
+    a = dict(U=FAKE, W1=FAKE, W2t=FAKE, dtype=1, anchor=FAKE, bs=4, gamma=7, V=1024, r=32,
+             temperature=1.0, seed=0, step=0, tokens=FAKE, logit_x=FAKE, lse=FAKE, h=FAKE, d=64, w=FAKE, b=0.0,
+             sts_T=FAKE, conf=FAKE, surv=FAKE, z_logit=None, ws=FAKE, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return L.dspark_draft_confidence_block(*a.values())
+
+
+def test_draft_confidence_host_validation(L):
+    """The fused call checks both calls' arguments before anything runs."""
+    assert _draft_conf(L, U=None) == B.DSPARK_EINVAL
+    assert _draft_conf(L, gamma=17) == B.DSPARK_EUNSUPPORTED
+    assert _draft_conf(L, h=None) == B.DSPARK_EINVAL
+    assert _draft_conf(L, surv=None) == B.DSPARK_EINVAL
+    assert _draft_conf(L, d=60) == B.DSPARK_EINVAL
+    assert _draft_conf(L, d=1 << 17) == B.DSPARK_EUNSUPPORTED
+    assert _draft_conf(L, b=float("inf")) == B.DSPARK_EINVAL
+    assert _draft_conf(L, z_logit=FAKE + 2) == B.DSPARK_EINVAL
+    assert _draft_conf(L, ws=None) == B.DSPARK_EWORKSPACE
+
+
 def test_other_entry_points_host_validation(L):
     f = FAKE
     # confidence: d not a multiple of 8

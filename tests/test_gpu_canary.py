@@ -61,6 +61,14 @@ def test_step_entry_points_keep_their_bounds(shape):
     B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], tok.t, inp["w"], inp["b"], inp["sts_T"], conf.t, surv.t,
                         z_logit=z.t)
     _check(conf, surv, z)
+    # the fused draft + confidence call, into fresh guarded outputs
+    f_out = [Guarded((bs, gamma), t) for t in (torch.int32, torch.float32, torch.float32, torch.float32,
+                                                 torch.float32, torch.float32)]
+    B.dspark_draft_confidence_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], 1.0, 3, 4, f_out[0].t, f_out[1].t,
+                                    f_out[2].t, inp["h"], inp["w"], inp["b"], inp["sts_T"], f_out[3].t, f_out[4].t,
+                                    ws.t, z_logit=f_out[5].t)
+    _check(ws, *f_out)
+    assert B.dspark_read_device_status(ws.t) == B.DSPARK_OK
     sps = S.sps_table(inp["T_raw"], inp["tiers"], dev)
     win, K, th = Guarded((bs,), torch.int32), Guarded((1,), torch.int32), Guarded((1,), torch.float64)
     B.dspark_schedule(surv.t, sps, B.DSPARK_SCHED_GLOBAL_ARGMAX, win.t, K.t, th.t, ws.t)

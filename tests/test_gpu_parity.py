@@ -63,6 +63,34 @@ def test_draft_parity_small(name, temperature):
         assert checked >= wl.bs * wl.gamma - near * wl.gamma and near <= 1
 
 
+@pytest.mark.parametrize("name", ["tiny_fp32", "bf16_ragged", "bf16_r32_simt", "bf16_two_mtiles", "bf16_gamma16",
+                                  "mixed_bs256"])
+@pytest.mark.parametrize("temperature", [1.0, 0.0])
+def test_draft_confidence_block_equals_the_two_calls(name, temperature):
+    """dspark_draft_confidence_block = dspark_draft_block then dspark_confidence, bit for bit: on the
+    tensor-core pass the confidence head runs inside the draft's launch (a warp of each CTA, in the
+    confidence kernel's summation order), on the CUDA-core pass as its own launch."""
+    wl = I.WORKLOADS["mixed_bs256"] if name == "mixed_bs256" else SMALL[name]
+    inp = I.make_device_inputs(wl, "cuda", with_target=False)
+    bs, gamma, V = wl.bs, wl.gamma, wl.V
+
+    def outs():
+        return ([torch.zeros((bs, gamma), dtype=torch.int32, device="cuda")] +
+                [torch.zeros((bs, gamma), dtype=torch.float32, device="cuda") for _ in range(5)])
+
+    ws = B.alloc_workspace(bs, gamma, V)
+    a = outs()
+    B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], temperature, wl.seed, 6, a[0], a[1], a[2], ws)
+    B.dspark_confidence(inp["h"], inp["W1"], inp["anchor"], a[0], inp["w"], inp["b"], inp["sts_T"], a[3], a[4],
+                        z_logit=a[5])
+    f = outs()
+    B.dspark_draft_confidence_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], temperature, wl.seed, 6, f[0], f[1],
+                                    f[2], inp["h"], inp["w"], inp["b"], inp["sts_T"], f[3], f[4], ws, z_logit=f[5])
+    assert B.dspark_read_device_status(ws) == B.DSPARK_OK
+    for x, y, what in zip(a, f, ["tokens", "logit_x", "lse", "conf", "surv", "z"]):
+        assert torch.equal(x, y), what
+
+
 def test_draft_parity_full_size_sampled_rows():
     wl = I.WORKLOADS["mixed_bs256"]
     inp = I.make_device_inputs(wl, "cuda", with_target=False, with_hidden=False)
