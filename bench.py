@@ -263,7 +263,7 @@ def _profiled_traffic(name: str):
     return d.get("dram_bytes_per_call")
 
 
-DRAFT_SOURCES = ["draft_tc.cu", "draft.cu", "draft_select.cuh", "common.cuh", "tc_ptx.cuh", "tc_host.h"]
+DRAFT_SOURCES = ["draft_tc.cu", "draft.cu", "draft_select.cuh", "confidence.cuh", "common.cuh", "tc_ptx.cuh", "tc_host.h"]
 VERIFY_SOURCES = ["verify.cu", "decide_tc.cu", "common.cuh", "tc_ptx.cuh", "tc_host.h"]
 
 
@@ -274,7 +274,8 @@ def rooflines(wl, stage_ms, rows, tau, profile_key=None, conf_in_draft=False):
     db = draft_bytes(bs, gamma, V, r) + (bs * gamma * wl.d * 2 if conf_in_draft else 0)
     dflop = draft_flops(bs, gamma, V, r)
     dsec = stage_ms["draft"] * 1e-3
-    traffic = _profiled_traffic(f"draft_block_{profile_key}_dram") if profile_key else None
+    traffic = (_profiled_traffic(f"{'draft_confidence_block' if conf_in_draft else 'draft_block'}_{profile_key}_dram")
+               if profile_key else None)
     vb = verify_bytes(rows, bs, V, r, tau == 0.0)
     vsec = stage_ms["verify"] * 1e-3
     vtraffic = _profiled_traffic(f"verify_{profile_key}_dram") if profile_key else None
@@ -786,8 +787,7 @@ def run_profile_case(args):
         return
     if args.profile_case == "schedule":
         wl = I.WORKLOADS[WORKLOAD]
-    inp = I.make_device_inputs(wl, dev, with_hidden=args.profile_case != "draft",
-                               with_target=args.profile_case not in ("draft", "schedule"))
+    inp = I.make_device_inputs(wl, dev, with_target=args.profile_case not in ("draft", "schedule"))
     bs, gamma, V = wl.bs, wl.gamma, wl.V
     cap = bs * (gamma + 1)
     buf = S.StepBuffers.allocate(bs, gamma, V, cap, inp["U"].dtype, dev)
@@ -806,9 +806,11 @@ def run_profile_case(args):
             B.dspark_schedule(buf.surv, sps, SCHED, buf.window, buf.K, buf.theta, buf.ws)
             B.dspark_schedule_zos_select(buf.surv, sps, ring, it, buf.window, buf.K, buf.ws)
     elif args.profile_case == "draft":
+        # the benchmark's draft stage: the draft and the confidence head in one call
         def run(it):
-            B.dspark_draft_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], wl.temperature, wl.seed, it,
-                                 buf.tokens, buf.logit_x, buf.lse, buf.ws)
+            B.dspark_draft_confidence_block(inp["U"], inp["W1"], inp["W2t"], inp["anchor"], wl.temperature, wl.seed,
+                                            it, buf.tokens, buf.logit_x, buf.lse, inp["h"], inp["w"], inp["b"],
+                                            inp["sts_T"], buf.conf, buf.surv, buf.ws)
     else:
         # the benchmark's own packing: its cost table and graph tiers, the global scheduler
         cap = max(cap, int(inp["tiers"][-1]))
