@@ -6,11 +6,12 @@
 // linear projection of [h_k ; W1[x_{k-1}]] followed by a sigmoid; sequential temperature
 // scaling divides the logit by T_k; prefix survival is the running product.
 //
-// Fixed order: the d-long h part is split over `parts` warps (part q takes the 256-element
-// groups q, q + parts, ...; lane l the 8 elements 8l .. 8l + 7 of each group, kConfLoads groups'
-// loads in flight at once); part 0 adds the W1[x_{k-1}] part (lane l: elements 8l .. 8l + 7)
-// last; each part is reduced over its warp by the xor-shuffle tree, the parts are added in order,
-// then the bias.
+// Fixed order: z = ((H_0 + H_1 + ... + H_{parts-1}) + X) + b, where H_q is part q of the d-long
+// h term (part q takes the 256-element groups q, q + parts, ...; lane l the 8 elements
+// 8l .. 8l + 7 of each group, kConfLoads groups' loads in flight at once) and X the r-long
+// W1[x_{k-1}] term (lane l: elements 8l .. 8l + 7), each reduced over its warp by the
+// xor-shuffle tree.  The h terms do not depend on the drafted tokens, so the persistent draft
+// kernel computes them ahead, while x_{k-1} is still being drawn.
 #pragma once
 
 #include "common.cuh"
@@ -60,15 +61,11 @@ __device__ __forceinline__ float dot_hgroup(const uint4* q, const float* __restr
 // Warps per position of the confidence logit: at most 512 threads per block for gamma <= 8.
 __host__ __device__ inline int conf_parts(int gamma) { return gamma <= 8 ? 2 : 1; }
 
-// Lane `lane`'s share of part `part` of the logit of one (request, position): hr = the h row
-// (d), w1row = W1[x_{k-1}] (r) for part 0 (else ignored).  Not yet reduced over the warp.
+// Lane `lane`'s share of part `part` of the h term of one (request, position): hr = the h row
+// (d elements).  Not yet reduced over the warp.
 template <typename T>
-__device__ __forceinline__ float conf_part(const T* hr, const T* w1row, const float* __restrict__ w, int d, int r,
-                                           int part, int parts, int lane) {
-  // the W1[x_{k-1}] row is read first, so that its loads overlap the h loads below
-  const bool has_w1 = part == 0 && lane * 8 < r;
-  uint4 qa[sizeof(T) == 4 ? 2 : 1];
-  if (has_w1) load_hgroup<T>(w1row + lane * 8, qa);
+__device__ __forceinline__ float conf_hpart(const T* hr, const float* __restrict__ w, int d, int part, int parts,
+                                            int lane) {
   const int stride = parts * 256;
   float acc = 0.f;
   for (int e0 = part * 256 + lane * 8; e0 < d; e0 += kConfLoads * stride) {
@@ -84,8 +81,14 @@ __device__ __forceinline__ float conf_part(const T* hr, const T* w1row, const fl
       if (e < d) acc += dot_hgroup<T>(q[u], w + e);
     }
   }
-  if (has_w1) acc += dot_hgroup<T>(qa, w + d + lane * 8);
   return acc;
+}
+
+// Lane `lane`'s share of the W1[x_{k-1}] term from its 8-element group qa (loaded by the caller
+// from w1row + 8 lane when 8 lane < r): the dot with w[d + 8 lane ..).  Not yet reduced.
+template <typename T>
+__device__ __forceinline__ float conf_xpart(const uint4* qa, const float* __restrict__ w, int d, int r, int lane) {
+  return lane * 8 < r ? dot_hgroup<T>(qa, w + d + lane * 8) : 0.f;
 }
 
 }  // namespace dspark

@@ -56,9 +56,10 @@
 //               select merges one entry per CTA column.
 //   select    = the epilogue warps as two groups of eight, one request each (request
 //               blockIdx + (2 j + group) * gridDim)
-//   warp 19   = the confidence head when the call asks for it: position k's confidence and
-//               survival of the requests blockIdx + j gridDim, as soon as x_{k-1} is readable,
-//               so that it finishes under the draft's own time
+//   warp 19   = the confidence head when the call asks for it: the h terms of the requests
+//               blockIdx + j gridDim ahead of time (they need no drafted token), then position
+//               k's confidence and survival as soon as x_{k-1} is readable, so that it finishes
+//               under the draft's own time
 // Every mbarrier and grid-barrier wait is bounded (SM cycle-counter deadline + shared abort flag,
 // and a grid-wide abort word); on give-up the kernel records DSPARK_ETIMEOUT, waits (bounded) for
 // its own copies / MMAs in flight, frees TMEM and returns.  The grid barrier's words live in the
@@ -240,19 +241,42 @@ __device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* a) {
   return v;
 }
 
-// The confidence head, computed by one warp of each CTA while the draft runs: for position k
-// (once every CTA can read x_{k-1}) and the requests blockIdx + j gridDim, the logit
-// z = w [h_k ; W1[x_{k-1}]] + b in the confidence kernel's order (confidence.cuh), then
-// c = sigmoid(z / T_k) and the survival a_k = a_{k-1} c -- the same bits as dspark_confidence.
-// tok_pos (set by the epilogue after each position's tokens are visible grid-wide) counts the
-// positions whose feature rows are ready.  Returns false if a wait gave up.
+// The confidence head, computed by one warp of each CTA while the draft runs, for the requests
+// blockIdx + j gridDim: the logit z = w [h_k ; W1[x_{k-1}]] + b in the confidence kernel's order
+// (confidence.cuh), then c = sigmoid(z / T_k) and the survival a_k = a_{k-1} c -- the same bits
+// as dspark_confidence.  The h terms need no drafted token: they are computed ahead, position by
+// position, whenever the next position to finish is still waiting for its x_{k-1}, so that
+// finishing a position is one W1-row term per request.  tok_pos (set by the epilogue after each
+// position's tokens are visible grid-wide) counts the positions whose x_{k-1} is readable.
+// Returns false if a wait gave up.
+// The h term of one (request, position), reduced over the warp: its parts in order.
+__device__ __noinline__ float conf_h_term(const __nv_bfloat16* hr, const float* w, int d, int parts, int lane) {
+  float z = warp_sum(conf_hpart<__nv_bfloat16>(hr, w, d, 0, parts, lane));
+  for (int q = 1; q < parts; ++q) z += warp_sum(conf_hpart<__nv_bfloat16>(hr, w, d, q, parts, lane));
+  return z;
+}
+
 template <typename P>
 __device__ __noinline__ bool confidence_warp(const P& p, const uint32_t* tok_pos, int npos, long long deadline,
                                              const volatile int* abort, int lane) {
+  constexpr int kAhead = 2;  // requests per CTA whose h terms are kept (more are computed in place)
   const int parts = conf_parts(p.gamma);
+  float hsum[kAhead][DSPARK_MAX_GAMMA];
+  auto h_term = [&](int b, int k) {
+    return conf_h_term(p.h + (size_t(b) * p.gamma + k - 1) * p.d, p.wconf, p.d, parts, lane);
+  };
+  int ahead = 0;  // positions (from the first) whose h terms are in hsum
   for (int pi = 0; pi < npos; ++pi) {
     const int k = p.k_first + pi;
-    while (ld_acquire_cta(tok_pos) <= uint32_t(pi)) {
+    for (;;) {
+      const bool ready = ld_acquire_cta(tok_pos) > uint32_t(pi);
+      if (ready && ahead > pi) break;
+      if (ahead < npos && (ahead <= pi || !ready)) {  // the h terms of the next position
+        const int ka = p.k_first + ahead;
+        for (int j = 0, b = blockIdx.x; j < kAhead && b < p.bs; ++j, b += gridDim.x) hsum[j][ahead] = h_term(b, ka);
+        ++ahead;
+        continue;
+      }
       if (*abort) return false;
       if (clock64() > deadline) {
         if (lane == 0) note_timeout(p.status, p.diag, 9u, uint32_t(k));
@@ -260,12 +284,13 @@ __device__ __noinline__ bool confidence_warp(const P& p, const uint32_t* tok_pos
       }
       __nanosleep(256);
     }
-    for (int b = blockIdx.x; b < p.bs; b += gridDim.x) {
+    int j = 0;
+    for (int b = blockIdx.x; b < p.bs; b += gridDim.x, ++j) {
       const int xp = clamp_token(k == 1 ? p.anchor[b] : p.tokens[size_t(b) * p.gamma + k - 2], p.V);
-      const __nv_bfloat16* hr = p.h + (size_t(b) * p.gamma + k - 1) * p.d;
-      const __nv_bfloat16* w1row = p.W1 + size_t(xp) * p.r;
-      float z = warp_sum(conf_part<__nv_bfloat16>(hr, w1row, p.wconf, p.d, p.r, 0, parts, lane));
-      for (int q = 1; q < parts; ++q) z += warp_sum(conf_part<__nv_bfloat16>(hr, w1row, p.wconf, p.d, p.r, q, parts, lane));
+      uint4 qa[1];
+      if (lane * 8 < p.r) load_hgroup<__nv_bfloat16>(p.W1 + size_t(xp) * p.r + lane * 8, qa);
+      float z = j < kAhead ? hsum[j][pi] : h_term(b, k);
+      z += warp_sum(conf_xpart<__nv_bfloat16>(qa, p.wconf, p.d, p.r, lane));
       z += p.bconf;
       if (lane == 0) {
         const size_t o = size_t(b) * p.gamma + k - 1;

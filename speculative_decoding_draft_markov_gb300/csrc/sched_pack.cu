@@ -15,26 +15,33 @@ namespace dspark {
 // temperature scaling divides the logit by T_k; prefix survival is the running product.
 // fp32 dot products in a fixed order.
 // ---------------------------------------------------------------------------------------
-// One block per request; conf_parts(gamma) warps per position split the logit (confidence.cuh:
-// conf_part, the order shared with the persistent draft kernel).  Thread 0 then adds the parts in
-// order and runs the sigmoid / STS / product chain.
+// One block per request; conf_parts(gamma) warps per position split the h term, the first of
+// them also reduces the W1[x_{k-1}] term (confidence.cuh: the order shared with the persistent
+// draft kernel).  Thread 0 then adds the terms in order and runs the sigmoid / STS / product
+// chain.
 template <typename T>
 __global__ void __launch_bounds__(512) confidence_kernel(
     const T* __restrict__ h, const T* __restrict__ W1, const int32_t* __restrict__ anchor,
     const int32_t* __restrict__ tokens, const float* __restrict__ w, float b,
     const float* __restrict__ sts_T, int gamma, int d, int r, int V, int parts, float* __restrict__ conf,
     float* __restrict__ surv, float* __restrict__ z_out) {
-  __shared__ float zp[DSPARK_MAX_GAMMA * 4];
+  __shared__ float zp[DSPARK_MAX_GAMMA * 4], zx[DSPARK_MAX_GAMMA];
   pdl_enter();
   const int req = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pos = warp / parts, part = warp - pos * parts;
   if (pos < gamma) {
     const int k = pos + 1;
-    const T* w1row = nullptr;
+    // the W1[x_{k-1}] group is loaded first, so that its latency overlaps the h loads
+    uint4 qa[sizeof(T) == 4 ? 2 : 1];
     if (part == 0 && lane * 8 < r)
-      w1row = W1 + size_t(clamp_token((k == 1) ? anchor[req] : tokens[size_t(req) * gamma + k - 2], V)) * r;
-    const float acc = warp_sum(conf_part<T>(h + (size_t(req) * gamma + pos) * d, w1row, w, d, r, part, parts, lane));
-    if (lane == 0) zp[pos * 4 + part] = acc;
+      load_hgroup<T>(W1 + size_t(clamp_token((k == 1) ? anchor[req] : tokens[size_t(req) * gamma + k - 2], V)) * r +
+                         lane * 8, qa);
+    const float hq = warp_sum(conf_hpart<T>(h + (size_t(req) * gamma + pos) * d, w, d, part, parts, lane));
+    if (lane == 0) zp[pos * 4 + part] = hq;
+    if (part == 0) {
+      const float xq = warp_sum(conf_xpart<T>(qa, w, d, r, lane));
+      if (lane == 0) zx[pos] = xq;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -42,6 +49,7 @@ __global__ void __launch_bounds__(512) confidence_kernel(
     for (int k = 0; k < gamma; ++k) {
       float z = zp[k * 4];
       for (int q = 1; q < parts; ++q) z += zp[k * 4 + q];
+      z += zx[k];
       z += b;
       if (z_out) z_out[size_t(req) * gamma + k] = z;  // the logit before STS (calibration input)
       const float c = 1.f / (1.f + expf(-z / sts_T[k]));

@@ -36,24 +36,21 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// One 16-byte group of a row as raw bits (loaded ahead of use) and its values.
 template <typename T>
-__device__ __forceinline__ int load_group(const T* row, int e, float* x);
+__device__ __forceinline__ void unpack_group(const uint4& q, float* x);
 template <>
-__device__ __forceinline__ int load_group<__nv_bfloat16>(const __nv_bfloat16* row, int e, float* x) {
-  const uint4 q = reinterpret_cast<const uint4*>(row)[e];
+__device__ __forceinline__ void unpack_group<__nv_bfloat16>(const uint4& q, float* x) {
   x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
   x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
-  return 8;
 }
 template <>
-__device__ __forceinline__ int load_group<float>(const float* row, int e, float* x) {
-  const float4 q = reinterpret_cast<const float4*>(row)[e];
-  x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
-  return 4;
+__device__ __forceinline__ void unpack_group<float>(const uint4& q, float* x) {
+  x[0] = __uint_as_float(q.x); x[1] = __uint_as_float(q.y); x[2] = __uint_as_float(q.z); x[3] = __uint_as_float(q.w);
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
+__global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(
     const T* __restrict__ target, const int32_t* __restrict__ cu, const int32_t* __restrict__ tokens,
     int bs, int gamma, int V, float inv_tau, int greedy, RowStat* __restrict__ rs, uint32_t* status) {
   __shared__ float sv[kRowThreads / 32], ss[kRowThreads / 32];
@@ -75,23 +72,38 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
   const T* row = target + size_t(p) * V;
   constexpr int G = sizeof(T) == 2 ? 8 : 4;
   const int ng = V / G;
+  // Each thread reads groups tid, tid + 256, ... in batches of kBatch; the next batch's loads
+  // are issued before the current batch is reduced, so two batches (64 KB a block) are in
+  // flight.  The arithmetic and its order do not depend on the prefetch.
+  constexpr int kBatch = 8;
+  constexpr int kStride = kBatch * kRowThreads;
+  const uint4* rv = reinterpret_cast<const uint4*>(row);
+  uint4 cur[kBatch], nxt[kBatch];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    const int e = tid + u * kRowThreads;
+    if (e < ng) cur[u] = rv[e];
+  }
   if (greedy) {
     ArgMax best{-INFINITY, INT_MAX};
-    for (int e0 = tid; e0 < ng; e0 += 4 * kRowThreads) {
-      float xb[4][8];
+    for (int e0 = tid; e0 < ng; e0 += kStride) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = e0 + u * kRowThreads;
-        if (e < ng) load_group<T>(row, e, xb[u]);
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = e0 + kStride + u * kRowThreads;
+        if (e < ng) nxt[u] = rv[e];
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kBatch; ++u) {
         const int e = e0 + u * kRowThreads;
         if (e >= ng) break;
+        float x[8];
+        unpack_group<T>(cur[u], x);
 #pragma unroll
         for (int q = 0; q < G; ++q)
-          if (xb[u][q] > best.v) best = ArgMax{xb[u][q], e * G + q};
+          if (x[q] > best.v) best = ArgMax{x[q], e * G + q};
       }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) cur[u] = nxt[u];
     }
     best = block_argmax<kRowThreads>(best, sv, si);
     if (tid == 0) {
@@ -109,24 +121,22 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
   // rescaled only when a batch of kBatch * G values raises the max
   const float c2 = inv_tau * 1.4426950408889634f;
   float m2 = -INFINITY, s2 = 0.f;
-  constexpr int kBatch = 8;  // independent 16-byte loads in flight per thread
-  for (int e0 = tid; e0 < ng; e0 += kBatch * kRowThreads) {
-    float xb[kBatch][8];
+  for (int e0 = tid; e0 < ng; e0 += kStride) {
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      const int e = e0 + u * kRowThreads;
-      if (e < ng) {
-        load_group<T>(row, e, xb[u]);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) xb[u][q] = -INFINITY;
-      }
+      const int e = e0 + kStride + u * kRowThreads;
+      if (e < ng) nxt[u] = rv[e];
     }
     float bm = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u)
+    for (int u = 0; u < kBatch; ++u) {
+      if (e0 + u * kRowThreads < ng) {
+        float x[8];
+        unpack_group<T>(cur[u], x);
 #pragma unroll
-      for (int q = 0; q < G; ++q) bm = fmaxf(bm, xb[u][q]);
+        for (int q = 0; q < G; ++q) bm = fmaxf(bm, x[q]);
+      }
+    }
     const float bm2 = bm * c2;
     if (bm2 > m2) {
       s2 = (s2 == 0.f) ? 0.f : s2 * ex2_approx(m2 - bm2);
@@ -134,10 +144,17 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(
     }
     float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u)
+    for (int u = 0; u < kBatch; ++u) {
+      if (e0 + u * kRowThreads < ng) {
+        float x[8];
+        unpack_group<T>(cur[u], x);
 #pragma unroll
-      for (int q = 0; q < G; ++q) s4[q & 3] += ex2_approx(fmaf(xb[u][q], c2, -m2));  // 2^-inf = 0
+        for (int q = 0; q < G; ++q) s4[q & 3] += ex2_approx(fmaf(x[q], c2, -m2));
+      }
+    }
     s2 += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) cur[u] = nxt[u];
   }
   LsePair acc{m2 * 0.69314718055994531f, s2};  // natural units for the block merge
   acc = block_lse<kRowThreads>(acc, sv, ss);
