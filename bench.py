@@ -164,6 +164,24 @@ class ClockSampler:
                 "samples": len(sm), "source": "nvml" if self.samples else "nvidia-smi"}
 
 # ------------------------------------------------------------------------------- CPU oracle
+def _host_target(h, tok, dtype: str):
+    """The workloads' target model on the host, as step.markov_target_forward computes it on the
+    device: every (request, position) row j of the drawn base target (U + noise) plus W1[x_j] W2,
+    x_0 the anchor and x_j the drafted tokens; the term is accumulated in fp32 and rounded to the
+    logits' dtype, then added to the row with one more rounding."""
+    from speculative_decoding_draft_markov_gb300 import inputs as I
+    x = np.concatenate([np.asarray(h["anchor"])[:, None], np.asarray(tok)], axis=1)  # [n, gamma + 1]
+    if dtype == "f32":
+        W1, W2t = h["W1"], h["W2t"]
+        return np.ascontiguousarray(h["target"] + np.stack([W1[x[:, j]] @ W2t.T for j in range(x.shape[1])], 1))
+    W1, W2t = I.bf16_bits_to_f32(h["W1"]), I.bf16_bits_to_f32(h["W2t"])
+    out = np.empty_like(h["target"])
+    for j in range(x.shape[1]):  # a position at a time keeps the fp32 temporaries at [n, V]
+        term = I.bf16_bits_to_f32(I.f32_to_bf16_bits(W1[x[:, j]] @ W2t.T))
+        out[:, j] = I.f32_to_bf16_bits(I.bf16_bits_to_f32(h["target"][:, j]) + term)
+    return out
+
+
 def _oracle_steps(wl_name: str, n_req: int, steps, mode_name: str = "compact", sched: int = SCHED):
     """The oracle's full step (draft, confidence, schedule, pack, verify) on the first n_req
     requests of a workload, on every host core (oracle.pool: one worker per core, requests in
@@ -182,6 +200,9 @@ def _oracle_steps(wl_name: str, n_req: int, steps, mode_name: str = "compact", s
         for s in steps:
             t0 = time.perf_counter()
             (tok, lx, lse, _), _ = OP.draft_all(p, h["U"], h["anchor"], wl.temperature, wl.seed, s, per=per)
+            t1 = time.perf_counter()
+            target = _host_target(h, tok, wl.dtype)  # the target model's forward: not the oracle's time
+            t_fwd = time.perf_counter() - t1
             if mode == O.COMPACT:
                 _, surv, _ = O.confidence(h["h"], h["W1"], h["anchor"], tok, h["w"], h["b"], h["sts_T"],
                                           dtype=wl.dtype)
@@ -190,10 +211,10 @@ def _oracle_steps(wl_name: str, n_req: int, steps, mode_name: str = "compact", s
                                                                                  int(h["tiers"][-1])))
             else:
                 win = np.full(n_req, wl.gamma, dtype=np.int32)
-            (_, acc, _, _), _ = OP.verify_all(p, h["target"], h["U"], win, mode, h["anchor"], tok,
+            (_, acc, _, _), _ = OP.verify_all(p, target, h["U"], win, mode, h["anchor"], tok,
                                               lx.astype(np.float32), lse.astype(np.float32), wl.temperature,
                                               wl.seed, s, per=per)
-            out.append((O.step_tokens(acc), time.perf_counter() - t0))
+            out.append((O.step_tokens(acc), time.perf_counter() - t0 - t_fwd))
     return out, OP.workers()
 
 
@@ -336,7 +357,8 @@ class Path:
         self.buf = S.StepBuffers.allocate(wl.bs, wl.gamma, wl.V, self.cap, self.inp["U"].dtype, dev)
         self.sps = S.sps_table(self.inp["T_raw"], self.inp["tiers"], dev)
         self.tiers = torch.as_tensor(self.inp["tiers"], device=dev) if len(self.inp["tiers"]) else None
-        self.fwd = S.gather_target_forward(self.inp["target"])
+        self.fwd = S.markov_target_forward(S.gather_target_forward(self.inp["target"]), self.inp["W1"],
+                                           self.inp["W2t"])
         self.ring = S.zos_ring(dev)
         self.vmode = B.DSPARK_COMPACT if mode == "compact" else B.DSPARK_STATIC
         # the Markov head's compact step computes the confidence inside the draft's launch
@@ -475,10 +497,11 @@ def time_steps(path, steps, warmup, zos=False, world=1):
 def time_e2e(path, steps):
     """The same step end to end through the public API with host buffers (pinned), every copy
     inside the timing: U, h and the anchors of each step copied host -> device on a second stream
-    one step ahead (double-buffered); the target logits of every (request, position) stay in
-    pinned host memory (the target model's output) and each step's target forward reads the packed
-    layout back (cu_seqlens, after the pack) and copies exactly the rows that step verifies
-    (dspark_copy_packed_rows_async); out_tokens and acc_len come back every step.  Returns
+    one step ahead (double-buffered); the base target logits (U + noise) of every (request,
+    position) stay in pinned host memory and each step's target forward reads the packed layout
+    back (cu_seqlens, after the pack), copies exactly the rows that step verifies
+    (dspark_copy_packed_rows_async) and adds their Markov term on the device
+    (step.markov_target_forward); out_tokens and acc_len come back every step.  Returns
     (tokens/s, h2d bytes per step, d2h bytes per step, steps)."""
     import torch
     B, S, buf, inp, wl, dev = path.B, path.S, path.buf, path.inp, path.wl, path.dev
@@ -490,11 +513,15 @@ def time_e2e(path, steps):
     cu_host = torch.empty(bs + 1, dtype=torch.int32).pin_memory()
     target_rows = []
 
-    def host_target_forward(b):
+    def host_rows(b):
         cu_host.copy_(b.cu, non_blocking=True)
         stream.synchronize()  # the packed layout is known once the pack has run
         B.dspark_copy_packed_rows_async(b.packed, host_target, cu_host, stream)
         target_rows.append(int(cu_host[bs]))
+
+    # the Markov term over every row of the buffer: one GEMM shape for all steps (a new row count
+    # each step would make cuBLAS pick a kernel for each new shape inside the timing)
+    host_target_forward = S.markov_target_forward(host_rows, inp["W1"], inp["W2t"])
 
     inps = [inp, dict(inp)]
     for k in host:
@@ -626,8 +653,8 @@ def run_ours(args, rank: int, world: int):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
-        "data": "synthetic (seeded; U~N(0,3^2), W~N(0,0.05^2), target = base logits + N(0,sigma^2), "
-                "sigma 0.5/1/2 by thirds)",
+        "data": "synthetic (seeded; U~N(0,3^2), W~N(0,0.05^2), target = U + W1[x_{k-1}]W2 + N(0,sigma^2) at the "
+                "drafted prefix, sigma 0.5/1/2 by thirds)",
         "config": {"workload": "mixed_bs256: bs=256, gamma=7, V=151936, r=256, d=4096, compact verify, "
                                "temperature 1, sawtooth cost table with tiers every 64 to 2048, global-argmax scheduler",
                    "global_batch": wl.bs * world, "l2": "flushed between steps (256 MB write)",
@@ -642,8 +669,8 @@ def run_ours(args, rank: int, world: int):
         "roofline": head["roofline"],
         "e2e": dict(head["e2e"], note="U, h, anchors copied from pinned host memory every step on a second stream, "
                                       "one step ahead (double-buffered); the target forward copies the step's "
-                                      "packed target rows from pinned host memory after the pack (cu_seqlens read "
-                                      "back)"),
+                                      "packed base target rows (U + noise) from pinned host memory after the pack "
+                                      "(cu_seqlens read back) and adds their Markov term W1[x_j]W2 on the device"),
         "gpu_launches": head["gpu_launches"],
         "clocks": head["clocks"],
         "observability": obs,
@@ -818,7 +845,7 @@ def run_profile_case(args):
         sps = S.sps_table(inp["T_raw"], inp["tiers"], dev)
         S.draft_and_schedule(inp, buf, sps, wl.temperature, wl.seed, 0, SCHED,
                              tiers=torch.as_tensor(inp["tiers"], device=dev))
-        S.gather_target_forward(inp["target"])(buf)
+        S.markov_target_forward(S.gather_target_forward(inp["target"]), inp["W1"], inp["W2t"])(buf)
 
         def run(it):
             S.verify(inp, buf, wl.temperature, wl.seed, it)

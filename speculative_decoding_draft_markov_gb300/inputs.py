@@ -21,7 +21,9 @@ Tensors produced (layouts are the library's):
   W1      [V, r]              Markov factor, looked up by the previous token
   W2t     [V, r]              Markov projection stored transposed (W2 = W2t^T)
   anchor  [bs] int32          last committed token x_0
-  target  [bs, gamma+1, V]    target logits; row j scores the token at j+1
+  target  [bs, gamma+1, V]    base target logits U_{j+1} + noise; row j scores the token at
+                              j+1 (the workloads' target adds the Markov term W1[x_j] W2 of the
+                              drafted prefix: step.markov_target_forward, after the draft)
   h       [bs, gamma, d]      backbone hidden states
   w       [d + r] f32         confidence-head weight over [h_k ; W1[x_{k-1}]]
   b       float               confidence-head bias (0)

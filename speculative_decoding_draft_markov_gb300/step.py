@@ -107,6 +107,27 @@ def gather_target_forward(target_full):
     return fwd
 
 
+def markov_target_forward(base_forward, W1, W2t, n_rows=None):
+    """The workloads' target model, "target = U + W1[x_{k-1}] W2 + noise": the drafter's own
+    logits at the drafted prefix plus noise.  base_forward fills each packed row with its base
+    part (U + noise, drawn per (request, position) in advance); this adds the Markov term of the
+    row's prefix.  Packed row p scores the token after ids[p] (the pack's input token of the row:
+    the anchor, then the drafted tokens), so it gets W1[ids[p]] W2 -- a cuBLAS GEMM with fp32
+    accumulation, standing in for the target model's own compute, rounded to the rows' dtype and
+    then added to the row with one more rounding.  n_rows: a callable giving the packed total when the
+    caller knows it on the host; else every row of the buffer is computed (pad rows, whose ids
+    are -1, take W1[0]; verify never reads them)."""
+    import torch
+
+    def fwd(buf: StepBuffers) -> None:
+        base_forward(buf)
+        n = buf.packed.shape[0] if n_rows is None else int(n_rows())
+        if n > 0:
+            buf.packed[:n].add_(torch.matmul(W1.index_select(0, buf.ids[:n].clamp(min=0).long()), W2t.t()))
+
+    return fwd
+
+
 def zos_ring(device="cuda"):
     """The two-entry budget ring of the asynchronous scheduler, empty (-1) before the first step."""
     import torch
