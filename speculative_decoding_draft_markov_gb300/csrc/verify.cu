@@ -49,10 +49,62 @@ __device__ __forceinline__ void unpack_group<float>(const uint4& q, float* x) {
   x[0] = __uint_as_float(q.x); x[1] = __uint_as_float(q.y); x[2] = __uint_as_float(q.z); x[3] = __uint_as_float(q.w);
 }
 
-template <typename T>
+// One batch of the online row sum: groups cur[u] = row groups e0 + u 256 (kFull: all of them
+// inside the row, so no per-group test).  The batch maximum is taken on the raw bf16 pairs
+// (max.bf16x2: exact, a quarter of the instructions of unpacking first); then m2 and s2 are
+// rescaled if it raised the maximum, and s2 gains sum 2^(x c2 - m2) in the fixed order
+// (four partial sums by element index mod 4).
+template <typename T, bool kFull, int kBatch>
+__device__ __forceinline__ void lse_batch(const uint4 (&cur)[kBatch], int e0, int ng, float c2, float& m2,
+                                          float& s2) {
+  constexpr int G = sizeof(T) == 2 ? 8 : 4;
+  float bm;
+  if constexpr (sizeof(T) == 2) {
+    __nv_bfloat162 mv = __float2bfloat162_rn(-INFINITY);
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (kFull || e0 + u * kRowThreads < ng) {
+        const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&cur[u]);
+        mv = __hmax2(mv, __hmax2(__hmax2(v[0], v[1]), __hmax2(v[2], v[3])));
+      }
+    }
+    bm = fmaxf(__low2float(mv), __high2float(mv));
+  } else {
+    bm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (kFull || e0 + u * kRowThreads < ng) {
+        float x[8];
+        unpack_group<T>(cur[u], x);
+#pragma unroll
+        for (int q = 0; q < G; ++q) bm = fmaxf(bm, x[q]);
+      }
+    }
+  }
+  const float bm2 = bm * c2;
+  if (bm2 > m2) {
+    s2 = (s2 == 0.f) ? 0.f : s2 * ex2_approx(m2 - bm2);
+    m2 = bm2;
+  }
+  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    if (kFull || e0 + u * kRowThreads < ng) {
+      float x[8];
+      unpack_group<T>(cur[u], x);
+#pragma unroll
+      for (int q = 0; q < G; ++q) s4[q & 3] += ex2_approx(fmaf(x[q], c2, -m2));
+    }
+  }
+  s2 += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+}
+
+// greedy (temperature 0: the row's argmax) is a template parameter, so that each variant's
+// registers are allocated for its own loop
+template <typename T, bool greedy>
 __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(
     const T* __restrict__ target, const int32_t* __restrict__ cu, const int32_t* __restrict__ tokens,
-    int bs, int gamma, int V, float inv_tau, int greedy, RowStat* __restrict__ rs, uint32_t* status) {
+    int bs, int gamma, int V, float inv_tau, RowStat* __restrict__ rs, uint32_t* status) {
   __shared__ float sv[kRowThreads / 32], ss[kRowThreads / 32];
   __shared__ int si[kRowThreads / 32];
   __shared__ int s_cu[DSPARK_MAX_BS + 1];
@@ -84,7 +136,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(
     const int e = tid + u * kRowThreads;
     if (e < ng) cur[u] = rv[e];
   }
-  if (greedy) {
+  if constexpr (greedy) {
     ArgMax best{-INFINITY, INT_MAX};
     for (int e0 = tid; e0 < ng; e0 += kStride) {
 #pragma unroll
@@ -127,32 +179,8 @@ __global__ void __launch_bounds__(kRowThreads, 3) verify_rows_kernel(
       const int e = e0 + kStride + u * kRowThreads;
       if (e < ng) nxt[u] = rv[e];
     }
-    float bm = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      if (e0 + u * kRowThreads < ng) {
-        float x[8];
-        unpack_group<T>(cur[u], x);
-#pragma unroll
-        for (int q = 0; q < G; ++q) bm = fmaxf(bm, x[q]);
-      }
-    }
-    const float bm2 = bm * c2;
-    if (bm2 > m2) {
-      s2 = (s2 == 0.f) ? 0.f : s2 * ex2_approx(m2 - bm2);
-      m2 = bm2;
-    }
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      if (e0 + u * kRowThreads < ng) {
-        float x[8];
-        unpack_group<T>(cur[u], x);
-#pragma unroll
-        for (int q = 0; q < G; ++q) s4[q & 3] += ex2_approx(fmaf(x[q], c2, -m2));
-      }
-    }
-    s2 += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    if (e0 + (kBatch - 1) * kRowThreads < ng) lse_batch<T, true>(cur, e0, ng, c2, m2, s2);
+    else lse_batch<T, false>(cur, e0, ng, c2, m2, s2);
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) cur[u] = nxt[u];
   }
@@ -470,8 +498,10 @@ static cudaError_t verify_typed(const T* target, const int32_t* cu, const int32_
   DecideEntry* entries = reinterpret_cast<DecideEntry*>(w + L.stats);
   RowStat* rs = reinterpret_cast<RowStat*>(w + L.rowstats);
   Decision* dec = reinterpret_cast<Decision*>(w + L.dec);
-  cudaError_t le = launch_pdl(verify_rows_kernel<T>, dim3(bs * (gamma + 1)), dim3(kRowThreads), 0, s, target, cu,
-                              tokens, bs, gamma, V, inv_tau, greedy, rs, status);
+  cudaError_t le = greedy ? launch_pdl(verify_rows_kernel<T, true>, dim3(bs * (gamma + 1)), dim3(kRowThreads), 0, s,
+                                       target, cu, tokens, bs, gamma, V, inv_tau, rs, status)
+                          : launch_pdl(verify_rows_kernel<T, false>, dim3(bs * (gamma + 1)), dim3(kRowThreads), 0, s,
+                                       target, cu, tokens, bs, gamma, V, inv_tau, rs, status);
   if (le != cudaSuccess) return le;
   le = launch_pdl(verify_decide_kernel, dim3((bs + 127) / 128), dim3(128), 0, s, cu, window, mode, bs, gamma, tokens,
                   logit_x, lse, static_cast<const RowStat*>(rs), greedy, seed, step, out_tokens, acc_len, ceiling, dec,
