@@ -519,9 +519,15 @@ def time_e2e(path, steps):
         B.dspark_copy_packed_rows_async(b.packed, host_target, cu_host, stream)
         target_rows.append(int(cu_host[bs]))
 
-    # the Markov term over every row of the buffer: one GEMM shape for all steps (a new row count
-    # each step would make cuBLAS pick a kernel for each new shape inside the timing)
-    host_target_forward = S.markov_target_forward(host_rows, inp["W1"], inp["W2t"])
+    # the Markov term over the step's rows rounded up to a multiple of 256: a handful of GEMM
+    # shapes, each run once here before the timing (so that cuBLAS has picked its kernel for
+    # each), instead of a new shape at every step's packed total
+    cap = buf.packed.shape[0]
+    rounded = lambda: min(cap, -(-target_rows[-1] // 256) * 256)
+    host_target_forward = S.markov_target_forward(host_rows, inp["W1"], inp["W2t"], rounded)
+    for n in range(256, cap + 256, 256):
+        n = min(n, cap)
+        torch.matmul(inp["W1"][:n], inp["W2t"].t())
 
     inps = [inp, dict(inp)]
     for k in host:
@@ -828,10 +834,14 @@ def run_profile_case(args):
                             buf.conf, buf.surv)
         ring = S.zos_ring(dev)
         ring.fill_(200)
+        tiers = torch.as_tensor(inp["tiers"], device=dev)
 
         def run(it):
             B.dspark_schedule(buf.surv, sps, SCHED, buf.window, buf.K, buf.theta, buf.ws)
             B.dspark_schedule_zos_select(buf.surv, sps, ring, it, buf.window, buf.K, buf.ws)
+            # the benchmark's own call: the scheduler and the pack in one launch
+            B.dspark_schedule_pack(buf.surv, sps, SCHED, buf.window, buf.K, buf.theta, inp["anchor"], buf.tokens,
+                                   tiers, buf.cu, buf.ids, buf.req, buf.pos, buf.padded, buf.ws)
     elif args.profile_case == "draft":
         # the benchmark's draft stage: the draft and the confidence head in one call
         def run(it):

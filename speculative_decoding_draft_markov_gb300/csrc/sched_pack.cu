@@ -107,6 +107,8 @@ __device__ __forceinline__ double scaled_fixed(long long T) {
   return __longlong_as_double(static_cast<long long>((static_cast<unsigned long long>(e + 1023 - 40) << 52) | mant));
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 // Order-preserving 64-bit integer of a non-NaN double (-0 maps with +0).
 __device__ __forceinline__ long long dkey(double x) {
   long long b = __double_as_longlong(x);
@@ -183,6 +185,92 @@ __device__ void bitonic_sort(const float* __restrict__ surv, int n, unsigned lon
   for (int e = 0; e < E; ++e) out[tid * E + e] = v[e];
 }
 
+// Ascending bitonic sort of each warp's 32 E keys (thread t holds keys t E .. t E + E - 1) in
+// registers: exchanges at distance j < E inside the thread, longer ones by warp shuffles.  The
+// last stage sorts every warp's run ascending (instead of alternating the directions).
+template <int E>
+__device__ __forceinline__ void warp_bitonic(unsigned long long (&v)[E], int tid) {
+  constexpr int R = 32 * E;
+  const int lane = tid & 31;
+#pragma unroll
+  for (int k = 2; k <= R; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j < E) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int f = e ^ j;
+          if (f > e) {
+            const bool up = (k == R) || (((tid * E + e) & k) == 0);
+            const unsigned long long lo = v[e] < v[f] ? v[e] : v[f], hi = v[e] < v[f] ? v[f] : v[e];
+            v[e] = up ? lo : hi;
+            v[f] = up ? hi : lo;
+          }
+        }
+      } else {
+        const int lm = j / E;  // partner lane distance
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, v[e], lm);
+          const bool up = (k == R) || (((tid * E + e) & k) == 0);
+          const bool keep_min = up == ((lane & lm) == 0);
+          v[e] = keep_min ? (v[e] < o ? v[e] : o) : (v[e] < o ? o : v[e]);
+        }
+      }
+    }
+  }
+}
+
+// Ascending sort of the keys of slots 0 .. 1024 E - 1 by the 1024 threads of the block, for
+// 2 N <= kSchedMaxSlots (N = 1024 E): each warp sorts its 32 E keys in registers, then merge
+// rounds double the sorted runs up to N.  In a round a key's place in the merged run is its
+// place in its own run plus the number of keys of the partner run below it (a branch-free
+// binary search in shared memory: keys are distinct, the slot index being part of each), so the
+// result is the unique ascending order, and a round is one barrier.  The sorted keys end in
+// buf[0 .. N).
+template <int E>
+__device__ void merge_sort(const float* __restrict__ surv, int n, unsigned long long* buf, int tid) {
+  constexpr int N = 1024 * E;
+  static_assert(2 * N <= kSchedMaxSlots && (E == 1 || E == 2), "the merge sort ping-pongs between two halves of the buffer");
+  unsigned long long* src = buf;
+  unsigned long long* dst = buf + N;
+  unsigned long long v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = sched_key(surv, tid * E + e, n);
+  warp_bitonic<E>(v, tid);
+#pragma unroll
+  for (int e = 0; e < E; ++e) src[tid * E + e] = v[e];
+  constexpr int LG = E == 1 ? 10 : 11;  // log2 N
+  constexpr int S0 = E == 1 ? 5 : 6;    // log2 of the warp runs
+#pragma unroll
+  for (int s = S0; s < LG; ++s) {  // unrolled: each round's search length is a constant
+    const int L = 1 << s;
+    __syncthreads();  // src is complete (and dst no longer read by the previous round)
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int idx = tid * E + e;
+      const unsigned long long key = src[idx];
+      const int run = idx >> s;
+      const unsigned long long* pr = src + ((run ^ 1) << s);  // the partner run
+      int c = 0;  // keys of the partner run below key
+#pragma unroll
+      for (int h = L >> 1; h > 0; h >>= 1)
+        if (pr[c + h - 1] < key) c += h;
+      if (pr[c] < key) ++c;
+      dst[((run >> 1) << (s + 1)) + (idx & (L - 1)) + c] = key;
+    }
+    unsigned long long* t = src;
+    src = dst;
+    dst = t;
+  }
+  __syncthreads();
+  if (src != buf) {  // an odd number of rounds: copy the result down
+#pragma unroll
+    for (int e = 0; e < E; ++e) buf[tid * E + e] = src[tid * E + e];
+    __syncthreads();
+  }
+}
+
 // Shared state of one scheduler block.
 struct SchedShared {
   unsigned long long buf[kSchedMaxSlots];  // sorted keys, then prefix sums (radix histogram)
@@ -209,17 +297,18 @@ __device__ int sched_search(const float* __restrict__ surv, int bs, int gamma,
   long long* red_v = sh.red_v;
   int* win = sh.win;
 
-  // Bitonic sort of the n keys padded with sentinels (above every real key: survival 0 has high
-  // word 0xFFFFFFFF, real slot indices are below 4096) to N = max(1024, 2^ceil(log2 n)) <= 4096.
-  // Thread t holds keys t E .. t E + E - 1 (E = N / 1024) in registers: exchanges at distance
-  // j < E stay in the thread, j < 32 E go through warp shuffles, longer ones through shared
-  // memory.
+  // Sort of the n keys padded with sentinels (above every real key: survival 0 has high word
+  // 0xFFFFFFFF, real slot indices are below 4096) to N = max(1024, 2^ceil(log2 n)) <= 4096: the
+  // merge sort up to N = 2048, the bitonic network (registers, warp shuffles, one shared buffer)
+  // for N = 4096.  Both give the unique ascending order of the distinct keys.
+  // the table is read after the sort: pulled into L2 now (16 doubles per 128-byte line)
+  for (int i = tid * 16; i <= m_max; i += kSchedThreads * 16) prefetch_l2(sps + i);
   int lg_n = 10;
   while ((1 << lg_n) < n) ++lg_n;
   const int N = 1 << lg_n;
   for (int e = tid; e < DSPARK_MAX_BS; e += kSchedThreads) win[e] = 0;
-  if (N == 1024) bitonic_sort<1>(surv, n, src, tid);
-  else if (N == 2048) bitonic_sort<2>(surv, n, src, tid);
+  if (N == 1024) merge_sort<1>(surv, n, src, tid);
+  else if (N == 2048) merge_sort<2>(surv, n, src, tid);
   else bitonic_sort<4>(surv, n, src, tid);
   __syncthreads();
   unsigned long long* key = src;  // sorted keys, then inclusive prefix sums
@@ -282,9 +371,16 @@ __device__ int sched_search(const float* __restrict__ surv, int bs, int gamma,
   for (int K = tid; K <= kmax; K += kSchedThreads) {
     // the table entries the search reads must be finite, non-negative and non-increasing in M
     // (dspark_build_sps makes them so); a table that is not is reported, the search still runs
+    // (integer tests on the bits: this part's fp64 pipe is narrow) s0 finite and >= 0 (or -0),
+    // and the next entry not NaN and not above it
     const double s0 = sps[bs + K];
-    if (!(s0 >= 0.0) || dnan(s0) || s0 > 1.7976931348623157e308 || (K < kmax && !(sps[bs + K + 1] <= s0)))
-      bad_table = true;
+    const long long b0 = __double_as_longlong(s0);
+    bool ok = (b0 >= 0 && b0 < 0x7FF0000000000000ll) || b0 == static_cast<long long>(0x8000000000000000ull);
+    if (K < kmax) {
+      const double s1 = sps[bs + K + 1];
+      ok = ok && !dnan(s1) && dkey(s1) <= dkey(s0);
+    }
+    if (!ok) bad_table = true;
     const double t0 = theta(K);
     if (mode == DSPARK_SCHED_EARLY_STOP) {
       if (K < kmax) {
@@ -530,8 +626,12 @@ __device__ void pack_block(const int32_t* window, const int32_t* __restrict__ an
                            uint32_t* status) {
   __shared__ int wsum[32];
   __shared__ int s_padded, s_M, s_bad;
+  __shared__ unsigned long long s_first;  // (index << 32) | value of the first tier >= M
   const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
-  if (r == 0) s_bad = 0;
+  if (r == 0) {
+    s_bad = 0;
+    s_first = ~0ull;
+  }
   __syncthreads();
   // the tiers must be positive and strictly increasing (the search below takes the first >= M)
   for (int i = r; i < n_tiers; i += blockDim.x)
@@ -562,17 +662,17 @@ __device__ void pack_block(const int32_t* window, const int32_t* __restrict__ an
     s_M = start + n;
   }
   __syncthreads();
+  // the first tier >= M, found by all threads at once (a serial scan would be one dependent load
+  // per tier)
+  for (int i = r; i < n_tiers; i += blockDim.x) {
+    const int t = tiers[i];
+    if (t >= s_M) atomicMin(&s_first, (static_cast<unsigned long long>(i) << 32) | static_cast<uint32_t>(t));
+  }
+  __syncthreads();
   if (r == 0) {
     const int M = s_M;
     int padded = M;
-    if (n_tiers > 0) {
-      padded = -1;
-      for (int i = 0; i < n_tiers; ++i)
-        if (tiers[i] >= M) {
-          padded = tiers[i];
-          break;
-        }
-    }
+    if (n_tiers > 0) padded = (s_first == ~0ull) ? -1 : static_cast<int>(static_cast<uint32_t>(s_first));
     if (s_bad || padded < 0 || padded > cap) {
       set_status(status, DSPARK_EINVAL);
       padded = -1;
@@ -618,6 +718,10 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_pack_kernel(
     int32_t* __restrict__ pos, int32_t* __restrict__ padded_out, uint32_t* status) {
   __shared__ SchedShared sh;
   pdl_enter();
+  // the pack's inputs are pulled into L2 while the search runs
+  for (int i = threadIdx.x * 32; i < n_tiers; i += kSchedThreads * 32) prefetch_l2(tiers + i);
+  for (int i = threadIdx.x * 32; i < bs; i += kSchedThreads * 32) prefetch_l2(anchor + i);
+  for (int i = threadIdx.x * 32; i < bs * gamma; i += kSchedThreads * 32) prefetch_l2(tokens + i);
   const int ks = sched_search(surv, bs, gamma, sps, m_max, mode, sh, theta_out, status);
   if (threadIdx.x == 0) *K_out = ks;
   sched_windows(sh, ks, bs, gamma, window);

@@ -143,8 +143,8 @@ def _sched_cases():
                                           (1, 1, 4, False, "one"), (33, 5, 5, True, "steep"),
                                           (128, 15, 6, False, "long"), (64, 7, 7, False, "short"),
                                           (200, 3, 8, False, "unsorted"),
-                                          # above 1024 slots the search first sorts the top 1024 only:
-                                          # cases where that settles it and cases where it must fall back
+                                          # each sort size: up to 1024, 2048 (merge sort) and 4096
+                                          # (bitonic) slots, with and without ties
                                           (205, 5, 9, True, "tiers16"), (256, 5, 10, False, "flat"),
                                           (256, 8, 11, False, "const"), (129, 8, 12, False, "mixed"),
                                           (256, 4, 13, False, "unsorted")]:
