@@ -229,9 +229,7 @@ __device__ __forceinline__ bool epi_grid_barrier(Barriers* bar, uint32_t* ctl, i
   return bar->bail != 0;
 }
 
-// The select of position k for this CTA's requests: the epilogue's 512 threads (et) as two
-// groups of eight warps, group g taking requests blockIdx + (2 j + g) gridDim.  Out of line: its
-// registers are not added to the tile loop's.
+// Release / acquire on a shared-memory word of this CTA (the confidence warp's position count).
 __device__ __forceinline__ void st_release_cta(uint32_t* a, uint32_t v) {
   asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(tc::smem_u32(a)), "r"(v) : "memory");
 }
@@ -239,6 +237,13 @@ __device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* a) {
   uint32_t v;
   asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(tc::smem_u32(a)) : "memory");
   return v;
+}
+
+// The h term of one (request, position), reduced over the warp: its parts in order.
+__device__ __noinline__ float conf_h_term(const __nv_bfloat16* hr, const float* w, int d, int parts, int lane) {
+  float z = warp_sum(conf_hpart<__nv_bfloat16>(hr, w, d, 0, parts, lane));
+  for (int q = 1; q < parts; ++q) z += warp_sum(conf_hpart<__nv_bfloat16>(hr, w, d, q, parts, lane));
+  return z;
 }
 
 // The confidence head, computed by one warp of each CTA while the draft runs, for the requests
@@ -249,13 +254,6 @@ __device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* a) {
 // finishing a position is one W1-row term per request.  tok_pos (set by the epilogue after each
 // position's tokens are visible grid-wide) counts the positions whose x_{k-1} is readable.
 // Returns false if a wait gave up.
-// The h term of one (request, position), reduced over the warp: its parts in order.
-__device__ __noinline__ float conf_h_term(const __nv_bfloat16* hr, const float* w, int d, int parts, int lane) {
-  float z = warp_sum(conf_hpart<__nv_bfloat16>(hr, w, d, 0, parts, lane));
-  for (int q = 1; q < parts; ++q) z += warp_sum(conf_hpart<__nv_bfloat16>(hr, w, d, q, parts, lane));
-  return z;
-}
-
 template <typename P>
 __device__ __noinline__ bool confidence_warp(const P& p, const uint32_t* tok_pos, int npos, long long deadline,
                                              const volatile int* abort, int lane) {
@@ -371,6 +369,9 @@ __device__ __noinline__ void rnn_first_states(const P& p, int et, SelectScratch*
     rnn_next_state(p, b, 0, gt, sm->a, group_sync);
 }
 
+// The select of position k for this CTA's requests: the epilogue's 512 threads (et) as two
+// groups of eight warps, group g taking requests blockIdx + (2 j + g) gridDim.  Out of line: its
+// registers are not added to the tile loop's.
 template <typename P>
 __device__ __noinline__ void select_requests(const P& p, int k, int et, SelectScratch* sm) {
   const int grp = et >> 8, gt = et & 255;
