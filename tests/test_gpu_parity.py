@@ -64,13 +64,15 @@ def test_draft_parity_small(name, temperature):
 
 
 @pytest.mark.parametrize("name", ["tiny_fp32", "bf16_ragged", "bf16_r32_simt", "bf16_two_mtiles", "bf16_gamma16",
-                                  "mixed_bs256"])
+                                  "mixed_bs256", "dsv4_bs256"])
 @pytest.mark.parametrize("temperature", [1.0, 0.0])
 def test_draft_confidence_block_equals_the_two_calls(name, temperature):
     """dspark_draft_confidence_block = dspark_draft_block then dspark_confidence, bit for bit: on the
     tensor-core pass the confidence head runs inside the draft's launch (a warp of each CTA, in the
     confidence kernel's summation order), on the CUDA-core pass as its own launch."""
-    wl = I.WORKLOADS["mixed_bs256"] if name == "mixed_bs256" else SMALL[name]
+    # full shapes: d 4096 (two h parts of 8 groups a lane) and d 7168, gamma 5 (14 groups a part)
+    wl = {"mixed_bs256": I.WORKLOADS["mixed_bs256"],
+          "dsv4_bs256": I.WORKLOADS["dsv4_sweep"].with_(bs=256)}.get(name) or SMALL[name]
     inp = I.make_device_inputs(wl, "cuda", with_target=False)
     bs, gamma, V = wl.bs, wl.gamma, wl.V
 
@@ -118,7 +120,10 @@ def test_draft_parity_long_vocabulary_sampled_rows():
         compare_draft(tg[rows], lg[rows], sg[rows], to, lo, so, mo, "bf16", greedy=temperature == 0.0)
 
 
-@pytest.mark.parametrize("name,d", [("tiny_fp32", 64), ("bf16_ragged", 4096)])
+# d 4096 and 7168 (the benchmark's and DSV4's hidden sizes; two h parts at gamma <= 8) and
+# gamma 16 (one part)
+@pytest.mark.parametrize("name,d", [("tiny_fp32", 64), ("bf16_ragged", 4096), ("bf16_ragged", 7168),
+                                    ("bf16_gamma16", 4096)])
 def test_confidence_parity(name, d):
     wl = SMALL[name].with_(d=d, bs=24)
     host = I.make_host_inputs(wl, with_target=False)
