@@ -36,6 +36,27 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Two fp32 values in one 64-bit register, and the paired fp32 FMA / add on them.
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
+  unsigned long long d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void unpack_f32x2(unsigned long long d, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(d));
+}
+__device__ __forceinline__ unsigned long long fma_f32x2(unsigned long long a, unsigned long long b,
+                                                      unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long add_f32x2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // One 16-byte group of a row as raw bits (loaded ahead of use) and its values.
 template <typename T>
 __device__ __forceinline__ void unpack_group(const uint4& q, float* x);
@@ -86,17 +107,30 @@ __device__ __forceinline__ void lse_batch(const uint4 (&cur)[kBatch], int e0, in
     s2 = (s2 == 0.f) ? 0.f : s2 * ex2_approx(m2 - bm2);
     m2 = bm2;
   }
-  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+  // the four partial sums as two pairs (s4[0], s4[1]) and (s4[2], s4[3]): element q of a group
+  // goes to s4[q & 3] as before, with the scale-and-shift and the adds done two lanes at a time
+  // (fma.rn.f32x2 / add.rn.f32x2: each lane rounds exactly as fmaf / + do)
+  unsigned long long s01 = pack_f32x2(0.f, 0.f), s23 = pack_f32x2(0.f, 0.f);
+  const unsigned long long cc = pack_f32x2(c2, c2), mm = pack_f32x2(-m2, -m2);
 #pragma unroll
   for (int u = 0; u < kBatch; ++u) {
     if (kFull || e0 + u * kRowThreads < ng) {
       float x[8];
       unpack_group<T>(cur[u], x);
 #pragma unroll
-      for (int q = 0; q < G; ++q) s4[q & 3] += ex2_approx(fmaf(x[q], c2, -m2));
+      for (int q = 0; q < G; q += 2) {
+        float a0, a1;
+        unpack_f32x2(fma_f32x2(pack_f32x2(x[q], x[q + 1]), cc, mm), a0, a1);
+        const unsigned long long e = pack_f32x2(ex2_approx(a0), ex2_approx(a1));
+        if ((q & 3) == 0) s01 = add_f32x2(s01, e);
+        else s23 = add_f32x2(s23, e);
+      }
     }
   }
-  s2 += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+  float s0, s1, s2p, s3;
+  unpack_f32x2(s01, s0, s1);
+  unpack_f32x2(s23, s2p, s3);
+  s2 += (s0 + s1) + (s2p + s3);
 }
 
 // greedy (temperature 0: the row's argmax) is a template parameter, so that each variant's
