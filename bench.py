@@ -285,7 +285,7 @@ def _profiled_traffic(name: str):
 
 
 DRAFT_SOURCES = ["draft_tc.cu", "draft.cu", "draft_select.cuh", "confidence.cuh", "common.cuh", "tc_ptx.cuh", "tc_host.h"]
-VERIFY_SOURCES = ["verify.cu", "decide_tc.cu", "common.cuh", "tc_ptx.cuh", "tc_host.h"]
+VERIFY_SOURCES = ["verify.cu", "decide_tc.cu", "f32x2.cuh", "common.cuh", "tc_ptx.cuh", "tc_host.h"]
 
 
 def rooflines(wl, stage_ms, rows, tau, profile_key=None, conf_in_draft=False):

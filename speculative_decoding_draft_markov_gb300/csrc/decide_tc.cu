@@ -33,6 +33,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "f32x2.cuh"
 #include "internal.h"
 #include "tc_host.h"
 #include "tc_ptx.cuh"
@@ -440,8 +441,14 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
         }
         if (rm.live) {
           // w = max(0, p_t - p_d); a bonus row's p_d offset is -inf, so p_d = 0 and w = p_t.
-          // Full chunks take no per-element bound check.
+          // Full chunks take no per-element bound check (elements past V add +0 instead).  The
+          // arithmetic runs two elements at a time (paired fp32 FMA / add, each lane rounded as
+          // the scalar operation; element e still goes to sum e & 3, in the same order).
           auto half_sums = [&](auto full) {
+            const unsigned long long cc = pack_f32x2(c2, c2), at2 = pack_f32x2(neg_at, neg_at),
+                                     ad2 = pack_f32x2(neg_ad, neg_ad), neg1 = pack_f32x2(-1.f, -1.f);
+            unsigned long long r01 = pack_f32x2(R4[0], R4[1]), r23 = pack_f32x2(R4[2], R4[3]);
+            unsigned long long p01 = pack_f32x2(P4[0], P4[1]), p23 = pack_f32x2(P4[2], P4[3]);
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
               const uint32_t off = (jj ^ (m & 7)) << 4;
@@ -449,16 +456,37 @@ __global__ void __launch_bounds__(kThreads, 1) decide_tc_kernel(const __grid_con
               unpack8(*reinterpret_cast<const uint4*>(ub + off), xu);
               unpack8(*reinterpret_cast<const uint4*>(tb + off), xt);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float pt = tc::ex2_approx(fmaf(xt[e], c2, neg_at));
-                const float pd = tc::ex2_approx(fmaf(l[8 * jj + e] + xu[e], c2, neg_ad));
-                const float w = fmaxf(0.f, pt - pd);
-                if (decltype(full)::value || h * 64 + 8 * jj + e < valid) {
-                  R4[e & 3] += w;
-                  P4[e & 3] += pt;
+              for (int e = 0; e < 8; e += 2) {
+                float t0, t1, d0, d1;
+                unpack_f32x2(fma_f32x2(pack_f32x2(xt[e], xt[e + 1]), cc, at2), t0, t1);
+                const unsigned long long dl =
+                    add_f32x2(pack_f32x2(l[8 * jj + e], l[8 * jj + e + 1]), pack_f32x2(xu[e], xu[e + 1]));
+                unpack_f32x2(fma_f32x2(dl, cc, ad2), d0, d1);
+                const unsigned long long pt = pack_f32x2(tc::ex2_approx(t0), tc::ex2_approx(t1));
+                const unsigned long long pd = pack_f32x2(tc::ex2_approx(d0), tc::ex2_approx(d1));
+                float w0, w1, q0, q1;
+                unpack_f32x2(fma_f32x2(pd, neg1, pt), w0, w1);  // p_t - p_d, one rounding
+                unpack_f32x2(pt, q0, q1);
+                w0 = fmaxf(0.f, w0);
+                w1 = fmaxf(0.f, w1);
+                if (!decltype(full)::value) {
+                  const int v = h * 64 + 8 * jj + e;
+                  if (v >= valid) w0 = q0 = 0.f;
+                  if (v + 1 >= valid) w1 = q1 = 0.f;
+                }
+                if ((e & 3) == 0) {
+                  r01 = add_f32x2(r01, pack_f32x2(w0, w1));
+                  p01 = add_f32x2(p01, pack_f32x2(q0, q1));
+                } else {
+                  r23 = add_f32x2(r23, pack_f32x2(w0, w1));
+                  p23 = add_f32x2(p23, pack_f32x2(q0, q1));
                 }
               }
             }
+            unpack_f32x2(r01, R4[0], R4[1]);
+            unpack_f32x2(r23, R4[2], R4[3]);
+            unpack_f32x2(p01, P4[0], P4[1]);
+            unpack_f32x2(p23, P4[2], P4[3]);
           };
           if (valid == kBN) half_sums(std::true_type{});
           else half_sums(std::false_type{});
