@@ -425,6 +425,13 @@ __global__ void __launch_bounds__(256, 1) decision_select_kernel(
   const int b = blockIdx.x, tid = threadIdx.x;
   const Decision d = dec[b];
   if (d.kind == kDecNone) return;
+  // a residual decision's factor row (needed unless the residual has no mass) does not depend on
+  // the merge: warps 1.. fetch it while warp 0 merges
+  const bool maybe_recompute = d.kind == kDecResidual && draft_logits == nullptr;
+  if (maybe_recompute && tid >= 32) {
+    const T* arow = factor_row(W1, states, anchor, tokens, b, d.kdec, gamma, V, r);
+    for (int i = tid - 32; i < r; i += 256 - 32) sA[i] = ld_f32(arow, i);
+  }
   // merge the request's partial draws: total residual mass (does the residual have mass?) and
   // the winning chunk of the residual or, without residual mass, of the target draw
   if (tid < 32) {
@@ -455,12 +462,7 @@ __global__ void __launch_bounds__(256, 1) decision_select_kernel(
     cstar = 0;
   }
   const bool resid = (d.kind == kDecResidual) && use_res;
-  const bool recompute = resid && draft_logits == nullptr;
-  if (recompute) {
-    const T* arow = factor_row(W1, states, anchor, tokens, b, d.kdec, gamma, V, r);
-    for (int i = tid; i < r; i += 256) sA[i] = ld_f32(arow, i);
-  }
-  __syncthreads();
+  const bool recompute = resid && draft_logits == nullptr;  // sA was filled before the merge
   const float lse_t = rs[d.pdec].lse;
   if (recompute) chunk_dots<T>(W2t, r, V, cstar * kChunk, sA, tw, threadIdx.x);
   __syncthreads();
