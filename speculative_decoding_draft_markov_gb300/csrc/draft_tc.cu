@@ -17,17 +17,18 @@
 // Compared with a launch per pass this removes two kernel boundaries per position, and the TMA
 // producers run on into the next position's W2t / U tiles while the select runs.
 //
-// What paces the pass on this part is the issue of tcgen05.mma instructions: measured, an
-// issuing loop that also waits on its operand barriers sustains one MMA per ~180 SM cycles
-// whatever N is, while an M = 128, N = 128, K = 16 MMA's arithmetic takes ~64.  So each
-// instruction is made as wide as the tensor core allows, N = 256: a tile of 128 requests x
-// 256 vocabulary ids is 16 MMAs (K = 256), half the instructions per logit of N = 128.
+// Instruction width: back to back, with operands resident, the tensor core retires an
+// M = 128, K = 16 MMA in 64 SM cycles at N = 128 and 128 at N = 256 (its arithmetic rate; two
+// issuing warps share it).  In this pass every 64-K stage adds a barrier wait and a commit, so
+// wide N = 256 MMAs halve that per-stage overhead per logit: a tile of 128 requests x 256
+// vocabulary ids is 16 MMAs (K = 256).
 //
-// The second bound is how fast W2t reaches shared memory: every position streams all of W2t
-// from L2 (where it stays), so a CTA needs as many bytes in flight as the L2 round trip times
-// the tensor core's consumption.  Hence the A operand lives in tensor memory, not shared memory,
-// and the freed space holds a W2t ring of one whole tile (so the next tile's operands are in
-// flight while this tile's MMAs run) beside a ring of U_k boxes 1.5 tiles deep.
+// What bounds the pass is how fast W2t reaches shared memory: every position streams all of W2t
+// from L2 (where it stays), and a 32 KB stage takes about 2 us to arrive while the U stream loads
+// the memory system, so a CTA needs as many bytes in flight as that round trip times the tensor
+// core's consumption.  Hence the A operand lives in tensor memory, not shared memory, and the
+// freed space holds a W2t ring of one whole tile (so the next tile's operands are in flight
+// while this tile's MMAs run) beside a ring of U_k boxes 1.5 tiles deep.
 //
 // Work decomposition:
 //   tile      = 128 requests (TMEM lanes) x 256 vocabulary ids (= four 64-id draft chunks),
