@@ -1,6 +1,6 @@
 """Helpers for GPU-vs-oracle parity tests.
 
-Decision rule (spec tolerances): integer decisions (tokens, accepted lengths,
+Decision rule (the stated parity tolerances): integer decisions (tokens, accepted lengths,
 windows, cu_seqlens) must match exactly unless the oracle's own decision margin -- the
 top-two key gap of a Gumbel-max draw or argmax, or |u - p_t/p_d| of an accept test -- is
 below NEAR (1e-4); such near-margin decisions are counted and must stay rare.

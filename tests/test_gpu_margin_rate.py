@@ -8,7 +8,7 @@ divergence depend on the diverged token and are not counted) and the verificatio
 tests plus its one residual or bonus draw per request (fed forward: the oracle verifies the
 GPU's drafted tokens, windows and draft statistics).  A decision may differ from the oracle
 only where the oracle's own margin is below 1e-4; such divergences must stay below 0.01 % of
-all decisions (spec tolerance).  The rate is printed."""
+all decisions (the stated tolerance).  The rate is printed."""
 import numpy as np
 import pytest
 
