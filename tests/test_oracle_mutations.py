@@ -25,6 +25,8 @@ MUTS = {
  "verify_bonus_untempered": ("                t = trow(k) / temperature\n                x_new, m2 = two_level_gumbel(t,",
                              "                t = trow(k)\n                x_new, m2 = two_level_gumbel(t,",
                              "tests/test_oracle_verify.py::test_first_committed_token_is_target_distributed"),
+ "verify_explicit_pd_untempered": ("d = Df[r, k - 1] / temperature", "d = Df[r, k - 1]",
+                                   "tests/test_oracle_verify.py::test_explicit_draft_logits_first_committed_token_is_target_distributed"),
  "residual_flipped": ("res = np.maximum(0.0, p_t - p_d)", "res = np.maximum(0.0, p_d - p_t)", "tests/test_oracle_verify.py::test_first_committed_token_is_target_distributed"),
  "bias_wrong_token": ("x_prev = tokens[:, k - 1].astype(np.int64)", "x_prev = x_prev", "tests/test_oracle_sampling.py::test_draft_joint_distribution_of_first_two_tokens"),
  "conf_x_index": ("np.asarray(tokens, dtype=np.int64)[:, :gamma - 1]], axis=1)", "np.asarray(tokens, dtype=np.int64)[:, 1:gamma]], axis=1)", "tests/test_oracle_schedule_pack.py::test_confidence_feature_indexing"),

@@ -212,8 +212,12 @@ def test_explicit_draft_equal_to_target_accepts_everything():
     np.testing.assert_array_equal(out[:, :gamma], tok)
 
 
-def test_explicit_draft_logits_first_committed_token_is_target_distributed():
-    """Losslessness with an arbitrary draft distribution given as logits (not a Markov head)."""
+@pytest.mark.parametrize("tau", [1.0, 0.7])
+def test_explicit_draft_logits_first_committed_token_is_target_distributed(tau):
+    """Losslessness with an arbitrary draft distribution given as logits (not a Markov head), at
+    temperature tau: the draft draws from softmax(D / tau), reports the tempered logit of its
+    token and the tempered log-sum-exp, and the first committed token follows softmax(t / tau)
+    -- so the residual's p_d must be tempered too."""
     rng = np.random.default_rng(11)
     V, gamma, bs = 12, 1, 400
     t_row = rng.normal(0, 1.3, size=V)
@@ -221,17 +225,18 @@ def test_explicit_draft_logits_first_committed_token_is_target_distributed():
     target = np.broadcast_to(np.stack([t_row, rng.normal(0, 1.3, size=V)]).astype(np.float32),
                              (bs, gamma + 1, V)).copy()
     D = np.broadcast_to(d_row.astype(np.float32), (bs, gamma, V)).copy()
-    p_d = softmax(d_row)
-    lse_d = np.float32(np.log(np.exp(d_row - d_row.max()).sum()) + d_row.max())
+    p_d = softmax(d_row / tau)
+    dt = d_row / tau
+    lse_d = np.float32(np.log(np.exp(dt - dt.max()).sum()) + dt.max())
     counts = np.zeros(V)
     for step in range(40):
         tok = rng.choice(V, size=(bs, gamma), p=p_d).astype(np.int32)
-        lx = D[np.arange(bs)[:, None], np.arange(gamma)[None, :], tok]
+        lx = (D[np.arange(bs)[:, None], np.arange(gamma)[None, :], tok].astype(np.float64) / tau).astype(np.float32)
         lse = np.full((bs, gamma), lse_d, dtype=np.float32)
         anchor = np.zeros(bs, dtype=np.int32)
         cu, ids, req, pos, padded = O.pack(None, anchor, tok, [], cap=bs * (gamma + 1), gamma=gamma)
         packed = I.gather_packed_target(target, req, pos, padded)
-        out, _, _, _ = O.verify(packed, cu, None, O.STATIC, anchor, tok, lx, lse, None, None, None, 1.0, 4, step,
+        out, _, _, _ = O.verify(packed, cu, None, O.STATIC, anchor, tok, lx, lse, None, None, None, tau, 4, step,
                                 dtype="f32", draft_logits=D)
         np.add.at(counts, out[:, 0], 1)
-    assert stats.chisquare(counts, softmax(t_row) * counts.sum()).pvalue > 1e-4
+    assert stats.chisquare(counts, softmax(t_row.astype(np.float32).astype(np.float64) / tau) * counts.sum()).pvalue > 1e-4
