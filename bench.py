@@ -704,8 +704,9 @@ def run_ours(args, rank: int, world: int):
     res["rnn"] = {"value": rtokens / (rtotal_ms * 1e-3), "unit": "tokens/s", "ms_per_step": rtotal_ms / args.steps,
                   "tokens_per_step": rtokens / args.steps / world, "stage_ms": rstage,
                   "draft_frac_hbm": rroof["frac"], "verify_frac_hbm": rroof["verify"]["frac"],
-                  "head": "RNN sequential head: gated recurrent state s_k (bf16), bias s_k W2; one state-update "
-                          "launch per position before the vocabulary pass",
+                  "head": "RNN sequential head: gated recurrent state s_k (bf16), bias s_k W2; the same single "
+                          "persistent draft launch, which computes s_1 in its prologue and each request's "
+                          "next state right after its select; the confidence head in its own launch",
                   "gpu_launches": rpath.launches * args.steps, "clocks": rclocks}
     del rpath
     if not args.no_configs:
