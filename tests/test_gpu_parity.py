@@ -63,6 +63,23 @@ def test_draft_parity_small(name, temperature):
         assert checked >= wl.bs * wl.gamma - near * wl.gamma and near <= 1
 
 
+@pytest.mark.parametrize("name", ["bf16_ragged", "bf16_r32_simt", "bf16_two_mtiles"])
+@pytest.mark.parametrize("temperature", [0.2, 3.0])
+def test_draft_parity_far_temperatures(name, temperature):
+    """A sharply peaked (tau 0.2: tempered logits up to ~60 in magnitude) and a flat (tau 3.0)
+    draft distribution, on both statistics passes; bf16 (at tau 0.2 the fp32 rounding of the
+    logits, amplified five times, stays far inside the bf16 tolerance)."""
+    wl = SMALL[name]
+    host = I.make_host_inputs(wl, with_target=False, with_hidden=False)
+    inp = _dev(host)
+    for step in (0, 3):
+        tg, lg, sg = _draft_gpu(inp, temperature, wl.seed, step)
+        to, lo, so, mo = O.draft_block(host["U"], host["W1"], host["W2t"], host["anchor"], temperature,
+                                       wl.seed, step, dtype=wl.dtype)
+        checked, near = compare_draft(tg, lg, sg, to, lo, so, mo, wl.dtype)
+        assert checked >= wl.bs * wl.gamma - near * wl.gamma and near <= 1
+
+
 @pytest.mark.parametrize("name", ["tiny_fp32", "bf16_ragged", "bf16_r32_simt", "bf16_two_mtiles", "bf16_gamma16",
                                   "mixed_bs256", "dsv4_bs256"])
 @pytest.mark.parametrize("temperature", [1.0, 0.0])
@@ -270,15 +287,16 @@ def test_schedule_rejects_a_table_that_increases():
         assert B.dspark_read_device_status(ws) == expect
 
 
-def _verify_chain(wl, temperature, mode, windows_seed, step=0):
-    """GPU: draft -> pack(generator windows) -> gather target -> verify; oracle: the same chain."""
+def _verify_chain(wl, temperature, mode, windows_seed, step=0, windows=None):
+    """GPU: draft -> pack(generator windows, or the given ones) -> gather target -> verify;
+    oracle: the same chain."""
     host = I.make_host_inputs(wl, with_hidden=False)
     inp = _dev(host)
     bs, gamma, V = wl.bs, wl.gamma, wl.V
     tg, lg, sg = _draft_gpu(inp, temperature, wl.seed, step)
     to, lo, so, mo = O.draft_block(host["U"], host["W1"], host["W2t"], host["anchor"], temperature, wl.seed,
                                    step, dtype=wl.dtype)
-    win = I.random_windows(bs, gamma, windows_seed)
+    win = I.random_windows(bs, gamma, windows_seed) if windows is None else np.asarray(windows, np.int32)
     pack_win = win if mode == O.COMPACT else None
     cap = bs * (gamma + 1)
     # oracle chain
@@ -330,6 +348,79 @@ def test_verify_chain_parity(name, mode, temperature):
         assert near <= 1
         total_checked += checked
     assert total_checked >= 3 * wl.bs - 3
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "bf16_ragged"])
+@pytest.mark.parametrize("mode", [O.COMPACT, O.CAP_ACCEPT])
+@pytest.mark.parametrize("fill", ["none", "all"])
+@pytest.mark.parametrize("temperature", [1.0, 0.7, 0.0])
+def test_verify_degenerate_windows(name, mode, fill, temperature):
+    """The scheduler's two extremes: no slot admitted (every request packs its anchor row alone
+    and commits the bonus draw of row 0; cap-accept still tests the whole block for its ceiling)
+    and every slot admitted (the compact layout is then the static one)."""
+    wl = VERIFY_WL[name]
+    win = np.full(wl.bs, 0 if fill == "none" else wl.gamma, dtype=np.int32)
+    checked = 0
+    for step in (0, 1):
+        c, near, acc_o = _verify_chain(wl, temperature, mode, None, step, windows=win)
+        assert near <= 1
+        checked += c
+        if fill == "none":
+            assert (acc_o == 0).all()
+    assert checked >= 2 * wl.bs - 2
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "bf16_ragged"])
+@pytest.mark.parametrize("mode", [O.STATIC, O.COMPACT])
+@pytest.mark.parametrize("temperature", [1.0, 0.7])
+def test_verify_draft_equal_to_target_accepts_everything(name, mode, temperature):
+    """The degenerate draft p_d = p_t: the caller's draft logits are the target rows themselves, so
+    every tested token passes (u < p_t / p_d = 1) and the extra token is the bonus draw of the
+    row after the window -- on the GPU as in the oracle, except where |u - p_t / p_d| < 1e-4 (the
+    two sides round the row statistics differently)."""
+    wl = VERIFY_WL[name]
+    host = I.make_host_inputs(wl, with_hidden=False)
+    inp = _dev(host)
+    bs, gamma, V = wl.bs, wl.gamma, wl.V
+    D_host = np.ascontiguousarray(host["target"][:, :gamma])  # row k - 1 scores position k
+    Df = O.to_f64(D_host, wl.dtype)
+    D_dev = inp["target"][:, :gamma].contiguous()
+    rng = np.random.default_rng(78)
+    Dt = Df / temperature
+    m = Dt.max(-1, keepdims=True)
+    lse = np.log(np.exp(Dt - m).sum(-1)) + m[..., 0]
+    p = np.exp(Dt - lse[..., None])
+    tok = np.array([[rng.choice(V, p=p[b, k] / p[b, k].sum()) for k in range(gamma)] for b in range(bs)], np.int32)
+    lx = np.take_along_axis(Dt, tok[..., None].astype(np.int64), -1)[..., 0].astype(np.float32)
+    lse = lse.astype(np.float32)
+    win = I.random_windows(bs, gamma, 124)
+    pack_win = win if mode == O.COMPACT else None
+    cap = bs * (gamma + 1)
+    cu_o, ids_o, req_o, pos_o, pad_o = O.pack(pack_win, host["anchor"], tok, [], cap)
+    packed_o = I.gather_packed_target(host["target"], req_o, pos_o, cap)
+    commit = win if mode == O.COMPACT else np.full(bs, gamma, dtype=np.int32)
+    checked = near = 0
+    for step in range(2):
+        out_o, acc_o, _, mv_o = O.verify(packed_o, cu_o, win, mode, host["anchor"], tok, lx, lse, None, None, None,
+                                         temperature, wl.seed, step, dtype=wl.dtype, draft_logits=D_host)
+        sure = mv_o >= NEAR
+        np.testing.assert_array_equal(acc_o[sure], commit[sure])
+        buf = S.StepBuffers.allocate(bs, gamma, V, cap, inp["U"].dtype)
+        buf.tokens.copy_(torch.as_tensor(tok, device="cuda"))
+        buf.logit_x.copy_(torch.as_tensor(lx, device="cuda"))
+        buf.lse.copy_(torch.as_tensor(lse, device="cuda"))
+        buf.window.copy_(torch.as_tensor(win, device="cuda"))
+        B.dspark_pack(buf.window if mode == O.COMPACT else None, inp["anchor"], buf.tokens, None, buf.cu, buf.ids,
+                      buf.req, buf.pos, buf.padded, buf.ws)
+        S.gather_target_forward(inp["target"])(buf)
+        B.dspark_verify(buf.packed, buf.cu, buf.window, mode, inp["anchor"], buf.tokens, buf.logit_x, buf.lse,
+                        None, None, None, temperature, wl.seed, step, buf.out_tokens, buf.acc_len, buf.ceiling,
+                        buf.ws, draft_logits=D_dev)
+        assert B.dspark_read_device_status(buf.ws) == B.DSPARK_OK
+        c, n = compare_verify(buf.out_tokens.cpu().numpy(), buf.acc_len.cpu().numpy(), out_o, acc_o, mv_o)
+        checked += c
+        near += n
+    assert near <= 1 and checked >= 2 * bs - 1
 
 
 @pytest.mark.parametrize("name", list(VERIFY_WL))
