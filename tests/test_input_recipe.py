@@ -66,12 +66,28 @@ def _within(sample: np.ndarray, std: float, n_sigma: float = 5.0):
     assert abs(sample.std() - std) < n_sigma * std / math.sqrt(2 * n) + 2e-3 * std, (sample.std(), std)
 
 
+def _host(wl):
+    x = I.make_host_inputs(wl)
+    f = (lambda a: np.asarray(a, np.float64)) if wl.dtype == "f32" else (lambda a: I.bf16_bits_to_f32(a).astype(np.float64))
+    return x, f
+
+
+def _torch(wl):
+    """The generator the benchmark and the full-size tests use (torch's, here on the CPU)."""
+    torch = pytest.importorskip("torch")
+    x = I.make_device_inputs(wl, torch.device("cpu"))
+    x = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    x["anchor"] = x["anchor"].numpy()
+    x["sts_T"] = x["sts_T"].numpy()
+    return x, (lambda a: a.float().numpy().astype(np.float64) if isinstance(a, torch.Tensor) else np.asarray(a, np.float64))
+
+
+@pytest.mark.parametrize("gen", ["numpy", "torch"])
 @pytest.mark.parametrize("name", list(RECIPE))
-def test_laws_of_the_generated_inputs(name):
+def test_laws_of_the_generated_inputs(name, gen):
     wl = I.WORKLOADS[name]
     small = wl.with_(bs=24, V=4096, d=256)
-    x = I.make_host_inputs(small)
-    f = (lambda a: np.asarray(a, np.float64)) if wl.dtype == "f32" else (lambda a: I.bf16_bits_to_f32(a).astype(np.float64))
+    x, f = _host(small) if gen == "numpy" else _torch(small)
     U, W1, W2t, h, target = f(x["U"]), f(x["W1"]), f(x["W2t"]), f(x["h"]), f(x["target"])
     assert U.shape == (24, wl.gamma, 4096) and target.shape == (24, wl.gamma + 1, 4096)
     assert W1.shape == W2t.shape == (4096, wl.r) and h.shape == (24, wl.gamma, 256)
@@ -79,7 +95,8 @@ def test_laws_of_the_generated_inputs(name):
     _within(W1, wl.w_std)
     _within(W2t, wl.w_std)
     _within(h, 1.0)
-    _within(np.asarray(x["w"], np.float64), 1.0 / math.sqrt(256 + wl.r), n_sigma=6.0)
+    w = x["w"].numpy() if hasattr(x["w"], "numpy") else x["w"]  # float32 in both generators
+    _within(np.asarray(w, np.float64), 1.0 / math.sqrt(256 + wl.r), n_sigma=6.0)
     assert x["b"] == 0.0
     np.testing.assert_allclose(x["sts_T"], 1.0 + 0.1 * np.arange(1, wl.gamma + 1), rtol=1e-7)
     assert x["anchor"].min() >= 0 and x["anchor"].max() < 4096
